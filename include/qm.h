@@ -1,0 +1,153 @@
+/*
+ * qm.h -- C interface of libqm: weight-only quantized linear algebra over
+ * packed block formats, computed by CUDA kernels on one GB300 (sm_103a).
+ *
+ * Formats (a weight W is a float matrix [..., n, k]: n outputs by k inputs,
+ * stored along k in blocks of codes sharing a scale):
+ *
+ *   QM_AFFINE  MLX affine storage ("GPTQModel wiki: MLX Apple Silicon",
+ *              sections "Concepts: method, checkpoint, runtime, and tensor
+ *              layout" and "Packed layouts and exact transcoding"; "Quantized
+ *              inference in tinygpt's HFModel", section "Problem").
+ *              codes  uint32 [..., n, k*bits/32]: one continuous little-endian
+ *                     bit stream per row, code i in bits [i*bits, (i+1)*bits)
+ *                     (so a 4-bit word holds codes 8j..8j+7, lowest in bits 0..3);
+ *              scales [..., n, k/group_size] and
+ *              biases [..., n, k/group_size], both of scale_dtype, group g
+ *                     covering inputs [g*group_size, (g+1)*group_size).
+ *              value = code*scale + bias, rounded once to float32.
+ *   QM_Q8_0    GGUF Q8_0 ("Nx_quant (raven-ml.dev API docs)", section
+ *              "Weights", Q8_0): codes uint8 [..., n, k/32*34]; per 32 values
+ *              a little-endian float16 d then 32 int8 quants; value = d*q.
+ *   QM_MXFP4   MXFP4 with its scales apart (same page, "Weights", Mxfp4):
+ *              codes  uint8 [..., n, k/2], value 2i in byte i's low nibble and
+ *                     value 2i+1 in its high nibble, each an e2m1 code (sign
+ *                     bit 3 over magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6);
+ *              scales uint8 [..., n, k/32] e8m0: 2^(s-127), s = 255 is NaN.
+ *              value = e2m1(code) * 2^(s-127) (float32: infinite past its range).
+ *
+ * Every part is contiguous, row-major, on the device, with a 16-byte aligned
+ * base address. The caller owns every buffer and the stream. Entry points
+ * validate on the host, enqueue their kernels on `stream` and return; they
+ * allocate no memory, keep no state between calls, hold no decoded copy of a
+ * weight, and may be called from several host threads.
+ *
+ * Errors: QM_EINVAL for a bad argument, with qm_last_error() (thread-local,
+ * valid until the next call on the thread) naming the part: "w", "codes",
+ * "scales", "biases", "x", "y", "out", "ids", "axis", "workspace". QM_ECUDA if
+ * a launch fails. A device-side wait that runs past its limit (about one
+ * second) abandons its work and raises a device flag; qm_device_status()
+ * reads it. No entry point synchronizes the stream.
+ */
+#ifndef QM_H_
+#define QM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st* qm_stream_t;
+
+typedef enum qm_status {
+    QM_OK = 0,
+    QM_EINVAL = 1,   /* invalid argument: shape, dtype, format, alignment, axis */
+    QM_ECUDA = 2,    /* a CUDA runtime call or kernel launch failed */
+    QM_ETIMEOUT = 3, /* a device-side wait gave up; results of that work undefined */
+    QM_ENOTSUP = 4   /* a valid combination this library does not implement */
+} qm_status;
+
+typedef enum qm_format { QM_AFFINE = 0, QM_Q8_0 = 1, QM_MXFP4 = 2 } qm_format;
+typedef enum qm_dtype { QM_F32 = 0, QM_BF16 = 1, QM_F16 = 2 } qm_dtype;
+typedef enum qm_itype { QM_I32 = 0, QM_I64 = 1 } qm_itype;
+
+#define QM_MAX_NDIM 4
+
+/* A packed weight: its format, logical shape [..., n, k] and device parts. */
+typedef struct qm_weight {
+    int32_t format;      /* qm_format */
+    int32_t bits;        /* QM_AFFINE: 4 or 8. QM_Q8_0: 8 or 0. QM_MXFP4: 4 or 0 */
+    int32_t group_size;  /* QM_AFFINE: 32, 64 or 128. QM_Q8_0, QM_MXFP4: 32 or 0 */
+    int32_t scale_dtype; /* QM_AFFINE: QM_BF16 or QM_F16. Otherwise ignored */
+    int32_t ndim;        /* 2 .. QM_MAX_NDIM */
+    int64_t shape[QM_MAX_NDIM]; /* logical shape; shape[ndim-1] = k, a multiple of 32 */
+    const void* codes;   /* see the formats above */
+    const void* scales;  /* QM_AFFINE, QM_MXFP4; must be NULL for QM_Q8_0 */
+    const void* biases;  /* QM_AFFINE only; must be NULL otherwise */
+} qm_weight;
+
+/* dequant: out [..., n, k] of out_dtype (QM_F32, QM_BF16 or QM_F16) holds
+ * every value of w rounded once to out_dtype (round to nearest even,
+ * subnormals kept, overflow to infinity).
+ * Defined by "Nx_quant (raven-ml.dev API docs)", section "Products", dequant. */
+qm_status qm_dequant(const qm_weight* w, int32_t out_dtype, void* out, qm_stream_t stream);
+
+/* apply: y [M, n] = x [M, k] times W^T, summed at float32 and rounded once to
+ * x's dtype, for a 2-d weight [n, k]. x_dtype must be QM_BF16. M = 0 is valid
+ * and launches nothing. x and y must not overlap.
+ * Defined by "Nx_quant (raven-ml.dev API docs)", section "Products", apply. */
+qm_status qm_apply(const qm_weight* w, const void* x, int64_t M, int32_t x_dtype, void* y,
+                   qm_stream_t stream);
+
+/* take: gathers the rows (or matrices) of w at positions ids[0..n_ids) along
+ * `axis` (0 <= axis <= ndim-2; the last axis is refused because a gather along
+ * it would cut blocks), from the packed parts, decoding nothing. A position
+ * outside [0, shape[axis]) -- negative included -- gathers zero bytes.
+ * Packed outputs: out_codes / out_scales / out_biases have w's part shapes
+ * with shape[axis] replaced by n_ids (pass NULL for parts the format lacks).
+ * If out_dense is not NULL it also receives the gathered values decoded and
+ * rounded once to out_dtype, shape [..., n_ids, ..., k]. Either the packed
+ * outputs or out_dense may be omitted (NULL), not both.
+ * Defined by "Nx_quant (raven-ml.dev API docs)", section "Products", take. */
+qm_status qm_take(const qm_weight* w, int32_t axis, const void* ids, int32_t id_type,
+                  int64_t n_ids, void* out_codes, void* out_scales, void* out_biases,
+                  int32_t out_dtype, void* out_dense, qm_stream_t stream);
+
+/* Bytes of device workspace qm_apply_experts and qm_experts_route need for
+ * T*topk positions over E experts (a multiple of 256; 0 only if T*topk = 0). */
+size_t qm_apply_experts_workspace(int64_t T, int64_t topk, int64_t E);
+
+/* apply_experts: for a weight [E, n, k] and ids [T, topk], y [T, topk, n]
+ * holds, at each position p = t*topk + j, the product of expert ids[p]'s
+ * matrix with p's row of x, or zeros where ids[p] is outside [0, E), whatever
+ * that row holds. x is [x_rows, k] bf16 with x_rows = T (row t serves all topk
+ * positions of token t) or T*topk (one row per position). The positions are
+ * routed (a stable sort by expert) into `workspace`, then summed in one
+ * segmented product. A row's bits depend on the shapes, its row and its
+ * expert, never on the other positions' experts.
+ * Defined by "Nx_quant (raven-ml.dev API docs)", section "Products",
+ * apply_experts. */
+qm_status qm_apply_experts(const qm_weight* w, const void* ids, int32_t id_type, int64_t T,
+                           int64_t topk, const void* x, int64_t x_rows, int32_t x_dtype, void* y,
+                           void* workspace, size_t workspace_bytes, qm_stream_t stream);
+
+/* The routing step of qm_apply_experts on its own: for P flattened ids and E
+ * experts, counts[E] (positions per expert), offsets[E+1] (exclusive prefix
+ * sum; offsets[E] = positions in range) and perm[P]: first the in-range
+ * positions by ascending expert, ties by ascending position, then (from
+ * offsets[E] on) the out-of-range positions in ascending order. All three are
+ * int32 device buffers; workspace is qm_apply_experts_workspace(P, 1, E)
+ * bytes. */
+qm_status qm_experts_route(const void* ids, int32_t id_type, int64_t P, int64_t E,
+                           int32_t* counts, int32_t* offsets, int32_t* perm, void* workspace,
+                           size_t workspace_bytes, qm_stream_t stream);
+
+/* Synchronizes `stream`, then reports and clears the device flag raised by a
+ * device-side wait that gave up (QM_ETIMEOUT), or QM_ECUDA for an
+ * asynchronous CUDA error, or QM_OK. */
+qm_status qm_device_status(qm_stream_t stream);
+
+/* The message of the calling thread's last failed call ("" if none). */
+const char* qm_last_error(void);
+
+/* Library version: major * 10000 + minor * 100 + patch. */
+int32_t qm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QM_H_ */

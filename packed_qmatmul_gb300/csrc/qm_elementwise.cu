@@ -1,0 +1,316 @@
+// qm_elementwise.cu -- dequant, take (packed gather and gather-then-decode)
+// and the plain fallback product, all HBM-bound.
+//
+// Decoding follows "Nx_quant (raven-ml.dev API docs)", sections "Weights"
+// (Q8_0 and Mxfp4 layouts, e2m1 / e8m0 values) and "Products" (dequant: every
+// value a float32 rounded once to the output dtype; take: a gather of the
+// packed rows, an out-of-range position gathering zero bytes), and the MLX
+// affine rule of "GPTQModel wiki: MLX Apple Silicon" ("Concepts ..." and
+// "Packed layouts and exact transcoding": value = code*scale + bias over a
+// little-endian code stream).
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "qm_device.cuh"
+#include "qm_internal.h"
+
+namespace qm {
+
+static __device__ uint32_t g_err_elementwise = 0;
+
+uint32_t elementwise_read_clear_error() {
+    uint32_t v = 0, z = 0;
+    cudaMemcpyFromSymbol(&v, g_err_elementwise, sizeof(v));
+    cudaMemcpyToSymbol(g_err_elementwise, &z, sizeof(z));
+    return v;
+}
+
+namespace {
+
+struct DecodeArgs {
+    const uint8_t* codes;
+    const uint8_t* scales;
+    const uint8_t* biases;
+    int64_t k;
+    int64_t code_row_bytes;
+    int64_t scale_row_bytes;  // bytes per row of scales (and of biases)
+    int gs;
+    int sdt;  // QM_BF16 / QM_F16 (affine)
+};
+
+QM_DEV float scale_val(const uint8_t* p, int64_t idx, int sdt) {
+    const uint16_t h = reinterpret_cast<const uint16_t*>(p)[idx];
+    return sdt == QM_F16 ? f16_bits_to_f32(h) : bf16_bits_to_f32(h);
+}
+
+// The 32 float32 values of unit u (inputs 32u .. 32u+31) of source row r.
+template <int FMT, int BITS>
+QM_DEV void decode_unit(const DecodeArgs& a, int64_t r, int64_t u, float (&v)[32]) {
+    if constexpr (FMT == QM_AFFINE) {
+        const int64_t g = (32 * u) / a.gs;  // the unit lies in one group (gs >= 32)
+        const int64_t ng = a.k / a.gs;
+        const float s = scale_val(a.scales, r * ng + g, a.sdt);
+        const float b = scale_val(a.biases, r * ng + g, a.sdt);
+        const uint4* src = reinterpret_cast<const uint4*>(a.codes + r * a.code_row_bytes + u * 4 * BITS);
+        if constexpr (BITS == 4) {
+            const uint4 q = __ldg(src);
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    v[8 * j + i] = fmaf(static_cast<float>((w[j] >> (4 * i)) & 15u), s, b);
+        } else {
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const uint4 q = __ldg(src + h);
+                const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        v[16 * h + 4 * j + i] = fmaf(static_cast<float>((w[j] >> (8 * i)) & 255u), s, b);
+            }
+        }
+    } else if constexpr (FMT == QM_Q8_0) {
+        // A block: little-endian f16 d, then 32 int8 quants; 2-byte aligned.
+        const uint16_t* blk = reinterpret_cast<const uint16_t*>(a.codes + r * a.code_row_bytes + u * 34);
+        const float d = f16_bits_to_f32(__ldg(blk));
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t two = __ldg(blk + 1 + i);
+            v[2 * i] = d * static_cast<float>(static_cast<int8_t>(two & 0xFF));
+            v[2 * i + 1] = d * static_cast<float>(static_cast<int8_t>(two >> 8));
+        }
+    } else {  // MXFP4: 16 bytes of codes (value 2i low nibble, 2i+1 high), one e8m0 scale
+        const uint4 q = __ldg(reinterpret_cast<const uint4*>(a.codes + r * a.code_row_bytes + u * 16));
+        const float sc = e8m0_to_f32(__ldg(a.scales + r * a.scale_row_bytes + u));
+        const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t h2[4];
+            e2m1x8_to_f16x2(w[j], h2);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2[i]));
+                v[8 * j + 2 * i] = f.x * sc;
+                v[8 * j + 2 * i + 1] = f.y * sc;
+            }
+        }
+    }
+}
+
+template <int OUT>
+QM_DEV void store_unit(void* out, int64_t elem, const float (&v)[32]) {
+    if constexpr (OUT == QM_F32) {
+        float4* o = reinterpret_cast<float4*>(static_cast<float*>(out) + elem);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) o[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    } else {
+        uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + elem);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            uint32_t p[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float lo = v[8 * i + 2 * j], hi = v[8 * i + 2 * j + 1];
+                if constexpr (OUT == QM_BF16) {
+                    __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
+                    p[j] = *reinterpret_cast<uint32_t*>(&t);
+                } else {
+                    __half2 t = __floats2half2_rn(lo, hi);
+                    p[j] = *reinterpret_cast<uint32_t*>(&t);
+                }
+            }
+            o[i] = make_uint4(p[0], p[1], p[2], p[3]);
+        }
+    }
+}
+
+// Output row -> source row (or -1 for zeros).
+struct IdentityMap {
+    QM_DEV int64_t operator()(int64_t r) const { return r; }
+};
+
+struct GatherMap {
+    const void* ids;
+    int id64;
+    int64_t n_ids, len, inner_rows;
+    QM_DEV int64_t operator()(int64_t r) const {
+        const int64_t ii = r % inner_rows;
+        const int64_t op = r / inner_rows;
+        const int64_t p = op % n_ids, o = op / n_ids;
+        const int64_t id = id64 ? __ldg(static_cast<const int64_t*>(ids) + p)
+                                : static_cast<int64_t>(__ldg(static_cast<const int32_t*>(ids) + p));
+        if (id < 0 || id >= len) return -1;
+        return (o * len + id) * inner_rows + ii;
+    }
+};
+
+template <int FMT, int BITS, int OUT, class Map>
+__global__ void __launch_bounds__(256) decode_rows_kernel(DecodeArgs a, int64_t out_rows, Map map,
+                                                          void* out) {
+    const int64_t upr = a.k / 32;
+    const int64_t total = out_rows * upr;
+    for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < total;
+         t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = t / upr, u = t - r * upr;
+        const int64_t src = map(r);
+        float v[32];
+        if (src >= 0) {
+            decode_unit<FMT, BITS>(a, src, u, v);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+        }
+        store_unit<OUT>(out, t * 32, v);
+    }
+}
+
+template <class Map>
+cudaError_t launch_decode_rows(const WDesc& w, int64_t out_rows, Map map, int out_dtype, void* out,
+                               cudaStream_t st) {
+    DecodeArgs a{w.codes, w.scales, w.biases, w.k, w.code_row_bytes, w.scale_row_bytes, w.gs, w.sdt};
+    const int64_t total = out_rows * (w.k / 32);
+    if (total == 0) return cudaSuccess;
+    const int threads = 256;
+    const int64_t blocks = std::min<int64_t>((total + threads - 1) / threads, int64_t(num_sms()) * 16);
+#define QM_DECODE_CASE(F, B, O)                                                                  \
+    if (w.fmt == F && (F != QM_AFFINE || w.bits == B) && out_dtype == O) {                        \
+        decode_rows_kernel<F, B, O, Map><<<static_cast<unsigned>(blocks), threads, 0, st>>>(a, out_rows, \
+                                                                                         map, out); \
+        return cudaGetLastError();                                                               \
+    }
+#define QM_DECODE_OUTS(F, B) QM_DECODE_CASE(F, B, QM_F32) QM_DECODE_CASE(F, B, QM_BF16) QM_DECODE_CASE(F, B, QM_F16)
+    QM_DECODE_OUTS(QM_AFFINE, 4)
+    QM_DECODE_OUTS(QM_AFFINE, 8)
+    QM_DECODE_OUTS(QM_Q8_0, 8)
+    QM_DECODE_OUTS(QM_MXFP4, 4)
+#undef QM_DECODE_OUTS
+#undef QM_DECODE_CASE
+    return cudaErrorInvalidValue;
+}
+
+// ------------------------------------------------------------ packed gather
+// dst[o, p, :] = src[o, ids[p], :] (inner bytes each), zero bytes out of range.
+template <typename V>
+__global__ void __launch_bounds__(256) take_packed_kernel(const uint8_t* __restrict__ src, int64_t outer,
+                                                          int64_t len, int64_t inner_bytes,
+                                                          const void* ids, int id64, int64_t n_ids,
+                                                          uint8_t* __restrict__ dst) {
+    const int64_t vpr = inner_bytes / static_cast<int64_t>(sizeof(V));
+    const int64_t total = outer * n_ids * vpr;
+    for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < total;
+         t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t row = t / vpr, c = t - row * vpr;
+        const int64_t p = row % n_ids, o = row / n_ids;
+        const int64_t id = id64 ? __ldg(static_cast<const int64_t*>(ids) + p)
+                                : static_cast<int64_t>(__ldg(static_cast<const int32_t*>(ids) + p));
+        V v;
+        if (id >= 0 && id < len)
+            v = __ldg(reinterpret_cast<const V*>(src + (o * len + id) * inner_bytes) + c);
+        else
+            memset(&v, 0, sizeof(V));
+        reinterpret_cast<V*>(dst + row * inner_bytes)[c] = v;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_dequant(const WDesc& w, int out_dtype, void* out, cudaStream_t st) {
+    return launch_decode_rows(w, w.rows, IdentityMap{}, out_dtype, out, st);
+}
+
+cudaError_t launch_take_dense(const WDesc& w, int axis, const void* ids, int id64, int64_t n_ids,
+                              int out_dtype, void* out, cudaStream_t st) {
+    int64_t outer = 1, inner_rows = 1;
+    for (int i = 0; i < axis; ++i) outer *= w.shape[i];
+    for (int i = axis + 1; i < w.ndim - 1; ++i) inner_rows *= w.shape[i];
+    GatherMap m{ids, id64, n_ids, w.shape[axis], inner_rows};
+    return launch_decode_rows(w, outer * n_ids * inner_rows, m, out_dtype, out, st);
+}
+
+cudaError_t launch_take_packed(const uint8_t* src, int64_t outer, int64_t len, int64_t inner_bytes,
+                               const void* ids, int id64, int64_t n_ids, uint8_t* dst, cudaStream_t st) {
+    const int threads = 256;
+    auto go = [&](auto vec) -> cudaError_t {
+        using V = decltype(vec);
+        const int64_t total = outer * n_ids * (inner_bytes / static_cast<int64_t>(sizeof(V)));
+        if (total == 0) return cudaSuccess;
+        const int64_t blocks = std::min<int64_t>((total + threads - 1) / threads, int64_t(num_sms()) * 16);
+        take_packed_kernel<V><<<static_cast<unsigned>(blocks), threads, 0, st>>>(src, outer, len, inner_bytes,
+                                                                                ids, id64, n_ids, dst);
+        return cudaGetLastError();
+    };
+    if (inner_bytes % 16 == 0) return go(uint4{});
+    if (inner_bytes % 8 == 0) return go(uint2{});
+    if (inner_bytes % 4 == 0) return go(uint32_t{});
+    if (inner_bytes % 2 == 0) return go(uint16_t{});
+    return go(uint8_t{});
+}
+
+// ------------------------------------------------------------ plain product
+// One warp per (output row j, block of up to 8 rows of x): each lane decodes
+// 32-value units in turn and forms their dot products with x; the warp then
+// sums lanes in a fixed butterfly order. Used where the fast paths decline.
+namespace {
+template <int FMT, int BITS>
+__global__ void __launch_bounds__(256) apply_simple_kernel(DecodeArgs a, int64_t n, const uint16_t* x,
+                                                           int64_t M, uint16_t* y) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5;
+    const int64_t nwarps = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    const int64_t mblocks = (M + 7) / 8;
+    const int64_t upr = a.k / 32;
+    for (int64_t job = warp; job < n * mblocks; job += nwarps) {
+        const int64_t j = job / mblocks, m0 = (job % mblocks) * 8;
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+        for (int64_t u = lane; u < upr; u += 32) {
+            float v[32];
+            decode_unit<FMT, BITS>(a, j, u, v);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (m0 + i < M) {
+                    const uint16_t* xr = x + (m0 + i) * a.k + 32 * u;
+                    float s = 0.0f;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) s = fmaf(bf16_bits_to_f32(xr[e]), v[e], s);
+                    acc[i] += s;
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float s = acc[i];
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+            if (lane == 0 && m0 + i < M) {
+                __nv_bfloat16 b = __float2bfloat16_rn(s);
+                y[(m0 + i) * n + j] = *reinterpret_cast<uint16_t*>(&b);
+            }
+        }
+    }
+}
+}  // namespace
+
+cudaError_t launch_apply_simple(const WDesc& w, const void* x, int64_t M, void* y, cudaStream_t st) {
+    DecodeArgs a{w.codes, w.scales, w.biases, w.k, w.code_row_bytes, w.scale_row_bytes, w.gs, w.sdt};
+    const int64_t jobs = w.n * ((M + 7) / 8);
+    const int64_t blocks = std::min<int64_t>((jobs * 32 + 255) / 256, int64_t(num_sms()) * 8);
+    const uint16_t* xb = static_cast<const uint16_t*>(x);
+    uint16_t* yb = static_cast<uint16_t*>(y);
+    if (w.fmt == QM_AFFINE && w.bits == 4)
+        apply_simple_kernel<QM_AFFINE, 4><<<static_cast<unsigned>(blocks), 256, 0, st>>>(a, w.n, xb, M, yb);
+    else if (w.fmt == QM_AFFINE)
+        apply_simple_kernel<QM_AFFINE, 8><<<static_cast<unsigned>(blocks), 256, 0, st>>>(a, w.n, xb, M, yb);
+    else if (w.fmt == QM_Q8_0)
+        apply_simple_kernel<QM_Q8_0, 8><<<static_cast<unsigned>(blocks), 256, 0, st>>>(a, w.n, xb, M, yb);
+    else
+        apply_simple_kernel<QM_MXFP4, 4><<<static_cast<unsigned>(blocks), 256, 0, st>>>(a, w.n, xb, M, yb);
+    return cudaGetLastError();
+}
+
+}  // namespace qm

@@ -1,0 +1,705 @@
+// qm_gemv.cu -- decode product y[M, n] = x[M, k] * W^T for M <= 16 over packed
+// weights, HBM-bound.
+//
+// The product is the one "Nx_quant (raven-ml.dev API docs)", section
+// "Products", val apply, defines: summed at float32 over the weight's float32
+// values and rounded once to x's dtype. Like that page's block-scaled kernels,
+// it scales each block's (group's) partial sum rather than every element: the
+// codes enter the tensor cores as exact small integers, so the only roundings
+// are float32 sums.
+//
+// Design (one GB300: 152 SMs, HBM3e):
+//  * A CTA is 1 producer warp + 8 consumer warps. The producer streams
+//    16-row stages of the packed weight (codes, scales, biases) into shared
+//    memory with cp.async.bulk, one copy per row, completing on mbarriers.
+//  * Each consumer warp takes whole stages: 16 rows x the CTA's k range. It
+//    decodes codes in registers to f16 pairs that hold exact integers
+//    (1024 + code, via a magic-exponent OR), and multiplies them with the
+//    activations on mma.sync m16n8k16 (rows of W as the M side, tokens as the
+//    N side). Per group it applies scale (and bias) in float32.
+//  * Activations are rescaled per token by a power of two so that every bf16
+//    value is exact in f16; the scale is undone at the end.
+//  * Where one CTA per 16-row tile would leave SMs idle, a cluster of S CTAs
+//    splits k; the partial sums meet through distributed shared memory and
+//    are added in rank order (deterministic, no global scratch).
+//
+// MLX affine codes: "GPTQModel wiki: MLX Apple Silicon", "Packed layouts and
+// exact transcoding" (little-endian code stream) and "Concepts ..."
+// (value = code*scale + bias). Q8_0 and MXFP4 layouts: "Nx_quant", "Weights".
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+
+#include "qm_device.cuh"
+#include "qm_internal.h"
+
+namespace qm {
+
+static __device__ uint32_t g_err_gemv = 0;
+
+uint32_t gemv_read_clear_error() {
+    uint32_t v = 0, z = 0;
+    cudaMemcpyFromSymbol(&v, g_err_gemv, sizeof(v));
+    cudaMemcpyToSymbol(g_err_gemv, &z, sizeof(z));
+    return v;
+}
+
+namespace gemv {
+
+constexpr int kRows = 16;            // rows per stage (one MMA row tile)
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxStages = 16;
+constexpr uint32_t kMagic = 0x64006400u;  // f16x2 (1024, 1024)
+
+struct Params {
+    const uint8_t* codes;
+    const uint8_t* scales;
+    const uint8_t* biases;
+    const uint16_t* x;
+    uint16_t* y;
+    int64_t n, k;
+    int M;
+    int sdt;
+    int64_t code_row_bytes, scale_row_bytes;
+    // decomposition
+    int S;                   // CTAs per cluster, splitting k
+    int64_t krange;          // k values per CTA
+    int tiles_per_cluster;   // 16-row tiles per cluster
+    int64_t n_tiles;
+    // shared memory layout (byte offsets from the dynamic smem base)
+    uint32_t nstage, stage_bytes;
+    uint32_t code_seg, code_pitch;   // per row: bytes copied, smem pitch
+    uint32_t scale_seg;              // per row bytes of scales (and biases) in the stage
+    uint32_t off_scales, off_biases; // within a stage
+    uint32_t off_bars, off_xfrag, off_tok, off_tokscale, off_partial, off_stages;
+};
+
+// Format traits: codes per 32-bit word, MMAs per group, offset of the magic.
+template <int FMT, int BITS, int GS>
+struct Fmt {
+    static constexpr int kMmas = GS / 16;  // MMAs (k16) per group
+};
+
+// ---------------------------------------------------------------- decoders
+// Affine 4-bit word -> the A halves for MMA half h: (n[2h], n[4+2h]) and
+// 16 * (n[1+2h], n[5+2h]), each as f16 (1024 + value).
+QM_DEV void dec4(uint32_t w, int h, uint32_t& lo, uint32_t& hi) {
+    const uint32_t s = h ? (w >> 8) : w;
+    lo = (s & 0x000F000Fu) | kMagic;
+    hi = (s & 0x00F000F0u) | kMagic;
+}
+
+// Four 8-bit codes -> f16 (1024 + u0, 1024 + u1), (1024 + u2, 1024 + u3).
+QM_DEV void dec8(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    lo = prmt(w, 0x64646464u, 0x5140);
+    hi = prmt(w, 0x64646464u, 0x7362);
+}
+
+template <int NT>
+struct Acc {
+    float v[NT][4];
+};
+
+// Per-group weight scale data of one row for the epilogue.
+struct RowScale {
+    float s, b;
+};
+
+template <int FMT, int BITS, int GS, int NT>
+__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ Params p) {
+    extern __shared__ __align__(1024) uint8_t smem[];
+    constexpr int MM = GS / 16;  // MMAs per group
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = p.S;
+    const uint32_t rank = (S > 1) ? cluster_ctarank() : 0;
+    const int64_t cluster = blockIdx.x / S;
+    const int64_t tile0 = cluster * p.tiles_per_cluster;
+    const int ntiles = static_cast<int>(std::min<int64_t>(p.tiles_per_cluster, p.n_tiles - tile0));
+    const int64_t kbase = rank * p.krange;
+    const int groups = static_cast<int>(p.krange / GS);
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bars);
+    const uint32_t bar_full0 = smem_u32(bars), bar_empty0 = smem_u32(bars + kMaxStages);
+    int& s_abort = *reinterpret_cast<int*>(smem + p.off_bars + 2 * kMaxStages * 8);
+
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        for (uint32_t i = 0; i < p.nstage; ++i) {
+            mbar_init(bar_full0 + 8 * i, 32);  // the producer's lanes
+            mbar_init(bar_empty0 + 8 * i, 1);  // the one consumer warp of the stage
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    grid_launch_dependents();
+    grid_dependency_wait();  // x (and, conservatively, W) may come from the previous kernel
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------------ producer
+        int issued = 0;
+        for (int j = 0; j < ntiles; ++j) {
+            const uint32_t slot = j % p.nstage;
+            const uint32_t par = ((j / p.nstage) & 1) ^ 1;
+            if (!mbar_wait(bar_empty0 + 8 * slot, par) || *(volatile int*)&s_abort) {
+                if (lane == 0) { atomicOr(&g_err_gemv, DEV_ERR_TIMEOUT); s_abort = 1; }
+                break;
+            }
+            issued = j + 1;
+            const int64_t row0 = (tile0 + j) * kRows;
+            const int rows = static_cast<int>(std::min<int64_t>(kRows, p.n - row0));
+            uint8_t* st = smem + p.off_stages + slot * p.stage_bytes;
+            const uint32_t bar = bar_full0 + 8 * slot;
+            // bulk bytes: codes per row; scales/biases per row when split, else one span
+            uint32_t tx = rows * p.code_seg;
+            uint32_t span = 0, span_bulk = 0;
+            if (p.scale_seg) {
+                if (S > 1) {
+                    tx += rows * p.scale_seg * (p.biases ? 2 : 1);
+                } else {
+                    span = rows * p.scale_seg;
+                    span_bulk = span & ~15u;
+                    tx += span_bulk * (p.biases ? 2 : 1);
+                }
+            }
+            if (lane == 0) mbar_expect_tx(bar, tx);
+            __syncwarp();
+            if (lane < rows) {
+                const int64_t r = row0 + lane;
+                const uint8_t* src = p.codes + r * p.code_row_bytes + rank * p.code_seg;
+                bulk_g2s(smem_u32(st + lane * p.code_pitch), src, p.code_seg, bar);
+                if (p.scale_seg && S > 1) {
+                    const int64_t off = r * p.scale_row_bytes + rank * p.scale_seg;
+                    bulk_g2s(smem_u32(st + p.off_scales + lane * p.scale_seg), p.scales + off, p.scale_seg, bar);
+                    if (p.biases)
+                        bulk_g2s(smem_u32(st + p.off_biases + lane * p.scale_seg), p.biases + off, p.scale_seg, bar);
+                }
+            }
+            if (p.scale_seg && S == 1) {
+                const int64_t off = row0 * p.scale_row_bytes;
+                if (lane == 0 && span_bulk) {
+                    bulk_g2s(smem_u32(st + p.off_scales), p.scales + off, span_bulk, bar);
+                    if (p.biases) bulk_g2s(smem_u32(st + p.off_biases), p.biases + off, span_bulk, bar);
+                }
+                for (uint32_t b = span_bulk + lane; b < span; b += 32) {  // ragged tail of the last tile
+                    st[p.off_scales + b] = p.scales[off + b];
+                    if (p.biases) st[p.off_biases + b] = p.biases[off + b];
+                }
+            }
+            mbar_arrive(bar);
+        }
+        if (*(volatile int*)&s_abort) {
+            // abandoned: let the copies already issued land before the CTA exits
+            for (int j = std::max(0, issued - static_cast<int>(p.nstage)); j < issued; ++j)
+                (void)mbar_wait(bar_full0 + 8 * (j % p.nstage), (j / p.nstage) & 1);
+        }
+    } else {
+        // ------------------------------------------------------------ consumers
+        const int ctid = threadIdx.x;  // 0 .. 255
+        float* tokscale = reinterpret_cast<float*>(smem + p.off_tokscale);   // [16] 2^-E
+        float* tokmul = tokscale + 16;                                        // [16] 2^E
+        // 1. per-token power-of-two scale over this CTA's k range
+        for (int m = warp; m < 16; m += kConsumerWarps) {
+            float amax = 0.0f;
+            if (m < p.M) {
+                const uint16_t* xr = p.x + m * p.k + kbase;
+                for (int64_t i = lane * 8; i < p.krange; i += 256) {
+                    const uint4 q = __ldg(reinterpret_cast<const uint4*>(xr + i));
+                    const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w4[e] & 0xFFFF)));
+                        amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w4[e] >> 16)));
+                    }
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            }
+            if (lane == 0) {
+                int E = 0;  // x' = x * 2^E puts max |x'| in [2^14, 2^15)
+                if (amax > 0.0f) {
+                    const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF) - 127;
+                    E = min(max(14 - ex, -126), 126);
+                }
+                tokmul[m] = (m < p.M) ? __uint_as_float(static_cast<uint32_t>(E + 127) << 23) : 0.0f;
+                tokscale[m] = __uint_as_float(static_cast<uint32_t>(-E + 127) << 23);
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+        // 2. B fragments for every group of the k range, and per-token group sums
+        uint32_t* xfrag = reinterpret_cast<uint32_t*>(smem + p.off_xfrag);
+        float2* tok = reinterpret_cast<float2*>(smem + p.off_tok);  // [groups][16]
+        {
+            const int items = groups * 32 * NT;
+            for (int it = ctid; it < items; it += kConsumerWarps * 32) {
+                const int nt = it % NT, ln = (it / NT) % 32, gi = it / (NT * 32);
+                const int tg = ln >> 2, t = ln & 3;
+                const int m = nt * 8 + tg;
+                const bool live = m < p.M;  // padding tokens get exact zeros
+                const float mul = live ? tokmul[m] : 0.0f;
+                const uint16_t* xr = p.x + static_cast<int64_t>(live ? m : 0) * p.k + kbase;
+                uint32_t* dst = xfrag + ((static_cast<int64_t>(gi) * 32 + ln) * MM) * NT * 2 + nt * 2;
+                auto xv = [&](int64_t kk) { return live ? bf16_bits_to_f32(xr[kk]) * mul : 0.0f; };
+                if constexpr (FMT == QM_AFFINE && BITS == 4) {
+                    constexpr int V = GS / 32;
+#pragma unroll
+                    for (int v = 0; v < V; ++v) {
+                        const int64_t k0 = 8 * (static_cast<int64_t>(gi) * (GS / 8) + t * V + v);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int mm = 2 * v + h;
+                            dst[mm * NT * 2 + 0] = pack_f16x2(xv(k0 + 2 * h), xv(k0 + 4 + 2 * h));
+                            dst[mm * NT * 2 + 1] =
+                                pack_f16x2(xv(k0 + 1 + 2 * h) * 0.0625f, xv(k0 + 5 + 2 * h) * 0.0625f);
+                        }
+                    }
+                } else if constexpr (FMT == QM_AFFINE && BITS == 8) {
+                    constexpr int V = GS / 16;
+#pragma unroll
+                    for (int v = 0; v < V; ++v) {
+                        const int64_t k0 = 4 * (static_cast<int64_t>(gi) * (GS / 4) + t * V + v);
+                        dst[v * NT * 2 + 0] = pack_f16x2(xv(k0), xv(k0 + 1));
+                        dst[v * NT * 2 + 1] = pack_f16x2(xv(k0 + 2), xv(k0 + 3));
+                    }
+                } else {  // Q8_0, MXFP4: thread t holds values 8t .. 8t+7 of the block
+#pragma unroll
+                    for (int mm = 0; mm < 2; ++mm) {
+                        const int64_t k0 = 32 * static_cast<int64_t>(gi) + 8 * t + 4 * mm;
+                        dst[mm * NT * 2 + 0] = pack_f16x2(xv(k0), xv(k0 + 1));
+                        dst[mm * NT * 2 + 1] = pack_f16x2(xv(k0 + 2), xv(k0 + 3));
+                    }
+                }
+            }
+            // per (group, token): (offset, sum of x') -- offset = magic * sum of B values
+            for (int it = ctid; it < groups * 16; it += kConsumerWarps * 32) {
+                const int m = it % 16, gi = it / 16;
+                float F = 0.0f, X = 0.0f;
+                if (m < p.M) {
+                    const float mul = tokmul[m];
+                    const uint16_t* xr = p.x + m * p.k + kbase + static_cast<int64_t>(gi) * GS;
+                    for (int e = 0; e < GS; ++e) {
+                        const float xe = bf16_bits_to_f32(xr[e]) * mul;
+                        X += xe;
+                        F += (FMT == QM_AFFINE && BITS == 4 && (e & 1)) ? xe * 0.0625f : xe;
+                    }
+                }
+                const float magic = (FMT == QM_Q8_0) ? 1152.0f : 1024.0f;
+                tok[it] = make_float2(FMT == QM_MXFP4 ? 0.0f : magic * F, X);
+            }
+        }
+        asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+
+        // 3. main loop: warp w takes stages w, w + 8, ...
+        const int g = lane >> 2, t = lane & 3;
+        float* partial = reinterpret_cast<float*>(smem + p.off_partial);  // [tiles][16 rows][16 tok]
+        bool ok = true;
+        for (int j = warp; j < ntiles && ok; j += kConsumerWarps) {
+            const uint32_t slot = j % p.nstage;
+            const uint32_t par = (j / p.nstage) & 1;
+            if (!mbar_wait(bar_full0 + 8 * slot, par) || *(volatile int*)&s_abort) {
+                if (lane == 0) { atomicOr(&g_err_gemv, DEV_ERR_TIMEOUT); s_abort = 1; }
+                ok = false;
+                break;
+            }
+            const uint8_t* st = smem + p.off_stages + slot * p.stage_bytes;
+            const uint8_t* r0 = st + g * p.code_pitch;        // row g
+            const uint8_t* r8 = st + (g + 8) * p.code_pitch;  // row g + 8
+            Acc<NT> y;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) y.v[nt][i] = 0.0f;
+
+            for (int gi = 0; gi < groups; ++gi) {
+                Acc<NT> acc;
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) acc.v[nt][i] = 0.0f;
+                // B fragments of this group for this lane
+                uint32_t bf[MM][NT][2];
+                {
+                    const uint4* src = reinterpret_cast<const uint4*>(
+                        xfrag + ((static_cast<int64_t>(gi) * 32 + lane) * MM) * NT * 2);
+                    uint32_t* b = &bf[0][0][0];
+#pragma unroll
+                    for (int q = 0; q < MM * NT / 2; ++q) {
+                        const uint4 v = src[q];
+                        b[4 * q] = v.x; b[4 * q + 1] = v.y; b[4 * q + 2] = v.z; b[4 * q + 3] = v.w;
+                    }
+                }
+                if constexpr (FMT == QM_AFFINE && BITS == 4) {
+                    constexpr int V = GS / 32;
+                    uint32_t w0[V], w8[V];
+                    const int off = gi * (GS / 2) + t * V * 4;
+                    if constexpr (V == 1) {
+                        w0[0] = *reinterpret_cast<const uint32_t*>(r0 + off);
+                        w8[0] = *reinterpret_cast<const uint32_t*>(r8 + off);
+                    } else {
+#pragma unroll
+                        for (int v = 0; v < V; v += 2) {
+                            const uint2 a = *reinterpret_cast<const uint2*>(r0 + off + 4 * v);
+                            const uint2 c = *reinterpret_cast<const uint2*>(r8 + off + 4 * v);
+                            w0[v] = a.x; w0[v + 1] = a.y; w8[v] = c.x; w8[v + 1] = c.y;
+                        }
+                    }
+#pragma unroll
+                    for (int v = 0; v < V; ++v)
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            uint32_t a0, a2, a1, a3;
+                            dec4(w0[v], h, a0, a2);
+                            dec4(w8[v], h, a1, a3);
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt)
+                                mma_f16(acc.v[nt], a0, a1, a2, a3, bf[2 * v + h][nt][0], bf[2 * v + h][nt][1]);
+                        }
+                } else if constexpr (FMT == QM_AFFINE && BITS == 8) {
+                    constexpr int V = GS / 16;
+                    const int off = gi * GS + t * V * 4;
+#pragma unroll
+                    for (int v = 0; v < V; v += 2) {
+                        const uint2 a = *reinterpret_cast<const uint2*>(r0 + off + 4 * v);
+                        const uint2 c = *reinterpret_cast<const uint2*>(r8 + off + 4 * v);
+                        const uint32_t wa[2] = {a.x, a.y}, wc[2] = {c.x, c.y};
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            uint32_t a0, a2, a1, a3;
+                            dec8(wa[e], a0, a2);
+                            dec8(wc[e], a1, a3);
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt)
+                                mma_f16(acc.v[nt], a0, a1, a2, a3, bf[v + e][nt][0], bf[v + e][nt][1]);
+                        }
+                    }
+                } else if constexpr (FMT == QM_Q8_0) {
+                    // codes of block gi at byte 34*gi + 2 + 8t (2-byte aligned when gi is even)
+                    const int o = 34 * gi + 2 + 8 * t;
+                    uint32_t c0[2], c8[2];
+                    if (o & 2) {
+                        const uint32_t* q0 = reinterpret_cast<const uint32_t*>(r0 + o - 2);
+                        const uint32_t* q8 = reinterpret_cast<const uint32_t*>(r8 + o - 2);
+                        const uint32_t x0 = q0[0], x1 = q0[1], x2 = q0[2];
+                        const uint32_t z0 = q8[0], z1 = q8[1], z2 = q8[2];
+                        c0[0] = prmt(x0, x1, 0x5432); c0[1] = prmt(x1, x2, 0x5432);
+                        c8[0] = prmt(z0, z1, 0x5432); c8[1] = prmt(z1, z2, 0x5432);
+                    } else {
+                        const uint32_t* q0 = reinterpret_cast<const uint32_t*>(r0 + o);
+                        const uint32_t* q8 = reinterpret_cast<const uint32_t*>(r8 + o);
+                        c0[0] = q0[0]; c0[1] = q0[1]; c8[0] = q8[0]; c8[1] = q8[1];
+                    }
+#pragma unroll
+                    for (int mm = 0; mm < 2; ++mm) {
+                        uint32_t a0, a2, a1, a3;
+                        dec8(c0[mm] ^ 0x80808080u, a0, a2);
+                        dec8(c8[mm] ^ 0x80808080u, a1, a3);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            mma_f16(acc.v[nt], a0, a1, a2, a3, bf[mm][nt][0], bf[mm][nt][1]);
+                    }
+                } else {  // MXFP4
+                    const int o = 16 * gi + 4 * t;
+                    uint32_t h0[4], h8[4];
+                    e2m1x8_to_f16x2(*reinterpret_cast<const uint32_t*>(r0 + o), h0);
+                    e2m1x8_to_f16x2(*reinterpret_cast<const uint32_t*>(r8 + o), h8);
+#pragma unroll
+                    for (int mm = 0; mm < 2; ++mm)
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            mma_f16(acc.v[nt], h0[2 * mm], h8[2 * mm], h0[2 * mm + 1], h8[2 * mm + 1],
+                                    bf[mm][nt][0], bf[mm][nt][1]);
+                }
+                // ---- group epilogue: scale (and bias) per row, offsets per token
+                float s0, s8, b0 = 0.0f, b8 = 0.0f;
+                if constexpr (FMT == QM_AFFINE) {
+                    const uint16_t* sc = reinterpret_cast<const uint16_t*>(st + p.off_scales);
+                    const uint16_t* bi = reinterpret_cast<const uint16_t*>(st + p.off_biases);
+                    const int stride = p.scale_seg / 2;
+                    const uint32_t hs0 = sc[g * stride + gi], hs8 = sc[(g + 8) * stride + gi];
+                    const uint32_t hb0 = bi[g * stride + gi], hb8 = bi[(g + 8) * stride + gi];
+                    if (p.sdt == QM_F16) {
+                        s0 = f16_bits_to_f32(hs0); s8 = f16_bits_to_f32(hs8);
+                        b0 = f16_bits_to_f32(hb0); b8 = f16_bits_to_f32(hb8);
+                    } else {
+                        s0 = bf16_bits_to_f32(hs0); s8 = bf16_bits_to_f32(hs8);
+                        b0 = bf16_bits_to_f32(hb0); b8 = bf16_bits_to_f32(hb8);
+                    }
+                } else if constexpr (FMT == QM_Q8_0) {
+                    s0 = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(r0 + 34 * gi));
+                    s8 = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(r8 + 34 * gi));
+                } else {
+                    const uint8_t* sc = st + p.off_scales;
+                    s0 = e8m0_to_f32(sc[g * p.scale_seg + gi]);
+                    s8 = e8m0_to_f32(sc[(g + 8) * p.scale_seg + gi]);
+                }
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const float4 td = *reinterpret_cast<const float4*>(tok + gi * 16 + nt * 8 + 2 * t);
+                    // td = (O[2t], X[2t], O[2t+1], X[2t+1])
+                    if constexpr (FMT == QM_MXFP4) {
+                        y.v[nt][0] = fmaf(s0, acc.v[nt][0], y.v[nt][0]);
+                        y.v[nt][1] = fmaf(s0, acc.v[nt][1], y.v[nt][1]);
+                        y.v[nt][2] = fmaf(s8, acc.v[nt][2], y.v[nt][2]);
+                        y.v[nt][3] = fmaf(s8, acc.v[nt][3], y.v[nt][3]);
+                    } else {
+                        y.v[nt][0] = fmaf(s0, acc.v[nt][0] - td.x, fmaf(b0, td.y, y.v[nt][0]));
+                        y.v[nt][1] = fmaf(s0, acc.v[nt][1] - td.z, fmaf(b0, td.w, y.v[nt][1]));
+                        y.v[nt][2] = fmaf(s8, acc.v[nt][2] - td.x, fmaf(b8, td.y, y.v[nt][2]));
+                        y.v[nt][3] = fmaf(s8, acc.v[nt][3] - td.z, fmaf(b8, td.w, y.v[nt][3]));
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_empty0 + 8 * slot);
+
+            // ---- tile result: undo the token scale; store or keep the partial
+            const int64_t row0 = (tile0 + j) * kRows;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int m = nt * 8 + 2 * t + (i & 1);
+                    const int r = g + ((i & 2) ? 8 : 0);
+                    const float v = y.v[nt][i] * tokscale[m];
+                    if (S == 1) {
+                        if (m < p.M && row0 + r < p.n) {
+                            __nv_bfloat16 b = __float2bfloat16_rn(v);
+                            p.y[static_cast<int64_t>(m) * p.n + row0 + r] = *reinterpret_cast<uint16_t*>(&b);
+                        }
+                    } else {
+                        partial[(j * kRows + r) * 16 + m] = v;
+                    }
+                }
+        }
+    }
+
+    // ---------------------------------------------------------------- split-k reduction
+    if (S > 1) {
+        __syncthreads();
+        cluster_sync();
+        const uint32_t base = smem_u32(smem + p.off_partial);
+        const int entries = ntiles * kRows * 16;
+        for (int e = rank * blockDim.x + threadIdx.x; e < entries; e += S * blockDim.x) {
+            const int m = e % 16, rr = e / 16;
+            const int64_t row = tile0 * kRows + rr;
+            if (m >= p.M || row >= p.n) continue;
+            float sum = 0.0f;
+            for (int q = 0; q < S; ++q) sum += ld_shared_cluster_f32(map_shared_rank(base + 4u * e, q));
+            __nv_bfloat16 b = __float2bfloat16_rn(sum);
+            p.y[static_cast<int64_t>(m) * p.n + row] = *reinterpret_cast<uint16_t*>(&b);
+        }
+        cluster_sync();
+    }
+}
+
+// ---------------------------------------------------------------- host planning
+struct Plan {
+    Params p;
+    int S = 1;
+    int64_t grid = 0;
+    size_t smem = 0;
+    bool ok = false;
+};
+
+static uint32_t round_up(uint64_t v, uint64_t a) { return static_cast<uint32_t>((v + a - 1) / a * a); }
+
+// Bytes of codes for `kk` values of one row.
+static int64_t code_bytes(const WDesc& w, int64_t kk) {
+    if (w.fmt == QM_Q8_0) return kk / 32 * 34;
+    return kk * w.bits / 8;
+}
+
+static int lds_words(const WDesc& w) {
+    if (w.fmt == QM_AFFINE && w.bits == 4 && w.gs == 32) return 1;
+    if (w.fmt == QM_MXFP4 || w.fmt == QM_Q8_0) return 1;
+    return 2;
+}
+
+__global__ void cluster_probe_kernel() {}
+
+// Clusters of S CTAs (one per SM, `smem` bytes each) that can be resident at
+// once; cached per (device, S).
+static int max_clusters(int S, size_t smem) {
+    static int cache[64][9];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (S <= 1) return num_sms();
+    if (dev >= 0 && dev < 64 && cache[dev][S] > 0) return cache[dev][S];
+    int n = 0;
+    cudaFuncSetAttribute(cluster_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(smem));
+    cudaFuncSetAttribute(cluster_probe_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(S * 64);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute a;
+    a.id = cudaLaunchAttributeClusterDimension;
+    a.val.clusterDim.x = S;
+    a.val.clusterDim.y = 1;
+    a.val.clusterDim.z = 1;
+    cfg.attrs = &a;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&n, cluster_probe_kernel, &cfg) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        n = num_sms() / S;
+    }
+    if (dev >= 0 && dev < 64) cache[dev][S] = n;
+    return n;
+}
+
+static bool plan_for(const WDesc& w, int64_t M, int S, Plan* out) {
+    if (w.k % S) return false;
+    const int64_t kr = w.k / S;
+    if (kr % w.gs) return false;
+    const int NT = M > 8 ? 2 : 1;
+    const int64_t cseg = code_bytes(w, kr);
+    if (cseg % 16 || w.code_row_bytes % 16) return false;
+    int64_t sseg = 0;
+    if (w.fmt == QM_AFFINE) sseg = kr / w.gs * 2;
+    if (w.fmt == QM_MXFP4) sseg = kr / 32;
+    if (S > 1 && sseg % 16) return false;
+    Params& p = out->p;
+    p.code_seg = static_cast<uint32_t>(cseg);
+    p.code_pitch = round_up(cseg, 128) + 16 * lds_words(w);
+    p.scale_seg = static_cast<uint32_t>(sseg);
+    const uint32_t codes_bytes = kRows * p.code_pitch;
+    const uint32_t sc_bytes = round_up(kRows * sseg, 128);
+    p.off_scales = codes_bytes;
+    p.off_biases = codes_bytes + sc_bytes;
+    p.stage_bytes = round_up(codes_bytes + sc_bytes * (w.fmt == QM_AFFINE ? 2 : 1), 128);
+    const int64_t groups = kr / w.gs;
+    p.off_bars = 0;                                      // full/empty mbarriers, abort flag
+    p.off_tokscale = 512;                                // [16] 2^-E, [16] 2^E
+    p.off_tok = p.off_tokscale + 128;                    // [groups][16] float2
+    p.off_xfrag = round_up(p.off_tok + groups * 16 * 8, 128);
+    const uint64_t xfrag_bytes = static_cast<uint64_t>(kr) * 16 * NT;
+    p.off_partial = round_up(p.off_xfrag + xfrag_bytes, 128);
+    p.n_tiles = (w.n + kRows - 1) / kRows;
+    // clusters: as many as fit one CTA per SM
+    const int sms = num_sms();
+    int64_t G = std::max<int64_t>(1, sms / S);
+    if (S > 1) G = std::max<int64_t>(1, std::min<int64_t>(G, max_clusters(S, max_smem_optin() - 1024)));
+    G = std::min<int64_t>(G, p.n_tiles);
+    int64_t tpc = (p.n_tiles + G - 1) / G;
+    G = (p.n_tiles + tpc - 1) / tpc;
+    const uint64_t partial_bytes = S > 1 ? static_cast<uint64_t>(tpc) * kRows * 16 * 4 : 0;
+    p.off_stages = round_up(p.off_partial + partial_bytes, 1024);
+    const int64_t budget = max_smem_optin() - 1024;
+    const int64_t room = budget - p.off_stages;
+    if (room < 2 * static_cast<int64_t>(p.stage_bytes)) return false;
+    int64_t nst = std::min<int64_t>(kMaxStages, room / p.stage_bytes);
+    nst = std::min<int64_t>(nst, std::max<int64_t>(2, tpc));
+    p.nstage = static_cast<uint32_t>(nst);
+    p.S = S;
+    p.krange = kr;
+    p.tiles_per_cluster = static_cast<int>(tpc);
+    out->S = S;
+    out->grid = G * S;
+    out->smem = p.off_stages + nst * p.stage_bytes;
+    out->ok = true;
+    return true;
+}
+
+// Pick the k split: least per-CTA work (tiles x k range), then fewest splits.
+static Plan make_plan(const WDesc& w, int64_t M) {
+    Plan best;
+    double best_cost = 1e300;
+    for (int S = 1; S <= 8; ++S) {
+        Plan pl;
+        if (!plan_for(w, M, S, &pl)) continue;
+        if (pl.p.nstage < 3 && S < 8) {
+            // prefer a split that keeps three stages in flight
+            Plan more;
+            bool better = false;
+            for (int S2 = S + 1; S2 <= 8 && !better; ++S2)
+                if (plan_for(w, M, S2, &more) && more.p.nstage >= 3) better = true;
+            if (better) continue;
+        }
+        const double cost = static_cast<double>(pl.p.tiles_per_cluster) * pl.p.krange * (1.0 + 0.03 * (S - 1));
+        if (cost < best_cost * 0.999) {
+            best_cost = cost;
+            best = pl;
+        }
+    }
+    return best;
+}
+
+template <int FMT, int BITS, int GS, int NT>
+static cudaError_t launch_t(const Plan& pl, cudaStream_t st) {
+    auto kern = gemv_kernel<FMT, BITS, GS, NT>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(pl.smem));
+    if (e != cudaSuccess) return e;
+    if (pl.S > 1) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        if (e != cudaSuccess) return e;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(pl.grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attrs[2];
+    int na = 0;
+    attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+    if (pl.S > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = pl.S;
+        attrs[na].val.clusterDim.y = 1;
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
+    return cudaLaunchKernelEx(&cfg, kern, pl.p);
+}
+
+}  // namespace gemv
+
+bool gemv_supported(const WDesc& w, int64_t M) {
+    if (M < 1 || M > 16 || w.ndim != 2) return false;
+    return gemv::make_plan(w, M).ok;
+}
+
+qm_status launch_gemv(const WDesc& w, const void* x, int64_t M, void* y, cudaStream_t st) {
+    using namespace gemv;
+    Plan pl = make_plan(w, M);
+    if (!pl.ok) return fail(QM_ENOTSUP, "w: no decode plan for this shape");
+    Params& p = pl.p;
+    p.codes = w.codes;
+    p.scales = w.scales;
+    p.biases = w.biases;
+    p.x = static_cast<const uint16_t*>(x);
+    p.y = static_cast<uint16_t*>(y);
+    p.n = w.n;
+    p.k = w.k;
+    p.M = static_cast<int>(M);
+    p.sdt = w.sdt;
+    p.code_row_bytes = w.code_row_bytes;
+    p.scale_row_bytes = w.scale_row_bytes;
+    const bool two = M > 8;
+    cudaError_t e = cudaErrorInvalidValue;
+#define QM_GEMV_CASE(F, B, G)                                                                  \
+    if (w.fmt == F && (F != QM_AFFINE || (w.bits == B && w.gs == G))) {                         \
+        e = two ? launch_t<F, B, G, 2>(pl, st) : launch_t<F, B, G, 1>(pl, st);                 \
+        goto done;                                                                             \
+    }
+    QM_GEMV_CASE(QM_AFFINE, 4, 32)
+    QM_GEMV_CASE(QM_AFFINE, 4, 64)
+    QM_GEMV_CASE(QM_AFFINE, 4, 128)
+    QM_GEMV_CASE(QM_AFFINE, 8, 32)
+    QM_GEMV_CASE(QM_AFFINE, 8, 64)
+    QM_GEMV_CASE(QM_AFFINE, 8, 128)
+    QM_GEMV_CASE(QM_Q8_0, 8, 32)
+    QM_GEMV_CASE(QM_MXFP4, 4, 32)
+#undef QM_GEMV_CASE
+done:
+    if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
+    return QM_OK;
+}
+
+}  // namespace qm

@@ -1,0 +1,80 @@
+// qm_internal.h -- host-side declarations shared by libqm's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "qm.h"
+
+namespace qm {
+
+// A validated weight: the descriptor flattened to what the kernels read.
+struct WDesc {
+    int fmt = 0;          // qm_format
+    int bits = 0;         // code width (affine 4/8; Q8_0 8; MXFP4 4)
+    int gs = 32;          // values per scale group
+    int sdt = QM_BF16;    // affine scale/bias dtype
+    int ndim = 2;
+    int64_t shape[QM_MAX_NDIM] = {0, 0, 0, 0};
+    int64_t n = 0, k = 0;
+    int64_t rows = 0;     // product of all axes but the last
+    const uint8_t* codes = nullptr;
+    const uint8_t* scales = nullptr;
+    const uint8_t* biases = nullptr;
+    int64_t code_row_bytes = 0;   // bytes of one row (k values) of codes
+    int64_t scale_row_bytes = 0;  // bytes of one row of scales (0 if none)
+    int64_t bias_row_bytes = 0;   // bytes of one row of biases (0 if none)
+};
+
+// Thread-local error message of the calling thread (qm_last_error()).
+void set_error(const std::string& msg);
+qm_status fail(qm_status st, const std::string& msg);
+qm_status cuda_fail(cudaError_t e, const char* what);
+
+// Validates w and fills d. On failure sets the message and returns QM_EINVAL.
+qm_status validate_weight(const qm_weight* w, WDesc* d);
+
+int dtype_size(int dt);
+
+// Number of SMs on the current device (cached per device).
+int num_sms();
+// Opt-in shared memory per block on the current device (cached per device).
+int max_smem_optin();
+
+// ------------------------------------------------------------ launchers
+// Each returns the CUDA error of its launch (cudaSuccess when nothing ran).
+cudaError_t launch_dequant(const WDesc& w, int out_dtype, void* out, cudaStream_t st);
+cudaError_t launch_take_packed(const uint8_t* src, int64_t outer, int64_t len, int64_t inner_bytes,
+                               const void* ids, int id64, int64_t n_ids, uint8_t* dst,
+                               cudaStream_t st);
+cudaError_t launch_take_dense(const WDesc& w, int axis, const void* ids, int id64, int64_t n_ids,
+                              int out_dtype, void* out, cudaStream_t st);
+
+// y [M, n] = x [M, k] * W^T for a 2-d weight, M <= 16, x and y bf16.
+qm_status launch_gemv(const WDesc& w, const void* x, int64_t M, void* y, cudaStream_t st);
+bool gemv_supported(const WDesc& w, int64_t M);
+// Tensor-core product for larger M (tcgen05); returns QM_ENOTSUP if the
+// shape is outside what the kernel handles.
+qm_status launch_gemm(const WDesc& w, const void* x, int64_t M, void* y, cudaStream_t st);
+bool gemm_supported(const WDesc& w, int64_t M);
+// Plain reference-order kernel for shapes the fast paths refuse.
+cudaError_t launch_apply_simple(const WDesc& w, const void* x, int64_t M, void* y,
+                                cudaStream_t st);
+
+// Experts.
+size_t experts_workspace_bytes(int64_t P, int64_t E);
+cudaError_t launch_route(const void* ids, int id64, int64_t P, int64_t E, int32_t* counts,
+                         int32_t* offsets, int32_t* perm, void* ws, cudaStream_t st);
+qm_status launch_experts(const WDesc& w, const void* ids, int id64, int64_t T, int64_t topk,
+                         const void* x, int64_t x_rows, void* y, void* ws, size_t ws_bytes,
+                         cudaStream_t st);
+
+// Per-translation-unit device error flags: read-and-clear (after a sync).
+uint32_t elementwise_read_clear_error();
+uint32_t gemv_read_clear_error();
+uint32_t gemm_read_clear_error();
+uint32_t experts_read_clear_error();
+
+}  // namespace qm

@@ -1,0 +1,136 @@
+"""The C boundary on the host: the library loads, exports what include/qm.h
+declares, and refuses bad arguments naming the part -- all without a GPU
+(every case here fails validation before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import packed_qmatmul_gb300 as qm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from packed_qmatmul_gb300 import build
+
+    build.build()
+    return qm.load_library()
+
+
+def _declared():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", f)).read()
+            names |= set(re.findall(r"^\s*(?:qm_status|size_t|const char\*|int32_t)\s+(qm_\w+)\s*\(",
+                                    text, re.M))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    names = _declared()
+    assert {"qm_dequant", "qm_apply", "qm_take", "qm_apply_experts", "qm_experts_route",
+            "qm_apply_experts_workspace", "qm_device_status", "qm_last_error"} <= names
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_version(lib):
+    assert lib.qm_version() >= 100
+
+
+def _w(fmt=qm.QM_AFFINE, bits=4, gs=64, shape=(16, 64), codes=256, scales=512, biases=768, ndim=2):
+    w = qm._CWeight()
+    w.format, w.bits, w.group_size, w.scale_dtype, w.ndim = fmt, bits, gs, qm.QM_BF16, ndim
+    for i, s in enumerate(shape):
+        w.shape[i] = s
+    w.codes, w.scales, w.biases = codes, scales, biases
+    return w
+
+
+def _dequant_err(lib, w, out=1024, dt=qm.QM_BF16):
+    st = lib.qm_dequant(ctypes.byref(w), dt, out, None)
+    return st, lib.qm_last_error().decode()
+
+
+@pytest.mark.parametrize("mut,part", [
+    (dict(shape=(16, 48)), "codes"),          # k not a multiple of 32
+    (dict(bits=3), "w"),
+    (dict(gs=16), "w"),
+    (dict(shape=(16, 96), gs=64), "scales"),  # k not a multiple of group_size
+    (dict(codes=0), "codes"),
+    (dict(codes=264), "codes"),                # misaligned
+    (dict(scales=0), "scales"),
+    (dict(biases=8), "biases"),
+    (dict(fmt=7), "w"),
+    (dict(ndim=1), "w"),
+    (dict(fmt=qm.QM_Q8_0, bits=0, gs=0), "scales"),  # Q8_0 takes no scales part
+    (dict(fmt=qm.QM_MXFP4, bits=0, gs=0, scales=512), "biases"),
+])
+def test_invalid_weights_name_the_part(lib, mut, part):
+    st, msg = _dequant_err(lib, _w(**mut))
+    assert st == qm.QM_EINVAL
+    assert msg.startswith(part + ":"), msg
+
+
+def test_invalid_output(lib):
+    st, msg = _dequant_err(lib, _w(), out=0)
+    assert st == qm.QM_EINVAL and msg.startswith("out:")
+    st, msg = _dequant_err(lib, _w(), dt=9)
+    assert st == qm.QM_EINVAL and msg.startswith("out:")
+
+
+def test_empty_weight_is_ok(lib):
+    st, _ = _dequant_err(lib, _w(shape=(0, 64), codes=0, scales=0, biases=0), out=0)
+    assert st == qm.QM_OK
+
+
+def test_take_axis_rules(lib):
+    w = _w(shape=(3, 16, 64), ndim=3)
+    for axis, ok in ((2, False), (-1, False), (3, False), (-4, False)):
+        st = lib.qm_take(ctypes.byref(w), axis, 4096, qm.QM_I32, 4, 2048, 2304, 2560, qm.QM_BF16,
+                         None, None)
+        assert st == qm.QM_EINVAL and lib.qm_last_error().decode().startswith("axis:")
+
+
+def test_take_needs_an_output(lib):
+    st = lib.qm_take(ctypes.byref(_w()), 0, 4096, qm.QM_I32, 4, None, None, None, qm.QM_BF16, None,
+                     None)
+    assert st == qm.QM_EINVAL and lib.qm_last_error().decode().startswith("out:")
+
+
+def test_apply_validation(lib):
+    w = _w()
+    st = lib.qm_apply(ctypes.byref(w), 4096, 1, qm.QM_F16, 8192, None)
+    assert st == qm.QM_ENOTSUP and lib.qm_last_error().decode().startswith("x:")
+    st = lib.qm_apply(ctypes.byref(w), 4096, -1, qm.QM_BF16, 8192, None)
+    assert st == qm.QM_EINVAL
+    st = lib.qm_apply(ctypes.byref(w), 4096, 0, qm.QM_BF16, 8192, None)  # M = 0: nothing to do
+    assert st == qm.QM_OK
+    w3 = _w(shape=(2, 16, 64), ndim=3)
+    st = lib.qm_apply(ctypes.byref(w3), 4096, 1, qm.QM_BF16, 8192, None)
+    assert st == qm.QM_ENOTSUP and lib.qm_last_error().decode().startswith("w:")
+
+
+def test_experts_validation(lib):
+    w2 = _w()
+    st = lib.qm_apply_experts(ctypes.byref(w2), 4096, qm.QM_I32, 4, 2, 8192, 4, qm.QM_BF16, 16384,
+                              32768, 1 << 20, None)
+    assert st == qm.QM_EINVAL and lib.qm_last_error().decode().startswith("w:")
+    w3 = _w(shape=(4, 16, 64), ndim=3)
+    st = lib.qm_apply_experts(ctypes.byref(w3), 4096, qm.QM_I32, 4, 2, 8192, 5, qm.QM_BF16, 16384,
+                              32768, 1 << 20, None)
+    assert st == qm.QM_EINVAL and lib.qm_last_error().decode().startswith("x:")
+    st = lib.qm_apply_experts(ctypes.byref(w3), 4096, qm.QM_I32, 4, 2, 8192, 4, qm.QM_BF16, 16384,
+                              32768, 16, None)
+    assert st == qm.QM_EINVAL and lib.qm_last_error().decode().startswith("workspace:")
+
+
+def test_workspace_query(lib):
+    assert lib.qm_apply_experts_workspace(0, 4, 32) == 0
+    a = lib.qm_apply_experts_workspace(64, 4, 32)
+    b = lib.qm_apply_experts_workspace(4096, 4, 32)
+    assert 0 < a < b and a % 256 == 0 and b % 256 == 0

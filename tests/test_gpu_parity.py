@@ -1,0 +1,262 @@
+"""Parity of the CUDA path (through the C entry points) with the oracle.
+
+Dequant, take and routing must match bit for bit (NaN payloads aside);
+products must meet the stated bound element by element (see
+wutil.check_product) and the relative Frobenius bound.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import packed_qmatmul_gb300 as qm
+from packed_qmatmul_gb300 import synth
+from wutil import bf16_to_f64, check_product, row_norms, to_oracle
+
+pytestmark = pytest.mark.gpu
+
+ODT = {torch.float32: oracle.F32, torch.bfloat16: oracle.BF16, torch.float16: oracle.F16}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    from packed_qmatmul_gb300 import build
+
+    build.build()
+    qm.load_library()
+    torch.cuda.set_device(0)
+
+
+def _host(t: torch.Tensor) -> np.ndarray:
+    """Device tensor -> NumPy with the same bytes (16-bit floats as uint16)."""
+    t = t.detach().cpu()
+    if t.dtype in (torch.bfloat16, torch.float16):
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def _dev_bf16(bits: np.ndarray) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).cuda().view(torch.bfloat16)
+
+
+def _bits_equal(a: np.ndarray, b: np.ndarray, dt) -> bool:
+    """Equal bit patterns, with every NaN equal to every other NaN."""
+    if dt == torch.float32:
+        fa, fb = a.astype(np.float32), b.astype(np.float32)
+        nan = np.isnan(fa)
+        return np.array_equal(nan, np.isnan(fb)) and np.array_equal(fa[~nan].view(np.uint32),
+                                                                     fb[~nan].view(np.uint32))
+    ea = (a & 0x7F80) == 0x7F80 if dt == torch.bfloat16 else (a & 0x7C00) == 0x7C00
+    ma = (a & 0x7F) != 0 if dt == torch.bfloat16 else (a & 0x3FF) != 0
+    eb = (b & 0x7F80) == 0x7F80 if dt == torch.bfloat16 else (b & 0x7C00) == 0x7C00
+    mb = (b & 0x7F) != 0 if dt == torch.bfloat16 else (b & 0x3FF) != 0
+    na, nb = ea & ma, eb & mb
+    return np.array_equal(na, nb) and np.array_equal(a[~na], b[~nb])
+
+
+KINDS = ["affine4_g32", "affine4_g64", "affine4_g128", "affine8_g32", "affine8_g64",
+         "affine8_g128", "q8_0", "mxfp4"]
+
+
+def _make(kind, g, n, k, lead=()):
+    if kind.startswith("affine"):
+        bits = int(kind[6])
+        gs = int(kind.split("_g")[1])
+        return synth.affine_weight(g, n, k, bits=bits, group_size=gs, lead=lead)
+    if kind == "q8_0":
+        return synth.q8_0_weight(g, n, k, lead=lead)
+    return synth.mxfp4_weight(g, n, k, lead=lead)
+
+
+# ---------------------------------------------------------------- dequant
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16, torch.float16])
+def test_dequant_bit_exact(kind, dt):
+    g = synth.rng(100)
+    for n, k, lead in ((37, 256, ()), (5, 1024, (3,)), (1, 128, (2, 2))):
+        w = _make(kind, g, n, k, lead)
+        got = _host(qm.dequant(qm.QWeight.from_arrays(w), dt))
+        want = oracle.dequant(to_oracle(w), ODT[dt])
+        assert _bits_equal(got, want, dt), (kind, n, k, lead)
+
+
+def test_dequant_config1_seed0():
+    w, _ = synth.small_affine_config(0)
+    got = _host(qm.dequant(qm.QWeight.from_arrays(w), torch.bfloat16))
+    assert np.array_equal(got, oracle.dequant(to_oracle(w), oracle.BF16))
+
+
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16, torch.float16])
+def test_dequant_mxfp4_every_code_and_scale(dt):
+    k = 32 * 256
+    codes = np.tile(np.array([(2 * i % 16) | (((2 * i + 1) % 16) << 4) for i in range(16)], np.uint8),
+                    256).reshape(1, k // 2)
+    scales = np.arange(256, dtype=np.uint8).reshape(1, 256)
+    w = dict(format="mxfp4", shape=(1, k), codes=codes, scales=scales, biases=None)
+    got = _host(qm.dequant(qm.QWeight.from_arrays(w), dt))
+    assert _bits_equal(got, oracle.dequant(to_oracle(w), ODT[dt]), dt)
+
+
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16, torch.float16])
+def test_dequant_q8_0_every_scale_and_quant(dt):
+    d = np.arange(65536, dtype=np.uint16)
+    q = np.arange(-128, 128, dtype=np.int16).astype(np.int8)
+    blocks = np.empty((65536, 8, 34), np.uint8)
+    blocks[:, :, 0] = (d & 0xFF)[:, None]
+    blocks[:, :, 1] = (d >> 8)[:, None]
+    blocks[:, :, 2:] = q.view(np.uint8).reshape(8, 32)[None]
+    w = dict(format="q8_0", shape=(65536, 256), codes=blocks.reshape(65536, 272))
+    got = _host(qm.dequant(qm.QWeight.from_arrays(w), dt))
+    assert _bits_equal(got, oracle.dequant(to_oracle(w), ODT[dt]), dt)
+
+
+# ---------------------------------------------------------------- take
+@pytest.mark.parametrize("kind", ["affine4_g64", "affine8_g32", "q8_0", "mxfp4"])
+@pytest.mark.parametrize("id64", [False, True])
+def test_take_packed_and_dense(kind, id64):
+    g = synth.rng(200)
+    for lead, axis in (((), 0), ((3,), 0), ((3,), 1), ((2, 3), 1)):
+        w = _make(kind, g, 24, 256, lead)
+        ow = to_oracle(w)
+        L = ow.shape[axis]
+        ids = np.array([L - 1, 0, -1, L, 2, 2, -L, 1, L + 7], dtype=np.int64 if id64 else np.int32)
+        tw, dense = qm.take(qm.QWeight.from_arrays(w), axis, torch.from_numpy(ids).cuda(),
+                            dense_dtype=torch.bfloat16)
+        ot = oracle.take(ow, axis, ids)
+        for name, part in (("codes", tw.codes), ("scales", tw.scales), ("biases", tw.biases)):
+            want = ot.parts()[name]
+            if want is None:
+                assert part is None
+                continue
+            assert np.array_equal(_host(part).view(np.uint8).reshape(-1),
+                                  want.view(np.uint8).reshape(-1)), (kind, lead, axis, name)
+        assert np.array_equal(_host(dense), oracle.dequant(ot, oracle.BF16)), (kind, lead, axis)
+
+
+def test_take_embedding_shape():
+    # the embedding-table shape, scaled down: affine 4-bit gs64, k = 1024
+    g = synth.rng(4)
+    w = synth.affine_weight(g, 4096, 1024, bits=4, group_size=64)
+    ids = synth.uniform_ids(g, 512, 4096)
+    tw, dense = qm.take(qm.QWeight.from_arrays(w), 0, torch.from_numpy(ids).cuda(),
+                        dense_dtype=torch.bfloat16)
+    ot = oracle.take(to_oracle(w), 0, ids)
+    assert np.array_equal(_host(tw.codes).view(np.uint32), ot.codes)
+    assert np.array_equal(_host(dense), oracle.dequant(ot, oracle.BF16))
+
+
+# ---------------------------------------------------------------- products
+def _check_apply(w, x, what):
+    ow = to_oracle(w)
+    y = qm.apply(qm.QWeight.from_arrays(w), _dev_bf16(x))
+    got = bf16_to_f64(_host(y))
+    ref = oracle.apply(ow, x)
+    xn = np.linalg.norm(oracle.decode_array(x, oracle.BF16), axis=1)
+    return check_product(got, ref, row_norms(ow), xn, ow.k, what)
+
+
+@pytest.mark.parametrize("kind", KINDS)
+@pytest.mark.parametrize("M", [1, 2, 3, 8, 9, 16])
+def test_apply_decode(kind, M):
+    g = synth.rng(300 + M)
+    for n, k in ((48, 256), (300, 512), (17, 1024)):
+        w = _make(kind, g, n, k)
+        x = synth.activations(g, M, k)
+        _check_apply(w, x, f"{kind} M={M} n={n} k={k}")
+
+
+@pytest.mark.parametrize("M", [1, 8])
+def test_apply_config1_seed0(M):
+    w, xs = synth.small_affine_config(0)
+    _check_apply(w, xs[M], f"config1 M={M}")
+
+
+@pytest.mark.parametrize("kind", ["affine4_g64", "affine8_g64", "q8_0", "mxfp4"])
+def test_apply_split_k(kind):
+    # few rows, long k: the decode path splits k over a cluster
+    g = synth.rng(400)
+    for n, k, M in ((64, 4096, 1), (40, 14336, 4), (1024, 3072, 2)):
+        w = _make(kind, g, n, k)
+        x = synth.activations(g, M, k)
+        _check_apply(w, x, f"{kind} split n={n} k={k} M={M}")
+
+
+@pytest.mark.parametrize("kind", ["affine4_g64", "q8_0", "mxfp4"])
+def test_apply_larger_m(kind):
+    g = synth.rng(500)
+    for n, k, M in ((64, 256, 17), (96, 512, 33)):
+        w = _make(kind, g, n, k)
+        x = synth.activations(g, M, k)
+        _check_apply(w, x, f"{kind} n={n} k={k} M={M}")
+
+
+def test_apply_activation_range():
+    # activations far from 1 in magnitude: the power-of-two rescale keeps them exact
+    g = synth.rng(600)
+    w = _make("affine4_g64", g, 64, 512)
+    for sigma in (1e-30, 1e-6, 1e4, 1e30):
+        x = synth.activations(g, 4, 512, sigma=sigma)
+        _check_apply(w, x, f"sigma={sigma}")
+
+
+def test_apply_deterministic():
+    g = synth.rng(700)
+    w = _make("q8_0", g, 256, 4096)
+    qw = qm.QWeight.from_arrays(w)
+    x = _dev_bf16(synth.activations(g, 4, 4096))
+    a = _host(qm.apply(qw, x))
+    b = _host(qm.apply(qw, x))
+    assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------- routing and experts
+@pytest.mark.parametrize("id64", [False, True])
+def test_route_bit_exact(id64):
+    g = synth.rng(800)
+    for E, T, topk in ((32, 64, 4), (8, 700, 2), (3, 5, 1), (256, 1024, 8)):
+        ids = synth.expert_ids(g, T, topk, E).astype(np.int64 if id64 else np.int32)
+        flat = ids.reshape(-1)
+        flat[::7] = -1
+        flat[3::11] = E + 3
+        counts, offsets, perm = qm.route(torch.from_numpy(ids).cuda(), E)
+        oc, oo, op, n_out = oracle.route(ids, E)
+        assert np.array_equal(counts.cpu().numpy(), oc)
+        assert np.array_equal(offsets.cpu().numpy(), oo)
+        pm = perm.cpu().numpy()
+        assert np.array_equal(pm[: oo[E]], op)
+        out_pos = np.where((flat < 0) | (flat >= E))[0]
+        assert np.array_equal(pm[oo[E]:], out_pos)
+
+
+@pytest.mark.parametrize("kind", ["affine4_g64", "q8_0", "mxfp4"])
+@pytest.mark.parametrize("broadcast", [True, False])
+def test_apply_experts_small(kind, broadcast):
+    g = synth.rng(900)
+    E, n, k, T, topk = 4, 40, 256, 6, 2
+    w = _make(kind, g, n, k, lead=(E,))
+    ids = synth.expert_ids(g, T, topk, E)
+    ids[1, 0] = -1
+    ids[4, 1] = E
+    x = synth.activations(g, T if broadcast else T * topk, k)
+    if broadcast:
+        x[1] = 0x7FC0  # NaN row: its in-range position sees it, the other gives zeros
+    else:
+        x[2] = 0x7FC0  # position (1, 0), out of range: zeros whatever the row holds
+    ow = to_oracle(w)
+    y = qm.apply_experts(qm.QWeight.from_arrays(w), torch.from_numpy(ids).cuda(), _dev_bf16(x))
+    got = bf16_to_f64(_host(y)).reshape(T * topk, n)
+    ref = oracle.apply_experts(ow, ids, x).reshape(T * topk, n)
+    flat = ids.reshape(-1)
+    out = (flat < 0) | (flat >= E)
+    assert np.all(got[out] == 0) and not np.any(np.signbit(got[out]))
+    ok = ~out & np.all(np.isfinite(ref), axis=1)
+    rows = np.where(ok)[0]
+    xr = rows // topk if broadcast else rows
+    xn = np.linalg.norm(oracle.decode_array(x, oracle.BF16), axis=1)[xr]
+    wn = row_norms(ow).reshape(E, n)[flat[rows]]
+    bound = 1e-2 * xn[:, None] * wn / np.sqrt(k)
+    err = np.abs(got[rows] - ref[rows])
+    from wutil import bf16_half_ulp
+    assert np.all(err <= bound + bf16_half_ulp(got[rows])), err.max()
+    nanrows = ~out & ~np.all(np.isfinite(ref), axis=1)
+    assert np.all(np.isnan(got[nanrows]))
