@@ -1,0 +1,401 @@
+"""Benchmark: packed-weight GB/s of the M = 1 decode product on one GB300.
+
+Workload (one step): the decode-time products of a Qwen3-0.6B-shaped stack
+with MLX affine 4-bit, group-size-64 weights -- 28 layers of q_proj 2048x1024,
+k_proj and v_proj 1024x1024, gate_proj and up_proj 3072x1024, down_proj
+1024x3072, plus lm_head 151936x1024 -- 169 qm_apply calls on distinct
+weights (302 MB packed, more than the 129 MB L2), each on its own synthetic
+bf16 activation row. The step is captured once in a CUDA graph and replayed.
+
+`value` is packed weight bytes per second over the timed steps (inputs
+resident in HBM); `e2e` repeats the step with its activations copied in from
+pinned host memory and every result copied back, inside the timed region.
+
+--impl reference times the oracle (oracle/, plain C in float64) on the host
+cores over a bounded sample of the same workload. Under torchrun (N > 1) each
+rank runs an independent replica (the product does not shard here).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from packed_qmatmul_gb300 import synth  # noqa: E402
+
+LAYERS = synth.QWEN3_0_6B_LAYERS
+SHAPES = synth.QWEN3_0_6B_LAYER
+LM_HEAD = synth.QWEN3_0_6B_LM_HEAD
+METRIC = "packed-weight GB/s (M=1 GEMV)"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--bits", type=int, default=4)
+    ap.add_argument("--M", type=int, default=1)
+    ap.add_argument("--no-detail", action="store_true", help="skip the secondary measurements")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
+    ap.add_argument("--only", default=None,
+                    help="profiling aid: a step of just the projections whose name ends with this")
+    return ap.parse_args()
+
+
+def workload_list(bits):
+    """[(name, n, k)] for one step, in call order."""
+    out = []
+    for layer in range(LAYERS):
+        for name, (n, k) in SHAPES.items():
+            out.append((f"layers.{layer}.{name}", n, k))
+    out.append(("lm_head", *LM_HEAD))
+    return out
+
+
+def packed_bytes(n, k, bits, gs=64):
+    return n * k * bits // 8 + 2 * n * (k // gs) * 2
+
+
+def config_dict(bits, M):
+    return {
+        "workload": f"qwen3-0.6b-shaped decode step: 28 x (q 2048x1024, k/v 1024x1024, gate/up "
+                    f"3072x1024, down 1024x3072) + lm_head 151936x1024, MLX affine {bits}-bit gs64, "
+                    f"M={M}, 169 qm_apply calls on distinct weights",
+        "format": "mlx_affine", "bits": bits, "group_size": 64, "M": M,
+        "weight_bytes_per_step": sum(packed_bytes(n, k, bits) for _, n, k in workload_list(bits)),
+        "l2": "inputs larger than L2 (distinct weights per layer, 302 MB at 4-bit)",
+        "graph": "step captured once as a CUDA graph",
+    }
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples during the timed region (clocks and throttle reasons)."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = float(f[2])
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our arm
+def build_step(bits, M, device, only=None):
+    import torch
+
+    import packed_qmatmul_gb300 as qm
+
+    g = synth.rng(1)
+    items = []
+    for name, n, k in workload_list(bits):
+        if only and not name.endswith(only):
+            continue
+        w = synth.affine_weight(g, n, k, bits=bits, group_size=64)
+        qw = qm.QWeight.from_arrays(w, device)
+        x = torch.from_numpy(synth.activations(g, M, k).view(np.int16)).to(device).view(torch.bfloat16)
+        y = torch.empty((M, n), dtype=torch.bfloat16, device=device)
+        items.append((name, n, k, qw, x, y))
+    return items
+
+
+def time_graph(step, stream, steps, warmup, clock_index=None):
+    """Captures `step` once as a CUDA graph; returns (seconds for `steps`
+    replays timed with CUDA events on `stream`, clock summary or None)."""
+    import torch
+
+    with torch.cuda.stream(stream):
+        step()
+    stream.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        step()
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            graph.replay()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clk = ClockSampler(clock_index) if clock_index is not None else None
+    if clk:
+        clk.__enter__()
+        time.sleep(0.3)  # let the sampler start
+    ev0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(steps):
+            graph.replay()
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    if clk:
+        clk.__exit__(None, None, None)
+    return ev0.elapsed_time(ev1) / 1e3, (clk.summary() if clk else None)
+
+
+def run_ours(args, rank, world):
+    import torch
+
+    import packed_qmatmul_gb300 as qm
+    from packed_qmatmul_gb300 import build as qbuild
+
+    qbuild.build()
+    qm.load_library()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    bits, M = args.bits, args.M
+    items = build_step(bits, M, dev, args.only)
+    step_bytes = sum(packed_bytes(n, k, bits) for _, n, k, *_ in items)
+    algo_bytes = step_bytes + sum(2 * M * (n + k) for _, n, k, *_ in items)
+    launches_per_step = len(items)
+    stream = torch.cuda.Stream()
+
+    def step():
+        for _, _, _, qw, x, y in items:
+            qm.qm_apply(qw, x, y, stream)
+
+    dist = world > 1
+    if dist:
+        import torch.distributed as tdist
+        tdist.barrier()
+    elapsed, clocks = time_graph(step, stream, args.steps, args.warmup, dev.index)
+    qm.qm_device_status(stream)
+    if dist:
+        t = torch.tensor([elapsed], device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        elapsed = float(t.item())
+        tdist.barrier()
+    ms_per_step = elapsed / args.steps * 1e3
+    value = step_bytes * args.steps * world / elapsed / 1e9
+    avg_launch = elapsed / (args.steps * launches_per_step)
+    achieved = algo_bytes / launches_per_step / avg_launch / 1e9
+
+    e2e = run_e2e(items, stream, args, step_bytes)
+
+    peaks = load_peaks()
+    peak = peaks.get("hbm_gbs", 6800.0)
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; weights and activations drawn as the workload states)",
+        "config": config_dict(bits, M),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": f"gemv_kernel<affine,{bits},64> (every launch of the step)",
+                     "peak_source": "measured" if "hbm_gbs" in peaks else "fallback"},
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    if args.only:
+        res["config"]["workload"] += f" (profiling aid: only *{args.only})"
+    if not args.no_detail and not args.only and rank == 0:
+        res["detail"] = detail_measurements(args, dev, stream)
+    return res
+
+
+def run_e2e(items, stream, args, step_bytes):
+    """Same step through the public API with host buffers: H2D of every
+    activation row from pinned memory, the products, D2H of every result."""
+    import torch
+
+    import packed_qmatmul_gb300 as qm
+
+    hx = [x.cpu().pin_memory() for *_, x, _ in items]
+    hy = [torch.empty(y.shape, dtype=y.dtype).pin_memory() for *_, y in items]
+    h2d = sum(t.numel() * t.element_size() for t in hx)
+    d2h = sum(t.numel() * t.element_size() for t in hy)
+
+    def step():
+        for (_, _, _, qw, x, y), a, b in zip(items, hx, hy):
+            x.copy_(a, non_blocking=True)
+            qm.qm_apply(qw, x, y, stream)
+            b.copy_(y, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            step()
+    stream.synchronize()
+    steps = max(1, min(args.steps, 20))
+    t0 = time.perf_counter()
+    with torch.cuda.stream(stream):
+        for _ in range(steps):
+            step()
+    stream.synchronize()
+    el = time.perf_counter() - t0
+    return {"value": round(step_bytes * steps / el / 1e9, 2), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "note": "qm_apply per projection, no graph; activations H2D and results D2H each step"}
+
+
+def detail_measurements(args, dev, stream):
+    """Secondary numbers (not the headline): 8-bit and M in {2, 4, 8}."""
+    import torch
+
+    import packed_qmatmul_gb300 as qm
+
+    out = {}
+    for bits, M in ((8, 1), (4, 2), (4, 4), (4, 8)):
+        items = build_step(bits, M, dev)
+        sb = sum(packed_bytes(n, k, bits) for _, n, k, *_ in items)
+
+        def step():
+            for _, _, _, qw, x, y in items:
+                qm.qm_apply(qw, x, y, stream)
+
+        reps = 20
+        el, _ = time_graph(step, stream, reps, 3)
+        out[f"affine{bits}_M{M}"] = {"GB/s": round(sb * reps / el / 1e9, 1),
+                                     "ms_per_step": round(el / reps * 1e3, 4)}
+        del items
+        torch.cuda.empty_cache()
+    return out
+
+
+def load_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f)
+    except OSError:
+        return {}
+
+
+# ---------------------------------------------------------------- oracle (CPU)
+def oracle_sample(bits):
+    """One twenty-eighth of the step: one layer's six projections and 1/28 of
+    lm_head's rows -- the same mix of shapes, so the same rate."""
+    g = synth.rng(1)
+    items = []
+    for name, (n, k) in SHAPES.items():
+        items.append((n, k, synth.affine_weight(g, n, k, bits=bits, group_size=64),
+                      synth.activations(g, 1, k)))
+    n, k = LM_HEAD
+    nh = n // LAYERS
+    items.append((nh, k, synth.affine_weight(g, nh, k, bits=bits, group_size=64),
+                  synth.activations(g, 1, k)))
+    return items
+
+
+def time_oracle(bits, min_seconds=10.0, reps=None):
+    import oracle
+
+    items = oracle_sample(bits)
+    ows = [(oracle.Weight(oracle.AFFINE, w["shape"], w["codes"], w["scales"], w["biases"], bits=bits,
+                          group_size=64), x) for n, k, w, x in items]
+    sb = sum(packed_bytes(n, k, bits) for n, k, _, _ in items)
+    oracle.apply(*ows[0])  # build + page in
+    done, t0 = 0, time.perf_counter()
+    while True:
+        for w, x in ows:
+            oracle.apply(w, x)
+        done += 1
+        el = time.perf_counter() - t0
+        if (reps is not None and done >= reps) or (reps is None and el >= min_seconds):
+            break
+    return sb * done / el / 1e9, el, done, oracle.num_threads()
+
+
+def cpu_baseline(bits):
+    v, el, reps, cores = time_oracle(bits, min_seconds=10.0)
+    return {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"1/28 of the step (one layer's 6 projections + 5426 lm_head rows), "
+                      f"repeated {reps}x in {el:.1f} s"}
+
+
+def run_reference(args):
+    import oracle
+
+    oracle.build()
+    bits = args.bits
+    for _ in range(args.warmup):
+        time_oracle(bits, reps=1)
+    v, el, reps, cores = time_oracle(bits, reps=max(1, args.steps))
+    return {"impl": "reference", "metric": METRIC, "value": round(v, 4), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(el / reps * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config_dict(bits, 1),
+            "cpu_baseline": {"value": round(v, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+                             "sample": "each step: 1/28 of the workload (one layer's six "
+                                       "projections + 5426 lm_head rows)"},
+            "e2e": {"value": round(v, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)))
+        return
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.init_process_group("nccl")
+    res = run_ours(args, rank, world)
+    if rank == 0 and not args.no_cpu:
+        res["cpu_baseline"] = cpu_baseline(args.bits)
+    if rank == 0:
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as tdist
+        tdist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
