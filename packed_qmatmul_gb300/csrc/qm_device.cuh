@@ -72,6 +72,11 @@ QM_DEV bool mbar_wait(uint32_t bar, uint32_t parity) {
     }
 }
 
+// Named barrier `id` (1..15) over `count` threads (a multiple of 32).
+QM_DEV void named_bar_sync(uint32_t id, uint32_t count) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // ---------------------------------------------------------------- bulk copies
 // Global -> shared bulk copy completing on an mbarrier. dst, src and bytes
 // must be multiples of 16.

@@ -9,19 +9,23 @@
 // are float32 sums.
 //
 // Design (one GB300: 152 SMs, HBM3e):
-//  * A CTA is 1 producer warp + 8 consumer warps. The producer streams
-//    16-row stages of the packed weight (codes, scales, biases) into shared
-//    memory with cp.async.bulk, one copy per row, completing on mbarriers.
-//  * Each consumer warp takes whole stages: 16 rows x the CTA's k range. It
+//  * A CTA is 1 producer warp + 16 consumer warps. The producer bulk-copies
+//    the activation rows once, then streams 32-row stages of the packed
+//    weight (codes, scales, biases) into shared memory with cp.async.bulk,
+//    completing on mbarriers.
+//  * Consumer warps form teams of T. A team takes whole stages; its warps
+//    split the stage's groups along k, so a stage is worked on by T warps at
+//    once and each warp carries two independent 16-row MMA tiles. A warp
 //    decodes codes in registers to f16 pairs that hold exact integers
-//    (1024 + code, via a magic-exponent OR), and multiplies them with the
-//    activations on mma.sync m16n8k16 (rows of W as the M side, tokens as the
-//    N side). Per group it applies scale (and bias) in float32.
+//    (1024 + code, by a magic-exponent OR) and multiplies them with the
+//    activations on mma.sync m16n8k16 (rows of W on the M side, tokens on
+//    the N side); per group it applies scale (and bias) in float32. The team
+//    adds its warps' partial sums in warp order through shared memory.
 //  * Activations are rescaled per token by a power of two so that every bf16
 //    value is exact in f16; the scale is undone at the end.
-//  * Where one CTA per 16-row tile would leave SMs idle, a cluster of S CTAs
-//    splits k; the partial sums meet through distributed shared memory and
-//    are added in rank order (deterministic, no global scratch).
+//  * Where one CTA per stage would leave SMs idle, a cluster of S CTAs splits
+//    k; their partial sums meet through distributed shared memory and are
+//    added in rank order (deterministic, no global scratch).
 //
 // MLX affine codes: "GPTQModel wiki: MLX Apple Silicon", "Packed layouts and
 // exact transcoding" (little-endian code stream) and "Concepts ..."
@@ -47,9 +51,9 @@ uint32_t gemv_read_clear_error() {
 
 namespace gemv {
 
-constexpr int kRows = 16;            // rows per stage (one MMA row tile)
-constexpr int kConsumerWarps = 8;
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kRows = 32;            // rows per stage (two MMA row tiles)
+constexpr int kWarps = 16;           // consumer warps
+constexpr int kThreads = (kWarps + 1) * 32;
 constexpr int kMaxStages = 16;
 constexpr uint32_t kMagic = 0x64006400u;  // f16x2 (1024, 1024)
 
@@ -66,20 +70,15 @@ struct Params {
     // decomposition
     int S;                   // CTAs per cluster, splitting k
     int64_t krange;          // k values per CTA
-    int tiles_per_cluster;   // 16-row tiles per cluster
-    int64_t n_tiles;
+    int stages_per_cluster;  // 32-row stages per cluster
+    int64_t n_stages;        // 32-row stages in all
+    int team;                // warps per team (1, 2, 4, 8 or 16)
     // shared memory layout (byte offsets from the dynamic smem base)
     uint32_t nstage, stage_bytes;
-    uint32_t code_seg, code_pitch;   // per row: bytes copied, smem pitch
-    uint32_t scale_seg;              // per row bytes of scales (and biases) in the stage
-    uint32_t off_scales, off_biases; // within a stage
-    uint32_t off_bars, off_xfrag, off_tok, off_tokscale, off_partial, off_stages;
-};
-
-// Format traits: codes per 32-bit word, MMAs per group, offset of the magic.
-template <int FMT, int BITS, int GS>
-struct Fmt {
-    static constexpr int kMmas = GS / 16;  // MMAs (k16) per group
+    uint32_t code_seg, code_pitch;    // per row: bytes copied, smem pitch
+    uint32_t scale_seg;               // per row bytes of scales (and of biases) in a stage
+    uint32_t off_scales, off_biases;  // within a stage
+    uint32_t off_tokscale, off_tok, off_xfrag, off_red, off_xraw, off_stages;
 };
 
 // ---------------------------------------------------------------- decoders
@@ -97,15 +96,97 @@ QM_DEV void dec8(uint32_t w, uint32_t& lo, uint32_t& hi) {
     hi = prmt(w, 0x64646464u, 0x7362);
 }
 
-template <int NT>
-struct Acc {
-    float v[NT][4];
-};
+QM_DEV float sval(uint32_t h, int sdt) { return sdt == QM_F16 ? f16_bits_to_f32(h) : bf16_bits_to_f32(h); }
 
-// Per-group weight scale data of one row for the epilogue.
-struct RowScale {
-    float s, b;
-};
+// One group of one 16-row tile: MMAs into acc, rows r0 (= g) and r8 (= g + 8).
+template <int FMT, int BITS, int GS, int NT>
+QM_DEV void tile_group(const uint8_t* r0, const uint8_t* r8, int gi, int t,
+                       const uint32_t (&bf)[GS / 16][NT][2], float (&acc)[NT][4]) {
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[nt][i] = 0.0f;
+    if constexpr (FMT == QM_AFFINE && BITS == 4) {
+        constexpr int V = GS / 32;  // words of a row per lane per group
+        uint32_t w0[V], w8[V];
+        const int off = gi * (GS / 2) + t * V * 4;
+        if constexpr (V == 1) {
+            w0[0] = *reinterpret_cast<const uint32_t*>(r0 + off);
+            w8[0] = *reinterpret_cast<const uint32_t*>(r8 + off);
+        } else {
+#pragma unroll
+            for (int v = 0; v < V; v += 2) {
+                const uint2 a = *reinterpret_cast<const uint2*>(r0 + off + 4 * v);
+                const uint2 c = *reinterpret_cast<const uint2*>(r8 + off + 4 * v);
+                w0[v] = a.x; w0[v + 1] = a.y; w8[v] = c.x; w8[v + 1] = c.y;
+            }
+        }
+#pragma unroll
+        for (int v = 0; v < V; ++v)
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t a0, a2, a1, a3;
+                dec4(w0[v], h, a0, a2);
+                dec4(w8[v], h, a1, a3);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    mma_f16(acc[nt], a0, a1, a2, a3, bf[2 * v + h][nt][0], bf[2 * v + h][nt][1]);
+            }
+    } else if constexpr (FMT == QM_AFFINE && BITS == 8) {
+        constexpr int V = GS / 16;
+        const int off = gi * GS + t * V * 4;
+#pragma unroll
+        for (int v = 0; v < V; v += 2) {
+            const uint2 a = *reinterpret_cast<const uint2*>(r0 + off + 4 * v);
+            const uint2 c = *reinterpret_cast<const uint2*>(r8 + off + 4 * v);
+            const uint32_t wa[2] = {a.x, a.y}, wc[2] = {c.x, c.y};
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                uint32_t a0, a2, a1, a3;
+                dec8(wa[e], a0, a2);
+                dec8(wc[e], a1, a3);
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+                    mma_f16(acc[nt], a0, a1, a2, a3, bf[v + e][nt][0], bf[v + e][nt][1]);
+            }
+        }
+    } else if constexpr (FMT == QM_Q8_0) {
+        // codes of block gi at byte 34*gi + 2 + 8t (2-byte aligned when gi is even)
+        const int o = 34 * gi + 2 + 8 * t;
+        uint32_t c0[2], c8[2];
+        if (o & 2) {
+            const uint32_t* q0 = reinterpret_cast<const uint32_t*>(r0 + o - 2);
+            const uint32_t* q8 = reinterpret_cast<const uint32_t*>(r8 + o - 2);
+            const uint32_t x0 = q0[0], x1 = q0[1], x2 = q0[2];
+            const uint32_t z0 = q8[0], z1 = q8[1], z2 = q8[2];
+            c0[0] = prmt(x0, x1, 0x5432); c0[1] = prmt(x1, x2, 0x5432);
+            c8[0] = prmt(z0, z1, 0x5432); c8[1] = prmt(z1, z2, 0x5432);
+        } else {
+            const uint32_t* q0 = reinterpret_cast<const uint32_t*>(r0 + o);
+            const uint32_t* q8 = reinterpret_cast<const uint32_t*>(r8 + o);
+            c0[0] = q0[0]; c0[1] = q0[1]; c8[0] = q8[0]; c8[1] = q8[1];
+        }
+#pragma unroll
+        for (int mm = 0; mm < 2; ++mm) {
+            uint32_t a0, a2, a1, a3;
+            dec8(c0[mm] ^ 0x80808080u, a0, a2);
+            dec8(c8[mm] ^ 0x80808080u, a1, a3);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_f16(acc[nt], a0, a1, a2, a3, bf[mm][nt][0], bf[mm][nt][1]);
+        }
+    } else {  // MXFP4
+        const int o = 16 * gi + 4 * t;
+        uint32_t h0[4], h8[4];
+        e2m1x8_to_f16x2(*reinterpret_cast<const uint32_t*>(r0 + o), h0);
+        e2m1x8_to_f16x2(*reinterpret_cast<const uint32_t*>(r8 + o), h8);
+#pragma unroll
+        for (int mm = 0; mm < 2; ++mm)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                mma_f16(acc[nt], h0[2 * mm], h8[2 * mm], h0[2 * mm + 1], h8[2 * mm + 1], bf[mm][nt][0],
+                        bf[mm][nt][1]);
+    }
+}
 
 template <int FMT, int BITS, int GS, int NT>
 __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ Params p) {
@@ -115,43 +196,54 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     const int S = p.S;
     const uint32_t rank = (S > 1) ? cluster_ctarank() : 0;
     const int64_t cluster = blockIdx.x / S;
-    const int64_t tile0 = cluster * p.tiles_per_cluster;
-    const int ntiles = static_cast<int>(std::min<int64_t>(p.tiles_per_cluster, p.n_tiles - tile0));
+    const int64_t stage0 = cluster * p.stages_per_cluster;
+    const int nst = static_cast<int>(std::min<int64_t>(p.stages_per_cluster, p.n_stages - stage0));
     const int64_t kbase = rank * p.krange;
     const int groups = static_cast<int>(p.krange / GS);
 
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bars);
+    // barriers: full[16], empty[16], x, then the abort flag
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
     const uint32_t bar_full0 = smem_u32(bars), bar_empty0 = smem_u32(bars + kMaxStages);
-    int& s_abort = *reinterpret_cast<int*>(smem + p.off_bars + 2 * kMaxStages * 8);
+    const uint32_t bar_x = smem_u32(bars + 2 * kMaxStages);
+    volatile int& s_abort = *reinterpret_cast<volatile int*>(smem + (2 * kMaxStages + 1) * 8);
 
     if (threadIdx.x == 0) {
         s_abort = 0;
         for (uint32_t i = 0; i < p.nstage; ++i) {
-            mbar_init(bar_full0 + 8 * i, 32);  // the producer's lanes
-            mbar_init(bar_empty0 + 8 * i, 1);  // the one consumer warp of the stage
+            mbar_init(bar_full0 + 8 * i, 32);      // the producer's lanes
+            mbar_init(bar_empty0 + 8 * i, p.team);  // the warps of the team that read it
         }
+        mbar_init(bar_x, 1);
         fence_mbar_init();
     }
     __syncthreads();
     grid_launch_dependents();
     grid_dependency_wait();  // x (and, conservatively, W) may come from the previous kernel
 
-    if (warp == kConsumerWarps) {
+    if (warp == kWarps) {
         // ------------------------------------------------------------ producer
+        const uint32_t xbytes = static_cast<uint32_t>(p.krange * 2);
+        if (lane == 0) {
+            mbar_expect_tx(bar_x, xbytes * p.M);
+            mbar_arrive(bar_x);
+        }
+        __syncwarp();
+        if (lane < p.M)
+            bulk_g2s(smem_u32(smem + p.off_xraw + lane * xbytes), p.x + lane * p.k + kbase, xbytes, bar_x);
         int issued = 0;
-        for (int j = 0; j < ntiles; ++j) {
+        for (int j = 0; j < nst; ++j) {
             const uint32_t slot = j % p.nstage;
             const uint32_t par = ((j / p.nstage) & 1) ^ 1;
-            if (!mbar_wait(bar_empty0 + 8 * slot, par) || *(volatile int*)&s_abort) {
+            if (!mbar_wait(bar_empty0 + 8 * slot, par) || s_abort) {
                 if (lane == 0) { atomicOr(&g_err_gemv, DEV_ERR_TIMEOUT); s_abort = 1; }
                 break;
             }
             issued = j + 1;
-            const int64_t row0 = (tile0 + j) * kRows;
+            const int64_t row0 = (stage0 + j) * kRows;
             const int rows = static_cast<int>(std::min<int64_t>(kRows, p.n - row0));
             uint8_t* st = smem + p.off_stages + slot * p.stage_bytes;
             const uint32_t bar = bar_full0 + 8 * slot;
-            // bulk bytes: codes per row; scales/biases per row when split, else one span
+            // bulk bytes: codes per row; scales/biases per row when k is split, else one span
             uint32_t tx = rows * p.code_seg;
             uint32_t span = 0, span_bulk = 0;
             if (p.scale_seg) {
@@ -167,8 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             __syncwarp();
             if (lane < rows) {
                 const int64_t r = row0 + lane;
-                const uint8_t* src = p.codes + r * p.code_row_bytes + rank * p.code_seg;
-                bulk_g2s(smem_u32(st + lane * p.code_pitch), src, p.code_seg, bar);
+                bulk_g2s(smem_u32(st + lane * p.code_pitch), p.codes + r * p.code_row_bytes + rank * p.code_seg,
+                         p.code_seg, bar);
                 if (p.scale_seg && S > 1) {
                     const int64_t off = r * p.scale_row_bytes + rank * p.scale_seg;
                     bulk_g2s(smem_u32(st + p.off_scales + lane * p.scale_seg), p.scales + off, p.scale_seg, bar);
@@ -182,30 +274,36 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                     bulk_g2s(smem_u32(st + p.off_scales), p.scales + off, span_bulk, bar);
                     if (p.biases) bulk_g2s(smem_u32(st + p.off_biases), p.biases + off, span_bulk, bar);
                 }
-                for (uint32_t b = span_bulk + lane; b < span; b += 32) {  // ragged tail of the last tile
+                for (uint32_t b = span_bulk + lane; b < span; b += 32) {  // ragged tail of the last stage
                     st[p.off_scales + b] = p.scales[off + b];
                     if (p.biases) st[p.off_biases + b] = p.biases[off + b];
                 }
             }
             mbar_arrive(bar);
         }
-        if (*(volatile int*)&s_abort) {
+        if (s_abort) {
             // abandoned: let the copies already issued land before the CTA exits
             for (int j = std::max(0, issued - static_cast<int>(p.nstage)); j < issued; ++j)
                 (void)mbar_wait(bar_full0 + 8 * (j % p.nstage), (j / p.nstage) & 1);
+            (void)mbar_wait(bar_x, 0);
         }
     } else {
         // ------------------------------------------------------------ consumers
-        const int ctid = threadIdx.x;  // 0 .. 255
-        float* tokscale = reinterpret_cast<float*>(smem + p.off_tokscale);   // [16] 2^-E
-        float* tokmul = tokscale + 16;                                        // [16] 2^E
-        // 1. per-token power-of-two scale over this CTA's k range
-        for (int m = warp; m < 16; m += kConsumerWarps) {
+        const int ctid = threadIdx.x;  // 0 .. 511
+        float* tokscale = reinterpret_cast<float*>(smem + p.off_tokscale);  // [16] 2^-E
+        float* tokmul = tokscale + 16;                                       // [16] 2^E
+        const uint16_t* xs = reinterpret_cast<const uint16_t*>(smem + p.off_xraw);  // [M][krange]
+        if (!mbar_wait(bar_x, 0)) {
+            if (lane == 0) { atomicOr(&g_err_gemv, DEV_ERR_TIMEOUT); s_abort = 1; }
+        }
+        // 1. per-token power-of-two scale over this CTA's k range (warp m: token m)
+        {
+            const int m = warp;
             float amax = 0.0f;
             if (m < p.M) {
-                const uint16_t* xr = p.x + m * p.k + kbase;
+                const uint16_t* xr = xs + m * p.krange;
                 for (int64_t i = lane * 8; i < p.krange; i += 256) {
-                    const uint4 q = __ldg(reinterpret_cast<const uint4*>(xr + i));
+                    const uint4 q = *reinterpret_cast<const uint4*>(xr + i);
                     const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
@@ -226,26 +324,26 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                 tokscale[m] = __uint_as_float(static_cast<uint32_t>(-E + 127) << 23);
             }
         }
-        asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+        named_bar_sync(1, kWarps * 32);
         // 2. B fragments for every group of the k range, and per-token group sums
         uint32_t* xfrag = reinterpret_cast<uint32_t*>(smem + p.off_xfrag);
         float2* tok = reinterpret_cast<float2*>(smem + p.off_tok);  // [groups][16]
         {
             const int items = groups * 32 * NT;
-            for (int it = ctid; it < items; it += kConsumerWarps * 32) {
+            for (int it = ctid; it < items; it += kWarps * 32) {
                 const int nt = it % NT, ln = (it / NT) % 32, gi = it / (NT * 32);
                 const int tg = ln >> 2, t = ln & 3;
                 const int m = nt * 8 + tg;
                 const bool live = m < p.M;  // padding tokens get exact zeros
                 const float mul = live ? tokmul[m] : 0.0f;
-                const uint16_t* xr = p.x + static_cast<int64_t>(live ? m : 0) * p.k + kbase;
-                uint32_t* dst = xfrag + ((static_cast<int64_t>(gi) * 32 + ln) * MM) * NT * 2 + nt * 2;
-                auto xv = [&](int64_t kk) { return live ? bf16_bits_to_f32(xr[kk]) * mul : 0.0f; };
+                const uint16_t* xr = xs + (live ? m : 0) * p.krange;
+                uint32_t* dst = xfrag + ((gi * 32 + ln) * MM) * NT * 2 + nt * 2;
+                auto xv = [&](int kk) { return live ? bf16_bits_to_f32(xr[kk]) * mul : 0.0f; };
                 if constexpr (FMT == QM_AFFINE && BITS == 4) {
                     constexpr int V = GS / 32;
 #pragma unroll
                     for (int v = 0; v < V; ++v) {
-                        const int64_t k0 = 8 * (static_cast<int64_t>(gi) * (GS / 8) + t * V + v);
+                        const int k0 = 8 * (gi * (GS / 8) + t * V + v);
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
                             const int mm = 2 * v + h;
@@ -258,70 +356,81 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                     constexpr int V = GS / 16;
 #pragma unroll
                     for (int v = 0; v < V; ++v) {
-                        const int64_t k0 = 4 * (static_cast<int64_t>(gi) * (GS / 4) + t * V + v);
+                        const int k0 = 4 * (gi * (GS / 4) + t * V + v);
                         dst[v * NT * 2 + 0] = pack_f16x2(xv(k0), xv(k0 + 1));
                         dst[v * NT * 2 + 1] = pack_f16x2(xv(k0 + 2), xv(k0 + 3));
                     }
-                } else {  // Q8_0, MXFP4: thread t holds values 8t .. 8t+7 of the block
+                } else {  // Q8_0, MXFP4: lane t holds values 8t .. 8t+7 of the block
 #pragma unroll
                     for (int mm = 0; mm < 2; ++mm) {
-                        const int64_t k0 = 32 * static_cast<int64_t>(gi) + 8 * t + 4 * mm;
+                        const int k0 = 32 * gi + 8 * t + 4 * mm;
                         dst[mm * NT * 2 + 0] = pack_f16x2(xv(k0), xv(k0 + 1));
                         dst[mm * NT * 2 + 1] = pack_f16x2(xv(k0 + 2), xv(k0 + 3));
                     }
                 }
             }
-            // per (group, token): (offset, sum of x') -- offset = magic * sum of B values
-            for (int it = ctid; it < groups * 16; it += kConsumerWarps * 32) {
-                const int m = it % 16, gi = it / 16;
-                float F = 0.0f, X = 0.0f;
-                if (m < p.M) {
+            // per (group, token): (offset, sum of x'), one warp per pair; the
+            // offset is the magic times the sum of the B values the MMAs saw
+            if constexpr (FMT != QM_MXFP4) {
+                const float magic = (FMT == QM_Q8_0) ? 1152.0f : 1024.0f;
+                for (int it = warp; it < groups * p.M; it += kWarps) {
+                    const int m = it % p.M, gi = it / p.M;
                     const float mul = tokmul[m];
-                    const uint16_t* xr = p.x + m * p.k + kbase + static_cast<int64_t>(gi) * GS;
-                    for (int e = 0; e < GS; ++e) {
+                    const uint16_t* xr = xs + m * p.krange + gi * GS;
+                    float F = 0.0f, X = 0.0f;
+#pragma unroll
+                    for (int e = lane; e < GS; e += 32) {
                         const float xe = bf16_bits_to_f32(xr[e]) * mul;
                         X += xe;
                         F += (FMT == QM_AFFINE && BITS == 4 && (e & 1)) ? xe * 0.0625f : xe;
                     }
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        X += __shfl_xor_sync(0xffffffffu, X, o);
+                        F += __shfl_xor_sync(0xffffffffu, F, o);
+                    }
+                    if (lane == 0) tok[gi * 16 + m] = make_float2(magic * F, X);
                 }
-                const float magic = (FMT == QM_Q8_0) ? 1152.0f : 1024.0f;
-                tok[it] = make_float2(FMT == QM_MXFP4 ? 0.0f : magic * F, X);
+                for (int it = ctid; it < groups * (16 - p.M); it += kWarps * 32) {
+                    const int gi = it / (16 - p.M), m = p.M + it % (16 - p.M);
+                    tok[gi * 16 + m] = make_float2(0.0f, 0.0f);
+                }
             }
         }
-        asm volatile("bar.sync 1, %0;" ::"r"(kConsumerWarps * 32) : "memory");
+        named_bar_sync(1, kWarps * 32);
 
-        // 3. main loop: warp w takes stages w, w + 8, ...
+        // 3. main loop: team `team` takes stages team, team + nteams, ...;
+        //    warp wi of the team covers groups [gb, ge) of each.
+        const int T = p.team, nteams = kWarps / T;
+        const int team = warp / T, wi = warp % T;
+        const int gb = wi * groups / T, ge = (wi + 1) * groups / T;
         const int g = lane >> 2, t = lane & 3;
-        float* partial = reinterpret_cast<float*>(smem + p.off_partial);  // [tiles][16 rows][16 tok]
-        bool ok = true;
-        for (int j = warp; j < ntiles && ok; j += kConsumerWarps) {
+        float* partial = reinterpret_cast<float*>(smem + p.off_xraw);  // [stages][32 rows][16 tok]
+        float* red = reinterpret_cast<float*>(smem + p.off_red);       // [teams][2][T][2][NT][4][32]
+        int buf = 0;
+        // Every warp of a team runs the same iterations and meets the team
+        // barrier once per stage, abandoned or not, so no barrier is left waiting.
+        for (int j = team; j < nst; j += nteams) {
             const uint32_t slot = j % p.nstage;
-            const uint32_t par = (j / p.nstage) & 1;
-            if (!mbar_wait(bar_full0 + 8 * slot, par) || *(volatile int*)&s_abort) {
+            bool live = !s_abort;
+            if (live && !mbar_wait(bar_full0 + 8 * slot, (j / p.nstage) & 1)) {
                 if (lane == 0) { atomicOr(&g_err_gemv, DEV_ERR_TIMEOUT); s_abort = 1; }
-                ok = false;
-                break;
+                live = false;
             }
+            live = __shfl_sync(0xffffffffu, live ? 1 : 0, 0) != 0;
             const uint8_t* st = smem + p.off_stages + slot * p.stage_bytes;
-            const uint8_t* r0 = st + g * p.code_pitch;        // row g
-            const uint8_t* r8 = st + (g + 8) * p.code_pitch;  // row g + 8
-            Acc<NT> y;
+            float y[2][NT][4];
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                for (int i = 0; i < 4; ++i) y.v[nt][i] = 0.0f;
-
-            for (int gi = 0; gi < groups; ++gi) {
-                Acc<NT> acc;
+            for (int tt = 0; tt < 2; ++tt)
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) acc.v[nt][i] = 0.0f;
-                // B fragments of this group for this lane
+                    for (int i = 0; i < 4; ++i) y[tt][nt][i] = 0.0f;
+
+            for (int gi = gb; gi < (live ? ge : gb); ++gi) {
                 uint32_t bf[MM][NT][2];
                 {
-                    const uint4* src = reinterpret_cast<const uint4*>(
-                        xfrag + ((static_cast<int64_t>(gi) * 32 + lane) * MM) * NT * 2);
+                    const uint4* src = reinterpret_cast<const uint4*>(xfrag + ((gi * 32 + lane) * MM) * NT * 2);
                     uint32_t* b = &bf[0][0][0];
 #pragma unroll
                     for (int q = 0; q < MM * NT / 2; ++q) {
@@ -329,148 +438,110 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                         b[4 * q] = v.x; b[4 * q + 1] = v.y; b[4 * q + 2] = v.z; b[4 * q + 3] = v.w;
                     }
                 }
-                if constexpr (FMT == QM_AFFINE && BITS == 4) {
-                    constexpr int V = GS / 32;
-                    uint32_t w0[V], w8[V];
-                    const int off = gi * (GS / 2) + t * V * 4;
-                    if constexpr (V == 1) {
-                        w0[0] = *reinterpret_cast<const uint32_t*>(r0 + off);
-                        w8[0] = *reinterpret_cast<const uint32_t*>(r8 + off);
-                    } else {
+                float4 td[NT];  // (O[2t], X[2t], O[2t+1], X[2t+1]) per token half
+                if constexpr (FMT != QM_MXFP4) {
 #pragma unroll
-                        for (int v = 0; v < V; v += 2) {
-                            const uint2 a = *reinterpret_cast<const uint2*>(r0 + off + 4 * v);
-                            const uint2 c = *reinterpret_cast<const uint2*>(r8 + off + 4 * v);
-                            w0[v] = a.x; w0[v + 1] = a.y; w8[v] = c.x; w8[v + 1] = c.y;
-                        }
-                    }
-#pragma unroll
-                    for (int v = 0; v < V; ++v)
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            uint32_t a0, a2, a1, a3;
-                            dec4(w0[v], h, a0, a2);
-                            dec4(w8[v], h, a1, a3);
-#pragma unroll
-                            for (int nt = 0; nt < NT; ++nt)
-                                mma_f16(acc.v[nt], a0, a1, a2, a3, bf[2 * v + h][nt][0], bf[2 * v + h][nt][1]);
-                        }
-                } else if constexpr (FMT == QM_AFFINE && BITS == 8) {
-                    constexpr int V = GS / 16;
-                    const int off = gi * GS + t * V * 4;
-#pragma unroll
-                    for (int v = 0; v < V; v += 2) {
-                        const uint2 a = *reinterpret_cast<const uint2*>(r0 + off + 4 * v);
-                        const uint2 c = *reinterpret_cast<const uint2*>(r8 + off + 4 * v);
-                        const uint32_t wa[2] = {a.x, a.y}, wc[2] = {c.x, c.y};
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            uint32_t a0, a2, a1, a3;
-                            dec8(wa[e], a0, a2);
-                            dec8(wc[e], a1, a3);
-#pragma unroll
-                            for (int nt = 0; nt < NT; ++nt)
-                                mma_f16(acc.v[nt], a0, a1, a2, a3, bf[v + e][nt][0], bf[v + e][nt][1]);
-                        }
-                    }
-                } else if constexpr (FMT == QM_Q8_0) {
-                    // codes of block gi at byte 34*gi + 2 + 8t (2-byte aligned when gi is even)
-                    const int o = 34 * gi + 2 + 8 * t;
-                    uint32_t c0[2], c8[2];
-                    if (o & 2) {
-                        const uint32_t* q0 = reinterpret_cast<const uint32_t*>(r0 + o - 2);
-                        const uint32_t* q8 = reinterpret_cast<const uint32_t*>(r8 + o - 2);
-                        const uint32_t x0 = q0[0], x1 = q0[1], x2 = q0[2];
-                        const uint32_t z0 = q8[0], z1 = q8[1], z2 = q8[2];
-                        c0[0] = prmt(x0, x1, 0x5432); c0[1] = prmt(x1, x2, 0x5432);
-                        c8[0] = prmt(z0, z1, 0x5432); c8[1] = prmt(z1, z2, 0x5432);
-                    } else {
-                        const uint32_t* q0 = reinterpret_cast<const uint32_t*>(r0 + o);
-                        const uint32_t* q8 = reinterpret_cast<const uint32_t*>(r8 + o);
-                        c0[0] = q0[0]; c0[1] = q0[1]; c8[0] = q8[0]; c8[1] = q8[1];
-                    }
-#pragma unroll
-                    for (int mm = 0; mm < 2; ++mm) {
-                        uint32_t a0, a2, a1, a3;
-                        dec8(c0[mm] ^ 0x80808080u, a0, a2);
-                        dec8(c8[mm] ^ 0x80808080u, a1, a3);
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-                            mma_f16(acc.v[nt], a0, a1, a2, a3, bf[mm][nt][0], bf[mm][nt][1]);
-                    }
-                } else {  // MXFP4
-                    const int o = 16 * gi + 4 * t;
-                    uint32_t h0[4], h8[4];
-                    e2m1x8_to_f16x2(*reinterpret_cast<const uint32_t*>(r0 + o), h0);
-                    e2m1x8_to_f16x2(*reinterpret_cast<const uint32_t*>(r8 + o), h8);
-#pragma unroll
-                    for (int mm = 0; mm < 2; ++mm)
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-                            mma_f16(acc.v[nt], h0[2 * mm], h8[2 * mm], h0[2 * mm + 1], h8[2 * mm + 1],
-                                    bf[mm][nt][0], bf[mm][nt][1]);
+                    for (int nt = 0; nt < NT; ++nt)
+                        td[nt] = *reinterpret_cast<const float4*>(tok + gi * 16 + nt * 8 + 2 * t);
                 }
-                // ---- group epilogue: scale (and bias) per row, offsets per token
-                float s0, s8, b0 = 0.0f, b8 = 0.0f;
-                if constexpr (FMT == QM_AFFINE) {
-                    const uint16_t* sc = reinterpret_cast<const uint16_t*>(st + p.off_scales);
-                    const uint16_t* bi = reinterpret_cast<const uint16_t*>(st + p.off_biases);
-                    const int stride = p.scale_seg / 2;
-                    const uint32_t hs0 = sc[g * stride + gi], hs8 = sc[(g + 8) * stride + gi];
-                    const uint32_t hb0 = bi[g * stride + gi], hb8 = bi[(g + 8) * stride + gi];
-                    if (p.sdt == QM_F16) {
-                        s0 = f16_bits_to_f32(hs0); s8 = f16_bits_to_f32(hs8);
-                        b0 = f16_bits_to_f32(hb0); b8 = f16_bits_to_f32(hb8);
-                    } else {
-                        s0 = bf16_bits_to_f32(hs0); s8 = bf16_bits_to_f32(hs8);
-                        b0 = bf16_bits_to_f32(hb0); b8 = bf16_bits_to_f32(hb8);
-                    }
-                } else if constexpr (FMT == QM_Q8_0) {
-                    s0 = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(r0 + 34 * gi));
-                    s8 = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(r8 + 34 * gi));
-                } else {
-                    const uint8_t* sc = st + p.off_scales;
-                    s0 = e8m0_to_f32(sc[g * p.scale_seg + gi]);
-                    s8 = e8m0_to_f32(sc[(g + 8) * p.scale_seg + gi]);
-                }
+                float acc[2][NT][4];
 #pragma unroll
-                for (int nt = 0; nt < NT; ++nt) {
-                    const float4 td = *reinterpret_cast<const float4*>(tok + gi * 16 + nt * 8 + 2 * t);
-                    // td = (O[2t], X[2t], O[2t+1], X[2t+1])
-                    if constexpr (FMT == QM_MXFP4) {
-                        y.v[nt][0] = fmaf(s0, acc.v[nt][0], y.v[nt][0]);
-                        y.v[nt][1] = fmaf(s0, acc.v[nt][1], y.v[nt][1]);
-                        y.v[nt][2] = fmaf(s8, acc.v[nt][2], y.v[nt][2]);
-                        y.v[nt][3] = fmaf(s8, acc.v[nt][3], y.v[nt][3]);
+                for (int tt = 0; tt < 2; ++tt)
+                    tile_group<FMT, BITS, GS, NT>(st + (16 * tt + g) * p.code_pitch,
+                                                  st + (16 * tt + g + 8) * p.code_pitch, gi, t, bf, acc[tt]);
+#pragma unroll
+                for (int tt = 0; tt < 2; ++tt) {
+                    const int ra = 16 * tt + g, rb = ra + 8;
+                    float s0, s8, b0 = 0.0f, b8 = 0.0f;
+                    if constexpr (FMT == QM_AFFINE) {
+                        const uint16_t* sc = reinterpret_cast<const uint16_t*>(st + p.off_scales);
+                        const uint16_t* bi = reinterpret_cast<const uint16_t*>(st + p.off_biases);
+                        const int stride = p.scale_seg / 2;
+                        s0 = sval(sc[ra * stride + gi], p.sdt);
+                        s8 = sval(sc[rb * stride + gi], p.sdt);
+                        b0 = sval(bi[ra * stride + gi], p.sdt);
+                        b8 = sval(bi[rb * stride + gi], p.sdt);
+                    } else if constexpr (FMT == QM_Q8_0) {
+                        s0 = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(st + ra * p.code_pitch + 34 * gi));
+                        s8 = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(st + rb * p.code_pitch + 34 * gi));
                     } else {
-                        y.v[nt][0] = fmaf(s0, acc.v[nt][0] - td.x, fmaf(b0, td.y, y.v[nt][0]));
-                        y.v[nt][1] = fmaf(s0, acc.v[nt][1] - td.z, fmaf(b0, td.w, y.v[nt][1]));
-                        y.v[nt][2] = fmaf(s8, acc.v[nt][2] - td.x, fmaf(b8, td.y, y.v[nt][2]));
-                        y.v[nt][3] = fmaf(s8, acc.v[nt][3] - td.z, fmaf(b8, td.w, y.v[nt][3]));
+                        const uint8_t* sc = st + p.off_scales;
+                        s0 = e8m0_to_f32(sc[ra * p.scale_seg + gi]);
+                        s8 = e8m0_to_f32(sc[rb * p.scale_seg + gi]);
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        float* yv = y[tt][nt];
+                        const float* a = acc[tt][nt];
+                        if constexpr (FMT == QM_MXFP4) {
+                            yv[0] = fmaf(s0, a[0], yv[0]);
+                            yv[1] = fmaf(s0, a[1], yv[1]);
+                            yv[2] = fmaf(s8, a[2], yv[2]);
+                            yv[3] = fmaf(s8, a[3], yv[3]);
+                        } else {
+                            const float4 d = td[nt];
+                            yv[0] = fmaf(s0, a[0] - d.x, fmaf(b0, d.y, yv[0]));
+                            yv[1] = fmaf(s0, a[1] - d.z, fmaf(b0, d.w, yv[1]));
+                            yv[2] = fmaf(s8, a[2] - d.x, fmaf(b8, d.y, yv[2]));
+                            yv[3] = fmaf(s8, a[3] - d.z, fmaf(b8, d.w, yv[3]));
+                        }
                     }
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(bar_empty0 + 8 * slot);
+            if (lane == 0 && live) mbar_arrive(bar_empty0 + 8 * slot);
 
-            // ---- tile result: undo the token scale; store or keep the partial
-            const int64_t row0 = (tile0 + j) * kRows;
+            // ---- the team's sum, in warp order; then undo the token scale
+            bool writer = true;
+            if (T > 1) {
+                float* mine = red + ((((team * 2 + buf) * T + wi) * 2) * NT * 4) * 32;
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+                for (int tt = 0; tt < 2; ++tt)
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const int m = nt * 8 + 2 * t + (i & 1);
-                    const int r = g + ((i & 2) ? 8 : 0);
-                    const float v = y.v[nt][i] * tokscale[m];
-                    if (S == 1) {
-                        if (m < p.M && row0 + r < p.n) {
-                            __nv_bfloat16 b = __float2bfloat16_rn(v);
-                            p.y[static_cast<int64_t>(m) * p.n + row0 + r] = *reinterpret_cast<uint16_t*>(&b);
+                    for (int nt = 0; nt < NT; ++nt)
+                        *reinterpret_cast<float4*>(mine + ((tt * NT + nt) * 32 + lane) * 4) =
+                            make_float4(y[tt][nt][0], y[tt][nt][1], y[tt][nt][2], y[tt][nt][3]);
+                named_bar_sync(2 + team, T * 32);
+                writer = (wi == 0);
+                if (writer) {
+                    const float* base = red + (((team * 2 + buf) * T) * 2) * NT * 4 * 32;
+#pragma unroll
+                    for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt) {
+                            float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                            for (int q = 0; q < T; ++q) {
+                                const float4 v = *reinterpret_cast<const float4*>(
+                                    base + (((q * 2 + tt) * NT + nt) * 32 + lane) * 4);
+                                s4[0] += v.x; s4[1] += v.y; s4[2] += v.z; s4[3] += v.w;
+                            }
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) y[tt][nt][i] = s4[i];
                         }
-                    } else {
-                        partial[(j * kRows + r) * 16 + m] = v;
-                    }
                 }
+                buf ^= 1;
+            }
+            if (writer && live && !s_abort) {
+                const int64_t row0 = (stage0 + j) * kRows;
+#pragma unroll
+                for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const int m = nt * 8 + 2 * t + (i & 1);
+                            const int r = 16 * tt + g + ((i & 2) ? 8 : 0);
+                            const float v = y[tt][nt][i] * tokscale[m];
+                            if (S == 1) {
+                                if (m < p.M && row0 + r < p.n) {
+                                    __nv_bfloat16 b = __float2bfloat16_rn(v);
+                                    p.y[static_cast<int64_t>(m) * p.n + row0 + r] = *reinterpret_cast<uint16_t*>(&b);
+                                }
+                            } else {
+                                partial[(j * kRows + r) * 16 + m] = v;
+                            }
+                        }
+            }
         }
     }
 
@@ -478,11 +549,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     if (S > 1) {
         __syncthreads();
         cluster_sync();
-        const uint32_t base = smem_u32(smem + p.off_partial);
-        const int entries = ntiles * kRows * 16;
+        const uint32_t base = smem_u32(smem + p.off_xraw);
+        const int entries = nst * kRows * 16;
         for (int e = rank * blockDim.x + threadIdx.x; e < entries; e += S * blockDim.x) {
             const int m = e % 16, rr = e / 16;
-            const int64_t row = tile0 * kRows + rr;
+            const int64_t row = stage0 * kRows + rr;
             if (m >= p.M || row >= p.n) continue;
             float sum = 0.0f;
             for (int q = 0; q < S; ++q) sum += ld_shared_cluster_f32(map_shared_rank(base + 4u * e, q));
@@ -510,6 +581,8 @@ static int64_t code_bytes(const WDesc& w, int64_t kk) {
     return kk * w.bits / 8;
 }
 
+// 32-bit words one lane reads from a row per load (sets the pitch padding
+// that keeps the 8 rows of a load on distinct banks).
 static int lds_words(const WDesc& w) {
     if (w.fmt == QM_AFFINE && w.bits == 4 && w.gs == 32) return 1;
     if (w.fmt == QM_MXFP4 || w.fmt == QM_Q8_0) return 1;
@@ -561,6 +634,7 @@ static bool plan_for(const WDesc& w, int64_t M, int S, Plan* out) {
     if (w.fmt == QM_MXFP4) sseg = kr / 32;
     if (S > 1 && sseg % 16) return false;
     Params& p = out->p;
+    p = Params{};
     p.code_seg = static_cast<uint32_t>(cseg);
     p.code_pitch = round_up(cseg, 128) + 16 * lds_words(w);
     p.scale_seg = static_cast<uint32_t>(sseg);
@@ -570,31 +644,39 @@ static bool plan_for(const WDesc& w, int64_t M, int S, Plan* out) {
     p.off_biases = codes_bytes + sc_bytes;
     p.stage_bytes = round_up(codes_bytes + sc_bytes * (w.fmt == QM_AFFINE ? 2 : 1), 128);
     const int64_t groups = kr / w.gs;
-    p.off_bars = 0;                                      // full/empty mbarriers, abort flag
-    p.off_tokscale = 512;                                // [16] 2^-E, [16] 2^E
-    p.off_tok = p.off_tokscale + 128;                    // [groups][16] float2
+    // work split: as many clusters as fit one CTA per SM
+    p.n_stages = (w.n + kRows - 1) / kRows;
+    int64_t G = std::max<int64_t>(1, num_sms() / S);
+    if (S > 1) G = std::max<int64_t>(1, std::min<int64_t>(G, max_clusters(S, max_smem_optin() - 1024)));
+    G = std::min<int64_t>(G, p.n_stages);
+    const int64_t spc = (p.n_stages + G - 1) / G;
+    G = (p.n_stages + spc - 1) / spc;
+    // teams: enough teams for the stages a CTA has, each warp at least one group
+    int teams = 1;
+    while (teams * 2 <= kWarps && teams * 2 <= spc) teams *= 2;
+    int T = kWarps / teams;
+    while (T > 1 && T > groups) T /= 2;
+    p.team = T;
+    // shared memory
+    p.off_tokscale = 512;
+    p.off_tok = p.off_tokscale + 128;
     p.off_xfrag = round_up(p.off_tok + groups * 16 * 8, 128);
     const uint64_t xfrag_bytes = static_cast<uint64_t>(kr) * 16 * NT;
-    p.off_partial = round_up(p.off_xfrag + xfrag_bytes, 128);
-    p.n_tiles = (w.n + kRows - 1) / kRows;
-    // clusters: as many as fit one CTA per SM
-    const int sms = num_sms();
-    int64_t G = std::max<int64_t>(1, sms / S);
-    if (S > 1) G = std::max<int64_t>(1, std::min<int64_t>(G, max_clusters(S, max_smem_optin() - 1024)));
-    G = std::min<int64_t>(G, p.n_tiles);
-    int64_t tpc = (p.n_tiles + G - 1) / G;
-    G = (p.n_tiles + tpc - 1) / tpc;
-    const uint64_t partial_bytes = S > 1 ? static_cast<uint64_t>(tpc) * kRows * 16 * 4 : 0;
-    p.off_stages = round_up(p.off_partial + partial_bytes, 1024);
+    p.off_red = round_up(p.off_xfrag + xfrag_bytes, 128);
+    const uint64_t red_bytes = T > 1 ? static_cast<uint64_t>(kWarps / T) * 2 * T * 2 * NT * 4 * 32 * 4 : 0;
+    p.off_xraw = round_up(p.off_red + red_bytes, 128);
+    const uint64_t partial_bytes = S > 1 ? static_cast<uint64_t>(spc) * kRows * 16 * 4 : 0;
+    const uint64_t xraw_bytes = static_cast<uint64_t>(M) * kr * 2;
+    p.off_stages = round_up(p.off_xraw + std::max(partial_bytes, xraw_bytes), 1024);
     const int64_t budget = max_smem_optin() - 1024;
     const int64_t room = budget - p.off_stages;
     if (room < 2 * static_cast<int64_t>(p.stage_bytes)) return false;
     int64_t nst = std::min<int64_t>(kMaxStages, room / p.stage_bytes);
-    nst = std::min<int64_t>(nst, std::max<int64_t>(2, tpc));
+    nst = std::min<int64_t>(nst, std::max<int64_t>(2, spc));
     p.nstage = static_cast<uint32_t>(nst);
     p.S = S;
     p.krange = kr;
-    p.tiles_per_cluster = static_cast<int>(tpc);
+    p.stages_per_cluster = static_cast<int>(spc);
     out->S = S;
     out->grid = G * S;
     out->smem = p.off_stages + nst * p.stage_bytes;
@@ -602,22 +684,17 @@ static bool plan_for(const WDesc& w, int64_t M, int S, Plan* out) {
     return true;
 }
 
-// Pick the k split: least per-CTA work (tiles x k range), then fewest splits.
+// Pick the k split: least per-CTA work (stages x k range), then fewest
+// splits; a split that keeps three stages in flight beats one that cannot.
 static Plan make_plan(const WDesc& w, int64_t M) {
     Plan best;
     double best_cost = 1e300;
     for (int S = 1; S <= 8; ++S) {
         Plan pl;
         if (!plan_for(w, M, S, &pl)) continue;
-        if (pl.p.nstage < 3 && S < 8) {
-            // prefer a split that keeps three stages in flight
-            Plan more;
-            bool better = false;
-            for (int S2 = S + 1; S2 <= 8 && !better; ++S2)
-                if (plan_for(w, M, S2, &more) && more.p.nstage >= 3) better = true;
-            if (better) continue;
-        }
-        const double cost = static_cast<double>(pl.p.tiles_per_cluster) * pl.p.krange * (1.0 + 0.03 * (S - 1));
+        const bool shallow = pl.p.nstage < 3 && pl.p.stages_per_cluster >= 3;
+        const double cost = static_cast<double>(pl.p.stages_per_cluster) * pl.p.krange *
+                            (1.0 + 0.03 * (S - 1)) * (shallow ? 2.0 : 1.0);
         if (cost < best_cost * 0.999) {
             best_cost = cost;
             best = pl;
