@@ -201,14 +201,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     const int64_t kbase = rank * p.krange;
     const int groups = static_cast<int>(p.krange / GS);
 
-    // barriers: full[16], empty[16], x, then the abort flag
+    // barriers: full[16], empty[16], x, the abort flag, then slot_stage[16]:
+    // the stage a slot was last filled with. Teams take stages round-robin,
+    // so a consumer may reach a slot more than one fill ahead of the
+    // producer; it waits for the slot's tag before trusting the parity.
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
     const uint32_t bar_full0 = smem_u32(bars), bar_empty0 = smem_u32(bars + kMaxStages);
     const uint32_t bar_x = smem_u32(bars + 2 * kMaxStages);
     volatile int& s_abort = *reinterpret_cast<volatile int*>(smem + (2 * kMaxStages + 1) * 8);
+    volatile int* slot_stage = reinterpret_cast<volatile int*>(smem + (2 * kMaxStages + 2) * 8);
 
     if (threadIdx.x == 0) {
         s_abort = 0;
+        for (int i = 0; i < kMaxStages; ++i) slot_stage[i] = -1;
         for (uint32_t i = 0; i < p.nstage; ++i) {
             mbar_init(bar_full0 + 8 * i, 32);      // the producer's lanes
             mbar_init(bar_empty0 + 8 * i, p.team);  // the warps of the team that read it
@@ -255,7 +260,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                     tx += span_bulk * (p.biases ? 2 : 1);
                 }
             }
-            if (lane == 0) mbar_expect_tx(bar, tx);
+            if (lane == 0) {
+                slot_stage[slot] = j;
+                mbar_expect_tx(bar, tx);
+            }
             __syncwarp();
             if (lane < rows) {
                 const int64_t r = row0 + lane;
@@ -413,6 +421,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         for (int j = team; j < nst; j += nteams) {
             const uint32_t slot = j % p.nstage;
             bool live = !s_abort;
+            if (live && lane == 0) {  // the producer has started filling the slot with stage j
+                const uint64_t t0 = globaltimer();
+                while (slot_stage[slot] != j && !s_abort)
+                    if (globaltimer() - t0 > kWaitLimitNs) {
+                        atomicOr(&g_err_gemv, DEV_ERR_TIMEOUT);
+                        s_abort = 1;
+                        break;
+                    }
+                live = !s_abort;
+            }
+            live = __shfl_sync(0xffffffffu, live ? 1 : 0, 0) != 0;
             if (live && !mbar_wait(bar_full0 + 8 * slot, (j / p.nstage) & 1)) {
                 if (lane == 0) { atomicOr(&g_err_gemv, DEV_ERR_TIMEOUT); s_abort = 1; }
                 live = false;

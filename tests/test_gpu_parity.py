@@ -260,3 +260,31 @@ def test_apply_experts_small(kind, broadcast):
     assert np.all(err <= bound + bf16_half_ulp(got[rows])), err.max()
     nanrows = ~out & ~np.all(np.isfinite(ref), axis=1)
     assert np.all(np.isnan(got[nanrows]))
+
+
+# ---------------------------------------------------------------- long pipelines
+@pytest.mark.parametrize("kind,n,k", [("affine4_g64", 40000, 1024), ("affine8_g32", 20000, 512),
+                                      ("q8_0", 12000, 1024), ("mxfp4", 30000, 256)])
+@pytest.mark.parametrize("M", [1, 3])
+def test_apply_many_stages_per_cta(kind, n, k, M):
+    # many more stages per CTA than shared-memory slots: slots are refilled
+    # several times while different teams work on them
+    g = synth.rng(1000 + M)
+    w = _make(kind, g, n, k)
+    x = synth.activations(g, M, k)
+    _check_apply(w, x, f"{kind} n={n} k={k} M={M}")
+
+
+def test_apply_lm_head_shape_sampled():
+    # the full lm_head shape (151936 x 1024, affine 4-bit gs64) at M = 1,
+    # checked on sampled outputs the oracle computes one by one
+    g = synth.rng(1100)
+    w = synth.affine_weight(g, 151936, 1024, bits=4, group_size=64)
+    x = synth.activations(g, 1, 1024)
+    ow = to_oracle(w)
+    y = bf16_to_f64(_host(qm.apply(qm.QWeight.from_arrays(w), _dev_bf16(x))))[0]
+    j = np.unique(np.concatenate([g.integers(0, 151936, 3000), [0, 1, 151935, 151904]]))
+    ref = oracle.apply_entries(ow, x, np.zeros_like(j), j)
+    wn = np.array([np.linalg.norm(oracle.row_values(ow, int(r)).astype(np.float64)) for r in j])
+    xn = np.linalg.norm(oracle.decode_array(x, oracle.BF16), axis=1)
+    check_product(y[j][None], ref[None], wn, xn, 1024, "lm_head sampled")
