@@ -3,6 +3,7 @@
 // Every check here names the part it refuses, the way the constructors and
 // products of "Nx_quant (raven-ml.dev API docs)" (sections "Weights" and
 // "Products") raise Invalid_argument naming the part.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -145,6 +146,42 @@ qm_status validate_weight(const qm_weight* w, WDesc* d) {
         }
     }
     return QM_OK;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled() {
+    static std::atomic<EncodeTiledFn> fn{nullptr};
+    EncodeTiledFn f = fn.load(std::memory_order_acquire);
+    if (!f) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !ptr)
+            return nullptr;
+        f = reinterpret_cast<EncodeTiledFn>(ptr);
+        fn.store(f, std::memory_order_release);
+    }
+    return f;
+}
+
+bool make_tmap_2d(void* map, const void* base, uint64_t inner_bytes, uint64_t rows, uint64_t row_stride,
+                  uint32_t box_inner, uint32_t box_rows, bool swizzle128) {
+    EncodeTiledFn f = encode_tiled();
+    if (!f) return false;
+    const cuuint64_t dims[2] = {inner_bytes, rows};
+    const cuuint64_t strides[1] = {row_stride};
+    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = f(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                   strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                   swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
 }
 
 static qm_status check_launch(cudaError_t e, const char* what) {

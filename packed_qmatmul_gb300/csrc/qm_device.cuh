@@ -87,6 +87,19 @@ QM_DEV void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar
         : "memory");
 }
 
+// 2-d tiled TMA load of the box at (x bytes, y rows) of a tensor map (a
+// __grid_constant__ parameter) into shared memory, completing on an mbarrier.
+QM_DEV void tma_load_2d(uint32_t dst, const void* tmap, int32_t x, int32_t y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(dst), "l"(tmap), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+QM_DEV void prefetch_tmap(const void* tmap) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
 QM_DEV void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }

@@ -30,6 +30,7 @@
 // MLX affine codes: "GPTQModel wiki: MLX Apple Silicon", "Packed layouts and
 // exact transcoding" (little-endian code stream) and "Concepts ..."
 // (value = code*scale + bias). Q8_0 and MXFP4 layouts: "Nx_quant", "Weights".
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -58,6 +59,9 @@ constexpr int kMaxStages = 16;
 constexpr uint32_t kMagic = 0x64006400u;  // f16x2 (1024, 1024)
 
 struct Params {
+    CUtensorMap tm_codes;    // codes as a byte array [n, code_row_bytes], 128 B x 32-row boxes, swizzled
+    CUtensorMap tm_scales;   // scales [n, scale_row_bytes], scale_seg x 32-row boxes (k split only)
+    CUtensorMap tm_biases;
     const uint8_t* codes;
     const uint8_t* scales;
     const uint8_t* biases;
@@ -75,7 +79,7 @@ struct Params {
     int team;                // warps per team (1, 2, 4, 8 or 16)
     // shared memory layout (byte offsets from the dynamic smem base)
     uint32_t nstage, stage_bytes;
-    uint32_t code_seg, code_pitch;    // per row: bytes copied, smem pitch
+    uint32_t code_seg, nbox;          // per row: bytes of codes; 128-byte boxes per stage
     uint32_t scale_seg;               // per row bytes of scales (and of biases) in a stage
     uint32_t off_scales, off_biases;  // within a stage
     uint32_t off_tokscale, off_tok, off_xfrag, off_red, off_xraw, off_stages;
@@ -98,9 +102,25 @@ QM_DEV void dec8(uint32_t w, uint32_t& lo, uint32_t& hi) {
 
 QM_DEV float sval(uint32_t h, int sdt) { return sdt == QM_F16 ? f16_bits_to_f32(h) : bf16_bits_to_f32(h); }
 
+// A stage's codes are 128-byte boxes of 32 rows, each box 128B-swizzled by
+// the TMA unit: byte b of row r sits in box b / 128, at row r's 128-byte
+// line, 16-byte chunk ((b / 16) mod 8) XOR (r mod 8). Reads never straddle a
+// 16-byte chunk, so one address per read suffices.
+struct CodeRow {
+    const uint8_t* line;  // stage + r * 128
+    uint32_t key;         // (r mod 8) << 4
+    QM_DEV const uint8_t* at(uint32_t b) const {
+        return line + (b >> 7) * (kRows * 128) + (((b & 0x70u) ^ key) | (b & 15u));
+    }
+};
+
+QM_DEV CodeRow code_row(const uint8_t* st, int r) {
+    return CodeRow{st + r * 128, static_cast<uint32_t>(r & 7) << 4};
+}
+
 // One group of one 16-row tile: MMAs into acc, rows r0 (= g) and r8 (= g + 8).
 template <int FMT, int BITS, int GS, int NT>
-QM_DEV void tile_group(const uint8_t* r0, const uint8_t* r8, int gi, int t,
+QM_DEV void tile_group(const CodeRow& r0, const CodeRow& r8, int gi, int t,
                        const uint32_t (&bf)[GS / 16][NT][2], float (&acc)[NT][4]) {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
@@ -109,17 +129,19 @@ QM_DEV void tile_group(const uint8_t* r0, const uint8_t* r8, int gi, int t,
     if constexpr (FMT == QM_AFFINE && BITS == 4) {
         constexpr int V = GS / 32;  // words of a row per lane per group
         uint32_t w0[V], w8[V];
-        const int off = gi * (GS / 2) + t * V * 4;
+        const uint32_t off = gi * (GS / 2) + t * V * 4;
         if constexpr (V == 1) {
-            w0[0] = *reinterpret_cast<const uint32_t*>(r0 + off);
-            w8[0] = *reinterpret_cast<const uint32_t*>(r8 + off);
+            w0[0] = *reinterpret_cast<const uint32_t*>(r0.at(off));
+            w8[0] = *reinterpret_cast<const uint32_t*>(r8.at(off));
+        } else if constexpr (V == 2) {
+            const uint2 a = *reinterpret_cast<const uint2*>(r0.at(off));
+            const uint2 c = *reinterpret_cast<const uint2*>(r8.at(off));
+            w0[0] = a.x; w0[1] = a.y; w8[0] = c.x; w8[1] = c.y;
         } else {
-#pragma unroll
-            for (int v = 0; v < V; v += 2) {
-                const uint2 a = *reinterpret_cast<const uint2*>(r0 + off + 4 * v);
-                const uint2 c = *reinterpret_cast<const uint2*>(r8 + off + 4 * v);
-                w0[v] = a.x; w0[v + 1] = a.y; w8[v] = c.x; w8[v + 1] = c.y;
-            }
+            const uint4 a = *reinterpret_cast<const uint4*>(r0.at(off));
+            const uint4 c = *reinterpret_cast<const uint4*>(r8.at(off));
+            w0[0] = a.x; w0[1] = a.y; w0[2] = a.z; w0[3] = a.w;
+            w8[0] = c.x; w8[1] = c.y; w8[2] = c.z; w8[3] = c.w;
         }
 #pragma unroll
         for (int v = 0; v < V; ++v)
@@ -133,38 +155,42 @@ QM_DEV void tile_group(const uint8_t* r0, const uint8_t* r8, int gi, int t,
                     mma_f16(acc[nt], a0, a1, a2, a3, bf[2 * v + h][nt][0], bf[2 * v + h][nt][1]);
             }
     } else if constexpr (FMT == QM_AFFINE && BITS == 8) {
-        constexpr int V = GS / 16;
-        const int off = gi * GS + t * V * 4;
+        constexpr int V = GS / 16;  // 2, 4 or 8 words
+        const uint32_t off = gi * GS + t * V * 4;
+        uint32_t wa[V], wc[V];
+        if constexpr (V == 2) {
+            const uint2 a = *reinterpret_cast<const uint2*>(r0.at(off));
+            const uint2 c = *reinterpret_cast<const uint2*>(r8.at(off));
+            wa[0] = a.x; wa[1] = a.y; wc[0] = c.x; wc[1] = c.y;
+        } else {
 #pragma unroll
-        for (int v = 0; v < V; v += 2) {
-            const uint2 a = *reinterpret_cast<const uint2*>(r0 + off + 4 * v);
-            const uint2 c = *reinterpret_cast<const uint2*>(r8 + off + 4 * v);
-            const uint32_t wa[2] = {a.x, a.y}, wc[2] = {c.x, c.y};
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                uint32_t a0, a2, a1, a3;
-                dec8(wa[e], a0, a2);
-                dec8(wc[e], a1, a3);
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-                    mma_f16(acc[nt], a0, a1, a2, a3, bf[v + e][nt][0], bf[v + e][nt][1]);
+            for (int q = 0; q < V / 4; ++q) {
+                const uint4 a = *reinterpret_cast<const uint4*>(r0.at(off + 16 * q));
+                const uint4 c = *reinterpret_cast<const uint4*>(r8.at(off + 16 * q));
+                wa[4 * q] = a.x; wa[4 * q + 1] = a.y; wa[4 * q + 2] = a.z; wa[4 * q + 3] = a.w;
+                wc[4 * q] = c.x; wc[4 * q + 1] = c.y; wc[4 * q + 2] = c.z; wc[4 * q + 3] = c.w;
             }
+        }
+#pragma unroll
+        for (int v = 0; v < V; ++v) {
+            uint32_t a0, a2, a1, a3;
+            dec8(wa[v], a0, a2);
+            dec8(wc[v], a1, a3);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_f16(acc[nt], a0, a1, a2, a3, bf[v][nt][0], bf[v][nt][1]);
         }
     } else if constexpr (FMT == QM_Q8_0) {
         // codes of block gi at byte 34*gi + 2 + 8t (2-byte aligned when gi is even)
-        const int o = 34 * gi + 2 + 8 * t;
+        const uint32_t o = 34 * gi + 2 + 8 * t;
         uint32_t c0[2], c8[2];
+        auto w32 = [](const CodeRow& r, uint32_t b) { return *reinterpret_cast<const uint32_t*>(r.at(b)); };
         if (o & 2) {
-            const uint32_t* q0 = reinterpret_cast<const uint32_t*>(r0 + o - 2);
-            const uint32_t* q8 = reinterpret_cast<const uint32_t*>(r8 + o - 2);
-            const uint32_t x0 = q0[0], x1 = q0[1], x2 = q0[2];
-            const uint32_t z0 = q8[0], z1 = q8[1], z2 = q8[2];
+            const uint32_t x0 = w32(r0, o - 2), x1 = w32(r0, o + 2), x2 = w32(r0, o + 6);
+            const uint32_t z0 = w32(r8, o - 2), z1 = w32(r8, o + 2), z2 = w32(r8, o + 6);
             c0[0] = prmt(x0, x1, 0x5432); c0[1] = prmt(x1, x2, 0x5432);
             c8[0] = prmt(z0, z1, 0x5432); c8[1] = prmt(z1, z2, 0x5432);
         } else {
-            const uint32_t* q0 = reinterpret_cast<const uint32_t*>(r0 + o);
-            const uint32_t* q8 = reinterpret_cast<const uint32_t*>(r8 + o);
-            c0[0] = q0[0]; c0[1] = q0[1]; c8[0] = q8[0]; c8[1] = q8[1];
+            c0[0] = w32(r0, o); c0[1] = w32(r0, o + 4); c8[0] = w32(r8, o); c8[1] = w32(r8, o + 4);
         }
 #pragma unroll
         for (int mm = 0; mm < 2; ++mm) {
@@ -175,10 +201,10 @@ QM_DEV void tile_group(const uint8_t* r0, const uint8_t* r8, int gi, int t,
             for (int nt = 0; nt < NT; ++nt) mma_f16(acc[nt], a0, a1, a2, a3, bf[mm][nt][0], bf[mm][nt][1]);
         }
     } else {  // MXFP4
-        const int o = 16 * gi + 4 * t;
+        const uint32_t o = 16 * gi + 4 * t;
         uint32_t h0[4], h8[4];
-        e2m1x8_to_f16x2(*reinterpret_cast<const uint32_t*>(r0 + o), h0);
-        e2m1x8_to_f16x2(*reinterpret_cast<const uint32_t*>(r8 + o), h8);
+        e2m1x8_to_f16x2(*reinterpret_cast<const uint32_t*>(r0.at(o)), h0);
+        e2m1x8_to_f16x2(*reinterpret_cast<const uint32_t*>(r8.at(o)), h8);
 #pragma unroll
         for (int mm = 0; mm < 2; ++mm)
 #pragma unroll
@@ -211,9 +237,12 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     volatile int& s_abort = *reinterpret_cast<volatile int*>(smem + (2 * kMaxStages + 1) * 8);
     volatile int* slot_stage = reinterpret_cast<volatile int*>(smem + (2 * kMaxStages + 2) * 8);
 
+    unsigned int* xmax = reinterpret_cast<unsigned int*>(smem + p.off_tokscale) + 32;  // [16] max |x| bits
     if (threadIdx.x == 0) {
         s_abort = 0;
         for (int i = 0; i < kMaxStages; ++i) slot_stage[i] = -1;
+        for (int i = 0; i < 16; ++i) xmax[i] = 0u;
+        prefetch_tmap(&p.tm_codes);
         for (uint32_t i = 0; i < p.nstage; ++i) {
             mbar_init(bar_full0 + 8 * i, 32);      // the producer's lanes
             mbar_init(bar_empty0 + 8 * i, p.team);  // the warps of the team that read it
@@ -248,12 +277,13 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             const int rows = static_cast<int>(std::min<int64_t>(kRows, p.n - row0));
             uint8_t* st = smem + p.off_stages + slot * p.stage_bytes;
             const uint32_t bar = bar_full0 + 8 * slot;
-            // bulk bytes: codes per row; scales/biases per row when k is split, else one span
-            uint32_t tx = rows * p.code_seg;
+            // whole boxes count in full (rows past n arrive as zeros); scales and
+            // biases come as one span when k is whole, else as one box each
+            uint32_t tx = p.nbox * kRows * 128;
             uint32_t span = 0, span_bulk = 0;
             if (p.scale_seg) {
                 if (S > 1) {
-                    tx += rows * p.scale_seg * (p.biases ? 2 : 1);
+                    tx += kRows * p.scale_seg * (p.biases ? 2 : 1);
                 } else {
                     span = rows * p.scale_seg;
                     span_bulk = span & ~15u;
@@ -263,19 +293,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             if (lane == 0) {
                 slot_stage[slot] = j;
                 mbar_expect_tx(bar, tx);
-            }
-            __syncwarp();
-            if (lane < rows) {
-                const int64_t r = row0 + lane;
-                bulk_g2s(smem_u32(st + lane * p.code_pitch), p.codes + r * p.code_row_bytes + rank * p.code_seg,
-                         p.code_seg, bar);
+                const int32_t x0 = static_cast<int32_t>(rank * p.code_seg), y0 = static_cast<int32_t>(row0);
+                for (uint32_t c = 0; c < p.nbox; ++c)
+                    tma_load_2d(smem_u32(st + c * kRows * 128), &p.tm_codes, x0 + 128 * c, y0, bar);
                 if (p.scale_seg && S > 1) {
-                    const int64_t off = r * p.scale_row_bytes + rank * p.scale_seg;
-                    bulk_g2s(smem_u32(st + p.off_scales + lane * p.scale_seg), p.scales + off, p.scale_seg, bar);
-                    if (p.biases)
-                        bulk_g2s(smem_u32(st + p.off_biases + lane * p.scale_seg), p.biases + off, p.scale_seg, bar);
+                    const int32_t xs0 = static_cast<int32_t>(rank * p.scale_seg);
+                    tma_load_2d(smem_u32(st + p.off_scales), &p.tm_scales, xs0, y0, bar);
+                    if (p.biases) tma_load_2d(smem_u32(st + p.off_biases), &p.tm_biases, xs0, y0, bar);
                 }
             }
+            __syncwarp();
             if (p.scale_seg && S == 1) {
                 const int64_t off = row0 * p.scale_row_bytes;
                 if (lane == 0 && span_bulk) {
@@ -299,54 +326,59 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
         // ------------------------------------------------------------ consumers
         const int ctid = threadIdx.x;  // 0 .. 511
         float* tokscale = reinterpret_cast<float*>(smem + p.off_tokscale);  // [16] 2^-E
-        float* tokmul = tokscale + 16;                                       // [16] 2^E
         const uint16_t* xs = reinterpret_cast<const uint16_t*>(smem + p.off_xraw);  // [M][krange]
         if (!mbar_wait(bar_x, 0)) {
             if (lane == 0) { atomicOr(&g_err_gemv, DEV_ERR_TIMEOUT); s_abort = 1; }
         }
         // 1. per-token power-of-two scale over this CTA's k range (warp m: token m)
         {
-            const int m = warp;
-            float amax = 0.0f;
-            if (m < p.M) {
-                const uint16_t* xr = xs + m * p.krange;
-                for (int64_t i = lane * 8; i < p.krange; i += 256) {
-                    const uint4 q = *reinterpret_cast<const uint4*>(xr + i);
-                    const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+            // max |x| per token: one pass over the staged rows, order-free
+            const int per_row = static_cast<int>(p.krange / 8);
+            for (int i = ctid; i < p.M * per_row; i += kWarps * 32) {
+                const uint4 q = *reinterpret_cast<const uint4*>(xs + 8 * i);
+                const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
+                float amax = 0.0f;
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w4[e] & 0xFFFF)));
-                        amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w4[e] >> 16)));
-                    }
+                for (int e = 0; e < 4; ++e) {
+                    amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w4[e] & 0xFFFF)));
+                    amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w4[e] >> 16)));
                 }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-            }
-            if (lane == 0) {
-                int E = 0;  // x' = x * 2^E puts max |x'| in [2^14, 2^15)
-                if (amax > 0.0f) {
-                    const int ex = static_cast<int>((__float_as_uint(amax) >> 23) & 0xFF) - 127;
-                    E = min(max(14 - ex, -126), 126);
-                }
-                tokmul[m] = (m < p.M) ? __uint_as_float(static_cast<uint32_t>(E + 127) << 23) : 0.0f;
-                tokscale[m] = __uint_as_float(static_cast<uint32_t>(-E + 127) << 23);
+                if (amax > 0.0f) atomicMax(&xmax[i / per_row], __float_as_uint(amax));
             }
         }
         named_bar_sync(1, kWarps * 32);
-        // 2. B fragments for every group of the k range, and per-token group sums
+        // x' = x * 2^E puts max |x'| in [2^14, 2^15): every bf16 value is then exact in f16
+        auto token_exp = [&](int m) {
+            const uint32_t bits = xmax[m];
+            if (bits == 0u) return 0;
+            const int ex = static_cast<int>((bits >> 23) & 0xFF) - 127;
+            return min(max(14 - ex, -126), 126);
+        };
+        if (ctid < 16) {
+            const int E = token_exp(ctid);
+            tokscale[ctid] = __uint_as_float(static_cast<uint32_t>(-E + 127) << 23);
+        }
+        // 2. B fragments for every group of the k range; each quad of lanes
+        //    also sums its token's B values (F) and x' (X) over the group
         uint32_t* xfrag = reinterpret_cast<uint32_t*>(smem + p.off_xfrag);
         float2* tok = reinterpret_cast<float2*>(smem + p.off_tok);  // [groups][16]
         {
-            const int items = groups * 32 * NT;
+            const int items = groups * 32 * NT;  // a multiple of 32: a warp shares (gi, nt)
             for (int it = ctid; it < items; it += kWarps * 32) {
-                const int nt = it % NT, ln = (it / NT) % 32, gi = it / (NT * 32);
+                const int ln = it % 32, nt = (it / 32) % NT, gi = it / (32 * NT);
                 const int tg = ln >> 2, t = ln & 3;
                 const int m = nt * 8 + tg;
                 const bool live = m < p.M;  // padding tokens get exact zeros
-                const float mul = live ? tokmul[m] : 0.0f;
+                const float mul = live ? __uint_as_float(static_cast<uint32_t>(token_exp(m) + 127) << 23) : 0.0f;
                 const uint16_t* xr = xs + (live ? m : 0) * p.krange;
                 uint32_t* dst = xfrag + ((gi * 32 + ln) * MM) * NT * 2 + nt * 2;
+                float F = 0.0f, X = 0.0f;
                 auto xv = [&](int kk) { return live ? bf16_bits_to_f32(xr[kk]) * mul : 0.0f; };
+                auto put = [&](int idx, float lo, float hi, float flo, float fhi) {
+                    dst[idx] = pack_f16x2(lo * flo, hi * fhi);
+                    X += lo + hi;
+                    F += lo * flo + hi * fhi;
+                };
                 if constexpr (FMT == QM_AFFINE && BITS == 4) {
                     constexpr int V = GS / 32;
 #pragma unroll
@@ -355,9 +387,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
                             const int mm = 2 * v + h;
-                            dst[mm * NT * 2 + 0] = pack_f16x2(xv(k0 + 2 * h), xv(k0 + 4 + 2 * h));
-                            dst[mm * NT * 2 + 1] =
-                                pack_f16x2(xv(k0 + 1 + 2 * h) * 0.0625f, xv(k0 + 5 + 2 * h) * 0.0625f);
+                            put(mm * NT * 2 + 0, xv(k0 + 2 * h), xv(k0 + 4 + 2 * h), 1.0f, 1.0f);
+                            put(mm * NT * 2 + 1, xv(k0 + 1 + 2 * h), xv(k0 + 5 + 2 * h), 0.0625f, 0.0625f);
                         }
                     }
                 } else if constexpr (FMT == QM_AFFINE && BITS == 8) {
@@ -365,43 +396,25 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 #pragma unroll
                     for (int v = 0; v < V; ++v) {
                         const int k0 = 4 * (gi * (GS / 4) + t * V + v);
-                        dst[v * NT * 2 + 0] = pack_f16x2(xv(k0), xv(k0 + 1));
-                        dst[v * NT * 2 + 1] = pack_f16x2(xv(k0 + 2), xv(k0 + 3));
+                        put(v * NT * 2 + 0, xv(k0), xv(k0 + 1), 1.0f, 1.0f);
+                        put(v * NT * 2 + 1, xv(k0 + 2), xv(k0 + 3), 1.0f, 1.0f);
                     }
                 } else {  // Q8_0, MXFP4: lane t holds values 8t .. 8t+7 of the block
 #pragma unroll
                     for (int mm = 0; mm < 2; ++mm) {
                         const int k0 = 32 * gi + 8 * t + 4 * mm;
-                        dst[mm * NT * 2 + 0] = pack_f16x2(xv(k0), xv(k0 + 1));
-                        dst[mm * NT * 2 + 1] = pack_f16x2(xv(k0 + 2), xv(k0 + 3));
+                        put(mm * NT * 2 + 0, xv(k0), xv(k0 + 1), 1.0f, 1.0f);
+                        put(mm * NT * 2 + 1, xv(k0 + 2), xv(k0 + 3), 1.0f, 1.0f);
                     }
                 }
-            }
-            // per (group, token): (offset, sum of x'), one warp per pair; the
-            // offset is the magic times the sum of the B values the MMAs saw
-            if constexpr (FMT != QM_MXFP4) {
-                const float magic = (FMT == QM_Q8_0) ? 1152.0f : 1024.0f;
-                for (int it = warp; it < groups * p.M; it += kWarps) {
-                    const int m = it % p.M, gi = it / p.M;
-                    const float mul = tokmul[m];
-                    const uint16_t* xr = xs + m * p.krange + gi * GS;
-                    float F = 0.0f, X = 0.0f;
-#pragma unroll
-                    for (int e = lane; e < GS; e += 32) {
-                        const float xe = bf16_bits_to_f32(xr[e]) * mul;
-                        X += xe;
-                        F += (FMT == QM_AFFINE && BITS == 4 && (e & 1)) ? xe * 0.0625f : xe;
-                    }
-#pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) {
-                        X += __shfl_xor_sync(0xffffffffu, X, o);
-                        F += __shfl_xor_sync(0xffffffffu, F, o);
-                    }
-                    if (lane == 0) tok[gi * 16 + m] = make_float2(magic * F, X);
-                }
-                for (int it = ctid; it < groups * (16 - p.M); it += kWarps * 32) {
-                    const int gi = it / (16 - p.M), m = p.M + it % (16 - p.M);
-                    tok[gi * 16 + m] = make_float2(0.0f, 0.0f);
+                if constexpr (FMT != QM_MXFP4) {
+                    // the offset the magic adds: magic * sum of the B values the MMAs see
+                    X += __shfl_xor_sync(0xffffffffu, X, 1);
+                    F += __shfl_xor_sync(0xffffffffu, F, 1);
+                    X += __shfl_xor_sync(0xffffffffu, X, 2);
+                    F += __shfl_xor_sync(0xffffffffu, F, 2);
+                    const float magic = (FMT == QM_Q8_0) ? 1152.0f : 1024.0f;
+                    if (t == 0) tok[gi * 16 + m] = make_float2(magic * F, X);
                 }
             }
         }
@@ -466,8 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                 float acc[2][NT][4];
 #pragma unroll
                 for (int tt = 0; tt < 2; ++tt)
-                    tile_group<FMT, BITS, GS, NT>(st + (16 * tt + g) * p.code_pitch,
-                                                  st + (16 * tt + g + 8) * p.code_pitch, gi, t, bf, acc[tt]);
+                    tile_group<FMT, BITS, GS, NT>(code_row(st, 16 * tt + g), code_row(st, 16 * tt + g + 8), gi, t,
+                                                  bf, acc[tt]);
 #pragma unroll
                 for (int tt = 0; tt < 2; ++tt) {
                     const int ra = 16 * tt + g, rb = ra + 8;
@@ -481,8 +494,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                         b0 = sval(bi[ra * stride + gi], p.sdt);
                         b8 = sval(bi[rb * stride + gi], p.sdt);
                     } else if constexpr (FMT == QM_Q8_0) {
-                        s0 = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(st + ra * p.code_pitch + 34 * gi));
-                        s8 = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(st + rb * p.code_pitch + 34 * gi));
+                        s0 = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(code_row(st, ra).at(34 * gi)));
+                        s8 = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(code_row(st, rb).at(34 * gi)));
                     } else {
                         const uint8_t* sc = st + p.off_scales;
                         s0 = e8m0_to_f32(sc[ra * p.scale_seg + gi]);
@@ -600,14 +613,6 @@ static int64_t code_bytes(const WDesc& w, int64_t kk) {
     return kk * w.bits / 8;
 }
 
-// 32-bit words one lane reads from a row per load (sets the pitch padding
-// that keeps the 8 rows of a load on distinct banks).
-static int lds_words(const WDesc& w) {
-    if (w.fmt == QM_AFFINE && w.bits == 4 && w.gs == 32) return 1;
-    if (w.fmt == QM_MXFP4 || w.fmt == QM_Q8_0) return 1;
-    return 2;
-}
-
 __global__ void cluster_probe_kernel() {}
 
 // Clusters of S CTAs (one per SM, `smem` bytes each) that can be resident at
@@ -654,14 +659,15 @@ static bool plan_for(const WDesc& w, int64_t M, int S, Plan* out) {
     if (S > 1 && sseg % 16) return false;
     Params& p = out->p;
     p = Params{};
+    if (S > 1 && (sseg > 256 || w.scale_row_bytes % 16)) return false;  // scale boxes
     p.code_seg = static_cast<uint32_t>(cseg);
-    p.code_pitch = round_up(cseg, 128) + 16 * lds_words(w);
+    p.nbox = static_cast<uint32_t>((cseg + 127) / 128);
     p.scale_seg = static_cast<uint32_t>(sseg);
-    const uint32_t codes_bytes = kRows * p.code_pitch;
+    const uint32_t codes_bytes = p.nbox * kRows * 128;
     const uint32_t sc_bytes = round_up(kRows * sseg, 128);
     p.off_scales = codes_bytes;
     p.off_biases = codes_bytes + sc_bytes;
-    p.stage_bytes = round_up(codes_bytes + sc_bytes * (w.fmt == QM_AFFINE ? 2 : 1), 128);
+    p.stage_bytes = round_up(codes_bytes + sc_bytes * (w.fmt == QM_AFFINE ? 2 : 1), 1024);  // swizzled boxes
     const int64_t groups = kr / w.gs;
     // work split: as many clusters as fit one CTA per SM
     p.n_stages = (w.n + kRows - 1) / kRows;
@@ -677,8 +683,8 @@ static bool plan_for(const WDesc& w, int64_t M, int S, Plan* out) {
     while (T > 1 && T > groups) T /= 2;
     p.team = T;
     // shared memory
-    p.off_tokscale = 512;
-    p.off_tok = p.off_tokscale + 128;
+    p.off_tokscale = 512;                  // [16] 2^-E, [16] unused, [16] max |x| bits
+    p.off_tok = p.off_tokscale + 256;
     p.off_xfrag = round_up(p.off_tok + groups * 16 * 8, 128);
     const uint64_t xfrag_bytes = static_cast<uint64_t>(kr) * 16 * NT;
     p.off_red = round_up(p.off_xfrag + xfrag_bytes, 128);
@@ -777,6 +783,18 @@ qm_status launch_gemv(const WDesc& w, const void* x, int64_t M, void* y, cudaStr
     p.sdt = w.sdt;
     p.code_row_bytes = w.code_row_bytes;
     p.scale_row_bytes = w.scale_row_bytes;
+    bool maps = make_tmap_2d(&p.tm_codes, w.codes, w.code_row_bytes, w.n, w.code_row_bytes, 128, kRows, true);
+    if (maps && p.S > 1 && p.scale_seg) {
+        maps = make_tmap_2d(&p.tm_scales, w.scales, w.scale_row_bytes, w.n, w.scale_row_bytes, p.scale_seg,
+                            kRows, false);
+        if (maps && w.biases)
+            maps = make_tmap_2d(&p.tm_biases, w.biases, w.scale_row_bytes, w.n, w.scale_row_bytes, p.scale_seg,
+                                kRows, false);
+    }
+    if (!maps) {  // the driver refused a descriptor for this shape: the plain kernel
+        cudaError_t e = launch_apply_simple(w, x, M, y, st);
+        return e == cudaSuccess ? QM_OK : cuda_fail(e, "apply launch");
+    }
     const bool two = M > 8;
     cudaError_t e = cudaErrorInvalidValue;
 #define QM_GEMV_CASE(F, B, G)                                                                  \

@@ -38,6 +38,13 @@ qm_status validate_weight(const qm_weight* w, WDesc* d);
 
 int dtype_size(int dt);
 
+// Encodes a 2-d tiled TMA descriptor (CUtensorMap, 128 bytes) over a byte
+// array of `rows` rows of `inner_bytes` bytes at `row_stride` bytes apart; a
+// box is `box_inner` bytes by `box_rows` rows, 128-byte swizzled if asked,
+// out-of-range elements read as zeros. Returns false if the driver refuses.
+bool make_tmap_2d(void* map, const void* base, uint64_t inner_bytes, uint64_t rows,
+                  uint64_t row_stride, uint32_t box_inner, uint32_t box_rows, bool swizzle128);
+
 // Number of SMs on the current device (cached per device).
 int num_sms();
 // Opt-in shared memory per block on the current device (cached per device).
