@@ -9,10 +9,12 @@
 // are float32 sums.
 //
 // Design (one GB300: 152 SMs, HBM3e):
-//  * A CTA is 1 producer warp + 16 consumer warps. The producer bulk-copies
-//    the activation rows once, then streams 32-row stages of the packed
-//    weight (codes, scales, biases) into shared memory with cp.async.bulk,
-//    completing on mbarriers.
+//  * A CTA is 1 producer warp + 8 consumer warps, two CTAs to an SM where
+//    shared memory allows (so the next launch's CTAs can start beside the
+//    last ones of this launch). The producer streams 32-row stages of the
+//    packed weight into shared memory with 2-d TMA boxes (codes, 128B-
+//    swizzled) and bulk copies (scales, biases), completing on mbarriers,
+//    and bulk-copies the activation rows once.
 //  * Consumer warps form teams of T. A team takes whole stages; its warps
 //    split the stage's groups along k, so a stage is worked on by T warps at
 //    once and each warp carries two independent 16-row MMA tiles. A warp
@@ -53,7 +55,7 @@ uint32_t gemv_read_clear_error() {
 namespace gemv {
 
 constexpr int kRows = 32;            // rows per stage (two MMA row tiles)
-constexpr int kWarps = 16;           // consumer warps
+constexpr int kWarps = 8;            // consumer warps
 constexpr int kThreads = (kWarps + 1) * 32;
 constexpr int kMaxStages = 16;
 constexpr uint32_t kMagic = 0x64006400u;  // f16x2 (1024, 1024)
@@ -215,7 +217,7 @@ QM_DEV void tile_group(const CodeRow& r0, const CodeRow& r8, int gi, int t,
 }
 
 template <int FMT, int BITS, int GS, int NT>
-__global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(1024) uint8_t smem[];
     constexpr int MM = GS / 16;  // MMAs per group
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -257,14 +259,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
     if (warp == kWarps) {
         // ------------------------------------------------------------ producer
         const uint32_t xbytes = static_cast<uint32_t>(p.krange * 2);
-        if (lane == 0) {
-            mbar_expect_tx(bar_x, xbytes * p.M);
-            mbar_arrive(bar_x);
-        }
-        __syncwarp();
-        if (lane < p.M)
-            bulk_g2s(smem_u32(smem + p.off_xraw + lane * xbytes), p.x + lane * p.k + kbase, xbytes, bar_x);
+        auto copy_x = [&]() {  // after the first stage's copies are under way
+            if (lane == 0) {
+                mbar_expect_tx(bar_x, xbytes * p.M);
+                mbar_arrive(bar_x);
+            }
+            __syncwarp();
+            if (lane < p.M)
+                bulk_g2s(smem_u32(smem + p.off_xraw + lane * xbytes), p.x + lane * p.k + kbase, xbytes, bar_x);
+        };
         int issued = 0;
+        if (nst == 0) copy_x();
         for (int j = 0; j < nst; ++j) {
             const uint32_t slot = j % p.nstage;
             const uint32_t par = ((j / p.nstage) & 1) ^ 1;
@@ -315,7 +320,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                 }
             }
             mbar_arrive(bar);
+            if (j == 0) copy_x();
         }
+        if (issued == 0 && nst > 0) copy_x();  // abandoned before the first stage
         if (s_abort) {
             // abandoned: let the copies already issued land before the CTA exits
             for (int j = std::max(0, issued - static_cast<int>(p.nstage)); j < issued; ++j)
@@ -451,6 +458,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
             }
             live = __shfl_sync(0xffffffffu, live ? 1 : 0, 0) != 0;
             const uint8_t* st = smem + p.off_stages + slot * p.stage_bytes;
+            const CodeRow rows_[4] = {code_row(st, g), code_row(st, g + 8), code_row(st, 16 + g),
+                                      code_row(st, 24 + g)};
             float y[2][NT][4];
 #pragma unroll
             for (int tt = 0; tt < 2; ++tt)
@@ -459,28 +468,29 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 #pragma unroll
                     for (int i = 0; i < 4; ++i) y[tt][nt][i] = 0.0f;
 
-            for (int gi = gb; gi < (live ? ge : gb); ++gi) {
+            // one group of both tiles: MMAs, then scale (and bias) into y
+            auto do_group = [&](int gi, float (&acc)[2][NT][4]) {
                 uint32_t bf[MM][NT][2];
                 {
                     const uint4* src = reinterpret_cast<const uint4*>(xfrag + ((gi * 32 + lane) * MM) * NT * 2);
-                    uint32_t* b = &bf[0][0][0];
+                    uint32_t* bb = &bf[0][0][0];
 #pragma unroll
                     for (int q = 0; q < MM * NT / 2; ++q) {
                         const uint4 v = src[q];
-                        b[4 * q] = v.x; b[4 * q + 1] = v.y; b[4 * q + 2] = v.z; b[4 * q + 3] = v.w;
+                        bb[4 * q] = v.x; bb[4 * q + 1] = v.y; bb[4 * q + 2] = v.z; bb[4 * q + 3] = v.w;
                     }
                 }
+#pragma unroll
+                for (int tt = 0; tt < 2; ++tt)
+                    tile_group<FMT, BITS, GS, NT>(rows_[2 * tt], rows_[2 * tt + 1], gi, t, bf, acc[tt]);
+            };
+            auto epilogue = [&](int gi, const float (&acc)[2][NT][4]) {
                 float4 td[NT];  // (O[2t], X[2t], O[2t+1], X[2t+1]) per token half
                 if constexpr (FMT != QM_MXFP4) {
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
                         td[nt] = *reinterpret_cast<const float4*>(tok + gi * 16 + nt * 8 + 2 * t);
                 }
-                float acc[2][NT][4];
-#pragma unroll
-                for (int tt = 0; tt < 2; ++tt)
-                    tile_group<FMT, BITS, GS, NT>(code_row(st, 16 * tt + g), code_row(st, 16 * tt + g + 8), gi, t,
-                                                  bf, acc[tt]);
 #pragma unroll
                 for (int tt = 0; tt < 2; ++tt) {
                     const int ra = 16 * tt + g, rb = ra + 8;
@@ -494,8 +504,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                         b0 = sval(bi[ra * stride + gi], p.sdt);
                         b8 = sval(bi[rb * stride + gi], p.sdt);
                     } else if constexpr (FMT == QM_Q8_0) {
-                        s0 = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(code_row(st, ra).at(34 * gi)));
-                        s8 = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(code_row(st, rb).at(34 * gi)));
+                        s0 = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(rows_[2 * tt].at(34 * gi)));
+                        s8 = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(rows_[2 * tt + 1].at(34 * gi)));
                     } else {
                         const uint8_t* sc = st + p.off_scales;
                         s0 = e8m0_to_f32(sc[ra * p.scale_seg + gi]);
@@ -504,29 +514,70 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         float* yv = y[tt][nt];
-                        const float* a = acc[tt][nt];
+                        const float* c = acc[tt][nt];
                         if constexpr (FMT == QM_MXFP4) {
-                            yv[0] = fmaf(s0, a[0], yv[0]);
-                            yv[1] = fmaf(s0, a[1], yv[1]);
-                            yv[2] = fmaf(s8, a[2], yv[2]);
-                            yv[3] = fmaf(s8, a[3], yv[3]);
+                            yv[0] = fmaf(s0, c[0], yv[0]);
+                            yv[1] = fmaf(s0, c[1], yv[1]);
+                            yv[2] = fmaf(s8, c[2], yv[2]);
+                            yv[3] = fmaf(s8, c[3], yv[3]);
                         } else {
                             const float4 d = td[nt];
-                            yv[0] = fmaf(s0, a[0] - d.x, fmaf(b0, d.y, yv[0]));
-                            yv[1] = fmaf(s0, a[1] - d.z, fmaf(b0, d.w, yv[1]));
-                            yv[2] = fmaf(s8, a[2] - d.x, fmaf(b8, d.y, yv[2]));
-                            yv[3] = fmaf(s8, a[3] - d.z, fmaf(b8, d.w, yv[3]));
+                            yv[0] = fmaf(s0, c[0] - d.x, fmaf(b0, d.y, yv[0]));
+                            yv[1] = fmaf(s0, c[1] - d.z, fmaf(b0, d.w, yv[1]));
+                            yv[2] = fmaf(s8, c[2] - d.x, fmaf(b8, d.y, yv[2]));
+                            yv[3] = fmaf(s8, c[3] - d.z, fmaf(b8, d.w, yv[3]));
                         }
                     }
                 }
+            };
+            // groups two at a time: four independent MMA chains in flight
+            const int gend = live ? ge : gb;
+            int gi = gb;
+            for (; gi + 1 < gend; gi += 2) {
+                float acc0[2][NT][4], acc1[2][NT][4];
+                do_group(gi, acc0);
+                do_group(gi + 1, acc1);
+                epilogue(gi, acc0);
+                epilogue(gi + 1, acc1);
+            }
+            if (gi < gend) {
+                float acc0[2][NT][4];
+                do_group(gi, acc0);
+                epilogue(gi, acc0);
             }
             __syncwarp();
             if (lane == 0 && live) mbar_arrive(bar_empty0 + 8 * slot);
 
-            // ---- the team's sum, in warp order; then undo the token scale
-            bool writer = true;
-            if (T > 1) {
-                float* mine = red + ((((team * 2 + buf) * T + wi) * 2) * NT * 4) * 32;
+            // ---- the team's sum in warp order, spread over the team's warps;
+            //      then undo the token scale and store
+            const int64_t row0 = (stage0 + j) * kRows;
+            auto store = [&](int tt, int nt, int ln, int i, float v) {
+                const int m = nt * 8 + 2 * (ln & 3) + (i & 1);
+                const int r = 16 * tt + (ln >> 2) + ((i & 2) ? 8 : 0);
+                v *= tokscale[m];
+                if (S == 1) {
+                    if (m < p.M && row0 + r < p.n) {
+                        __nv_bfloat16 bv = __float2bfloat16_rn(v);
+                        p.y[static_cast<int64_t>(m) * p.n + row0 + r] = *reinterpret_cast<uint16_t*>(&bv);
+                    }
+                } else {
+                    partial[(j * kRows + r) * 16 + m] = v;
+                }
+            };
+            if (T == 1) {
+                if (live && !s_abort) {
+#pragma unroll
+                    for (int tt = 0; tt < 2; ++tt)
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                            for (int i = 0; i < 4; ++i) store(tt, nt, lane, i, y[tt][nt][i]);
+                }
+            } else {
+                // red[team][buf][warp of team][tt][nt][lane][4]
+                constexpr int E = 2 * NT * 32 * 4;  // floats per warp partial
+                float* base = red + ((team * 2 + buf) * T) * E;
+                float* mine = base + wi * E;
 #pragma unroll
                 for (int tt = 0; tt < 2; ++tt)
 #pragma unroll
@@ -534,45 +585,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_kernel(const __grid_constant
                         *reinterpret_cast<float4*>(mine + ((tt * NT + nt) * 32 + lane) * 4) =
                             make_float4(y[tt][nt][0], y[tt][nt][1], y[tt][nt][2], y[tt][nt][3]);
                 named_bar_sync(2 + team, T * 32);
-                writer = (wi == 0);
-                if (writer) {
-                    const float* base = red + (((team * 2 + buf) * T) * 2) * NT * 4 * 32;
-#pragma unroll
-                    for (int tt = 0; tt < 2; ++tt)
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt) {
-                            float s4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-                            for (int q = 0; q < T; ++q) {
-                                const float4 v = *reinterpret_cast<const float4*>(
-                                    base + (((q * 2 + tt) * NT + nt) * 32 + lane) * 4);
-                                s4[0] += v.x; s4[1] += v.y; s4[2] += v.z; s4[3] += v.w;
-                            }
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) y[tt][nt][i] = s4[i];
-                        }
+                if (live && !s_abort) {
+                    // warp wi adds entries [wi*E/T, (wi+1)*E/T) over the team's warps in order
+                    for (int e = wi * (E / T) + lane; e < (wi + 1) * (E / T); e += 32) {
+                        float sum = 0.0f;
+                        for (int q = 0; q < T; ++q) sum += base[q * E + e];
+                        const int i = e & 3, ln = (e >> 2) & 31, tn = e >> 7;
+                        store(tn / NT, tn % NT, ln, i, sum);
+                    }
                 }
                 buf ^= 1;
-            }
-            if (writer && live && !s_abort) {
-                const int64_t row0 = (stage0 + j) * kRows;
-#pragma unroll
-                for (int tt = 0; tt < 2; ++tt)
-#pragma unroll
-                    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const int m = nt * 8 + 2 * t + (i & 1);
-                            const int r = 16 * tt + g + ((i & 2) ? 8 : 0);
-                            const float v = y[tt][nt][i] * tokscale[m];
-                            if (S == 1) {
-                                if (m < p.M && row0 + r < p.n) {
-                                    __nv_bfloat16 b = __float2bfloat16_rn(v);
-                                    p.y[static_cast<int64_t>(m) * p.n + row0 + r] = *reinterpret_cast<uint16_t*>(&b);
-                                }
-                            } else {
-                                partial[(j * kRows + r) * 16 + m] = v;
-                            }
-                        }
             }
         }
     }
@@ -646,7 +668,8 @@ static int max_clusters(int S, size_t smem) {
     return n;
 }
 
-static bool plan_for(const WDesc& w, int64_t M, int S, Plan* out) {
+// A plan for S CTAs per cluster (splitting k) and `per_sm` CTAs per SM.
+static bool plan_for(const WDesc& w, int64_t M, int S, int per_sm, Plan* out) {
     if (w.k % S) return false;
     const int64_t kr = w.k / S;
     if (kr % w.gs) return false;
@@ -657,9 +680,9 @@ static bool plan_for(const WDesc& w, int64_t M, int S, Plan* out) {
     if (w.fmt == QM_AFFINE) sseg = kr / w.gs * 2;
     if (w.fmt == QM_MXFP4) sseg = kr / 32;
     if (S > 1 && sseg % 16) return false;
+    if (S > 1 && (sseg > 256 || w.scale_row_bytes % 16)) return false;  // scale boxes
     Params& p = out->p;
     p = Params{};
-    if (S > 1 && (sseg > 256 || w.scale_row_bytes % 16)) return false;  // scale boxes
     p.code_seg = static_cast<uint32_t>(cseg);
     p.nbox = static_cast<uint32_t>((cseg + 127) / 128);
     p.scale_seg = static_cast<uint32_t>(sseg);
@@ -669,35 +692,38 @@ static bool plan_for(const WDesc& w, int64_t M, int S, Plan* out) {
     p.off_biases = codes_bytes + sc_bytes;
     p.stage_bytes = round_up(codes_bytes + sc_bytes * (w.fmt == QM_AFFINE ? 2 : 1), 1024);  // swizzled boxes
     const int64_t groups = kr / w.gs;
-    // work split: as many clusters as fit one CTA per SM
+    const int64_t budget = (per_sm == 2 ? (max_smem_optin() + 1024) / 2 : max_smem_optin()) - 1024;
+    // work split: clusters of S CTAs, per_sm CTAs to an SM
     p.n_stages = (w.n + kRows - 1) / kRows;
-    int64_t G = std::max<int64_t>(1, num_sms() / S);
-    if (S > 1) G = std::max<int64_t>(1, std::min<int64_t>(G, max_clusters(S, max_smem_optin() - 1024)));
+    int64_t G = std::max<int64_t>(1, int64_t(num_sms()) * per_sm / S);
+    if (S > 1) G = std::max<int64_t>(1, std::min<int64_t>(G, max_clusters(S, budget)));
     G = std::min<int64_t>(G, p.n_stages);
     const int64_t spc = (p.n_stages + G - 1) / G;
     G = (p.n_stages + spc - 1) / spc;
-    // teams: enough teams for the stages a CTA has, each warp at least one group
+    // shared memory: fixed part, then as many stage slots as fit
+    auto layout = [&](bool with_red) -> int64_t {
+        p.off_tokscale = 512;  // [16] 2^-E, [16] unused, [16] max |x| bits
+        p.off_tok = p.off_tokscale + 256;
+        p.off_xfrag = round_up(p.off_tok + groups * 16 * 8, 128);
+        const uint64_t xfrag_bytes = static_cast<uint64_t>(kr) * 16 * NT;
+        p.off_red = round_up(p.off_xfrag + xfrag_bytes, 128);
+        const uint64_t red_bytes = with_red ? static_cast<uint64_t>(kWarps) * 2 * 2 * NT * 32 * 4 * 4 : 0;
+        p.off_xraw = round_up(p.off_red + red_bytes, 128);
+        const uint64_t partial_bytes = S > 1 ? static_cast<uint64_t>(spc) * kRows * 16 * 4 : 0;
+        const uint64_t xraw_bytes = static_cast<uint64_t>(M) * kr * 2;
+        p.off_stages = round_up(p.off_xraw + std::max(partial_bytes, xraw_bytes), 1024);
+        const int64_t room = budget - p.off_stages;
+        return std::min<int64_t>(std::min<int64_t>(kMaxStages, room / p.stage_bytes), std::max<int64_t>(2, spc));
+    };
+    int64_t nst = layout(true);
+    if (nst < 2) return false;
+    // teams: one per stage a CTA can hold in flight, each warp at least one group
     int teams = 1;
-    while (teams * 2 <= kWarps && teams * 2 <= spc) teams *= 2;
+    while (teams * 2 <= kWarps && teams * 2 <= spc && teams * 2 <= nst) teams *= 2;
     int T = kWarps / teams;
     while (T > 1 && T > groups) T /= 2;
+    if (T == 1) nst = layout(false);
     p.team = T;
-    // shared memory
-    p.off_tokscale = 512;                  // [16] 2^-E, [16] unused, [16] max |x| bits
-    p.off_tok = p.off_tokscale + 256;
-    p.off_xfrag = round_up(p.off_tok + groups * 16 * 8, 128);
-    const uint64_t xfrag_bytes = static_cast<uint64_t>(kr) * 16 * NT;
-    p.off_red = round_up(p.off_xfrag + xfrag_bytes, 128);
-    const uint64_t red_bytes = T > 1 ? static_cast<uint64_t>(kWarps / T) * 2 * T * 2 * NT * 4 * 32 * 4 : 0;
-    p.off_xraw = round_up(p.off_red + red_bytes, 128);
-    const uint64_t partial_bytes = S > 1 ? static_cast<uint64_t>(spc) * kRows * 16 * 4 : 0;
-    const uint64_t xraw_bytes = static_cast<uint64_t>(M) * kr * 2;
-    p.off_stages = round_up(p.off_xraw + std::max(partial_bytes, xraw_bytes), 1024);
-    const int64_t budget = max_smem_optin() - 1024;
-    const int64_t room = budget - p.off_stages;
-    if (room < 2 * static_cast<int64_t>(p.stage_bytes)) return false;
-    int64_t nst = std::min<int64_t>(kMaxStages, room / p.stage_bytes);
-    nst = std::min<int64_t>(nst, std::max<int64_t>(2, spc));
     p.nstage = static_cast<uint32_t>(nst);
     p.S = S;
     p.krange = kr;
@@ -709,22 +735,24 @@ static bool plan_for(const WDesc& w, int64_t M, int S, Plan* out) {
     return true;
 }
 
-// Pick the k split: least per-CTA work (stages x k range), then fewest
-// splits; a split that keeps three stages in flight beats one that cannot.
+// Pick the k split and CTAs per SM: least per-CTA work (stages x k range,
+// halved where two CTAs share an SM), then fewest splits; a plan that keeps
+// three stages in flight beats one that cannot.
 static Plan make_plan(const WDesc& w, int64_t M) {
     Plan best;
     double best_cost = 1e300;
-    for (int S = 1; S <= 8; ++S) {
-        Plan pl;
-        if (!plan_for(w, M, S, &pl)) continue;
-        const bool shallow = pl.p.nstage < 3 && pl.p.stages_per_cluster >= 3;
-        const double cost = static_cast<double>(pl.p.stages_per_cluster) * pl.p.krange *
-                            (1.0 + 0.03 * (S - 1)) * (shallow ? 2.0 : 1.0);
-        if (cost < best_cost * 0.999) {
-            best_cost = cost;
-            best = pl;
+    for (int per_sm = 2; per_sm >= 1; --per_sm)
+        for (int S = 1; S <= 8; ++S) {
+            Plan pl;
+            if (!plan_for(w, M, S, per_sm, &pl)) continue;
+            const bool shallow = pl.p.nstage < 3 && pl.p.stages_per_cluster >= 3;
+            const double cost = static_cast<double>(pl.p.stages_per_cluster) * pl.p.krange / per_sm *
+                                (1.0 + 0.03 * (S - 1)) * (shallow ? 2.0 : 1.0);
+            if (cost < best_cost * 0.999) {
+                best_cost = cost;
+                best = pl;
+            }
         }
-    }
     return best;
 }
 
