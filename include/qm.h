@@ -124,6 +124,22 @@ qm_status qm_apply_experts(const qm_weight* w, const void* ids, int32_t id_type,
                            int64_t topk, const void* x, int64_t x_rows, int32_t x_dtype, void* y,
                            void* workspace, size_t workspace_bytes, qm_stream_t stream);
 
+/* qm_apply_experts without a workspace argument, for callers that cannot
+ * allocate device memory themselves: a plug-in living inside a host program
+ * that owns every device allocation, or a latency-critical loop that must not
+ * pay cudaMalloc's implicit synchronization. The routing tables go to a 1 MiB
+ * array that the library reserves on every GPU that loads it, enough for, e.g.,
+ * 245,760 positions over 32 experts; a larger T*topk*E is refused with
+ * QM_EINVAL naming "workspace". The first call on a device looks up that
+ * array's device address, so make the first call on each device before any
+ * stream capture. All calls share the one array: calls that may overlap on the
+ * GPU (other streams, other host threads) race, so serialize them. Nothing in
+ * the array needs clearing between calls. Otherwise identical to
+ * qm_apply_experts; the pages have no counterpart to this entry point. */
+qm_status qm_apply_experts_static(const qm_weight* w, const void* ids, int32_t id_type, int64_t T,
+                                  int64_t topk, const void* x, int64_t x_rows, int32_t x_dtype,
+                                  void* y, qm_stream_t stream);
+
 /* The routing step of qm_apply_experts on its own: for P flattened ids and E
  * experts, counts[E] (positions per expert), offsets[E+1] (exclusive prefix
  * sum; offsets[E] = positions in range) and perm[P]: first the in-range

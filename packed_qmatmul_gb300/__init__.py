@@ -23,7 +23,7 @@ __all__ = [
     "QM_AFFINE", "QM_Q8_0", "QM_MXFP4", "QM_F32", "QM_BF16", "QM_F16", "QM_I32", "QM_I64",
     "QMError", "QWeight", "library_path", "load_library",
     "qm_dequant", "qm_apply", "qm_take", "qm_apply_experts", "qm_apply_experts_workspace",
-    "qm_experts_route", "qm_device_status", "qm_last_error", "qm_version",
+    "qm_experts_route", "qm_apply_experts_static", "qm_device_status", "qm_last_error", "qm_version",
     "dequant", "apply", "take", "apply_experts", "route",
 ]
 
@@ -83,6 +83,7 @@ def load_library():
             "qm_apply_experts_workspace": ([i64, i64, i64], sz),
             "qm_apply_experts": ([wp, vp, i32, i64, i64, vp, i64, i32, vp, vp, sz, vp], i32),
             "qm_experts_route": ([vp, i32, i64, i64, vp, vp, vp, vp, sz, vp], i32),
+            "qm_apply_experts_static": ([wp, vp, i32, i64, i64, vp, i64, i32, vp, vp], i32),
             "qm_device_status": ([vp], i32),
             "qm_last_error": ([], ctypes.c_char_p),
             "qm_version": ([], i32),
@@ -214,6 +215,16 @@ def qm_apply_experts(w: QWeight, ids: torch.Tensor, x: torch.Tensor, y: torch.Te
     _check(load_library().qm_apply_experts(
         ctypes.byref(w._c()), _ptr(ids), id_type, T, topk, _ptr(x), x.shape[0], _DTYPES[x.dtype],
         _ptr(y), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def qm_apply_experts_static(w: QWeight, ids: torch.Tensor, x: torch.Tensor, y: torch.Tensor,
+                            stream=None) -> None:
+    """qm_apply_experts with the library's own 1 MiB routing scratch (no workspace)."""
+    T, topk = ids.shape
+    id_type = QM_I64 if ids.dtype == torch.int64 else QM_I32
+    _check(load_library().qm_apply_experts_static(
+        ctypes.byref(w._c()), _ptr(ids), id_type, T, topk, _ptr(x), x.shape[0], _DTYPES[x.dtype],
+        _ptr(y), _stream(stream)))
 
 
 def qm_experts_route(ids: torch.Tensor, E: int, counts: torch.Tensor, offsets: torch.Tensor,

@@ -10,6 +10,8 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <mutex>
+#include <string>
 
 #include "qm_device.cuh"
 #include "qm_internal.h"
@@ -272,3 +274,56 @@ qm_status launch_experts(const WDesc& w, const void* ids, int id64, int64_t T, i
 }
 
 }  // namespace qm
+
+// ---------------------------------------------------------------- allocation-free variant
+// qm_apply_experts_static: the same work as qm_apply_experts, with its routing
+// tables kept in this file-scope device array instead of caller workspace.
+// Every GPU that loads the library holds the array until the process exits.
+namespace qm {
+
+constexpr size_t kStaticScratchBytes = size_t(1) << 20;  // 1 MiB
+static __device__ __align__(256) unsigned char g_experts_scratch[kStaticScratchBytes];
+
+// The array's device address on the current device, looked up once per
+// device (host code only sees a host-side stand-in for the symbol).
+static cudaError_t static_scratch(void** out) {
+    static std::mutex mu;
+    static void* ptr[64] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!ptr[dev]) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_experts_scratch);
+        if (e != cudaSuccess) return e;
+        ptr[dev] = p;
+    }
+    *out = ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace qm
+
+extern "C" qm_status qm_apply_experts_static(const qm_weight* w, const void* ids, int32_t id_type,
+                                             int64_t T, int64_t topk, const void* x, int64_t x_rows,
+                                             int32_t x_dtype, void* y, qm_stream_t stream) {
+    using namespace qm;
+    set_error("");
+    if (w && w->ndim == 3 && T > 0 && topk > 0 && w->shape[0] >= 0) {
+        const size_t need = experts_workspace_bytes(T * topk, w->shape[0]);
+        if (need > kStaticScratchBytes)
+            return fail(QM_EINVAL, "workspace: " + std::to_string(T * topk) + " positions over " +
+                                       std::to_string(w->shape[0]) + " experts need " + std::to_string(need) +
+                                       " bytes of routing scratch, more than the 1 MiB this entry point "
+                                       "holds; use qm_apply_experts with caller workspace");
+    }
+    void* scratch = nullptr;
+    cudaError_t e = static_scratch(&scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "static scratch address");
+    // Every entry of the routing tables is written before it is read, so the
+    // array needs no clearing between calls.
+    return qm_apply_experts(w, ids, id_type, T, topk, x, x_rows, x_dtype, y, scratch, kStaticScratchBytes,
+                            stream);
+}
