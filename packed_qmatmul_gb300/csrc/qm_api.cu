@@ -170,14 +170,16 @@ static EncodeTiledFn encode_tiled() {
 }
 
 bool make_tmap_2d(void* map, const void* base, uint64_t inner_bytes, uint64_t rows, uint64_t row_stride,
-                  uint32_t box_inner, uint32_t box_rows, bool swizzle128) {
+                  uint32_t box_inner, uint32_t box_rows, bool swizzle128, int elem_bytes) {
     EncodeTiledFn f = encode_tiled();
     if (!f) return false;
-    const cuuint64_t dims[2] = {inner_bytes, rows};
+    if (elem_bytes != 1 && elem_bytes != 2) return false;
+    const cuuint64_t dims[2] = {inner_bytes / elem_bytes, rows};
     const cuuint64_t strides[1] = {row_stride};
-    const cuuint32_t box[2] = {box_inner, box_rows};
+    const cuuint32_t box[2] = {box_inner / static_cast<uint32_t>(elem_bytes), box_rows};
     const cuuint32_t estr[2] = {1, 1};
-    CUresult r = f(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+    const CUtensorMapDataType dt = elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    CUresult r = f(static_cast<CUtensorMap*>(map), dt, 2, const_cast<void*>(base), dims,
                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);

@@ -1,5 +1,30 @@
-// qm_gemm.cu -- tensor-core product for M > 16 (tcgen05, TMEM, TMA).
+// qm_gemm.cu -- prefill product y[M, n] = x[M, k] * W^T for M >= 17 on the
+// 5th-generation tensor cores (tcgen05), decoding the packed weight in the
+// pipeline.
+//
+// The product is "Nx_quant (raven-ml.dev API docs)", section "Products", val
+// apply: summed at float32, rounded once to x's dtype. Here each weight value
+// (the float32 value of "Weights" / "Products", dequant) is rounded to bf16 to
+// enter a kind::f16 MMA; the sums are float32 in TMEM. The rounding of the
+// weights stays inside the product's error bound (a relative 2^-9 per value).
+//
+// One CTA per 128 x 128 output tile (tokens x weight rows):
+//  * warp 0, one lane: TMA producer. Activation tiles (128 tokens x 64 k,
+//    bf16, 128B-swizzled: the canonical K-major layout the MMA reads) and raw
+//    packed chunks of the weight tile (128 rows x 256 or 128 k values).
+//  * warps 2..9: decoders. Each thread turns half of one weight row's 64
+//    values per k step into bf16 and writes them, 128B-swizzled, into the
+//    B tile; scales are fetched from global memory one chunk ahead. After
+//    the k loop they read the accumulator out of TMEM and store y.
+//  * warp 1, one lane: issues tcgen05.mma (M = 128, N = 128, K = 16, four per
+//    k step) into a 128-column TMEM accumulator and commits each stage back
+//    to its producers through mbarriers.
+// Every wait is bounded; a wait that gives up raises the device flag and the
+// CTA winds down with its copies and MMAs drained.
+#include <cuda.h>
 #include <cuda_runtime.h>
+
+#include <algorithm>
 
 #include "qm_device.cuh"
 #include "qm_internal.h"
@@ -15,10 +40,384 @@ uint32_t gemm_read_clear_error() {
     return v;
 }
 
-bool gemm_supported(const WDesc&, int64_t) { return false; }
+namespace gemm {
 
-qm_status launch_gemm(const WDesc&, const void*, int64_t, void*, cudaStream_t) {
-    return fail(QM_ENOTSUP, "w: tensor-core path not available");
+constexpr int BM = 128, BN = 128, BK = 64;
+constexpr int kDecWarps = 8;
+constexpr int kThreads = 64 + kDecWarps * 32;
+constexpr int NX = 4, NB = 3, NR = 2;  // ring depths: activation tiles, bf16 B tiles, raw chunks
+constexpr uint32_t kTileBytes = BM * BK * 2;  // 16 KB (x tile, and B tile with BN = 128)
+constexpr uint32_t kTmemCols = BN;
+
+// Raw chunk geometry per format: values per chunk, bytes per row per chunk,
+// whether the TMA box is 128B-swizzled, and the tensor map's element size.
+template <int FMT, int BITS>
+struct Raw {
+    static constexpr int RAWK = (FMT == QM_AFFINE && BITS == 8) ? 128 : 256;
+    static constexpr int BYTES = (FMT == QM_Q8_0) ? 272 : 128;
+    static constexpr bool SW = FMT != QM_Q8_0;
+    static constexpr int ELEM = (FMT == QM_Q8_0) ? 2 : 1;
+    static constexpr int SPR = RAWK / BK;  // k steps per chunk
+};
+
+struct Params {
+    CUtensorMap tm_x;    // x as bytes [M, 2k], boxes of 128 B x 128 rows, 128B-swizzled
+    CUtensorMap tm_raw;  // codes as [n, code_row_bytes], boxes of Raw::BYTES x 128 rows
+    const uint8_t* scales;
+    const uint8_t* biases;
+    uint16_t* y;
+    int64_t M, n, k;
+    int64_t scale_row_bytes;
+    int sdt;
+    int ksteps, mtiles;
+    uint32_t off_x, off_b, off_raw, raw_stage_bytes;
+};
+
+// Where 16-byte chunk c of row r of a 128B-swizzled, 128-byte-row tile sits.
+QM_DEV uint32_t sw128(uint32_t r, uint32_t c) { return r * 128 + ((c ^ (r & 7)) << 4); }
+
+QM_DEV float sval(uint32_t h, int sdt) { return sdt == QM_F16 ? f16_bits_to_f32(h) : bf16_bits_to_f32(h); }
+
+QM_DEV float code_f(uint32_t c) { return __uint_as_float(c | 0x4B000000u) - 8388608.0f; }  // exact for c < 2^23
+
+QM_DEV uint32_t bf2(float lo, float hi) {
+    __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&t);
+}
+
+// The scale (and bias) one decoder thread needs for k step kk of a chunk.
+struct Sc {
+    float s, b;
+};
+
+template <int FMT, int BITS, int GS>
+QM_DEV Sc load_scale(const Params& p, int64_t grow, int64_t vidx) {
+    Sc r{0.0f, 0.0f};
+    if (vidx >= p.k) return r;
+    if constexpr (FMT == QM_AFFINE) {
+        const int64_t ng = p.k / GS;
+        const int64_t g = vidx / GS;
+        const uint16_t* sc = reinterpret_cast<const uint16_t*>(p.scales) + grow * ng + g;
+        const uint16_t* bi = reinterpret_cast<const uint16_t*>(p.biases) + grow * ng + g;
+        r.s = sval(__ldg(sc), p.sdt);
+        r.b = sval(__ldg(bi), p.sdt);
+    } else if constexpr (FMT == QM_MXFP4) {
+        r.s = e8m0_to_f32(__ldg(p.scales + grow * p.scale_row_bytes + vidx / 32));
+    }
+    return r;
+}
+
+// 32 float32 values of one decoder thread's half row (values kk*64 + half*32 ..
+// of the chunk) from the raw chunk in shared memory.
+template <int FMT, int BITS, int GS>
+QM_DEV void decode32(const uint8_t* raw, int row, int kk, int half, Sc sc, float (&v)[32]) {
+    if constexpr (FMT == QM_AFFINE && BITS == 4) {
+        const uint32_t q = kk * 2 + half;
+        const uint4 w = *reinterpret_cast<const uint4*>(raw + sw128(row, q));
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) v[8 * j + i] = fmaf(code_f((ws[j] >> (4 * i)) & 15u), sc.s, sc.b);
+    } else if constexpr (FMT == QM_AFFINE && BITS == 8) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t q = kk * 4 + half * 2 + h;
+            const uint4 w = *reinterpret_cast<const uint4*>(raw + sw128(row, q));
+            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    v[16 * h + 4 * j + i] = fmaf(code_f((ws[j] >> (8 * i)) & 255u), sc.s, sc.b);
+        }
+    } else if constexpr (FMT == QM_MXFP4) {
+        const uint32_t q = kk * 2 + half;
+        const uint4 w = *reinterpret_cast<const uint4*>(raw + sw128(row, q));
+        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            uint32_t h2[4];
+            e2m1x8_to_f16x2(ws[j], h2);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2[i]));
+                v[8 * j + 2 * i] = f.x * sc.s;
+                v[8 * j + 2 * i + 1] = f.y * sc.s;
+            }
+        }
+    } else {  // Q8_0: block kk*2 + half of the chunk, 34 bytes, rows 272 bytes apart
+        const uint16_t* blk = reinterpret_cast<const uint16_t*>(raw + row * 272 + (kk * 2 + half) * 34);
+        const float d = f16_bits_to_f32(blk[0]);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const uint32_t two = blk[1 + i];
+            v[2 * i] = d * static_cast<float>(static_cast<int8_t>(two & 0xFF));
+            v[2 * i + 1] = d * static_cast<float>(static_cast<int8_t>(two >> 8));
+        }
+    }
+}
+
+template <int FMT, int BITS, int GS>
+__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ Params p) {
+    using R = Raw<FMT, BITS>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int mt = blockIdx.x % p.mtiles, nt = blockIdx.x / p.mtiles;
+    const int64_t m0 = static_cast<int64_t>(mt) * BM, n0 = static_cast<int64_t>(nt) * BN;
+    const int ks_n = p.ksteps;
+    const int nchunks = (ks_n + R::SPR - 1) / R::SPR;
+
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+    const uint32_t b0 = smem_u32(bars);
+    auto x_full = [&](int i) { return b0 + 8 * i; };
+    auto x_empty = [&](int i) { return b0 + 8 * (NX + i); };
+    auto b_full = [&](int i) { return b0 + 8 * (2 * NX + i); };
+    auto b_empty = [&](int i) { return b0 + 8 * (2 * NX + NB + i); };
+    auto r_full = [&](int i) { return b0 + 8 * (2 * NX + 2 * NB + i); };
+    auto r_empty = [&](int i) { return b0 + 8 * (2 * NX + 2 * NB + NR + i); };
+    const uint32_t done = b0 + 8 * (2 * NX + 2 * NB + 2 * NR);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 8 * (2 * NX + 2 * NB + 2 * NR + 1));
+    volatile int& s_abort = *reinterpret_cast<volatile int*>(smem + 8 * (2 * NX + 2 * NB + 2 * NR + 2));
+
+    if (threadIdx.x == 0) {
+        s_abort = 0;
+        for (int i = 0; i < NX; ++i) { mbar_init(x_full(i), 1); mbar_init(x_empty(i), 1); }
+        for (int i = 0; i < NB; ++i) { mbar_init(b_full(i), kDecWarps); mbar_init(b_empty(i), 1); }
+        for (int i = 0; i < NR; ++i) { mbar_init(r_full(i), 1); mbar_init(r_empty(i), kDecWarps); }
+        mbar_init(done, 1);
+        fence_mbar_init();
+        prefetch_tmap(&p.tm_x);
+        prefetch_tmap(&p.tm_raw);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    grid_launch_dependents();
+    grid_dependency_wait();
+
+    auto give_up = [&]() {
+        atomicOr(&g_err_gemm, DEV_ERR_TIMEOUT);
+        s_abort = 1;
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        if (lane == 0) {
+            int last_x = -1, last_r = -1;
+            for (int ks = 0; ks < ks_n && !s_abort; ++ks) {
+                if (ks % R::SPR == 0) {
+                    const int rc = ks / R::SPR, sr = rc % NR;
+                    if (!mbar_wait(r_empty(sr), ((rc / NR) & 1) ^ 1)) { give_up(); break; }
+                    mbar_expect_tx(r_full(sr), R::BYTES * BN);
+                    tma_load_2d(smem_u32(smem + p.off_raw + sr * p.raw_stage_bytes), &p.tm_raw,
+                                rc * R::BYTES / R::ELEM, static_cast<int32_t>(n0), r_full(sr));
+                    mbar_arrive(r_full(sr));
+                    last_r = rc;
+                }
+                const int sx = ks % NX;
+                if (!mbar_wait(x_empty(sx), ((ks / NX) & 1) ^ 1)) { give_up(); break; }
+                mbar_expect_tx(x_full(sx), kTileBytes);
+                tma_load_2d(smem_u32(smem + p.off_x + sx * kTileBytes), &p.tm_x, ks * 128, static_cast<int32_t>(m0),
+                            x_full(sx));
+                mbar_arrive(x_full(sx));
+                last_x = ks;
+            }
+            if (s_abort) {  // let issued copies land before the CTA winds down
+                for (int ks = std::max(0, last_x - NX + 1); ks <= last_x; ++ks)
+                    (void)mbar_wait(x_full(ks % NX), (ks / NX) & 1);
+                for (int rc = std::max(0, last_r - NR + 1); rc <= last_r; ++rc)
+                    (void)mbar_wait(r_full(rc % NR), (rc / NR) & 1);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = umma_idesc_bf16(BM, BN);
+            for (int ks = 0; ks < ks_n && !s_abort; ++ks) {
+                const int sx = ks % NX, sb = ks % NB;
+                if (!mbar_wait(x_full(sx), (ks / NX) & 1) || !mbar_wait(b_full(sb), (ks / NB) & 1)) {
+                    give_up();
+                    break;
+                }
+                tc_fence_after();
+                const uint64_t ad = umma_desc_sw128(smem_u32(smem + p.off_x + sx * kTileBytes));
+                const uint64_t bd = umma_desc_sw128(smem_u32(smem + p.off_b + sb * kTileBytes));
+#pragma unroll
+                for (int kk = 0; kk < BK / 16; ++kk)  // advance 16 values = 32 bytes inside the swizzle atom
+                    umma_f16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, ks > 0 || kk > 0);
+                umma_commit(x_empty(sx));
+                umma_commit(b_empty(sb));
+            }
+            umma_commit(done);  // also drains whatever was issued when abandoning
+        }
+    } else {
+        // ------------------------------------------------------------ decoders
+        const int d = threadIdx.x - 64;
+        const int row = d >> 1, half = d & 1;
+        const int64_t grow = n0 + row;
+        const bool rowok = grow < p.n;
+        Sc cur[R::SPR], nxt[R::SPR];
+        auto fetch = [&](int rc, Sc (&dst)[R::SPR]) {
+#pragma unroll
+            for (int kk = 0; kk < R::SPR; ++kk)
+                dst[kk] = rowok ? load_scale<FMT, BITS, GS>(p, grow, static_cast<int64_t>(rc) * R::RAWK + kk * BK + half * 32)
+                                : Sc{0.0f, 0.0f};
+        };
+        fetch(0, cur);
+        for (int rc = 0; rc < nchunks; ++rc) {
+            if (rc + 1 < nchunks) fetch(rc + 1, nxt);
+            const int sr = rc % NR;
+            bool live = !s_abort && mbar_wait(r_full(sr), (rc / NR) & 1);
+            const uint8_t* raw = smem + p.off_raw + sr * p.raw_stage_bytes;
+#pragma unroll
+            for (int kk = 0; kk < R::SPR; ++kk) {
+                const int ks = rc * R::SPR + kk;
+                if (ks >= ks_n) break;
+                const int sb = ks % NB;
+                if (live && !mbar_wait(b_empty(sb), ((ks / NB) & 1) ^ 1)) live = false;
+                if (!live) {
+                    if (lane == 0) give_up();
+                    break;
+                }
+                const int64_t vidx = static_cast<int64_t>(ks) * BK + half * 32;
+                float v[32];
+                if (rowok && vidx < p.k) {
+                    decode32<FMT, BITS, GS>(raw, row, kk, half, cur[kk], v);
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+                }
+                uint8_t* bt = smem + p.off_b + sb * kTileBytes;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const uint4 q = make_uint4(bf2(v[8 * j], v[8 * j + 1]), bf2(v[8 * j + 2], v[8 * j + 3]),
+                                               bf2(v[8 * j + 4], v[8 * j + 5]), bf2(v[8 * j + 6], v[8 * j + 7]));
+                    *reinterpret_cast<uint4*>(bt + sw128(row, half * 4 + j)) = q;
+                }
+                fence_proxy_async_smem();  // the tensor cores read B through the async proxy
+                __syncwarp();
+                if (lane == 0) mbar_arrive(b_full(sb));
+            }
+            __syncwarp();
+            if (lane == 0 && live) mbar_arrive(r_empty(sr));
+            if (!live) break;
+#pragma unroll
+            for (int kk = 0; kk < R::SPR; ++kk) cur[kk] = nxt[kk];
+        }
+        // ------------------------------------------------------------ epilogue
+        const bool ok = mbar_wait(done, 0);
+        if (!ok && lane == 0) give_up();
+        tc_fence_after();
+        const int quarter = warp & 3, colhalf = (warp - 2) >> 2;
+        const int64_t m = m0 + 32 * quarter + lane;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int c0 = 64 * colhalf + 32 * j;
+            uint32_t r[32];
+            tmem_ld32(tmem + (static_cast<uint32_t>(32 * quarter) << 16) + c0, r);
+            tmem_wait_ld();
+            if (!ok || s_abort || m >= p.M) continue;
+            uint16_t* yr = p.y + m * p.n + n0 + c0;
+            const int64_t left = p.n - (n0 + c0);
+            if (left >= 32 && (p.n & 7) == 0) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    *reinterpret_cast<uint4*>(yr + 8 * q) =
+                        make_uint4(bf2(__uint_as_float(r[8 * q]), __uint_as_float(r[8 * q + 1])),
+                                   bf2(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3])),
+                                   bf2(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5])),
+                                   bf2(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7])));
+            } else {
+#pragma unroll
+                for (int c = 0; c < 32; ++c) {
+                    if (c < left) {
+                        __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(r[c]));
+                        yr[c] = *reinterpret_cast<uint16_t*>(&b);
+                    }
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+template <int FMT, int BITS, int GS>
+static cudaError_t launch_t(Params& p, const WDesc& w, cudaStream_t st) {
+    using R = Raw<FMT, BITS>;
+    p.off_x = 1024;
+    p.off_b = p.off_x + NX * kTileBytes;
+    p.off_raw = p.off_b + NB * kTileBytes;
+    p.raw_stage_bytes = (R::BYTES * BN + 1023) / 1024 * 1024;
+    const size_t smem = p.off_raw + NR * p.raw_stage_bytes;
+    if (!make_tmap_2d(&p.tm_raw, w.codes, w.code_row_bytes, w.n, w.code_row_bytes, R::BYTES, BN, R::SW, R::ELEM))
+        return cudaErrorNotSupported;
+    auto kern = gemm_kernel<FMT, BITS, GS>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const int64_t ntiles = (w.n + BN - 1) / BN;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(p.mtiles * ntiles));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+}  // namespace gemm
+
+bool gemm_supported(const WDesc& w, int64_t M) {
+    if (M < 1 || w.ndim != 2 || w.n < 1 || w.k < 64) return false;
+    if (w.code_row_bytes % 16) return false;  // TMA row stride
+    if ((w.n + gemm::BN - 1) / gemm::BN * ((M + gemm::BM - 1) / gemm::BM) > 0x7FFFFFFF) return false;
+    return true;
+}
+
+qm_status launch_gemm(const WDesc& w, const void* x, int64_t M, void* y, cudaStream_t st) {
+    using namespace gemm;
+    Params p{};
+    p.scales = w.scales;
+    p.biases = w.biases;
+    p.y = static_cast<uint16_t*>(y);
+    p.M = M;
+    p.n = w.n;
+    p.k = w.k;
+    p.scale_row_bytes = w.scale_row_bytes;
+    p.sdt = w.sdt;
+    p.ksteps = static_cast<int>((w.k + BK - 1) / BK);
+    p.mtiles = static_cast<int>((M + BM - 1) / BM);
+    if (!make_tmap_2d(&p.tm_x, x, static_cast<uint64_t>(w.k) * 2, M, static_cast<uint64_t>(w.k) * 2, 128, BM, true))
+        return fail(QM_ENOTSUP, "x: no TMA descriptor for this shape");
+    cudaError_t e = cudaErrorInvalidValue;
+    if (w.fmt == QM_AFFINE && w.bits == 4 && w.gs == 32) e = launch_t<QM_AFFINE, 4, 32>(p, w, st);
+    else if (w.fmt == QM_AFFINE && w.bits == 4 && w.gs == 64) e = launch_t<QM_AFFINE, 4, 64>(p, w, st);
+    else if (w.fmt == QM_AFFINE && w.bits == 4 && w.gs == 128) e = launch_t<QM_AFFINE, 4, 128>(p, w, st);
+    else if (w.fmt == QM_AFFINE && w.bits == 8 && w.gs == 32) e = launch_t<QM_AFFINE, 8, 32>(p, w, st);
+    else if (w.fmt == QM_AFFINE && w.bits == 8 && w.gs == 64) e = launch_t<QM_AFFINE, 8, 64>(p, w, st);
+    else if (w.fmt == QM_AFFINE && w.bits == 8 && w.gs == 128) e = launch_t<QM_AFFINE, 8, 128>(p, w, st);
+    else if (w.fmt == QM_Q8_0) e = launch_t<QM_Q8_0, 8, 32>(p, w, st);
+    else if (w.fmt == QM_MXFP4) e = launch_t<QM_MXFP4, 4, 32>(p, w, st);
+    if (e == cudaErrorNotSupported) {  // no descriptor for the weight: the plain kernel
+        e = launch_apply_simple(w, x, M, y, st);
+        return e == cudaSuccess ? QM_OK : cuda_fail(e, "apply launch");
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
+    return QM_OK;
 }
 
 }  // namespace qm

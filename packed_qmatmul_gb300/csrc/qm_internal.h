@@ -43,7 +43,8 @@ int dtype_size(int dt);
 // box is `box_inner` bytes by `box_rows` rows, 128-byte swizzled if asked,
 // out-of-range elements read as zeros. Returns false if the driver refuses.
 bool make_tmap_2d(void* map, const void* base, uint64_t inner_bytes, uint64_t rows,
-                  uint64_t row_stride, uint32_t box_inner, uint32_t box_rows, bool swizzle128);
+                  uint64_t row_stride, uint32_t box_inner, uint32_t box_rows, bool swizzle128,
+                  int elem_bytes = 1);
 
 // Number of SMs on the current device (cached per device).
 int num_sms();

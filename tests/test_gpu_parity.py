@@ -288,3 +288,35 @@ def test_apply_lm_head_shape_sampled():
     wn = np.array([np.linalg.norm(oracle.row_values(ow, int(r)).astype(np.float64)) for r in j])
     xn = np.linalg.norm(oracle.decode_array(x, oracle.BF16), axis=1)
     check_product(y[j][None], ref[None], wn, xn, 1024, "lm_head sampled")
+
+
+# ---------------------------------------------------------------- prefill (tensor cores)
+@pytest.mark.parametrize("kind", KINDS)
+def test_apply_prefill(kind):
+    # several 128 x 128 tiles along both axes, ragged M and n, k not a multiple of 256
+    g = synth.rng(1200)
+    for n, k, M in ((200, 512, 130), (256, 1024, 64), (130, 320, 257)):
+        if kind == "q8_0" and k % 256:
+            k = 512  # Q8_0 rows must be 16-byte multiples for the TMA path
+        w = _make(kind, g, n, k)
+        x = synth.activations(g, M, k)
+        _check_apply(w, x, f"{kind} prefill n={n} k={k} M={M}")
+
+
+def test_apply_prefill_q8_0_full_shape_sampled():
+    # Q8_0 4096 x 4096 at M = 2048, checked on sampled outputs
+    g = synth.rng(1201)
+    w = synth.q8_0_weight(g, 4096, 4096)
+    x = synth.activations(g, 2048, 4096)
+    ow = to_oracle(w)
+    y = bf16_to_f64(_host(qm.apply(qm.QWeight.from_arrays(w), _dev_bf16(x))))
+    m_idx = np.concatenate([g.integers(0, 2048, 1500), [0, 2047, 127, 128]])
+    j_idx = np.concatenate([g.integers(0, 4096, 1500), [0, 4095, 128, 127]])
+    ref = oracle.apply_entries(ow, x, m_idx, j_idx)
+    wn = np.array([np.linalg.norm(oracle.row_values(ow, int(r)).astype(np.float64)) for r in j_idx])
+    xn = np.linalg.norm(oracle.decode_array(x[m_idx], oracle.BF16), axis=1)
+    got = y[m_idx, j_idx]
+    bound = 1e-2 * xn * wn / np.sqrt(4096)
+    from wutil import bf16_half_ulp
+    assert np.all(np.abs(got - ref) <= bound + bf16_half_ulp(got)), np.max(np.abs(got - ref) / bound)
+    assert np.linalg.norm(got - ref) <= 4e-3 * np.linalg.norm(ref)
