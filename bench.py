@@ -46,8 +46,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="decode", choices=["decode", "prefill"],
+                    help="decode: the headline M=1 step; prefill: Q8_0 products at M >= 128")
     ap.add_argument("--bits", type=int, default=4)
-    ap.add_argument("--M", type=int, default=1)
+    ap.add_argument("--M", type=int, default=None)
     ap.add_argument("--no-detail", action="store_true", help="skip the secondary measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
     ap.add_argument("--only", default=None,
@@ -187,6 +189,68 @@ def time_graph(step, stream, steps, warmup, clock_index=None):
     return ev0.elapsed_time(ev1) / 1e3, (clk.summary() if clk else None)
 
 
+PREFILL_METRIC = "TFLOP/s (M>=128 qmatmul)"
+
+
+def run_prefill(args, rank, world):
+    """GGUF Q8_0 products 4096x4096, 14336x4096 and 4096x14336 at M tokens
+    (2048 by default): one step = the three qm_apply calls, graph-captured."""
+    import torch
+
+    import packed_qmatmul_gb300 as qm
+    from packed_qmatmul_gb300 import build as qbuild
+
+    qbuild.build()
+    qm.load_library()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    M = args.M or 2048
+    g = synth.rng(2)
+    items = []
+    for n, k in synth.Q8_0_SHAPES:
+        if args.only and f"{n}x{k}" != args.only:
+            continue
+        qw = qm.QWeight.from_arrays(synth.q8_0_weight(g, n, k), dev)
+        x = torch.from_numpy(synth.activations(g, M, k).view(np.int16)).to(dev).view(torch.bfloat16)
+        y = torch.empty((M, n), dtype=torch.bfloat16, device=dev)
+        items.append((n, k, qw, x, y))
+    flops = sum(2.0 * M * n * k for n, k, *_ in items)
+    wbytes = sum(n * (k // 32) * 34 for n, k, *_ in items)
+    stream = torch.cuda.Stream()
+
+    def step():
+        for _, _, qw, x, y in items:
+            qm.qm_apply(qw, x, y, stream)
+
+    elapsed, clocks = time_graph(step, stream, args.steps, args.warmup, dev.index)
+    qm.qm_device_status(stream)
+    if world > 1:
+        import torch.distributed as tdist
+        t = torch.tensor([elapsed], device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        elapsed = float(t.item())
+    tflops = flops * args.steps * world / elapsed / 1e12
+    achieved = flops * args.steps / elapsed / 1e12
+    peaks = load_peaks()
+    peak = peaks.get("bf16_tflops", 1900.0)
+    return {
+        "metric": PREFILL_METRIC, "value": round(tflops, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(elapsed / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16xbf16->f32",
+        "data": "synthetic (seeded)",
+        "config": {"workload": f"GGUF Q8_0 qmatmul, W 4096x4096, 14336x4096, 4096x14336, M={M}"
+                               + (f" (only {args.only})" if args.only else ""),
+                   "M": M, "weight_bytes_per_step": wbytes, "flops_per_step": flops,
+                   "l2": "weights 143 MB per step, more than L2"},
+        "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "kernel": "gemm_kernel<Q8_0> (every launch of the step)",
+                     "peak_source": "measured bf16 dense, burst" if "bf16_tflops" in peaks else "fallback"},
+        "gpu_launches": len(items) * args.steps,
+        "clocks": clocks,
+    }
+
+
 def run_ours(args, rank, world):
     import torch
 
@@ -197,7 +261,7 @@ def run_ours(args, rank, world):
     qm.load_library()
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    bits, M = args.bits, args.M
+    bits, M = args.bits, (args.M or 1)
     items = build_step(bits, M, dev, args.only)
     step_bytes = sum(packed_bytes(n, k, bits) for _, n, k, *_ in items)
     algo_bytes = step_bytes + sum(2 * M * (n + k) for _, n, k, *_ in items)
@@ -387,6 +451,14 @@ def main():
     if world > 1:
         import torch.distributed as tdist
         tdist.init_process_group("nccl")
+    if args.workload == "prefill":
+        res = run_prefill(args, rank, world)
+        if rank == 0:
+            print(json.dumps(res))
+        if world > 1:
+            import torch.distributed as tdist
+            tdist.destroy_process_group()
+        return
     res = run_ours(args, rank, world)
     if rank == 0 and not args.no_cpu:
         res["cpu_baseline"] = cpu_baseline(args.bits)
