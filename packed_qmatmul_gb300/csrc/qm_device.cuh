@@ -241,6 +241,36 @@ QM_DEV void e2m1x8_to_f16x2(uint32_t w, uint32_t (&d)[4]) {
         : "r"(w));
 }
 
+// Packed float32 pairs (Blackwell f32x2 ALU ops): one instruction, two lanes.
+QM_DEV float2 add2(float2 a, float2 b) {
+    uint64_t d, x, y;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b.x), "f"(b.y));
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(x), "l"(y));
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
+    return r;
+}
+QM_DEV float2 mul2(float2 a, float2 b) {
+    uint64_t d, x, y;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b.x), "f"(b.y));
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(x), "l"(y));
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
+    return r;
+}
+QM_DEV float2 fma2(float2 a, float2 b, float2 c) {
+    uint64_t d, x, y, z;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a.x), "f"(a.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(b.x), "f"(b.y));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(z) : "f"(c.x), "f"(c.y));
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(x), "l"(y), "l"(z));
+    float2 r;
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
+    return r;
+}
+
 QM_DEV float bf16_bits_to_f32(uint32_t h) { return __uint_as_float(h << 16); }
 
 QM_DEV float f16_bits_to_f32(uint32_t h) {

@@ -42,12 +42,12 @@ uint32_t gemm_read_clear_error() {
 
 namespace gemm {
 
-constexpr int BM = 128, BN = 128, BK = 64;
+constexpr int BN = 128, BK = 64;
 constexpr int kDecWarps = 8;
 constexpr int kThreads = 64 + kDecWarps * 32;
-constexpr int NX = 4, NB = 3, NR = 2;  // ring depths: activation tiles, bf16 B tiles, raw chunks
-constexpr uint32_t kTileBytes = BM * BK * 2;  // 16 KB (x tile, and B tile with BN = 128)
-constexpr uint32_t kTmemCols = BN;
+constexpr int NB = 3, NR = 2;  // ring depths: bf16 B tiles, raw chunks
+constexpr uint32_t kBTileBytes = BN * BK * 2;  // 16 KB
+constexpr int NXof(int BM) { return BM == 256 ? 3 : 4; }  // activation tiles in flight
 
 // Raw chunk geometry per format: values per chunk, bytes per row per chunk,
 // whether the TMA box is 128B-swizzled, and the tensor map's element size.
@@ -61,7 +61,7 @@ struct Raw {
 };
 
 struct Params {
-    CUtensorMap tm_x;    // x as bytes [M, 2k], boxes of 128 B x 128 rows, 128B-swizzled
+    CUtensorMap tm_x;    // x as bytes [M, 2k], boxes of 128 B x BM rows, 128B-swizzled
     CUtensorMap tm_raw;  // codes as [n, code_row_bytes], boxes of Raw::BYTES x 128 rows
     const uint8_t* scales;
     const uint8_t* biases;
@@ -78,14 +78,15 @@ QM_DEV uint32_t sw128(uint32_t r, uint32_t c) { return r * 128 + ((c ^ (r & 7)) 
 
 QM_DEV float sval(uint32_t h, int sdt) { return sdt == QM_F16 ? f16_bits_to_f32(h) : bf16_bits_to_f32(h); }
 
-QM_DEV float code_f(uint32_t c) { return __uint_as_float(c | 0x4B000000u) - 8388608.0f; }  // exact for c < 2^23
-
 QM_DEV uint32_t bf2(float lo, float hi) {
     __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t*>(&t);
 }
 
-// The scale (and bias) one decoder thread needs for k step kk of a chunk.
+// 2^23 + u as a float32, for u < 2^23 already placed in the low bits.
+QM_DEV float magic_f(uint32_t bits_or_u) { return __uint_as_float(bits_or_u | 0x4B000000u); }
+
+// The scale (and bias) one decoder thread needs for one k step.
 struct Sc {
     float s, b;
 };
@@ -97,70 +98,89 @@ QM_DEV Sc load_scale(const Params& p, int64_t grow, int64_t vidx) {
     if constexpr (FMT == QM_AFFINE) {
         const int64_t ng = p.k / GS;
         const int64_t g = vidx / GS;
-        const uint16_t* sc = reinterpret_cast<const uint16_t*>(p.scales) + grow * ng + g;
-        const uint16_t* bi = reinterpret_cast<const uint16_t*>(p.biases) + grow * ng + g;
-        r.s = sval(__ldg(sc), p.sdt);
-        r.b = sval(__ldg(bi), p.sdt);
+        r.s = sval(__ldg(reinterpret_cast<const uint16_t*>(p.scales) + grow * ng + g), p.sdt);
+        r.b = sval(__ldg(reinterpret_cast<const uint16_t*>(p.biases) + grow * ng + g), p.sdt);
     } else if constexpr (FMT == QM_MXFP4) {
         r.s = e8m0_to_f32(__ldg(p.scales + grow * p.scale_row_bytes + vidx / 32));
     }
     return r;
 }
 
-// 32 float32 values of one decoder thread's half row (values kk*64 + half*32 ..
-// of the chunk) from the raw chunk in shared memory.
+// The 32 values of one decoder thread's half row (values kk*64 + half*32 .. of
+// the chunk) as 16 bf16 pairs, from the raw chunk in shared memory.
 template <int FMT, int BITS, int GS>
-QM_DEV void decode32(const uint8_t* raw, int row, int kk, int half, Sc sc, float (&v)[32]) {
-    if constexpr (FMT == QM_AFFINE && BITS == 4) {
-        const uint32_t q = kk * 2 + half;
-        const uint4 w = *reinterpret_cast<const uint4*>(raw + sw128(row, q));
-        const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+QM_DEV void decode32(const uint8_t* raw, int row, int kk, int half, Sc sc, uint32_t (&o)[16]) {
+    if constexpr (FMT == QM_AFFINE) {
+        const float2 neg = make_float2(-8388608.0f, -8388608.0f);
+        const float2 s2 = make_float2(sc.s, sc.s), b2 = make_float2(sc.b, sc.b);
+        constexpr int PER = 32 / BITS;       // codes per word
+        constexpr int WORDS = 32 / PER;      // words per half row: 4 (4-bit) or 8 (8-bit)
+        uint32_t ws[WORDS];
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-#pragma unroll
-            for (int i = 0; i < 8; ++i) v[8 * j + i] = fmaf(code_f((ws[j] >> (4 * i)) & 15u), sc.s, sc.b);
-    } else if constexpr (FMT == QM_AFFINE && BITS == 8) {
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const uint32_t q = kk * 4 + half * 2 + h;
-            const uint4 w = *reinterpret_cast<const uint4*>(raw + sw128(row, q));
-            const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    v[16 * h + 4 * j + i] = fmaf(code_f((ws[j] >> (8 * i)) & 255u), sc.s, sc.b);
+        for (int q = 0; q < WORDS / 4; ++q) {
+            const uint4 w = *reinterpret_cast<const uint4*>(raw + sw128(row, (kk * 64 + half * 32) * BITS / 128 + q));
+            ws[4 * q] = w.x; ws[4 * q + 1] = w.y; ws[4 * q + 2] = w.z; ws[4 * q + 3] = w.w;
         }
+#pragma unroll
+        for (int j = 0; j < WORDS; ++j)
+#pragma unroll
+            for (int i = 0; i < PER; i += 2) {
+                float2 f;
+                if constexpr (BITS == 4) {
+                    f = make_float2(magic_f((ws[j] >> (4 * i)) & 15u), magic_f((ws[j] >> (4 * i + 4)) & 15u));
+                } else {
+                    f = make_float2(__uint_as_float(prmt(ws[j], 0x4B000000u, 0x7540 + i)),
+                                    __uint_as_float(prmt(ws[j], 0x4B000000u, 0x7541 + i)));
+                }
+                const float2 v = fma2(add2(f, neg), s2, b2);  // exact code, then one rounding
+                o[(j * PER + i) / 2] = bf2(v.x, v.y);
+            }
     } else if constexpr (FMT == QM_MXFP4) {
-        const uint32_t q = kk * 2 + half;
-        const uint4 w = *reinterpret_cast<const uint4*>(raw + sw128(row, q));
+        const uint4 w = *reinterpret_cast<const uint4*>(raw + sw128(row, kk * 2 + half));
         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+        const float2 s2 = make_float2(sc.s, sc.s);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             uint32_t h2[4];
             e2m1x8_to_f16x2(ws[j], h2);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2[i]));
-                v[8 * j + 2 * i] = f.x * sc.s;
-                v[8 * j + 2 * i + 1] = f.y * sc.s;
+                const float2 v = mul2(__half22float2(*reinterpret_cast<const __half2*>(&h2[i])), s2);
+                o[4 * j + i] = bf2(v.x, v.y);
             }
         }
-    } else {  // Q8_0: block kk*2 + half of the chunk, 34 bytes, rows 272 bytes apart
-        const uint16_t* blk = reinterpret_cast<const uint16_t*>(raw + row * 272 + (kk * 2 + half) * 34);
-        const float d = f16_bits_to_f32(blk[0]);
+    } else {  // Q8_0: block kk*2 + half of the chunk; 34 bytes, rows 272 bytes apart
+        const uint32_t base = row * 272 + (kk * 2 + half) * 34;  // 2-byte aligned
+        const uint32_t* wp = reinterpret_cast<const uint32_t*>(raw + ((base + 2) & ~3u));
+        const uint32_t dw = *reinterpret_cast<const uint32_t*>(raw + (base & ~3u));
+        const float d = f16_bits_to_f32((base & 2) ? (dw >> 16) : (dw & 0xFFFF));
+        const uint32_t sh = ((base + 2) & 3) * 8;  // 0 or 16
+        uint32_t w[9];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const uint32_t two = blk[1 + i];
-            v[2 * i] = d * static_cast<float>(static_cast<int8_t>(two & 0xFF));
-            v[2 * i + 1] = d * static_cast<float>(static_cast<int8_t>(two >> 8));
+        for (int j = 0; j < 9; ++j) w[j] = wp[j];
+        const float2 neg = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
+        const float2 d2 = make_float2(d, d);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t u = __funnelshift_r(w[j], w[j + 1], sh) ^ 0x80808080u;  // q + 128 per byte
+#pragma unroll
+            for (int i = 0; i < 4; i += 2) {
+                const float2 f = make_float2(__uint_as_float(prmt(u, 0x4B000000u, 0x7540 + i)),
+                                             __uint_as_float(prmt(u, 0x4B000000u, 0x7541 + i)));
+                const float2 v = mul2(add2(f, neg), d2);
+                o[(4 * j + i) / 2] = bf2(v.x, v.y);
+            }
         }
     }
 }
 
-template <int FMT, int BITS, int GS>
+template <int FMT, int BITS, int GS, int BM>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ Params p) {
     using R = Raw<FMT, BITS>;
+    constexpr int NX = NXof(BM);
+    constexpr int NACC = BM / 128;                 // 128-token accumulators sharing each B tile
+    constexpr uint32_t kXBytes = BM * BK * 2;      // activation tile per k step
+    constexpr uint32_t kTmemCols = BN * NACC;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int mt = blockIdx.x % p.mtiles, nt = blockIdx.x / p.mtiles;
@@ -222,8 +242,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 }
                 const int sx = ks % NX;
                 if (!mbar_wait(x_empty(sx), ((ks / NX) & 1) ^ 1)) { give_up(); break; }
-                mbar_expect_tx(x_full(sx), kTileBytes);
-                tma_load_2d(smem_u32(smem + p.off_x + sx * kTileBytes), &p.tm_x, ks * 128, static_cast<int32_t>(m0),
+                mbar_expect_tx(x_full(sx), kXBytes);
+                tma_load_2d(smem_u32(smem + p.off_x + sx * kXBytes), &p.tm_x, ks * 128, static_cast<int32_t>(m0),
                             x_full(sx));
                 mbar_arrive(x_full(sx));
                 last_x = ks;
@@ -238,7 +258,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = umma_idesc_bf16(BM, BN);
+            constexpr uint32_t idesc = umma_idesc_bf16(128, BN);
             for (int ks = 0; ks < ks_n && !s_abort; ++ks) {
                 const int sx = ks % NX, sb = ks % NB;
                 if (!mbar_wait(x_full(sx), (ks / NX) & 1) || !mbar_wait(b_full(sb), (ks / NB) & 1)) {
@@ -246,11 +266,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     break;
                 }
                 tc_fence_after();
-                const uint64_t ad = umma_desc_sw128(smem_u32(smem + p.off_x + sx * kTileBytes));
-                const uint64_t bd = umma_desc_sw128(smem_u32(smem + p.off_b + sb * kTileBytes));
+                const uint32_t xa = smem_u32(smem + p.off_x + sx * kXBytes);
+                const uint64_t bd = umma_desc_sw128(smem_u32(smem + p.off_b + sb * kBTileBytes));
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)  // advance 16 values = 32 bytes inside the swizzle atom
-                    umma_f16(tmem, ad + 2 * kk, bd + 2 * kk, idesc, ks > 0 || kk > 0);
+#pragma unroll
+                    for (int a = 0; a < NACC; ++a)
+                        umma_f16(tmem + a * BN, umma_desc_sw128(xa + a * 128 * 128) + 2 * kk, bd + 2 * kk, idesc,
+                                 ks > 0 || kk > 0);
                 umma_commit(x_empty(sx));
                 umma_commit(b_empty(sb));
             }
@@ -285,21 +308,18 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     if (lane == 0) give_up();
                     break;
                 }
-                const int64_t vidx = static_cast<int64_t>(ks) * BK + half * 32;
-                float v[32];
-                if (rowok && vidx < p.k) {
-                    decode32<FMT, BITS, GS>(raw, row, kk, half, cur[kk], v);
+                uint32_t o[16];
+                if (rowok && static_cast<int64_t>(ks) * BK + half * 32 < p.k) {
+                    decode32<FMT, BITS, GS>(raw, row, kk, half, cur[kk], o);
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+                    for (int i = 0; i < 16; ++i) o[i] = 0u;
                 }
-                uint8_t* bt = smem + p.off_b + sb * kTileBytes;
+                uint8_t* bt = smem + p.off_b + sb * kBTileBytes;
 #pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint4 q = make_uint4(bf2(v[8 * j], v[8 * j + 1]), bf2(v[8 * j + 2], v[8 * j + 3]),
-                                               bf2(v[8 * j + 4], v[8 * j + 5]), bf2(v[8 * j + 6], v[8 * j + 7]));
-                    *reinterpret_cast<uint4*>(bt + sw128(row, half * 4 + j)) = q;
-                }
+                for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<uint4*>(bt + sw128(row, half * 4 + j)) =
+                        make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
                 fence_proxy_async_smem();  // the tensor cores read B through the async proxy
                 __syncwarp();
                 if (lane == 0) mbar_arrive(b_full(sb));
@@ -314,14 +334,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const bool ok = mbar_wait(done, 0);
         if (!ok && lane == 0) give_up();
         tc_fence_after();
-        const int quarter = warp & 3, colhalf = (warp - 2) >> 2;
-        const int64_t m = m0 + 32 * quarter + lane;
+        // warp -> TMEM lane quarter (tokens) and a share of the accumulator columns
+        const int quarter = warp & 3, part = (warp - 2) >> 2;  // part 0 / 1
+        constexpr int COLS = BN * NACC / 2;                    // columns per warp
 #pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int c0 = 64 * colhalf + 32 * j;
+        for (int j = 0; j < COLS / 32; ++j) {
+            const int col = part * COLS + 32 * j;  // 0 .. BN*NACC
+            const int acc = col / BN, c0 = col % BN;
             uint32_t r[32];
-            tmem_ld32(tmem + (static_cast<uint32_t>(32 * quarter) << 16) + c0, r);
+            tmem_ld32(tmem + (static_cast<uint32_t>(32 * quarter) << 16) + col, r);
             tmem_wait_ld();
+            const int64_t m = m0 + 128 * acc + 32 * quarter + lane;
             if (!ok || s_abort || m >= p.M) continue;
             uint16_t* yr = p.y + m * p.n + n0 + c0;
             const int64_t left = p.n - (n0 + c0);
@@ -352,17 +375,21 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     }
 }
 
-template <int FMT, int BITS, int GS>
-static cudaError_t launch_t(Params& p, const WDesc& w, cudaStream_t st) {
+template <int FMT, int BITS, int GS, int BM>
+static cudaError_t launch_t(Params& p, const WDesc& w, const void* x, cudaStream_t st) {
     using R = Raw<FMT, BITS>;
+    constexpr int NX = NXof(BM);
+    p.mtiles = static_cast<int>((p.M + BM - 1) / BM);
     p.off_x = 1024;
-    p.off_b = p.off_x + NX * kTileBytes;
-    p.off_raw = p.off_b + NB * kTileBytes;
+    p.off_b = p.off_x + NX * BM * BK * 2;
+    p.off_raw = p.off_b + NB * kBTileBytes;
     p.raw_stage_bytes = (R::BYTES * BN + 1023) / 1024 * 1024;
     const size_t smem = p.off_raw + NR * p.raw_stage_bytes;
+    if (!make_tmap_2d(&p.tm_x, x, static_cast<uint64_t>(w.k) * 2, p.M, static_cast<uint64_t>(w.k) * 2, 128, BM, true))
+        return cudaErrorNotSupported;
     if (!make_tmap_2d(&p.tm_raw, w.codes, w.code_row_bytes, w.n, w.code_row_bytes, R::BYTES, BN, R::SW, R::ELEM))
         return cudaErrorNotSupported;
-    auto kern = gemm_kernel<FMT, BITS, GS>;
+    auto kern = gemm_kernel<FMT, BITS, GS, BM>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int64_t ntiles = (w.n + BN - 1) / BN;
@@ -379,12 +406,17 @@ static cudaError_t launch_t(Params& p, const WDesc& w, cudaStream_t st) {
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+template <int FMT, int BITS, int GS>
+static cudaError_t launch_bm(Params& p, const WDesc& w, const void* x, cudaStream_t st) {
+    return p.M > 128 ? launch_t<FMT, BITS, GS, 256>(p, w, x, st) : launch_t<FMT, BITS, GS, 128>(p, w, x, st);
+}
+
 }  // namespace gemm
 
 bool gemm_supported(const WDesc& w, int64_t M) {
     if (M < 1 || w.ndim != 2 || w.n < 1 || w.k < 64) return false;
     if (w.code_row_bytes % 16) return false;  // TMA row stride
-    if ((w.n + gemm::BN - 1) / gemm::BN * ((M + gemm::BM - 1) / gemm::BM) > 0x7FFFFFFF) return false;
+    if (M > (int64_t(1) << 31) || w.n > (int64_t(1) << 31)) return false;
     return true;
 }
 
@@ -400,19 +432,16 @@ qm_status launch_gemm(const WDesc& w, const void* x, int64_t M, void* y, cudaStr
     p.scale_row_bytes = w.scale_row_bytes;
     p.sdt = w.sdt;
     p.ksteps = static_cast<int>((w.k + BK - 1) / BK);
-    p.mtiles = static_cast<int>((M + BM - 1) / BM);
-    if (!make_tmap_2d(&p.tm_x, x, static_cast<uint64_t>(w.k) * 2, M, static_cast<uint64_t>(w.k) * 2, 128, BM, true))
-        return fail(QM_ENOTSUP, "x: no TMA descriptor for this shape");
     cudaError_t e = cudaErrorInvalidValue;
-    if (w.fmt == QM_AFFINE && w.bits == 4 && w.gs == 32) e = launch_t<QM_AFFINE, 4, 32>(p, w, st);
-    else if (w.fmt == QM_AFFINE && w.bits == 4 && w.gs == 64) e = launch_t<QM_AFFINE, 4, 64>(p, w, st);
-    else if (w.fmt == QM_AFFINE && w.bits == 4 && w.gs == 128) e = launch_t<QM_AFFINE, 4, 128>(p, w, st);
-    else if (w.fmt == QM_AFFINE && w.bits == 8 && w.gs == 32) e = launch_t<QM_AFFINE, 8, 32>(p, w, st);
-    else if (w.fmt == QM_AFFINE && w.bits == 8 && w.gs == 64) e = launch_t<QM_AFFINE, 8, 64>(p, w, st);
-    else if (w.fmt == QM_AFFINE && w.bits == 8 && w.gs == 128) e = launch_t<QM_AFFINE, 8, 128>(p, w, st);
-    else if (w.fmt == QM_Q8_0) e = launch_t<QM_Q8_0, 8, 32>(p, w, st);
-    else if (w.fmt == QM_MXFP4) e = launch_t<QM_MXFP4, 4, 32>(p, w, st);
-    if (e == cudaErrorNotSupported) {  // no descriptor for the weight: the plain kernel
+    if (w.fmt == QM_AFFINE && w.bits == 4 && w.gs == 32) e = launch_bm<QM_AFFINE, 4, 32>(p, w, x, st);
+    else if (w.fmt == QM_AFFINE && w.bits == 4 && w.gs == 64) e = launch_bm<QM_AFFINE, 4, 64>(p, w, x, st);
+    else if (w.fmt == QM_AFFINE && w.bits == 4 && w.gs == 128) e = launch_bm<QM_AFFINE, 4, 128>(p, w, x, st);
+    else if (w.fmt == QM_AFFINE && w.bits == 8 && w.gs == 32) e = launch_bm<QM_AFFINE, 8, 32>(p, w, x, st);
+    else if (w.fmt == QM_AFFINE && w.bits == 8 && w.gs == 64) e = launch_bm<QM_AFFINE, 8, 64>(p, w, x, st);
+    else if (w.fmt == QM_AFFINE && w.bits == 8 && w.gs == 128) e = launch_bm<QM_AFFINE, 8, 128>(p, w, x, st);
+    else if (w.fmt == QM_Q8_0) e = launch_bm<QM_Q8_0, 8, 32>(p, w, x, st);
+    else if (w.fmt == QM_MXFP4) e = launch_bm<QM_MXFP4, 4, 32>(p, w, x, st);
+    if (e == cudaErrorNotSupported) {  // no TMA descriptor for these operands: the plain kernel
         e = launch_apply_simple(w, x, M, y, st);
         return e == cudaSuccess ? QM_OK : cuda_fail(e, "apply launch");
     }
