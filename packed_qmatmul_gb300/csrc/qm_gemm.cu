@@ -155,9 +155,12 @@ QM_DEV void decode32(const uint8_t* raw, int row, int kk, int half, Sc sc, uint3
         const uint32_t dw = *reinterpret_cast<const uint32_t*>(raw + (base & ~3u));
         const float d = f16_bits_to_f32((base & 2) ? (dw >> 16) : (dw & 0xFFFF));
         const uint32_t sh = ((base + 2) & 3) * 8;  // 0 or 16
+        // words 0..7 hold the codes when they start word-aligned (odd blocks);
+        // even blocks also need word 8, which still ends inside the row
         uint32_t w[9];
 #pragma unroll
-        for (int j = 0; j < 9; ++j) w[j] = wp[j];
+        for (int j = 0; j < 8; ++j) w[j] = wp[j];
+        w[8] = sh ? wp[8] : 0u;
         const float2 neg = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
         const float2 d2 = make_float2(d, d);
 #pragma unroll
@@ -383,7 +386,7 @@ static cudaError_t launch_t(Params& p, const WDesc& w, const void* x, cudaStream
     p.off_x = 1024;
     p.off_b = p.off_x + NX * BM * BK * 2;
     p.off_raw = p.off_b + NB * kBTileBytes;
-    p.raw_stage_bytes = (R::BYTES * BN + 1023) / 1024 * 1024;
+    p.raw_stage_bytes = (R::BYTES * BN + 16 + 1023) / 1024 * 1024;  // 16 spare bytes after each slot
     const size_t smem = p.off_raw + NR * p.raw_stage_bytes;
     if (!make_tmap_2d(&p.tm_x, x, static_cast<uint64_t>(w.k) * 2, p.M, static_cast<uint64_t>(w.k) * 2, 128, BM, true))
         return cudaErrorNotSupported;
