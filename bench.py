@@ -151,7 +151,7 @@ def build_step(bits, M, device, only=None):
         if only and not name.endswith(only):
             continue
         w = synth.affine_weight(g, n, k, bits=bits, group_size=64)
-        qw = qm.QWeight.from_arrays(w, device)
+        qw = qm.QWeight.from_arrays(w, device, flags=qm.QM_WEIGHT_STATIC)  # model weights do not change
         x = torch.from_numpy(synth.activations(g, M, k).view(np.int16)).to(device).view(torch.bfloat16)
         y = torch.empty((M, n), dtype=torch.bfloat16, device=device)
         items.append((name, n, k, qw, x, y))

@@ -77,7 +77,16 @@ typedef struct qm_weight {
     const void* codes;   /* see the formats above */
     const void* scales;  /* QM_AFFINE, QM_MXFP4; must be NULL for QM_Q8_0 */
     const void* biases;  /* QM_AFFINE only; must be NULL otherwise */
+    uint32_t flags;      /* QM_WEIGHT_* bits; 0 for none */
 } qm_weight;
+
+/* The weight's parts are not written by any work that may still be running on
+ * the stream when a call that reads them is enqueued -- as with the weights of
+ * a deployed model. Products may then start reading the weight before the
+ * preceding kernel on the stream has finished (its activations are still read
+ * only after it). Leave it clear if the kernel just before the call writes the
+ * weight (for example a qm_take producing it). */
+#define QM_WEIGHT_STATIC 1u
 
 /* dequant: out [..., n, k] of out_dtype (QM_F32, QM_BF16 or QM_F16) holds
  * every value of w rounded once to out_dtype (round to nearest even,

@@ -20,7 +20,7 @@ from typing import Optional, Sequence
 import torch
 
 __all__ = [
-    "QM_AFFINE", "QM_Q8_0", "QM_MXFP4", "QM_F32", "QM_BF16", "QM_F16", "QM_I32", "QM_I64",
+    "QM_AFFINE", "QM_Q8_0", "QM_MXFP4", "QM_WEIGHT_STATIC", "QM_F32", "QM_BF16", "QM_F16", "QM_I32", "QM_I64",
     "QMError", "QWeight", "library_path", "load_library",
     "qm_dequant", "qm_apply", "qm_take", "qm_apply_experts", "qm_apply_experts_workspace",
     "qm_experts_route", "qm_apply_experts_static", "qm_device_status", "qm_last_error", "qm_version",
@@ -31,6 +31,7 @@ QM_OK, QM_EINVAL, QM_ECUDA, QM_ETIMEOUT, QM_ENOTSUP = 0, 1, 2, 3, 4
 QM_AFFINE, QM_Q8_0, QM_MXFP4 = 0, 1, 2
 QM_F32, QM_BF16, QM_F16 = 0, 1, 2
 QM_I32, QM_I64 = 0, 1
+QM_WEIGHT_STATIC = 1
 QM_MAX_NDIM = 4
 
 _STATUS = {QM_EINVAL: "QM_EINVAL", QM_ECUDA: "QM_ECUDA", QM_ETIMEOUT: "QM_ETIMEOUT",
@@ -56,6 +57,7 @@ class _CWeight(ctypes.Structure):
         ("scale_dtype", ctypes.c_int32), ("ndim", ctypes.c_int32),
         ("shape", ctypes.c_int64 * QM_MAX_NDIM),
         ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("biases", ctypes.c_void_p),
+        ("flags", ctypes.c_uint32),
     ]
 
 
@@ -128,16 +130,17 @@ class QWeight:
 
     def __init__(self, fmt, shape: Sequence[int], codes: torch.Tensor,
                  scales: Optional[torch.Tensor] = None, biases: Optional[torch.Tensor] = None,
-                 bits: int = 0, group_size: int = 0, scale_dtype: int = QM_BF16):
+                 bits: int = 0, group_size: int = 0, scale_dtype: int = QM_BF16, flags: int = 0):
         self.format = _FORMATS[fmt] if isinstance(fmt, str) else int(fmt)
         self.shape = tuple(int(s) for s in shape)
         self.codes, self.scales, self.biases = codes, scales, biases
         self.bits = int(bits)
         self.group_size = int(group_size)
         self.scale_dtype = int(scale_dtype)
+        self.flags = int(flags)
 
     @classmethod
-    def from_arrays(cls, d: dict, device="cuda") -> "QWeight":
+    def from_arrays(cls, d: dict, device="cuda", flags: int = 0) -> "QWeight":
         """From a dict of NumPy parts as packed_qmatmul_gb300.synth returns."""
         import numpy as np
 
@@ -152,7 +155,7 @@ class QWeight:
         sdt = QM_F16 if d.get("scale_dtype") == "f16" else QM_BF16
         return cls(d["format"], d["shape"], dev(d["codes"]), dev(d.get("scales")),
                    dev(d.get("biases")), bits=d.get("bits", 0), group_size=d.get("group_size", 0),
-                   scale_dtype=sdt)
+                   scale_dtype=sdt, flags=flags)
 
     def _c(self) -> _CWeight:
         w = _CWeight()
@@ -162,6 +165,7 @@ class QWeight:
         for i, s in enumerate(self.shape[:QM_MAX_NDIM]):
             w.shape[i] = s
         w.codes, w.scales, w.biases = _ptr(self.codes), _ptr(self.scales), _ptr(self.biases)
+        w.flags = self.flags
         return w
 
     def part_shapes(self, lead: Sequence[int]):

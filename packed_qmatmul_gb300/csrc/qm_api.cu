@@ -133,6 +133,8 @@ qm_status validate_weight(const qm_weight* w, WDesc* d) {
     d->codes = static_cast<const uint8_t*>(w->codes);
     d->scales = static_cast<const uint8_t*>(w->scales);
     d->biases = static_cast<const uint8_t*>(w->biases);
+    if (w->flags & ~QM_WEIGHT_STATIC) return fail(QM_EINVAL, "w: unknown flags");
+    d->is_static = (w->flags & QM_WEIGHT_STATIC) != 0;
     if (!empty) {
         if (!w->codes) return fail(QM_EINVAL, "codes: NULL");
         if (!aligned16(w->codes)) return fail(QM_EINVAL, "codes: base address must be 16-byte aligned");

@@ -79,6 +79,7 @@ struct Params {
     int stages_per_cluster;  // 32-row stages per cluster
     int64_t n_stages;        // 32-row stages in all
     int team;                // warps per team (1, 2, 4, 8 or 16)
+    int static_w;            // weight may be read before the previous kernel ends
     // shared memory layout (byte offsets from the dynamic smem base)
     uint32_t nstage, stage_bytes;
     uint32_t code_seg, nbox;          // per row: bytes of codes; 128-byte boxes per stage
@@ -254,7 +255,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
     }
     __syncthreads();
     grid_launch_dependents();
-    grid_dependency_wait();  // x (and, conservatively, W) may come from the previous kernel
+    // x comes from the previous kernel; so may W, unless the caller marked it
+    // static, in which case the producer streams its first stages before waiting
+    if (!p.static_w || warp != kWarps) grid_dependency_wait();
 
     if (warp == kWarps) {
         // ------------------------------------------------------------ producer
@@ -269,8 +272,14 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                 bulk_g2s(smem_u32(smem + p.off_xraw + lane * xbytes), p.x + lane * p.k + kbase, xbytes, bar_x);
         };
         int issued = 0;
-        if (nst == 0) copy_x();
+        bool xdone = false;
+        const int npre = p.static_w ? std::min(nst, static_cast<int>(p.nstage)) : 0;
         for (int j = 0; j < nst; ++j) {
+            if (p.static_w && !xdone && j == npre) {
+                grid_dependency_wait();
+                copy_x();
+                xdone = true;
+            }
             const uint32_t slot = j % p.nstage;
             const uint32_t par = ((j / p.nstage) & 1) ^ 1;
             if (!mbar_wait(bar_empty0 + 8 * slot, par) || s_abort) {
@@ -320,9 +329,15 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                 }
             }
             mbar_arrive(bar);
-            if (j == 0) copy_x();
+            if (!p.static_w && !xdone) {
+                copy_x();
+                xdone = true;
+            }
         }
-        if (issued == 0 && nst > 0) copy_x();  // abandoned before the first stage
+        if (!xdone) {  // every stage prefetched, or abandoned before the first
+            if (p.static_w) grid_dependency_wait();
+            copy_x();
+        }
         if (s_abort) {
             // abandoned: let the copies already issued land before the CTA exits
             for (int j = std::max(0, issued - static_cast<int>(p.nstage)); j < issued; ++j)
@@ -811,6 +826,7 @@ qm_status launch_gemv(const WDesc& w, const void* x, int64_t M, void* y, cudaStr
     p.sdt = w.sdt;
     p.code_row_bytes = w.code_row_bytes;
     p.scale_row_bytes = w.scale_row_bytes;
+    p.static_w = w.is_static ? 1 : 0;
     bool maps = make_tmap_2d(&p.tm_codes, w.codes, w.code_row_bytes, w.n, w.code_row_bytes, 128, kRows, true);
     if (maps && p.S > 1 && p.scale_seg) {
         maps = make_tmap_2d(&p.tm_scales, w.scales, w.scale_row_bytes, w.n, w.scale_row_bytes, p.scale_seg,

@@ -26,6 +26,7 @@ struct WDesc {
     int64_t code_row_bytes = 0;   // bytes of one row (k values) of codes
     int64_t scale_row_bytes = 0;  // bytes of one row of scales (0 if none)
     int64_t bias_row_bytes = 0;   // bytes of one row of biases (0 if none)
+    bool is_static = false;       // QM_WEIGHT_STATIC: may be read before the previous kernel ends
 };
 
 // Thread-local error message of the calling thread (qm_last_error()).

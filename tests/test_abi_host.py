@@ -42,12 +42,13 @@ def test_version(lib):
     assert lib.qm_version() >= 100
 
 
-def _w(fmt=qm.QM_AFFINE, bits=4, gs=64, shape=(16, 64), codes=256, scales=512, biases=768, ndim=2):
+def _w(fmt=qm.QM_AFFINE, bits=4, gs=64, shape=(16, 64), codes=256, scales=512, biases=768, ndim=2, flags=0):
     w = qm._CWeight()
     w.format, w.bits, w.group_size, w.scale_dtype, w.ndim = fmt, bits, gs, qm.QM_BF16, ndim
     for i, s in enumerate(shape):
         w.shape[i] = s
     w.codes, w.scales, w.biases = codes, scales, biases
+    w.flags = flags
     return w
 
 
@@ -67,6 +68,7 @@ def _dequant_err(lib, w, out=1024, dt=qm.QM_BF16):
     (dict(biases=8), "biases"),
     (dict(fmt=7), "w"),
     (dict(ndim=1), "w"),
+    (dict(flags=2), "w"),                      # no such flag
     (dict(fmt=qm.QM_Q8_0, bits=0, gs=0), "scales"),  # Q8_0 takes no scales part
     (dict(fmt=qm.QM_MXFP4, bits=0, gs=0, scales=512), "biases"),
 ])

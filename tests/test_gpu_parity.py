@@ -209,6 +209,36 @@ def test_apply_deterministic():
     assert np.array_equal(a, b)
 
 
+@pytest.mark.parametrize("M", [1, 4])
+@pytest.mark.parametrize("n", [64, 1024])
+def test_apply_static_weight_chain(M, n):
+    # weights marked static are streamed before the previous kernel in the stream
+    # ends; the activations, which that kernel writes, must still be read after it
+    g = synth.rng(710 + M)
+    k = n
+    ws = [_make("affine4_g64", g, n, k) for _ in range(4)]
+    x0 = synth.activations(g, M, k)
+    ys = {}
+    for flags in (0, qm.QM_WEIGHT_STATIC):
+        qws = [qm.QWeight.from_arrays(w, flags=flags) for w in ws]
+        x = _dev_bf16(x0)
+        outs = []
+        for qw in qws:  # each product reads the one before it, no sync between
+            x = qm.apply(qw, x)
+            outs.append(x)
+        ys[flags] = [_host(o) for o in outs]
+    for a, b in zip(ys[0], ys[qm.QM_WEIGHT_STATIC]):
+        assert np.array_equal(a, b)
+    xin = x0
+    for i, w in enumerate(ws):
+        ow = to_oracle(w)
+        got = bf16_to_f64(ys[qm.QM_WEIGHT_STATIC][i])
+        ref = oracle.apply(ow, xin)
+        xn = np.linalg.norm(oracle.decode_array(xin, oracle.BF16), axis=1)
+        check_product(got, ref, row_norms(ow), xn, k, f"static chain step {i}")
+        xin = ys[qm.QM_WEIGHT_STATIC][i]
+
+
 # ---------------------------------------------------------------- routing and experts
 @pytest.mark.parametrize("id64", [False, True])
 def test_route_bit_exact(id64):
