@@ -73,11 +73,12 @@ __global__ void __launch_bounds__(256) route_count_kernel(const void* ids, int i
 
 // One warp per chunk: scan the chunk counts into this chunk's start offsets,
 // then place the chunk's positions 32 at a time, each step ranking equal ids
-// by lane so the order stays stable.
+// by lane so the order stays stable. With zy set, the rows of zy [P, zn] at
+// out-of-range positions are cleared on the way (their product is zero).
 __global__ void __launch_bounds__(32) route_scatter_kernel(const void* ids, int id64, int64_t P,
                                                            int64_t E, const int32_t* chunk_counts,
                                                            int32_t* counts, int32_t* offsets,
-                                                           int32_t* perm) {
+                                                           int32_t* perm, uint16_t* zy, int64_t zn) {
     extern __shared__ int32_t sm[];
     int32_t* base = sm;           // [E + 1]: where this chunk's positions of expert e start
     int32_t* run = sm + E + 1;    // [E + 1]: how many of them are placed so far
@@ -141,6 +142,14 @@ __global__ void __launch_bounds__(32) route_scatter_kernel(const void* ids, int 
         __syncwarp();
         if (valid && (mask & lt) == 0) run[b] += __popc(mask);
         __syncwarp();
+        if (zy) {
+            uint32_t out = __ballot_sync(0xffffffffu, valid && b == static_cast<int32_t>(E));
+            while (out) {
+                const int64_t q = s + (__ffs(out) - 1);
+                out &= out - 1;
+                for (int64_t j = lane; j < zn; j += 32) zy[q * zn + j] = 0;
+            }
+        }
     }
 }
 
@@ -220,7 +229,8 @@ size_t experts_workspace_bytes(int64_t P, int64_t E) {
 }
 
 cudaError_t launch_route(const void* ids, int id64, int64_t P, int64_t E, int32_t* counts,
-                         int32_t* offsets, int32_t* perm, void* ws, cudaStream_t st) {
+                         int32_t* offsets, int32_t* perm, void* ws, cudaStream_t st, uint16_t* zy,
+                         int64_t zn) {
     if (P == 0) {
         if (E > 0) {
             cudaError_t e = cudaMemsetAsync(counts, 0, E * 4, st);
@@ -238,7 +248,7 @@ cudaError_t launch_route(const void* ids, int id64, int64_t P, int64_t E, int32_
     }
     route_count_kernel<<<static_cast<unsigned>(nchunks), 256, sm1, st>>>(ids, id64, P, E, chunk_counts);
     route_scatter_kernel<<<static_cast<unsigned>(nchunks), 32, sm2, st>>>(ids, id64, P, E, chunk_counts,
-                                                                          counts, offsets, perm);
+                                                                          counts, offsets, perm, zy, zn);
     return cudaGetLastError();
 }
 
@@ -252,8 +262,12 @@ qm_status launch_experts(const WDesc& w, const void* ids, int id64, int64_t T, i
     int32_t* counts = reinterpret_cast<int32_t*>(wb + l.counts);
     int32_t* offsets = reinterpret_cast<int32_t*>(wb + l.offsets);
     int32_t* perm = reinterpret_cast<int32_t*>(wb + l.perm);
-    cudaError_t e = launch_route(ids, id64, P, E, counts, offsets, perm, ws, st);
+    const bool grouped = P <= 32 * E && gemv_grouped_supported(w, P);
+    cudaError_t e = launch_route(ids, id64, P, E, counts, offsets, perm, ws, st,
+                                 grouped ? static_cast<uint16_t*>(y) : nullptr, w.n);
     if (e != cudaSuccess) return cuda_fail(e, "route launch");
+    if (grouped)  // experts averaging few positions: chunks through the decode product
+        return launch_gemv_grouped(w, offsets, perm, P, x_rows == T ? static_cast<int>(topk) : 1, x, y, st);
     ExpArgs a{w.codes, w.scales, w.biases, E, w.n, w.k, w.code_row_bytes, w.scale_row_bytes, w.gs, w.sdt};
     const int64_t jobs = P * w.n;
     const int64_t blocks = std::min<int64_t>((jobs * 32 + 255) / 256, int64_t(num_sms()) * 8);

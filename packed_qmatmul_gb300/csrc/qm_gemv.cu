@@ -80,6 +80,15 @@ struct Params {
     int64_t n_stages;        // 32-row stages in all
     int team;                // warps per team (1, 2, 4, 8 or 16)
     int static_w;            // weight may be read before the previous kernel ends
+    // grouped mode (apply_experts), off when g_off is null: the weight is
+    // [E, n, k] and each cluster slot is one chunk of up to g_Q routed positions
+    // of one expert, times one share of that expert's rows
+    const int32_t* g_off;    // [E + 1] start of each expert's positions in g_perm
+    const int32_t* g_perm;   // routed order -> position
+    int64_t g_E;
+    int g_Q;                 // positions per chunk
+    int g_xdiv;              // activation row of position q: q / g_xdiv
+    int64_t g_wclusters;     // clusters per chunk
     // shared memory layout (byte offsets from the dynamic smem base)
     uint32_t nstage, stage_bytes;
     uint32_t code_seg, nbox;          // per row: bytes of codes; 128-byte boxes per stage
@@ -224,9 +233,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = p.S;
     const uint32_t rank = (S > 1) ? cluster_ctarank() : 0;
-    const int64_t cluster = blockIdx.x / S;
-    const int64_t stage0 = cluster * p.stages_per_cluster;
-    const int nst = static_cast<int>(std::min<int64_t>(p.stages_per_cluster, p.n_stages - stage0));
+    int64_t cluster = blockIdx.x / S;
     const int64_t kbase = rank * p.krange;
     const int groups = static_cast<int>(p.krange / GS);
 
@@ -239,6 +246,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
     const uint32_t bar_x = smem_u32(bars + 2 * kMaxStages);
     volatile int& s_abort = *reinterpret_cast<volatile int*>(smem + (2 * kMaxStages + 1) * 8);
     volatile int* slot_stage = reinterpret_cast<volatile int*>(smem + (2 * kMaxStages + 2) * 8);
+    // grouped mode: the chunk's size and expert, its positions and activation rows
+    int* s_grp = reinterpret_cast<int*>(smem + 360);        // [2]
+    int* s_pos = reinterpret_cast<int*>(smem + 368);        // [16]
+    int* s_xrow = reinterpret_cast<int*>(smem + 432);       // [16], ends before 512
 
     unsigned int* xmax = reinterpret_cast<unsigned int*>(smem + p.off_tokscale) + 32;  // [16] max |x| bits
     if (threadIdx.x == 0) {
@@ -255,21 +266,80 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
     }
     __syncthreads();
     grid_launch_dependents();
+    int M = p.M;
+    int64_t wrow0 = 0;  // first row of this CTA's matrix in the codes and scales
+    if (p.g_off) {
+        // which chunk of which expert: the routing tables come from the previous kernel
+        if (warp == 0) {
+            grid_dependency_wait();
+            const int64_t slot = cluster / p.g_wclusters;
+            int64_t before = 0;  // chunks of the experts already passed
+            int gm = 0, ge = 0, gb = 0;
+            for (int64_t e0 = 0; e0 < p.g_E; e0 += 32) {
+                const int64_t e = e0 + lane;
+                int o0 = 0, cnt = 0;
+                if (e < p.g_E) {
+                    o0 = __ldg(p.g_off + e);
+                    cnt = __ldg(p.g_off + e + 1) - o0;
+                }
+                const int64_t nch = (cnt + p.g_Q - 1) / p.g_Q;
+                int64_t inc = nch;  // inclusive scan over the lanes
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int64_t t = __shfl_up_sync(0xffffffffu, inc, o);
+                    if (lane >= o) inc += t;
+                }
+                const int64_t lo = before + inc - nch;
+                const bool mine = e < p.g_E && slot >= lo && slot < lo + nch;
+                const uint32_t hit = __ballot_sync(0xffffffffu, mine);
+                if (mine) {
+                    const int ch = static_cast<int>(slot - lo);
+                    gb = o0 + ch * p.g_Q;
+                    gm = min(p.g_Q, cnt - ch * p.g_Q);
+                    ge = static_cast<int>(e);
+                }
+                if (hit) {
+                    const int src = __ffs(hit) - 1;
+                    gm = __shfl_sync(0xffffffffu, gm, src);
+                    ge = __shfl_sync(0xffffffffu, ge, src);
+                    gb = __shfl_sync(0xffffffffu, gb, src);
+                    break;
+                }
+                before += __shfl_sync(0xffffffffu, inc, 31);
+            }
+            if (lane == 0) { s_grp[0] = gm; s_grp[1] = ge; }
+            if (lane < gm) {
+                const int q = __ldg(p.g_perm + gb + lane);
+                s_pos[lane] = q;
+                s_xrow[lane] = q / p.g_xdiv;
+            }
+        }
+        __syncthreads();
+        M = s_grp[0];
+        if (M == 0) return;  // a slot past the last chunk; the same for every CTA of the cluster
+        wrow0 = static_cast<int64_t>(s_grp[1]) * p.n;
+        cluster %= p.g_wclusters;
+    }
+    const int64_t stage0 = cluster * p.stages_per_cluster;
+    const int nst = static_cast<int>(std::min<int64_t>(p.stages_per_cluster, p.n_stages - stage0));
     // x comes from the previous kernel; so may W, unless the caller marked it
     // static, in which case the producer streams its first stages before waiting
-    if (!p.static_w || warp != kWarps) grid_dependency_wait();
+    if (!p.g_off && (!p.static_w || warp != kWarps)) grid_dependency_wait();
+    else if (p.g_off && warp != 0) grid_dependency_wait();
 
     if (warp == kWarps) {
         // ------------------------------------------------------------ producer
         const uint32_t xbytes = static_cast<uint32_t>(p.krange * 2);
         auto copy_x = [&]() {  // after the first stage's copies are under way
             if (lane == 0) {
-                mbar_expect_tx(bar_x, xbytes * p.M);
+                mbar_expect_tx(bar_x, xbytes * M);
                 mbar_arrive(bar_x);
             }
             __syncwarp();
-            if (lane < p.M)
-                bulk_g2s(smem_u32(smem + p.off_xraw + lane * xbytes), p.x + lane * p.k + kbase, xbytes, bar_x);
+            if (lane < M) {
+                const int64_t xr = p.g_off ? s_xrow[lane] : lane;
+                bulk_g2s(smem_u32(smem + p.off_xraw + lane * xbytes), p.x + xr * p.k + kbase, xbytes, bar_x);
+            }
         };
         int issued = 0;
         bool xdone = false;
@@ -307,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
             if (lane == 0) {
                 slot_stage[slot] = j;
                 mbar_expect_tx(bar, tx);
-                const int32_t x0 = static_cast<int32_t>(rank * p.code_seg), y0 = static_cast<int32_t>(row0);
+                const int32_t x0 = static_cast<int32_t>(rank * p.code_seg), y0 = static_cast<int32_t>(wrow0 + row0);
                 for (uint32_t c = 0; c < p.nbox; ++c)
                     tma_load_2d(smem_u32(st + c * kRows * 128), &p.tm_codes, x0 + 128 * c, y0, bar);
                 if (p.scale_seg && S > 1) {
@@ -318,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
             }
             __syncwarp();
             if (p.scale_seg && S == 1) {
-                const int64_t off = row0 * p.scale_row_bytes;
+                const int64_t off = (wrow0 + row0) * p.scale_row_bytes;
                 if (lane == 0 && span_bulk) {
                     bulk_g2s(smem_u32(st + p.off_scales), p.scales + off, span_bulk, bar);
                     if (p.biases) bulk_g2s(smem_u32(st + p.off_biases), p.biases + off, span_bulk, bar);
@@ -356,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
         {
             // max |x| per token: one pass over the staged rows, order-free
             const int per_row = static_cast<int>(p.krange / 8);
-            for (int i = ctid; i < p.M * per_row; i += kWarps * 32) {
+            for (int i = ctid; i < M * per_row; i += kWarps * 32) {
                 const uint4 q = *reinterpret_cast<const uint4*>(xs + 8 * i);
                 const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
                 float amax = 0.0f;
@@ -390,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                 const int ln = it % 32, nt = (it / 32) % NT, gi = it / (32 * NT);
                 const int tg = ln >> 2, t = ln & 3;
                 const int m = nt * 8 + tg;
-                const bool live = m < p.M;  // padding tokens get exact zeros
+                const bool live = m < M;  // padding tokens get exact zeros
                 const float mul = live ? __uint_as_float(static_cast<uint32_t>(token_exp(m) + 127) << 23) : 0.0f;
                 const uint16_t* xr = xs + (live ? m : 0) * p.krange;
                 uint32_t* dst = xfrag + ((gi * 32 + ln) * MM) * NT * 2 + nt * 2;
@@ -571,9 +641,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                 const int r = 16 * tt + (ln >> 2) + ((i & 2) ? 8 : 0);
                 v *= tokscale[m];
                 if (S == 1) {
-                    if (m < p.M && row0 + r < p.n) {
+                    if (m < M && row0 + r < p.n) {
                         __nv_bfloat16 bv = __float2bfloat16_rn(v);
-                        p.y[static_cast<int64_t>(m) * p.n + row0 + r] = *reinterpret_cast<uint16_t*>(&bv);
+                        const int64_t yr = p.g_off ? s_pos[m] : m;
+                        p.y[yr * p.n + row0 + r] = *reinterpret_cast<uint16_t*>(&bv);
                     }
                 } else {
                     partial[(j * kRows + r) * 16 + m] = v;
@@ -623,11 +694,12 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
         for (int e = rank * blockDim.x + threadIdx.x; e < entries; e += S * blockDim.x) {
             const int m = e % 16, rr = e / 16;
             const int64_t row = stage0 * kRows + rr;
-            if (m >= p.M || row >= p.n) continue;
+            if (m >= M || row >= p.n) continue;
             float sum = 0.0f;
             for (int q = 0; q < S; ++q) sum += ld_shared_cluster_f32(map_shared_rank(base + 4u * e, q));
             __nv_bfloat16 b = __float2bfloat16_rn(sum);
-            p.y[static_cast<int64_t>(m) * p.n + row] = *reinterpret_cast<uint16_t*>(&b);
+            const int64_t yr = p.g_off ? s_pos[m] : m;
+            p.y[yr * p.n + row] = *reinterpret_cast<uint16_t*>(&b);
         }
         cluster_sync();
     }
@@ -683,8 +755,10 @@ static int max_clusters(int S, size_t smem) {
     return n;
 }
 
-// A plan for S CTAs per cluster (splitting k) and `per_sm` CTAs per SM.
-static bool plan_for(const WDesc& w, int64_t M, int S, int per_sm, Plan* out) {
+// A plan for S CTAs per cluster (splitting k) and `per_sm` CTAs per SM, the
+// matrix getting `share` of the GPU's CTA slots (other chunks of a grouped
+// product take the rest).
+static bool plan_for(const WDesc& w, int64_t M, int S, int per_sm, Plan* out, double share = 1.0) {
     if (w.k % S) return false;
     const int64_t kr = w.k / S;
     if (kr % w.gs) return false;
@@ -710,7 +784,7 @@ static bool plan_for(const WDesc& w, int64_t M, int S, int per_sm, Plan* out) {
     const int64_t budget = (per_sm == 2 ? (max_smem_optin() + 1024) / 2 : max_smem_optin()) - 1024;
     // work split: clusters of S CTAs, per_sm CTAs to an SM
     p.n_stages = (w.n + kRows - 1) / kRows;
-    int64_t G = std::max<int64_t>(1, int64_t(num_sms()) * per_sm / S);
+    int64_t G = std::max<int64_t>(1, static_cast<int64_t>(num_sms() * per_sm * share) / S);
     if (S > 1) G = std::max<int64_t>(1, std::min<int64_t>(G, max_clusters(S, budget)));
     G = std::min<int64_t>(G, p.n_stages);
     const int64_t spc = (p.n_stages + G - 1) / G;
@@ -753,13 +827,13 @@ static bool plan_for(const WDesc& w, int64_t M, int S, int per_sm, Plan* out) {
 // Pick the k split and CTAs per SM: least per-CTA work (stages x k range,
 // halved where two CTAs share an SM), then fewest splits; a plan that keeps
 // three stages in flight beats one that cannot.
-static Plan make_plan(const WDesc& w, int64_t M) {
+static Plan make_plan(const WDesc& w, int64_t M, double share = 1.0) {
     Plan best;
     double best_cost = 1e300;
     for (int per_sm = 2; per_sm >= 1; --per_sm)
         for (int S = 1; S <= 8; ++S) {
             Plan pl;
-            if (!plan_for(w, M, S, per_sm, &pl)) continue;
+            if (!plan_for(w, M, S, per_sm, &pl, share)) continue;
             const bool shallow = pl.p.nstage < 3 && pl.p.stages_per_cluster >= 3;
             const double cost = static_cast<double>(pl.p.stages_per_cluster) * pl.p.krange / per_sm *
                                 (1.0 + 0.03 * (S - 1)) * (shallow ? 2.0 : 1.0);
@@ -857,6 +931,95 @@ qm_status launch_gemv(const WDesc& w, const void* x, int64_t M, void* y, cudaStr
 #undef QM_GEMV_CASE
 done:
     if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
+    return QM_OK;
+}
+
+// ---------------------------------------------------------------- grouped (apply_experts)
+// Chunks of Q routed positions of one expert, each a decode product over that
+// expert's [n, k] matrix. The chunk list lives on the device (the routing
+// offsets), so the grid covers the most chunks P positions can make; slots
+// past the last chunk exit at once.
+namespace gemv {
+
+static int grouped_q(int64_t P, int64_t E) { return P <= 8 * E ? 8 : 16; }
+
+static bool grouped_plan(const WDesc& w, int64_t P, Plan* out, int64_t* slots) {
+    const int64_t E = w.shape[0];
+    if (w.ndim != 3 || E < 1 || P < 1 || E * w.n >= (int64_t(1) << 31)) return false;
+    if ((w.n * w.scale_row_bytes) % 16) return false;  // each expert's scales start 16-byte aligned
+    const int Q = grouped_q(P, E);
+    *slots = std::min<int64_t>(P, P / Q + E);  // sum over experts of ceil(count / Q) is below P/Q + E
+    // chunks expected when ids spread evenly: every expert used, about half a chunk extra each
+    const int64_t est = std::max<int64_t>(1, std::min<int64_t>(*slots, (P + Q - 1) / Q + std::min(E, P) / 2));
+    *out = make_plan(w, Q, 1.0 / static_cast<double>(est));
+    return out->ok;
+}
+
+}  // namespace gemv
+
+bool gemv_grouped_supported(const WDesc& w, int64_t P) {
+    gemv::Plan pl;
+    int64_t slots = 0;
+    return gemv::grouped_plan(w, P, &pl, &slots);
+}
+
+qm_status launch_gemv_grouped(const WDesc& w, const int32_t* offsets, const int32_t* perm, int64_t P,
+                              int xdiv, const void* x, void* y, cudaStream_t st) {
+    using namespace gemv;
+    Plan pl;
+    int64_t slots = 0;
+    if (!grouped_plan(w, P, &pl, &slots)) return fail(QM_ENOTSUP, "w: no grouped decode plan for this shape");
+    const int64_t E = w.shape[0];
+    const int Q = grouped_q(P, E);
+    Params& p = pl.p;
+    p.codes = w.codes;
+    p.scales = w.scales;
+    p.biases = w.biases;
+    p.x = static_cast<const uint16_t*>(x);
+    p.y = static_cast<uint16_t*>(y);
+    p.n = w.n;
+    p.k = w.k;
+    p.M = Q;
+    p.sdt = w.sdt;
+    p.code_row_bytes = w.code_row_bytes;
+    p.scale_row_bytes = w.scale_row_bytes;
+    p.static_w = 0;
+    p.g_off = offsets;
+    p.g_perm = perm;
+    p.g_E = E;
+    p.g_Q = Q;
+    p.g_xdiv = xdiv;
+    p.g_wclusters = pl.grid / pl.S;
+    const int64_t rows = E * w.n;
+    bool maps = make_tmap_2d(&p.tm_codes, w.codes, w.code_row_bytes, rows, w.code_row_bytes, 128, kRows, true);
+    if (maps && p.S > 1 && p.scale_seg) {
+        maps = make_tmap_2d(&p.tm_scales, w.scales, w.scale_row_bytes, rows, w.scale_row_bytes, p.scale_seg,
+                            kRows, false);
+        if (maps && w.biases)
+            maps = make_tmap_2d(&p.tm_biases, w.biases, w.scale_row_bytes, rows, w.scale_row_bytes, p.scale_seg,
+                                kRows, false);
+    }
+    if (!maps) return fail(QM_ENOTSUP, "w: no tensor map for the grouped decode product");
+    if (pl.grid * slots >= (int64_t(1) << 31)) return fail(QM_ENOTSUP, "ids: too many positions for one launch");
+    pl.grid *= slots;
+    const bool two = Q > 8;
+    cudaError_t e = cudaErrorInvalidValue;
+#define QM_GEMV_CASE(F, B, G)                                                                  \
+    if (w.fmt == F && (F != QM_AFFINE || (w.bits == B && w.gs == G))) {                         \
+        e = two ? launch_t<F, B, G, 2>(pl, st) : launch_t<F, B, G, 1>(pl, st);                 \
+        goto done;                                                                             \
+    }
+    QM_GEMV_CASE(QM_AFFINE, 4, 32)
+    QM_GEMV_CASE(QM_AFFINE, 4, 64)
+    QM_GEMV_CASE(QM_AFFINE, 4, 128)
+    QM_GEMV_CASE(QM_AFFINE, 8, 32)
+    QM_GEMV_CASE(QM_AFFINE, 8, 64)
+    QM_GEMV_CASE(QM_AFFINE, 8, 128)
+    QM_GEMV_CASE(QM_Q8_0, 8, 32)
+    QM_GEMV_CASE(QM_MXFP4, 4, 32)
+#undef QM_GEMV_CASE
+done:
+    if (e != cudaSuccess) return cuda_fail(e, "grouped gemv launch");
     return QM_OK;
 }
 

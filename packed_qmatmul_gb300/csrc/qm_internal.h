@@ -64,6 +64,12 @@ cudaError_t launch_take_dense(const WDesc& w, int axis, const void* ids, int id6
 // y [M, n] = x [M, k] * W^T for a 2-d weight, M <= 16, x and y bf16.
 qm_status launch_gemv(const WDesc& w, const void* x, int64_t M, void* y, cudaStream_t st);
 bool gemv_supported(const WDesc& w, int64_t M);
+// Grouped decode product over a weight [E, n, k]: chunks of routed positions
+// (offsets [E+1] and perm from the routing step, on the device), activation
+// row of position q is q / xdiv; y [P, n] by position.
+qm_status launch_gemv_grouped(const WDesc& w, const int32_t* offsets, const int32_t* perm, int64_t P,
+                              int xdiv, const void* x, void* y, cudaStream_t st);
+bool gemv_grouped_supported(const WDesc& w, int64_t P);
 // Tensor-core product for larger M (tcgen05); returns QM_ENOTSUP if the
 // shape is outside what the kernel handles.
 qm_status launch_gemm(const WDesc& w, const void* x, int64_t M, void* y, cudaStream_t st);
@@ -75,7 +81,8 @@ cudaError_t launch_apply_simple(const WDesc& w, const void* x, int64_t M, void* 
 // Experts.
 size_t experts_workspace_bytes(int64_t P, int64_t E);
 cudaError_t launch_route(const void* ids, int id64, int64_t P, int64_t E, int32_t* counts,
-                         int32_t* offsets, int32_t* perm, void* ws, cudaStream_t st);
+                         int32_t* offsets, int32_t* perm, void* ws, cudaStream_t st,
+                         uint16_t* zero_y = nullptr, int64_t zero_n = 0);
 qm_status launch_experts(const WDesc& w, const void* ids, int id64, int64_t T, int64_t topk,
                          const void* x, int64_t x_rows, void* y, void* ws, size_t ws_bytes,
                          cudaStream_t st);

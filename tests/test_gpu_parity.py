@@ -292,6 +292,96 @@ def test_apply_experts_small(kind, broadcast):
     assert np.all(np.isnan(got[nanrows]))
 
 
+def _check_experts(w, ids, x, what):
+    """y of apply_experts against the oracle: zeros out of range, the product
+    tolerance per in-range row; returns the device result [P, n] as float64."""
+    E, n, k = w["shape"]
+    T, topk = ids.shape
+    ow = to_oracle(w)
+    y = qm.apply_experts(qm.QWeight.from_arrays(w), torch.from_numpy(ids).cuda(), _dev_bf16(x))
+    got = bf16_to_f64(_host(y)).reshape(T * topk, n)
+    ref = oracle.apply_experts(ow, ids, x).reshape(T * topk, n)
+    flat = ids.reshape(-1)
+    out = (flat < 0) | (flat >= E)
+    assert np.all(got[out] == 0) and not np.any(np.signbit(got[out])), what
+    rows = np.where(~out)[0]
+    xr = rows // topk if x.shape[0] == T else rows
+    xn = np.linalg.norm(oracle.decode_array(x, oracle.BF16), axis=1)[xr]
+    wn = row_norms(ow).reshape(E, n)[flat[rows]]
+    for i, r in enumerate(rows):
+        check_product(got[r:r + 1], ref[r:r + 1], wn[i], xn[i:i + 1], k, f"{what} position {r}")
+    return got
+
+
+@pytest.mark.parametrize("kind", KINDS)
+def test_apply_experts_chunks(kind):
+    # experts with many positions (several chunks), empty experts, positions
+    # out of range, per-token and per-position activations
+    g = synth.rng(910)
+    E, n, k = 6, 100, 512
+    w = _make(kind, g, n, k, lead=(E,))
+    T, topk = 24, 2
+    ids = synth.expert_ids(g, T, topk, E)
+    ids[:, 0] = 2           # expert 2: 24+ positions, more than one chunk
+    ids[:, 1] = np.where(ids[:, 1] == 2, 5, ids[:, 1])
+    ids[ids == 4] = 3       # expert 4 empty
+    ids[3, 1] = -7
+    ids[9, 1] = E
+    for rows in (T, T * topk):
+        x = synth.activations(g, rows, k)
+        _check_experts(w, ids, x, f"{kind} x_rows={rows}")
+
+
+def test_apply_experts_all_out_of_range():
+    g = synth.rng(920)
+    w = _make("mxfp4", g, 64, 256, lead=(4,))
+    ids = np.full((5, 2), 9, dtype=np.int32)
+    ids[0, 0] = -1
+    y = qm.apply_experts(qm.QWeight.from_arrays(w), torch.from_numpy(ids).cuda(),
+                         _dev_bf16(synth.activations(g, 5, 256)))
+    h = _host(y)
+    assert np.all(h.view(np.uint16) == 0)
+
+
+def test_apply_experts_rows_independent_of_other_experts():
+    # a row's bits depend on its own row and expert only
+    g = synth.rng(930)
+    E, n, k, T, topk = 8, 96, 512, 16, 2
+    w = _make("affine4_g64", g, n, k, lead=(E,))
+    qw = qm.QWeight.from_arrays(w)
+    x = _dev_bf16(synth.activations(g, T, k))
+    ids1 = synth.expert_ids(g, T, topk, E)
+    ids2 = ids1.copy()
+    ids2[::3, 1] = (ids2[::3, 1] + 3) % E
+    ids2[ids2[:, 0] == ids2[:, 1], 1] = (ids2[ids2[:, 0] == ids2[:, 1], 1] + 1) % E
+    y1 = _host(qm.apply_experts(qw, torch.from_numpy(ids1).cuda(), x)).reshape(T * topk, n)
+    y2 = _host(qm.apply_experts(qw, torch.from_numpy(ids2).cuda(), x)).reshape(T * topk, n)
+    same = (ids1 == ids2).reshape(-1)
+    assert same.sum() > 0 and (~same).sum() > 0
+    assert np.array_equal(y1[same].view(np.uint16), y2[same].view(np.uint16))
+
+
+def test_apply_experts_moe_shape_t64_sampled():
+    # 32 MXFP4 experts [5760, 2880], 64 tokens x 4: every output row of a
+    # sample of positions against the oracle
+    w, ids, x = synth.moe_config(64)
+    E, n, k = w["shape"]
+    T, topk = ids.shape
+    ow = to_oracle(w)
+    y = qm.apply_experts(qm.QWeight.from_arrays(w), torch.from_numpy(ids).cuda(), _dev_bf16(x))
+    got = bf16_to_f64(_host(y)).reshape(T * topk, n)
+    pos = np.sort(synth.rng(940).choice(T * topk, size=16, replace=False))
+    sub_ids = ids.reshape(-1)[pos].reshape(-1, 1).astype(np.int32)
+    sub_x = x[pos // topk]
+    ref = oracle.apply_experts(ow, sub_ids, sub_x).reshape(len(pos), n)
+    xn = np.linalg.norm(oracle.decode_array(sub_x, oracle.BF16), axis=1)
+    used = np.unique(sub_ids[:, 0])
+    sub_w = dict(w, shape=(len(used), n, k), codes=w["codes"][used], scales=w["scales"][used])
+    wn = row_norms(to_oracle(sub_w)).reshape(len(used), n)[np.searchsorted(used, sub_ids[:, 0])]
+    for i, r in enumerate(pos):
+        check_product(got[r:r + 1], ref[i:i + 1], wn[i], xn[i:i + 1], k, f"moe T=64 position {r}")
+
+
 # ---------------------------------------------------------------- long pipelines
 @pytest.mark.parametrize("kind,n,k", [("affine4_g64", 40000, 1024), ("affine8_g32", 20000, 512),
                                       ("q8_0", 12000, 1024), ("mxfp4", 30000, 256)])
