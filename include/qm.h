@@ -115,9 +115,16 @@ qm_status qm_take(const qm_weight* w, int32_t axis, const void* ids, int32_t id_
                   int64_t n_ids, void* out_codes, void* out_scales, void* out_biases,
                   int32_t out_dtype, void* out_dense, qm_stream_t stream);
 
-/* Bytes of device workspace qm_apply_experts and qm_experts_route need for
- * T*topk positions over E experts (a multiple of 256; 0 only if T*topk = 0). */
-size_t qm_apply_experts_workspace(int64_t T, int64_t topk, int64_t E);
+/* Bytes of device workspace qm_apply_experts needs for weight w [E, n, k]
+ * and T*topk positions (a multiple of 256; 0 if T*topk = 0 or w is not a
+ * valid 3-d weight). It holds the routing tables and, where the experts
+ * average more than 32 positions each, the routed activation rows (T*topk*k
+ * bf16) that the tensor-core path reads. */
+size_t qm_apply_experts_workspace(const qm_weight* w, int64_t T, int64_t topk);
+
+/* Bytes of device workspace qm_experts_route needs for P positions over E
+ * experts (a multiple of 256; 0 only if P = 0). */
+size_t qm_experts_route_workspace(int64_t P, int64_t E);
 
 /* apply_experts: for a weight [E, n, k] and ids [T, topk], y [T, topk, n]
  * holds, at each position p = t*topk + j, the product of expert ids[p]'s
@@ -125,8 +132,12 @@ size_t qm_apply_experts_workspace(int64_t T, int64_t topk, int64_t E);
  * that row holds. x is [x_rows, k] bf16 with x_rows = T (row t serves all topk
  * positions of token t) or T*topk (one row per position). The positions are
  * routed (a stable sort by expert) into `workspace`, then summed in one
- * segmented product. A row's bits depend on the shapes, its row and its
- * expert, never on the other positions' experts.
+ * segmented product: chunks of up to 16 positions of one expert through the
+ * decode kernel where experts average at most 32 positions, else the routed
+ * rows gathered expert by expert into `workspace` and multiplied on the tensor
+ * cores. The path follows from the shapes alone, so a row's bits depend on the
+ * shapes, its row and its expert, never on the other positions' experts.
+ * workspace_bytes must be at least qm_apply_experts_workspace(w, T, topk).
  * Defined by "Nx_quant (raven-ml.dev API docs)", section "Products",
  * apply_experts. */
 qm_status qm_apply_experts(const qm_weight* w, const void* ids, int32_t id_type, int64_t T,
@@ -143,8 +154,12 @@ qm_status qm_apply_experts(const qm_weight* w, const void* ids, int32_t id_type,
  * array's device address, so make the first call on each device before any
  * stream capture. All calls share the one array: calls that may overlap on the
  * GPU (other streams, other host threads) race, so serialize them. Nothing in
- * the array needs clearing between calls. Otherwise identical to
- * qm_apply_experts; the pages have no counterpart to this entry point. */
+ * the array needs clearing between calls. The array holds no gathered
+ * activations, so this entry point always takes the decode path; where
+ * qm_apply_experts would use the tensor cores (experts averaging more than 32
+ * positions) the two agree within the product's error bound, not bit for bit.
+ * Otherwise identical to qm_apply_experts; the pages have no counterpart to
+ * this entry point. */
 qm_status qm_apply_experts_static(const qm_weight* w, const void* ids, int32_t id_type, int64_t T,
                                   int64_t topk, const void* x, int64_t x_rows, int32_t x_dtype,
                                   void* y, qm_stream_t stream);
@@ -154,8 +169,7 @@ qm_status qm_apply_experts_static(const qm_weight* w, const void* ids, int32_t i
  * sum; offsets[E] = positions in range) and perm[P]: first the in-range
  * positions by ascending expert, ties by ascending position, then (from
  * offsets[E] on) the out-of-range positions in ascending order. All three are
- * int32 device buffers; workspace is qm_apply_experts_workspace(P, 1, E)
- * bytes. */
+ * int32 device buffers; workspace is qm_experts_route_workspace(P, E) bytes. */
 qm_status qm_experts_route(const void* ids, int32_t id_type, int64_t P, int64_t E,
                            int32_t* counts, int32_t* offsets, int32_t* perm, void* workspace,
                            size_t workspace_bytes, qm_stream_t stream);

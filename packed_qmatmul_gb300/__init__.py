@@ -23,6 +23,7 @@ __all__ = [
     "QM_AFFINE", "QM_Q8_0", "QM_MXFP4", "QM_WEIGHT_STATIC", "QM_F32", "QM_BF16", "QM_F16", "QM_I32", "QM_I64",
     "QMError", "QWeight", "library_path", "load_library",
     "qm_dequant", "qm_apply", "qm_take", "qm_apply_experts", "qm_apply_experts_workspace",
+    "qm_experts_route_workspace",
     "qm_experts_route", "qm_apply_experts_static", "qm_device_status", "qm_last_error", "qm_version",
     "dequant", "apply", "take", "apply_experts", "route",
 ]
@@ -82,7 +83,8 @@ def load_library():
             "qm_dequant": ([wp, i32, vp, vp], i32),
             "qm_apply": ([wp, vp, i64, i32, vp, vp], i32),
             "qm_take": ([wp, i32, vp, i32, i64, vp, vp, vp, i32, vp, vp], i32),
-            "qm_apply_experts_workspace": ([i64, i64, i64], sz),
+            "qm_apply_experts_workspace": ([wp, i64, i64], sz),
+            "qm_experts_route_workspace": ([i64, i64], sz),
             "qm_apply_experts": ([wp, vp, i32, i64, i64, vp, i64, i32, vp, vp, sz, vp], i32),
             "qm_experts_route": ([vp, i32, i64, i64, vp, vp, vp, vp, sz, vp], i32),
             "qm_apply_experts_static": ([wp, vp, i32, i64, i64, vp, i64, i32, vp, vp], i32),
@@ -208,8 +210,12 @@ def qm_take(w: QWeight, axis: int, ids: torch.Tensor, out_codes=None, out_scales
                                   _ptr(out_dense), _stream(stream)))
 
 
-def qm_apply_experts_workspace(T: int, topk: int, E: int) -> int:
-    return load_library().qm_apply_experts_workspace(T, topk, E)
+def qm_apply_experts_workspace(w: QWeight, T: int, topk: int) -> int:
+    return load_library().qm_apply_experts_workspace(ctypes.byref(w._c()), T, topk)
+
+
+def qm_experts_route_workspace(P: int, E: int) -> int:
+    return load_library().qm_experts_route_workspace(P, E)
 
 
 def qm_apply_experts(w: QWeight, ids: torch.Tensor, x: torch.Tensor, y: torch.Tensor,
@@ -278,7 +284,7 @@ def take(w: QWeight, axis: int, ids: torch.Tensor, dense_dtype=None, packed=True
 def apply_experts(w: QWeight, ids: torch.Tensor, x: torch.Tensor, stream=None) -> torch.Tensor:
     T, topk = ids.shape
     y = torch.empty((T, topk, w.shape[-2]), dtype=x.dtype, device=x.device)
-    ws = torch.empty(max(qm_apply_experts_workspace(T, topk, w.shape[0]), 256), dtype=torch.uint8,
+    ws = torch.empty(max(qm_apply_experts_workspace(w, T, topk), 256), dtype=torch.uint8,
                      device=x.device)
     qm_apply_experts(w, ids, x, y, ws, stream)
     return y
@@ -290,6 +296,6 @@ def route(ids: torch.Tensor, E: int, stream=None):
     counts = torch.empty(max(E, 1), dtype=torch.int32, device=dev)
     offsets = torch.empty(E + 1, dtype=torch.int32, device=dev)
     perm = torch.empty(max(P, 1), dtype=torch.int32, device=dev)
-    ws = torch.empty(max(qm_apply_experts_workspace(P, 1, E), 256), dtype=torch.uint8, device=dev)
+    ws = torch.empty(max(qm_experts_route_workspace(P, E), 256), dtype=torch.uint8, device=dev)
     qm_experts_route(ids, E, counts, offsets, perm, ws, stream)
     return counts[:E], offsets, perm[:P]

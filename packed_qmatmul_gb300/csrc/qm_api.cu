@@ -303,14 +303,31 @@ qm_status qm_take(const qm_weight* w, int32_t axis, const void* ids, int32_t id_
     return QM_OK;
 }
 
-size_t qm_apply_experts_workspace(int64_t T, int64_t topk, int64_t E) {
-    if (T <= 0 || topk <= 0 || E < 0) return 0;
-    return experts_workspace_bytes(T * topk, E);
+size_t qm_apply_experts_workspace(const qm_weight* w, int64_t T, int64_t topk) {
+    set_error("");
+    WDesc d;
+    if (validate_weight(w, &d) != QM_OK || d.ndim != 3 || T <= 0 || topk <= 0) return 0;
+    return experts_workspace_bytes(d, T * topk, true);
+}
+
+size_t qm_experts_route_workspace(int64_t P, int64_t E) {
+    if (P <= 0 || E < 0) return 0;
+    return route_workspace_bytes(P, E);
 }
 
 qm_status qm_apply_experts(const qm_weight* w, const void* ids, int32_t id_type, int64_t T,
                            int64_t topk, const void* x, int64_t x_rows, int32_t x_dtype, void* y,
                            void* workspace, size_t workspace_bytes, qm_stream_t stream) {
+    return apply_experts_checked(w, ids, id_type, T, topk, x, x_rows, x_dtype, y, workspace,
+                                 workspace_bytes, stream, true);
+}
+
+}  // extern "C"
+
+qm_status qm::apply_experts_checked(const qm_weight* w, const void* ids, int32_t id_type, int64_t T,
+                                    int64_t topk, const void* x, int64_t x_rows, int32_t x_dtype, void* y,
+                                    void* workspace, size_t workspace_bytes, qm_stream_t stream,
+                                    bool allow_tensor) {
     set_error("");
     WDesc d;
     qm_status s = validate_weight(w, &d);
@@ -333,13 +350,15 @@ qm_status qm_apply_experts(const qm_weight* w, const void* ids, int32_t id_type,
         return check_launch(cudaMemsetAsync(y, 0, static_cast<size_t>(P * d.n * 2), st), "experts memset");
     if (!x) return fail(QM_EINVAL, "x: NULL");
     if (!aligned16(x)) return fail(QM_EINVAL, "x: base address must be 16-byte aligned");
-    const size_t need = experts_workspace_bytes(P, d.shape[0]);
+    const size_t need = experts_workspace_bytes(d, P, allow_tensor);
     if (!workspace || workspace_bytes < need)
         return fail(QM_EINVAL, "workspace: needs " + std::to_string(need) + " bytes");
     if (!aligned16(workspace)) return fail(QM_EINVAL, "workspace: must be 16-byte aligned");
     return launch_experts(d, ids, id_type == QM_I64, T, topk, x, x_rows, y, workspace,
-                          workspace_bytes, st);
+                          workspace_bytes, st, allow_tensor);
 }
+
+extern "C" {
 
 qm_status qm_experts_route(const void* ids, int32_t id_type, int64_t P, int64_t E,
                            int32_t* counts, int32_t* offsets, int32_t* perm, void* workspace,
@@ -350,7 +369,7 @@ qm_status qm_experts_route(const void* ids, int32_t id_type, int64_t P, int64_t 
     if (P > std::numeric_limits<int32_t>::max()) return fail(QM_EINVAL, "ids: more than 2^31-1 positions");
     if (!counts || !offsets) return fail(QM_EINVAL, "out: counts and offsets are required");
     if (P > 0 && (!ids || !perm)) return fail(QM_EINVAL, "ids: NULL");
-    const size_t need = experts_workspace_bytes(P, E);
+    const size_t need = route_workspace_bytes(P, E);
     if (P > 0 && (!workspace || workspace_bytes < need))
         return fail(QM_EINVAL, "workspace: needs " + std::to_string(need) + " bytes");
     return check_launch(launch_route(ids, id_type == QM_I64, P, E, counts, offsets, perm, workspace,

@@ -38,20 +38,50 @@ QM_DEV int64_t load_id(const void* ids, int id64, int64_t p) {
 
 size_t round256(size_t v) { return (v + 255) / 256 * 256; }
 
-// Workspace layout for P positions over E experts.
+// Workspace layout for P positions over E experts, plus `xs_bytes` for the
+// routed activation rows where the tensor-core path takes them.
 struct WsLayout {
-    size_t counts, offsets, perm, chunk_counts, total;
+    size_t counts, offsets, perm, chunk_counts, xs, total;
 };
 
-WsLayout ws_layout(int64_t P, int64_t E) {
+WsLayout ws_layout(int64_t P, int64_t E, size_t xs_bytes = 0) {
     WsLayout l;
     const int64_t nchunks = (P + kChunk - 1) / kChunk;
     l.counts = 0;
     l.offsets = round256(static_cast<size_t>(E) * 4);
     l.perm = l.offsets + round256(static_cast<size_t>(E + 1) * 4);
     l.chunk_counts = l.perm + round256(static_cast<size_t>(P) * 4);
-    l.total = l.chunk_counts + round256(static_cast<size_t>(nchunks) * E * 4);
+    l.xs = l.chunk_counts + round256(static_cast<size_t>(nchunks) * E * 4);
+    l.total = l.xs + round256(xs_bytes);
     return l;
+}
+
+// How the segmented product runs, from the shapes alone (never from the ids,
+// so a row's bits cannot depend on the other positions' experts).
+enum class Path { kSimple, kDecode, kTensor };
+
+Path experts_path(const WDesc& w, int64_t P, bool allow_tensor) {
+    const int64_t E = w.shape[0];
+    const bool decode = gemv_grouped_supported(w, P);
+    if (decode && P <= 32 * E) return Path::kDecode;   // few positions per expert: HBM-bound
+    if (allow_tensor && gemm_grouped_supported(w, P)) return Path::kTensor;
+    return decode ? Path::kDecode : Path::kSimple;
+}
+
+// Routed activation rows: xs[i] = x[perm[i] / xdiv] for the n_in = offsets[E]
+// positions in range, one warp per row in 16-byte pieces.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const int32_t* n_in_p, const int32_t* perm, int xdiv,
+                                                          const uint4* x, int64_t row_vecs, uint4* xs) {
+    grid_dependency_wait();
+    const int64_t n_in = *n_in_p;
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; i < n_in; i += nw) {
+        const int64_t src = __ldg(perm + i) / xdiv;
+        const uint4* a = x + src * row_vecs;
+        uint4* b = xs + i * row_vecs;
+        for (int64_t v = lane; v < row_vecs; v += 32) b[v] = __ldg(a + v);
+    }
 }
 
 // Per-chunk histogram of in-range ids: chunk_counts[chunk][e].
@@ -223,9 +253,15 @@ __global__ void __launch_bounds__(256) experts_simple_kernel(ExpArgs a, const vo
 
 }  // namespace
 
-size_t experts_workspace_bytes(int64_t P, int64_t E) {
+size_t route_workspace_bytes(int64_t P, int64_t E) {
     if (P <= 0) return 0;
     return ws_layout(P, E).total;
+}
+
+size_t experts_workspace_bytes(const WDesc& w, int64_t P, bool allow_tensor) {
+    if (P <= 0) return 0;
+    const bool tensor = experts_path(w, P, allow_tensor) == Path::kTensor;
+    return ws_layout(P, w.shape[0], tensor ? static_cast<size_t>(P) * w.k * 2 : 0).total;
 }
 
 cudaError_t launch_route(const void* ids, int id64, int64_t P, int64_t E, int32_t* counts,
@@ -238,7 +274,7 @@ cudaError_t launch_route(const void* ids, int id64, int64_t P, int64_t E, int32_
         }
         return cudaMemsetAsync(offsets, 0, (E + 1) * 4, st);
     }
-    const WsLayout l = ws_layout(P, E);
+    const WsLayout l = ws_layout(P, E);  // the routing part comes first whatever follows
     int32_t* chunk_counts = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(ws) + l.chunk_counts);
     const int64_t nchunks = (P + kChunk - 1) / kChunk;
     const size_t sm1 = static_cast<size_t>(E) * 4, sm2 = static_cast<size_t>(E + 1) * 8;
@@ -254,20 +290,30 @@ cudaError_t launch_route(const void* ids, int id64, int64_t P, int64_t E, int32_
 
 qm_status launch_experts(const WDesc& w, const void* ids, int id64, int64_t T, int64_t topk,
                          const void* x, int64_t x_rows, void* y, void* ws, size_t ws_bytes,
-                         cudaStream_t st) {
+                         cudaStream_t st, bool allow_tensor) {
     (void)ws_bytes;
     const int64_t P = T * topk, E = w.shape[0];
-    const WsLayout l = ws_layout(P, E);
+    const Path path = experts_path(w, P, allow_tensor);
+    const WsLayout l = ws_layout(P, E, path == Path::kTensor ? static_cast<size_t>(P) * w.k * 2 : 0);
     uint8_t* wb = static_cast<uint8_t*>(ws);
     int32_t* counts = reinterpret_cast<int32_t*>(wb + l.counts);
     int32_t* offsets = reinterpret_cast<int32_t*>(wb + l.offsets);
     int32_t* perm = reinterpret_cast<int32_t*>(wb + l.perm);
-    const bool grouped = P <= 32 * E && gemv_grouped_supported(w, P);
+    const int xdiv = x_rows == T ? static_cast<int>(topk) : 1;
     cudaError_t e = launch_route(ids, id64, P, E, counts, offsets, perm, ws, st,
-                                 grouped ? static_cast<uint16_t*>(y) : nullptr, w.n);
+                                 path != Path::kSimple ? static_cast<uint16_t*>(y) : nullptr, w.n);
     if (e != cudaSuccess) return cuda_fail(e, "route launch");
-    if (grouped)  // experts averaging few positions: chunks through the decode product
-        return launch_gemv_grouped(w, offsets, perm, P, x_rows == T ? static_cast<int>(topk) : 1, x, y, st);
+    if (path == Path::kDecode)  // experts averaging few positions: chunks through the decode product
+        return launch_gemv_grouped(w, offsets, perm, P, xdiv, x, y, st);
+    if (path == Path::kTensor) {  // routed rows gathered expert by expert, then the tensor-core product
+        uint4* xs = reinterpret_cast<uint4*>(wb + l.xs);
+        const int64_t blocks = std::min<int64_t>((P + 7) / 8, int64_t(num_sms()) * 8);
+        gather_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
+            offsets + E, perm, xdiv, static_cast<const uint4*>(x), w.k * 2 / 16, xs);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "gather launch");
+        return launch_gemm_grouped(w, offsets, perm, P, xs, y, st);
+    }
     ExpArgs a{w.codes, w.scales, w.biases, E, w.n, w.k, w.code_row_bytes, w.scale_row_bytes, w.gs, w.sdt};
     const int64_t jobs = P * w.n;
     const int64_t blocks = std::min<int64_t>((jobs * 32 + 255) / 256, int64_t(num_sms()) * 8);
@@ -326,7 +372,7 @@ extern "C" qm_status qm_apply_experts_static(const qm_weight* w, const void* ids
     using namespace qm;
     set_error("");
     if (w && w->ndim == 3 && T > 0 && topk > 0 && w->shape[0] >= 0) {
-        const size_t need = experts_workspace_bytes(T * topk, w->shape[0]);
+        const size_t need = route_workspace_bytes(T * topk, w->shape[0]);
         if (need > kStaticScratchBytes)
             return fail(QM_EINVAL, "workspace: " + std::to_string(T * topk) + " positions over " +
                                        std::to_string(w->shape[0]) + " experts need " + std::to_string(need) +
@@ -338,6 +384,6 @@ extern "C" qm_status qm_apply_experts_static(const qm_weight* w, const void* ids
     if (e != cudaSuccess) return cuda_fail(e, "static scratch address");
     // Every entry of the routing tables is written before it is read, so the
     // array needs no clearing between calls.
-    return qm_apply_experts(w, ids, id_type, T, topk, x, x_rows, x_dtype, y, scratch, kStaticScratchBytes,
-                            stream);
+    return apply_experts_checked(w, ids, id_type, T, topk, x, x_rows, x_dtype, y, scratch, kStaticScratchBytes,
+                                 stream, /*allow_tensor=*/false);
 }

@@ -71,6 +71,12 @@ struct Params {
     int sdt;
     int ksteps, mtiles;
     uint32_t off_x, off_b, off_raw, raw_stage_bytes;
+    // grouped mode (apply_experts), off when g_off is null: x holds the routed
+    // activation rows expert by expert, the weight is [E, n, k], and m tile
+    // slot t is the t-th BM-row tile of the experts' row ranges in order
+    const int32_t* g_off;   // [E + 1] each expert's first row of x
+    const int32_t* g_perm;  // row of x -> row of y
+    int64_t g_E;
 };
 
 // Where 16-byte chunk c of row r of a 128B-swizzled, 128-byte-row tile sits.
@@ -187,7 +193,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int mt = blockIdx.x % p.mtiles, nt = blockIdx.x / p.mtiles;
-    const int64_t m0 = static_cast<int64_t>(mt) * BM, n0 = static_cast<int64_t>(nt) * BN;
+    int64_t m0 = static_cast<int64_t>(mt) * BM, mend = p.M;  // this tile's rows of x: [m0, min(m0 + BM, mend))
+    int64_t wrow0 = 0;                                       // first row of the tile's matrix in the weight
+    const int64_t n0 = static_cast<int64_t>(nt) * BN;
     const int ks_n = p.ksteps;
     const int nchunks = (ks_n + R::SPR - 1) / R::SPR;
 
@@ -202,6 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     const uint32_t done = b0 + 8 * (2 * NX + 2 * NB + 2 * NR);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 8 * (2 * NX + 2 * NB + 2 * NR + 1));
     volatile int& s_abort = *reinterpret_cast<volatile int*>(smem + 8 * (2 * NX + 2 * NB + 2 * NR + 2));
+    int* s_grp = reinterpret_cast<int*>(smem + 8 * (2 * NX + 2 * NB + 2 * NR + 3));  // [4], below 1 KB
 
     if (threadIdx.x == 0) {
         s_abort = 0;
@@ -212,6 +221,53 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         fence_mbar_init();
         prefetch_tmap(&p.tm_x);
         prefetch_tmap(&p.tm_raw);
+    }
+    if (p.g_off) {
+        // which expert's rows: the routing offsets come from an earlier kernel
+        if (warp == 0) {
+            grid_dependency_wait();
+            int64_t before = 0;  // tiles of the experts already passed
+            int found = 0, ge = 0, gm0 = 0, gend = 0;
+            for (int64_t e0 = 0; e0 < p.g_E; e0 += 32) {
+                const int64_t e = e0 + lane;
+                int o0 = 0, cnt = 0;
+                if (e < p.g_E) {
+                    o0 = __ldg(p.g_off + e);
+                    cnt = __ldg(p.g_off + e + 1) - o0;
+                }
+                const int64_t nch = (cnt + BM - 1) / BM;
+                int64_t inc = nch;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const int64_t t = __shfl_up_sync(0xffffffffu, inc, o);
+                    if (lane >= o) inc += t;
+                }
+                const int64_t lo = before + inc - nch;
+                const bool mine = e < p.g_E && mt >= lo && mt < lo + nch;
+                const uint32_t hit = __ballot_sync(0xffffffffu, mine);
+                if (mine) {
+                    found = 1;
+                    ge = static_cast<int>(e);
+                    gm0 = o0 + static_cast<int>(mt - lo) * BM;
+                    gend = o0 + cnt;
+                }
+                if (hit) {
+                    const int src = __ffs(hit) - 1;
+                    found = __shfl_sync(0xffffffffu, found, src);
+                    ge = __shfl_sync(0xffffffffu, ge, src);
+                    gm0 = __shfl_sync(0xffffffffu, gm0, src);
+                    gend = __shfl_sync(0xffffffffu, gend, src);
+                    break;
+                }
+                before += __shfl_sync(0xffffffffu, inc, 31);
+            }
+            if (lane == 0) { s_grp[0] = found; s_grp[1] = ge; s_grp[2] = gm0; s_grp[3] = gend; }
+        }
+        __syncthreads();
+        if (!s_grp[0]) return;  // a slot past the last tile: nothing allocated yet
+        wrow0 = static_cast<int64_t>(s_grp[1]) * p.n;
+        m0 = s_grp[2];
+        mend = s_grp[3];
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(tmem_slot), kTmemCols);
@@ -239,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                     if (!mbar_wait(r_empty(sr), ((rc / NR) & 1) ^ 1)) { give_up(); break; }
                     mbar_expect_tx(r_full(sr), R::BYTES * BN);
                     tma_load_2d(smem_u32(smem + p.off_raw + sr * p.raw_stage_bytes), &p.tm_raw,
-                                rc * R::BYTES / R::ELEM, static_cast<int32_t>(n0), r_full(sr));
+                                rc * R::BYTES / R::ELEM, static_cast<int32_t>(wrow0 + n0), r_full(sr));
                     mbar_arrive(r_full(sr));
                     last_r = rc;
                 }
@@ -292,7 +348,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         auto fetch = [&](int rc, Sc (&dst)[R::SPR]) {
 #pragma unroll
             for (int kk = 0; kk < R::SPR; ++kk)
-                dst[kk] = rowok ? load_scale<FMT, BITS, GS>(p, grow, static_cast<int64_t>(rc) * R::RAWK + kk * BK + half * 32)
+                dst[kk] = rowok ? load_scale<FMT, BITS, GS>(p, wrow0 + grow, static_cast<int64_t>(rc) * R::RAWK + kk * BK + half * 32)
                                 : Sc{0.0f, 0.0f};
         };
         fetch(0, cur);
@@ -348,8 +404,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             tmem_ld32(tmem + (static_cast<uint32_t>(32 * quarter) << 16) + col, r);
             tmem_wait_ld();
             const int64_t m = m0 + 128 * acc + 32 * quarter + lane;
-            if (!ok || s_abort || m >= p.M) continue;
-            uint16_t* yr = p.y + m * p.n + n0 + c0;
+            if (!ok || s_abort || m >= mend) continue;
+            const int64_t ym = p.g_off ? static_cast<int64_t>(__ldg(p.g_perm + m)) : m;
+            uint16_t* yr = p.y + ym * p.n + n0 + c0;
             const int64_t left = p.n - (n0 + c0);
             if (left >= 32 && (p.n & 7) == 0) {
 #pragma unroll
@@ -382,7 +439,8 @@ template <int FMT, int BITS, int GS, int BM>
 static cudaError_t launch_t(Params& p, const WDesc& w, const void* x, cudaStream_t st) {
     using R = Raw<FMT, BITS>;
     constexpr int NX = NXof(BM);
-    p.mtiles = static_cast<int>((p.M + BM - 1) / BM);
+    p.mtiles = p.g_off ? static_cast<int>(std::min<int64_t>(p.M, p.M / BM + p.g_E))  // sum of ceil(count / BM)
+                       : static_cast<int>((p.M + BM - 1) / BM);
     p.off_x = 1024;
     p.off_b = p.off_x + NX * BM * BK * 2;
     p.off_raw = p.off_b + NB * kBTileBytes;
@@ -390,7 +448,7 @@ static cudaError_t launch_t(Params& p, const WDesc& w, const void* x, cudaStream
     const size_t smem = p.off_raw + NR * p.raw_stage_bytes;
     if (!make_tmap_2d(&p.tm_x, x, static_cast<uint64_t>(w.k) * 2, p.M, static_cast<uint64_t>(w.k) * 2, 128, BM, true))
         return cudaErrorNotSupported;
-    if (!make_tmap_2d(&p.tm_raw, w.codes, w.code_row_bytes, w.n, w.code_row_bytes, R::BYTES, BN, R::SW, R::ELEM))
+    if (!make_tmap_2d(&p.tm_raw, w.codes, w.code_row_bytes, w.rows, w.code_row_bytes, R::BYTES, BN, R::SW, R::ELEM))
         return cudaErrorNotSupported;
     auto kern = gemm_kernel<FMT, BITS, GS, BM>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -411,7 +469,21 @@ static cudaError_t launch_t(Params& p, const WDesc& w, const void* x, cudaStream
 
 template <int FMT, int BITS, int GS>
 static cudaError_t launch_bm(Params& p, const WDesc& w, const void* x, cudaStream_t st) {
-    return p.M > 128 ? launch_t<FMT, BITS, GS, 256>(p, w, x, st) : launch_t<FMT, BITS, GS, 128>(p, w, x, st);
+    const int64_t rows_per_matrix = p.g_off ? p.M / std::max<int64_t>(1, p.g_E) : p.M;
+    return rows_per_matrix > 128 ? launch_t<FMT, BITS, GS, 256>(p, w, x, st)
+                                 : launch_t<FMT, BITS, GS, 128>(p, w, x, st);
+}
+
+static cudaError_t dispatch(Params& p, const WDesc& w, const void* x, cudaStream_t st) {
+    if (w.fmt == QM_AFFINE && w.bits == 4 && w.gs == 32) return launch_bm<QM_AFFINE, 4, 32>(p, w, x, st);
+    if (w.fmt == QM_AFFINE && w.bits == 4 && w.gs == 64) return launch_bm<QM_AFFINE, 4, 64>(p, w, x, st);
+    if (w.fmt == QM_AFFINE && w.bits == 4 && w.gs == 128) return launch_bm<QM_AFFINE, 4, 128>(p, w, x, st);
+    if (w.fmt == QM_AFFINE && w.bits == 8 && w.gs == 32) return launch_bm<QM_AFFINE, 8, 32>(p, w, x, st);
+    if (w.fmt == QM_AFFINE && w.bits == 8 && w.gs == 64) return launch_bm<QM_AFFINE, 8, 64>(p, w, x, st);
+    if (w.fmt == QM_AFFINE && w.bits == 8 && w.gs == 128) return launch_bm<QM_AFFINE, 8, 128>(p, w, x, st);
+    if (w.fmt == QM_Q8_0) return launch_bm<QM_Q8_0, 8, 32>(p, w, x, st);
+    if (w.fmt == QM_MXFP4) return launch_bm<QM_MXFP4, 4, 32>(p, w, x, st);
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace gemm
@@ -435,20 +507,42 @@ qm_status launch_gemm(const WDesc& w, const void* x, int64_t M, void* y, cudaStr
     p.scale_row_bytes = w.scale_row_bytes;
     p.sdt = w.sdt;
     p.ksteps = static_cast<int>((w.k + BK - 1) / BK);
-    cudaError_t e = cudaErrorInvalidValue;
-    if (w.fmt == QM_AFFINE && w.bits == 4 && w.gs == 32) e = launch_bm<QM_AFFINE, 4, 32>(p, w, x, st);
-    else if (w.fmt == QM_AFFINE && w.bits == 4 && w.gs == 64) e = launch_bm<QM_AFFINE, 4, 64>(p, w, x, st);
-    else if (w.fmt == QM_AFFINE && w.bits == 4 && w.gs == 128) e = launch_bm<QM_AFFINE, 4, 128>(p, w, x, st);
-    else if (w.fmt == QM_AFFINE && w.bits == 8 && w.gs == 32) e = launch_bm<QM_AFFINE, 8, 32>(p, w, x, st);
-    else if (w.fmt == QM_AFFINE && w.bits == 8 && w.gs == 64) e = launch_bm<QM_AFFINE, 8, 64>(p, w, x, st);
-    else if (w.fmt == QM_AFFINE && w.bits == 8 && w.gs == 128) e = launch_bm<QM_AFFINE, 8, 128>(p, w, x, st);
-    else if (w.fmt == QM_Q8_0) e = launch_bm<QM_Q8_0, 8, 32>(p, w, x, st);
-    else if (w.fmt == QM_MXFP4) e = launch_bm<QM_MXFP4, 4, 32>(p, w, x, st);
+    cudaError_t e = dispatch(p, w, x, st);
     if (e == cudaErrorNotSupported) {  // no TMA descriptor for these operands: the plain kernel
         e = launch_apply_simple(w, x, M, y, st);
         return e == cudaSuccess ? QM_OK : cuda_fail(e, "apply launch");
     }
     if (e != cudaSuccess) return cuda_fail(e, "gemm launch");
+    return QM_OK;
+}
+
+bool gemm_grouped_supported(const WDesc& w, int64_t P) {
+    if (w.ndim != 3 || w.shape[0] < 1 || w.n < 1 || w.k < 64 || P < 1) return false;
+    if (w.code_row_bytes % 16 || (w.k * 2) % 16) return false;  // TMA row strides
+    if (P >= (int64_t(1) << 31) || w.rows >= (int64_t(1) << 31)) return false;
+    return true;
+}
+
+qm_status launch_gemm_grouped(const WDesc& w, const int32_t* offsets, const int32_t* perm, int64_t P,
+                              const void* xs, void* y, cudaStream_t st) {
+    using namespace gemm;
+    if (!gemm_grouped_supported(w, P)) return fail(QM_ENOTSUP, "w: no grouped tensor-core plan for this shape");
+    Params p{};
+    p.scales = w.scales;
+    p.biases = w.biases;
+    p.y = static_cast<uint16_t*>(y);
+    p.M = P;
+    p.n = w.n;
+    p.k = w.k;
+    p.scale_row_bytes = w.scale_row_bytes;
+    p.sdt = w.sdt;
+    p.ksteps = static_cast<int>((w.k + BK - 1) / BK);
+    p.g_off = offsets;
+    p.g_perm = perm;
+    p.g_E = w.shape[0];
+    const cudaError_t e = dispatch(p, w, xs, st);
+    if (e == cudaErrorNotSupported) return fail(QM_ENOTSUP, "w: no tensor map for the grouped product");
+    if (e != cudaSuccess) return cuda_fail(e, "grouped gemm launch");
     return QM_OK;
 }
 

@@ -74,18 +74,32 @@ bool gemv_grouped_supported(const WDesc& w, int64_t P);
 // shape is outside what the kernel handles.
 qm_status launch_gemm(const WDesc& w, const void* x, int64_t M, void* y, cudaStream_t st);
 bool gemm_supported(const WDesc& w, int64_t M);
+// Grouped tensor-core product over a weight [E, n, k]: xs holds the routed
+// activation rows expert by expert (offsets [E+1]); row i of the result goes
+// to row perm[i] of y [P, n].
+qm_status launch_gemm_grouped(const WDesc& w, const int32_t* offsets, const int32_t* perm, int64_t P,
+                              const void* xs, void* y, cudaStream_t st);
+bool gemm_grouped_supported(const WDesc& w, int64_t P);
 // Plain reference-order kernel for shapes the fast paths refuse.
 cudaError_t launch_apply_simple(const WDesc& w, const void* x, int64_t M, void* y,
                                 cudaStream_t st);
 
 // Experts.
-size_t experts_workspace_bytes(int64_t P, int64_t E);
+size_t route_workspace_bytes(int64_t P, int64_t E);
+// allow_tensor: the tensor-core path may be chosen (it needs the routed rows
+// of x in the workspace).
+size_t experts_workspace_bytes(const WDesc& w, int64_t P, bool allow_tensor);
 cudaError_t launch_route(const void* ids, int id64, int64_t P, int64_t E, int32_t* counts,
                          int32_t* offsets, int32_t* perm, void* ws, cudaStream_t st,
                          uint16_t* zero_y = nullptr, int64_t zero_n = 0);
 qm_status launch_experts(const WDesc& w, const void* ids, int id64, int64_t T, int64_t topk,
                          const void* x, int64_t x_rows, void* y, void* ws, size_t ws_bytes,
-                         cudaStream_t st);
+                         cudaStream_t st, bool allow_tensor);
+// qm_apply_experts's checks, then launch_experts.
+qm_status apply_experts_checked(const qm_weight* w, const void* ids, int32_t id_type, int64_t T,
+                                int64_t topk, const void* x, int64_t x_rows, int32_t x_dtype, void* y,
+                                void* workspace, size_t workspace_bytes, qm_stream_t stream,
+                                bool allow_tensor);
 
 // Per-translation-unit device error flags: read-and-clear (after a sync).
 uint32_t elementwise_read_clear_error();

@@ -33,7 +33,7 @@ def _declared():
 def test_exports_every_declared_symbol(lib):
     names = _declared()
     assert {"qm_dequant", "qm_apply", "qm_take", "qm_apply_experts", "qm_experts_route",
-            "qm_apply_experts_workspace", "qm_device_status", "qm_last_error"} <= names
+            "qm_apply_experts_workspace", "qm_experts_route_workspace", "qm_device_status", "qm_last_error"} <= names
     for n in names:
         assert hasattr(lib, n), n
 
@@ -132,7 +132,14 @@ def test_experts_validation(lib):
 
 
 def test_workspace_query(lib):
-    assert lib.qm_apply_experts_workspace(0, 4, 32) == 0
-    a = lib.qm_apply_experts_workspace(64, 4, 32)
-    b = lib.qm_apply_experts_workspace(4096, 4, 32)
+    w3 = _w(fmt=qm.QM_MXFP4, bits=0, gs=0, shape=(32, 5760, 2880), ndim=3, biases=0)
+    assert lib.qm_apply_experts_workspace(ctypes.byref(w3), 0, 4) == 0
+    a = lib.qm_apply_experts_workspace(ctypes.byref(w3), 64, 4)
+    b = lib.qm_apply_experts_workspace(ctypes.byref(w3), 4096, 4)
     assert 0 < a < b and a % 256 == 0 and b % 256 == 0
+    assert a < 4096 * 4 * 2880 * 2 <= b  # many positions per expert: routed rows of x too
+    bad = _w(shape=(16, 64))  # not a stack of experts
+    assert lib.qm_apply_experts_workspace(ctypes.byref(bad), 64, 4) == 0
+    assert lib.qm_experts_route_workspace(0, 32) == 0
+    r = lib.qm_experts_route_workspace(256, 32)
+    assert 0 < r <= a and r % 256 == 0

@@ -314,13 +314,15 @@ def _check_experts(w, ids, x, what):
 
 
 @pytest.mark.parametrize("kind", KINDS)
-def test_apply_experts_chunks(kind):
-    # experts with many positions (several chunks), empty experts, positions
-    # out of range, per-token and per-position activations
+@pytest.mark.parametrize("T", [24, 160])
+def test_apply_experts_chunks(kind, T):
+    # experts with many positions (several chunks or tiles), empty experts,
+    # positions out of range, per-token and per-position activations; T = 24
+    # takes the decode path, T = 160 (over 32 positions per expert) the tensor cores
     g = synth.rng(910)
     E, n, k = 6, 100, 512
     w = _make(kind, g, n, k, lead=(E,))
-    T, topk = 24, 2
+    topk = 2
     ids = synth.expert_ids(g, T, topk, E)
     ids[:, 0] = 2           # expert 2: 24+ positions, more than one chunk
     ids[:, 1] = np.where(ids[:, 1] == 2, 5, ids[:, 1])
@@ -343,10 +345,11 @@ def test_apply_experts_all_out_of_range():
     assert np.all(h.view(np.uint16) == 0)
 
 
-def test_apply_experts_rows_independent_of_other_experts():
-    # a row's bits depend on its own row and expert only
+@pytest.mark.parametrize("T", [16, 200])
+def test_apply_experts_rows_independent_of_other_experts(T):
+    # a row's bits depend on its own row and expert only (decode and tensor paths)
     g = synth.rng(930)
-    E, n, k, T, topk = 8, 96, 512, 16, 2
+    E, n, k, topk = 8, 96, 512, 2
     w = _make("affine4_g64", g, n, k, lead=(E,))
     qw = qm.QWeight.from_arrays(w)
     x = _dev_bf16(synth.activations(g, T, k))
@@ -361,16 +364,17 @@ def test_apply_experts_rows_independent_of_other_experts():
     assert np.array_equal(y1[same].view(np.uint16), y2[same].view(np.uint16))
 
 
-def test_apply_experts_moe_shape_t64_sampled():
-    # 32 MXFP4 experts [5760, 2880], 64 tokens x 4: every output row of a
+@pytest.mark.parametrize("T", [64, 1024, 4096])
+def test_apply_experts_moe_shape_sampled(T):
+    # 32 MXFP4 experts [5760, 2880], T tokens x 4: every output row of a
     # sample of positions against the oracle
-    w, ids, x = synth.moe_config(64)
+    w, ids, x = synth.moe_config(T)
     E, n, k = w["shape"]
     T, topk = ids.shape
     ow = to_oracle(w)
     y = qm.apply_experts(qm.QWeight.from_arrays(w), torch.from_numpy(ids).cuda(), _dev_bf16(x))
     got = bf16_to_f64(_host(y)).reshape(T * topk, n)
-    pos = np.sort(synth.rng(940).choice(T * topk, size=16, replace=False))
+    pos = np.sort(synth.rng(940 + T).choice(T * topk, size=16, replace=False))
     sub_ids = ids.reshape(-1)[pos].reshape(-1, 1).astype(np.int32)
     sub_x = x[pos // topk]
     ref = oracle.apply_experts(ow, sub_ids, sub_x).reshape(len(pos), n)
@@ -379,7 +383,7 @@ def test_apply_experts_moe_shape_t64_sampled():
     sub_w = dict(w, shape=(len(used), n, k), codes=w["codes"][used], scales=w["scales"][used])
     wn = row_norms(to_oracle(sub_w)).reshape(len(used), n)[np.searchsorted(used, sub_ids[:, 0])]
     for i, r in enumerate(pos):
-        check_product(got[r:r + 1], ref[i:i + 1], wn[i], xn[i:i + 1], k, f"moe T=64 position {r}")
+        check_product(got[r:r + 1], ref[i:i + 1], wn[i], xn[i:i + 1], k, f"moe T={T} position {r}")
 
 
 # ---------------------------------------------------------------- long pipelines
