@@ -308,8 +308,7 @@ def _check_experts(w, ids, x, what):
     xr = rows // topk if x.shape[0] == T else rows
     xn = np.linalg.norm(oracle.decode_array(x, oracle.BF16), axis=1)[xr]
     wn = row_norms(ow).reshape(E, n)[flat[rows]]
-    for i, r in enumerate(rows):
-        check_product(got[r:r + 1], ref[r:r + 1], wn[i], xn[i:i + 1], k, f"{what} position {r}")
+    check_product(got[rows], ref[rows], wn, xn, k, what)
     return got
 
 
@@ -382,8 +381,7 @@ def test_apply_experts_moe_shape_sampled(T):
     used = np.unique(sub_ids[:, 0])
     sub_w = dict(w, shape=(len(used), n, k), codes=w["codes"][used], scales=w["scales"][used])
     wn = row_norms(to_oracle(sub_w)).reshape(len(used), n)[np.searchsorted(used, sub_ids[:, 0])]
-    for i, r in enumerate(pos):
-        check_product(got[r:r + 1], ref[i:i + 1], wn[i], xn[i:i + 1], k, f"moe T={T} position {r}")
+    check_product(got[pos], ref, wn, xn, k, f"moe T={T} positions {pos.tolist()}")
 
 
 # ---------------------------------------------------------------- long pipelines

@@ -41,7 +41,8 @@ def check_product(y_gpu: np.ndarray, y_ref: np.ndarray, wnorm: np.ndarray, xnorm
     """The product contract, element by element and as a whole.
 
     y_gpu: the library's result decoded to float64 [M, n]; y_ref: the oracle's
-    unrounded float64 product [M, n]; wnorm [n], xnorm [M] the row norms.
+    unrounded float64 product [M, n]; wnorm [n] (or [M, n] where each output
+    row has its own matrix, as with experts), xnorm [M] the row norms.
 
     Per element: |y_gpu - y_ref| <= 1e-2 * ||w_j|| * ||x_m|| / sqrt(k) plus half
     a bfloat16 ulp of y_gpu -- the single final rounding to x's dtype that the
@@ -52,7 +53,9 @@ def check_product(y_gpu: np.ndarray, y_ref: np.ndarray, wnorm: np.ndarray, xnorm
     y_ref = np.asarray(y_ref, dtype=np.float64)
     assert y_gpu.shape == y_ref.shape, (y_gpu.shape, y_ref.shape)
     assert np.all(np.isfinite(y_gpu)), f"{what}: non-finite outputs"
-    bound = 1e-2 * np.outer(xnorm, wnorm) / np.sqrt(k)
+    wnorm = np.asarray(wnorm, dtype=np.float64)
+    xnorm = np.asarray(xnorm, dtype=np.float64)
+    bound = 1e-2 * (np.outer(xnorm, wnorm) if wnorm.ndim == 1 else xnorm[:, None] * wnorm) / np.sqrt(k)
     err = np.abs(y_gpu - y_ref)
     allowed = bound + bf16_half_ulp(y_gpu)
     bad = err > allowed
