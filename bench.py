@@ -46,8 +46,10 @@ def parse():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="decode", choices=["decode", "prefill"],
-                    help="decode: the headline M=1 step; prefill: Q8_0 products at M >= 128")
+    ap.add_argument("--workload", default="decode", choices=["decode", "prefill", "experts", "take"],
+                    help="decode: the headline M=1 step; prefill: Q8_0 products at M >= 128; "
+                         "experts: MXFP4 apply_experts; take: quantized embedding take + dequant")
+    ap.add_argument("--T", type=int, default=None, help="experts: tokens (default 4096)")
     ap.add_argument("--bits", type=int, default=4)
     ap.add_argument("--M", type=int, default=None)
     ap.add_argument("--no-detail", action="store_true", help="skip the secondary measurements")
@@ -251,6 +253,209 @@ def run_prefill(args, rank, world):
     }
 
 
+def _reduce_max(elapsed, dev, world):
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        t = torch.tensor([elapsed], device=dev)
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+        return float(t.item())
+    return elapsed
+
+
+def _setup():
+    import torch
+
+    import packed_qmatmul_gb300 as qm
+    from packed_qmatmul_gb300 import build as qbuild
+
+    qbuild.build()
+    qm.load_library()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    return dev
+
+
+EXPERTS_SHAPE = (32, 5760, 2880)
+
+
+def experts_step(T, dev):
+    """One apply_experts call: 32 MXFP4 experts [5760, 2880], ids [T, 4]
+    distinct per token and uniform over the experts, x [T, 2880]. Returns
+    (step, flops, weight bytes of the experts the ids use, launches)."""
+    import torch
+
+    import packed_qmatmul_gb300 as qm
+
+    w, ids, x = synth.moe_config(T)
+    E, n, k = w["shape"]
+    qw = qm.QWeight.from_arrays(w, dev)
+    ids_d = torch.from_numpy(ids).to(dev)
+    x_d = torch.from_numpy(x.view(np.int16)).to(dev).view(torch.bfloat16)
+    y = torch.empty((T, ids.shape[1], n), dtype=torch.bfloat16, device=dev)
+    ws = torch.empty(max(qm.qm_apply_experts_workspace(qw, T, ids.shape[1]), 256), dtype=torch.uint8,
+                     device=dev)
+    used = len(np.unique(ids))
+    wbytes = used * (n * k // 2 + n * k // 32)
+    flops = 2.0 * ids.size * n * k
+    tensor = ids.size > 32 * E
+    launches = 4 if tensor else 3  # route count + route scatter + (gather + grouped GEMM | grouped GEMV)
+
+    def step(stream):
+        qm.qm_apply_experts(qw, ids_d, x_d, y, ws, stream)
+
+    return step, flops, wbytes, launches, tensor
+
+
+EXPERTS_TFLOPS = "TFLOP/s (MXFP4 apply_experts)"
+EXPERTS_GBS = "packed-weight GB/s (MXFP4 apply_experts, few tokens)"
+
+
+def run_experts(args, rank, world):
+    import torch
+
+    import packed_qmatmul_gb300 as qm
+
+    dev = _setup()
+    T = args.T or 4096
+    fn, flops, wbytes, launches, tensor = experts_step(T, dev)
+    stream = torch.cuda.Stream()
+    elapsed, clocks = time_graph(lambda: fn(stream), stream, args.steps, args.warmup, dev.index)
+    qm.qm_device_status(stream)
+    elapsed = _reduce_max(elapsed, dev, world)
+    t_step = elapsed / args.steps
+    peaks = load_peaks()
+    if tensor:
+        peak = peaks.get("bf16_tflops", 1900.0)
+        value, unit, metric = flops * world / t_step / 1e12, "TFLOP/s", EXPERTS_TFLOPS
+        roof = {"bound": "tensor", "achieved": round(flops / t_step / 1e12, 2), "peak": peak, "unit": "TFLOP/s",
+                "frac": round(flops / t_step / 1e12 / peak, 4), "traffic": None,
+                "kernel": "grouped gemm_kernel<MXFP4> with routing and gather in the step time",
+                "peak_source": "measured bf16 dense, burst" if "bf16_tflops" in peaks else "fallback"}
+    else:
+        peak = peaks.get("hbm_gbs", 6800.0)
+        value, unit, metric = wbytes * world / t_step / 1e9, "GB/s", EXPERTS_GBS
+        roof = {"bound": "hbm", "achieved": round(wbytes / t_step / 1e9, 2), "peak": peak, "unit": "GB/s",
+                "frac": round(wbytes / t_step / 1e9 / peak, 4), "traffic": None,
+                "kernel": "grouped gemv_kernel<MXFP4> with routing in the step time",
+                "peak_source": "measured" if "hbm_gbs" in peaks else "fallback"}
+    return {
+        "metric": metric, "value": round(value, 2), "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16xbf16->f32" if tensor else "f16xf16->f32",
+        "data": "synthetic (seeded)",
+        "config": {"workload": f"MXFP4 apply_experts, 32 experts [5760, 2880] (gate_up), T={T} tokens x top-4, "
+                               "ids distinct per token, uniform", "T": T, "topk": 4,
+                   "flops_per_step": flops, "weight_bytes_used": wbytes,
+                   "l2": "expert weights 282 MB, more than L2", "graph": "step captured once as a CUDA graph"},
+        "roofline": roof, "gpu_launches": launches * args.steps, "clocks": clocks,
+    }
+
+
+TAKE_METRIC = "GB/s (quantized embedding take + full dequant)"
+
+
+def take_step(dev):
+    """Affine 4-bit gs64 table 151936 x 1024: take of 4096 uniform ids into
+    bf16 [4096, 1024], then dequant of the whole table to bf16. Returns
+    (take fn, dequant fn, packed-take fn, bytes of each)."""
+    import torch
+
+    import packed_qmatmul_gb300 as qm
+
+    g = synth.rng(5)
+    n, k = LM_HEAD
+    qw = qm.QWeight.from_arrays(synth.affine_weight(g, n, k, bits=4, group_size=64), dev)
+    nid = 4096
+    ids = torch.from_numpy(synth.uniform_ids(g, nid, n)).to(dev)
+    dense = torch.empty((nid, k), dtype=torch.bfloat16, device=dev)
+    table = torch.empty((n, k), dtype=torch.bfloat16, device=dev)
+    row = packed_bytes(1, k, 4)
+    shapes = qw.part_shapes((nid,))
+    outs = [None if sh is None else torch.empty(sh, dtype=torch.uint8, device=dev) for sh in shapes]
+    take_bytes = nid * (row + 2 * k) + nid * 4
+    deq_bytes = n * (row + 2 * k)
+    ptake_bytes = 2 * nid * row + nid * 4
+
+    def take(stream):
+        qm.qm_take(qw, 0, ids, None, None, None, dense, stream)
+
+    def deq(stream):
+        qm.qm_dequant(qw, table, stream)
+
+    def ptake(stream):
+        qm.qm_take(qw, 0, ids, outs[0], outs[1], outs[2], None, stream)
+
+    return take, deq, ptake, take_bytes, deq_bytes, ptake_bytes
+
+
+def run_take(args, rank, world):
+    import torch
+
+    import packed_qmatmul_gb300 as qm
+
+    dev = _setup()
+    take, deq, ptake, tb, db, pb = take_step(dev)
+    stream = torch.cuda.Stream()
+
+    def step():
+        take(stream)
+        deq(stream)
+
+    elapsed, clocks = time_graph(step, stream, args.steps, args.warmup, dev.index)
+    t_deq, _ = time_graph(lambda: deq(stream), stream, args.steps, args.warmup)
+    qm.qm_device_status(stream)
+    elapsed = _reduce_max(elapsed, dev, world)
+    t_step = elapsed / args.steps
+    t_d = t_deq / args.steps
+    peaks = load_peaks()
+    peak = peaks.get("hbm_gbs", 6800.0)
+    return {
+        "metric": TAKE_METRIC, "value": round((tb + db) * world / t_step / 1e9, 2), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded)",
+        "config": {"workload": "MLX affine 4-bit gs64 table 151936x1024: take of 4096 uniform ids to bf16 "
+                               "[4096, 1024] + dequant of the whole table to bf16",
+                   "bytes_per_step": tb + db, "take_bytes": tb, "dequant_bytes": db,
+                   "l2": "the dequant writes 311 MB (more than L2) between takes",
+                   "graph": "step captured once as a CUDA graph"},
+        "roofline": {"bound": "hbm", "achieved": round(db / t_d / 1e9, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(db / t_d / 1e9 / peak, 4), "traffic": None,
+                     "kernel": "decode_rows_kernel<affine,4> (the full dequant, timed alone)",
+                     "peak_source": "measured" if "hbm_gbs" in peaks else "fallback"},
+        "gpu_launches": 2 * args.steps, "clocks": clocks,
+    }
+
+
+def other_workloads(dev, stream):
+    """The other configs' headline numbers, for the default run's detail."""
+    import torch
+
+    out = {}
+    for T in (64, 1024, 4096):
+        fn, flops, wbytes, _, tensor = experts_step(T, dev)
+        el, _ = time_graph(lambda: fn(stream), stream, 10, 3)
+        t = el / 10
+        out[f"experts_T{T}"] = {"ms": round(t * 1e3, 4), "TFLOP/s": round(flops / t / 1e12, 1),
+                                "weight GB/s": round(wbytes / t / 1e9, 1),
+                                "path": "grouped tcgen05 GEMM" if tensor else "grouped GEMV"}
+        del fn
+        torch.cuda.empty_cache()
+    take, deq, ptake, tb, db, pb = take_step(dev)
+    # each take follows a full dequant (311 MB written): its reads start cold
+    el_td, _ = time_graph(lambda: (deq(stream), take(stream)), stream, 10, 3)
+    el_pd, _ = time_graph(lambda: (deq(stream), ptake(stream)), stream, 10, 3)
+    el_d, _ = time_graph(lambda: deq(stream), stream, 10, 3)
+    td = (el_td - el_d) / 10
+    pd = (el_pd - el_d) / 10
+    out["dequant_table"] = {"ms": round(el_d / 10 * 1e3, 4), "GB/s": round(db / (el_d / 10) / 1e9, 1)}
+    out["take_dense_4096"] = {"us": round(td * 1e6, 2), "GB/s": round(tb / td / 1e9, 1)}
+    out["take_packed_4096"] = {"us": round(pd * 1e6, 2), "GB/s": round(pb / pd / 1e9, 1)}
+    del take, deq, ptake
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, rank, world):
     import torch
 
@@ -310,6 +515,7 @@ def run_ours(args, rank, world):
         res["config"]["workload"] += f" (profiling aid: only *{args.only})"
     if not args.no_detail and not args.only and rank == 0:
         res["detail"] = detail_measurements(args, dev, stream)
+        res["detail"].update(other_workloads(dev, stream))
     return res
 
 
@@ -451,8 +657,8 @@ def main():
     if world > 1:
         import torch.distributed as tdist
         tdist.init_process_group("nccl")
-    if args.workload == "prefill":
-        res = run_prefill(args, rank, world)
+    if args.workload in ("prefill", "experts", "take"):
+        res = {"prefill": run_prefill, "experts": run_experts, "take": run_take}[args.workload](args, rank, world)
         if rank == 0:
             print(json.dumps(res))
         if world > 1:
