@@ -116,6 +116,28 @@ QM_DEV void cluster_sync() {
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The two halves of cluster_sync, for work in between: arrive (relaxed: it
+// publishes nothing but what a fence before it released) ...
+QM_DEV void cluster_arrive_relaxed() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+// ... and wait for every CTA of the cluster to have arrived.
+QM_DEV void cluster_wait() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Store to shared memory of another CTA of the cluster (address from mapa).
+QM_DEV void st_shared_cluster_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
+// Arrive on an mbarrier in another CTA of the cluster, releasing this
+// thread's earlier writes at cluster scope.
+QM_DEV void mbar_arrive_cluster(uint32_t remote_bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+}
+
 // Address of the same shared variable in CTA `rank` of this cluster.
 QM_DEV uint32_t map_shared_rank(uint32_t addr, uint32_t rank) {
     uint32_t r;

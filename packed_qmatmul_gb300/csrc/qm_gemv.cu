@@ -94,7 +94,7 @@ struct Params {
     uint32_t code_seg, nbox;          // per row: bytes of codes; 128-byte boxes per stage
     uint32_t scale_seg;               // per row bytes of scales (and of biases) in a stage
     uint32_t off_scales, off_biases;  // within a stage
-    uint32_t off_tokscale, off_tok, off_xfrag, off_red, off_xraw, off_stages;
+    uint32_t off_tokscale, off_tok, off_xfrag, off_red, off_xraw, off_recv, off_stages;
 };
 
 // ---------------------------------------------------------------- decoders
@@ -244,6 +244,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
     const uint32_t bar_full0 = smem_u32(bars), bar_empty0 = smem_u32(bars + kMaxStages);
     const uint32_t bar_x = smem_u32(bars + 2 * kMaxStages);
+    const uint32_t bar_red = smem_u32(smem + 344);  // split k: the other CTAs' partial sums are in (rank 0)
     volatile int& s_abort = *reinterpret_cast<volatile int*>(smem + (2 * kMaxStages + 1) * 8);
     volatile int* slot_stage = reinterpret_cast<volatile int*>(smem + (2 * kMaxStages + 2) * 8);
     // grouped mode: the chunk's size and expert, its positions and activation rows
@@ -262,6 +263,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
             mbar_init(bar_empty0 + 8 * i, p.team);  // the warps of the team that read it
         }
         mbar_init(bar_x, 1);
+        if (S > 1 && rank == 0) mbar_init(bar_red, (S - 1) * kThreads);
         fence_mbar_init();
     }
     __syncthreads();
@@ -322,6 +324,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
     }
     const int64_t stage0 = cluster * p.stages_per_cluster;
     const int nst = static_cast<int>(std::min<int64_t>(p.stages_per_cluster, p.n_stages - stage0));
+    if (S > 1) cluster_arrive_relaxed();  // waited for before the first access to another CTA
     // x comes from the previous kernel; so may W, unless the caller marked it
     // static, in which case the producer streams its first stages before waiting
     if (!p.g_off && (!p.static_w || warp != kWarps)) grid_dependency_wait();
@@ -425,18 +428,24 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
         // 1. per-token power-of-two scale over this CTA's k range (warp m: token m)
         {
             // max |x| per token: one pass over the staged rows, order-free
+            // (warp maxima first: one shared atomic per warp and token)
             const int per_row = static_cast<int>(p.krange / 8);
-            for (int i = ctid; i < M * per_row; i += kWarps * 32) {
-                const uint4 q = *reinterpret_cast<const uint4*>(xs + 8 * i);
-                const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
-                float amax = 0.0f;
+            for (int m = 0; m < M; ++m)
+                for (int i0 = 0; i0 < per_row; i0 += kWarps * 32) {
+                    const int i = i0 + ctid;
+                    float amax = 0.0f;
+                    if (i < per_row) {
+                        const uint4 q = *reinterpret_cast<const uint4*>(xs + m * p.krange + 8 * i);
+                        const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w4[e] & 0xFFFF)));
-                    amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w4[e] >> 16)));
+                        for (int e = 0; e < 4; ++e) {
+                            amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w4[e] & 0xFFFF)));
+                            amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w4[e] >> 16)));
+                        }
+                    }
+                    const uint32_t b = __reduce_max_sync(0xffffffffu, __float_as_uint(amax));
+                    if (lane == 0 && b) atomicMax(&xmax[m], b);
                 }
-                if (amax > 0.0f) atomicMax(&xmax[i / per_row], __float_as_uint(amax));
-            }
         }
         named_bar_sync(1, kWarps * 32);
         // x' = x * 2^E puts max |x'| in [2^14, 2^15): every bf16 value is then exact in f16
@@ -526,10 +535,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
         for (int j = team; j < nst; j += nteams) {
             const uint32_t slot = j % p.nstage;
             bool live = !s_abort;
-            if (live && lane == 0) {  // the producer has started filling the slot with stage j
+            if (live && lane == 0 && slot_stage[slot] != j) {  // the producer has not started stage j yet
                 const uint64_t t0 = globaltimer();
-                while (slot_stage[slot] != j && !s_abort)
-                    if (globaltimer() - t0 > kWaitLimitNs) {
+                for (int spin = 0; slot_stage[slot] != j && !s_abort; ++spin)
+                    if ((spin & 63) == 63 && globaltimer() - t0 > kWaitLimitNs) {
                         atomicOr(&g_err_gemv, DEV_ERR_TIMEOUT);
                         s_abort = 1;
                         break;
@@ -686,22 +695,34 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
     }
 
     // ---------------------------------------------------------------- split-k reduction
+    // The CTAs of rank 1.. push their sums into rank 0's receive area and
+    // leave; rank 0 adds them in rank order and stores y.
     if (S > 1) {
-        __syncthreads();
-        cluster_sync();
-        const uint32_t base = smem_u32(smem + p.off_xraw);
-        const int entries = nst * kRows * 16;
-        for (int e = rank * blockDim.x + threadIdx.x; e < entries; e += S * blockDim.x) {
-            const int m = e % 16, rr = e / 16;
-            const int64_t row = stage0 * kRows + rr;
-            if (m >= M || row >= p.n) continue;
-            float sum = 0.0f;
-            for (int q = 0; q < S; ++q) sum += ld_shared_cluster_f32(map_shared_rank(base + 4u * e, q));
-            __nv_bfloat16 b = __float2bfloat16_rn(sum);
-            const int64_t yr = p.g_off ? s_pos[m] : m;
-            p.y[yr * p.n + row] = *reinterpret_cast<uint16_t*>(&b);
+        __syncthreads();  // this CTA's partial sums are complete
+        cluster_wait();   // rank 0's barrier is initialized
+        const int ent = nst * kRows * M;  // [row][token] of this cluster's stages
+        const float* own = reinterpret_cast<const float*>(smem + p.off_xraw);  // [row][16]
+        if (rank != 0) {
+            const uint32_t dst = map_shared_rank(smem_u32(smem + p.off_recv), 0) + (rank - 1) * ent * 4u;
+            for (int e = threadIdx.x; e < ent; e += blockDim.x)
+                st_shared_cluster_f32(dst + 4u * e, own[(e / M) * 16 + e % M]);
+            mbar_arrive_cluster(map_shared_rank(bar_red, 0));
+        } else {
+            const bool ok = mbar_wait(bar_red, 0);
+            if (!ok && threadIdx.x == 0) atomicOr(&g_err_gemv, DEV_ERR_TIMEOUT);
+            const float* recv = reinterpret_cast<const float*>(smem + p.off_recv);  // [rank - 1][ent]
+            for (int e = threadIdx.x; ok && e < ent; e += blockDim.x) {
+                const int rr = e / M, m = e % M;
+                const int64_t row = stage0 * kRows + rr;
+                if (row >= p.n) continue;
+                float sum = 0.0f;
+                sum += own[rr * 16 + m];
+                for (int q = 1; q < S; ++q) sum += recv[(q - 1) * ent + e];
+                __nv_bfloat16 b = __float2bfloat16_rn(sum);
+                const int64_t yr = p.g_off ? s_pos[m] : m;
+                p.y[yr * p.n + row] = *reinterpret_cast<uint16_t*>(&b);
+            }
         }
-        cluster_sync();
     }
 }
 
@@ -800,7 +821,10 @@ static bool plan_for(const WDesc& w, int64_t M, int S, int per_sm, Plan* out, do
         p.off_xraw = round_up(p.off_red + red_bytes, 128);
         const uint64_t partial_bytes = S > 1 ? static_cast<uint64_t>(spc) * kRows * 16 * 4 : 0;
         const uint64_t xraw_bytes = static_cast<uint64_t>(M) * kr * 2;
-        p.off_stages = round_up(p.off_xraw + std::max(partial_bytes, xraw_bytes), 1024);
+        // split k: rank 0 receives the other ranks' sums apart from everything it may still be reading
+        const uint64_t recv_bytes = S > 1 ? static_cast<uint64_t>(S - 1) * spc * kRows * M * 4 : 0;
+        p.off_recv = round_up(p.off_xraw + std::max(partial_bytes, xraw_bytes), 128);
+        p.off_stages = round_up(p.off_recv + recv_bytes, 1024);
         const int64_t room = budget - p.off_stages;
         return std::min<int64_t>(std::min<int64_t>(kMaxStages, room / p.stage_bytes), std::max<int64_t>(2, spc));
     };
