@@ -60,16 +60,23 @@ QM_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete. Returns false if
-// the wait ran past kWaitLimitNs (the caller then abandons its work).
-QM_DEV bool mbar_wait(uint32_t bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
+// The waiting part of mbar_wait, kept out of line: every call site then
+// costs one try_wait and a call, not a copy of the spin loop.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity) {
     const uint64_t t0 = globaltimer();
     for (;;) {
+#pragma unroll 1
         for (int i = 0; i < 64; ++i)
             if (mbar_try_wait(bar, parity)) return true;
         if (globaltimer() - t0 > kWaitLimitNs) return false;
     }
+}
+
+// Waits for the phase with the given parity to complete. Returns false if
+// the wait ran past kWaitLimitNs (the caller then abandons its work).
+QM_DEV bool mbar_wait(uint32_t bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    return mbar_wait_slow(bar, parity);
 }
 
 // Named barrier `id` (1..15) over `count` threads (a multiple of 32).

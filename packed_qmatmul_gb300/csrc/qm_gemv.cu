@@ -85,10 +85,10 @@ struct Params {
     // of one expert, times one share of that expert's rows
     const int32_t* g_off;    // [E + 1] start of each expert's positions in g_perm
     const int32_t* g_perm;   // routed order -> position
-    int64_t g_E;
+    int g_E;
     int g_Q;                 // positions per chunk
     int g_xdiv;              // activation row of position q: q / g_xdiv
-    int64_t g_wclusters;     // clusters per chunk
+    int g_wclusters;         // clusters per chunk
     // shared memory layout (byte offsets from the dynamic smem base)
     uint32_t nstage, stage_bytes;
     uint32_t code_seg, nbox;          // per row: bytes of codes; 128-byte boxes per stage
@@ -226,6 +226,53 @@ QM_DEV void tile_group(const CodeRow& r0, const CodeRow& r8, int gi, int t,
     }
 }
 
+// Grouped mode, one warp: which chunk cluster slot `slot` is -- its size
+// (s_grp[0], 0 past the last chunk), expert (s_grp[1]), positions and
+// activation rows -- from the routing offsets, 32 experts per step.
+static __device__ __noinline__ void group_lookup(const Params& p, int slot, int lane, int* s_grp, int* s_pos,
+                                                 int* s_xrow) {
+    int before = 0;  // chunks of the experts already passed
+    int gm = 0, ge = 0, gb = 0;
+    for (int e0 = 0; e0 < p.g_E; e0 += 32) {
+        const int e = e0 + lane;
+        int o0 = 0, cnt = 0;
+        if (e < p.g_E) {
+            o0 = __ldg(p.g_off + e);
+            cnt = __ldg(p.g_off + e + 1) - o0;
+        }
+        const int nch = (cnt + p.g_Q - 1) / p.g_Q;
+        int inc = nch;  // inclusive scan over the lanes
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += t;
+        }
+        const int lo = before + inc - nch;
+        const bool mine = e < p.g_E && slot >= lo && slot < lo + nch;
+        const uint32_t hit = __ballot_sync(0xffffffffu, mine);
+        if (mine) {
+            const int ch = slot - lo;
+            gb = o0 + ch * p.g_Q;
+            gm = min(p.g_Q, cnt - ch * p.g_Q);
+            ge = e;
+        }
+        if (hit) {
+            const int src = __ffs(hit) - 1;
+            gm = __shfl_sync(0xffffffffu, gm, src);
+            ge = __shfl_sync(0xffffffffu, ge, src);
+            gb = __shfl_sync(0xffffffffu, gb, src);
+            break;
+        }
+        before += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    if (lane == 0) { s_grp[0] = gm; s_grp[1] = ge; }
+    if (lane < gm) {
+        const int q = __ldg(p.g_perm + gb + lane);
+        s_pos[lane] = q;
+        s_xrow[lane] = q / p.g_xdiv;
+    }
+}
+
 template <int FMT, int BITS, int GS, int NT>
 __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -233,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = p.S;
     const uint32_t rank = (S > 1) ? cluster_ctarank() : 0;
-    int64_t cluster = blockIdx.x / S;
+    int cluster = static_cast<int>(blockIdx.x) / S;
     const int64_t kbase = rank * p.krange;
     const int groups = static_cast<int>(p.krange / GS);
 
@@ -255,9 +302,12 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
     unsigned int* xmax = reinterpret_cast<unsigned int*>(smem + p.off_tokscale) + 32;  // [16] max |x| bits
     if (threadIdx.x == 0) {
         s_abort = 0;
+        #pragma unroll 1
         for (int i = 0; i < kMaxStages; ++i) slot_stage[i] = -1;
+        #pragma unroll 1
         for (int i = 0; i < 16; ++i) xmax[i] = 0u;
         prefetch_tmap(&p.tm_codes);
+        #pragma unroll 1
         for (uint32_t i = 0; i < p.nstage; ++i) {
             mbar_init(bar_full0 + 8 * i, 32);      // the producer's lanes
             mbar_init(bar_empty0 + 8 * i, p.team);  // the warps of the team that read it
@@ -274,53 +324,13 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
         // which chunk of which expert: the routing tables come from the previous kernel
         if (warp == 0) {
             grid_dependency_wait();
-            const int64_t slot = cluster / p.g_wclusters;
-            int64_t before = 0;  // chunks of the experts already passed
-            int gm = 0, ge = 0, gb = 0;
-            for (int64_t e0 = 0; e0 < p.g_E; e0 += 32) {
-                const int64_t e = e0 + lane;
-                int o0 = 0, cnt = 0;
-                if (e < p.g_E) {
-                    o0 = __ldg(p.g_off + e);
-                    cnt = __ldg(p.g_off + e + 1) - o0;
-                }
-                const int64_t nch = (cnt + p.g_Q - 1) / p.g_Q;
-                int64_t inc = nch;  // inclusive scan over the lanes
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int64_t t = __shfl_up_sync(0xffffffffu, inc, o);
-                    if (lane >= o) inc += t;
-                }
-                const int64_t lo = before + inc - nch;
-                const bool mine = e < p.g_E && slot >= lo && slot < lo + nch;
-                const uint32_t hit = __ballot_sync(0xffffffffu, mine);
-                if (mine) {
-                    const int ch = static_cast<int>(slot - lo);
-                    gb = o0 + ch * p.g_Q;
-                    gm = min(p.g_Q, cnt - ch * p.g_Q);
-                    ge = static_cast<int>(e);
-                }
-                if (hit) {
-                    const int src = __ffs(hit) - 1;
-                    gm = __shfl_sync(0xffffffffu, gm, src);
-                    ge = __shfl_sync(0xffffffffu, ge, src);
-                    gb = __shfl_sync(0xffffffffu, gb, src);
-                    break;
-                }
-                before += __shfl_sync(0xffffffffu, inc, 31);
-            }
-            if (lane == 0) { s_grp[0] = gm; s_grp[1] = ge; }
-            if (lane < gm) {
-                const int q = __ldg(p.g_perm + gb + lane);
-                s_pos[lane] = q;
-                s_xrow[lane] = q / p.g_xdiv;
-            }
+            group_lookup(p, static_cast<int>(cluster / p.g_wclusters), lane, s_grp, s_pos, s_xrow);
         }
         __syncthreads();
         M = s_grp[0];
         if (M == 0) return;  // a slot past the last chunk; the same for every CTA of the cluster
         wrow0 = static_cast<int64_t>(s_grp[1]) * p.n;
-        cluster %= p.g_wclusters;
+        cluster = static_cast<int>(cluster % p.g_wclusters);
     }
     const int64_t stage0 = cluster * p.stages_per_cluster;
     const int nst = static_cast<int>(std::min<int64_t>(p.stages_per_cluster, p.n_stages - stage0));
@@ -347,6 +357,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
         int issued = 0;
         bool xdone = false;
         const int npre = p.static_w ? std::min(nst, static_cast<int>(p.nstage)) : 0;
+        #pragma unroll 1
         for (int j = 0; j < nst; ++j) {
             if (p.static_w && !xdone && j == npre) {
                 grid_dependency_wait();
@@ -381,6 +392,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                 slot_stage[slot] = j;
                 mbar_expect_tx(bar, tx);
                 const int32_t x0 = static_cast<int32_t>(rank * p.code_seg), y0 = static_cast<int32_t>(wrow0 + row0);
+                #pragma unroll 1
                 for (uint32_t c = 0; c < p.nbox; ++c)
                     tma_load_2d(smem_u32(st + c * kRows * 128), &p.tm_codes, x0 + 128 * c, y0, bar);
                 if (p.scale_seg && S > 1) {
@@ -396,6 +408,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                     bulk_g2s(smem_u32(st + p.off_scales), p.scales + off, span_bulk, bar);
                     if (p.biases) bulk_g2s(smem_u32(st + p.off_biases), p.biases + off, span_bulk, bar);
                 }
+                #pragma unroll 1
                 for (uint32_t b = span_bulk + lane; b < span; b += 32) {  // ragged tail of the last stage
                     st[p.off_scales + b] = p.scales[off + b];
                     if (p.biases) st[p.off_biases + b] = p.biases[off + b];
@@ -413,6 +426,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
         }
         if (s_abort) {
             // abandoned: let the copies already issued land before the CTA exits
+            #pragma unroll 1
             for (int j = std::max(0, issued - static_cast<int>(p.nstage)); j < issued; ++j)
                 (void)mbar_wait(bar_full0 + 8 * (j % p.nstage), (j / p.nstage) & 1);
             (void)mbar_wait(bar_x, 0);
@@ -430,7 +444,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
             // max |x| per token: one pass over the staged rows, order-free
             // (warp maxima first: one shared atomic per warp and token)
             const int per_row = static_cast<int>(p.krange / 8);
+            #pragma unroll 1
             for (int m = 0; m < M; ++m)
+                #pragma unroll 1
                 for (int i0 = 0; i0 < per_row; i0 += kWarps * 32) {
                     const int i = i0 + ctid;
                     float amax = 0.0f;
@@ -465,6 +481,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
         float2* tok = reinterpret_cast<float2*>(smem + p.off_tok);  // [groups][16]
         {
             const int items = groups * 32 * NT;  // a multiple of 32: a warp shares (gi, nt)
+            #pragma unroll 1
             for (int it = ctid; it < items; it += kWarps * 32) {
                 const int ln = it % 32, nt = (it / 32) % NT, gi = it / (32 * NT);
                 const int tg = ln >> 2, t = ln & 3;
@@ -532,11 +549,13 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
         int buf = 0;
         // Every warp of a team runs the same iterations and meets the team
         // barrier once per stage, abandoned or not, so no barrier is left waiting.
+        #pragma unroll 1
         for (int j = team; j < nst; j += nteams) {
             const uint32_t slot = j % p.nstage;
             bool live = !s_abort;
             if (live && lane == 0 && slot_stage[slot] != j) {  // the producer has not started stage j yet
                 const uint64_t t0 = globaltimer();
+                #pragma unroll 1
                 for (int spin = 0; slot_stage[slot] != j && !s_abort; ++spin)
                     if ((spin & 63) == 63 && globaltimer() - t0 > kWaitLimitNs) {
                         atomicOr(&g_err_gemv, DEV_ERR_TIMEOUT);
@@ -627,6 +646,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
             // groups two at a time: four independent MMA chains in flight
             const int gend = live ? ge : gb;
             int gi = gb;
+            #pragma unroll 1
             for (; gi + 1 < gend; gi += 2) {
                 float acc0[2][NT][4], acc1[2][NT][4];
                 do_group(gi, acc0);
@@ -659,17 +679,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                     partial[(j * kRows + r) * 16 + m] = v;
                 }
             };
-            if (T == 1) {
-                if (live && !s_abort) {
-#pragma unroll
-                    for (int tt = 0; tt < 2; ++tt)
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                            for (int i = 0; i < 4; ++i) store(tt, nt, lane, i, y[tt][nt][i]);
-                }
-            } else {
-                // red[team][buf][warp of team][tt][nt][lane][4]
+            {
+                // red[team][buf][warp of team][tt][nt][lane][4] (a team of one
+                // goes through it too: one store loop instead of an unrolled one)
                 constexpr int E = 2 * NT * 32 * 4;  // floats per warp partial
                 float* base = red + ((team * 2 + buf) * T) * E;
                 float* mine = base + wi * E;
@@ -682,8 +694,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                 named_bar_sync(2 + team, T * 32);
                 if (live && !s_abort) {
                     // warp wi adds entries [wi*E/T, (wi+1)*E/T) over the team's warps in order
+                    #pragma unroll 1
                     for (int e = wi * (E / T) + lane; e < (wi + 1) * (E / T); e += 32) {
                         float sum = 0.0f;
+                        #pragma unroll 1
                         for (int q = 0; q < T; ++q) sum += base[q * E + e];
                         const int i = e & 3, ln = (e >> 2) & 31, tn = e >> 7;
                         store(tn / NT, tn % NT, ln, i, sum);
@@ -704,6 +718,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
         const float* own = reinterpret_cast<const float*>(smem + p.off_xraw);  // [row][16]
         if (rank != 0) {
             const uint32_t dst = map_shared_rank(smem_u32(smem + p.off_recv), 0) + (rank - 1) * ent * 4u;
+            #pragma unroll 1
             for (int e = threadIdx.x; e < ent; e += blockDim.x)
                 st_shared_cluster_f32(dst + 4u * e, own[(e / M) * 16 + e % M]);
             mbar_arrive_cluster(map_shared_rank(bar_red, 0));
@@ -711,12 +726,14 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
             const bool ok = mbar_wait(bar_red, 0);
             if (!ok && threadIdx.x == 0) atomicOr(&g_err_gemv, DEV_ERR_TIMEOUT);
             const float* recv = reinterpret_cast<const float*>(smem + p.off_recv);  // [rank - 1][ent]
+            #pragma unroll 1
             for (int e = threadIdx.x; ok && e < ent; e += blockDim.x) {
                 const int rr = e / M, m = e % M;
                 const int64_t row = stage0 * kRows + rr;
                 if (row >= p.n) continue;
                 float sum = 0.0f;
                 sum += own[rr * 16 + m];
+                #pragma unroll 1
                 for (int q = 1; q < S; ++q) sum += recv[(q - 1) * ent + e];
                 __nv_bfloat16 b = __float2bfloat16_rn(sum);
                 const int64_t yr = p.g_off ? s_pos[m] : m;
@@ -811,13 +828,13 @@ static bool plan_for(const WDesc& w, int64_t M, int S, int per_sm, Plan* out, do
     const int64_t spc = (p.n_stages + G - 1) / G;
     G = (p.n_stages + spc - 1) / spc;
     // shared memory: fixed part, then as many stage slots as fit
-    auto layout = [&](bool with_red) -> int64_t {
+    auto layout = [&]() -> int64_t {
         p.off_tokscale = 512;  // [16] 2^-E, [16] unused, [16] max |x| bits
         p.off_tok = p.off_tokscale + 256;
         p.off_xfrag = round_up(p.off_tok + groups * 16 * 8, 128);
         const uint64_t xfrag_bytes = static_cast<uint64_t>(kr) * 16 * NT;
         p.off_red = round_up(p.off_xfrag + xfrag_bytes, 128);
-        const uint64_t red_bytes = with_red ? static_cast<uint64_t>(kWarps) * 2 * 2 * NT * 32 * 4 * 4 : 0;
+        const uint64_t red_bytes = static_cast<uint64_t>(kWarps) * 2 * 2 * NT * 32 * 4 * 4;
         p.off_xraw = round_up(p.off_red + red_bytes, 128);
         const uint64_t partial_bytes = S > 1 ? static_cast<uint64_t>(spc) * kRows * 16 * 4 : 0;
         const uint64_t xraw_bytes = static_cast<uint64_t>(M) * kr * 2;
@@ -828,14 +845,13 @@ static bool plan_for(const WDesc& w, int64_t M, int S, int per_sm, Plan* out, do
         const int64_t room = budget - p.off_stages;
         return std::min<int64_t>(std::min<int64_t>(kMaxStages, room / p.stage_bytes), std::max<int64_t>(2, spc));
     };
-    int64_t nst = layout(true);
+    const int64_t nst = layout();
     if (nst < 2) return false;
     // teams: one per stage a CTA can hold in flight, each warp at least one group
     int teams = 1;
     while (teams * 2 <= kWarps && teams * 2 <= spc && teams * 2 <= nst) teams *= 2;
     int T = kWarps / teams;
     while (T > 1 && T > groups) T /= 2;
-    if (T == 1) nst = layout(false);
     p.team = T;
     p.nstage = static_cast<uint32_t>(nst);
     p.S = S;
@@ -1010,10 +1026,10 @@ qm_status launch_gemv_grouped(const WDesc& w, const int32_t* offsets, const int3
     p.static_w = 0;
     p.g_off = offsets;
     p.g_perm = perm;
-    p.g_E = E;
+    p.g_E = static_cast<int>(E);
     p.g_Q = Q;
     p.g_xdiv = xdiv;
-    p.g_wclusters = pl.grid / pl.S;
+    p.g_wclusters = static_cast<int>(pl.grid / pl.S);
     const int64_t rows = E * w.n;
     bool maps = make_tmap_2d(&p.tm_codes, w.codes, w.code_row_bytes, rows, w.code_row_bytes, 128, kRows, true);
     if (maps && p.S > 1 && p.scale_seg) {
