@@ -8,7 +8,7 @@
 // enter a kind::f16 MMA; the sums are float32 in TMEM. The rounding of the
 // weights stays inside the product's error bound (a relative 2^-9 per value).
 //
-// One CTA per 128 x 128 output tile (tokens x weight rows):
+// One CTA per BM x 128 output tile (tokens x weight rows; BM 128 or 256):
 //  * warp 0, one lane: TMA producer. Activation tiles (128 tokens x 64 k,
 //    bf16, 128B-swizzled: the canonical K-major layout the MMA reads) and raw
 //    packed chunks of the weight tile (128 rows x 256 or 128 k values).
@@ -69,7 +69,7 @@ struct Params {
     int64_t M, n, k;
     int64_t scale_row_bytes;
     int sdt;
-    int ksteps, mtiles;
+    int ksteps, mtiles, ntiles;
     uint32_t off_x, off_b, off_raw, raw_stage_bytes;
     // grouped mode (apply_experts), off when g_off is null: x holds the routed
     // activation rows expert by expert, the weight is [E, n, k], and m tile
@@ -110,6 +110,41 @@ QM_DEV Sc load_scale(const Params& p, int64_t grow, int64_t vidx) {
         r.s = e8m0_to_f32(__ldg(p.scales + grow * p.scale_row_bytes + vidx / 32));
     }
     return r;
+}
+
+// Q8_0 block B (0..7) of a raw chunk row as 16 bf16 pairs. Rows are 272
+// bytes apart; block B starts 2B bytes past the 16-byte boundary at 32B, so
+// three aligned 16-byte loads cover it (and end inside the row). A warp's
+// lanes take consecutive rows, whose 16-byte pieces then fall in distinct
+// bank groups: 272 is 17 sixteen-byte units.
+template <int B>
+QM_DEV void decode_q8_block(const uint8_t* raw, int row, uint32_t (&o)[16]) {
+    const uint4* src = reinterpret_cast<const uint4*>(raw + row * 272 + 32 * B);
+    uint32_t w[12];
+#pragma unroll
+    for (int q = 0; q < 3; ++q) {
+        const uint4 v = src[q];
+        w[4 * q] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
+    }
+    constexpr int kD = B / 2, kDs = (B & 1) * 16;              // f16 scale: word, shift
+    constexpr int kQ = (B + 1) / 2, kQs = ((B + 1) & 1) * 16;  // first code byte: word, shift
+    const float d = f16_bits_to_f32((w[kD] >> kDs) & 0xFFFFu);
+    const float2 neg = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
+    const float2 d2 = make_float2(d, d);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        uint32_t u;
+        if constexpr (kQs == 0) u = w[kQ + j];
+        else u = __funnelshift_r(w[kQ + j], w[kQ + j + 1], kQs);
+        u ^= 0x80808080u;  // q + 128 per byte
+#pragma unroll
+        for (int i = 0; i < 4; i += 2) {
+            const float2 f = make_float2(__uint_as_float(prmt(u, 0x4B000000u, 0x7540 + i)),
+                                         __uint_as_float(prmt(u, 0x4B000000u, 0x7541 + i)));
+            const float2 v = mul2(add2(f, neg), d2);
+            o[(4 * j + i) / 2] = bf2(v.x, v.y);
+        }
+    }
 }
 
 // The 32 values of one decoder thread's half row (values kk*64 + half*32 .. of
@@ -155,30 +190,16 @@ QM_DEV void decode32(const uint8_t* raw, int row, int kk, int half, Sc sc, uint3
                 o[4 * j + i] = bf2(v.x, v.y);
             }
         }
-    } else {  // Q8_0: block kk*2 + half of the chunk; 34 bytes, rows 272 bytes apart
-        const uint32_t base = row * 272 + (kk * 2 + half) * 34;  // 2-byte aligned
-        const uint32_t* wp = reinterpret_cast<const uint32_t*>(raw + ((base + 2) & ~3u));
-        const uint32_t dw = *reinterpret_cast<const uint32_t*>(raw + (base & ~3u));
-        const float d = f16_bits_to_f32((base & 2) ? (dw >> 16) : (dw & 0xFFFF));
-        const uint32_t sh = ((base + 2) & 3) * 8;  // 0 or 16
-        // words 0..7 hold the codes when they start word-aligned (odd blocks);
-        // even blocks also need word 8, which still ends inside the row
-        uint32_t w[9];
-#pragma unroll
-        for (int j = 0; j < 8; ++j) w[j] = wp[j];
-        w[8] = sh ? wp[8] : 0u;
-        const float2 neg = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
-        const float2 d2 = make_float2(d, d);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const uint32_t u = __funnelshift_r(w[j], w[j + 1], sh) ^ 0x80808080u;  // q + 128 per byte
-#pragma unroll
-            for (int i = 0; i < 4; i += 2) {
-                const float2 f = make_float2(__uint_as_float(prmt(u, 0x4B000000u, 0x7540 + i)),
-                                             __uint_as_float(prmt(u, 0x4B000000u, 0x7541 + i)));
-                const float2 v = mul2(add2(f, neg), d2);
-                o[(4 * j + i) / 2] = bf2(v.x, v.y);
-            }
+    } else {  // Q8_0: block kk*2 + half of the chunk (kk is a constant once the k loop unrolls)
+        switch (2 * kk + half) {
+            case 0: decode_q8_block<0>(raw, row, o); break;
+            case 1: decode_q8_block<1>(raw, row, o); break;
+            case 2: decode_q8_block<2>(raw, row, o); break;
+            case 3: decode_q8_block<3>(raw, row, o); break;
+            case 4: decode_q8_block<4>(raw, row, o); break;
+            case 5: decode_q8_block<5>(raw, row, o); break;
+            case 6: decode_q8_block<6>(raw, row, o); break;
+            default: decode_q8_block<7>(raw, row, o); break;
         }
     }
 }
@@ -192,7 +213,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     constexpr uint32_t kTmemCols = BN * NACC;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int mt = blockIdx.x % p.mtiles, nt = blockIdx.x / p.mtiles;
+    // plain: m tiles fastest (the activations stay in L2 while each weight tile
+    // is read once); grouped: n tiles fastest, so one expert's tiles run
+    // together and share its weight and its rows of x through L2
+    const int mt = p.g_off ? blockIdx.x / p.ntiles : blockIdx.x % p.mtiles;
+    const int nt = p.g_off ? blockIdx.x % p.ntiles : blockIdx.x / p.mtiles;
     int64_t m0 = static_cast<int64_t>(mt) * BM, mend = p.M;  // this tile's rows of x: [m0, min(m0 + BM, mend))
     int64_t wrow0 = 0;                                       // first row of the tile's matrix in the weight
     const int64_t n0 = static_cast<int64_t>(nt) * BN;
@@ -340,8 +365,10 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         }
     } else {
         // ------------------------------------------------------------ decoders
-        const int d = threadIdx.x - 64;
-        const int row = d >> 1, half = d & 1;
+        // a warp takes 32 consecutive rows and one half of their values:
+        // its shared-memory reads and writes then hit distinct banks
+        const int dw = warp - 2;
+        const int row = (dw >> 1) * 32 + lane, half = dw & 1;
         const int64_t grow = n0 + row;
         const bool rowok = grow < p.n;
         Sc cur[R::SPR], nxt[R::SPR];
@@ -454,6 +481,7 @@ static cudaError_t launch_t(Params& p, const WDesc& w, const void* x, cudaStream
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int64_t ntiles = (w.n + BN - 1) / BN;
+    p.ntiles = static_cast<int>(ntiles);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.mtiles * ntiles));
     cfg.blockDim = dim3(kThreads);
