@@ -8,17 +8,25 @@
 // enter a kind::f16 MMA; the sums are float32 in TMEM. The rounding of the
 // weights stays inside the product's error bound (a relative 2^-9 per value).
 //
-// One CTA per BM x 128 output tile (tokens x weight rows; BM 128 or 256):
-//  * warp 0, one lane: TMA producer. Activation tiles (128 tokens x 64 k,
-//    bf16, 128B-swizzled: the canonical K-major layout the MMA reads) and raw
-//    packed chunks of the weight tile (128 rows x 256 or 128 k values).
-//  * warps 2..9: decoders. Each thread turns half of one weight row's 64
-//    values per k step into bf16 and writes them, 128B-swizzled, into the
-//    B tile; scales are fetched from global memory one chunk ahead. After
-//    the k loop they read the accumulator out of TMEM and store y.
-//  * warp 1, one lane: issues tcgen05.mma (M = 128, N = 128, K = 16, four per
-//    k step) into a 128-column TMEM accumulator and commits each stage back
-//    to its producers through mbarriers.
+// One CTA per tile of 128 weight rows x NTOK tokens (NTOK 128 or 256; grid:
+// token tiles fastest so x stays in L2 while each weight tile is read once;
+// experts: weight tiles fastest within each expert's rows). The roles of the
+// MMA operands are turned round from y = x W^T: the decoded weight tile is
+// A (M = 128 rows, one TMEM lane each) and lives in tensor memory, written
+// there by the decoders with tcgen05.st; the activation tile is B (N = NTOK)
+// in shared memory. Decoded weights never pass through shared memory, whose
+// bandwidth then serves only the TMA fills and the MMA's activation reads.
+//  * warp 0, one lane: TMA producer. Activation tiles (NTOK tokens x 64 k,
+//    bf16, 128B-swizzled: the canonical K-major layout) and raw packed chunks
+//    of the weight tile (128 rows x 256 or 128 k values).
+//  * warp 1, one lane: tcgen05.mma (M = 128, N = NTOK, K = 16, four per k
+//    step, A from TMEM) into an NTOK-column accumulator, committing each stage
+//    back to its producers through mbarriers; warp 1 also owns the TMEM
+//    allocation (512 columns: accumulator, then four 32-column weight stages).
+//  * warps 2..9: decoders, two groups of four taking alternate k steps; warp w
+//    owns TMEM lane quarter w % 4, so a thread decodes one weight row's 64
+//    values per k step (scales fetched from global memory one chunk ahead).
+//    After the k loop they read the accumulator back and store y.
 // Every wait is bounded; a wait that gives up raises the device flag and the
 // CTA winds down with its copies and MMAs drained.
 #include <cuda.h>
@@ -42,12 +50,10 @@ uint32_t gemm_read_clear_error() {
 
 namespace gemm {
 
-constexpr int BN = 128, BK = 64;
+constexpr int BK = 64;          // k values per step
 constexpr int kDecWarps = 8;
 constexpr int kThreads = 64 + kDecWarps * 32;
-constexpr int NB = 3, NR = 2;  // ring depths: bf16 B tiles, raw chunks
-constexpr uint32_t kBTileBytes = BN * BK * 2;  // 16 KB
-constexpr int NXof(int BM) { return BM == 256 ? 3 : 4; }  // activation tiles in flight
+constexpr int NR = 2;           // raw chunk slots
 
 // Raw chunk geometry per format: values per chunk, bytes per row per chunk,
 // whether the TMA box is 128B-swizzled, and the tensor map's element size.
@@ -61,7 +67,7 @@ struct Raw {
 };
 
 struct Params {
-    CUtensorMap tm_x;    // x as bytes [M, 2k], boxes of 128 B x BM rows, 128B-swizzled
+    CUtensorMap tm_x;    // x as bytes [M, 2k], boxes of 128 B x NTOK rows, 128B-swizzled
     CUtensorMap tm_raw;  // codes as [n, code_row_bytes], boxes of Raw::BYTES x 128 rows
     const uint8_t* scales;
     const uint8_t* biases;
@@ -70,7 +76,7 @@ struct Params {
     int64_t scale_row_bytes;
     int sdt;
     int ksteps, mtiles, ntiles;
-    uint32_t off_x, off_b, off_raw, raw_stage_bytes;
+    uint32_t off_x, off_raw, raw_stage_bytes;
     // grouped mode (apply_experts), off when g_off is null: x holds the routed
     // activation rows expert by expert, the weight is [E, n, k], and m tile
     // slot t is the t-th BM-row tile of the experts' row ranges in order
@@ -204,43 +210,89 @@ QM_DEV void decode32(const uint8_t* raw, int row, int kk, int half, Sc sc, uint3
     }
 }
 
-template <int FMT, int BITS, int GS, int BM>
+// ---------------------------------------------------------------- kernel
+namespace ts {
+constexpr int BW = 128;                // weight rows per CTA
+constexpr int NA = 4;                  // decoded weight stages in TMEM
+constexpr int NXT = 4;                 // activation tiles in flight
+constexpr uint32_t kAcol = 256;        // first TMEM column of the weight stages (32 columns each)
+constexpr uint32_t kCols = 512;        // TMEM columns held: accumulator [0, NTOK), weight stages
+}  // namespace ts
+
+// Grouped mode, one warp: which expert's rows of x m-tile slot `mt` covers
+// (s_grp: found, expert, first row, end row), bm rows to a tile.
+static __device__ __noinline__ void tile_lookup(const Params& p, int mt, int bm, int lane, int* s_grp) {
+    int before = 0;  // tiles of the experts already passed
+    int found = 0, ge = 0, gm0 = 0, gend = 0;
+    for (int e0 = 0; e0 < p.g_E; e0 += 32) {
+        const int e = e0 + lane;
+        int o0 = 0, cnt = 0;
+        if (e < p.g_E) {
+            o0 = __ldg(p.g_off + e);
+            cnt = __ldg(p.g_off + e + 1) - o0;
+        }
+        const int nch = (cnt + bm - 1) / bm;
+        int inc = nch;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += t;
+        }
+        const int lo = before + inc - nch;
+        const bool mine = e < p.g_E && mt >= lo && mt < lo + nch;
+        const uint32_t hit = __ballot_sync(0xffffffffu, mine);
+        if (mine) {
+            found = 1;
+            ge = e;
+            gm0 = o0 + (mt - lo) * bm;
+            gend = o0 + cnt;
+        }
+        if (hit) {
+            const int src = __ffs(hit) - 1;
+            found = __shfl_sync(0xffffffffu, found, src);
+            ge = __shfl_sync(0xffffffffu, ge, src);
+            gm0 = __shfl_sync(0xffffffffu, gm0, src);
+            gend = __shfl_sync(0xffffffffu, gend, src);
+            break;
+        }
+        before += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    if (lane == 0) { s_grp[0] = found; s_grp[1] = ge; s_grp[2] = gm0; s_grp[3] = gend; }
+}
+
+template <int FMT, int BITS, int GS, int NTOK>
 __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ Params p) {
     using R = Raw<FMT, BITS>;
-    constexpr int NX = NXof(BM);
-    constexpr int NACC = BM / 128;                 // 128-token accumulators sharing each B tile
-    constexpr uint32_t kXBytes = BM * BK * 2;      // activation tile per k step
-    constexpr uint32_t kTmemCols = BN * NACC;
+    using namespace ts;
+    constexpr uint32_t kXBytes = NTOK * BK * 2;  // activation tile per k step
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // plain: m tiles fastest (the activations stay in L2 while each weight tile
-    // is read once); grouped: n tiles fastest, so one expert's tiles run
-    // together and share its weight and its rows of x through L2
     const int mt = p.g_off ? blockIdx.x / p.ntiles : blockIdx.x % p.mtiles;
     const int nt = p.g_off ? blockIdx.x % p.ntiles : blockIdx.x / p.mtiles;
-    int64_t m0 = static_cast<int64_t>(mt) * BM, mend = p.M;  // this tile's rows of x: [m0, min(m0 + BM, mend))
-    int64_t wrow0 = 0;                                       // first row of the tile's matrix in the weight
-    const int64_t n0 = static_cast<int64_t>(nt) * BN;
+    int64_t m0 = static_cast<int64_t>(mt) * NTOK, mend = p.M;  // this tile's rows of x
+    int64_t wrow0 = 0;                                          // first row of the tile's matrix
+    const int64_t n0 = static_cast<int64_t>(nt) * BW;
     const int ks_n = p.ksteps;
     const int nchunks = (ks_n + R::SPR - 1) / R::SPR;
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
     const uint32_t b0 = smem_u32(bars);
     auto x_full = [&](int i) { return b0 + 8 * i; };
-    auto x_empty = [&](int i) { return b0 + 8 * (NX + i); };
-    auto b_full = [&](int i) { return b0 + 8 * (2 * NX + i); };
-    auto b_empty = [&](int i) { return b0 + 8 * (2 * NX + NB + i); };
-    auto r_full = [&](int i) { return b0 + 8 * (2 * NX + 2 * NB + i); };
-    auto r_empty = [&](int i) { return b0 + 8 * (2 * NX + 2 * NB + NR + i); };
-    const uint32_t done = b0 + 8 * (2 * NX + 2 * NB + 2 * NR);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 8 * (2 * NX + 2 * NB + 2 * NR + 1));
-    volatile int& s_abort = *reinterpret_cast<volatile int*>(smem + 8 * (2 * NX + 2 * NB + 2 * NR + 2));
-    int* s_grp = reinterpret_cast<int*>(smem + 8 * (2 * NX + 2 * NB + 2 * NR + 3));  // [4], below 1 KB
+    auto x_empty = [&](int i) { return b0 + 8 * (NXT + i); };
+    auto a_full = [&](int i) { return b0 + 8 * (2 * NXT + i); };
+    auto a_empty = [&](int i) { return b0 + 8 * (2 * NXT + NA + i); };
+    auto r_full = [&](int i) { return b0 + 8 * (2 * NXT + 2 * NA + i); };
+    auto r_empty = [&](int i) { return b0 + 8 * (2 * NXT + 2 * NA + NR + i); };
+    constexpr int kB = 2 * NXT + 2 * NA + 2 * NR;
+    const uint32_t done = b0 + 8 * kB;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + 8 * (kB + 1));
+    volatile int& s_abort = *reinterpret_cast<volatile int*>(smem + 8 * (kB + 2));
+    int* s_grp = reinterpret_cast<int*>(smem + 8 * (kB + 3));  // [4], below 1 KB
 
     if (threadIdx.x == 0) {
         s_abort = 0;
-        for (int i = 0; i < NX; ++i) { mbar_init(x_full(i), 1); mbar_init(x_empty(i), 1); }
-        for (int i = 0; i < NB; ++i) { mbar_init(b_full(i), kDecWarps); mbar_init(b_empty(i), 1); }
+        for (int i = 0; i < NXT; ++i) { mbar_init(x_full(i), 1); mbar_init(x_empty(i), 1); }
+        for (int i = 0; i < NA; ++i) { mbar_init(a_full(i), 4); mbar_init(a_empty(i), 1); }
         for (int i = 0; i < NR; ++i) { mbar_init(r_full(i), 1); mbar_init(r_empty(i), kDecWarps); }
         mbar_init(done, 1);
         fence_mbar_init();
@@ -248,45 +300,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         prefetch_tmap(&p.tm_raw);
     }
     if (p.g_off) {
-        // which expert's rows: the routing offsets come from an earlier kernel
         if (warp == 0) {
-            grid_dependency_wait();
-            int64_t before = 0;  // tiles of the experts already passed
-            int found = 0, ge = 0, gm0 = 0, gend = 0;
-            for (int64_t e0 = 0; e0 < p.g_E; e0 += 32) {
-                const int64_t e = e0 + lane;
-                int o0 = 0, cnt = 0;
-                if (e < p.g_E) {
-                    o0 = __ldg(p.g_off + e);
-                    cnt = __ldg(p.g_off + e + 1) - o0;
-                }
-                const int64_t nch = (cnt + BM - 1) / BM;
-                int64_t inc = nch;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const int64_t t = __shfl_up_sync(0xffffffffu, inc, o);
-                    if (lane >= o) inc += t;
-                }
-                const int64_t lo = before + inc - nch;
-                const bool mine = e < p.g_E && mt >= lo && mt < lo + nch;
-                const uint32_t hit = __ballot_sync(0xffffffffu, mine);
-                if (mine) {
-                    found = 1;
-                    ge = static_cast<int>(e);
-                    gm0 = o0 + static_cast<int>(mt - lo) * BM;
-                    gend = o0 + cnt;
-                }
-                if (hit) {
-                    const int src = __ffs(hit) - 1;
-                    found = __shfl_sync(0xffffffffu, found, src);
-                    ge = __shfl_sync(0xffffffffu, ge, src);
-                    gm0 = __shfl_sync(0xffffffffu, gm0, src);
-                    gend = __shfl_sync(0xffffffffu, gend, src);
-                    break;
-                }
-                before += __shfl_sync(0xffffffffu, inc, 31);
-            }
-            if (lane == 0) { s_grp[0] = found; s_grp[1] = ge; s_grp[2] = gm0; s_grp[3] = gend; }
+            grid_dependency_wait();  // the routing offsets come from an earlier kernel
+            tile_lookup(p, mt, NTOK, lane, s_grp);
         }
         __syncthreads();
         if (!s_grp[0]) return;  // a slot past the last tile: nothing allocated yet
@@ -295,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         mend = s_grp[3];
     }
     if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_alloc(smem_u32(tmem_slot), kCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -318,14 +334,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 if (ks % R::SPR == 0) {
                     const int rc = ks / R::SPR, sr = rc % NR;
                     if (!mbar_wait(r_empty(sr), ((rc / NR) & 1) ^ 1)) { give_up(); break; }
-                    mbar_expect_tx(r_full(sr), R::BYTES * BN);
+                    mbar_expect_tx(r_full(sr), R::BYTES * BW);
                     tma_load_2d(smem_u32(smem + p.off_raw + sr * p.raw_stage_bytes), &p.tm_raw,
                                 rc * R::BYTES / R::ELEM, static_cast<int32_t>(wrow0 + n0), r_full(sr));
                     mbar_arrive(r_full(sr));
                     last_r = rc;
                 }
-                const int sx = ks % NX;
-                if (!mbar_wait(x_empty(sx), ((ks / NX) & 1) ^ 1)) { give_up(); break; }
+                const int sx = ks % NXT;
+                if (!mbar_wait(x_empty(sx), ((ks / NXT) & 1) ^ 1)) { give_up(); break; }
                 mbar_expect_tx(x_full(sx), kXBytes);
                 tma_load_2d(smem_u32(smem + p.off_x + sx * kXBytes), &p.tm_x, ks * 128, static_cast<int32_t>(m0),
                             x_full(sx));
@@ -333,8 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 last_x = ks;
             }
             if (s_abort) {  // let issued copies land before the CTA winds down
-                for (int ks = std::max(0, last_x - NX + 1); ks <= last_x; ++ks)
-                    (void)mbar_wait(x_full(ks % NX), (ks / NX) & 1);
+                for (int ks = std::max(0, last_x - NXT + 1); ks <= last_x; ++ks)
+                    (void)mbar_wait(x_full(ks % NXT), (ks / NXT) & 1);
                 for (int rc = std::max(0, last_r - NR + 1); rc <= last_r; ++rc)
                     (void)mbar_wait(r_full(rc % NR), (rc / NR) & 1);
             }
@@ -342,41 +358,41 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            constexpr uint32_t idesc = umma_idesc_bf16(128, BN);
+            constexpr uint32_t idesc = umma_idesc_bf16(BW, NTOK);
             for (int ks = 0; ks < ks_n && !s_abort; ++ks) {
-                const int sx = ks % NX, sb = ks % NB;
-                if (!mbar_wait(x_full(sx), (ks / NX) & 1) || !mbar_wait(b_full(sb), (ks / NB) & 1)) {
+                const int sx = ks % NXT, sa = ks % NA;
+                if (!mbar_wait(x_full(sx), (ks / NXT) & 1) || !mbar_wait(a_full(sa), (ks / NA) & 1)) {
                     give_up();
                     break;
                 }
                 tc_fence_after();
-                const uint32_t xa = smem_u32(smem + p.off_x + sx * kXBytes);
-                const uint64_t bd = umma_desc_sw128(smem_u32(smem + p.off_b + sb * kBTileBytes));
+                const uint64_t bd = umma_desc_sw128(smem_u32(smem + p.off_x + sx * kXBytes));
+                const uint32_t ad = tmem + kAcol + 32 * sa;
 #pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk)  // advance 16 values = 32 bytes inside the swizzle atom
-#pragma unroll
-                    for (int a = 0; a < NACC; ++a)
-                        umma_f16(tmem + a * BN, umma_desc_sw128(xa + a * 128 * 128) + 2 * kk, bd + 2 * kk, idesc,
-                                 ks > 0 || kk > 0);
+                for (int kk = 0; kk < BK / 16; ++kk)  // 16 values: 8 TMEM columns of A, 32 bytes of B
+                    umma_f16_ts(tmem, ad + 8 * kk, bd + 2 * kk, idesc, ks > 0 || kk > 0);
                 umma_commit(x_empty(sx));
-                umma_commit(b_empty(sb));
+                umma_commit(a_empty(sa));
             }
             umma_commit(done);  // also drains whatever was issued when abandoning
         }
     } else {
         // ------------------------------------------------------------ decoders
-        // a warp takes 32 consecutive rows and one half of their values:
-        // its shared-memory reads and writes then hit distinct banks
-        const int dw = warp - 2;
-        const int row = (dw >> 1) * 32 + lane, half = dw & 1;
+        const int grp = (warp - 2) >> 2;           // k steps ks with ks % 2 == grp
+        const int quarter = warp & 3;              // this warp's TMEM lanes
+        const int row = 32 * quarter + lane;
+        const uint32_t lane_addr = static_cast<uint32_t>(32 * quarter) << 16;
         const int64_t grow = n0 + row;
         const bool rowok = grow < p.n;
-        Sc cur[R::SPR], nxt[R::SPR];
-        auto fetch = [&](int rc, Sc (&dst)[R::SPR]) {
+        Sc cur[R::SPR][2], nxt[R::SPR][2];
+        auto fetch = [&](int rc, Sc (&dst)[R::SPR][2]) {
 #pragma unroll
             for (int kk = 0; kk < R::SPR; ++kk)
-                dst[kk] = rowok ? load_scale<FMT, BITS, GS>(p, wrow0 + grow, static_cast<int64_t>(rc) * R::RAWK + kk * BK + half * 32)
-                                : Sc{0.0f, 0.0f};
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+                    dst[kk][h] = rowok ? load_scale<FMT, BITS, GS>(p, wrow0 + grow,
+                                                                   static_cast<int64_t>(rc) * R::RAWK + kk * BK + h * 32)
+                                       : Sc{0.0f, 0.0f};
         };
         fetch(0, cur);
         for (int rc = 0; rc < nchunks; ++rc) {
@@ -388,99 +404,115 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
             for (int kk = 0; kk < R::SPR; ++kk) {
                 const int ks = rc * R::SPR + kk;
                 if (ks >= ks_n) break;
-                const int sb = ks % NB;
-                if (live && !mbar_wait(b_empty(sb), ((ks / NB) & 1) ^ 1)) live = false;
+                if ((ks & 1) != grp) continue;
+                const int sa = ks % NA;
+                if (live && !mbar_wait(a_empty(sa), ((ks / NA) & 1) ^ 1)) live = false;
                 if (!live) {
                     if (lane == 0) give_up();
                     break;
                 }
-                uint32_t o[16];
-                if (rowok && static_cast<int64_t>(ks) * BK + half * 32 < p.k) {
-                    decode32<FMT, BITS, GS>(raw, row, kk, half, cur[kk], o);
+                uint32_t o0[16], o1[16];
+                if (rowok && static_cast<int64_t>(ks) * BK < p.k) {
+                    decode32<FMT, BITS, GS>(raw, row, kk, 0, cur[kk][0], o0);
                 } else {
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) o[i] = 0u;
+                    for (int i = 0; i < 16; ++i) o0[i] = 0u;
                 }
-                uint8_t* bt = smem + p.off_b + sb * kBTileBytes;
+                if (rowok && static_cast<int64_t>(ks) * BK + 32 < p.k) {
+                    decode32<FMT, BITS, GS>(raw, row, kk, 1, cur[kk][1], o1);
+                } else {
 #pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    *reinterpret_cast<uint4*>(bt + sw128(row, half * 4 + j)) =
-                        make_uint4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-                fence_proxy_async_smem();  // the tensor cores read B through the async proxy
+                    for (int i = 0; i < 16; ++i) o1[i] = 0u;
+                }
+                const uint32_t ta = tmem + lane_addr + kAcol + 32 * sa;
+                tmem_st16(ta, o0);
+                tmem_st16(ta + 16, o1);
+                tmem_wait_st();
+                tc_fence_before();  // the MMA reads the stage after the barrier
                 __syncwarp();
-                if (lane == 0) mbar_arrive(b_full(sb));
+                if (lane == 0) mbar_arrive(a_full(sa));
             }
             __syncwarp();
             if (lane == 0 && live) mbar_arrive(r_empty(sr));
             if (!live) break;
 #pragma unroll
-            for (int kk = 0; kk < R::SPR; ++kk) cur[kk] = nxt[kk];
+            for (int kk = 0; kk < R::SPR; ++kk) {
+                cur[kk][0] = nxt[kk][0];
+                cur[kk][1] = nxt[kk][1];
+            }
         }
         // ------------------------------------------------------------ epilogue
         const bool ok = mbar_wait(done, 0);
         if (!ok && lane == 0) give_up();
         tc_fence_after();
-        // warp -> TMEM lane quarter (tokens) and a share of the accumulator columns
-        const int quarter = warp & 3, part = (warp - 2) >> 2;  // part 0 / 1
-        constexpr int COLS = BN * NACC / 2;                    // columns per warp
-#pragma unroll
-        for (int j = 0; j < COLS / 32; ++j) {
-            const int col = part * COLS + 32 * j;  // 0 .. BN*NACC
-            const int acc = col / BN, c0 = col % BN;
+        // Each 32 x 32 block (this warp's rows x 32 tokens) turns round through
+        // shared memory (the activation tiles are free now): lane pairs swap
+        // values so each thread holds two adjacent rows of one token, rows are
+        // written token-major (80-byte pitch: conflict-free both ways), then
+        // lane t stores token t's 32 rows as four 16-byte pieces.
+        const int part = grp;  // token columns [part * NTOK / 2, (part + 1) * NTOK / 2)
+        uint8_t* stage = smem + p.off_x + (warp - 2) * (32 * 80);
+        const int64_t row0 = n0 + 32 * quarter;  // this warp's first weight row
+        const bool vec = (p.n & 7) == 0 && row0 + 32 <= p.n;
+        const int odd = lane & 1;
+#pragma unroll 1
+        for (int j = 0; j < NTOK / 64; ++j) {
+            const int col = part * (NTOK / 2) + 32 * j;
             uint32_t r[32];
-            tmem_ld32(tmem + (static_cast<uint32_t>(32 * quarter) << 16) + col, r);
+            tmem_ld32(tmem + lane_addr + col, r);
             tmem_wait_ld();
-            const int64_t m = m0 + 128 * acc + 32 * quarter + lane;
-            if (!ok || s_abort || m >= mend) continue;
-            const int64_t ym = p.g_off ? static_cast<int64_t>(__ldg(p.g_perm + m)) : m;
-            uint16_t* yr = p.y + ym * p.n + n0 + c0;
-            const int64_t left = p.n - (n0 + c0);
-            if (left >= 32 && (p.n & 7) == 0) {
+            if (!ok || s_abort) continue;
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    *reinterpret_cast<uint4*>(yr + 8 * q) =
-                        make_uint4(bf2(__uint_as_float(r[8 * q]), __uint_as_float(r[8 * q + 1])),
-                                   bf2(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3])),
-                                   bf2(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5])),
-                                   bf2(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7])));
-            } else {
+            for (int c = 0; c < 32; c += 2) {
+                const float lo = __uint_as_float(r[c]), hi = __uint_as_float(r[c + 1]);
+                const float got = __shfl_xor_sync(0xffffffffu, odd ? lo : hi, 1);
+                const uint32_t pair = odd ? bf2(got, hi) : bf2(lo, got);  // rows (2i, 2i + 1) of token c + odd
+                *reinterpret_cast<uint32_t*>(stage + (c + odd) * 80 + (lane >> 1) * 4) = pair;
+            }
+            __syncwarp();
+            const int64_t m = m0 + col + lane;
+            if (m < mend) {
+                const int64_t ym = p.g_off ? static_cast<int64_t>(__ldg(p.g_perm + m)) : m;
+                uint16_t* yr = p.y + ym * p.n + row0;
+                const uint8_t* src = stage + lane * 80;
+                if (vec) {
 #pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    if (c < left) {
-                        __nv_bfloat16 b = __float2bfloat16_rn(__uint_as_float(r[c]));
-                        yr[c] = *reinterpret_cast<uint16_t*>(&b);
-                    }
+                    for (int q = 0; q < 4; ++q)
+                        reinterpret_cast<uint4*>(yr)[q] = *reinterpret_cast<const uint4*>(src + 16 * q);
+                } else {
+                    for (int i = 0; i < 32 && row0 + i < p.n; ++i)
+                        yr[i] = reinterpret_cast<const uint16_t*>(src)[i];
                 }
             }
+            __syncwarp();
         }
     }
     tc_fence_before();
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, kTmemCols);
+        tmem_dealloc(tmem, ts::kCols);
     }
 }
 
-template <int FMT, int BITS, int GS, int BM>
+template <int FMT, int BITS, int GS, int NTOK>
 static cudaError_t launch_t(Params& p, const WDesc& w, const void* x, cudaStream_t st) {
     using R = Raw<FMT, BITS>;
-    constexpr int NX = NXof(BM);
-    p.mtiles = p.g_off ? static_cast<int>(std::min<int64_t>(p.M, p.M / BM + p.g_E))  // sum of ceil(count / BM)
-                       : static_cast<int>((p.M + BM - 1) / BM);
+    p.mtiles = p.g_off ? static_cast<int>(std::min<int64_t>(p.M, p.M / NTOK + p.g_E))  // sum of ceil(count / NTOK)
+                       : static_cast<int>((p.M + NTOK - 1) / NTOK);
     p.off_x = 1024;
-    p.off_b = p.off_x + NX * BM * BK * 2;
-    p.off_raw = p.off_b + NB * kBTileBytes;
-    p.raw_stage_bytes = (R::BYTES * BN + 16 + 1023) / 1024 * 1024;  // 16 spare bytes after each slot
+    p.off_raw = p.off_x + ts::NXT * NTOK * BK * 2;
+    p.raw_stage_bytes = (R::BYTES * ts::BW + 16 + 1023) / 1024 * 1024;  // 16 spare bytes after each slot
     const size_t smem = p.off_raw + NR * p.raw_stage_bytes;
-    if (!make_tmap_2d(&p.tm_x, x, static_cast<uint64_t>(w.k) * 2, p.M, static_cast<uint64_t>(w.k) * 2, 128, BM, true))
+    if (!make_tmap_2d(&p.tm_x, x, static_cast<uint64_t>(w.k) * 2, p.M, static_cast<uint64_t>(w.k) * 2, 128, NTOK, true))
         return cudaErrorNotSupported;
-    if (!make_tmap_2d(&p.tm_raw, w.codes, w.code_row_bytes, w.rows, w.code_row_bytes, R::BYTES, BN, R::SW, R::ELEM))
+    if (!make_tmap_2d(&p.tm_raw, w.codes, w.code_row_bytes, w.rows, w.code_row_bytes, R::BYTES, ts::BW, R::SW,
+                      R::ELEM))
         return cudaErrorNotSupported;
-    auto kern = gemm_kernel<FMT, BITS, GS, BM>;
+    auto kern = gemm_kernel<FMT, BITS, GS, NTOK>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    const int64_t ntiles = (w.n + BN - 1) / BN;
+    const int64_t ntiles = (w.n + ts::BW - 1) / ts::BW;
     p.ntiles = static_cast<int>(ntiles);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(p.mtiles * ntiles));
