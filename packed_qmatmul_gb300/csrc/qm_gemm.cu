@@ -529,9 +529,11 @@ static cudaError_t launch_t(Params& p, const WDesc& w, const void* x, cudaStream
 
 template <int FMT, int BITS, int GS>
 static cudaError_t launch_bm(Params& p, const WDesc& w, const void* x, cudaStream_t st) {
-    const int64_t rows_per_matrix = p.g_off ? p.M / std::max<int64_t>(1, p.g_E) : p.M;
-    return rows_per_matrix > 128 ? launch_t<FMT, BITS, GS, 256>(p, w, x, st)
-                                 : launch_t<FMT, BITS, GS, 128>(p, w, x, st);
+    // grouped: 256-token tiles once experts average over 64 positions, so an
+    // expert near the average fills one tile instead of spilling a second one
+    // that decodes its weights again for a few rows
+    const bool wide = p.g_off ? p.M > 64 * std::max<int64_t>(1, p.g_E) : p.M > 128;
+    return wide ? launch_t<FMT, BITS, GS, 256>(p, w, x, st) : launch_t<FMT, BITS, GS, 128>(p, w, x, st);
 }
 
 static cudaError_t dispatch(Params& p, const WDesc& w, const void* x, cudaStream_t st) {
