@@ -329,7 +329,8 @@ def run_experts(args, rank, world):
         peak = peaks.get("bf16_tflops", 1900.0)
         value, unit, metric = flops * world / t_step / 1e12, "TFLOP/s", EXPERTS_TFLOPS
         roof = {"bound": "tensor", "achieved": round(flops / t_step / 1e12, 2), "peak": peak, "unit": "TFLOP/s",
-                "frac": round(flops / t_step / 1e12 / peak, 4), "traffic": None,
+                "frac": round(flops / t_step / 1e12 / peak, 4), "traffic": traffic("experts_gemm", T == 4096)[0],
+                "traffic_source": traffic("experts_gemm", T == 4096)[1],
                 "kernel": "grouped gemm_kernel<MXFP4> with routing and gather in the step time",
                 "peak_source": "measured bf16 dense, burst" if "bf16_tflops" in peaks else "fallback"}
     else:
@@ -420,7 +421,8 @@ def run_take(args, rank, world):
                    "l2": "the dequant writes 311 MB (more than L2) between takes",
                    "graph": "step captured once as a CUDA graph"},
         "roofline": {"bound": "hbm", "achieved": round(db / t_d / 1e9, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(db / t_d / 1e9 / peak, 4), "traffic": None,
+                     "frac": round(db / t_d / 1e9 / peak, 4), "traffic": traffic("dequant")[0],
+                     "traffic_source": traffic("dequant")[1],
                      "kernel": "decode_rows_kernel<affine,4> (the full dequant, timed alone)",
                      "peak_source": "measured" if "hbm_gbs" in peaks else "fallback"},
         "gpu_launches": 2 * args.steps, "clocks": clocks,
@@ -504,7 +506,10 @@ def run_ours(args, rank, world):
         "data": "synthetic (seeded; weights and activations drawn as the workload states)",
         "config": config_dict(bits, M),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
-                     "frac": round(achieved / peak, 4), "traffic": None,
+                     "frac": round(achieved / peak, 4),
+                     "traffic": traffic("decode", bits == 4 and M == 1 and not args.only)[0],
+                     "traffic_source": traffic("decode", bits == 4 and M == 1 and not args.only)[1],
+                     "algorithmic_bytes_per_launch": round(algo_bytes / launches_per_step),
                      "kernel": f"gemv_kernel<affine,{bits},64> (every launch of the step)",
                      "peak_source": "measured" if "hbm_gbs" in peaks else "fallback"},
         "e2e": e2e,
@@ -575,6 +580,23 @@ def detail_measurements(args, dev, stream):
         del items
         torch.cuda.empty_cache()
     return out
+
+
+# DRAM bytes (read + write) per launch of each roofline kernel, from one ncu capture
+# (the profiles/ summary named beside each); the commit is the kernel version measured.
+# A kernel changed after its capture reports null until it is captured again.
+TRAFFIC = {
+    "decode": (1.831e6, "d17444d", "profiles/gemv_affine4_qwen3_decode_step.md"),
+    "experts_gemm": (539.9e6, "d17444d", "profiles/gemm_mxfp4_experts_t4096.md"),
+    "dequant": (337.4e6, "d17444d", "profiles/take_dequant_affine4_table.md"),
+}
+
+
+def traffic(key, applies=True):
+    if not applies or key not in TRAFFIC:
+        return None, None
+    v, commit, src = TRAFFIC[key]
+    return v, f"ncu dram__bytes_read.sum + dram__bytes_write.sum per launch at commit {commit} ({src})"
 
 
 def load_peaks():
