@@ -273,8 +273,13 @@ static __device__ __noinline__ void group_lookup(const Params& p, int slot, int 
     }
 }
 
-template <int FMT, int BITS, int GS, int NT>
+// NTK: token tiles of 8 (1 for M <= 8, 2 for M <= 16), or 0 for exactly one
+// token: the layout of NTK = 1, with the epilogue and the sums over a team
+// restricted to the accumulator entries that hold token 0.
+template <int FMT, int BITS, int GS, int NTK>
 __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant__ Params p) {
+    constexpr int NT = NTK == 0 ? 1 : NTK;
+    constexpr bool ONE = NTK == 0;
     extern __shared__ __align__(1024) uint8_t smem[];
     constexpr int MM = GS / 16;  // MMAs per group
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -630,15 +635,19 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                         const float* c = acc[tt][nt];
                         if constexpr (FMT == QM_MXFP4) {
                             yv[0] = fmaf(s0, c[0], yv[0]);
-                            yv[1] = fmaf(s0, c[1], yv[1]);
                             yv[2] = fmaf(s8, c[2], yv[2]);
-                            yv[3] = fmaf(s8, c[3], yv[3]);
+                            if constexpr (!ONE) {
+                                yv[1] = fmaf(s0, c[1], yv[1]);
+                                yv[3] = fmaf(s8, c[3], yv[3]);
+                            }
                         } else {
                             const float4 d = td[nt];
                             yv[0] = fmaf(s0, c[0] - d.x, fmaf(b0, d.y, yv[0]));
-                            yv[1] = fmaf(s0, c[1] - d.z, fmaf(b0, d.w, yv[1]));
                             yv[2] = fmaf(s8, c[2] - d.x, fmaf(b8, d.y, yv[2]));
-                            yv[3] = fmaf(s8, c[3] - d.z, fmaf(b8, d.w, yv[3]));
+                            if constexpr (!ONE) {  // odd columns: tokens 2t + 1
+                                yv[1] = fmaf(s0, c[1] - d.z, fmaf(b0, d.w, yv[1]));
+                                yv[3] = fmaf(s8, c[3] - d.z, fmaf(b8, d.w, yv[3]));
+                            }
                         }
                     }
                 }
@@ -679,7 +688,39 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                     partial[(j * kRows + r) * 16 + m] = v;
                 }
             };
-            {
+            if constexpr (ONE) {
+                // one token: a warp's partial is 32 floats, one per row of the
+                // stage, held by the lanes with t = 0 (column 0 of each tile)
+                float* base = red + ((team * 2 + buf) * T) * 32;
+                if (t == 0) {
+                    float* mine = base + wi * 32;
+#pragma unroll
+                    for (int tt = 0; tt < 2; ++tt) {
+                        mine[16 * tt + g] = y[tt][0][0];
+                        mine[16 * tt + g + 8] = y[tt][0][2];
+                    }
+                }
+                named_bar_sync(2 + team, T * 32);
+                if (live && !s_abort) {
+                    const int e = wi * (32 / T) + lane;  // warp wi adds rows [wi*32/T, (wi+1)*32/T)
+                    if (lane < 32 / T) {
+                        float sum = 0.0f;
+#pragma unroll 1
+                        for (int q = 0; q < T; ++q) sum += base[q * 32 + e];
+                        const float v = sum * tokscale[0];
+                        if (S == 1) {
+                            if (row0 + e < p.n) {
+                                __nv_bfloat16 bv = __float2bfloat16_rn(v);
+                                const int64_t yr = p.g_off ? s_pos[0] : 0;
+                                p.y[yr * p.n + row0 + e] = *reinterpret_cast<uint16_t*>(&bv);
+                            }
+                        } else {
+                            partial[(j * kRows + e) * 16] = v;
+                        }
+                    }
+                }
+                buf ^= 1;
+            } else {
                 // red[team][buf][warp of team][tt][nt][lane][4] (a team of one
                 // goes through it too: one store loop instead of an unrolled one)
                 constexpr int E = 2 * NT * 32 * 4;  // floats per warp partial
@@ -885,9 +926,9 @@ static Plan make_plan(const WDesc& w, int64_t M, double share = 1.0) {
     return best;
 }
 
-template <int FMT, int BITS, int GS, int NT>
+template <int FMT, int BITS, int GS, int NTK>
 static cudaError_t launch_t(const Plan& pl, cudaStream_t st) {
-    auto kern = gemv_kernel<FMT, BITS, GS, NT>;
+    auto kern = gemv_kernel<FMT, BITS, GS, NTK>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(pl.smem));
     if (e != cudaSuccess) return e;
@@ -953,11 +994,12 @@ qm_status launch_gemv(const WDesc& w, const void* x, int64_t M, void* y, cudaStr
         cudaError_t e = launch_apply_simple(w, x, M, y, st);
         return e == cudaSuccess ? QM_OK : cuda_fail(e, "apply launch");
     }
-    const bool two = M > 8;
+    const int ntk = M > 8 ? 2 : (M > 1 ? 1 : 0);
     cudaError_t e = cudaErrorInvalidValue;
 #define QM_GEMV_CASE(F, B, G)                                                                  \
     if (w.fmt == F && (F != QM_AFFINE || (w.bits == B && w.gs == G))) {                         \
-        e = two ? launch_t<F, B, G, 2>(pl, st) : launch_t<F, B, G, 1>(pl, st);                 \
+        e = ntk == 2 ? launch_t<F, B, G, 2>(pl, st)                                            \
+                     : (ntk == 1 ? launch_t<F, B, G, 1>(pl, st) : launch_t<F, B, G, 0>(pl, st)); \
         goto done;                                                                             \
     }
     QM_GEMV_CASE(QM_AFFINE, 4, 32)
