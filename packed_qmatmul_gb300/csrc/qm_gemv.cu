@@ -485,20 +485,24 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
         uint32_t* xfrag = reinterpret_cast<uint32_t*>(smem + p.off_xfrag);
         float2* tok = reinterpret_cast<float2*>(smem + p.off_tok);  // [groups][16]
         {
-            const int items = groups * 32 * NT;  // a multiple of 32: a warp shares (gi, nt)
+            // one token: only lanes 0..3 (t) of a warp hold nonzero B values,
+            // so the fragments are kept for those four lanes alone, [gi][t][MM][2]
+            const int items = ONE ? (groups * 4 + 31) / 32 * 32 : groups * 32 * NT;  // whole warps
             #pragma unroll 1
             for (int it = ctid; it < items; it += kWarps * 32) {
-                const int ln = it % 32, nt = (it / 32) % NT, gi = it / (32 * NT);
-                const int tg = ln >> 2, t = ln & 3;
+                const int ln = it % 32;
+                const int nt = ONE ? 0 : (it / 32) % NT;
+                const int gi = ONE ? it / 4 : it / (32 * NT);
+                const int tg = ONE ? 0 : ln >> 2, t = ln & 3;
                 const int m = nt * 8 + tg;
-                const bool live = m < M;  // padding tokens get exact zeros
+                const bool live = m < M && (!ONE || gi < groups);  // padding gets exact zeros
                 const float mul = live ? __uint_as_float(static_cast<uint32_t>(token_exp(m) + 127) << 23) : 0.0f;
                 const uint16_t* xr = xs + (live ? m : 0) * p.krange;
-                uint32_t* dst = xfrag + ((gi * 32 + ln) * MM) * NT * 2 + nt * 2;
+                uint32_t* dst = ONE ? xfrag + (gi * 4 + t) * MM * 2 : xfrag + ((gi * 32 + ln) * MM) * NT * 2 + nt * 2;
                 float F = 0.0f, X = 0.0f;
                 auto xv = [&](int kk) { return live ? bf16_bits_to_f32(xr[kk]) * mul : 0.0f; };
                 auto put = [&](int idx, float lo, float hi, float flo, float fhi) {
-                    dst[idx] = pack_f16x2(lo * flo, hi * fhi);
+                    if (!ONE || gi < groups) dst[idx] = pack_f16x2(lo * flo, hi * fhi);
                     X += lo + hi;
                     F += lo * flo + hi * fhi;
                 };
@@ -537,7 +541,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                     X += __shfl_xor_sync(0xffffffffu, X, 2);
                     F += __shfl_xor_sync(0xffffffffu, F, 2);
                     const float magic = (FMT == QM_Q8_0) ? 1152.0f : 1024.0f;
-                    if (t == 0) tok[gi * 16 + m] = make_float2(magic * F, X);
+                    if (t == 0 && (!ONE || gi < groups)) tok[gi * 16 + m] = make_float2(magic * F, X);
                 }
             }
         }
@@ -590,11 +594,13 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
             auto do_group = [&](int gi, float (&acc)[2][NT][4]) {
                 uint32_t bf[MM][NT][2];
                 {
-                    const uint4* src = reinterpret_cast<const uint4*>(xfrag + ((gi * 32 + lane) * MM) * NT * 2);
+                    const uint4* src = reinterpret_cast<const uint4*>(
+                        ONE ? xfrag + (gi * 4 + t) * MM * 2 : xfrag + ((gi * 32 + lane) * MM) * NT * 2);
                     uint32_t* bb = &bf[0][0][0];
 #pragma unroll
                     for (int q = 0; q < MM * NT / 2; ++q) {
-                        const uint4 v = src[q];
+                        uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                        if (!ONE || g == 0) v = src[q];  // one token: the other lanes' columns are zero
                         bb[4 * q] = v.x; bb[4 * q + 1] = v.y; bb[4 * q + 2] = v.z; bb[4 * q + 3] = v.w;
                     }
                 }
@@ -873,9 +879,11 @@ static bool plan_for(const WDesc& w, int64_t M, int S, int per_sm, Plan* out, do
         p.off_tokscale = 512;  // [16] 2^-E, [16] unused, [16] max |x| bits
         p.off_tok = p.off_tokscale + 256;
         p.off_xfrag = round_up(p.off_tok + groups * 16 * 8, 128);
-        const uint64_t xfrag_bytes = static_cast<uint64_t>(kr) * 16 * NT;
+        // B fragments: 16 bytes per k value and token tile, or 2 for exactly one token
+        const uint64_t xfrag_bytes = M == 1 ? static_cast<uint64_t>(kr) * 2 : static_cast<uint64_t>(kr) * 16 * NT;
         p.off_red = round_up(p.off_xfrag + xfrag_bytes, 128);
-        const uint64_t red_bytes = static_cast<uint64_t>(kWarps) * 2 * 2 * NT * 32 * 4 * 4;
+        const uint64_t red_bytes = M == 1 ? static_cast<uint64_t>(kWarps) * 2 * 32 * 4
+                                          : static_cast<uint64_t>(kWarps) * 2 * 2 * NT * 32 * 4 * 4;
         p.off_xraw = round_up(p.off_red + red_bytes, 128);
         const uint64_t partial_bytes = S > 1 ? static_cast<uint64_t>(spc) * kRows * 16 * 4 : 0;
         const uint64_t xraw_bytes = static_cast<uint64_t>(M) * kr * 2;
