@@ -79,6 +79,35 @@ QM_DEV bool mbar_wait(uint32_t bar, uint32_t parity) {
     return mbar_wait_slow(bar, parity);
 }
 
+// Shared-memory loads at 32-bit shared addresses (smem_u32 and offsets). They
+// read what TMA copies and other threads wrote: the "memory" clobber keeps them
+// after the barrier waits that publish that data.
+QM_DEV uint32_t lds_u8(uint32_t a) {
+    uint16_t v;
+    asm("ld.shared.u8 %0, [%1];" : "=h"(v) : "r"(a) : "memory");
+    return v;
+}
+QM_DEV uint32_t lds_u16(uint32_t a) {
+    uint16_t v;
+    asm("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a) : "memory");
+    return v;
+}
+QM_DEV uint32_t lds_u32(uint32_t a) {
+    uint32_t v;
+    asm("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(a) : "memory");
+    return v;
+}
+QM_DEV uint2 lds_v2(uint32_t a) {
+    uint2 v;
+    asm("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "r"(a) : "memory");
+    return v;
+}
+QM_DEV uint4 lds_v4(uint32_t a) {
+    uint4 v;
+    asm("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
+    return v;
+}
+
 // Named barrier `id` (1..15) over `count` threads (a multiple of 32).
 QM_DEV void named_bar_sync(uint32_t id, uint32_t count) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
@@ -261,7 +290,7 @@ QM_DEV void grid_launch_dependents() { asm volatile("griddepcontrol.launch_depen
 // D += A * B, m16n8k16, f16 inputs, f32 accumulators.
 QM_DEV void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                     uint32_t b0, uint32_t b1) {
-    asm volatile(
+    asm(  // registers in, registers out: free to schedule
         "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])

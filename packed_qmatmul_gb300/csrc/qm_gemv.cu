@@ -117,16 +117,18 @@ QM_DEV float sval(uint32_t h, int sdt) { return sdt == QM_F16 ? f16_bits_to_f32(
 // A stage's codes are 128-byte boxes of 32 rows, each box 128B-swizzled by
 // the TMA unit: byte b of row r sits in box b / 128, at row r's 128-byte
 // line, 16-byte chunk ((b / 16) mod 8) XOR (r mod 8). Reads never straddle a
-// 16-byte chunk, so one address per read suffices.
+// 16-byte chunk, so one address per read suffices. Addresses are 32-bit
+// shared-memory addresses; rows r, r + 8, r + 16 and r + 24 share the swizzle
+// key, so their reads differ by whole 1 KB steps.
 struct CodeRow {
-    const uint8_t* line;  // stage + r * 128
-    uint32_t key;         // (r mod 8) << 4
-    QM_DEV const uint8_t* at(uint32_t b) const {
+    uint32_t line;  // shared address of stage + r * 128
+    uint32_t key;   // (r mod 8) << 4
+    QM_DEV uint32_t at(uint32_t b) const {
         return line + (b >> 7) * (kRows * 128) + (((b & 0x70u) ^ key) | (b & 15u));
     }
 };
 
-QM_DEV CodeRow code_row(const uint8_t* st, int r) {
+QM_DEV CodeRow code_row(uint32_t st, int r) {
     return CodeRow{st + r * 128, static_cast<uint32_t>(r & 7) << 4};
 }
 
@@ -142,16 +144,17 @@ QM_DEV void tile_group(const CodeRow& r0, const CodeRow& r8, int gi, int t,
         constexpr int V = GS / 32;  // words of a row per lane per group
         uint32_t w0[V], w8[V];
         const uint32_t off = gi * (GS / 2) + t * V * 4;
+        const uint32_t a0_ = r0.at(off), a8_ = a0_ + (r8.line - r0.line);
         if constexpr (V == 1) {
-            w0[0] = *reinterpret_cast<const uint32_t*>(r0.at(off));
-            w8[0] = *reinterpret_cast<const uint32_t*>(r8.at(off));
+            w0[0] = lds_u32(a0_);
+            w8[0] = lds_u32(a8_);
         } else if constexpr (V == 2) {
-            const uint2 a = *reinterpret_cast<const uint2*>(r0.at(off));
-            const uint2 c = *reinterpret_cast<const uint2*>(r8.at(off));
+            const uint2 a = lds_v2(a0_);
+            const uint2 c = lds_v2(a8_);
             w0[0] = a.x; w0[1] = a.y; w8[0] = c.x; w8[1] = c.y;
         } else {
-            const uint4 a = *reinterpret_cast<const uint4*>(r0.at(off));
-            const uint4 c = *reinterpret_cast<const uint4*>(r8.at(off));
+            const uint4 a = lds_v4(a0_);
+            const uint4 c = lds_v4(a8_);
             w0[0] = a.x; w0[1] = a.y; w0[2] = a.z; w0[3] = a.w;
             w8[0] = c.x; w8[1] = c.y; w8[2] = c.z; w8[3] = c.w;
         }
@@ -170,15 +173,16 @@ QM_DEV void tile_group(const CodeRow& r0, const CodeRow& r8, int gi, int t,
         constexpr int V = GS / 16;  // 2, 4 or 8 words
         const uint32_t off = gi * GS + t * V * 4;
         uint32_t wa[V], wc[V];
+        const uint32_t d8 = r8.line - r0.line;
         if constexpr (V == 2) {
-            const uint2 a = *reinterpret_cast<const uint2*>(r0.at(off));
-            const uint2 c = *reinterpret_cast<const uint2*>(r8.at(off));
+            const uint2 a = lds_v2(r0.at(off));
+            const uint2 c = lds_v2(r0.at(off) + d8);
             wa[0] = a.x; wa[1] = a.y; wc[0] = c.x; wc[1] = c.y;
         } else {
 #pragma unroll
             for (int q = 0; q < V / 4; ++q) {
-                const uint4 a = *reinterpret_cast<const uint4*>(r0.at(off + 16 * q));
-                const uint4 c = *reinterpret_cast<const uint4*>(r8.at(off + 16 * q));
+                const uint4 a = lds_v4(r0.at(off + 16 * q));
+                const uint4 c = lds_v4(r0.at(off + 16 * q) + d8);
                 wa[4 * q] = a.x; wa[4 * q + 1] = a.y; wa[4 * q + 2] = a.z; wa[4 * q + 3] = a.w;
                 wc[4 * q] = c.x; wc[4 * q + 1] = c.y; wc[4 * q + 2] = c.z; wc[4 * q + 3] = c.w;
             }
@@ -195,7 +199,7 @@ QM_DEV void tile_group(const CodeRow& r0, const CodeRow& r8, int gi, int t,
         // codes of block gi at byte 34*gi + 2 + 8t (2-byte aligned when gi is even)
         const uint32_t o = 34 * gi + 2 + 8 * t;
         uint32_t c0[2], c8[2];
-        auto w32 = [](const CodeRow& r, uint32_t b) { return *reinterpret_cast<const uint32_t*>(r.at(b)); };
+        auto w32 = [](const CodeRow& r, uint32_t b) { return lds_u32(r.at(b)); };
         if (o & 2) {
             const uint32_t x0 = w32(r0, o - 2), x1 = w32(r0, o + 2), x2 = w32(r0, o + 6);
             const uint32_t z0 = w32(r8, o - 2), z1 = w32(r8, o + 2), z2 = w32(r8, o + 6);
@@ -215,8 +219,9 @@ QM_DEV void tile_group(const CodeRow& r0, const CodeRow& r8, int gi, int t,
     } else {  // MXFP4
         const uint32_t o = 16 * gi + 4 * t;
         uint32_t h0[4], h8[4];
-        e2m1x8_to_f16x2(*reinterpret_cast<const uint32_t*>(r0.at(o)), h0);
-        e2m1x8_to_f16x2(*reinterpret_cast<const uint32_t*>(r8.at(o)), h8);
+        const uint32_t a = r0.at(o);
+        e2m1x8_to_f16x2(lds_u32(a), h0);
+        e2m1x8_to_f16x2(lds_u32(a + (r8.line - r0.line)), h8);
 #pragma unroll
         for (int mm = 0; mm < 2; ++mm)
 #pragma unroll
@@ -579,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                 live = false;
             }
             live = __shfl_sync(0xffffffffu, live ? 1 : 0, 0) != 0;
-            const uint8_t* st = smem + p.off_stages + slot * p.stage_bytes;
+            const uint32_t st = smem_u32(smem) + p.off_stages + slot * p.stage_bytes;
             const CodeRow rows_[4] = {code_row(st, g), code_row(st, g + 8), code_row(st, 16 + g),
                                       code_row(st, 24 + g)};
             float y[2][NT][4];
@@ -594,13 +599,13 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
             auto do_group = [&](int gi, float (&acc)[2][NT][4]) {
                 uint32_t bf[MM][NT][2];
                 {
-                    const uint4* src = reinterpret_cast<const uint4*>(
-                        ONE ? xfrag + (gi * 4 + t) * MM * 2 : xfrag + ((gi * 32 + lane) * MM) * NT * 2);
+                    const uint32_t src = smem_u32(smem) + p.off_xfrag +
+                                         4u * (ONE ? (gi * 4 + t) * MM * 2 : ((gi * 32 + lane) * MM) * NT * 2);
                     uint32_t* bb = &bf[0][0][0];
 #pragma unroll
                     for (int q = 0; q < MM * NT / 2; ++q) {
                         uint4 v = make_uint4(0u, 0u, 0u, 0u);
-                        if (!ONE || g == 0) v = src[q];  // one token: the other lanes' columns are zero
+                        if (!ONE || g == 0) v = lds_v4(src + 16 * q);  // one token: the other lanes' columns are zero
                         bb[4 * q] = v.x; bb[4 * q + 1] = v.y; bb[4 * q + 2] = v.z; bb[4 * q + 3] = v.w;
                     }
                 }
@@ -620,20 +625,22 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                     const int ra = 16 * tt + g, rb = ra + 8;
                     float s0, s8, b0 = 0.0f, b8 = 0.0f;
                     if constexpr (FMT == QM_AFFINE) {
-                        const uint16_t* sc = reinterpret_cast<const uint16_t*>(st + p.off_scales);
-                        const uint16_t* bi = reinterpret_cast<const uint16_t*>(st + p.off_biases);
-                        const int stride = p.scale_seg / 2;
-                        s0 = sval(sc[ra * stride + gi], p.sdt);
-                        s8 = sval(sc[rb * stride + gi], p.sdt);
-                        b0 = sval(bi[ra * stride + gi], p.sdt);
-                        b8 = sval(bi[rb * stride + gi], p.sdt);
+                        // row ra, group gi; row rb = ra + 8 lies 8 rows of scale_seg bytes on
+                        const uint32_t sa = st + p.off_scales + ra * p.scale_seg + 2 * gi;
+                        const uint32_t ba = sa + (p.off_biases - p.off_scales);
+                        const uint32_t r8 = 8 * p.scale_seg;
+                        s0 = sval(lds_u16(sa), p.sdt);
+                        s8 = sval(lds_u16(sa + r8), p.sdt);
+                        b0 = sval(lds_u16(ba), p.sdt);
+                        b8 = sval(lds_u16(ba + r8), p.sdt);
                     } else if constexpr (FMT == QM_Q8_0) {
-                        s0 = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(rows_[2 * tt].at(34 * gi)));
-                        s8 = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(rows_[2 * tt + 1].at(34 * gi)));
+                        const uint32_t da = rows_[2 * tt].at(34 * gi);
+                        s0 = f16_bits_to_f32(lds_u16(da));
+                        s8 = f16_bits_to_f32(lds_u16(da + (rows_[2 * tt + 1].line - rows_[2 * tt].line)));
                     } else {
-                        const uint8_t* sc = st + p.off_scales;
-                        s0 = e8m0_to_f32(sc[ra * p.scale_seg + gi]);
-                        s8 = e8m0_to_f32(sc[rb * p.scale_seg + gi]);
+                        const uint32_t sa = st + p.off_scales + ra * p.scale_seg + gi;
+                        s0 = e8m0_to_f32(lds_u8(sa));
+                        s8 = e8m0_to_f32(lds_u8(sa + 8 * p.scale_seg));
                     }
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
