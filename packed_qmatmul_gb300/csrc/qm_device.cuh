@@ -168,6 +168,11 @@ QM_DEV void st_shared_cluster_f32(uint32_t addr, float v) {
     asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
 
+QM_DEV void st_shared_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
+
 // Arrive on an mbarrier in another CTA of the cluster, releasing this
 // thread's earlier writes at cluster scope.
 QM_DEV void mbar_arrive_cluster(uint32_t remote_bar) {

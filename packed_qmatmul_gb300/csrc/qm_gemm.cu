@@ -77,6 +77,11 @@ struct Params {
     int sdt;
     int ksteps, mtiles, ntiles;
     uint32_t off_x, off_raw, raw_stage_bytes;
+    // split k (plain products with few tiles): a cluster of `splitk` CTAs takes
+    // chunks [rank * cps, (rank + 1) * cps) of one tile; partial sums meet in
+    // the receive areas at off_recv, each CTA adding one slice of the tokens
+    int splitk, cps;
+    uint32_t off_recv;
     // grouped mode (apply_experts), off when g_off is null: x holds the routed
     // activation rows expert by expert, the weight is [E, n, k], and m tile
     // slot t is the t-th BM-row tile of the experts' row ranges in order
@@ -267,13 +272,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     constexpr uint32_t kXBytes = NTOK * BK * 2;  // activation tile per k step
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int mt = p.g_off ? blockIdx.x / p.ntiles : blockIdx.x % p.mtiles;
-    const int nt = p.g_off ? blockIdx.x % p.ntiles : blockIdx.x / p.mtiles;
+    const int S = p.splitk;
+    const uint32_t rank = S > 1 ? cluster_ctarank() : 0;
+    const int tile = static_cast<int>(blockIdx.x) / S;
+    const int mt = p.g_off ? tile / p.ntiles : tile % p.mtiles;
+    const int nt = p.g_off ? tile % p.ntiles : tile / p.mtiles;
     int64_t m0 = static_cast<int64_t>(mt) * NTOK, mend = p.M;  // this tile's rows of x
     int64_t wrow0 = 0;                                          // first row of the tile's matrix
     const int64_t n0 = static_cast<int64_t>(nt) * BW;
     const int ks_n = p.ksteps;
     const int nchunks = (ks_n + R::SPR - 1) / R::SPR;
+    // this CTA's chunks and k steps (all of them without a split); ring slots
+    // and parities count from the first
+    const int c_lo = static_cast<int>(rank) * p.cps, c_hi = min(nchunks, c_lo + p.cps);
+    const int ks_lo = c_lo * R::SPR, ks_hi = min(ks_n, c_hi * R::SPR);
 
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
     const uint32_t b0 = smem_u32(bars);
@@ -329,39 +341,41 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         if (lane == 0) {
-            int last_x = -1, last_r = -1;
-            for (int ks = 0; ks < ks_n && !s_abort; ++ks) {
-                if (ks % R::SPR == 0) {
-                    const int rc = ks / R::SPR, sr = rc % NR;
-                    if (!mbar_wait(r_empty(sr), ((rc / NR) & 1) ^ 1)) { give_up(); break; }
+            int last_x = -1, last_r = -1;  // local indices
+            for (int ks = ks_lo; ks < ks_hi && !s_abort; ++ks) {
+                const int li = ks - ks_lo;
+                if (li % R::SPR == 0) {
+                    const int rc = ks / R::SPR, lc = rc - c_lo, sr = lc % NR;
+                    if (!mbar_wait(r_empty(sr), ((lc / NR) & 1) ^ 1)) { give_up(); break; }
                     mbar_expect_tx(r_full(sr), R::BYTES * BW);
                     tma_load_2d(smem_u32(smem + p.off_raw + sr * p.raw_stage_bytes), &p.tm_raw,
                                 rc * R::BYTES / R::ELEM, static_cast<int32_t>(wrow0 + n0), r_full(sr));
                     mbar_arrive(r_full(sr));
-                    last_r = rc;
+                    last_r = lc;
                 }
-                const int sx = ks % NXT;
-                if (!mbar_wait(x_empty(sx), ((ks / NXT) & 1) ^ 1)) { give_up(); break; }
+                const int sx = li % NXT;
+                if (!mbar_wait(x_empty(sx), ((li / NXT) & 1) ^ 1)) { give_up(); break; }
                 mbar_expect_tx(x_full(sx), kXBytes);
                 tma_load_2d(smem_u32(smem + p.off_x + sx * kXBytes), &p.tm_x, ks * 128, static_cast<int32_t>(m0),
                             x_full(sx));
                 mbar_arrive(x_full(sx));
-                last_x = ks;
+                last_x = li;
             }
             if (s_abort) {  // let issued copies land before the CTA winds down
-                for (int ks = std::max(0, last_x - NXT + 1); ks <= last_x; ++ks)
-                    (void)mbar_wait(x_full(ks % NXT), (ks / NXT) & 1);
-                for (int rc = std::max(0, last_r - NR + 1); rc <= last_r; ++rc)
-                    (void)mbar_wait(r_full(rc % NR), (rc / NR) & 1);
+                for (int li = std::max(0, last_x - NXT + 1); li <= last_x; ++li)
+                    (void)mbar_wait(x_full(li % NXT), (li / NXT) & 1);
+                for (int lc = std::max(0, last_r - NR + 1); lc <= last_r; ++lc)
+                    (void)mbar_wait(r_full(lc % NR), (lc / NR) & 1);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             constexpr uint32_t idesc = umma_idesc_bf16(BW, NTOK);
-            for (int ks = 0; ks < ks_n && !s_abort; ++ks) {
-                const int sx = ks % NXT, sa = ks % NA;
-                if (!mbar_wait(x_full(sx), (ks / NXT) & 1) || !mbar_wait(a_full(sa), (ks / NA) & 1)) {
+            for (int ks = ks_lo; ks < ks_hi && !s_abort; ++ks) {
+                const int li = ks - ks_lo;
+                const int sx = li % NXT, sa = li % NA;
+                if (!mbar_wait(x_full(sx), (li / NXT) & 1) || !mbar_wait(a_full(sa), (li / NA) & 1)) {
                     give_up();
                     break;
                 }
@@ -370,7 +384,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 const uint32_t ad = tmem + kAcol + 32 * sa;
 #pragma unroll
                 for (int kk = 0; kk < BK / 16; ++kk)  // 16 values: 8 TMEM columns of A, 32 bytes of B
-                    umma_f16_ts(tmem, ad + 8 * kk, bd + 2 * kk, idesc, ks > 0 || kk > 0);
+                    umma_f16_ts(tmem, ad + 8 * kk, bd + 2 * kk, idesc, li > 0 || kk > 0);
                 umma_commit(x_empty(sx));
                 umma_commit(a_empty(sa));
             }
@@ -394,19 +408,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                                                                    static_cast<int64_t>(rc) * R::RAWK + kk * BK + h * 32)
                                        : Sc{0.0f, 0.0f};
         };
-        fetch(0, cur);
-        for (int rc = 0; rc < nchunks; ++rc) {
-            if (rc + 1 < nchunks) fetch(rc + 1, nxt);
-            const int sr = rc % NR;
-            bool live = !s_abort && mbar_wait(r_full(sr), (rc / NR) & 1);
+        fetch(c_lo, cur);
+        for (int rc = c_lo; rc < c_hi; ++rc) {
+            if (rc + 1 < c_hi) fetch(rc + 1, nxt);
+            const int lc = rc - c_lo, sr = lc % NR;
+            bool live = !s_abort && mbar_wait(r_full(sr), (lc / NR) & 1);
             const uint8_t* raw = smem + p.off_raw + sr * p.raw_stage_bytes;
 #pragma unroll
             for (int kk = 0; kk < R::SPR; ++kk) {
-                const int ks = rc * R::SPR + kk;
-                if (ks >= ks_n) break;
-                if ((ks & 1) != grp) continue;
-                const int sa = ks % NA;
-                if (live && !mbar_wait(a_empty(sa), ((ks / NA) & 1) ^ 1)) live = false;
+                const int ks = rc * R::SPR + kk, li = ks - ks_lo;
+                if (ks >= ks_hi) break;
+                if ((li & 1) != grp) continue;
+                const int sa = li % NA;
+                if (live && !mbar_wait(a_empty(sa), ((li / NA) & 1) ^ 1)) live = false;
                 if (!live) {
                     if (lane == 0) give_up();
                     break;
@@ -455,13 +469,8 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
         const int64_t row0 = n0 + 32 * quarter;  // this warp's first weight row
         const bool vec = (p.n & 7) == 0 && row0 + 32 <= p.n;
         const int odd = lane & 1;
-#pragma unroll 1
-        for (int j = 0; j < NTOK / 64; ++j) {
-            const int col = part * (NTOK / 2) + 32 * j;
-            uint32_t r[32];
-            tmem_ld32(tmem + lane_addr + col, r);
-            tmem_wait_ld();
-            if (!ok || s_abort) continue;
+        // tokens col .. col + 31 of this warp's 32 rows (r[c]: token col + c) to y
+        auto store32 = [&](const uint32_t (&r)[32], int col) {
 #pragma unroll
             for (int c = 0; c < 32; c += 2) {
                 const float lo = __uint_as_float(r[c]), hi = __uint_as_float(r[c + 1]);
@@ -485,6 +494,93 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
                 }
             }
             __syncwarp();
+        };
+        if (S == 1) {
+#pragma unroll 1
+            for (int j = 0; j < NTOK / 64; ++j) {
+                const int col = part * (NTOK / 2) + 32 * j;
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_addr + col, r);
+                tmem_wait_ld();
+                if (!ok || s_abort) continue;
+                store32(r, col);
+            }
+        } else {
+            // Split k. The tokens are cut into S slices of NTOK / S; CTA q adds
+            // slice q. Every CTA puts its partial sums for slice q into CTA q's
+            // receive area at [its rank][row][token] (pitch slice + 4 floats:
+            // 16-byte rows that land in distinct bank groups), then, after the
+            // cluster barrier, each CTA adds its S partials in rank order.
+            const int slice = NTOK / S;
+            const int pitch = slice + 4;
+            const int row = 32 * quarter + lane;
+            const uint32_t recv = smem_u32(smem + p.off_recv);
+#pragma unroll 1
+            for (int j = 0; j < NTOK / 64; ++j) {
+                const int col = part * (NTOK / 2) + 32 * j;
+                uint32_t r[32];
+                tmem_ld32(tmem + lane_addr + col, r);
+                tmem_wait_ld();
+                const int q = col / slice, cc = col - q * slice;
+                const uint32_t dst = map_shared_rank(recv, static_cast<uint32_t>(q)) +
+                                     4u * static_cast<uint32_t>((static_cast<int>(rank) * BW + row) * pitch + cc);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    st_shared_cluster_v4(dst + 16 * i, r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+            }
+        }
+    }
+    if (S > 1) {
+        __syncthreads();
+        cluster_sync();  // every partial sum has arrived; nothing is written remotely after this
+        if (warp >= 2) {
+            const int quarter = warp & 3, part = (warp - 2) >> 2;
+            const int slice = NTOK / S, pitch = slice + 4;
+            const int row = 32 * quarter + lane;
+            const float* recv = reinterpret_cast<const float*>(smem + p.off_recv);
+            const int64_t row0 = n0 + 32 * quarter;
+            const bool vec = (p.n & 7) == 0 && row0 + 32 <= p.n;
+            const int odd = lane & 1;
+            uint8_t* stage = smem + p.off_x + (warp - 2) * (32 * 80);
+            // this warp's tokens of the slice: 32 when the slice has 64, else 16 (slice 32)
+            const int cols = slice / 2;
+            const int c0 = part * cols;
+            const bool live = !s_abort;
+            uint32_t r[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                float v = 0.0f;
+                if (c < cols) {
+                    for (int q = 0; q < S; ++q) v += recv[(q * BW + row) * pitch + c0 + c];
+                }
+                r[c] = __float_as_uint(v);
+            }
+            if (live) {
+                // the store's tokens past `cols` belong to the next warp's part: keep them out
+                const int64_t keep_end = mend;
+                const int64_t first = m0 + static_cast<int64_t>(rank) * slice + c0;
+#pragma unroll
+                for (int c = 0; c < 32; c += 2) {
+                    const float lo = __uint_as_float(r[c]), hi = __uint_as_float(r[c + 1]);
+                    const float got = __shfl_xor_sync(0xffffffffu, odd ? lo : hi, 1);
+                    const uint32_t pair = odd ? bf2(got, hi) : bf2(lo, got);
+                    *reinterpret_cast<uint32_t*>(stage + (c + odd) * 80 + (lane >> 1) * 4) = pair;
+                }
+                __syncwarp();
+                const int64_t m = first + lane;
+                if (lane < cols && m < keep_end) {
+                    uint16_t* yr = p.y + m * p.n + row0;
+                    const uint8_t* src = stage + lane * 80;
+                    if (vec) {
+#pragma unroll
+                        for (int qq = 0; qq < 4; ++qq)
+                            reinterpret_cast<uint4*>(yr)[qq] = *reinterpret_cast<const uint4*>(src + 16 * qq);
+                    } else {
+                        for (int i = 0; i < 32 && row0 + i < p.n; ++i)
+                            yr[i] = reinterpret_cast<const uint16_t*>(src)[i];
+                    }
+                }
+            }
         }
     }
     tc_fence_before();
@@ -503,7 +599,20 @@ static cudaError_t launch_t(Params& p, const WDesc& w, const void* x, cudaStream
     p.off_x = 1024;
     p.off_raw = p.off_x + ts::NXT * NTOK * BK * 2;
     p.raw_stage_bytes = (R::BYTES * ts::BW + 16 + 1023) / 1024 * 1024;  // 16 spare bytes after each slot
-    const size_t smem = p.off_raw + NR * p.raw_stage_bytes;
+    p.off_recv = p.off_raw + NR * p.raw_stage_bytes;
+    const int64_t ntiles = (w.n + ts::BW - 1) / ts::BW;
+    const int nchunks = (p.ksteps + R::SPR - 1) / R::SPR;
+    // split k while the tiles alone leave most SMs idle: 128-token tiles only
+    // (slices of at least 32 tokens), at least two chunks per CTA
+    int S = 1;
+    if (!p.g_off && NTOK == 128) {
+        const int64_t tiles = p.mtiles * ntiles;
+        while (S < 4 && tiles * S * 2 <= num_sms() && nchunks >= 2 * S * 2) S *= 2;
+    }
+    p.splitk = S;
+    p.cps = (nchunks + S - 1) / S;
+    const size_t recv_bytes = S > 1 ? static_cast<size_t>(S) * ts::BW * (NTOK / S + 4) * 4 : 0;
+    const size_t smem = p.off_recv + recv_bytes;
     if (!make_tmap_2d(&p.tm_x, x, static_cast<uint64_t>(w.k) * 2, p.M, static_cast<uint64_t>(w.k) * 2, 128, NTOK, true))
         return cudaErrorNotSupported;
     if (!make_tmap_2d(&p.tm_raw, w.codes, w.code_row_bytes, w.rows, w.code_row_bytes, R::BYTES, ts::BW, R::SW,
@@ -512,18 +621,25 @@ static cudaError_t launch_t(Params& p, const WDesc& w, const void* x, cudaStream
     auto kern = gemm_kernel<FMT, BITS, GS, NTOK>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    const int64_t ntiles = (w.n + ts::BW - 1) / ts::BW;
     p.ntiles = static_cast<int>(ntiles);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(p.mtiles * ntiles));
+    cfg.gridDim = dim3(static_cast<unsigned>(p.mtiles * ntiles * S));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr;
-    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr.val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = &attr;
-    cfg.numAttrs = 1;
+    cudaLaunchAttribute attrs[2];
+    attrs[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[0].val.programmaticStreamSerializationAllowed = 1;
+    int na = 1;
+    if (S > 1) {
+        attrs[1].id = cudaLaunchAttributeClusterDimension;
+        attrs[1].val.clusterDim.x = S;
+        attrs[1].val.clusterDim.y = 1;
+        attrs[1].val.clusterDim.z = 1;
+        na = 2;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 

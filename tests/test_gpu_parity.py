@@ -425,6 +425,26 @@ def test_apply_prefill(kind):
         _check_apply(w, x, f"{kind} prefill n={n} k={k} M={M}")
 
 
+@pytest.mark.parametrize("kind", ["affine4_g64", "affine8_g32", "q8_0", "mxfp4"])
+def test_apply_prefill_split_k(kind):
+    # few weight tiles and a long k: a cluster splits k and adds its partial
+    # sums across CTAs (ragged M and n included)
+    g = synth.rng(1210)
+    for n, k, M in ((256, 4096, 17), (200, 4096, 64), (384, 2048, 128), (130, 8192, 100)):
+        w = _make(kind, g, n, k)
+        x = synth.activations(g, M, k)
+        _check_apply(w, x, f"{kind} split-k n={n} k={k} M={M}")
+
+
+def test_apply_prefill_split_k_deterministic():
+    g = synth.rng(1211)
+    qw = qm.QWeight.from_arrays(synth.q8_0_weight(g, 512, 4096))
+    x = _dev_bf16(synth.activations(g, 96, 4096))
+    a = _host(qm.apply(qw, x))
+    b = _host(qm.apply(qw, x))
+    assert np.array_equal(a, b)
+
+
 def test_apply_prefill_q8_0_full_shape_sampled():
     # Q8_0 4096 x 4096 at M = 2048, checked on sampled outputs
     g = synth.rng(1201)
