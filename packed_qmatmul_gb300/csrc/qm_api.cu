@@ -288,12 +288,16 @@ qm_status qm_take(const qm_weight* w, int32_t axis, const void* ids, int32_t id_
             if (!rb[p]) continue;
             if (!aligned16(outs[p])) return fail(QM_EINVAL, std::string(names[p]) + ": output must be 16-byte aligned");
         }
+        TakeParts tp;
         for (int p = 0; p < 3; ++p) {
             if (!rb[p]) continue;
-            cudaError_t e = launch_take_packed(srcs[p], outer, len, inner_rows * rb[p], ids, id64,
-                                               n_ids, static_cast<uint8_t*>(const_cast<void*>(outs[p])), st);
-            if (e != cudaSuccess) return cuda_fail(e, "take launch");
+            tp.src[tp.n] = srcs[p];
+            tp.dst[tp.n] = static_cast<uint8_t*>(const_cast<void*>(outs[p]));
+            tp.inner[tp.n] = inner_rows * rb[p];
+            ++tp.n;
         }
+        cudaError_t e = launch_take_packed(tp, outer, len, ids, id64, n_ids, st);  // one launch for every part
+        if (e != cudaSuccess) return cuda_fail(e, "take launch");
     }
     if (out_dense) {
         if (!aligned16(out_dense)) return fail(QM_EINVAL, "out: dense output must be 16-byte aligned");

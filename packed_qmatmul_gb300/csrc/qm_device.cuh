@@ -291,6 +291,25 @@ constexpr uint32_t umma_idesc_bf16(int M, int N) {
 QM_DEV void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 QM_DEV void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
 
+// Launch with programmatic dependent launch allowed: the kernel may start
+// while the previous kernel in the stream finishes; it must call
+// grid_dependency_wait() before touching anything that kernel writes.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), unsigned grid, unsigned block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute a;
+    a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &a;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // ---------------------------------------------------------------- warp MMA
 // D += A * B, m16n8k16, f16 inputs, f32 accumulators.
 QM_DEV void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,

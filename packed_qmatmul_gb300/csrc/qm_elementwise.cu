@@ -151,6 +151,8 @@ struct GatherMap {
 template <int FMT, int BITS, int OUT, class Map>
 __global__ void __launch_bounds__(256) decode_rows_kernel(DecodeArgs a, int64_t out_rows, Map map,
                                                           void* out) {
+    grid_launch_dependents();
+    grid_dependency_wait();  // the weight, ids or output may belong to the previous kernel
     const int64_t upr = a.k / 32;
     const int64_t total = out_rows * upr;
     for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < total;
@@ -178,9 +180,8 @@ cudaError_t launch_decode_rows(const WDesc& w, int64_t out_rows, Map map, int ou
     const int64_t blocks = std::min<int64_t>((total + threads - 1) / threads, int64_t(num_sms()) * 16);
 #define QM_DECODE_CASE(F, B, O)                                                                  \
     if (w.fmt == F && (F != QM_AFFINE || w.bits == B) && out_dtype == O) {                        \
-        decode_rows_kernel<F, B, O, Map><<<static_cast<unsigned>(blocks), threads, 0, st>>>(a, out_rows, \
-                                                                                         map, out); \
-        return cudaGetLastError();                                                               \
+        return launch_pdl(decode_rows_kernel<F, B, O, Map>, static_cast<unsigned>(blocks), threads, 0, st, a, \
+                          out_rows, map, out);                                                  \
     }
 #define QM_DECODE_OUTS(F, B) QM_DECODE_CASE(F, B, QM_F32) QM_DECODE_CASE(F, B, QM_BF16) QM_DECODE_CASE(F, B, QM_F16)
     QM_DECODE_OUTS(QM_AFFINE, 4)
@@ -194,25 +195,34 @@ cudaError_t launch_decode_rows(const WDesc& w, int64_t out_rows, Map map, int ou
 
 // ------------------------------------------------------------ packed gather
 // dst[o, p, :] = src[o, ids[p], :] (inner bytes each), zero bytes out of range.
+// One warp per gathered row (outer index o, position q): the id is read once
+// and the row's bytes of every part are copied in V-sized pieces; positions
+// outside [0, len) get zero bytes.
 template <typename V>
-__global__ void __launch_bounds__(256) take_packed_kernel(const uint8_t* __restrict__ src, int64_t outer,
-                                                          int64_t len, int64_t inner_bytes,
-                                                          const void* ids, int id64, int64_t n_ids,
-                                                          uint8_t* __restrict__ dst) {
-    const int64_t vpr = inner_bytes / static_cast<int64_t>(sizeof(V));
-    const int64_t total = outer * n_ids * vpr;
-    for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < total;
-         t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t row = t / vpr, c = t - row * vpr;
-        const int64_t p = row % n_ids, o = row / n_ids;
-        const int64_t id = id64 ? __ldg(static_cast<const int64_t*>(ids) + p)
-                                : static_cast<int64_t>(__ldg(static_cast<const int32_t*>(ids) + p));
-        V v;
-        if (id >= 0 && id < len)
-            v = __ldg(reinterpret_cast<const V*>(src + (o * len + id) * inner_bytes) + c);
-        else
-            memset(&v, 0, sizeof(V));
-        reinterpret_cast<V*>(dst + row * inner_bytes)[c] = v;
+__global__ void __launch_bounds__(256) take_packed_kernel(TakeParts tp, int64_t outer, int64_t len,
+                                                          const void* ids, int id64, int64_t n_ids) {
+    grid_launch_dependents();
+    grid_dependency_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t rows = outer * n_ids;
+    const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t r = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; r < rows; r += nw) {
+        const int64_t o = r / n_ids, q = r - o * n_ids;
+        const int64_t id = id64 ? __ldg(static_cast<const int64_t*>(ids) + q)
+                                : static_cast<int64_t>(__ldg(static_cast<const int32_t*>(ids) + q));
+        const bool in = id >= 0 && id < len;
+#pragma unroll 1
+        for (int part = 0; part < tp.n; ++part) {
+            const int64_t vpr = tp.inner[part] / static_cast<int64_t>(sizeof(V));
+            const V* src = reinterpret_cast<const V*>(tp.src[part] + (o * len + (in ? id : 0)) * tp.inner[part]);
+            V* dst = reinterpret_cast<V*>(tp.dst[part] + r * tp.inner[part]);
+            for (int64_t c = lane; c < vpr; c += 32) {
+                V v;
+                if (in) v = __ldg(src + c);
+                else memset(&v, 0, sizeof(V));
+                dst[c] = v;
+            }
+        }
     }
 }
 
@@ -231,22 +241,22 @@ cudaError_t launch_take_dense(const WDesc& w, int axis, const void* ids, int id6
     return launch_decode_rows(w, outer * n_ids * inner_rows, m, out_dtype, out, st);
 }
 
-cudaError_t launch_take_packed(const uint8_t* src, int64_t outer, int64_t len, int64_t inner_bytes,
-                               const void* ids, int id64, int64_t n_ids, uint8_t* dst, cudaStream_t st) {
-    const int threads = 256;
+cudaError_t launch_take_packed(const TakeParts& tp, int64_t outer, int64_t len, const void* ids, int id64,
+                               int64_t n_ids, cudaStream_t st) {
+    const int64_t rows = outer * n_ids;
+    if (rows == 0 || tp.n == 0) return cudaSuccess;
+    const int64_t blocks = std::min<int64_t>((rows + 7) / 8, int64_t(num_sms()) * 16);
+    int64_t common = 0;  // the widest piece that divides every part's row
+    for (int part = 0; part < tp.n; ++part) common |= tp.inner[part];
     auto go = [&](auto vec) -> cudaError_t {
         using V = decltype(vec);
-        const int64_t total = outer * n_ids * (inner_bytes / static_cast<int64_t>(sizeof(V)));
-        if (total == 0) return cudaSuccess;
-        const int64_t blocks = std::min<int64_t>((total + threads - 1) / threads, int64_t(num_sms()) * 16);
-        take_packed_kernel<V><<<static_cast<unsigned>(blocks), threads, 0, st>>>(src, outer, len, inner_bytes,
-                                                                                ids, id64, n_ids, dst);
-        return cudaGetLastError();
+        return launch_pdl(take_packed_kernel<V>, static_cast<unsigned>(blocks), 256, 0, st, tp, outer, len, ids,
+                          id64, n_ids);
     };
-    if (inner_bytes % 16 == 0) return go(uint4{});
-    if (inner_bytes % 8 == 0) return go(uint2{});
-    if (inner_bytes % 4 == 0) return go(uint32_t{});
-    if (inner_bytes % 2 == 0) return go(uint16_t{});
+    if (common % 16 == 0) return go(uint4{});
+    if (common % 8 == 0) return go(uint2{});
+    if (common % 4 == 0) return go(uint32_t{});
+    if (common % 2 == 0) return go(uint16_t{});
     return go(uint8_t{});
 }
 

@@ -72,6 +72,7 @@ Path experts_path(const WDesc& w, int64_t P, bool allow_tensor) {
 // positions in range, one warp per row in 16-byte pieces.
 __global__ void __launch_bounds__(256) gather_rows_kernel(const int32_t* n_in_p, const int32_t* perm, int xdiv,
                                                           const uint4* x, int64_t row_vecs, uint4* xs) {
+    grid_launch_dependents();
     grid_dependency_wait();
     const int64_t n_in = *n_in_p;
     const int lane = threadIdx.x & 31;
@@ -87,6 +88,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const int32_t* n_in_p,
 // Per-chunk histogram of in-range ids: chunk_counts[chunk][e].
 __global__ void __launch_bounds__(256) route_count_kernel(const void* ids, int id64, int64_t P,
                                                           int64_t E, int32_t* chunk_counts) {
+    grid_launch_dependents();
+    grid_dependency_wait();  // ids may come from the previous kernel
     extern __shared__ int32_t cnt[];
     for (int64_t e = threadIdx.x; e < E; e += blockDim.x) cnt[e] = 0;
     __syncthreads();
@@ -109,6 +112,8 @@ __global__ void __launch_bounds__(32) route_scatter_kernel(const void* ids, int 
                                                            int64_t E, const int32_t* chunk_counts,
                                                            int32_t* counts, int32_t* offsets,
                                                            int32_t* perm, uint16_t* zy, int64_t zn) {
+    grid_launch_dependents();
+    grid_dependency_wait();
     extern __shared__ int32_t sm[];
     int32_t* base = sm;           // [E + 1]: where this chunk's positions of expert e start
     int32_t* run = sm + E + 1;    // [E + 1]: how many of them are placed so far
@@ -282,10 +287,11 @@ cudaError_t launch_route(const void* ids, int id64, int64_t P, int64_t E, int32_
         cudaFuncSetAttribute(route_count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm1));
         cudaFuncSetAttribute(route_scatter_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(sm2));
     }
-    route_count_kernel<<<static_cast<unsigned>(nchunks), 256, sm1, st>>>(ids, id64, P, E, chunk_counts);
-    route_scatter_kernel<<<static_cast<unsigned>(nchunks), 32, sm2, st>>>(ids, id64, P, E, chunk_counts,
-                                                                          counts, offsets, perm, zy, zn);
-    return cudaGetLastError();
+    cudaError_t e = launch_pdl(route_count_kernel, static_cast<unsigned>(nchunks), 256, sm1, st, ids, id64, P, E,
+                               chunk_counts);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(route_scatter_kernel, static_cast<unsigned>(nchunks), 32, sm2, st, ids, id64, P, E,
+                      static_cast<const int32_t*>(chunk_counts), counts, offsets, perm, zy, zn);
 }
 
 qm_status launch_experts(const WDesc& w, const void* ids, int id64, int64_t T, int64_t topk,
@@ -308,9 +314,9 @@ qm_status launch_experts(const WDesc& w, const void* ids, int id64, int64_t T, i
     if (path == Path::kTensor) {  // routed rows gathered expert by expert, then the tensor-core product
         uint4* xs = reinterpret_cast<uint4*>(wb + l.xs);
         const int64_t blocks = std::min<int64_t>((P + 7) / 8, int64_t(num_sms()) * 8);
-        gather_rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(
-            offsets + E, perm, xdiv, static_cast<const uint4*>(x), w.k * 2 / 16, xs);
-        e = cudaGetLastError();
+        e = launch_pdl(gather_rows_kernel, static_cast<unsigned>(blocks), 256, 0, st,
+                       static_cast<const int32_t*>(offsets + E), static_cast<const int32_t*>(perm), xdiv,
+                       static_cast<const uint4*>(x), static_cast<int64_t>(w.k * 2 / 16), xs);
         if (e != cudaSuccess) return cuda_fail(e, "gather launch");
         return launch_gemm_grouped(w, offsets, perm, P, xs, y, st);
     }

@@ -55,9 +55,16 @@ int max_smem_optin();
 // ------------------------------------------------------------ launchers
 // Each returns the CUDA error of its launch (cudaSuccess when nothing ran).
 cudaError_t launch_dequant(const WDesc& w, int out_dtype, void* out, cudaStream_t st);
-cudaError_t launch_take_packed(const uint8_t* src, int64_t outer, int64_t len, int64_t inner_bytes,
-                               const void* ids, int id64, int64_t n_ids, uint8_t* dst,
-                               cudaStream_t st);
+// The parts of a packed take: up to three (codes, scales, biases), each a
+// source of `len` rows of inner[part] bytes per outer index and a destination.
+struct TakeParts {
+    int n = 0;
+    const uint8_t* src[3] = {nullptr, nullptr, nullptr};
+    uint8_t* dst[3] = {nullptr, nullptr, nullptr};
+    int64_t inner[3] = {0, 0, 0};
+};
+cudaError_t launch_take_packed(const TakeParts& tp, int64_t outer, int64_t len, const void* ids, int id64,
+                               int64_t n_ids, cudaStream_t st);
 cudaError_t launch_take_dense(const WDesc& w, int axis, const void* ids, int id64, int64_t n_ids,
                               int out_dtype, void* out, cudaStream_t st);
 
