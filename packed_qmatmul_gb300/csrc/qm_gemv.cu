@@ -367,15 +367,15 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
         int issued = 0;
         bool xdone = false;
         const int npre = p.static_w ? std::min(nst, static_cast<int>(p.nstage)) : 0;
+        uint32_t slot = 0, fill = 0;  // stage j goes to slot j mod nstage, fill j / nstage of it
         #pragma unroll 1
-        for (int j = 0; j < nst; ++j) {
+        for (int j = 0; j < nst; ++j, (++slot == p.nstage) ? (slot = 0, ++fill) : 0u) {
             if (p.static_w && !xdone && j == npre) {
                 grid_dependency_wait();
                 copy_x();
                 xdone = true;
             }
-            const uint32_t slot = j % p.nstage;
-            const uint32_t par = ((j / p.nstage) & 1) ^ 1;
+            const uint32_t par = (fill & 1) ^ 1;
             if (!mbar_wait(bar_empty0 + 8 * slot, par) || s_abort) {
                 if (lane == 0) { atomicOr(&g_err_gemv, DEV_ERR_TIMEOUT); s_abort = 1; }
                 break;
@@ -563,9 +563,16 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
         int buf = 0;
         // Every warp of a team runs the same iterations and meets the team
         // barrier once per stage, abandoned or not, so no barrier is left waiting.
+        // slot of stage j and how many times it was filled before, kept
+        // incrementally (nteams <= nstage): j mod nstage and j / nstage
+        uint32_t slot = team, fill = 0;
+        while (slot >= p.nstage) { slot -= p.nstage; ++fill; }
         #pragma unroll 1
         for (int j = team; j < nst; j += nteams) {
-            const uint32_t slot = j % p.nstage;
+            if (j != team) {
+                slot += nteams;
+                while (slot >= p.nstage) { slot -= p.nstage; ++fill; }
+            }
             bool live = !s_abort;
             if (live && lane == 0 && slot_stage[slot] != j) {  // the producer has not started stage j yet
                 const uint64_t t0 = globaltimer();
@@ -579,7 +586,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                 live = !s_abort;
             }
             live = __shfl_sync(0xffffffffu, live ? 1 : 0, 0) != 0;
-            if (live && !mbar_wait(bar_full0 + 8 * slot, (j / p.nstage) & 1)) {
+            if (live && !mbar_wait(bar_full0 + 8 * slot, fill & 1)) {
                 if (lane == 0) { atomicOr(&g_err_gemv, DEV_ERR_TIMEOUT); s_abort = 1; }
                 live = false;
             }
