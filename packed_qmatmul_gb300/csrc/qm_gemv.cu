@@ -112,7 +112,11 @@ QM_DEV void dec8(uint32_t w, uint32_t& lo, uint32_t& hi) {
     hi = prmt(w, 0x64646464u, 0x7362);
 }
 
-QM_DEV float sval(uint32_t h, int sdt) { return sdt == QM_F16 ? f16_bits_to_f32(h) : bf16_bits_to_f32(h); }
+template <int SDT>
+QM_DEV float sval(uint32_t h) {
+    if constexpr (SDT == QM_F16) return f16_bits_to_f32(h);
+    else return bf16_bits_to_f32(h);
+}
 
 // A stage's codes are 128-byte boxes of 32 rows, each box 128B-swizzled by
 // the TMA unit: byte b of row r sits in box b / 128, at row r's 128-byte
@@ -280,8 +284,9 @@ static __device__ __noinline__ void group_lookup(const Params& p, int slot, int 
 
 // NTK: token tiles of 8 (1 for M <= 8, 2 for M <= 16), or 0 for exactly one
 // token: the layout of NTK = 1, with the epilogue and the sums over a team
-// restricted to the accumulator entries that hold token 0.
-template <int FMT, int BITS, int GS, int NTK>
+// restricted to the accumulator entries that hold token 0. SDT: the affine
+// scale and bias dtype (QM_BF16 or QM_F16; unused by the other formats).
+template <int FMT, int BITS, int GS, int NTK, int SDT>
 __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant__ Params p) {
     constexpr int NT = NTK == 0 ? 1 : NTK;
     constexpr bool ONE = NTK == 0;
@@ -636,10 +641,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                         const uint32_t sa = st + p.off_scales + ra * p.scale_seg + 2 * gi;
                         const uint32_t ba = sa + (p.off_biases - p.off_scales);
                         const uint32_t r8 = 8 * p.scale_seg;
-                        s0 = sval(lds_u16(sa), p.sdt);
-                        s8 = sval(lds_u16(sa + r8), p.sdt);
-                        b0 = sval(lds_u16(ba), p.sdt);
-                        b8 = sval(lds_u16(ba + r8), p.sdt);
+                        s0 = sval<SDT>(lds_u16(sa));
+                        s8 = sval<SDT>(lds_u16(sa + r8));
+                        b0 = sval<SDT>(lds_u16(ba));
+                        b8 = sval<SDT>(lds_u16(ba + r8));
                     } else if constexpr (FMT == QM_Q8_0) {
                         const uint32_t da = rows_[2 * tt].at(34 * gi);
                         s0 = f16_bits_to_f32(lds_u16(da));
@@ -948,9 +953,9 @@ static Plan make_plan(const WDesc& w, int64_t M, double share = 1.0) {
     return best;
 }
 
-template <int FMT, int BITS, int GS, int NTK>
-static cudaError_t launch_t(const Plan& pl, cudaStream_t st) {
-    auto kern = gemv_kernel<FMT, BITS, GS, NTK>;
+template <int FMT, int BITS, int GS, int NTK, int SDT>
+static cudaError_t launch_k(const Plan& pl, cudaStream_t st) {
+    auto kern = gemv_kernel<FMT, BITS, GS, NTK, SDT>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(pl.smem));
     if (e != cudaSuccess) return e;
@@ -978,6 +983,14 @@ static cudaError_t launch_t(const Plan& pl, cudaStream_t st) {
     cfg.attrs = attrs;
     cfg.numAttrs = na;
     return cudaLaunchKernelEx(&cfg, kern, pl.p);
+}
+
+template <int FMT, int BITS, int GS, int NTK>
+static cudaError_t launch_t(const Plan& pl, cudaStream_t st) {
+    if constexpr (FMT == QM_AFFINE) {
+        if (pl.p.sdt == QM_F16) return launch_k<FMT, BITS, GS, NTK, QM_F16>(pl, st);
+    }
+    return launch_k<FMT, BITS, GS, NTK, QM_BF16>(pl, st);
 }
 
 }  // namespace gemv
