@@ -47,16 +47,27 @@ def normal_bf16(g: np.random.Generator, shape, sigma=1.0, absolute=False, add=0.
     return to_bf16_bits(v)
 
 
+def normal_f16(g: np.random.Generator, shape, sigma=1.0, absolute=False, add=0.0):
+    """float16 bit patterns of N(0, sigma) draws (NumPy's conversion, round to nearest even)."""
+    v = g.standard_normal(shape, dtype=np.float32) * np.float32(sigma)
+    if absolute:
+        v = np.abs(v)
+    if add:
+        v = v + np.float32(add)
+    return v.astype(np.float16).view(np.uint16)
+
+
 def affine_weight(g, n, k, bits=4, group_size=64, lead=(), scale_sigma=0.02, scale_add=0.0,
-                  bias_sigma=0.02):
-    """MLX affine weight [*lead, n, k]."""
+                  bias_sigma=0.02, scale_dtype="bf16"):
+    """MLX affine weight [*lead, n, k]; scales and biases bf16 or f16."""
     assert (k * bits) % 32 == 0 and k % group_size == 0
     shape = tuple(lead) + (n,)
     codes = g.integers(0, 2**32, size=shape + (k * bits // 32,), dtype=np.uint64).astype(np.uint32)
-    scales = normal_bf16(g, shape + (k // group_size,), scale_sigma, absolute=True, add=scale_add)
-    biases = normal_bf16(g, shape + (k // group_size,), bias_sigma)
+    draw = normal_f16 if scale_dtype == "f16" else normal_bf16
+    scales = draw(g, shape + (k // group_size,), scale_sigma, absolute=True, add=scale_add)
+    biases = draw(g, shape + (k // group_size,), bias_sigma)
     return dict(format=AFFINE, shape=shape + (k,), bits=bits, group_size=group_size,
-                scale_dtype="bf16", codes=codes, scales=scales, biases=biases)
+                scale_dtype=scale_dtype, codes=codes, scales=scales, biases=biases)
 
 
 def q8_0_weight(g, n, k, lead=(), d_sigma=0.005):

@@ -384,6 +384,35 @@ def test_apply_experts_moe_shape_sampled(T):
     check_product(got[pos], ref, wn, xn, k, f"moe T={T} positions {pos.tolist()}")
 
 
+@pytest.mark.parametrize("bits,gs", [(4, 64), (8, 32), (4, 128)])
+def test_f16_scales_every_entry_point(bits, gs):
+    # affine scales and biases stored as float16 (the other dtype the format
+    # allows): dequant bit-exact, take, decode and tensor-core products, experts
+    g = synth.rng(1220 + bits + gs)
+    n, k = 200, 1024
+    w = synth.affine_weight(g, n, k, bits=bits, group_size=gs, scale_dtype="f16")
+    ow = to_oracle(w)
+    qw = qm.QWeight.from_arrays(w)
+    for dt in (torch.bfloat16, torch.float16, torch.float32):
+        got = _host(qm.dequant(qw, dt))
+        assert _bits_equal(got, oracle.dequant(ow, ODT[dt]), dt), dt
+    ids = synth.uniform_ids(g, 50, n)
+    tw, dense = qm.take(qw, 0, torch.from_numpy(ids).cuda(), dense_dtype=torch.bfloat16)
+    ot = oracle.take(ow, 0, ids)
+    for name, part in (("codes", tw.codes), ("scales", tw.scales), ("biases", tw.biases)):
+        assert np.array_equal(_host(part).view(np.uint8).reshape(-1),
+                              ot.parts()[name].view(np.uint8).reshape(-1)), name
+    assert np.array_equal(_host(dense), oracle.dequant(ot, oracle.BF16))
+    for M in (1, 3, 16, 64, 200):
+        x = synth.activations(g, M, k)
+        _check_apply(w, x, f"f16 scales bits={bits} gs={gs} M={M}")
+    E = 4
+    we = synth.affine_weight(g, 96, 512, bits=bits, group_size=gs, lead=(E,), scale_dtype="f16")
+    for T in (6, 80):  # decode path, then the tensor cores
+        ide = synth.expert_ids(g, T, 2, E)
+        _check_experts(we, ide, synth.activations(g, T, 512), f"f16 scales experts T={T}")
+
+
 # ---------------------------------------------------------------- long pipelines
 @pytest.mark.parametrize("kind,n,k", [("affine4_g64", 40000, 1024), ("affine8_g32", 20000, 512),
                                       ("q8_0", 12000, 1024), ("mxfp4", 30000, 256)])
