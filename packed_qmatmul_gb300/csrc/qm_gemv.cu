@@ -494,25 +494,69 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
         //    also sums its token's B values (F) and x' (X) over the group
         uint32_t* xfrag = reinterpret_cast<uint32_t*>(smem + p.off_xfrag);
         float2* tok = reinterpret_cast<float2*>(smem + p.off_tok);  // [groups][16]
-        {
-            // one token: only lanes 0..3 (t) of a warp hold nonzero B values,
-            // so the fragments are kept for those four lanes alone, [gi][t][MM][2]
-            const int items = ONE ? (groups * 4 + 31) / 32 * 32 : groups * 32 * NT;  // whole warps
+        if constexpr (ONE) {
+            // One token: only lanes 0..3 (t) of a warp hold nonzero B values, so
+            // the fragments are kept for those four lanes alone, [gi][t][MM][2].
+            // A work item is one MMA's pair of registers (gi, mm, t): a group's
+            // 4 MM items sit in adjacent lanes of one warp, which add its sums.
+            const int items = (groups * MM * 4 + 31) / 32 * 32;
+            const float mul = __uint_as_float(static_cast<uint32_t>(token_exp(0) + 127) << 23);
             #pragma unroll 1
             for (int it = ctid; it < items; it += kWarps * 32) {
-                const int ln = it % 32;
-                const int nt = ONE ? 0 : (it / 32) % NT;
-                const int gi = ONE ? it / 4 : it / (32 * NT);
-                const int tg = ONE ? 0 : ln >> 2, t = ln & 3;
+                const int t = it & 3, mm = (it >> 2) % MM, gi = (it >> 2) / MM;
+                const bool live = gi < groups;
+                auto xv = [&](int kk) { return live ? bf16_bits_to_f32(xs[kk]) * mul : 0.0f; };
+                float lo0, hi0, lo1, hi1, f1 = 1.0f;  // registers 2mm: (lo0, hi0), 2mm+1: f1 (lo1, hi1)
+                if constexpr (FMT == QM_AFFINE && BITS == 4) {
+                    constexpr int V = GS / 32;
+                    const int v = mm >> 1, h = mm & 1;
+                    const int k0 = 8 * (gi * (GS / 8) + t * V + v);
+                    lo0 = xv(k0 + 2 * h);
+                    hi0 = xv(k0 + 4 + 2 * h);
+                    lo1 = xv(k0 + 1 + 2 * h);
+                    hi1 = xv(k0 + 5 + 2 * h);
+                    f1 = 0.0625f;
+                } else if constexpr (FMT == QM_AFFINE && BITS == 8) {
+                    constexpr int V = GS / 16;
+                    const int k0 = 4 * (gi * (GS / 4) + t * V + mm);
+                    lo0 = xv(k0); hi0 = xv(k0 + 1); lo1 = xv(k0 + 2); hi1 = xv(k0 + 3);
+                } else {  // Q8_0, MXFP4: lane t holds values 8t .. 8t+7 of the block
+                    const int k0 = 32 * gi + 8 * t + 4 * mm;
+                    lo0 = xv(k0); hi0 = xv(k0 + 1); lo1 = xv(k0 + 2); hi1 = xv(k0 + 3);
+                }
+                if (live) {
+                    uint32_t* dst = xfrag + (gi * 4 + t) * MM * 2 + mm * 2;
+                    dst[0] = pack_f16x2(lo0, hi0);
+                    dst[1] = pack_f16x2(lo1 * f1, hi1 * f1);
+                }
+                if constexpr (FMT != QM_MXFP4) {
+                    // the offset the magic adds: magic * sum of the B values the MMAs see
+                    float X = (lo0 + hi0) + (lo1 + hi1);
+                    float F = (lo0 + hi0) + (lo1 * f1 + hi1 * f1);
+#pragma unroll
+                    for (int o = 1; o < 4 * MM; o <<= 1) {
+                        X += __shfl_xor_sync(0xffffffffu, X, o);
+                        F += __shfl_xor_sync(0xffffffffu, F, o);
+                    }
+                    const float magic = (FMT == QM_Q8_0) ? 1152.0f : 1024.0f;
+                    if (t == 0 && mm == 0 && live) tok[gi * 16] = make_float2(magic * F, X);
+                }
+            }
+        } else {
+            const int items = groups * 32 * NT;  // a multiple of 32: a warp shares (gi, nt)
+            #pragma unroll 1
+            for (int it = ctid; it < items; it += kWarps * 32) {
+                const int ln = it % 32, nt = (it / 32) % NT, gi = it / (32 * NT);
+                const int tg = ln >> 2, t = ln & 3;
                 const int m = nt * 8 + tg;
-                const bool live = m < M && (!ONE || gi < groups);  // padding gets exact zeros
+                const bool live = m < M;  // padding tokens get exact zeros
                 const float mul = live ? __uint_as_float(static_cast<uint32_t>(token_exp(m) + 127) << 23) : 0.0f;
                 const uint16_t* xr = xs + (live ? m : 0) * p.krange;
-                uint32_t* dst = ONE ? xfrag + (gi * 4 + t) * MM * 2 : xfrag + ((gi * 32 + ln) * MM) * NT * 2 + nt * 2;
+                uint32_t* dst = xfrag + ((gi * 32 + ln) * MM) * NT * 2 + nt * 2;
                 float F = 0.0f, X = 0.0f;
                 auto xv = [&](int kk) { return live ? bf16_bits_to_f32(xr[kk]) * mul : 0.0f; };
                 auto put = [&](int idx, float lo, float hi, float flo, float fhi) {
-                    if (!ONE || gi < groups) dst[idx] = pack_f16x2(lo * flo, hi * fhi);
+                    dst[idx] = pack_f16x2(lo * flo, hi * fhi);
                     X += lo + hi;
                     F += lo * flo + hi * fhi;
                 };
@@ -551,7 +595,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                     X += __shfl_xor_sync(0xffffffffu, X, 2);
                     F += __shfl_xor_sync(0xffffffffu, F, 2);
                     const float magic = (FMT == QM_Q8_0) ? 1152.0f : 1024.0f;
-                    if (t == 0 && (!ONE || gi < groups)) tok[gi * 16 + m] = make_float2(magic * F, X);
+                    if (t == 0) tok[gi * 16 + m] = make_float2(magic * F, X);
                 }
             }
         }
