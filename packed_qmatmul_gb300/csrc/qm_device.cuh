@@ -163,20 +163,18 @@ QM_DEV void cluster_wait() {
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Store to shared memory of another CTA of the cluster (address from mapa).
-QM_DEV void st_shared_cluster_f32(uint32_t addr, float v) {
-    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
-}
-
 QM_DEV void st_shared_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                  : "memory");
 }
 
-// Arrive on an mbarrier in another CTA of the cluster, releasing this
-// thread's earlier writes at cluster scope.
-QM_DEV void mbar_arrive_cluster(uint32_t remote_bar) {
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(remote_bar) : "memory");
+// Asynchronous store into another CTA's shared memory that counts its 4 bytes
+// against that CTA's mbarrier (complete_tx): the receiver's wait on the
+// barrier sees the data, and the sender needs no arrival of its own.
+QM_DEV void st_async_f32(uint32_t remote_addr, float v, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(remote_addr),
+                 "r"(__float_as_uint(v)), "r"(remote_bar)
+                 : "memory");
 }
 
 // Address of the same shared variable in CTA `rank` of this cluster.
@@ -186,11 +184,6 @@ QM_DEV uint32_t map_shared_rank(uint32_t addr, uint32_t rank) {
     return r;
 }
 
-QM_DEV float ld_shared_cluster_f32(uint32_t addr) {
-    float v;
-    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
-    return v;
-}
 
 // ---------------------------------------------------------------- tcgen05 (5th-gen tensor cores)
 // TMEM allocation: the whole warp executes; the base address lands in smem.

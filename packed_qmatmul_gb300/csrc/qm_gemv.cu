@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
             mbar_init(bar_empty0 + 8 * i, p.team);  // the warps of the team that read it
         }
         mbar_init(bar_x, 1);
-        if (S > 1 && rank == 0) mbar_init(bar_red, (S - 1) * kThreads);
+        if (S > 1 && rank == 0) mbar_init(bar_red, 1);  // rank 0's own arrival; the pushes count bytes
         fence_mbar_init();
     }
     __syncthreads();
@@ -819,8 +819,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
     }
 
     // ---------------------------------------------------------------- split-k reduction
-    // The CTAs of rank 1.. push their sums into rank 0's receive area and
-    // leave; rank 0 adds them in rank order and stores y.
+    // The CTAs of rank 1.. push their sums into rank 0's receive area with
+    // asynchronous stores that count against rank 0's barrier, and leave;
+    // rank 0 adds them in rank order and stores y.
     if (S > 1) {
         __syncthreads();  // this CTA's partial sums are complete
         cluster_wait();   // rank 0's barrier is initialized
@@ -828,11 +829,15 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
         const float* own = reinterpret_cast<const float*>(smem + p.off_xraw);  // [row][16]
         if (rank != 0) {
             const uint32_t dst = map_shared_rank(smem_u32(smem + p.off_recv), 0) + (rank - 1) * ent * 4u;
+            const uint32_t rbar = map_shared_rank(bar_red, 0);
             #pragma unroll 1
             for (int e = threadIdx.x; e < ent; e += blockDim.x)
-                st_shared_cluster_f32(dst + 4u * e, own[(e / M) * 16 + e % M]);
-            mbar_arrive_cluster(map_shared_rank(bar_red, 0));
+                st_async_f32(dst + 4u * e, own[(e / M) * 16 + e % M], rbar);
         } else {
+            if (threadIdx.x == 0) {
+                mbar_expect_tx(bar_red, static_cast<uint32_t>((S - 1) * ent * 4));
+                mbar_arrive(bar_red);
+            }
             const bool ok = mbar_wait(bar_red, 0);
             if (!ok && threadIdx.x == 0) atomicOr(&g_err_gemv, DEV_ERR_TIMEOUT);
             const float* recv = reinterpret_cast<const float*>(smem + p.off_recv);  // [rank - 1][ent]
