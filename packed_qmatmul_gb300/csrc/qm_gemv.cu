@@ -603,9 +603,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
 
         // 3. main loop: team `team` takes stages team, team + nteams, ...;
         //    warp wi of the team covers groups [gb, ge) of each.
-        const int T = p.team, nteams = kWarps / T;
-        const int team = warp / T, wi = warp % T;
-        const int gb = wi * groups / T, ge = (wi + 1) * groups / T;
+        // the team size is a power of two: shifts, not divisions
+        const int T = p.team, lt = __ffs(T) - 1, nteams = kWarps >> lt;
+        const int team = warp >> lt, wi = warp & (T - 1);
+        const int gb = (wi * groups) >> lt, ge = ((wi + 1) * groups) >> lt;
         const int g = lane >> 2, t = lane & 3;
         float* partial = reinterpret_cast<float*>(smem + p.off_xraw);  // [stages][32 rows][16 tok]
         float* red = reinterpret_cast<float*>(smem + p.off_red);       // [teams][2][T][2][NT][4][32]
@@ -623,7 +624,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                 while (slot >= p.nstage) { slot -= p.nstage; ++fill; }
             }
             bool live = !s_abort;
-            if (live && lane == 0 && slot_stage[slot] != j) {  // the producer has not started stage j yet
+            // A slot's first fill needs no tag: its barrier's first phase can only
+            // be that fill. Later fills check that the producer has started stage j.
+            if (fill > 0 && live && lane == 0 && slot_stage[slot] != j) {
                 const uint64_t t0 = globaltimer();
                 #pragma unroll 1
                 for (int spin = 0; slot_stage[slot] != j && !s_abort; ++spin)
