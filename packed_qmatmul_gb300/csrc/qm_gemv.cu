@@ -92,7 +92,12 @@ struct Params {
     // shared memory layout (byte offsets from the dynamic smem base)
     uint32_t nstage, stage_bytes;
     uint32_t code_seg, nbox;          // per row: bytes of codes; 128-byte boxes per stage
-    uint32_t scale_seg;               // per row bytes of scales (and of biases) in a stage
+    uint32_t scale_seg;               // per row bytes of scales (and of biases) of this CTA's k range
+    // scale_span: a stage holds whole rows of scales (and biases), copied as one
+    // span, scale_row_bytes apart, this CTA's part at rank * scale_seg; else
+    // (a k split whose part is a 16-byte multiple) one 2-d box of scale_seg-byte rows
+    int scale_span;
+    uint32_t scale_pitch;
     uint32_t off_scales, off_biases;  // within a stage
     uint32_t off_tokscale, off_tok, off_xfrag, off_red, off_xraw, off_recv, off_stages;
 };
@@ -395,10 +400,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
             uint32_t tx = p.nbox * kRows * 128;
             uint32_t span = 0, span_bulk = 0;
             if (p.scale_seg) {
-                if (S > 1) {
+                if (!p.scale_span) {
                     tx += kRows * p.scale_seg * (p.biases ? 2 : 1);
                 } else {
-                    span = rows * p.scale_seg;
+                    span = rows * static_cast<uint32_t>(p.scale_row_bytes);
                     span_bulk = span & ~15u;
                     tx += span_bulk * (p.biases ? 2 : 1);
                 }
@@ -410,14 +415,14 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                 #pragma unroll 1
                 for (uint32_t c = 0; c < p.nbox; ++c)
                     tma_load_2d(smem_u32(st + c * kRows * 128), &p.tm_codes, x0 + 128 * c, y0, bar);
-                if (p.scale_seg && S > 1) {
+                if (p.scale_seg && !p.scale_span) {
                     const int32_t xs0 = static_cast<int32_t>(rank * p.scale_seg);
                     tma_load_2d(smem_u32(st + p.off_scales), &p.tm_scales, xs0, y0, bar);
                     if (p.biases) tma_load_2d(smem_u32(st + p.off_biases), &p.tm_biases, xs0, y0, bar);
                 }
             }
             __syncwarp();
-            if (p.scale_seg && S == 1) {
+            if (p.scale_seg && p.scale_span) {
                 const int64_t off = (wrow0 + row0) * p.scale_row_bytes;
                 if (lane == 0 && span_bulk) {
                     bulk_g2s(smem_u32(st + p.off_scales), p.scales + off, span_bulk, bar);
@@ -608,6 +613,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
         const int team = warp >> lt, wi = warp & (T - 1);
         const int gb = (wi * groups) >> lt, ge = ((wi + 1) * groups) >> lt;
         const int g = lane >> 2, t = lane & 3;
+        const uint32_t soff = p.scale_span ? rank * p.scale_seg : 0u;  // this CTA's part of a scale row
         float* partial = reinterpret_cast<float*>(smem + p.off_xraw);  // [stages][32 rows][16 tok]
         float* red = reinterpret_cast<float*>(smem + p.off_red);       // [teams][2][T][2][NT][4][32]
         int buf = 0;
@@ -684,10 +690,10 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                     const int ra = 16 * tt + g, rb = ra + 8;
                     float s0, s8, b0 = 0.0f, b8 = 0.0f;
                     if constexpr (FMT == QM_AFFINE) {
-                        // row ra, group gi; row rb = ra + 8 lies 8 rows of scale_seg bytes on
-                        const uint32_t sa = st + p.off_scales + ra * p.scale_seg + 2 * gi;
+                        // row ra, group gi; row rb = ra + 8 lies 8 rows of scale_pitch bytes on
+                        const uint32_t sa = st + p.off_scales + ra * p.scale_pitch + soff + 2 * gi;
                         const uint32_t ba = sa + (p.off_biases - p.off_scales);
-                        const uint32_t r8 = 8 * p.scale_seg;
+                        const uint32_t r8 = 8 * p.scale_pitch;
                         s0 = sval<SDT>(lds_u16(sa));
                         s8 = sval<SDT>(lds_u16(sa + r8));
                         b0 = sval<SDT>(lds_u16(ba));
@@ -697,9 +703,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                         s0 = f16_bits_to_f32(lds_u16(da));
                         s8 = f16_bits_to_f32(lds_u16(da + (rows_[2 * tt + 1].line - rows_[2 * tt].line)));
                     } else {
-                        const uint32_t sa = st + p.off_scales + ra * p.scale_seg + gi;
+                        const uint32_t sa = st + p.off_scales + ra * p.scale_pitch + soff + gi;
                         s0 = e8m0_to_f32(lds_u8(sa));
-                        s8 = e8m0_to_f32(lds_u8(sa + 8 * p.scale_seg));
+                        s8 = e8m0_to_f32(lds_u8(sa + 8 * p.scale_pitch));
                     }
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
@@ -924,15 +930,19 @@ static bool plan_for(const WDesc& w, int64_t M, int S, int per_sm, Plan* out, do
     int64_t sseg = 0;
     if (w.fmt == QM_AFFINE) sseg = kr / w.gs * 2;
     if (w.fmt == QM_MXFP4) sseg = kr / 32;
-    if (S > 1 && sseg % 16) return false;
-    if (S > 1 && (sseg > 256 || w.scale_row_bytes % 16)) return false;  // scale boxes
+    // scales by 2-d boxes of this CTA's part, where a box can take it; else
+    // whole rows as a span (k whole, or a part that is no 16-byte multiple)
+    const bool boxes = S > 1 && sseg % 16 == 0 && sseg <= 256 && w.scale_row_bytes % 16 == 0;
+    if (S > 1 && !boxes && M > 1) return false;  // whole scale rows per rank: measured slower with several tokens
     Params& p = out->p;
     p = Params{};
     p.code_seg = static_cast<uint32_t>(cseg);
     p.nbox = static_cast<uint32_t>((cseg + 127) / 128);
     p.scale_seg = static_cast<uint32_t>(sseg);
+    p.scale_span = boxes ? 0 : 1;
+    p.scale_pitch = static_cast<uint32_t>(boxes ? sseg : w.scale_row_bytes);
     const uint32_t codes_bytes = p.nbox * kRows * 128;
-    const uint32_t sc_bytes = round_up(kRows * sseg, 128);
+    const uint32_t sc_bytes = round_up(kRows * (sseg ? p.scale_pitch : 0), 128);
     p.off_scales = codes_bytes;
     p.off_biases = codes_bytes + sc_bytes;
     p.stage_bytes = round_up(codes_bytes + sc_bytes * (w.fmt == QM_AFFINE ? 2 : 1), 1024);  // swizzled boxes
@@ -985,8 +995,9 @@ static bool plan_for(const WDesc& w, int64_t M, int S, int per_sm, Plan* out, do
 }
 
 // Pick the k split and CTAs per SM: least per-CTA work (stages x k range,
-// halved where two CTAs share an SM), then fewest splits; a plan that keeps
-// three stages in flight beats one that cannot.
+// halved where two CTAs share an SM) plus a fixed cost per extra rank of a k
+// split, then fewest splits; a plan that keeps three stages in flight beats
+// one that cannot.
 static Plan make_plan(const WDesc& w, int64_t M, double share = 1.0) {
     Plan best;
     double best_cost = 1e300;
@@ -995,8 +1006,13 @@ static Plan make_plan(const WDesc& w, int64_t M, double share = 1.0) {
             Plan pl;
             if (!plan_for(w, M, S, per_sm, &pl, share)) continue;
             const bool shallow = pl.p.nstage < 3 && pl.p.stages_per_cluster >= 3;
+            // one token: each extra rank of a k split costs a fixed hand-off
+            // (its partial sums reach rank 0 through distributed shared memory),
+            // measured on GB300 to be worth about 1024 k values of one stage; with
+            // more tokens the activation work per CTA favors the wider splits
             const double cost = static_cast<double>(pl.p.stages_per_cluster) * pl.p.krange / per_sm *
-                                (1.0 + 0.03 * (S - 1)) * (shallow ? 2.0 : 1.0);
+                                    (1.0 + 0.03 * (S - 1)) * (shallow ? 2.0 : 1.0) +
+                                (M == 1 ? 1024.0 * (S - 1) : 0.0);
             if (cost < best_cost * 0.999) {
                 best_cost = cost;
                 best = pl;
@@ -1070,7 +1086,7 @@ qm_status launch_gemv(const WDesc& w, const void* x, int64_t M, void* y, cudaStr
     p.scale_row_bytes = w.scale_row_bytes;
     p.static_w = w.is_static ? 1 : 0;
     bool maps = make_tmap_2d(&p.tm_codes, w.codes, w.code_row_bytes, w.n, w.code_row_bytes, 128, kRows, true);
-    if (maps && p.S > 1 && p.scale_seg) {
+    if (maps && !p.scale_span && p.scale_seg) {
         maps = make_tmap_2d(&p.tm_scales, w.scales, w.scale_row_bytes, w.n, w.scale_row_bytes, p.scale_seg,
                             kRows, false);
         if (maps && w.biases)
@@ -1161,7 +1177,7 @@ qm_status launch_gemv_grouped(const WDesc& w, const int32_t* offsets, const int3
     p.g_wclusters = static_cast<int>(pl.grid / pl.S);
     const int64_t rows = E * w.n;
     bool maps = make_tmap_2d(&p.tm_codes, w.codes, w.code_row_bytes, rows, w.code_row_bytes, 128, kRows, true);
-    if (maps && p.S > 1 && p.scale_seg) {
+    if (maps && !p.scale_span && p.scale_seg) {
         maps = make_tmap_2d(&p.tm_scales, w.scales, w.scale_row_bytes, rows, w.scale_row_bytes, p.scale_seg,
                             kRows, false);
         if (maps && w.biases)
