@@ -687,7 +687,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
                 }
 #pragma unroll
                 for (int tt = 0; tt < 2; ++tt) {
-                    const int ra = 16 * tt + g, rb = ra + 8;
+                    const int ra = 16 * tt + g;  // and ra + 8
                     float s0, s8, b0 = 0.0f, b8 = 0.0f;
                     if constexpr (FMT == QM_AFFINE) {
                         // row ra, group gi; row rb = ra + 8 lies 8 rows of scale_pitch bytes on
