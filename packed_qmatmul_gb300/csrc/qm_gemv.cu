@@ -55,8 +55,9 @@ uint32_t gemv_read_clear_error() {
 namespace gemv {
 
 constexpr int kRows = 32;            // rows per stage (two MMA row tiles)
-constexpr int kWarps = 8;            // consumer warps
-constexpr int kThreads = (kWarps + 1) * 32;
+// consumer warps: 8 where two CTAs share an SM, 16 where one CTA has it alone
+constexpr int kThreadsOf(int cw) { return (cw + 1) * 32; }
+constexpr int kMaxTeams = 8;  // named barriers 2 .. 9
 constexpr int kMaxStages = 16;
 constexpr uint32_t kMagic = 0x64006400u;  // f16x2 (1024, 1024)
 
@@ -291,8 +292,9 @@ static __device__ __noinline__ void group_lookup(const Params& p, int slot, int 
 // token: the layout of NTK = 1, with the epilogue and the sums over a team
 // restricted to the accumulator entries that hold token 0. SDT: the affine
 // scale and bias dtype (QM_BF16 or QM_F16; unused by the other formats).
-template <int FMT, int BITS, int GS, int NTK, int SDT>
-__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant__ Params p) {
+template <int FMT, int BITS, int GS, int NTK, int SDT, int CW>
+__global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(const __grid_constant__ Params p) {
+    constexpr int kWarps = CW;
     constexpr int NT = NTK == 0 ? 1 : NTK;
     constexpr bool ONE = NTK == 0;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -871,6 +873,7 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
 struct Plan {
     Params p;
     int S = 1;
+    int cw = 8;  // consumer warps
     int64_t grid = 0;
     size_t smem = 0;
     bool ok = false;
@@ -886,21 +889,22 @@ static int64_t code_bytes(const WDesc& w, int64_t kk) {
 
 __global__ void cluster_probe_kernel() {}
 
-// Clusters of S CTAs (one per SM, `smem` bytes each) that can be resident at
-// once; cached per (device, S).
-static int max_clusters(int S, size_t smem) {
-    static int cache[64][9];
+// Clusters of S CTAs (`threads` threads and `smem` bytes each) that can be
+// resident at once; cached per (device, S, CTAs per SM), which fixes the other two.
+static int max_clusters(int S, int per_sm, int threads, size_t smem) {
+    static int cache[64][9][2];
     int dev = 0;
     cudaGetDevice(&dev);
     if (S <= 1) return num_sms();
-    if (dev >= 0 && dev < 64 && cache[dev][S] > 0) return cache[dev][S];
+    int* slot = (dev >= 0 && dev < 64) ? &cache[dev][S][per_sm - 1] : nullptr;
+    if (slot && *slot > 0) return *slot;
     int n = 0;
     cudaFuncSetAttribute(cluster_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                          static_cast<int>(smem));
     cudaFuncSetAttribute(cluster_probe_kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(S * 64);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute a;
     a.id = cudaLaunchAttributeClusterDimension;
@@ -913,7 +917,7 @@ static int max_clusters(int S, size_t smem) {
         cudaGetLastError();
         n = num_sms() / S;
     }
-    if (dev >= 0 && dev < 64) cache[dev][S] = n;
+    if (slot) *slot = n;
     return n;
 }
 
@@ -950,8 +954,9 @@ static bool plan_for(const WDesc& w, int64_t M, int S, int per_sm, Plan* out, do
     const int64_t budget = (per_sm == 2 ? (max_smem_optin() + 1024) / 2 : max_smem_optin()) - 1024;
     // work split: clusters of S CTAs, per_sm CTAs to an SM
     p.n_stages = (w.n + kRows - 1) / kRows;
+    const int cw = per_sm == 1 ? 16 : 8;
     int64_t G = std::max<int64_t>(1, static_cast<int64_t>(num_sms() * per_sm * share) / S);
-    if (S > 1) G = std::max<int64_t>(1, std::min<int64_t>(G, max_clusters(S, budget)));
+    if (S > 1) G = std::max<int64_t>(1, std::min<int64_t>(G, max_clusters(S, per_sm, kThreadsOf(cw), budget)));
     G = std::min<int64_t>(G, p.n_stages);
     const int64_t spc = (p.n_stages + G - 1) / G;
     G = (p.n_stages + spc - 1) / spc;
@@ -962,15 +967,25 @@ static bool plan_for(const WDesc& w, int64_t M, int S, int per_sm, Plan* out, do
         p.off_xfrag = round_up(p.off_tok + groups * 16 * 8, 128);
         // B fragments: 16 bytes per k value and token tile, or 2 for exactly one token
         const uint64_t xfrag_bytes = M == 1 ? static_cast<uint64_t>(kr) * 2 : static_cast<uint64_t>(kr) * 16 * NT;
-        p.off_red = round_up(p.off_xfrag + xfrag_bytes, 128);
-        const uint64_t red_bytes = M == 1 ? static_cast<uint64_t>(kWarps) * 2 * 32 * 4
-                                          : static_cast<uint64_t>(kWarps) * 2 * 2 * NT * 32 * 4 * 4;
-        p.off_xraw = round_up(p.off_red + red_bytes, 128);
+        const uint64_t red_bytes = M == 1 ? static_cast<uint64_t>(cw) * 2 * 32 * 4
+                                          : static_cast<uint64_t>(cw) * 2 * 2 * NT * 32 * 4 * 4;
         const uint64_t partial_bytes = S > 1 ? static_cast<uint64_t>(spc) * kRows * 16 * 4 : 0;
         const uint64_t xraw_bytes = static_cast<uint64_t>(M) * kr * 2;
+        // The raw activations are dead once the fragments are built (a barrier of
+        // all consumers), so the team sums, which start after it, reuse their
+        // room; with a k split the stages' partial sums take that room instead.
+        p.off_xraw = round_up(p.off_xfrag + xfrag_bytes, 128);
+        uint64_t end;
+        if (S == 1) {
+            p.off_red = p.off_xraw;
+            end = p.off_xraw + std::max(xraw_bytes, red_bytes);
+        } else {
+            p.off_red = round_up(p.off_xraw + std::max(partial_bytes, xraw_bytes), 128);
+            end = p.off_red + red_bytes;
+        }
         // split k: rank 0 receives the other ranks' sums apart from everything it may still be reading
         const uint64_t recv_bytes = S > 1 ? static_cast<uint64_t>(S - 1) * spc * kRows * M * 4 : 0;
-        p.off_recv = round_up(p.off_xraw + std::max(partial_bytes, xraw_bytes), 128);
+        p.off_recv = round_up(end, 128);
         p.off_stages = round_up(p.off_recv + recv_bytes, 1024);
         const int64_t room = budget - p.off_stages;
         return std::min<int64_t>(std::min<int64_t>(kMaxStages, room / p.stage_bytes), std::max<int64_t>(2, spc));
@@ -979,15 +994,16 @@ static bool plan_for(const WDesc& w, int64_t M, int S, int per_sm, Plan* out, do
     if (nst < 2) return false;
     // teams: one per stage a CTA can hold in flight, each warp at least one group
     int teams = 1;
-    while (teams * 2 <= kWarps && teams * 2 <= spc && teams * 2 <= nst) teams *= 2;
-    int T = kWarps / teams;
-    while (T > 1 && T > groups) T /= 2;
+    while (teams * 2 <= kMaxTeams && teams * 2 <= spc && teams * 2 <= nst) teams *= 2;
+    int T = cw / teams;
+    while (T > 1 && T > groups && cw / (T / 2) <= kMaxTeams) T /= 2;
     p.team = T;
     p.nstage = static_cast<uint32_t>(nst);
     p.S = S;
     p.krange = kr;
     p.stages_per_cluster = static_cast<int>(spc);
     out->S = S;
+    out->cw = cw;
     out->grid = G * S;
     out->smem = p.off_stages + nst * p.stage_bytes;
     out->ok = true;
@@ -1021,9 +1037,9 @@ static Plan make_plan(const WDesc& w, int64_t M, double share = 1.0) {
     return best;
 }
 
-template <int FMT, int BITS, int GS, int NTK, int SDT>
+template <int FMT, int BITS, int GS, int NTK, int SDT, int CW>
 static cudaError_t launch_k(const Plan& pl, cudaStream_t st) {
-    auto kern = gemv_kernel<FMT, BITS, GS, NTK, SDT>;
+    auto kern = gemv_kernel<FMT, BITS, GS, NTK, SDT, CW>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(pl.smem));
     if (e != cudaSuccess) return e;
@@ -1033,7 +1049,7 @@ static cudaError_t launch_k(const Plan& pl, cudaStream_t st) {
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(pl.grid));
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kThreadsOf(CW));
     cfg.dynamicSmemBytes = pl.smem;
     cfg.stream = st;
     cudaLaunchAttribute attrs[2];
@@ -1053,12 +1069,17 @@ static cudaError_t launch_k(const Plan& pl, cudaStream_t st) {
     return cudaLaunchKernelEx(&cfg, kern, pl.p);
 }
 
+template <int FMT, int BITS, int GS, int NTK, int CW>
+static cudaError_t launch_c(const Plan& pl, cudaStream_t st) {
+    if constexpr (FMT == QM_AFFINE) {
+        if (pl.p.sdt == QM_F16) return launch_k<FMT, BITS, GS, NTK, QM_F16, CW>(pl, st);
+    }
+    return launch_k<FMT, BITS, GS, NTK, QM_BF16, CW>(pl, st);
+}
+
 template <int FMT, int BITS, int GS, int NTK>
 static cudaError_t launch_t(const Plan& pl, cudaStream_t st) {
-    if constexpr (FMT == QM_AFFINE) {
-        if (pl.p.sdt == QM_F16) return launch_k<FMT, BITS, GS, NTK, QM_F16>(pl, st);
-    }
-    return launch_k<FMT, BITS, GS, NTK, QM_BF16>(pl, st);
+    return pl.cw == 16 ? launch_c<FMT, BITS, GS, NTK, 16>(pl, st) : launch_c<FMT, BITS, GS, NTK, 8>(pl, st);
 }
 
 }  // namespace gemv
