@@ -384,4 +384,15 @@ QM_DEV float e8m0_to_f32(uint32_t s) {
     return __uint_as_float(bits);
 }
 
+// Two e8m0 scale bytes at once (bits 0..7 and 8..15 of `pair`): Blackwell's
+// conversion to a bf16 pair is exact for every byte, since bf16 has float32's
+// exponent range (0 gives the subnormal 2^-127, 255 gives NaN); a bf16 is
+// the top half of the float32 of the same value.
+QM_DEV void e8m0x2_to_f32(uint32_t pair, float& lo, float& hi) {
+    uint32_t d;
+    asm("cvt.rn.bf16x2.ue8m0x2 %0, %1;" : "=r"(d) : "h"(static_cast<uint16_t>(pair)));
+    lo = __uint_as_float(d << 16);
+    hi = __uint_as_float(d & 0xFFFF0000u);
+}
+
 }  // namespace qm

@@ -680,7 +680,33 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
                 for (int tt = 0; tt < 2; ++tt)
                     tile_group<FMT, BITS, GS, NT>(rows_[2 * tt], rows_[2 * tt + 1], gi, t, bf, acc[tt]);
             };
-            auto epilogue = [&](int gi, const float (&acc)[2][NT][4]) {
+            // a group's scales (and biases) as raw bits, [tile][s0, s8, b0, b8]
+            // (rows ra and ra + 8 of the tile), loaded ahead of the group's MMAs
+            auto ep_load = [&](int gi, uint32_t (&raw)[2][4]) {
+#pragma unroll
+                for (int tt = 0; tt < 2; ++tt) {
+                    const int ra = 16 * tt + g;
+                    if constexpr (FMT == QM_AFFINE) {
+                        // row ra, group gi; row rb = ra + 8 lies 8 rows of scale_pitch bytes on
+                        const uint32_t sa = st + p.off_scales + ra * p.scale_pitch + soff + 2 * gi;
+                        const uint32_t ba = sa + (p.off_biases - p.off_scales);
+                        const uint32_t r8 = 8 * p.scale_pitch;
+                        raw[tt][0] = lds_u16(sa);
+                        raw[tt][1] = lds_u16(sa + r8);
+                        raw[tt][2] = lds_u16(ba);
+                        raw[tt][3] = lds_u16(ba + r8);
+                    } else if constexpr (FMT == QM_Q8_0) {
+                        const uint32_t da = rows_[2 * tt].at(34 * gi);
+                        raw[tt][0] = lds_u16(da);
+                        raw[tt][1] = lds_u16(da + (rows_[2 * tt + 1].line - rows_[2 * tt].line));
+                    } else {
+                        const uint32_t sa = st + p.off_scales + ra * p.scale_pitch + soff + gi;
+                        raw[tt][0] = lds_u8(sa);
+                        raw[tt][1] = lds_u8(sa + 8 * p.scale_pitch);
+                    }
+                }
+            };
+            auto epilogue = [&](int gi, const float (&acc)[2][NT][4], const uint32_t (&raw)[2][4]) {
                 float4 td[NT];  // (O[2t], X[2t], O[2t+1], X[2t+1]) per token half
                 if constexpr (FMT != QM_MXFP4) {
 #pragma unroll
@@ -689,25 +715,17 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
                 }
 #pragma unroll
                 for (int tt = 0; tt < 2; ++tt) {
-                    const int ra = 16 * tt + g;  // and ra + 8
                     float s0, s8, b0 = 0.0f, b8 = 0.0f;
                     if constexpr (FMT == QM_AFFINE) {
-                        // row ra, group gi; row rb = ra + 8 lies 8 rows of scale_pitch bytes on
-                        const uint32_t sa = st + p.off_scales + ra * p.scale_pitch + soff + 2 * gi;
-                        const uint32_t ba = sa + (p.off_biases - p.off_scales);
-                        const uint32_t r8 = 8 * p.scale_pitch;
-                        s0 = sval<SDT>(lds_u16(sa));
-                        s8 = sval<SDT>(lds_u16(sa + r8));
-                        b0 = sval<SDT>(lds_u16(ba));
-                        b8 = sval<SDT>(lds_u16(ba + r8));
+                        s0 = sval<SDT>(raw[tt][0]);
+                        s8 = sval<SDT>(raw[tt][1]);
+                        b0 = sval<SDT>(raw[tt][2]);
+                        b8 = sval<SDT>(raw[tt][3]);
                     } else if constexpr (FMT == QM_Q8_0) {
-                        const uint32_t da = rows_[2 * tt].at(34 * gi);
-                        s0 = f16_bits_to_f32(lds_u16(da));
-                        s8 = f16_bits_to_f32(lds_u16(da + (rows_[2 * tt + 1].line - rows_[2 * tt].line)));
+                        s0 = f16_bits_to_f32(raw[tt][0]);
+                        s8 = f16_bits_to_f32(raw[tt][1]);
                     } else {
-                        const uint32_t sa = st + p.off_scales + ra * p.scale_pitch + soff + gi;
-                        s0 = e8m0_to_f32(lds_u8(sa));
-                        s8 = e8m0_to_f32(lds_u8(sa + 8 * p.scale_pitch));
+                        e8m0x2_to_f32(raw[tt][0] | (raw[tt][1] << 8), s0, s8);
                     }
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
@@ -737,16 +755,21 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
             int gi = gb;
             #pragma unroll 1
             for (; gi + 1 < gend; gi += 2) {
+                uint32_t raw0[2][4], raw1[2][4];
+                ep_load(gi, raw0);
+                ep_load(gi + 1, raw1);
                 float acc0[2][NT][4], acc1[2][NT][4];
                 do_group(gi, acc0);
                 do_group(gi + 1, acc1);
-                epilogue(gi, acc0);
-                epilogue(gi + 1, acc1);
+                epilogue(gi, acc0, raw0);
+                epilogue(gi + 1, acc1, raw1);
             }
             if (gi < gend) {
+                uint32_t raw0[2][4];
+                ep_load(gi, raw0);
                 float acc0[2][NT][4];
                 do_group(gi, acc0);
-                epilogue(gi, acc0);
+                epilogue(gi, acc0, raw0);
             }
             __syncwarp();
             if (lane == 0 && live) mbar_arrive(bar_empty0 + 8 * slot);

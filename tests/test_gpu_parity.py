@@ -199,6 +199,32 @@ def test_apply_activation_range():
         _check_apply(w, x, f"sigma={sigma}")
 
 
+@pytest.mark.parametrize("M", [1, 8, 16])
+def test_apply_mxfp4_scale_range(M):
+    # e8m0 scales over the range a product stays finite in: row r < 201 has
+    # every group at scale byte r (from 2^-127, below float32's normal range,
+    # up to 2^73), the rows after it mix them; three rows hold one group at
+    # 255, which makes every value of the group NaN and so the row's outputs
+    g = synth.rng(650 + M)
+    n, k = 256, 512
+    w = synth.mxfp4_weight(g, n, k)
+    sc = np.empty((n, k // 32), np.uint8)
+    sc[:201] = np.arange(201, dtype=np.uint8)[:, None]
+    sc[201:] = g.integers(0, 201, size=(n - 201, k // 32))
+    nanrows = [7, 150, 230]
+    for r, grp in zip(nanrows, (0, 9, 15)):
+        sc[r, grp] = 255
+    w["scales"] = sc
+    x = synth.activations(g, M, k)
+    ow = to_oracle(w)
+    got = bf16_to_f64(_host(qm.apply(qm.QWeight.from_arrays(w), _dev_bf16(x))))
+    ref = oracle.apply(ow, x)
+    assert np.all(np.isnan(ref[:, nanrows])) and np.all(np.isnan(got[:, nanrows]))
+    keep = np.setdiff1d(np.arange(n), nanrows)
+    xn = np.linalg.norm(oracle.decode_array(x, oracle.BF16), axis=1)
+    check_product(got[:, keep], ref[:, keep], row_norms(ow)[keep], xn, k, f"mxfp4 scales M={M}")
+
+
 def test_apply_deterministic():
     g = synth.rng(700)
     w = _make("q8_0", g, 256, 4096)
