@@ -337,7 +337,8 @@ def run_experts(args, rank, world):
         peak = peaks.get("hbm_gbs", 6800.0)
         value, unit, metric = wbytes * world / t_step / 1e9, "GB/s", EXPERTS_GBS
         roof = {"bound": "hbm", "achieved": round(wbytes / t_step / 1e9, 2), "peak": peak, "unit": "GB/s",
-                "frac": round(wbytes / t_step / 1e9 / peak, 4), "traffic": None,
+                "frac": round(wbytes / t_step / 1e9 / peak, 4), "traffic": traffic("experts_gemv", T == 64)[0],
+                "traffic_source": traffic("experts_gemv", T == 64)[1],
                 "kernel": "grouped gemv_kernel<MXFP4> with routing in the step time",
                 "peak_source": "measured" if "hbm_gbs" in peaks else "fallback"}
     return {
@@ -600,9 +601,10 @@ def detail_measurements(args, dev, stream):
 # (the profiles/ summary named beside each); the commit is the kernel version measured.
 # A kernel changed after its capture reports null until it is captured again.
 TRAFFIC = {
-    "decode": (1.831e6, "d17444d", "profiles/gemv_affine4_qwen3_decode_step.md"),
-    "experts_gemm": (539.9e6, "d17444d", "profiles/gemm_mxfp4_experts_t4096.md"),
-    "dequant": (337.4e6, "d17444d", "profiles/take_dequant_affine4_table.md"),
+    "decode": (1.828e6, "6d4178e", "profiles/gemv_affine4_qwen3_decode_step.md"),
+    "experts_gemm": (539.3e6, "5f65fc6", "profiles/gemm_mxfp4_experts_t4096.md"),
+    "experts_gemv": (287.3e6, "6d4178e", "profiles/gemv_mxfp4_experts_t64.md"),
+    "dequant": (337.4e6, "6d4178e", "profiles/take_dequant_affine4_table.md"),
 }
 
 
