@@ -69,6 +69,8 @@ def library_path() -> str:
 def load_library():
     """Loads libqm.so (built by packed_qmatmul_gb300/build.py); raises if absent."""
     global _lib
+    if _lib is not None:
+        return _lib
     with _lock:
         if _lib is not None:
             return _lib
@@ -127,8 +129,15 @@ class QWeight:
     """A packed weight: format, logical shape [..., n, k] and device parts.
 
     Parts are device tensors whose bytes are the format's (any integer dtype of
-    the right byte size; uint32 codes may be held as int32).
+    the right byte size; uint32 codes may be held as int32). The descriptor
+    passed to the library is built once and rebuilt when a field is assigned;
+    parts are read through their tensors' addresses at that time.
     """
+
+    def __setattr__(self, name, value):
+        object.__setattr__(self, name, value)
+        if name != "_cref":
+            object.__setattr__(self, "_cref", None)
 
     def __init__(self, fmt, shape: Sequence[int], codes: torch.Tensor,
                  scales: Optional[torch.Tensor] = None, biases: Optional[torch.Tensor] = None,
@@ -158,6 +167,14 @@ class QWeight:
         return cls(d["format"], d["shape"], dev(d["codes"]), dev(d.get("scales")),
                    dev(d.get("biases")), bits=d.get("bits", 0), group_size=d.get("group_size", 0),
                    scale_dtype=sdt, flags=flags)
+
+    def _ref(self):
+        """ctypes reference to the descriptor (cached)."""
+        ref = self._cref
+        if ref is None:
+            ref = ctypes.byref(self._c())
+            object.__setattr__(self, "_cref", ref)
+        return ref
 
     def _c(self) -> _CWeight:
         w = _CWeight()
@@ -191,13 +208,13 @@ def qm_last_error() -> str:
 
 
 def qm_dequant(w: QWeight, out: torch.Tensor, stream=None) -> None:
-    _check(load_library().qm_dequant(ctypes.byref(w._c()), _DTYPES[out.dtype], _ptr(out),
+    _check(load_library().qm_dequant(w._ref(), _DTYPES[out.dtype], _ptr(out),
                                      _stream(stream)))
 
 
 def qm_apply(w: QWeight, x: torch.Tensor, y: torch.Tensor, stream=None) -> None:
     M = x.shape[0] if x.dim() == 2 else 1
-    _check(load_library().qm_apply(ctypes.byref(w._c()), _ptr(x), M, _DTYPES[x.dtype], _ptr(y),
+    _check(load_library().qm_apply(w._ref(), _ptr(x), M, _DTYPES[x.dtype], _ptr(y),
                                    _stream(stream)))
 
 
@@ -205,13 +222,13 @@ def qm_take(w: QWeight, axis: int, ids: torch.Tensor, out_codes=None, out_scales
             out_biases=None, out_dense: Optional[torch.Tensor] = None, stream=None) -> None:
     id_type = QM_I64 if ids.dtype == torch.int64 else QM_I32
     out_dtype = _DTYPES[out_dense.dtype] if out_dense is not None else QM_F32
-    _check(load_library().qm_take(ctypes.byref(w._c()), axis, _ptr(ids), id_type, ids.numel(),
+    _check(load_library().qm_take(w._ref(), axis, _ptr(ids), id_type, ids.numel(),
                                   _ptr(out_codes), _ptr(out_scales), _ptr(out_biases), out_dtype,
                                   _ptr(out_dense), _stream(stream)))
 
 
 def qm_apply_experts_workspace(w: QWeight, T: int, topk: int) -> int:
-    return load_library().qm_apply_experts_workspace(ctypes.byref(w._c()), T, topk)
+    return load_library().qm_apply_experts_workspace(w._ref(), T, topk)
 
 
 def qm_experts_route_workspace(P: int, E: int) -> int:
@@ -223,7 +240,7 @@ def qm_apply_experts(w: QWeight, ids: torch.Tensor, x: torch.Tensor, y: torch.Te
     T, topk = ids.shape
     id_type = QM_I64 if ids.dtype == torch.int64 else QM_I32
     _check(load_library().qm_apply_experts(
-        ctypes.byref(w._c()), _ptr(ids), id_type, T, topk, _ptr(x), x.shape[0], _DTYPES[x.dtype],
+        w._ref(), _ptr(ids), id_type, T, topk, _ptr(x), x.shape[0], _DTYPES[x.dtype],
         _ptr(y), _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
@@ -233,7 +250,7 @@ def qm_apply_experts_static(w: QWeight, ids: torch.Tensor, x: torch.Tensor, y: t
     T, topk = ids.shape
     id_type = QM_I64 if ids.dtype == torch.int64 else QM_I32
     _check(load_library().qm_apply_experts_static(
-        ctypes.byref(w._c()), _ptr(ids), id_type, T, topk, _ptr(x), x.shape[0], _DTYPES[x.dtype],
+        w._ref(), _ptr(ids), id_type, T, topk, _ptr(x), x.shape[0], _DTYPES[x.dtype],
         _ptr(y), _stream(stream)))
 
 

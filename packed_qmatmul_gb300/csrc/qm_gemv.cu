@@ -36,7 +36,10 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
+#include <cstring>
+#include <unordered_map>
 
 #include "qm_device.cuh"
 #include "qm_internal.h"
@@ -1063,12 +1066,19 @@ static Plan make_plan(const WDesc& w, int64_t M, double share = 1.0) {
 template <int FMT, int BITS, int GS, int NTK, int SDT, int CW>
 static cudaError_t launch_k(const Plan& pl, cudaStream_t st) {
     auto kern = gemv_kernel<FMT, BITS, GS, NTK, SDT, CW>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(pl.smem));
+    // the kernel's attributes, once per device: the most dynamic shared memory
+    // any plan may ask for, and clusters past the portable size
+    static std::atomic<uint64_t> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (pl.S > 1) {
+    const uint64_t bit = dev < 64 ? (uint64_t(1) << dev) : 0;
+    if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, max_smem_optin());
+        if (e != cudaSuccess) return e;
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(pl.grid));
@@ -1107,21 +1117,23 @@ static cudaError_t launch_t(const Plan& pl, cudaStream_t st) {
 
 }  // namespace gemv
 
-bool gemv_supported(const WDesc& w, int64_t M) {
-    if (M < 1 || M > 16 || w.ndim != 2) return false;
-    return gemv::make_plan(w, M).ok;
-}
+namespace gemv {
 
-qm_status launch_gemv(const WDesc& w, const void* x, int64_t M, void* y, cudaStream_t st) {
-    using namespace gemv;
-    Plan pl = make_plan(w, M);
-    if (!pl.ok) return fail(QM_ENOTSUP, "w: no decode plan for this shape");
-    Params& p = pl.p;
+// A plan with the weight's fields and tensor maps filled in: everything of a
+// launch that depends only on the weight descriptor, M and the device.
+struct Prepared {
+    Plan pl;
+    bool maps = false;  // the driver encoded the tensor maps (else the plain kernel runs)
+};
+
+static void prepare(const WDesc& w, int64_t M, Prepared* out) {
+    out->pl = make_plan(w, M);
+    out->maps = false;
+    if (!out->pl.ok) return;
+    Params& p = out->pl.p;
     p.codes = w.codes;
     p.scales = w.scales;
     p.biases = w.biases;
-    p.x = static_cast<const uint16_t*>(x);
-    p.y = static_cast<uint16_t*>(y);
     p.n = w.n;
     p.k = w.k;
     p.M = static_cast<int>(M);
@@ -1137,10 +1149,84 @@ qm_status launch_gemv(const WDesc& w, const void* x, int64_t M, void* y, cudaStr
             maps = make_tmap_2d(&p.tm_biases, w.biases, w.scale_row_bytes, w.n, w.scale_row_bytes, p.scale_seg,
                                 kRows, false);
     }
-    if (!maps) {  // the driver refused a descriptor for this shape: the plain kernel
+    out->maps = maps;
+}
+
+// What a prepared plan depends on, with no padding bytes (compared bytewise).
+struct PlanKey {
+    const void* codes;
+    const void* scales;
+    const void* biases;
+    int64_t n, k, code_row_bytes, scale_row_bytes;
+    int32_t fmt, bits, gs, sdt, M, is_static, dev, unused;
+};
+static_assert(sizeof(PlanKey) == 3 * 8 + 4 * 8 + 8 * 4, "PlanKey has padding");
+
+struct PlanKeyHash {
+    size_t operator()(const PlanKey& k) const {
+        uint64_t h = 1469598103934665603ull;  // FNV-1a over the key's bytes
+        const unsigned char* b = reinterpret_cast<const unsigned char*>(&k);
+        for (size_t i = 0; i < sizeof k; ++i) h = (h ^ b[i]) * 1099511628211ull;
+        return static_cast<size_t>(h);
+    }
+};
+struct PlanKeyEq {
+    bool operator()(const PlanKey& a, const PlanKey& b) const { return std::memcmp(&a, &b, sizeof a) == 0; }
+};
+
+// Prepared plans, memoized per calling thread: a decode step calls the same
+// few hundred (weight, M) pairs over and over, and planning plus tensor-map
+// encoding costs microseconds of host time per call. Only host-side launch
+// metadata is kept (at most kMaxPlans entries, then the table starts over);
+// no device memory is held.
+static const Prepared* prepared(const WDesc& w, int64_t M) {
+    PlanKey key;
+    std::memset(&key, 0, sizeof key);
+    key.codes = w.codes;
+    key.scales = w.scales;
+    key.biases = w.biases;
+    key.n = w.n;
+    key.k = w.k;
+    key.code_row_bytes = w.code_row_bytes;
+    key.scale_row_bytes = w.scale_row_bytes;
+    key.fmt = w.fmt;
+    key.bits = w.bits;
+    key.gs = w.gs;
+    key.sdt = w.sdt;
+    key.M = static_cast<int32_t>(M);
+    key.is_static = w.is_static ? 1 : 0;
+    if (cudaGetDevice(&key.dev) != cudaSuccess) return nullptr;
+    constexpr size_t kMaxPlans = 4096;
+    thread_local std::unordered_map<PlanKey, Prepared, PlanKeyHash, PlanKeyEq> table;
+    auto it = table.find(key);
+    if (it != table.end()) return &it->second;
+    if (table.size() >= kMaxPlans) table.clear();
+    Prepared& pr = table[key];
+    prepare(w, M, &pr);
+    return &pr;
+}
+
+}  // namespace gemv
+
+bool gemv_supported(const WDesc& w, int64_t M) {
+    if (M < 1 || M > 16 || w.ndim != 2) return false;
+    const gemv::Prepared* pr = gemv::prepared(w, M);
+    return pr && pr->pl.ok;
+}
+
+qm_status launch_gemv(const WDesc& w, const void* x, int64_t M, void* y, cudaStream_t st) {
+    using namespace gemv;
+    const Prepared* pr = prepared(w, M);
+    if (!pr) return cuda_fail(cudaGetLastError(), "cudaGetDevice");
+    if (!pr->pl.ok) return fail(QM_ENOTSUP, "w: no decode plan for this shape");
+    if (!pr->maps) {  // the driver refused a descriptor for this shape: the plain kernel
         cudaError_t e = launch_apply_simple(w, x, M, y, st);
         return e == cudaSuccess ? QM_OK : cuda_fail(e, "apply launch");
     }
+    Plan pl = pr->pl;
+    Params& p = pl.p;
+    p.x = static_cast<const uint16_t*>(x);
+    p.y = static_cast<uint16_t*>(y);
     const int ntk = M > 8 ? 2 : (M > 1 ? 1 : 0);
     cudaError_t e = cudaErrorInvalidValue;
 #define QM_GEMV_CASE(F, B, G)                                                                  \
