@@ -29,8 +29,11 @@
  * Every part is contiguous, row-major, on the device, with a 16-byte aligned
  * base address. The caller owns every buffer and the stream. Entry points
  * validate on the host, enqueue their kernels on `stream` and return; they
- * allocate no memory, keep no state between calls, hold no decoded copy of a
- * weight, and may be called from several host threads.
+ * allocate no device memory, hold no decoded copy of a weight, and may be
+ * called from several host threads. The only state kept between calls is
+ * host-side launch metadata: each calling thread memoizes the launch plan and
+ * tensor-map descriptors of a (weight descriptor, M, device) it has seen,
+ * which depend on nothing but those (results never depend on it).
  *
  * Errors: QM_EINVAL for a bad argument, with qm_last_error() (thread-local,
  * valid until the next call on the thread) naming the part: "w", "codes",
