@@ -220,8 +220,12 @@ namespace ts {
 constexpr int BW = 128;                // weight rows per CTA
 constexpr int NA = 4;                  // decoded weight stages in TMEM
 constexpr int NXT = 4;                 // activation tiles in flight
-constexpr uint32_t kAcol = 256;        // first TMEM column of the weight stages (32 columns each)
-constexpr uint32_t kCols = 512;        // TMEM columns held: accumulator [0, NTOK), weight stages
+// TMEM columns of a CTA: the accumulator [0, NTOK), then NA weight stages of
+// 32 columns from the next power of two; 128-token tiles hold half the SM's
+// 512 columns, so two CTAs share an SM (one's epilogue and setup overlap the
+// other's main loop)
+constexpr uint32_t acol(int ntok) { return ntok <= 128 ? 128u : 256u; }
+constexpr uint32_t cols(int ntok) { return ntok <= 128 ? 256u : 512u; }
 }  // namespace ts
 
 // Grouped mode, one warp: which expert's rows of x m-tile slot `mt` covers
@@ -266,9 +270,11 @@ static __device__ __noinline__ void tile_lookup(const Params& p, int mt, int bm,
 }
 
 template <int FMT, int BITS, int GS, int NTOK>
-__global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kThreads, NTOK <= 128 ? 2 : 1) gemm_kernel(const __grid_constant__ Params p) {
     using R = Raw<FMT, BITS>;
     using namespace ts;
+    constexpr uint32_t kAcol = acol(NTOK), kCols = cols(NTOK);
+    static_assert(kAcol + 32 * NA <= kCols && NTOK <= kAcol, "TMEM columns");
     constexpr uint32_t kXBytes = NTOK * BK * 2;  // activation tile per k step
     extern __shared__ __align__(1024) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -587,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemm_kernel(const __grid_constant
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, ts::kCols);
+        tmem_dealloc(tmem, kCols);
     }
 }
 
@@ -645,10 +651,11 @@ static cudaError_t launch_t(Params& p, const WDesc& w, const void* x, cudaStream
 
 template <int FMT, int BITS, int GS>
 static cudaError_t launch_bm(Params& p, const WDesc& w, const void* x, cudaStream_t st) {
-    // grouped: 256-token tiles once experts average over 64 positions, so an
-    // expert near the average fills one tile instead of spilling a second one
-    // that decodes its weights again for a few rows
-    const bool wide = p.g_off ? p.M > 64 * std::max<int64_t>(1, p.g_E) : p.M > 128;
+    // grouped: 256-token tiles once experts average over 256 positions; below
+    // that, 128-token tiles (two CTAs to an SM) measured faster even where an
+    // expert spills a second, nearly empty tile (T = 1024 x top-4 over 32
+    // experts: 376 -> 392 TFLOP/s)
+    const bool wide = p.g_off ? p.M > 256 * std::max<int64_t>(1, p.g_E) : p.M > 128;
     return wide ? launch_t<FMT, BITS, GS, 256>(p, w, x, st) : launch_t<FMT, BITS, GS, 128>(p, w, x, st);
 }
 
