@@ -11,7 +11,8 @@
 // Design (one GB300: 152 SMs, HBM3e):
 //  * A CTA is 1 producer warp + 8 consumer warps, two CTAs to an SM where
 //    shared memory allows (so the next launch's CTAs can start beside the
-//    last ones of this launch). The producer streams 32-row stages of the
+//    last ones of this launch), else 1 producer + 16 consumer warps alone on
+//    the SM (large k with several tokens). The producer streams 32-row stages of the
 //    packed weight into shared memory with 2-d TMA boxes (codes, 128B-
 //    swizzled) and bulk copies (scales, biases), completing on mbarriers,
 //    and bulk-copies the activation rows once.
@@ -458,7 +459,7 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
         }
     } else {
         // ------------------------------------------------------------ consumers
-        const int ctid = threadIdx.x;  // 0 .. 511
+        const int ctid = threadIdx.x;  // 0 .. 32 * kWarps - 1
         float* tokscale = reinterpret_cast<float*>(smem + p.off_tokscale);  // [16] 2^-E
         const uint16_t* xs = reinterpret_cast<const uint16_t*>(smem + p.off_xraw);  // [M][krange]
         if (!mbar_wait(bar_x, 0)) {

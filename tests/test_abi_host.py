@@ -143,3 +143,25 @@ def test_workspace_query(lib):
     assert lib.qm_experts_route_workspace(0, 32) == 0
     r = lib.qm_experts_route_workspace(256, 32)
     assert 0 < r <= a and r % 256 == 0
+
+
+def test_descriptor_follows_assigned_parts():
+    # the binding builds the descriptor once and rebuilds it when a field is
+    # assigned: the library must always see the current tensors' addresses
+    import torch
+
+    codes = torch.zeros((16, 32), dtype=torch.int32)
+    scales = torch.zeros((16, 4), dtype=torch.int16)
+    biases = torch.zeros((16, 4), dtype=torch.int16)
+    w = qm.QWeight("affine", (16, 256), codes, scales, biases, bits=4, group_size=64)
+    first = w._ref()
+    assert w._ref() is first  # cached between calls
+    d = first._obj
+    assert (d.codes, d.scales, d.biases) == (codes.data_ptr(), scales.data_ptr(), biases.data_ptr())
+    assert (d.format, d.bits, d.group_size, d.ndim, d.shape[0], d.shape[1]) == (qm.QM_AFFINE, 4, 64, 2, 16, 256)
+    other = torch.zeros_like(codes)
+    w.codes = other
+    d2 = w._ref()._obj
+    assert d2.codes == other.data_ptr() and d2.scales == scales.data_ptr()
+    w.flags = qm.QM_WEIGHT_STATIC
+    assert w._ref()._obj.flags == qm.QM_WEIGHT_STATIC
