@@ -1180,7 +1180,7 @@ struct PlanKeyEq {
 // encoding costs microseconds of host time per call. Only host-side launch
 // metadata is kept (at most kMaxPlans entries, then the table starts over);
 // no device memory is held.
-static const Prepared* prepared(const WDesc& w, int64_t M) {
+static const Prepared* prepared(const WDesc& w, int64_t M, cudaError_t* err = nullptr) {
     PlanKey key;
     std::memset(&key, 0, sizeof key);
     key.codes = w.codes;
@@ -1196,7 +1196,11 @@ static const Prepared* prepared(const WDesc& w, int64_t M) {
     key.sdt = w.sdt;
     key.M = static_cast<int32_t>(M);
     key.is_static = w.is_static ? 1 : 0;
-    if (cudaGetDevice(&key.dev) != cudaSuccess) return nullptr;
+    const cudaError_t e = cudaGetDevice(&key.dev);
+    if (e != cudaSuccess) {
+        if (err) *err = e;
+        return nullptr;
+    }
     constexpr size_t kMaxPlans = 4096;
     thread_local std::unordered_map<PlanKey, Prepared, PlanKeyHash, PlanKeyEq> table;
     auto it = table.find(key);
@@ -1217,8 +1221,9 @@ bool gemv_supported(const WDesc& w, int64_t M) {
 
 qm_status launch_gemv(const WDesc& w, const void* x, int64_t M, void* y, cudaStream_t st) {
     using namespace gemv;
-    const Prepared* pr = prepared(w, M);
-    if (!pr) return cuda_fail(cudaGetLastError(), "cudaGetDevice");
+    cudaError_t err = cudaSuccess;
+    const Prepared* pr = prepared(w, M, &err);
+    if (!pr) return cuda_fail(err, "cudaGetDevice");
     if (!pr->pl.ok) return fail(QM_ENOTSUP, "w: no decode plan for this shape");
     if (!pr->maps) {  // the driver refused a descriptor for this shape: the plain kernel
         cudaError_t e = launch_apply_simple(w, x, M, y, st);
