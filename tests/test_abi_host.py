@@ -165,3 +165,20 @@ def test_descriptor_follows_assigned_parts():
     assert d2.codes == other.data_ptr() and d2.scales == scales.data_ptr()
     w.flags = qm.QM_WEIGHT_STATIC
     assert w._ref()._obj.flags == qm.QM_WEIGHT_STATIC
+
+
+def test_empty_inputs_return_ok_without_work(lib):
+    # nothing to compute: every entry point accepts it before touching a pointer
+    w = _w(shape=(16, 64))
+    assert lib.qm_take(ctypes.byref(w), 0, None, qm.QM_I32, 0, 2048, 2304, 2560, qm.QM_BF16, None, None) == qm.QM_OK
+    assert lib.qm_take(ctypes.byref(w), 0, None, qm.QM_I64, 0, None, None, None, qm.QM_BF16, 4096, None) == qm.QM_OK
+    w3 = _w(shape=(4, 16, 64), ndim=3)
+    for T, topk in ((0, 4), (8, 0)):
+        st = lib.qm_apply_experts(ctypes.byref(w3), None, qm.QM_I32, T, topk, None, T, qm.QM_BF16, None,
+                                  None, 0, None)
+        assert st == qm.QM_OK, (T, topk, lib.qm_last_error())
+    assert lib.qm_apply(ctypes.byref(_w(shape=(0, 64), codes=0, scales=0, biases=0)), 4096, 3, qm.QM_BF16,
+                        8192, None) == qm.QM_OK  # n = 0
+    # a negative count is refused, naming ids
+    st = lib.qm_take(ctypes.byref(w), 0, 4096, qm.QM_I32, -1, 2048, 2304, 2560, qm.QM_BF16, None, None)
+    assert st == qm.QM_EINVAL and lib.qm_last_error().decode().startswith("ids:")
