@@ -9,7 +9,8 @@ The arithmetic lives in ``qm_oracle.c`` (plain C, compiled with gcc, OpenMP
 over output rows). This module builds it on first use and wraps it for NumPy
 arrays. Format and dtype codes here are the oracle's own:
 
-    format: AFFINE = 0 (MLX affine), Q8_0 = 1 (GGUF), MXFP4 = 2 (scales apart)
+    format: AFFINE = 0 (MLX affine), Q8_0 = 1 (GGUF), MXFP4 = 2 (scales apart),
+            MXFP4_BLOCKS = 3 (MXFP4 in GGUF's 17-byte blocks)
     dtype : F32 = 0, BF16 = 1, F16 = 2   (16-bit data is passed as uint16 bits)
 
 Sources, by page title and section:
@@ -26,7 +27,7 @@ import threading
 
 import numpy as np
 
-AFFINE, Q8_0, MXFP4 = 0, 1, 2
+AFFINE, Q8_0, MXFP4, MXFP4_BLOCKS = 0, 1, 2, 3
 F32, BF16, F16 = 0, 1, 2
 
 _HERE = os.path.dirname(os.path.abspath(__file__))

@@ -20,7 +20,8 @@
  *          words, companion .scales/.biases, bf16 scales).
  *
  * Conventions shared with the Python wrapper (oracle/__init__.py) only:
- *   format: 0 = MLX affine, 1 = GGUF Q8_0, 2 = MXFP4 (scales apart)
+ *   format: 0 = MLX affine, 1 = GGUF Q8_0, 2 = MXFP4 (scales apart),
+ *           3 = MXFP4 in GGUF's blocks
  *   dtype : 0 = float32, 1 = bfloat16, 2 = float16
  *   An index array is int32 when its `ids64` flag is 0, int64 otherwise.
  *
@@ -196,6 +197,15 @@ int or_mxfp4_code(const uint8_t* row_bytes, int64_t i)
     return (i % 2 == 0) ? (b & 0xF) : (b >> 4);
 }
 
+/* MXFP4 in GGUF's blocks ([NXQ] "Weights", Mxfp4_blocks.blocks): 17 bytes per
+ * 32 values, the e8m0 scale byte first, then 16 bytes; byte j holds value j
+ * of the block in its low nibble and value j + 16 in its high nibble. */
+static int or_mxfp4_block_code(const uint8_t* block, int t)
+{
+    uint8_t b = block[1 + (t % 16)];
+    return (t < 16) ? (b & 0xF) : (b >> 4);
+}
+
 /* Q8_0 block layout ([NXQ] "Weights", Q8_0.blocks): 34 bytes per 32 values,
  * a little-endian float16 d, then 32 int8 quants. */
 static double or_q8_0_d(const uint8_t* block)
@@ -229,6 +239,13 @@ void or_row_values(int fmt, int bits, int gs, int sdt, int64_t k,
         for (int64_t i = 0; i < k; ++i) {
             const uint8_t* blk = rb + (i / 32) * 34;
             v[i] = (float)(or_q8_0_d(blk) * (double)or_q8_0_q(blk, (int)(i % 32)));
+        }
+    } else if (fmt == 3) {                            /* MXFP4 in GGUF's blocks */
+        const uint8_t* rb = (const uint8_t*)codes + r * (k / 32) * 17;
+        for (int64_t i = 0; i < k; ++i) {
+            const uint8_t* blk = rb + (i / 32) * 17;
+            double x = or_e2m1_to_f64(or_mxfp4_block_code(blk, (int)(i % 32))) * or_e8m0_to_f64(blk[0]);
+            v[i] = (float)x;                          /* exact, or +-inf past float32 */
         }
     } else {                                          /* MXFP4, scales apart */
         const uint8_t* rc = (const uint8_t*)codes + r * (k / 2);

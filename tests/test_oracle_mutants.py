@@ -17,6 +17,10 @@ SRC = os.path.join(ROOT, "oracle", "qm_oracle.c")
 MUTANTS = {
     "mxfp4_nibble_swap": ("return (i % 2 == 0) ? (b & 0xF) : (b >> 4);",
                           "return (i % 2 == 0) ? (b >> 4) : (b & 0xF);"),
+    "mxfp4_blocks_half_swap": ("return (t < 16) ? (b & 0xF) : (b >> 4);",
+                               "return (t < 16) ? (b >> 4) : (b & 0xF);"),
+    "mxfp4_blocks_byte_index": ("uint8_t b = block[1 + (t % 16)];", "uint8_t b = block[1 + (t / 2)];"),
+    "mxfp4_blocks_scale_byte": ("or_e8m0_to_f64(blk[0])", "or_e8m0_to_f64(blk[16])"),
     "affine_bias_dropped": ("v[i] = fmaf((float)c, s, b);", "v[i] = fmaf((float)c, s, 0.0f * b);"),
     "affine_bit_order": ("c |= bit << t;", "c |= bit << (bits - 1 - t);"),
     "affine_group_index": ("r * ng + i / gs, sdt);\n            float b",

@@ -162,8 +162,17 @@ def test_packing_worked_examples():
             w = oracle.Weight(oracle.Q8_0, (1, 32), blk)
             got = oracle.dequant(w, oracle.F32)[0].astype(np.float64)
             assert np.array_equal(got, d * q.astype(np.float64)), line
+        elif f[0] == "mxfp4_blocks":
+            blk = np.frombuffer(bytes.fromhex(f[1] + f[2]), dtype=np.uint8).reshape(1, 17).copy()
+            codes = [int(c) for c in tail.split()]
+            w = oracle.Weight(oracle.MXFP4_BLOCKS, (1, 32), blk)
+            got = oracle.dequant(w, oracle.F32)[0]
+            table = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]  # the page's magnitudes
+            scale = 2.0 ** (int(f[1], 16) - 127)
+            want = [(-1.0 if c & 8 else 1.0) * table[c & 7] * scale for c in codes]
+            assert all(_same(float(a), b) for a, b in zip(got, want)), line
         n += 1
-    assert n >= 15
+    assert n >= 17
 
 
 @pytest.mark.parametrize("bits", [2, 3, 4, 5, 6, 8])
@@ -288,10 +297,53 @@ def test_zero_bytes_decode_to_zero():
          np.zeros((2, 1), np.uint16)),
         (oracle.Q8_0, np.zeros((2, 68), np.uint8), None, None),
         (oracle.MXFP4, np.zeros((2, 32), np.uint8), np.zeros((2, 2), np.uint8), None),
+        (oracle.MXFP4_BLOCKS, np.zeros((2, 34), np.uint8), None, None),
     ):
         k = 64
         w = oracle.Weight(fmt, (2, k), codes, scales, biases, bits=4, group_size=64)
         assert not np.any(oracle.dequant(w, oracle.F32))
+
+
+def _blocks_to_apart(blocks, k):
+    # GGUF's blocks ("Nx_quant", "Weights", Mxfp4_blocks: the scale byte, then
+    # byte j holding value j low and value j + 16 high) to the scales-apart
+    # layout (Mxfp4: value 2i low and 2i + 1 high in byte i), by NumPy indexing
+    rows = blocks.shape[0]
+    b = blocks.reshape(rows, k // 32, 17)
+    scales = b[:, :, 0].copy()
+    body = b[:, :, 1:]
+    codes = np.concatenate([body & 0xF, body >> 4], axis=2).reshape(rows, k)  # value order
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    return packed, scales
+
+
+def test_mxfp4_blocks_transcode_identity():
+    # GGUF's blocks and the scales-apart layout hold the same values; the two
+    # decoders read different byte positions, so a wrong nibble, byte or scale
+    # position in either shows up as a mismatch
+    g = np.random.default_rng(17)
+    rows, k = 64, 256
+    blocks = g.integers(0, 256, size=(rows, k // 32 * 17), dtype=np.int64).astype(np.uint8)
+    b = blocks.reshape(rows, k // 32, 17)
+    b[:, :, 0] = g.integers(100, 140, size=(rows, k // 32))  # finite scales ...
+    b[0, 0, 0], b[1, 3, 0], b[2, 5, 0] = 255, 0, 254         # ... and the edges
+    packed, scales = _blocks_to_apart(blocks, k)
+    wb = oracle.Weight(oracle.MXFP4_BLOCKS, (rows, k), blocks)
+    wa = oracle.Weight(oracle.MXFP4, (rows, k), packed, scales)
+    for dt in (oracle.F32, oracle.BF16, oracle.F16):
+        a, c = oracle.dequant(wb, dt), oracle.dequant(wa, dt)
+        if dt == oracle.F32:
+            nan = np.isnan(a)
+            assert np.array_equal(nan, np.isnan(c)) and nan[0, :32].all() and not nan[0, 32:].any()
+            assert np.array_equal(a[~nan].view(np.uint32), c[~nan].view(np.uint32))
+        else:
+            assert np.array_equal(a, c)
+    x = synth.activations(g, 3, k)
+    with np.errstate(invalid="ignore", over="ignore"):
+        ya, yc = oracle.apply(wb, x), oracle.apply(wa, x)
+    assert np.array_equal(np.isnan(ya), np.isnan(yc))
+    ok = ~np.isnan(ya)
+    assert np.array_equal(ya[ok], yc[ok])
 
 
 def test_q8_0_to_affine_transcode_identity():
