@@ -25,6 +25,13 @@
  *                     bit 3 over magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6);
  *              scales uint8 [..., n, k/32] e8m0: 2^(s-127), s = 255 is NaN.
  *              value = e2m1(code) * 2^(s-127) (float32: infinite past its range).
+ *   QM_MXFP4_BLOCKS  MXFP4 in GGUF's blocks (same page, "Weights",
+ *              Mxfp4_blocks): codes uint8 [..., n, k/32*17]; per 32 values the
+ *              e8m0 scale byte, then 16 bytes, byte j holding value j of the
+ *              block in its low nibble and value j+16 in its high nibble.
+ *              Values as QM_MXFP4. dequant and take decode it in their own
+ *              kernels; apply and apply_experts run the plain per-row kernels
+ *              for it (no tensor-map pipeline yet).
  *
  * Every part is contiguous, row-major, on the device, with a 16-byte aligned
  * base address. The caller owns every buffer and the stream. Entry points
@@ -63,7 +70,7 @@ typedef enum qm_status {
     QM_ENOTSUP = 4   /* a valid combination this library does not implement */
 } qm_status;
 
-typedef enum qm_format { QM_AFFINE = 0, QM_Q8_0 = 1, QM_MXFP4 = 2 } qm_format;
+typedef enum qm_format { QM_AFFINE = 0, QM_Q8_0 = 1, QM_MXFP4 = 2, QM_MXFP4_BLOCKS = 3 } qm_format;
 typedef enum qm_dtype { QM_F32 = 0, QM_BF16 = 1, QM_F16 = 2 } qm_dtype;
 typedef enum qm_itype { QM_I32 = 0, QM_I64 = 1 } qm_itype;
 
@@ -72,13 +79,13 @@ typedef enum qm_itype { QM_I32 = 0, QM_I64 = 1 } qm_itype;
 /* A packed weight: its format, logical shape [..., n, k] and device parts. */
 typedef struct qm_weight {
     int32_t format;      /* qm_format */
-    int32_t bits;        /* QM_AFFINE: 4 or 8. QM_Q8_0: 8 or 0. QM_MXFP4: 4 or 0 */
-    int32_t group_size;  /* QM_AFFINE: 32, 64 or 128. QM_Q8_0, QM_MXFP4: 32 or 0 */
+    int32_t bits;        /* QM_AFFINE: 4 or 8. QM_Q8_0: 8 or 0. QM_MXFP4(_BLOCKS): 4 or 0 */
+    int32_t group_size;  /* QM_AFFINE: 32, 64 or 128. Otherwise 32 or 0 */
     int32_t scale_dtype; /* QM_AFFINE: QM_BF16 or QM_F16. Otherwise ignored */
     int32_t ndim;        /* 2 .. QM_MAX_NDIM */
     int64_t shape[QM_MAX_NDIM]; /* logical shape; shape[ndim-1] = k, a multiple of 32 */
     const void* codes;   /* see the formats above */
-    const void* scales;  /* QM_AFFINE, QM_MXFP4; must be NULL for QM_Q8_0 */
+    const void* scales;  /* QM_AFFINE, QM_MXFP4; must be NULL otherwise */
     const void* biases;  /* QM_AFFINE only; must be NULL otherwise */
     uint32_t flags;      /* QM_WEIGHT_* bits; 0 for none */
 } qm_weight;

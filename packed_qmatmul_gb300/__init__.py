@@ -20,7 +20,7 @@ from typing import Optional, Sequence
 import torch
 
 __all__ = [
-    "QM_AFFINE", "QM_Q8_0", "QM_MXFP4", "QM_WEIGHT_STATIC", "QM_F32", "QM_BF16", "QM_F16", "QM_I32", "QM_I64",
+    "QM_AFFINE", "QM_Q8_0", "QM_MXFP4", "QM_MXFP4_BLOCKS", "QM_WEIGHT_STATIC", "QM_F32", "QM_BF16", "QM_F16", "QM_I32", "QM_I64",
     "QMError", "QWeight", "library_path", "load_library",
     "qm_dequant", "qm_apply", "qm_take", "qm_apply_experts", "qm_apply_experts_workspace",
     "qm_experts_route_workspace",
@@ -29,7 +29,7 @@ __all__ = [
 ]
 
 QM_OK, QM_EINVAL, QM_ECUDA, QM_ETIMEOUT, QM_ENOTSUP = 0, 1, 2, 3, 4
-QM_AFFINE, QM_Q8_0, QM_MXFP4 = 0, 1, 2
+QM_AFFINE, QM_Q8_0, QM_MXFP4, QM_MXFP4_BLOCKS = 0, 1, 2, 3
 QM_F32, QM_BF16, QM_F16 = 0, 1, 2
 QM_I32, QM_I64 = 0, 1
 QM_WEIGHT_STATIC = 1
@@ -37,7 +37,7 @@ QM_MAX_NDIM = 4
 
 _STATUS = {QM_EINVAL: "QM_EINVAL", QM_ECUDA: "QM_ECUDA", QM_ETIMEOUT: "QM_ETIMEOUT",
            QM_ENOTSUP: "QM_ENOTSUP"}
-_FORMATS = {"affine": QM_AFFINE, "q8_0": QM_Q8_0, "mxfp4": QM_MXFP4}
+_FORMATS = {"affine": QM_AFFINE, "q8_0": QM_Q8_0, "mxfp4": QM_MXFP4, "mxfp4_blocks": QM_MXFP4_BLOCKS}
 _DTYPES = {torch.float32: QM_F32, torch.bfloat16: QM_BF16, torch.float16: QM_F16}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -195,6 +195,8 @@ class QWeight:
             return (tuple(lead) + (cb,), tuple(lead) + (sb,), tuple(lead) + (sb,))
         if self.format == QM_Q8_0:
             return (tuple(lead) + (k // 32 * 34,), None, None)
+        if self.format == QM_MXFP4_BLOCKS:
+            return (tuple(lead) + (k // 32 * 17,), None, None)
         return (tuple(lead) + (k // 2,), tuple(lead) + (k // 32,), None)
 
 

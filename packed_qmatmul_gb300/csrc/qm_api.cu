@@ -74,7 +74,7 @@ int max_smem_optin() {
 
 qm_status validate_weight(const qm_weight* w, WDesc* d) {
     if (!w) return fail(QM_EINVAL, "w: NULL weight descriptor");
-    if (w->format != QM_AFFINE && w->format != QM_Q8_0 && w->format != QM_MXFP4)
+    if (w->format != QM_AFFINE && w->format != QM_Q8_0 && w->format != QM_MXFP4 && w->format != QM_MXFP4_BLOCKS)
         return fail(QM_EINVAL, "w: unknown format " + std::to_string(w->format));
     if (w->ndim < 2 || w->ndim > QM_MAX_NDIM)
         return fail(QM_EINVAL, "w: ndim must be 2.." + std::to_string(QM_MAX_NDIM));
@@ -117,6 +117,15 @@ qm_status validate_weight(const qm_weight* w, WDesc* d) {
         d->bits = 8;
         d->gs = 32;
         d->code_row_bytes = k / 32 * 34;
+    } else if (w->format == QM_MXFP4_BLOCKS) {
+        if (w->bits != 0 && w->bits != 4) return fail(QM_EINVAL, "w: MXFP4 bits must be 4 (or 0)");
+        if (w->group_size != 0 && w->group_size != 32)
+            return fail(QM_EINVAL, "w: MXFP4 group_size must be 32 (or 0)");
+        if (w->scales) return fail(QM_EINVAL, "scales: MXFP4 blocks keep their scales in the blocks; pass NULL");
+        if (w->biases) return fail(QM_EINVAL, "biases: MXFP4 has no biases; pass NULL");
+        d->bits = 4;
+        d->gs = 32;
+        d->code_row_bytes = k / 32 * 17;
     } else {
         if (w->bits != 0 && w->bits != 4) return fail(QM_EINVAL, "w: MXFP4 bits must be 4 (or 0)");
         if (w->group_size != 0 && w->group_size != 32)

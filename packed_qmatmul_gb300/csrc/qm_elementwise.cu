@@ -83,6 +83,26 @@ QM_DEV void decode_unit(const DecodeArgs& a, int64_t r, int64_t u, float (&v)[32
             v[2 * i] = d * static_cast<float>(static_cast<int8_t>(two & 0xFF));
             v[2 * i + 1] = d * static_cast<float>(static_cast<int8_t>(two >> 8));
         }
+    } else if constexpr (FMT == QM_MXFP4_BLOCKS) {
+        // GGUF's 17-byte block: the e8m0 scale byte, then byte j holding value j
+        // (low nibble) and value j + 16 (high nibble); blocks are byte-aligned
+        const uint8_t* blk = a.codes + r * a.code_row_bytes + u * 17;
+        const float sc = e8m0_to_f32(__ldg(blk));
+#pragma unroll
+        for (int j = 0; j < 16; j += 4) {
+            const uint32_t w = static_cast<uint32_t>(__ldg(blk + 1 + j)) |
+                               (static_cast<uint32_t>(__ldg(blk + 2 + j)) << 8) |
+                               (static_cast<uint32_t>(__ldg(blk + 3 + j)) << 16) |
+                               (static_cast<uint32_t>(__ldg(blk + 4 + j)) << 24);
+            uint32_t h2[4];
+            e2m1x8_to_f16x2(w, h2);  // byte i -> (its low nibble, its high nibble)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&h2[i]));
+                v[j + i] = f.x * sc;
+                v[j + i + 16] = f.y * sc;
+            }
+        }
     } else {  // MXFP4: 16 bytes of codes (value 2i low nibble, 2i+1 high), one e8m0 scale
         const uint4 q = __ldg(reinterpret_cast<const uint4*>(a.codes + r * a.code_row_bytes + u * 16));
         const float sc = e8m0_to_f32(__ldg(a.scales + r * a.scale_row_bytes + u));
@@ -188,6 +208,7 @@ cudaError_t launch_decode_rows(const WDesc& w, int64_t out_rows, Map map, int ou
     QM_DECODE_OUTS(QM_AFFINE, 8)
     QM_DECODE_OUTS(QM_Q8_0, 8)
     QM_DECODE_OUTS(QM_MXFP4, 4)
+    QM_DECODE_OUTS(QM_MXFP4_BLOCKS, 4)
 #undef QM_DECODE_OUTS
 #undef QM_DECODE_CASE
     return cudaErrorInvalidValue;
@@ -318,6 +339,8 @@ cudaError_t launch_apply_simple(const WDesc& w, const void* x, int64_t M, void* 
         apply_simple_kernel<QM_AFFINE, 8><<<static_cast<unsigned>(blocks), 256, 0, st>>>(a, w.n, xb, M, yb);
     else if (w.fmt == QM_Q8_0)
         apply_simple_kernel<QM_Q8_0, 8><<<static_cast<unsigned>(blocks), 256, 0, st>>>(a, w.n, xb, M, yb);
+    else if (w.fmt == QM_MXFP4_BLOCKS)
+        apply_simple_kernel<QM_MXFP4_BLOCKS, 4><<<static_cast<unsigned>(blocks), 256, 0, st>>>(a, w.n, xb, M, yb);
     else
         apply_simple_kernel<QM_MXFP4, 4><<<static_cast<unsigned>(blocks), 256, 0, st>>>(a, w.n, xb, M, yb);
     return cudaGetLastError();

@@ -215,6 +215,17 @@ QM_DEV float value_at(const ExpArgs& a, int64_t r, int64_t i) {
         const uint8_t* blk = a.codes + r * a.code_row_bytes + (i / 32) * 34;
         const float d = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(blk));
         return d * static_cast<float>(static_cast<int8_t>(blk[2 + i % 32]));
+    } else if constexpr (FMT == QM_MXFP4_BLOCKS) {
+        // GGUF's 17-byte block: the scale byte, then byte j holding value j
+        // (low nibble) and value j + 16 (high nibble)
+        const uint8_t* blk = a.codes + r * a.code_row_bytes + (i / 32) * 17;
+        const int t = static_cast<int>(i % 32);
+        const uint8_t b = blk[1 + (t & 15)];
+        const uint32_t c = t < 16 ? (b & 15) : (b >> 4);
+        uint32_t f2[4];
+        e2m1x8_to_f16x2(c, f2);  // byte 0 holds the code in its low nibble
+        const float v = __half2float(__ushort_as_half(static_cast<unsigned short>(f2[0] & 0xFFFF)));
+        return v * e8m0_to_f32(blk[0]);
     } else {
         const uint8_t b = a.codes[r * a.code_row_bytes + i / 2];
         const uint32_t c = (i & 1) ? (b >> 4) : (b & 15);
@@ -332,6 +343,7 @@ qm_status launch_experts(const WDesc& w, const void* ids, int id64, int64_t T, i
     if (w.fmt == QM_AFFINE && w.bits == 4) QM_EXP_CASE(QM_AFFINE, 4);
     else if (w.fmt == QM_AFFINE) QM_EXP_CASE(QM_AFFINE, 8);
     else if (w.fmt == QM_Q8_0) QM_EXP_CASE(QM_Q8_0, 8);
+    else if (w.fmt == QM_MXFP4_BLOCKS) QM_EXP_CASE(QM_MXFP4_BLOCKS, 4);
     else QM_EXP_CASE(QM_MXFP4, 4);
 #undef QM_EXP_CASE
     e = cudaGetLastError();

@@ -674,7 +674,7 @@ static cudaError_t dispatch(Params& p, const WDesc& w, const void* x, cudaStream
 }  // namespace gemm
 
 bool gemm_supported(const WDesc& w, int64_t M) {
-    if (M < 1 || w.ndim != 2 || w.n < 1 || w.k < 64) return false;
+    if (M < 1 || w.ndim != 2 || w.n < 1 || w.k < 64 || !pipelined_format(w.fmt)) return false;
     if (w.code_row_bytes % 16) return false;  // TMA row stride
     if (M > (int64_t(1) << 31) || w.n > (int64_t(1) << 31)) return false;
     return true;
@@ -702,7 +702,7 @@ qm_status launch_gemm(const WDesc& w, const void* x, int64_t M, void* y, cudaStr
 }
 
 bool gemm_grouped_supported(const WDesc& w, int64_t P) {
-    if (w.ndim != 3 || w.shape[0] < 1 || w.n < 1 || w.k < 64 || P < 1) return false;
+    if (w.ndim != 3 || w.shape[0] < 1 || w.n < 1 || w.k < 64 || P < 1 || !pipelined_format(w.fmt)) return false;
     if (w.code_row_bytes % 16 || (w.k * 2) % 16) return false;  // TMA row strides
     if (P >= (int64_t(1) << 31) || w.rows >= (int64_t(1) << 31)) return false;
     return true;

@@ -1214,7 +1214,7 @@ static const Prepared* prepared(const WDesc& w, int64_t M, cudaError_t* err = nu
 }  // namespace gemv
 
 bool gemv_supported(const WDesc& w, int64_t M) {
-    if (M < 1 || M > 16 || w.ndim != 2) return false;
+    if (M < 1 || M > 16 || w.ndim != 2 || !pipelined_format(w.fmt)) return false;
     const gemv::Prepared* pr = gemv::prepared(w, M);
     return pr && pr->pl.ok;
 }
@@ -1266,7 +1266,7 @@ static int grouped_q(int64_t P, int64_t E) { return P <= 8 * E ? 8 : 16; }
 
 static bool grouped_plan(const WDesc& w, int64_t P, Plan* out, int64_t* slots) {
     const int64_t E = w.shape[0];
-    if (w.ndim != 3 || E < 1 || P < 1 || E * w.n >= (int64_t(1) << 31)) return false;
+    if (w.ndim != 3 || E < 1 || P < 1 || E * w.n >= (int64_t(1) << 31) || !pipelined_format(w.fmt)) return false;
     if ((w.n * w.scale_row_bytes) % 16) return false;  // each expert's scales start 16-byte aligned
     const int Q = grouped_q(P, E);
     *slots = std::min<int64_t>(P, P / Q + E);  // sum over experts of ceil(count / Q) is below P/Q + E

@@ -52,6 +52,10 @@ int num_sms();
 // Opt-in shared memory per block on the current device (cached per device).
 int max_smem_optin();
 
+// Formats the tensor-map pipelines (decode GEMV, tensor-core GEMM) decode;
+// the others take the plain kernels for products.
+inline bool pipelined_format(int fmt) { return fmt == QM_AFFINE || fmt == QM_Q8_0 || fmt == QM_MXFP4; }
+
 // ------------------------------------------------------------ launchers
 // Each returns the CUDA error of its launch (cudaSuccess when nothing ran).
 cudaError_t launch_dequant(const WDesc& w, int out_dtype, void* out, cudaStream_t st);

@@ -15,13 +15,15 @@ patterns) plus the metadata a caller needs to describe the weight:
   [-127, 127].
 * MXFP4: ``codes`` uint8 [..., n, k/2] uniform bytes, ``scales`` uint8
   [..., n, k/32] e8m0 bytes uniform in [lo, hi].
+* MXFP4 in GGUF's blocks: ``codes`` uint8 [..., n, k/32*17], each 17-byte
+  block an e8m0 byte uniform in [lo, hi] then 16 uniform bytes.
 """
 from __future__ import annotations
 
 import numpy as np
 import torch
 
-AFFINE, Q8_0, MXFP4 = "affine", "q8_0", "mxfp4"
+AFFINE, Q8_0, MXFP4, MXFP4_BLOCKS = "affine", "q8_0", "mxfp4", "mxfp4_blocks"
 
 
 def rng(seed: int) -> np.random.Generator:
@@ -92,6 +94,16 @@ def mxfp4_weight(g, n, k, lead=(), scale_lo=118, scale_hi=126):
     scales = g.integers(scale_lo, scale_hi + 1, size=shape + (k // 32,), dtype=np.int64)
     return dict(format=MXFP4, shape=shape + (k,), bits=4, group_size=32, scale_dtype=None,
                 codes=codes, scales=scales.astype(np.uint8), biases=None)
+
+
+def mxfp4_blocks_weight(g, n, k, lead=(), scale_lo=118, scale_hi=126):
+    """MXFP4 weight [*lead, n, k] in GGUF's 17-byte blocks."""
+    assert k % 32 == 0
+    shape = tuple(lead) + (n,)
+    blocks = g.integers(0, 256, size=shape + (k // 32, 17), dtype=np.int64)
+    blocks[..., 0] = g.integers(scale_lo, scale_hi + 1, size=shape + (k // 32,), dtype=np.int64)
+    return dict(format=MXFP4_BLOCKS, shape=shape + (k,), bits=4, group_size=32, scale_dtype=None,
+                codes=blocks.astype(np.uint8).reshape(shape + (k // 32 * 17,)), scales=None, biases=None)
 
 
 def activations(g, M, k, sigma=1.0):

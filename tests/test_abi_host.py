@@ -182,3 +182,22 @@ def test_empty_inputs_return_ok_without_work(lib):
     # a negative count is refused, naming ids
     st = lib.qm_take(ctypes.byref(w), 0, 4096, qm.QM_I32, -1, 2048, 2304, 2560, qm.QM_BF16, None, None)
     assert st == qm.QM_EINVAL and lib.qm_last_error().decode().startswith("ids:")
+
+
+def test_mxfp4_blocks_validation(lib):
+    # MXFP4 in GGUF's blocks: one part, [.., n, k/32*17]; scales and biases refused
+    def err(**kw):
+        base = dict(fmt=qm.QM_MXFP4_BLOCKS, bits=0, gs=0, shape=(16, 64), scales=0, biases=0)
+        base.update(kw)
+        st, msg = _dequant_err(lib, _w(**base))
+        return st, msg
+
+    for kw, part in ((dict(scales=512), "scales"), (dict(biases=768), "biases"), (dict(bits=8), "w"),
+                     (dict(gs=64), "w"), (dict(shape=(16, 48)), "codes"), (dict(codes=8), "codes")):
+        st, msg = err(**kw)
+        assert st == qm.QM_EINVAL and msg.startswith(part + ":"), (kw, msg)
+    w3 = _w(fmt=qm.QM_MXFP4_BLOCKS, bits=0, gs=0, shape=(32, 5760, 2880), ndim=3, scales=0, biases=0)
+    ws = lib.qm_apply_experts_workspace(ctypes.byref(w3), 64, 4)
+    assert 0 < ws == lib.qm_experts_route_workspace(256, 32)  # plain kernels: routing tables only
+    qw = qm.QWeight("mxfp4_blocks", (3, 16, 64), None)
+    assert qw.part_shapes((3, 5)) == ((3, 5, 34), None, None)

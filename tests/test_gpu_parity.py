@@ -517,3 +517,56 @@ def test_apply_prefill_q8_0_full_shape_sampled():
     from wutil import bf16_half_ulp
     assert np.all(np.abs(got - ref) <= bound + bf16_half_ulp(got)), np.max(np.abs(got - ref) / bound)
     assert np.linalg.norm(got - ref) <= 4e-3 * np.linalg.norm(ref)
+
+
+# ---------------------------------------------------------------- MXFP4 in GGUF's blocks
+# "Nx_quant", "Weights", Mxfp4_blocks: per 32 values the scale byte, then byte j
+# holding value j low and value j + 16 high. Dequant and take decode it in their
+# own kernels; products run the plain per-row kernels.
+def _blocks(g, n, k, lead=()):
+    w = synth.mxfp4_blocks_weight(g, n, k, lead=lead)
+    b = w["codes"].reshape(-1, 17)
+    b[0, 0], b[1, 0], b[2, 0], b[3, 0] = 255, 0, 254, 1  # NaN, 2^-127, 2^127, 2^-126 groups
+    return w
+
+
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16, torch.float16])
+def test_mxfp4_blocks_dequant_bit_exact(dt):
+    g = synth.rng(700)
+    for n, k, lead in ((37, 256, ()), (5, 1024, (3,)), (1, 128, (2, 2))):
+        w = _blocks(g, n, k, lead)
+        got = _host(qm.dequant(qm.QWeight.from_arrays(w), dt))
+        want = oracle.dequant(to_oracle(w), ODT[dt])
+        assert _bits_equal(got, want, dt), (n, k, lead)
+
+
+@pytest.mark.parametrize("id64", [False, True])
+def test_mxfp4_blocks_take(id64):
+    g = synth.rng(701)
+    for lead, axis in (((), 0), ((3,), 0), ((3,), 1)):
+        w = _blocks(g, 24, 256, lead)
+        ow = to_oracle(w)
+        L = ow.shape[axis]
+        ids = np.array([L - 1, 0, -1, L, 2, 2, 1], dtype=np.int64 if id64 else np.int32)
+        tw, dense = qm.take(qm.QWeight.from_arrays(w), axis, torch.from_numpy(ids).cuda(),
+                            dense_dtype=torch.bfloat16)
+        ot = oracle.take(ow, axis, ids)
+        assert tw.scales is None and tw.biases is None
+        assert np.array_equal(_host(tw.codes).view(np.uint8).reshape(-1), ot.codes.reshape(-1)), (lead, axis)
+        assert _bits_equal(_host(dense), oracle.dequant(ot, oracle.BF16), torch.bfloat16), (lead, axis)
+
+
+@pytest.mark.parametrize("M", [1, 8, 33])
+def test_mxfp4_blocks_apply(M):
+    g = synth.rng(702 + M)
+    w = synth.mxfp4_blocks_weight(g, 80, 512)
+    _check_apply(w, synth.activations(g, M, 512), f"mxfp4 blocks M={M}")
+
+
+def test_mxfp4_blocks_apply_experts():
+    g = synth.rng(705)
+    w = synth.mxfp4_blocks_weight(g, 48, 256, lead=(4,))
+    ids = synth.expert_ids(g, 16, 2, 4).astype(np.int32)
+    ids[3, 1] = 4   # out of range: zeros
+    ids[7, 0] = -1
+    _check_experts(w, ids, synth.activations(g, 16, 256), "mxfp4 blocks experts")

@@ -8,7 +8,7 @@ import numpy as np
 
 import oracle
 
-FMT = {"affine": oracle.AFFINE, "q8_0": oracle.Q8_0, "mxfp4": oracle.MXFP4}
+FMT = {"affine": oracle.AFFINE, "q8_0": oracle.Q8_0, "mxfp4": oracle.MXFP4, "mxfp4_blocks": oracle.MXFP4_BLOCKS}
 SDT = {"bf16": oracle.BF16, "f16": oracle.F16, None: oracle.BF16}
 
 
