@@ -85,6 +85,8 @@ def _load():
             lib.or_apply_entries.argtypes = [i32, i32, i32, i32, i64, i64, vp, vp, vp, vp, i32,
                                              i64, vp, vp, dp]
             lib.or_apply_entries.restype = None
+            lib.or_quantize_q8_0.argtypes = [vp, i64, i64, vp]
+            lib.or_quantize_q8_0.restype = None
             lib.or_take_part.argtypes = [vp, i64, i64, i64, vp, i32, i64, vp]
             lib.or_take_part.restype = None
             lib.or_route.argtypes = [vp, i32, i64, i64, vp, vp, vp]
@@ -251,6 +253,18 @@ def apply_entries(w: Weight, x: np.ndarray, m_idx, j_idx, xdt=None) -> np.ndarra
     _load().or_apply_entries(*w._args(), w.rows, w.k, _ptr(w.codes), _ptr(w.scales),
                              _ptr(w.biases), _ptr(x), _x_dtype(x, xdt), m_idx.shape[0],
                              _ptr(m_idx), _ptr(j_idx), _ptr(out))
+    return out
+
+
+def quantize_q8_0(x: np.ndarray) -> np.ndarray:
+    """Float32 x [..., n, k] (k a multiple of 32) as Q8_0 blocks [..., n, k/32*34]."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    k = x.shape[-1]
+    if k % 32:
+        raise ValueError("k must be a multiple of 32")
+    rows = x.size // k if k else 0
+    out = np.empty(x.shape[:-1] + (k // 32 * 34,), dtype=np.uint8)
+    _load().or_quantize_q8_0(_ptr(x), rows, k, _ptr(out))
     return out
 
 

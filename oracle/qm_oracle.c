@@ -272,6 +272,54 @@ static void or_store(void* out, int64_t idx, int dt, float v)
         ((uint16_t*)out)[idx] = or_f32_to_f16(v);
 }
 
+/* ------------------------------------------------------------------ */
+/* quantize_q8_0: float32 rows to Q8_0 blocks ([NXQ] "Weights",        */
+/* val quantize_q8_0)                                                   */
+/* ------------------------------------------------------------------ */
+
+/* x [rows, k] float32 -> blocks [rows, k/32*34]. Per block of 32 values:
+ * a NaN anywhere gives a NaN scale and quants 0; else an infinity gives the
+ * scale +inf and quants 0; else d = amax / 127 at float32, stored at float16
+ * rounded to nearest, and quant j = round(v_j * (1 / d)) with halves away from
+ * zero, the reciprocal and products at float32 and 1/d = 0 where d is 0; a
+ * product that is not finite (1/d past float32's range) has the quant 0. */
+void or_quantize_q8_0(const float* x, int64_t rows, int64_t k, uint8_t* blocks)
+{
+    int64_t nb = k / 32;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t b = 0; b < nb; ++b) {
+            const float* v = x + r * k + b * 32;
+            uint8_t* out = blocks + (r * nb + b) * 34;
+            int has_nan = 0, has_inf = 0;
+            float amax = 0.0f;
+            for (int j = 0; j < 32; ++j) {
+                if (isnan(v[j]))
+                    has_nan = 1;
+                else if (isinf(v[j]))
+                    has_inf = 1;
+                else if (fabsf(v[j]) > amax)
+                    amax = fabsf(v[j]);
+            }
+            uint16_t h;
+            int8_t q[32];
+            if (has_nan || has_inf) {
+                h = has_nan ? 0x7E00 : 0x7C00;
+                for (int j = 0; j < 32; ++j) q[j] = 0;
+            } else {
+                float d = amax / 127.0f;
+                float id = (d != 0.0f) ? 1.0f / d : 0.0f;
+                h = or_f32_to_f16(d);
+                for (int j = 0; j < 32; ++j) {
+                    float p = v[j] * id;
+                    q[j] = isfinite(p) ? (int8_t)roundf(p) : 0;
+                }
+            }
+            out[0] = (uint8_t)(h & 0xFF);          /* little-endian float16 */
+            out[1] = (uint8_t)(h >> 8);
+            for (int j = 0; j < 32; ++j) out[2 + j] = (uint8_t)q[j];
+        }
+}
+
 /* rows = product of the leading axes times n; out is [rows, k] of dtype dt. */
 void or_dequant(int fmt, int bits, int gs, int sdt, int64_t rows, int64_t k,
                 const void* codes, const void* scales, const void* biases,

@@ -21,6 +21,10 @@ MUTANTS = {
                                "return (t < 16) ? (b >> 4) : (b & 0xF);"),
     "mxfp4_blocks_byte_index": ("uint8_t b = block[1 + (t % 16)];", "uint8_t b = block[1 + (t / 2)];"),
     "mxfp4_blocks_scale_byte": ("or_e8m0_to_f64(blk[0])", "or_e8m0_to_f64(blk[16])"),
+    "quantize_half_even": ("q[j] = isfinite(p) ? (int8_t)roundf(p) : 0;",
+                           "q[j] = isfinite(p) ? (int8_t)rintf(p) : 0;"),
+    "quantize_amax_128": ("float d = amax / 127.0f;", "float d = amax / 128.0f;"),
+    "quantize_inf_scale_sign": ("h = has_nan ? 0x7E00 : 0x7C00;", "h = has_nan ? 0x7E00 : 0xFC00;"),
     "affine_bias_dropped": ("v[i] = fmaf((float)c, s, b);", "v[i] = fmaf((float)c, s, 0.0f * b);"),
     "affine_bit_order": ("c |= bit << t;", "c |= bit << (bits - 1 - t);"),
     "affine_group_index": ("r * ng + i / gs, sdt);\n            float b",

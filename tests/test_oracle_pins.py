@@ -384,6 +384,73 @@ def test_quantize_q8_0_round_trip():
     assert np.all(np.abs(v - xb) <= 0.5 * step * 1.002 + 1e-7)
 
 
+def _q8_block(x32):
+    b = oracle.quantize_q8_0(np.asarray(x32, np.float32).reshape(1, 32))[0]
+    return int(b[0]) | (int(b[1]) << 8), b[2:].view(np.int8)
+
+
+def test_quantize_q8_0_stated_cases():
+    # "Nx_quant", "val quantize_q8_0": d = amax / 127 stored at float16 rounded
+    # to nearest; quants round(v * (1/d)), halves away from zero; 0 where d is 0
+    x = np.zeros(32, np.float32)
+    x[:6] = [127.0, 2.5, -2.5, 0.5, -0.5, 126.5]    # d = 1 exactly
+    h, q = _q8_block(x)
+    assert h == 0x3C00 and list(q[:6]) == [127, 3, -3, 1, -1, 127] and not q[6:].any()
+    h, q = _q8_block(np.zeros(32))                 # d = 0: zero bytes
+    assert h == 0 and not q.any()
+    # 1/d infinite (amax below about 127 * 2^-128): zero bytes, which decode to +0.
+    tiny = np.zeros(32, np.float32)
+    tiny[3] = np.float32(1e-39)
+    h, q = _q8_block(tiny)
+    assert h == 0 and not q.any()
+    # an infinity: scale +inf, quants 0, whatever its sign
+    for s in (1.0, -1.0):
+        xi = np.linspace(-1, 1, 32).astype(np.float32)
+        xi[7] = s * np.inf
+        h, q = _q8_block(xi)
+        assert h == 0x7C00 and not q.any()
+    # a NaN: a NaN scale and quants 0, an infinity in the block or not
+    for extra in (False, True):
+        xn = np.linspace(-1, 1, 32).astype(np.float32)
+        xn[31] = np.nan
+        if extra:
+            xn[0] = np.inf
+        h, q = _q8_block(xn)
+        assert (h & 0x7C00) == 0x7C00 and (h & 0x3FF) != 0 and not q.any()
+    # d past float16's largest: the scale is +inf, the quants as usual
+    big = np.zeros(32, np.float32)
+    big[0], big[1] = 127.0 * 70000.0, -63.5 * 70000.0
+    h, q = _q8_block(big)
+    assert h == 0x7C00 and q[0] == 127 and q[1] == -64
+
+
+def test_quantize_q8_0_fixed_point_on_exact_blocks():
+    # x = d * q with a float16 d and |q| reaching 127: amax / 127 is d exactly,
+    # v * (1/d) lands within an ulp of q, so quantizing gives the same bytes back
+    g = np.random.default_rng(12)
+    rows, k = 16, 256
+    d = (np.abs(g.standard_normal((rows, k // 32))) * 0.01 + 1e-3).astype(np.float16)
+    q = g.integers(-127, 128, size=(rows, k // 32, 32)).astype(np.int8)
+    q[:, :, 5] = np.where(g.random((rows, k // 32)) < 0.5, 127, -127)
+    x = (d.astype(np.float32)[..., None] * q.astype(np.float32)).reshape(rows, k)
+    blocks = np.concatenate([d.view(np.uint8).reshape(rows, k // 32, 2), q.view(np.uint8)], -1)
+    assert np.array_equal(oracle.quantize_q8_0(x), blocks.reshape(rows, k // 32 * 34))
+
+
+def test_quantize_q8_0_dequant_within_half_a_step():
+    # the quants round v / d at float32 (half a step), and the stored d is d
+    # rounded to float16 (a relative 2^-11), which moves a decoded value by at
+    # most 127 * 2^-11 steps more
+    g = np.random.default_rng(13)
+    x = (g.standard_normal((8, 512)) * np.exp(g.standard_normal((8, 1)))).astype(np.float32)
+    blocks = oracle.quantize_q8_0(x)
+    v = oracle.dequant(oracle.Weight(oracle.Q8_0, x.shape, blocks), oracle.F32).reshape(8, 16, 32)
+    d = blocks.reshape(8, 16, 34)[:, :, :2].copy().view(np.float16).astype(np.float32)
+    err = np.abs(v - x.reshape(8, 16, 32))
+    assert np.all(err <= (0.5 + 127 * 2.0 ** -11) * d * 1.002 + 1e-7)
+    assert err.max() > 0.5 * d.min()  # the bound is not vacuous
+
+
 # ------------------------------------------------------------ take
 @pytest.mark.parametrize("kind", ["affine", "q8_0", "mxfp4"])
 def test_take_commutes_with_dequant(kind):
