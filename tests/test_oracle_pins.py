@@ -211,6 +211,33 @@ def test_affine_unit_scale_returns_codes():
         assert np.array_equal(v, want.reshape(8, 128).astype(np.float32))
 
 
+@pytest.mark.parametrize("bits", [2, 3, 5, 6])
+def test_affine_cross_word_widths_dequant(bits):
+    # "GPTQModel wiki: MLX Apple Silicon", "Packed layouts and exact transcoding":
+    # widths that do not divide 32 continue one little-endian bit stream across
+    # words. Codes packed here by a Python integer stream; value = code*scale + bias.
+    g = np.random.default_rng(20 + bits)
+    rows, k, gs = 6, 256, 64
+    codes = g.integers(0, 1 << bits, size=(rows, k))
+    words = np.empty((rows, k * bits // 32), np.uint32)
+    for r in range(rows):
+        stream = 0
+        for i, c in enumerate(codes[r]):
+            stream |= int(c) << (i * bits)
+        words[r] = [(stream >> (32 * t)) & 0xFFFFFFFF for t in range(k * bits // 32)]
+    one = np.full((rows, k // gs), 0x3F80, np.uint16)   # bf16 1.0
+    zero = np.zeros((rows, k // gs), np.uint16)
+    w = oracle.Weight(oracle.AFFINE, (rows, k), words, one, zero, bits=bits, group_size=gs)
+    assert np.array_equal(oracle.dequant(w, oracle.F32), codes.astype(np.float32))
+    sc = synth.normal_bf16(g, (rows, k // gs), 0.02)
+    bi = synth.normal_bf16(g, (rows, k // gs), 0.02)
+    w = oracle.Weight(oracle.AFFINE, (rows, k), words, sc, bi, bits=bits, group_size=gs)
+    s64 = torch.from_numpy(sc.view(np.int16)).view(torch.bfloat16).double().numpy()
+    b64 = torch.from_numpy(bi.view(np.int16)).view(torch.bfloat16).double().numpy()
+    want = (codes * np.repeat(s64, gs, axis=1) + np.repeat(b64, gs, axis=1)).astype(np.float32)
+    assert np.array_equal(oracle.dequant(w, oracle.F32), want)
+
+
 def test_affine_reconstruction_per_group():
     # value = code * scale + bias with the group's scale and bias: checked in
     # float64 (exact for these magnitudes), rounded once to float32
