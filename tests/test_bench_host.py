@@ -1,0 +1,31 @@
+"""bench.py's host-side bookkeeping, without a GPU: the decode step's products
+and bytes, and the provenance of every recorded DRAM-traffic figure."""
+import os
+import re
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_decode_step_products_and_bytes():
+    items = bench.workload_list(4)
+    assert len(items) == 28 * 6 + 1 and items[-1][0] == "lm_head"
+    # affine 4-bit gs64: half a byte per code plus two bf16 per 64 values
+    total = sum(bench.packed_bytes(n, k, 4) for _, n, k in items)
+    assert total == sum(n * k // 2 + 2 * n * (k // 64) * 2 for _, n, k in items) == 302211072
+    assert bench.config_dict(4, 1)["weight_bytes_per_step"] == total
+
+
+def test_traffic_figures_name_their_capture():
+    for key, (value, commit, src) in bench.TRAFFIC.items():
+        path = os.path.join(ROOT, src)
+        assert value > 0 and os.path.exists(path), (key, src)
+        text = open(path).read()
+        assert re.search(r"commit\s+" + commit, text), (key, commit, src)  # the summary names the same kernel version
+    assert bench.traffic("decode", False) == (None, None)
+    v, why = bench.traffic("decode")
+    assert v == bench.TRAFFIC["decode"][0] and "profiles/" in why
