@@ -45,9 +45,9 @@
  * Errors: QM_EINVAL for a bad argument, with qm_last_error() (thread-local,
  * valid until the next call on the thread) naming the part: "w", "codes",
  * "scales", "biases", "x", "y", "out", "ids", "axis", "workspace". QM_ECUDA if
- * a launch fails. A device-side wait that runs past its limit (about one
- * second) abandons its work and raises a device flag; qm_device_status()
- * reads it. No entry point synchronizes the stream.
+ * a launch fails. A device-side wait that runs past its limit (two seconds of
+ * the GPU's global timer) abandons its work and raises a device flag;
+ * qm_device_status() reads it. No entry point synchronizes the stream.
  */
 #ifndef QM_H_
 #define QM_H_
@@ -148,6 +148,8 @@ size_t qm_experts_route_workspace(int64_t P, int64_t E);
  * cores. The path follows from the shapes alone, so a row's bits depend on the
  * shapes, its row and its expert, never on the other positions' experts.
  * workspace_bytes must be at least qm_apply_experts_workspace(w, T, topk).
+ * Routing keeps positions as int32: T*topk past 2^31-1 is refused (QM_EINVAL
+ * naming "ids") before any device work, and so is E past 2^31-2 ("w").
  * Defined by "Nx_quant (raven-ml.dev API docs)", section "Products",
  * apply_experts. */
 qm_status qm_apply_experts(const qm_weight* w, const void* ids, int32_t id_type, int64_t T,
@@ -162,12 +164,17 @@ qm_status qm_apply_experts(const qm_weight* w, const void* ids, int32_t id_type,
  * 245,760 positions over 32 experts; a larger T*topk*E is refused with
  * QM_EINVAL naming "workspace". The first call on a device looks up that
  * array's device address, so make the first call on each device before any
- * stream capture. All calls share the one array: calls that may overlap on the
- * GPU (other streams, other host threads) race, so serialize them. Nothing in
- * the array needs clearing between calls. The array holds no gathered
- * activations, so this entry point always takes the decode path; where
- * qm_apply_experts would use the tensor cores (experts averaging more than 32
- * positions) the two agree within the product's error bound, not bit for bit.
+ * stream capture. The address is kept for the life of the process: after a
+ * cudaDeviceReset on a device this entry point must not be called there again
+ * (a launch that fails drops the kept address, so the next call looks it up
+ * anew). All calls share the one array: calls that may overlap on the GPU
+ * (other streams, other host threads) race, so serialize them. Nothing in the
+ * array needs clearing between calls. The array holds no gathered
+ * activations, so this entry point never takes the tensor-core path: it runs
+ * the decode product (or, for shapes that one declines, the plain per-position
+ * kernel). Where qm_apply_experts takes the same path the two give the same
+ * bits; where qm_apply_experts uses the tensor cores (experts averaging more
+ * than 32 positions) the two agree within the product's error bound.
  * Otherwise identical to qm_apply_experts; the pages have no counterpart to
  * this entry point. */
 qm_status qm_apply_experts_static(const qm_weight* w, const void* ids, int32_t id_type, int64_t T,

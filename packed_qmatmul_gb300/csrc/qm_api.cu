@@ -72,6 +72,16 @@ int max_smem_optin() {
     return v;
 }
 
+qm_status check_positions(int64_t T, int64_t topk, int64_t E) {
+    if (T < 0 || topk < 0) return fail(QM_EINVAL, "ids: negative shape");
+    // routing keeps positions, offsets and the permutation as int32
+    if (T > 0 && topk > std::numeric_limits<int32_t>::max() / T)
+        return fail(QM_EINVAL, "ids: T*topk = " + std::to_string(T) + "*" + std::to_string(topk) +
+                                   " positions, more than 2^31-1");
+    if (E > std::numeric_limits<int32_t>::max() - 1) return fail(QM_EINVAL, "w: more than 2^31-2 experts");
+    return QM_OK;
+}
+
 qm_status validate_weight(const qm_weight* w, WDesc* d) {
     if (!w) return fail(QM_EINVAL, "w: NULL weight descriptor");
     if (w->format != QM_AFFINE && w->format != QM_Q8_0 && w->format != QM_MXFP4 && w->format != QM_MXFP4_BLOCKS)
@@ -320,6 +330,7 @@ size_t qm_apply_experts_workspace(const qm_weight* w, int64_t T, int64_t topk) {
     set_error("");
     WDesc d;
     if (validate_weight(w, &d) != QM_OK || d.ndim != 3 || T <= 0 || topk <= 0) return 0;
+    if (check_positions(T, topk, d.shape[0]) != QM_OK) return 0;
     return experts_workspace_bytes(d, T * topk, true);
 }
 
@@ -348,6 +359,8 @@ qm_status qm::apply_experts_checked(const qm_weight* w, const void* ids, int32_t
     if (d.ndim != 3) return fail(QM_EINVAL, "w: apply_experts takes a 3-d weight [E, n, k]");
     if (T < 0 || topk < 0) return fail(QM_EINVAL, "ids: negative shape");
     if (id_type != QM_I32 && id_type != QM_I64) return fail(QM_EINVAL, "ids: id_type must be QM_I32 or QM_I64");
+    s = check_positions(T, topk, d.shape[0]);
+    if (s != QM_OK) return s;
     if (x_dtype != QM_BF16) return fail(QM_ENOTSUP, "x: apply_experts takes bfloat16 activations");
     if (x_rows != T && x_rows != T * topk)
         return fail(QM_EINVAL, "x: rows must be T (broadcast over topk) or T*topk");
@@ -379,7 +392,8 @@ qm_status qm_experts_route(const void* ids, int32_t id_type, int64_t P, int64_t 
     set_error("");
     if (id_type != QM_I32 && id_type != QM_I64) return fail(QM_EINVAL, "ids: id_type must be QM_I32 or QM_I64");
     if (P < 0 || E < 0) return fail(QM_EINVAL, "ids: negative size");
-    if (P > std::numeric_limits<int32_t>::max()) return fail(QM_EINVAL, "ids: more than 2^31-1 positions");
+    const qm_status cs = check_positions(P, 1, E);
+    if (cs != QM_OK) return cs;
     if (!counts || !offsets) return fail(QM_EINVAL, "out: counts and offsets are required");
     if (P > 0 && (!ids || !perm)) return fail(QM_EINVAL, "ids: NULL");
     const size_t need = route_workspace_bytes(P, E);

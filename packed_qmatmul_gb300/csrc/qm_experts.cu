@@ -362,11 +362,14 @@ namespace qm {
 constexpr size_t kStaticScratchBytes = size_t(1) << 20;  // 1 MiB
 static __device__ __align__(256) unsigned char g_experts_scratch[kStaticScratchBytes];
 
+static std::mutex g_scratch_mu;
+static void* g_scratch_ptr[64] = {};
+
 // The array's device address on the current device, looked up once per
 // device (host code only sees a host-side stand-in for the symbol).
 static cudaError_t static_scratch(void** out) {
-    static std::mutex mu;
-    static void* ptr[64] = {};
+    std::mutex& mu = g_scratch_mu;
+    void** ptr = g_scratch_ptr;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -390,6 +393,8 @@ extern "C" qm_status qm_apply_experts_static(const qm_weight* w, const void* ids
     using namespace qm;
     set_error("");
     if (w && w->ndim == 3 && T > 0 && topk > 0 && w->shape[0] >= 0) {
+        const qm_status s = check_positions(T, topk, w->shape[0]);
+        if (s != QM_OK) return s;
         const size_t need = route_workspace_bytes(T * topk, w->shape[0]);
         if (need > kStaticScratchBytes)
             return fail(QM_EINVAL, "workspace: " + std::to_string(T * topk) + " positions over " +
@@ -402,6 +407,14 @@ extern "C" qm_status qm_apply_experts_static(const qm_weight* w, const void* ids
     if (e != cudaSuccess) return cuda_fail(e, "static scratch address");
     // Every entry of the routing tables is written before it is read, so the
     // array needs no clearing between calls.
-    return apply_experts_checked(w, ids, id_type, T, topk, x, x_rows, x_dtype, y, scratch, kStaticScratchBytes,
-                                 stream, /*allow_tensor=*/false);
+    const qm_status st = apply_experts_checked(w, ids, id_type, T, topk, x, x_rows, x_dtype, y, scratch,
+                                               kStaticScratchBytes, stream, /*allow_tensor=*/false);
+    if (st == QM_ECUDA) {  // the kept address may be stale (a reset device): look it up anew next time
+        int dev = 0;
+        if (cudaGetDevice(&dev) == cudaSuccess && dev >= 0 && dev < 64) {
+            std::lock_guard<std::mutex> lock(g_scratch_mu);
+            g_scratch_ptr[dev] = nullptr;
+        }
+    }
+    return st;
 }

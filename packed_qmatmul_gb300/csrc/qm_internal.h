@@ -36,6 +36,10 @@ qm_status cuda_fail(cudaError_t e, const char* what);
 
 // Validates w and fills d. On failure sets the message and returns QM_EINVAL.
 qm_status validate_weight(const qm_weight* w, WDesc* d);
+// Refuses (QM_EINVAL naming "ids" or "w") T*topk positions past 2^31-1 or E
+// experts past 2^31-2, before anything multiplies them: routing stores
+// positions, offsets and the permutation as int32.
+qm_status check_positions(int64_t T, int64_t topk, int64_t E);
 
 int dtype_size(int dt);
 

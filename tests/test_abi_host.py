@@ -131,6 +131,25 @@ def test_experts_validation(lib):
     assert st == qm.QM_EINVAL and lib.qm_last_error().decode().startswith("workspace:")
 
 
+@pytest.mark.parametrize("T,topk", [(1 << 20, 1 << 12), (3, (1 << 62)), ((1 << 31), 1)])
+def test_experts_refuse_positions_past_int32(lib, T, topk):
+    # routing stores positions as int32: T*topk past 2^31-1 is refused before
+    # anything multiplies them (a wrapped product would index out of bounds)
+    w3 = _w(shape=(4, 16, 64), ndim=3)
+    st = lib.qm_apply_experts(ctypes.byref(w3), 4096, qm.QM_I32, T, topk, 8192, T, qm.QM_BF16, 16384,
+                              32768, 1 << 40, None)
+    assert st == qm.QM_EINVAL and lib.qm_last_error().decode().startswith("ids:"), lib.qm_last_error()
+    st = lib.qm_apply_experts_static(ctypes.byref(w3), 4096, qm.QM_I32, T, topk, 8192, T, qm.QM_BF16,
+                                     16384, None)
+    assert st == qm.QM_EINVAL and lib.qm_last_error().decode().startswith("ids:"), lib.qm_last_error()
+    assert lib.qm_apply_experts_workspace(ctypes.byref(w3), T, topk) == 0
+
+
+def test_route_refuses_positions_past_int32(lib):
+    st = lib.qm_experts_route(4096, qm.QM_I32, 1 << 31, 8, 8192, 8192, 8192, 16384, 1 << 40, None)
+    assert st == qm.QM_EINVAL and lib.qm_last_error().decode().startswith("ids:")
+
+
 def test_workspace_query(lib):
     w3 = _w(fmt=qm.QM_MXFP4, bits=0, gs=0, shape=(32, 5760, 2880), ndim=3, biases=0)
     assert lib.qm_apply_experts_workspace(ctypes.byref(w3), 0, 4) == 0

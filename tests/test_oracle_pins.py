@@ -648,3 +648,38 @@ def test_experts_broadcast_equals_repeated_rows():
             sub = oracle.Weight(w.fmt, (8, 128), w.codes[ids[t, j]], w.scales[ids[t, j]],
                                 w.biases[ids[t, j]], bits=4, group_size=64)
             assert np.array_equal(a[t, j], oracle.apply(sub, x[t:t + 1])[0])
+
+
+def test_experts_entries_are_per_matrix_products():
+    # sampled entries of apply_experts: entry (p, j) is row j of expert
+    # ids[p]'s matrix against p's row of x -- the product of apply on that one
+    # matrix (pinned above against torch.matmul) -- and zero where ids[p] is out
+    # of range, whatever x holds
+    g = np.random.default_rng(20)
+    E, n, k, T, topk = 3, 7, 96, 5, 2
+    w = to_oracle(synth.affine_weight(g, n, k, bits=4, group_size=32, lead=(E,)))
+    x = synth.activations(g, T, k)
+    x[4] = 0x7FC0  # NaN row, used only by out-of-range positions below
+    ids = synth.expert_ids(g, T, topk, E)
+    ids[4] = (-1, E)
+    p_idx = np.array([0, 1, 3, 5, 8, 9, 2, 6])
+    j_idx = np.array([0, 6, 3, 2, 5, 1, 4, 0])
+    ent = oracle.apply_experts_entries(w, ids, x, p_idx, j_idx)
+    for e, (p, j) in enumerate(zip(p_idx, j_idx)):
+        t, s = divmod(int(p), topk)
+        eid = int(ids[t, s])
+        if not 0 <= eid < E:
+            assert ent[e] == 0 and not np.signbit(ent[e])
+            continue
+        sub = oracle.Weight(w.fmt, (n, k), w.codes[eid], w.scales[eid], w.biases[eid], bits=4,
+                            group_size=32)
+        assert ent[e] == oracle.apply(sub, x[t:t + 1])[0, j]
+    # per-position rows of x (x_rows = T * topk) pick row p, not row p // topk
+    xp = synth.activations(g, T * topk, k)
+    ent2 = oracle.apply_experts_entries(w, ids, xp, p_idx[:4], j_idx[:4])
+    for e in range(4):
+        t, s = divmod(int(p_idx[e]), topk)
+        eid = int(ids[t, s])
+        sub = oracle.Weight(w.fmt, (n, k), w.codes[eid], w.scales[eid], w.biases[eid], bits=4,
+                            group_size=32)
+        assert ent2[e] == oracle.apply(sub, xp[p_idx[e]:p_idx[e] + 1])[0, j_idx[e]]

@@ -13,9 +13,10 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import packed_qmatmul_gb300 as qm
 from packed_qmatmul_gb300 import synth
-from wutil import bf16_half_ulp
+from wutil import bf16_half_ulp, check_product, row_norms, to_oracle
 
 
 def _lib():
@@ -29,17 +30,26 @@ def _bf16_f64(t):
     return t.float().cpu().numpy().astype(np.float64)
 
 
+# (format, E, n, k, T, topk): the first two take the decode path in both entry
+# points; the third has experts averaging over 32 positions, where
+# qm_apply_experts takes the tensor cores and the static entry point does not
+CASES = (("mxfp4", 8, 96, 512, 40, 2), ("affine", 5, 64, 256, 23, 3), ("q8_0", 4, 128, 256, 80, 2))
+
+
 @pytest.mark.gpu
 def test_static_scratch_matches_workspace_entry_point():
     _lib()
     torch.cuda.set_device(0)
-    # two calls in a row with different routing sizes: the second must not see
-    # anything the first left in the shared array
-    for call, (kind, E, n, k, T, topk) in enumerate((("mxfp4", 8, 96, 512, 40, 2),
-                                                     ("affine", 5, 64, 256, 23, 3))):
+    # calls in a row with different routing sizes: each must not see anything
+    # the one before left in the shared array
+    for call, (kind, E, n, k, T, topk) in enumerate(CASES):
         g = synth.rng(1300 + call)
-        w = (synth.mxfp4_weight(g, n, k, lead=(E,)) if kind == "mxfp4"
-             else synth.affine_weight(g, n, k, bits=4, group_size=64, lead=(E,)))
+        if kind == "mxfp4":
+            w = synth.mxfp4_weight(g, n, k, lead=(E,))
+        elif kind == "affine":
+            w = synth.affine_weight(g, n, k, bits=4, group_size=64, lead=(E,))
+        else:
+            w = synth.q8_0_weight(g, n, k, lead=(E,))
         ids = synth.expert_ids(g, T, topk, E)
         ids[1, 0] = -1
         ids[T - 1, topk - 1] = E + 2
@@ -54,19 +64,30 @@ def test_static_scratch_matches_workspace_entry_point():
         qm.qm_device_status()
         a, b = _bf16_f64(y_st), _bf16_f64(y_ws)
         assert np.all(np.isfinite(a))
-        # the product tolerance of the parity tests, taking the workspace
-        # entry point's result as the reference
+        a2, b2 = a.reshape(T * topk, n), b.reshape(T * topk, n)
+        flat = ids.reshape(-1)
+        inr = (flat >= 0) & (flat < E)
+        assert np.all(a2[~inr] == 0)
+        tensor = T * topk > 32 * E
+        if not tensor:
+            # the same decode path: the same bits
+            assert np.array_equal(y_st.view(torch.int16).cpu().numpy(), y_ws.view(torch.int16).cpu().numpy()), call
+        # the product tolerance of the parity tests, with the workspace entry
+        # point's result as the reference
         xn = np.linalg.norm(x_d.float().cpu().numpy().astype(np.float64), axis=1)
         wv = qm.dequant(qw, torch.float32).cpu().numpy().astype(np.float64)
         wn = np.linalg.norm(wv, axis=-1)  # [E, n]
-        flat = ids.reshape(-1)
-        inr = (flat >= 0) & (flat < E)
         bound = np.zeros((T * topk, n))
         bound[inr] = 1e-2 * xn[np.arange(T * topk)[inr] // topk][:, None] * wn[flat[inr]] / np.sqrt(k)
-        a2, b2 = a.reshape(T * topk, n), b.reshape(T * topk, n)
-        assert np.all(np.abs(a2 - b2) <= bound + bf16_half_ulp(a2)), call
+        assert np.all(np.abs(a2 - b2) <= bound + bf16_half_ulp(a2) + bf16_half_ulp(b2)), call
         assert np.linalg.norm(a2 - b2) <= 4e-3 * max(np.linalg.norm(b2), 1e-30)
-        assert np.all(a2[~inr] == 0)
+        # and both against the oracle
+        ow = to_oracle(w)
+        ref = oracle.apply_experts(ow, ids, x).reshape(T * topk, n)
+        rows = np.where(inr)[0]
+        wr = row_norms(ow).reshape(E, n)[flat[rows]]
+        for got, what in ((a2, "static"), (b2, "workspace")):
+            check_product(got[rows], ref[rows], wr, xn[rows // topk], k, f"{what} call {call}")
 
 
 def test_static_scratch_refuses_oversize_routing():
