@@ -194,6 +194,24 @@ def time_graph(step, stream, steps, warmup, clock_index=None):
 PREFILL_METRIC = "TFLOP/s (M>=128 qmatmul)"
 
 
+def prefill_items(M, dev, only=None):
+    """GGUF Q8_0 weights 4096x4096, 14336x4096, 4096x14336 with x [M, k] and y [M, n]."""
+    import torch
+
+    import packed_qmatmul_gb300 as qm
+
+    g = synth.rng(2)
+    items = []
+    for n, k in synth.Q8_0_SHAPES:
+        if only and f"{n}x{k}" != only:
+            continue
+        qw = qm.QWeight.from_arrays(synth.q8_0_weight(g, n, k), dev)
+        x = torch.from_numpy(synth.activations(g, M, k).view(np.int16)).to(dev).view(torch.bfloat16)
+        y = torch.empty((M, n), dtype=torch.bfloat16, device=dev)
+        items.append((n, k, qw, x, y))
+    return items
+
+
 def run_prefill(args, rank, world):
     """GGUF Q8_0 products 4096x4096, 14336x4096 and 4096x14336 at M tokens
     (2048 by default): one step = the three qm_apply calls, graph-captured."""
@@ -207,15 +225,7 @@ def run_prefill(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     M = args.M or 2048
-    g = synth.rng(2)
-    items = []
-    for n, k in synth.Q8_0_SHAPES:
-        if args.only and f"{n}x{k}" != args.only:
-            continue
-        qw = qm.QWeight.from_arrays(synth.q8_0_weight(g, n, k), dev)
-        x = torch.from_numpy(synth.activations(g, M, k).view(np.int16)).to(dev).view(torch.bfloat16)
-        y = torch.empty((M, n), dtype=torch.bfloat16, device=dev)
-        items.append((n, k, qw, x, y))
+    items = prefill_items(M, dev, args.only)
     flops = sum(2.0 * M * n * k for n, k, *_ in items)
     wbytes = sum(n * (k // 32) * 34 for n, k, *_ in items)
     stream = torch.cuda.Stream()
@@ -415,7 +425,8 @@ def run_take(args, rank, world):
     return {
         "metric": TAKE_METRIC, "value": round((tb + db) * world / t_step / 1e9, 2), "unit": "GB/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step * 1e3, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded)",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "dtype_note": "values decoded to f32, rounded once to bf16", "data": "synthetic (seeded)",
         "config": {"workload": "MLX affine 4-bit gs64 table 151936x1024: take of 4096 uniform ids to bf16 "
                                "[4096, 1024] + dequant of the whole table to bf16",
                    "bytes_per_step": tb + db, "take_bytes": tb, "dequant_bytes": db,
@@ -430,11 +441,88 @@ def run_take(args, rank, world):
     }
 
 
+def chain_time(calls, stream, reps=10, warmup=3):
+    """Seconds per call of a CUDA graph that runs `calls` (callables taking the
+    stream) once each, in order, replayed `reps` times after `warmup`."""
+    el, _ = time_graph(lambda: [c(stream) for c in calls], stream, reps, warmup)
+    return el / (reps * len(calls))
+
+
 def other_workloads(dev, stream):
-    """The other configs' headline numbers, for the default run's detail."""
+    """The other configs' headline numbers, for the default run's detail. Each
+    sub-L2 problem is timed as a graph chain over distinct weights, tables or
+    outputs whose total exceeds twice the L2, so no call reads what an earlier
+    one left in L2."""
     import torch
 
+    import packed_qmatmul_gb300 as qm
+
+    peaks = load_peaks()
+    hbm = peaks.get("hbm_gbs", 6800.0)
+    tc = peaks.get("bf16_tflops", 1900.0)
     out = {}
+    # prefill: the TFLOP/s half of the metric (Q8_0, the three shapes per step)
+    for M in (128, 2048):
+        items = prefill_items(M, dev)
+        flops = sum(2.0 * M * n * k for n, k, *_ in items)
+        t = chain_time([lambda st, it=it: qm.qm_apply(it[2], it[3], it[4], st) for it in items], stream) * len(items)
+        out[f"prefill_q8_0_M{M}"] = {"TFLOP/s": round(flops / t / 1e12, 1), "frac": round(flops / t / 1e12 / tc, 4),
+                                     "ms_per_step": round(t * 1e3, 4),
+                                     "shapes": "4096x4096, 14336x4096, 4096x14336"}
+        del items
+        torch.cuda.empty_cache()
+    # Q8_0 14336 x 4096 at M = 1: five distinct weights (312 MB)
+    g = synth.rng(6)
+    n, k = 14336, 4096
+    ws = [qm.QWeight.from_arrays(synth.q8_0_weight(g, n, k), dev, flags=qm.QM_WEIGHT_STATIC) for _ in range(5)]
+    xs = [torch.from_numpy(synth.activations(g, 1, k).view(np.int16)).to(dev).view(torch.bfloat16) for _ in ws]
+    ys = [torch.empty((1, n), dtype=torch.bfloat16, device=dev) for _ in ws]
+    t = chain_time([lambda st, i=i: qm.qm_apply(ws[i], xs[i], ys[i], st) for i in range(len(ws))], stream, 20)
+    b = n * (k // 32) * 34
+    out["q8_0_14336x4096_M1"] = {"us": round(t * 1e6, 2), "GB/s": round(b / t / 1e9, 1),
+                                 "frac": round(b / t / 1e9 / hbm, 4)}
+    del ws, xs, ys
+    torch.cuda.empty_cache()
+    # the embedding-table shape, 151936 x 1024 affine 4-bit gs64, four distinct
+    # tables (350 MB): lm_head at M = 1, take of 4096 uniform ids, full dequant
+    g = synth.rng(5)
+    n, k = LM_HEAD
+    tabs = [qm.QWeight.from_arrays(synth.affine_weight(g, n, k, bits=4, group_size=64), dev,
+                                   flags=qm.QM_WEIGHT_STATIC) for _ in range(4)]
+    row = packed_bytes(1, k, 4)
+    xs = [torch.from_numpy(synth.activations(g, 1, k).view(np.int16)).to(dev).view(torch.bfloat16) for _ in tabs]
+    ys = [torch.empty((1, n), dtype=torch.bfloat16, device=dev) for _ in tabs]
+    t = chain_time([lambda st, i=i: qm.qm_apply(tabs[i], xs[i], ys[i], st) for i in range(4)], stream, 20)
+    out["lm_head_M1"] = {"us": round(t * 1e6, 2), "GB/s": round(n * row / t / 1e9, 1),
+                         "frac": round(n * row / t / 1e9 / hbm, 4)}
+    del xs, ys
+    nid, R = 4096, 64  # 64 takes of fresh ids into distinct outputs: 151 MB packed, 537 MB dense
+    ids = [torch.from_numpy(synth.uniform_ids(g, nid, n)).to(dev) for _ in range(R)]
+    shapes = tabs[0].part_shapes((nid,))
+    pouts = [[None if sh is None else torch.empty(sh, dtype=torch.uint8, device=dev) for sh in shapes]
+             for _ in range(R)]
+    t = chain_time([lambda st, i=i: qm.qm_take(tabs[i % 4], 0, ids[i], pouts[i][0], pouts[i][1], pouts[i][2],
+                                               None, st) for i in range(R)], stream)
+    pb = 2 * nid * row + nid * 4
+    out["take_packed_4096"] = {"us": round(t * 1e6, 2), "GB/s": round(pb / t / 1e9, 1),
+                               "frac": round(pb / t / 1e9 / hbm, 4),
+                               "bytes": "packed rows read and written once, plus the ids"}
+    del pouts
+    torch.cuda.empty_cache()
+    douts = [torch.empty((nid, k), dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    t = chain_time([lambda st, i=i: qm.qm_take(tabs[i % 4], 0, ids[i], None, None, None, douts[i], st)
+                    for i in range(R)], stream)
+    tb = nid * (row + 2 * k) + nid * 4
+    out["take_dense_4096"] = {"us": round(t * 1e6, 2), "GB/s": round(tb / t / 1e9, 1),
+                              "frac": round(tb / t / 1e9 / hbm, 4),
+                              "bytes": "packed rows read, bf16 rows written, plus the ids"}
+    del douts, ids
+    table = torch.empty((n, k), dtype=torch.bfloat16, device=dev)  # 311 MB written per call: past L2
+    t = chain_time([lambda st: qm.qm_dequant(tabs[0], table, st)], stream)
+    db = n * (row + 2 * k)
+    out["dequant_table"] = {"ms": round(t * 1e3, 4), "GB/s": round(db / t / 1e9, 1), "frac": round(db / t / 1e9 / hbm, 4)}
+    del tabs, table
+    torch.cuda.empty_cache()
     for T in (64, 1024, 4096):
         fn, flops, wbytes, _, tensor = experts_step(T, dev)
         el, _ = time_graph(lambda: fn(stream), stream, 10, 3)
@@ -444,18 +532,6 @@ def other_workloads(dev, stream):
                                 "path": "grouped tcgen05 GEMM" if tensor else "grouped GEMV"}
         del fn
         torch.cuda.empty_cache()
-    take, deq, ptake, tb, db, pb = take_step(dev)
-    # each take follows a full dequant (311 MB written): its reads start cold
-    el_td, _ = time_graph(lambda: (deq(stream), take(stream)), stream, 10, 3)
-    el_pd, _ = time_graph(lambda: (deq(stream), ptake(stream)), stream, 10, 3)
-    el_d, _ = time_graph(lambda: deq(stream), stream, 10, 3)
-    td = (el_td - el_d) / 10
-    pd = (el_pd - el_d) / 10
-    out["dequant_table"] = {"ms": round(el_d / 10 * 1e3, 4), "GB/s": round(db / (el_d / 10) / 1e9, 1)}
-    out["take_dense_4096"] = {"us": round(td * 1e6, 2), "GB/s": round(tb / td / 1e9, 1)}
-    out["take_packed_4096"] = {"us": round(pd * 1e6, 2), "GB/s": round(pb / pd / 1e9, 1)}
-    del take, deq, ptake
-    torch.cuda.empty_cache()
     return out
 
 
@@ -503,7 +579,9 @@ def run_ours(args, rank, world):
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16xf16->f32",
+        "dtype_note": "codes enter f16 tensor-core products as exact small integers, activations as exact "
+                      "power-of-two rescaled f16; sums and scales at f32",
         "data": "synthetic (seeded; weights and activations drawn as the workload states)",
         "config": config_dict(bits, M),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
@@ -522,6 +600,11 @@ def run_ours(args, rank, world):
     if not args.no_detail and not args.only and rank == 0:
         res["detail"] = detail_measurements(args, dev, stream)
         res["detail"].update(other_workloads(dev, stream))
+        pf = res["detail"].get("prefill_q8_0_M2048")
+        if pf:  # the metric's TFLOP/s half, on the Q8_0 prefill config
+            res["tflops_m2048"] = {"metric": PREFILL_METRIC, "value": pf["TFLOP/s"], "unit": "TFLOP/s",
+                                   "frac": pf["frac"], "peak_source": "measured bf16 dense, burst",
+                                   "config": "GGUF Q8_0 W 4096x4096, 14336x4096, 4096x14336 at M=2048"}
     return res
 
 
@@ -597,22 +680,22 @@ def detail_measurements(args, dev, stream):
     return out
 
 
-# DRAM bytes (read + write) per launch of each roofline kernel, from one ncu capture
-# (the profiles/ summary named beside each); the commit is the kernel version measured.
-# A kernel changed after its capture reports null until it is captured again.
+# DRAM bytes (read + write) per launch of each roofline kernel, from one ncu
+# capture, with the commit whose kernel was measured. A kernel changed after its
+# capture has None here (reported as null) until it is captured again.
 TRAFFIC = {
-    "decode": (1.828e6, "6d4178e", "profiles/gemv_affine4_qwen3_decode_step.md"),
-    "experts_gemm": (539.3e6, "5f65fc6", "profiles/gemm_mxfp4_experts_t4096.md"),
-    "experts_gemv": (287.3e6, "6d4178e", "profiles/gemv_mxfp4_experts_t64.md"),
-    "dequant": (337.4e6, "6d4178e", "profiles/take_dequant_affine4_table.md"),
+    "decode": (None, None),
+    "experts_gemm": (None, None),
+    "experts_gemv": (None, None),
+    "dequant": (337.4e6, "6d4178e"),
 }
 
 
 def traffic(key, applies=True):
-    if not applies or key not in TRAFFIC:
+    if not applies or key not in TRAFFIC or TRAFFIC[key][0] is None:
         return None, None
-    v, commit, src = TRAFFIC[key]
-    return v, f"ncu dram__bytes_read.sum + dram__bytes_write.sum per launch at commit {commit} ({src})"
+    v, commit = TRAFFIC[key]
+    return v, f"ncu dram__bytes_read.sum + dram__bytes_write.sum per launch, kernel as of commit {commit}"
 
 
 def load_peaks():

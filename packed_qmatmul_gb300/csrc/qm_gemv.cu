@@ -25,7 +25,19 @@
 //    the N side); per group it applies scale (and bias) in float32. The team
 //    adds its warps' partial sums in warp order through shared memory.
 //  * Activations are rescaled per token by a power of two so that every bf16
-//    value is exact in f16; the scale is undone at the end.
+//    value is exact in f16; each group's partial sum is taken back to its
+//    true size (an exact power-of-two product) before its scale multiplies
+//    it, so no intermediate is larger than the true partial product.
+//  * A group whose values are, or may be, infinite (an MXFP4 scale byte of
+//    253 or 254, a Q8_0 scale that is infinite, an affine scale or bias of
+//    magnitude 2^119 or more) -- or any group, if an activation is infinite
+//    or NaN -- is summed element by element instead: each value decoded at
+//    float32 as dequant decodes it, times its activation, added in ascending
+//    k. IEEE arithmetic then gives the infinities and NaNs that the
+//    per-element definition of the product gives ("Nx_quant", "Products",
+//    val apply and val dequant: an MXFP4 value past float32's range is
+//    infinite; a block whose float16 scale is infinite gives infinite or NaN
+//    values).
 //  * Where one CTA per stage would leave SMs idle, a cluster of S CTAs splits
 //    k; their partial sums meet through distributed shared memory and are
 //    added in rank order (deterministic, no global scratch).
@@ -245,6 +257,42 @@ QM_DEV void tile_group(const CodeRow& r0, const CodeRow& r8, int gi, int t,
     }
 }
 
+// Value i (0 .. GS-1) of group gi of one staged row, decoded at float32 as
+// dequant decodes it: affine fmaf(code, s, b); Q8_0 d * q; MXFP4 e2m1 * scale.
+template <int FMT, int BITS, int GS>
+QM_DEV float elem_value(const CodeRow& r, int gi, int i, float s, float b) {
+    if constexpr (FMT == QM_AFFINE) {
+        const uint32_t bit = static_cast<uint32_t>(gi * GS + i) * BITS;
+        const uint32_t c = (lds_u8(r.at(bit >> 3)) >> (bit & 7u)) & ((1u << BITS) - 1u);
+        return fmaf(static_cast<float>(c), s, b);
+    } else if constexpr (FMT == QM_Q8_0) {
+        const int q = static_cast<int8_t>(lds_u8(r.at(34 * gi + 2 + i)));
+        return s * static_cast<float>(q);
+    } else {
+        const uint32_t byte = lds_u8(r.at(16 * gi + (i >> 1)));
+        uint32_t h[4];
+        e2m1x8_to_f16x2((i & 1) ? (byte >> 4) : (byte & 15u), h);
+        return __half2float(__ushort_as_half(static_cast<unsigned short>(h[0] & 0xFFFFu))) * s;
+    }
+}
+
+// Group gi's exact contribution to rows ra and rb of a tile for one token:
+// the sums over the group's inputs of x * value at float32, in ascending k,
+// x read from global memory (xrow: the token's activations at this group's
+// first input). Kept out of line: it runs only for exceptional groups.
+template <int FMT, int BITS, int GS>
+static __device__ __noinline__ float2 group_exact(CodeRow ra, CodeRow rb, int gi, float sa, float ba, float sb,
+                                                  float bb, const uint16_t* xrow) {
+    float acc_a = 0.0f, acc_b = 0.0f;
+#pragma unroll 1
+    for (int i = 0; i < GS; ++i) {
+        const float xv = bf16_bits_to_f32(__ldg(xrow + i));
+        acc_a = fmaf(xv, elem_value<FMT, BITS, GS>(ra, gi, i, sa, ba), acc_a);
+        acc_b = fmaf(xv, elem_value<FMT, BITS, GS>(rb, gi, i, sb, bb), acc_b);
+    }
+    return make_float2(acc_a, acc_b);
+}
+
 // Grouped mode, one warp: which chunk cluster slot `slot` is -- its size
 // (s_grp[0], 0 past the last chunk), expert (s_grp[1]), positions and
 // activation rows -- from the routing offsets, 32 experts per step.
@@ -323,11 +371,13 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
     // grouped mode: the chunk's size and expert, its positions and activation rows
     int* s_grp = reinterpret_cast<int*>(smem + 360);        // [2]
     int* s_pos = reinterpret_cast<int*>(smem + 368);        // [16]
-    int* s_xrow = reinterpret_cast<int*>(smem + 432);       // [16], ends before 512
+    int* s_xrow = reinterpret_cast<int*>(smem + 432);       // [16], ends at 496
+    volatile int& s_xbad = *reinterpret_cast<volatile int*>(smem + 496);  // an activation is inf or NaN
 
-    unsigned int* xmax = reinterpret_cast<unsigned int*>(smem + p.off_tokscale) + 32;  // [16] max |x| bits
+    unsigned int* xmax = reinterpret_cast<unsigned int*>(smem + p.off_tokscale) + 32;  // [16] max |x| as bf16 bits
     if (threadIdx.x == 0) {
         s_abort = 0;
+        s_xbad = 0;
         #pragma unroll 1
         for (int i = 0; i < kMaxStages; ++i) slot_stage[i] = -1;
         #pragma unroll 1
@@ -467,25 +517,24 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
         }
         // 1. per-token power-of-two scale over this CTA's k range (warp m: token m)
         {
-            // max |x| per token: one pass over the staged rows, order-free
-            // (warp maxima first: one shared atomic per warp and token)
+            // max |x| per token as bf16 magnitude bits (integer order is value
+            // order, and an infinity or NaN sorts above every finite value):
+            // one pass over the staged rows, order-free (warp maxima first:
+            // one shared atomic per warp and token)
             const int per_row = static_cast<int>(p.krange / 8);
             #pragma unroll 1
             for (int m = 0; m < M; ++m)
                 #pragma unroll 1
                 for (int i0 = 0; i0 < per_row; i0 += kWarps * 32) {
                     const int i = i0 + ctid;
-                    float amax = 0.0f;
+                    uint32_t amax = 0u;
                     if (i < per_row) {
                         const uint4 q = *reinterpret_cast<const uint4*>(xs + m * p.krange + 8 * i);
-                        const uint32_t w4[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w4[e] & 0xFFFF)));
-                            amax = fmaxf(amax, fabsf(bf16_bits_to_f32(w4[e] >> 16)));
-                        }
+                        amax = __vmaxu2(__vmaxu2(q.x & 0x7FFF7FFFu, q.y & 0x7FFF7FFFu),
+                                        __vmaxu2(q.z & 0x7FFF7FFFu, q.w & 0x7FFF7FFFu));
+                        amax = max(amax & 0xFFFFu, amax >> 16);
                     }
-                    const uint32_t b = __reduce_max_sync(0xffffffffu, __float_as_uint(amax));
+                    const uint32_t b = __reduce_max_sync(0xffffffffu, amax);
                     if (lane == 0 && b) atomicMax(&xmax[m], b);
                 }
         }
@@ -493,13 +542,14 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
         // x' = x * 2^E puts max |x'| in [2^14, 2^15): every bf16 value is then exact in f16
         auto token_exp = [&](int m) {
             const uint32_t bits = xmax[m];
-            if (bits == 0u) return 0;
-            const int ex = static_cast<int>((bits >> 23) & 0xFF) - 127;
+            if (bits == 0u || bits >= 0x7F80u) return 0;  // zeros, or non-finite (summed per element)
+            const int ex = static_cast<int>((bits >> 7) & 0xFF) - 127;
             return min(max(14 - ex, -126), 126);
         };
         if (ctid < 16) {
             const int E = token_exp(ctid);
             tokscale[ctid] = __uint_as_float(static_cast<uint32_t>(-E + 127) << 23);
+            if (ctid < M && xmax[ctid] >= 0x7F80u) s_xbad = 1;
         }
         // 2. B fragments for every group of the k range; each quad of lanes
         //    also sums its token's B values (F) and x' (X) over the group
@@ -512,6 +562,7 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
             // 4 MM items sit in adjacent lanes of one warp, which add its sums.
             const int items = (groups * MM * 4 + 31) / 32 * 32;
             const float mul = __uint_as_float(static_cast<uint32_t>(token_exp(0) + 127) << 23);
+            const float inv = __uint_as_float(static_cast<uint32_t>(127 - token_exp(0)) << 23);
             #pragma unroll 1
             for (int it = ctid; it < items; it += kWarps * 32) {
                 const int t = it & 3, mm = (it >> 2) % MM, gi = (it >> 2) / MM;
@@ -549,8 +600,9 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
                         X += __shfl_xor_sync(0xffffffffu, X, o);
                         F += __shfl_xor_sync(0xffffffffu, F, o);
                     }
+                    // at the true size (x, not x'): exact power-of-two products
                     const float magic = (FMT == QM_Q8_0) ? 1152.0f : 1024.0f;
-                    if (t == 0 && mm == 0 && live) tok[gi * 16] = make_float2(magic * F, X);
+                    if (t == 0 && mm == 0 && live) tok[gi * 16] = make_float2(magic * F * inv, X * inv);
                 }
             }
         } else {
@@ -562,6 +614,7 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
                 const int m = nt * 8 + tg;
                 const bool live = m < M;  // padding tokens get exact zeros
                 const float mul = live ? __uint_as_float(static_cast<uint32_t>(token_exp(m) + 127) << 23) : 0.0f;
+                const float inv = __uint_as_float(static_cast<uint32_t>(127 - (live ? token_exp(m) : 0)) << 23);
                 const uint16_t* xr = xs + (live ? m : 0) * p.krange;
                 uint32_t* dst = xfrag + ((gi * 32 + ln) * MM) * NT * 2 + nt * 2;
                 float F = 0.0f, X = 0.0f;
@@ -606,7 +659,7 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
                     X += __shfl_xor_sync(0xffffffffu, X, 2);
                     F += __shfl_xor_sync(0xffffffffu, F, 2);
                     const float magic = (FMT == QM_Q8_0) ? 1152.0f : 1024.0f;
-                    if (t == 0) tok[gi * 16 + m] = make_float2(magic * F, X);
+                    if (t == 0) tok[gi * 16 + m] = make_float2(magic * F * inv, X * inv);
                 }
             }
         }
@@ -623,6 +676,16 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
         float* partial = reinterpret_cast<float*>(smem + p.off_xraw);  // [stages][32 rows][16 tok]
         float* red = reinterpret_cast<float*>(smem + p.off_red);       // [teams][2][T][2][NT][4][32]
         int buf = 0;
+        // 2^-E of the tokens of this lane's accumulator columns (2t and 2t + 1
+        // of each token tile): a group's MMA sum times it is at its true size
+        float tk[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            tk[nt][0] = tokscale[ONE ? 0 : nt * 8 + 2 * t];
+            tk[nt][1] = tokscale[ONE ? 0 : nt * 8 + 2 * t + 1];
+        }
+        const bool xbad = s_xbad != 0;
+        const int64_t xk0 = kbase;  // this CTA's first input
         // Every warp of a team runs the same iterations and meets the team
         // barrier once per stage, abandoned or not, so no barrier is left waiting.
         // slot of stage j and how many times it was filled before, kept
@@ -720,35 +783,61 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
 #pragma unroll
                 for (int tt = 0; tt < 2; ++tt) {
                     float s0, s8, b0 = 0.0f, b8 = 0.0f;
+                    bool exc = xbad;
                     if constexpr (FMT == QM_AFFINE) {
                         s0 = sval<SDT>(raw[tt][0]);
                         s8 = sval<SDT>(raw[tt][1]);
                         b0 = sval<SDT>(raw[tt][2]);
                         b8 = sval<SDT>(raw[tt][3]);
+                        // |code * s + b| < 2^128 whenever |s|, |b| < 2^119 (codes < 2^8)
+                        exc |= fmaxf(fmaxf(fabsf(s0), fabsf(s8)), fmaxf(fabsf(b0), fabsf(b8))) >= 0x1p119f;
                     } else if constexpr (FMT == QM_Q8_0) {
                         s0 = f16_bits_to_f32(raw[tt][0]);
                         s8 = f16_bits_to_f32(raw[tt][1]);
+                        exc |= fmaxf(fabsf(s0), fabsf(s8)) > 0x1p127f;  // an infinite d
                     } else {
                         e8m0x2_to_f32(raw[tt][0] | (raw[tt][1] << 8), s0, s8);
+                        exc |= max(raw[tt][0], raw[tt][1]) >= 253u;  // values that may pass float32's range
+                    }
+                    // (a NaN scale or bias needs no exception: it makes every
+                    // value of its group NaN, and the scaled sum NaN too)
+                    if (exc) {
+                        const CodeRow& ra = rows_[2 * tt];
+                        const CodeRow& rb = rows_[2 * tt + 1];
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const int m = nt * 8 + 2 * t + h;
+                                if ((ONE && (t != 0 || h != 0)) || m >= M) continue;
+                                const int64_t xr = p.g_off ? s_xrow[m] : m;
+                                const float2 e = group_exact<FMT, BITS, GS>(ra, rb, gi, s0, b0, s8, b8,
+                                                                            p.x + xr * p.k + xk0 + gi * GS);
+                                y[tt][nt][h] += e.x;
+                                y[tt][nt][2 + h] += e.y;
+                            }
+                        continue;
                     }
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         float* yv = y[tt][nt];
                         const float* c = acc[tt][nt];
                         if constexpr (FMT == QM_MXFP4) {
-                            yv[0] = fmaf(s0, c[0], yv[0]);
-                            yv[2] = fmaf(s8, c[2], yv[2]);
+                            yv[0] = fmaf(s0, c[0] * tk[nt][0], yv[0]);
+                            yv[2] = fmaf(s8, c[2] * tk[nt][0], yv[2]);
                             if constexpr (!ONE) {
-                                yv[1] = fmaf(s0, c[1], yv[1]);
-                                yv[3] = fmaf(s8, c[3], yv[3]);
+                                yv[1] = fmaf(s0, c[1] * tk[nt][1], yv[1]);
+                                yv[3] = fmaf(s8, c[3] * tk[nt][1], yv[3]);
                             }
                         } else {
+                            // (c - offset) at its true size in one rounding: c * 2^-E is
+                            // exact, and d holds the offset and sum of x already scaled
                             const float4 d = td[nt];
-                            yv[0] = fmaf(s0, c[0] - d.x, fmaf(b0, d.y, yv[0]));
-                            yv[2] = fmaf(s8, c[2] - d.x, fmaf(b8, d.y, yv[2]));
+                            yv[0] = fmaf(s0, fmaf(c[0], tk[nt][0], -d.x), fmaf(b0, d.y, yv[0]));
+                            yv[2] = fmaf(s8, fmaf(c[2], tk[nt][0], -d.x), fmaf(b8, d.y, yv[2]));
                             if constexpr (!ONE) {  // odd columns: tokens 2t + 1
-                                yv[1] = fmaf(s0, c[1] - d.z, fmaf(b0, d.w, yv[1]));
-                                yv[3] = fmaf(s8, c[3] - d.z, fmaf(b8, d.w, yv[3]));
+                                yv[1] = fmaf(s0, fmaf(c[1], tk[nt][1], -d.z), fmaf(b0, d.w, yv[1]));
+                                yv[3] = fmaf(s8, fmaf(c[3], tk[nt][1], -d.z), fmaf(b8, d.w, yv[3]));
                             }
                         }
                     }
@@ -784,7 +873,6 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
             auto store = [&](int tt, int nt, int ln, int i, float v) {
                 const int m = nt * 8 + 2 * (ln & 3) + (i & 1);
                 const int r = 16 * tt + (ln >> 2) + ((i & 2) ? 8 : 0);
-                v *= tokscale[m];
                 if (S == 1) {
                     if (m < M && row0 + r < p.n) {
                         __nv_bfloat16 bv = __float2bfloat16_rn(v);
@@ -814,7 +902,7 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
                         float sum = 0.0f;
 #pragma unroll 1
                         for (int q = 0; q < T; ++q) sum += base[q * 32 + e];
-                        const float v = sum * tokscale[0];
+                        const float v = sum;
                         if (S == 1) {
                             if (row0 + e < p.n) {
                                 __nv_bfloat16 bv = __float2bfloat16_rn(v);

@@ -500,23 +500,64 @@ def test_apply_prefill_split_k_deterministic():
     assert np.array_equal(a, b)
 
 
-def test_apply_prefill_q8_0_full_shape_sampled():
-    # Q8_0 4096 x 4096 at M = 2048, checked on sampled outputs
-    g = synth.rng(1201)
-    w = synth.q8_0_weight(g, 4096, 4096)
-    x = synth.activations(g, 2048, 4096)
+@pytest.mark.parametrize("n,k", [(4096, 4096), (14336, 4096), (4096, 14336)])
+def test_apply_prefill_q8_0_full_shape_sampled(n, k):
+    # the Q8_0 prefill shapes at M = 2048, in the launch configuration the
+    # benchmark times, checked on sampled outputs (tile corners included)
+    g = synth.rng(1201 + n + k)
+    w = synth.q8_0_weight(g, n, k)
+    x = synth.activations(g, 2048, k)
     ow = to_oracle(w)
     y = bf16_to_f64(_host(qm.apply(qm.QWeight.from_arrays(w), _dev_bf16(x))))
-    m_idx = np.concatenate([g.integers(0, 2048, 1500), [0, 2047, 127, 128]])
-    j_idx = np.concatenate([g.integers(0, 4096, 1500), [0, 4095, 128, 127]])
+    m_idx = np.concatenate([g.integers(0, 2048, 2000), [0, 2047, 127, 128, 255, 256]])
+    j_idx = np.concatenate([g.integers(0, n, 2000), [0, n - 1, 128, 127, n - 128, 129]])
     ref = oracle.apply_entries(ow, x, m_idx, j_idx)
     wn = np.array([np.linalg.norm(oracle.row_values(ow, int(r)).astype(np.float64)) for r in j_idx])
     xn = np.linalg.norm(oracle.decode_array(x[m_idx], oracle.BF16), axis=1)
     got = y[m_idx, j_idx]
-    bound = 1e-2 * xn * wn / np.sqrt(4096)
+    bound = 1e-2 * xn * wn / np.sqrt(k)
     from wutil import bf16_half_ulp
     assert np.all(np.abs(got - ref) <= bound + bf16_half_ulp(got)), np.max(np.abs(got - ref) / bound)
     assert np.linalg.norm(got - ref) <= 4e-3 * np.linalg.norm(ref)
+
+
+def test_apply_q8_0_decode_full_shapes_sampled():
+    # the Q8_0 shapes at M = 1 and 16 (the decode kernel, k split over clusters)
+    g = synth.rng(1205)
+    for n, k, M in ((14336, 4096, 1), (4096, 14336, 1), (4096, 4096, 16)):
+        w = synth.q8_0_weight(g, n, k)
+        x = synth.activations(g, M, k)
+        ow = to_oracle(w)
+        y = bf16_to_f64(_host(qm.apply(qm.QWeight.from_arrays(w), _dev_bf16(x))))
+        j = np.unique(np.concatenate([g.integers(0, n, 1500), [0, 1, 31, 32, n - 1]]))
+        m = g.integers(0, M, j.size)
+        ref = oracle.apply_entries(ow, x, m, j)
+        wn = np.array([np.linalg.norm(oracle.row_values(ow, int(r)).astype(np.float64)) for r in j])
+        xn = np.linalg.norm(oracle.decode_array(x, oracle.BF16), axis=1)[m]
+        from wutil import bf16_half_ulp
+        got = y[m, j]
+        bound = 1e-2 * xn * wn / np.sqrt(k)
+        assert np.all(np.abs(got - ref) <= bound + bf16_half_ulp(got)), (n, k, M)
+        assert np.linalg.norm(got - ref) <= 4e-3 * np.linalg.norm(ref)
+
+
+def test_embedding_table_full_dequant_and_take():
+    # the whole 151936 x 1024 affine 4-bit gs64 table: dequant to bf16 bit for
+    # bit, and a take of 4096 uniform ids, packed and decoded, bit for bit
+    g = synth.rng(5)
+    w = synth.affine_weight(g, 151936, 1024, bits=4, group_size=64)
+    ow = to_oracle(w)
+    qw = qm.QWeight.from_arrays(w)
+    got = _host(qm.dequant(qw, torch.bfloat16))
+    want = oracle.dequant(ow, oracle.BF16)
+    assert np.array_equal(got, want)
+    del got
+    ids = synth.uniform_ids(g, 4096, 151936)
+    tw, dense = qm.take(qw, 0, torch.from_numpy(ids).cuda(), dense_dtype=torch.bfloat16)
+    assert np.array_equal(_host(dense), want[ids])
+    ot = oracle.take(ow, 0, ids)
+    for name, part in (("codes", tw.codes), ("scales", tw.scales), ("biases", tw.biases)):
+        assert np.array_equal(_host(part).view(np.uint8).reshape(-1), ot.parts()[name].view(np.uint8).reshape(-1))
 
 
 # ---------------------------------------------------------------- MXFP4 in GGUF's blocks

@@ -36,6 +36,18 @@ def row_norms(wq: "oracle.Weight") -> np.ndarray:
     return np.sqrt((v * v).sum(axis=1))
 
 
+# Magnitudes from here up round to infinity in bfloat16: halfway between its
+# largest finite value, (2 - 2^-7) * 2^127, and 2^128.
+BF16_OVERFLOW = 2.0 ** 128 - 2.0 ** 119
+
+
+def expected_nonfinite(y_ref: np.ndarray):
+    """Where the oracle's product, rounded once to bfloat16, is NaN, +inf or -inf."""
+    nan = np.isnan(y_ref)
+    big = ~nan & (np.abs(y_ref) >= BF16_OVERFLOW)
+    return nan, big & (y_ref > 0), big & (y_ref < 0)
+
+
 def check_product(y_gpu: np.ndarray, y_ref: np.ndarray, wnorm: np.ndarray, xnorm: np.ndarray,
                   k: int, what: str = ""):
     """The product contract, element by element and as a whole.
@@ -44,25 +56,44 @@ def check_product(y_gpu: np.ndarray, y_ref: np.ndarray, wnorm: np.ndarray, xnorm
     unrounded float64 product [M, n]; wnorm [n] (or [M, n] where each output
     row has its own matrix, as with experts), xnorm [M] the row norms.
 
-    Per element: |y_gpu - y_ref| <= 1e-2 * ||w_j|| * ||x_m|| / sqrt(k) plus half
-    a bfloat16 ulp of y_gpu -- the single final rounding to x's dtype that the
-    product's definition itself applies. As a whole: relative Frobenius error
-    <= 4e-3. Returns a dict of statistics.
+    Non-finite results exactly: NaN where the oracle's product is NaN, and an
+    infinity of the same sign where it is infinite or, rounded once to
+    bfloat16, overflows (the per-element definition of "Nx_quant", "Products":
+    values and products are IEEE arithmetic, so an infinite value meets its
+    activation as IEEE says). Every other element must be finite and, per
+    element: |y_gpu - y_ref| <= 1e-2 * ||w_j|| * ||x_m|| / sqrt(k) plus half a
+    bfloat16 ulp of y_gpu -- the single final rounding to x's dtype that the
+    product's definition itself applies. As a whole, over the finite elements:
+    relative Frobenius error <= 4e-3. Returns a dict of statistics.
     """
     y_gpu = np.asarray(y_gpu, dtype=np.float64)
     y_ref = np.asarray(y_ref, dtype=np.float64)
     assert y_gpu.shape == y_ref.shape, (y_gpu.shape, y_ref.shape)
-    assert np.all(np.isfinite(y_gpu)), f"{what}: non-finite outputs"
+    nan, pinf, ninf = expected_nonfinite(y_ref)
+    for name, want, got in (("NaN", nan, np.isnan(y_gpu)), ("+inf", pinf, np.isposinf(y_gpu)),
+                            ("-inf", ninf, np.isneginf(y_gpu))):
+        if not np.array_equal(want, got):
+            idx = np.argwhere(want != got)[:8].tolist()
+            raise AssertionError(f"{what}: {name} pattern differs from the oracle at {idx} "
+                                 f"(gpu {[y_gpu[tuple(i)] for i in idx]}, oracle {[y_ref[tuple(i)] for i in idx]})")
+    fin = ~(nan | pinf | ninf)
     wnorm = np.asarray(wnorm, dtype=np.float64)
     xnorm = np.asarray(xnorm, dtype=np.float64)
-    bound = 1e-2 * (np.outer(xnorm, wnorm) if wnorm.ndim == 1 else xnorm[:, None] * wnorm) / np.sqrt(k)
-    err = np.abs(y_gpu - y_ref)
-    allowed = bound + bf16_half_ulp(y_gpu)
-    bad = err > allowed
-    fro = np.linalg.norm(y_gpu - y_ref) / max(np.linalg.norm(y_ref), 1e-300)
+    with np.errstate(invalid="ignore", over="ignore"):
+        bound = 1e-2 * (np.outer(xnorm, wnorm) if wnorm.ndim == 1 else xnorm[:, None] * wnorm) / np.sqrt(k)
+        bound = np.broadcast_to(bound, y_ref.shape)
+        err = np.abs(np.where(fin, y_gpu, 0.0) - np.where(fin, y_ref, 0.0))
+        allowed = bound + bf16_half_ulp(np.where(fin, y_gpu, 0.0))
+    bad = fin & ~(err <= allowed)
+    d = np.where(fin, y_gpu, 0.0) - np.where(fin, y_ref, 0.0)
+    r = np.where(fin, y_ref, 0.0)
+    fro = np.linalg.norm(d) / max(np.linalg.norm(r), 1e-300)
+    with np.errstate(invalid="ignore", divide="ignore"):
+        ratio = np.where(fin & (bound > 0), err / np.where(bound > 0, bound, 1.0), 0.0)
     stats = dict(max_err=float(err.max(initial=0.0)), n_bad=int(bad.sum()),
-                 literal_over=int((err > bound).sum()), fro=float(fro),
-                 max_ratio=float((err / np.maximum(bound, 1e-300)).max(initial=0.0)))
+                 literal_over=int((fin & (err > bound)).sum()), fro=float(fro),
+                 max_ratio=float(np.nan_to_num(ratio, nan=np.inf).max(initial=0.0)),
+                 n_nonfinite=int((~fin).sum()))
     assert stats["n_bad"] == 0, f"{what}: {stats}"
     assert fro <= 4e-3, f"{what}: {stats}"
     return stats
