@@ -104,6 +104,20 @@ typedef struct qm_weight {
  * Defined by "Nx_quant (raven-ml.dev API docs)", section "Products", dequant. */
 qm_status qm_dequant(const qm_weight* w, int32_t out_dtype, void* out, qm_stream_t stream);
 
+/* quantize_q8_0: x [rows, k] (k a multiple of 32) of x_dtype (QM_F32,
+ * QM_BF16 or QM_F16, read at float32) stored as GGUF Q8_0 blocks
+ * [rows, k/32*34] in `blocks` (caller-allocated, must not overlap x). Per block
+ * of 32 values: a NaN anywhere gives a NaN scale (0x7E00) and quants 0; else
+ * an infinity gives the scale +inf and quants 0; else d = amax / 127 at
+ * float32 (amax the largest magnitude), stored at float16 rounded to nearest
+ * even (past float16's largest: infinity), and quant j = round(v_j * (1 / d)),
+ * halves away from zero, the reciprocal and the products at float32 -- 1 / d
+ * of the float32 d, 0 where d is 0, and a product that is not finite gives 0.
+ * Defined by "Nx_quant (raven-ml.dev API docs)", section "Weights",
+ * val quantize_q8_0. */
+qm_status qm_quantize_q8_0(const void* x, int32_t x_dtype, int64_t rows, int64_t k, void* blocks,
+                           qm_stream_t stream);
+
 /* apply: y [M, n] = x [M, k] times W^T, summed at float32 and rounded once to
  * x's dtype, for a 2-d weight [n, k]. x_dtype must be QM_BF16. M = 0 is valid
  * and launches nothing. x and y must not overlap.

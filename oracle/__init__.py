@@ -10,7 +10,8 @@ over output rows). This module builds it on first use and wraps it for NumPy
 arrays. Format and dtype codes here are the oracle's own:
 
     format: AFFINE = 0 (MLX affine), Q8_0 = 1 (GGUF), MXFP4 = 2 (scales apart),
-            MXFP4_BLOCKS = 3 (MXFP4 in GGUF's 17-byte blocks)
+            MXFP4_BLOCKS = 3 (MXFP4 in GGUF's 17-byte blocks),
+            Q4_K = 4, Q6_K = 5 (GGUF's 256-value super-blocks)
     dtype : F32 = 0, BF16 = 1, F16 = 2   (16-bit data is passed as uint16 bits)
 
 Sources, by page title and section:
@@ -27,7 +28,7 @@ import threading
 
 import numpy as np
 
-AFFINE, Q8_0, MXFP4, MXFP4_BLOCKS = 0, 1, 2, 3
+AFFINE, Q8_0, MXFP4, MXFP4_BLOCKS, Q4_K, Q6_K = 0, 1, 2, 3, 4, 5
 F32, BF16, F16 = 0, 1, 2
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -192,8 +193,8 @@ class Weight:
         self.codes = np.ascontiguousarray(codes)
         self.scales = None if scales is None else np.ascontiguousarray(scales)
         self.biases = None if biases is None else np.ascontiguousarray(biases)
-        self.bits = bits if fmt == AFFINE else (8 if fmt == Q8_0 else 4)
-        self.group_size = group_size if fmt == AFFINE else 32
+        self.bits = bits if fmt == AFFINE else {Q8_0: 8, Q6_K: 6}.get(fmt, 4)
+        self.group_size = group_size if fmt == AFFINE else {Q4_K: 256, Q6_K: 256}.get(fmt, 32)
         self.scale_dtype = scale_dtype
 
     @property

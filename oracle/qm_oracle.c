@@ -21,7 +21,7 @@
  *
  * Conventions shared with the Python wrapper (oracle/__init__.py) only:
  *   format: 0 = MLX affine, 1 = GGUF Q8_0, 2 = MXFP4 (scales apart),
- *           3 = MXFP4 in GGUF's blocks
+ *           3 = MXFP4 in GGUF's blocks, 4 = GGUF Q4_K, 5 = GGUF Q6_K
  *   dtype : 0 = float32, 1 = bfloat16, 2 = float16
  *   An index array is int32 when its `ids64` flag is 0, int64 otherwise.
  *
@@ -219,6 +219,75 @@ static int or_q8_0_q(const uint8_t* block, int t)
     return (int)(int8_t)block[2 + t];
 }
 
+/* GGUF Q4_K ([NXQ] "Weights", Q4_K): 144 bytes per 256 values -- float16 d,
+ * float16 dmin, 12 bytes holding eight 6-bit scales and eight 6-bit mins (one
+ * each per sub-block of 32 values), then 128 bytes of 4-bit quants. The page
+ * gives the fields and their order and defers the arrangement inside them to
+ * ggml's block_q4_K; that arrangement, restated:
+ *   - the 12 bytes as bytes b0..b11: sub-blocks 0..3 take their scale from the
+ *     low 6 bits of b0..b3 and their min from the low 6 bits of b4..b7;
+ *     sub-blocks 4..7 take the low 4 bits of their scale from the low nibble
+ *     of b8..b11 and of their min from its high nibble, and the top 2 bits of
+ *     their scale from the top 2 bits of b0..b3, of their min from the top 2
+ *     bits of b4..b7;
+ *   - the quants in four runs of 32 bytes, run c serving values 64c .. 64c+63:
+ *     its byte l holds value 64c + l in the low nibble (sub-block 2c) and
+ *     value 64c + 32 + l in the high nibble (sub-block 2c + 1).
+ * Value = d * sc * q - dmin * m ([NXQ]), computed as ggml's float32 dequant
+ * computes it, products left to right: every product is exact in float32 and
+ * the value rounds once, at the subtraction ([NXQ] "Products", dequant). */
+static void or_q4_k_sub(const uint8_t* blk, int j, int* sc, int* m)
+{
+    const uint8_t* b = blk + 4;                 /* the 12 scale/min bytes */
+    if (j < 4) {
+        *sc = b[j] & 0x3F;
+        *m = b[4 + j] & 0x3F;
+    } else {
+        *sc = (b[8 + (j - 4)] & 0x0F) | ((b[j - 4] >> 6) << 4);
+        *m = (b[8 + (j - 4)] >> 4) | ((b[j] >> 6) << 4);
+    }
+}
+
+static float or_q4_k_value(const uint8_t* blk, int i)
+{
+    double d = or_f16_to_f64((uint16_t)(blk[0] | (blk[1] << 8)));
+    double dmin = or_f16_to_f64((uint16_t)(blk[2] | (blk[3] << 8)));
+    int c = i / 64, r = i % 64;
+    int j = 2 * c + (r >= 32);                  /* sub-block */
+    uint8_t byte = blk[16 + 32 * c + (r % 32)];
+    int q = (r < 32) ? (byte & 0x0F) : (byte >> 4);
+    int sc, m;
+    or_q4_k_sub(blk, j, &sc, &m);
+    /* d * sc * q and dmin * m are exact in float64 and their difference too
+     * (at most 50 bits apart): the cast is the one rounding */
+    return (float)(d * sc * q - dmin * m);
+}
+
+/* GGUF Q6_K ([NXQ] "Weights", Q6_K): 210 bytes per 256 values -- 128 bytes of
+ * the quants' low 4 bits (ql), 64 bytes of their high 2 bits (qh), sixteen
+ * int8 scales (one per sub-block of 16 values), then float16 d. The
+ * arrangement inside the fields (ggml's block_q6_K), restated: the block is two
+ * halves of 128 values, half h using ql[64h .. 64h+63], qh[32h .. 32h+31] and
+ * scales[8h .. 8h+7]; within a half, value 32t + l (t = 0..3, l = 0..31) has
+ * its low 4 bits in ql[64h + l + 32(t mod 2)] (the low nibble for t < 2, the
+ * high one for t >= 2), its high 2 bits in bits 2t, 2t+1 of qh[32h + l], and
+ * the scale scales[8h + 2t + l/16]. Value = d * sc * (q - 32) ([NXQ]), exact
+ * in float32. */
+static float or_q6_k_value(const uint8_t* blk, int i)
+{
+    const uint8_t* ql = blk;
+    const uint8_t* qh = blk + 128;
+    const int8_t* scales = (const int8_t*)(blk + 192);
+    double d = or_f16_to_f64((uint16_t)(blk[208] | (blk[209] << 8)));
+    int h = i / 128, r = i % 128, t = r / 32, l = r % 32;
+    uint8_t lo_byte = ql[64 * h + l + 32 * (t % 2)];
+    int lo = (t < 2) ? (lo_byte & 0x0F) : (lo_byte >> 4);
+    int hi = (qh[32 * h + l] >> (2 * t)) & 3;
+    int q = lo | (hi << 4);
+    int sc = scales[8 * h + 2 * t + l / 16];
+    return (float)(d * sc * (q - 32));
+}
+
 /* Float32 values of row r (of `rows`) of a weight, k of them, into v[k]. */
 void or_row_values(int fmt, int bits, int gs, int sdt, int64_t k,
                    const void* codes, const void* scales, const void* biases,
@@ -240,6 +309,14 @@ void or_row_values(int fmt, int bits, int gs, int sdt, int64_t k,
             const uint8_t* blk = rb + (i / 32) * 34;
             v[i] = (float)(or_q8_0_d(blk) * (double)or_q8_0_q(blk, (int)(i % 32)));
         }
+    } else if (fmt == 4) {                            /* GGUF Q4_K */
+        const uint8_t* rb = (const uint8_t*)codes + r * (k / 256) * 144;
+        for (int64_t i = 0; i < k; ++i)
+            v[i] = or_q4_k_value(rb + (i / 256) * 144, (int)(i % 256));
+    } else if (fmt == 5) {                            /* GGUF Q6_K */
+        const uint8_t* rb = (const uint8_t*)codes + r * (k / 256) * 210;
+        for (int64_t i = 0; i < k; ++i)
+            v[i] = or_q6_k_value(rb + (i / 256) * 210, (int)(i % 256));
     } else if (fmt == 3) {                            /* MXFP4 in GGUF's blocks */
         const uint8_t* rb = (const uint8_t*)codes + r * (k / 32) * 17;
         for (int64_t i = 0; i < k; ++i) {

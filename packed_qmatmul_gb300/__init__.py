@@ -22,10 +22,10 @@ import torch
 __all__ = [
     "QM_AFFINE", "QM_Q8_0", "QM_MXFP4", "QM_MXFP4_BLOCKS", "QM_WEIGHT_STATIC", "QM_F32", "QM_BF16", "QM_F16", "QM_I32", "QM_I64",
     "QMError", "QWeight", "library_path", "load_library",
-    "qm_dequant", "qm_apply", "qm_take", "qm_apply_experts", "qm_apply_experts_workspace",
+    "qm_dequant", "qm_quantize_q8_0", "qm_apply", "qm_take", "qm_apply_experts", "qm_apply_experts_workspace",
     "qm_experts_route_workspace",
     "qm_experts_route", "qm_apply_experts_static", "qm_device_status", "qm_last_error", "qm_version",
-    "dequant", "apply", "take", "apply_experts", "route",
+    "dequant", "quantize_q8_0", "apply", "take", "apply_experts", "route",
 ]
 
 QM_OK, QM_EINVAL, QM_ECUDA, QM_ETIMEOUT, QM_ENOTSUP = 0, 1, 2, 3, 4
@@ -83,6 +83,7 @@ def load_library():
         wp = ctypes.POINTER(_CWeight)
         sigs = {
             "qm_dequant": ([wp, i32, vp, vp], i32),
+            "qm_quantize_q8_0": ([vp, i32, i64, i64, vp, vp], i32),
             "qm_apply": ([wp, vp, i64, i32, vp, vp], i32),
             "qm_take": ([wp, i32, vp, i32, i64, vp, vp, vp, i32, vp, vp], i32),
             "qm_apply_experts_workspace": ([wp, i64, i64], sz),
@@ -214,6 +215,13 @@ def qm_dequant(w: QWeight, out: torch.Tensor, stream=None) -> None:
                                      _stream(stream)))
 
 
+def qm_quantize_q8_0(x: torch.Tensor, blocks: torch.Tensor, stream=None) -> None:
+    k = x.shape[-1]
+    rows = x.numel() // k if k else 0
+    _check(load_library().qm_quantize_q8_0(_ptr(x), _DTYPES[x.dtype], rows, k, _ptr(blocks),
+                                           _stream(stream)))
+
+
 def qm_apply(w: QWeight, x: torch.Tensor, y: torch.Tensor, stream=None) -> None:
     M = x.shape[0] if x.dim() == 2 else 1
     _check(load_library().qm_apply(w._ref(), _ptr(x), M, _DTYPES[x.dtype], _ptr(y),
@@ -273,6 +281,14 @@ def dequant(w: QWeight, dtype=torch.bfloat16, stream=None) -> torch.Tensor:
     out = torch.empty(w.shape, dtype=dtype, device=w.codes.device)
     qm_dequant(w, out, stream)
     return out
+
+
+def quantize_q8_0(x: torch.Tensor, stream=None) -> QWeight:
+    """The float weight x [..., n, k] (float32, bfloat16 or float16) stored as GGUF Q8_0."""
+    k = x.shape[-1]
+    blocks = torch.empty(tuple(x.shape[:-1]) + (k // 32 * 34,), dtype=torch.uint8, device=x.device)
+    qm_quantize_q8_0(x, blocks, stream)
+    return QWeight("q8_0", tuple(x.shape), blocks)
 
 
 def apply(w: QWeight, x: torch.Tensor, stream=None) -> torch.Tensor:

@@ -104,8 +104,8 @@ qm_status validate_weight(const qm_weight* w, WDesc* d) {
     if (k % 32 != 0) return fail(QM_EINVAL, "codes: k = " + std::to_string(k) + " is not a multiple of 32");
 
     if (w->format == QM_AFFINE) {
-        if (w->bits != 4 && w->bits != 8)
-            return fail(QM_EINVAL, "w: affine bits must be 4 or 8, got " + std::to_string(w->bits));
+        if (w->bits != 2 && w->bits != 3 && w->bits != 4 && w->bits != 5 && w->bits != 6 && w->bits != 8)
+            return fail(QM_EINVAL, "w: affine bits must be 2, 3, 4, 5, 6 or 8, got " + std::to_string(w->bits));
         if (w->group_size != 32 && w->group_size != 64 && w->group_size != 128)
             return fail(QM_EINVAL, "w: affine group_size must be 32, 64 or 128, got " +
                                        std::to_string(w->group_size));
@@ -236,6 +236,28 @@ qm_status qm_dequant(const qm_weight* w, int32_t out_dtype, void* out, qm_stream
                         "dequant launch");
 }
 
+qm_status qm_quantize_q8_0(const void* x, int32_t x_dtype, int64_t rows, int64_t k, void* blocks,
+                           qm_stream_t stream) {
+    set_error("");
+    if (x_dtype != QM_F32 && x_dtype != QM_BF16 && x_dtype != QM_F16)
+        return fail(QM_EINVAL, "x: dtype must be QM_F32, QM_BF16 or QM_F16");
+    if (rows < 0 || k < 0) return fail(QM_EINVAL, "x: negative shape");
+    if (k % 32 != 0) return fail(QM_EINVAL, "x: k = " + std::to_string(k) + " is not a multiple of 32");
+    int64_t n = 0;
+    if (!mul_ok(rows, k, &n)) return fail(QM_EINVAL, "x: shape too large");
+    if (n == 0) return QM_OK;
+    if (!x) return fail(QM_EINVAL, "x: NULL");
+    if (!aligned16(x)) return fail(QM_EINVAL, "x: base address must be 16-byte aligned");
+    if (!blocks) return fail(QM_EINVAL, "out: NULL");
+    if (!aligned16(blocks)) return fail(QM_EINVAL, "out: base address must be 16-byte aligned");
+    const char* xb = static_cast<const char*>(x);
+    const char* ob = static_cast<const char*>(blocks);
+    if (xb < ob + n / 32 * 34 && ob < xb + n * dtype_size(x_dtype)) return fail(QM_EINVAL, "out: overlaps x");
+    return check_launch(launch_quantize_q8_0(x, x_dtype, rows, k, static_cast<uint8_t*>(blocks),
+                                             reinterpret_cast<cudaStream_t>(stream)),
+                        "quantize launch");
+}
+
 qm_status qm_apply(const qm_weight* w, const void* x, int64_t M, int32_t x_dtype, void* y,
                    qm_stream_t stream) {
     set_error("");
@@ -258,6 +280,12 @@ qm_status qm_apply(const qm_weight* w, const void* x, int64_t M, int32_t x_dtype
     const char* xb = static_cast<const char*>(x);
     const char* yb = static_cast<const char*>(y);
     if (xb < yb + M * d.n * 2 && yb < xb + M * d.k * 2) return fail(QM_EINVAL, "y: overlaps x");
+    // one token: the register kernel for weights up to 24 MB (a dependent chain of
+    // such products is latency-bound); larger weights stream through the
+    // tensor-map pipeline, which keeps more bytes in flight
+    const bool small = d.n * d.code_row_bytes + d.n * (d.scale_row_bytes + d.bias_row_bytes) <= (int64_t(24) << 20);
+    if (M == 1 && gemv1_supported(d) && (small || !gemv_supported(d, 1)))
+        return check_launch(launch_gemv1(d, x, y, st), "gemv launch");
     if (M <= 16 && gemv_supported(d, M)) return launch_gemv(d, x, M, y, st);
     if (gemm_supported(d, M)) return launch_gemm(d, x, M, y, st);
     return check_launch(launch_apply_simple(d, x, M, y, st), "apply launch");

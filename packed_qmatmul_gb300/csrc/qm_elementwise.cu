@@ -53,7 +53,21 @@ QM_DEV void decode_unit(const DecodeArgs& a, int64_t r, int64_t u, float (&v)[32
         const float s = scale_val(a.scales, r * ng + g, a.sdt);
         const float b = scale_val(a.biases, r * ng + g, a.sdt);
         const uint4* src = reinterpret_cast<const uint4*>(a.codes + r * a.code_row_bytes + u * 4 * BITS);
-        if constexpr (BITS == 4) {
+        if constexpr (BITS != 4 && BITS != 8) {
+            // 2, 3, 5, 6 bits: the unit's BITS words (4-byte aligned), codes read
+            // across word boundaries from the little-endian bit stream
+            const uint32_t* wp = reinterpret_cast<const uint32_t*>(a.codes + r * a.code_row_bytes + u * 4 * BITS);
+            uint32_t w[BITS];
+#pragma unroll
+            for (int j = 0; j < BITS; ++j) w[j] = __ldg(wp + j);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+                const int bit = i * BITS, q = bit >> 5, sh = bit & 31;
+                uint32_t c = w[q] >> sh;
+                if (sh + BITS > 32) c |= w[q + 1] << (32 - sh);
+                v[i] = fmaf(static_cast<float>(c & ((1u << BITS) - 1u)), s, b);
+            }
+        } else if constexpr (BITS == 4) {
             const uint4 q = __ldg(src);
             const uint32_t w[4] = {q.x, q.y, q.z, q.w};
 #pragma unroll
@@ -204,7 +218,11 @@ cudaError_t launch_decode_rows(const WDesc& w, int64_t out_rows, Map map, int ou
                           out_rows, map, out);                                                  \
     }
 #define QM_DECODE_OUTS(F, B) QM_DECODE_CASE(F, B, QM_F32) QM_DECODE_CASE(F, B, QM_BF16) QM_DECODE_CASE(F, B, QM_F16)
+    QM_DECODE_OUTS(QM_AFFINE, 2)
+    QM_DECODE_OUTS(QM_AFFINE, 3)
     QM_DECODE_OUTS(QM_AFFINE, 4)
+    QM_DECODE_OUTS(QM_AFFINE, 5)
+    QM_DECODE_OUTS(QM_AFFINE, 6)
     QM_DECODE_OUTS(QM_AFFINE, 8)
     QM_DECODE_OUTS(QM_Q8_0, 8)
     QM_DECODE_OUTS(QM_MXFP4, 4)
@@ -248,6 +266,66 @@ __global__ void __launch_bounds__(256) take_packed_kernel(TakeParts tp, int64_t 
 }
 
 }  // namespace
+
+// ------------------------------------------------------------ quantize_q8_0
+// "Nx_quant (raven-ml.dev API docs)", val quantize_q8_0: x read at float32,
+// per block of 32 values d = amax / 127 (amax over the finite values) stored at
+// float16 rounded to nearest, and quant j = round(v_j * (1 / d)), halves away
+// from zero, the reciprocal and products at float32 (1 / d = 0 where d is 0,
+// and a product that is not finite gives the quant 0). A block holding a NaN
+// has a NaN scale and quants 0; else one holding an infinity has the scale +inf
+// and quants 0. One warp per block, lane j holding value j: the loads of a
+// block are one 128-byte line and its 34 bytes are one coalesced store.
+namespace {
+template <int XDT>
+QM_DEV float load_f32(const void* x, int64_t i) {
+    if constexpr (XDT == QM_F32) return __ldg(static_cast<const float*>(x) + i);
+    else if constexpr (XDT == QM_BF16) return bf16_bits_to_f32(__ldg(static_cast<const uint16_t*>(x) + i));
+    else return f16_bits_to_f32(__ldg(static_cast<const uint16_t*>(x) + i));
+}
+
+template <int XDT>
+__global__ void __launch_bounds__(256) quantize_q8_0_kernel(const void* x, int64_t nblocks, uint8_t* blocks) {
+    grid_launch_dependents();
+    grid_dependency_wait();
+    const int lane = threadIdx.x & 31;
+    const int64_t nw = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    for (int64_t b = (blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x) >> 5; b < nblocks; b += nw) {
+        const float v = load_f32<XDT>(x, b * 32 + lane);
+        const bool has_nan = __any_sync(0xffffffffu, isnan(v));
+        const bool has_inf = __any_sync(0xffffffffu, isinf(v));
+        // amax over the finite values: magnitude bits of non-negative floats order as the values
+        const uint32_t mag = isfinite(v) ? (__float_as_uint(v) & 0x7FFFFFFFu) : 0u;
+        const float amax = __uint_as_float(__reduce_max_sync(0xffffffffu, mag));
+        uint16_t h;
+        int8_t q = 0;
+        if (has_nan || has_inf) {
+            h = has_nan ? 0x7E00 : 0x7C00;
+        } else {
+            const float d = __fdiv_rn(amax, 127.0f);
+            const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
+            h = __half_as_ushort(__float2half_rn(d));
+            const float p = __fmul_rn(v, id);
+            q = isfinite(p) ? static_cast<int8_t>(roundf(p)) : static_cast<int8_t>(0);
+        }
+        uint8_t* out = blocks + b * 34;
+        if (lane < 2) out[lane] = static_cast<uint8_t>(lane == 0 ? (h & 0xFF) : (h >> 8));  // little-endian d
+        out[2 + lane] = static_cast<uint8_t>(q);
+    }
+}
+}  // namespace
+
+cudaError_t launch_quantize_q8_0(const void* x, int x_dtype, int64_t rows, int64_t k, uint8_t* blocks,
+                                 cudaStream_t st) {
+    const int64_t nblocks = rows * (k / 32);
+    if (nblocks == 0) return cudaSuccess;
+    const int64_t grid = std::min<int64_t>((nblocks + 7) / 8, int64_t(num_sms()) * 16);
+    if (x_dtype == QM_F32)
+        return launch_pdl(quantize_q8_0_kernel<QM_F32>, static_cast<unsigned>(grid), 256, 0, st, x, nblocks, blocks);
+    if (x_dtype == QM_BF16)
+        return launch_pdl(quantize_q8_0_kernel<QM_BF16>, static_cast<unsigned>(grid), 256, 0, st, x, nblocks, blocks);
+    return launch_pdl(quantize_q8_0_kernel<QM_F16>, static_cast<unsigned>(grid), 256, 0, st, x, nblocks, blocks);
+}
 
 cudaError_t launch_dequant(const WDesc& w, int out_dtype, void* out, cudaStream_t st) {
     return launch_decode_rows(w, w.rows, IdentityMap{}, out_dtype, out, st);
@@ -333,10 +411,14 @@ cudaError_t launch_apply_simple(const WDesc& w, const void* x, int64_t M, void* 
     const int64_t blocks = std::min<int64_t>((jobs * 32 + 255) / 256, int64_t(num_sms()) * 8);
     const uint16_t* xb = static_cast<const uint16_t*>(x);
     uint16_t* yb = static_cast<uint16_t*>(y);
-    if (w.fmt == QM_AFFINE && w.bits == 4)
-        apply_simple_kernel<QM_AFFINE, 4><<<static_cast<unsigned>(blocks), 256, 0, st>>>(a, w.n, xb, M, yb);
-    else if (w.fmt == QM_AFFINE)
-        apply_simple_kernel<QM_AFFINE, 8><<<static_cast<unsigned>(blocks), 256, 0, st>>>(a, w.n, xb, M, yb);
+#define QM_SIMPLE(B) apply_simple_kernel<QM_AFFINE, B><<<static_cast<unsigned>(blocks), 256, 0, st>>>(a, w.n, xb, M, yb)
+    if (w.fmt == QM_AFFINE && w.bits == 2) QM_SIMPLE(2);
+    else if (w.fmt == QM_AFFINE && w.bits == 3) QM_SIMPLE(3);
+    else if (w.fmt == QM_AFFINE && w.bits == 4) QM_SIMPLE(4);
+    else if (w.fmt == QM_AFFINE && w.bits == 5) QM_SIMPLE(5);
+    else if (w.fmt == QM_AFFINE && w.bits == 6) QM_SIMPLE(6);
+    else if (w.fmt == QM_AFFINE) QM_SIMPLE(8);
+#undef QM_SIMPLE
     else if (w.fmt == QM_Q8_0)
         apply_simple_kernel<QM_Q8_0, 8><<<static_cast<unsigned>(blocks), 256, 0, st>>>(a, w.n, xb, M, yb);
     else if (w.fmt == QM_MXFP4_BLOCKS)

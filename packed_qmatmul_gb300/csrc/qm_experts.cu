@@ -207,7 +207,11 @@ template <int FMT, int BITS>
 QM_DEV float value_at(const ExpArgs& a, int64_t r, int64_t i) {
     if constexpr (FMT == QM_AFFINE) {
         const uint32_t* row = reinterpret_cast<const uint32_t*>(a.codes + r * a.code_row_bytes);
-        const uint32_t c = (row[(i * BITS) / 32] >> ((i * BITS) % 32)) & ((1u << BITS) - 1u);
+        const int64_t bit = i * BITS;
+        const int sh = static_cast<int>(bit % 32);
+        uint32_t c = row[bit / 32] >> sh;
+        if (sh + BITS > 32) c |= row[bit / 32 + 1] << (32 - sh);  // a code across two words
+        c &= (1u << BITS) - 1u;
         const int64_t ng = a.k / a.gs;
         return fmaf(static_cast<float>(c), scale_val(a.scales, r * ng + i / a.gs, a.sdt),
                     scale_val(a.biases, r * ng + i / a.gs, a.sdt));
@@ -340,7 +344,11 @@ qm_status launch_experts(const WDesc& w, const void* ids, int id64, int64_t T, i
     experts_simple_kernel<F, B><<<static_cast<unsigned>(blocks), 256, 0, st>>>(a, ids, id64, P, topk, T, \
                                                                                xb, x_rows, perm, \
                                                                                offsets, yb)
-    if (w.fmt == QM_AFFINE && w.bits == 4) QM_EXP_CASE(QM_AFFINE, 4);
+    if (w.fmt == QM_AFFINE && w.bits == 2) QM_EXP_CASE(QM_AFFINE, 2);
+    else if (w.fmt == QM_AFFINE && w.bits == 3) QM_EXP_CASE(QM_AFFINE, 3);
+    else if (w.fmt == QM_AFFINE && w.bits == 4) QM_EXP_CASE(QM_AFFINE, 4);
+    else if (w.fmt == QM_AFFINE && w.bits == 5) QM_EXP_CASE(QM_AFFINE, 5);
+    else if (w.fmt == QM_AFFINE && w.bits == 6) QM_EXP_CASE(QM_AFFINE, 6);
     else if (w.fmt == QM_AFFINE) QM_EXP_CASE(QM_AFFINE, 8);
     else if (w.fmt == QM_Q8_0) QM_EXP_CASE(QM_Q8_0, 8);
     else if (w.fmt == QM_MXFP4_BLOCKS) QM_EXP_CASE(QM_MXFP4_BLOCKS, 4);

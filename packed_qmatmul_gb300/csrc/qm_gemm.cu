@@ -57,11 +57,14 @@ constexpr int NR = 2;           // raw chunk slots
 
 // Raw chunk geometry per format: values per chunk, bytes per row per chunk,
 // whether the TMA box is 128B-swizzled, and the tensor map's element size.
+// Affine 2, 3, 5 and 6-bit codes (GEN) come as 128 inputs per row, 16 * BITS
+// bytes, unswizzled (a row's codes then start on a 4-byte boundary).
 template <int FMT, int BITS>
 struct Raw {
-    static constexpr int RAWK = (FMT == QM_AFFINE && BITS == 8) ? 128 : 256;
-    static constexpr int BYTES = (FMT == QM_Q8_0) ? 272 : 128;
-    static constexpr bool SW = FMT != QM_Q8_0;
+    static constexpr bool GEN = FMT == QM_AFFINE && BITS != 4 && BITS != 8;
+    static constexpr int RAWK = (GEN || (FMT == QM_AFFINE && BITS == 8)) ? 128 : 256;
+    static constexpr int BYTES = GEN ? 16 * BITS : (FMT == QM_Q8_0) ? 272 : 128;
+    static constexpr bool SW = FMT != QM_Q8_0 && !GEN;
     static constexpr int ELEM = (FMT == QM_Q8_0) ? 2 : 1;
     static constexpr int SPR = RAWK / BK;  // k steps per chunk
 };
@@ -75,6 +78,7 @@ struct Params {
     int64_t M, n, k;
     int64_t scale_row_bytes;
     int sdt;
+    int gshift;  // log2(group_size) of an affine weight
     int ksteps, mtiles, ntiles;
     uint32_t off_x, off_raw, raw_stage_bytes;
     // split k (plain products with few tiles): a cluster of `splitk` CTAs takes
@@ -113,8 +117,8 @@ QM_DEV Sc load_scale(const Params& p, int64_t grow, int64_t vidx) {
     Sc r{0.0f, 0.0f};
     if (vidx >= p.k) return r;
     if constexpr (FMT == QM_AFFINE) {
-        const int64_t ng = p.k / GS;
-        const int64_t g = vidx / GS;
+        const int64_t ng = p.k >> p.gshift;
+        const int64_t g = vidx >> p.gshift;
         r.s = sval(__ldg(reinterpret_cast<const uint16_t*>(p.scales) + grow * ng + g), p.sdt);
         r.b = sval(__ldg(reinterpret_cast<const uint16_t*>(p.biases) + grow * ng + g), p.sdt);
     } else if constexpr (FMT == QM_MXFP4) {
@@ -162,7 +166,27 @@ QM_DEV void decode_q8_block(const uint8_t* raw, int row, uint32_t (&o)[16]) {
 // the chunk) as 16 bf16 pairs, from the raw chunk in shared memory.
 template <int FMT, int BITS, int GS>
 QM_DEV void decode32(const uint8_t* raw, int row, int kk, int half, Sc sc, uint32_t (&o)[16]) {
-    if constexpr (FMT == QM_AFFINE) {
+    if constexpr (Raw<FMT, BITS>::GEN) {
+        // BITS words of a little-endian code stream; codes may cross words
+        const uint32_t* wp = reinterpret_cast<const uint32_t*>(raw + row * (16 * BITS) + (kk * 64 + half * 32) * BITS / 8);
+        uint32_t w[BITS];
+#pragma unroll
+        for (int j = 0; j < BITS; ++j) w[j] = wp[j];
+        const float2 neg = make_float2(-8388608.0f, -8388608.0f);
+        const float2 s2 = make_float2(sc.s, sc.s), b2 = make_float2(sc.b, sc.b);
+        auto code = [&](int i) {
+            const int bit = i * BITS, q = bit >> 5, sh = bit & 31;
+            uint32_t c = w[q] >> sh;
+            if (sh + BITS > 32) c |= w[q + 1] << (32 - sh);
+            return c & ((1u << BITS) - 1u);
+        };
+#pragma unroll
+        for (int i = 0; i < 32; i += 2) {
+            const float2 f = make_float2(magic_f(code(i)), magic_f(code(i + 1)));
+            const float2 v = fma2(add2(f, neg), s2, b2);  // exact code, then one rounding
+            o[i / 2] = bf2(v.x, v.y);
+        }
+    } else if constexpr (FMT == QM_AFFINE) {
         const float2 neg = make_float2(-8388608.0f, -8388608.0f);
         const float2 s2 = make_float2(sc.s, sc.s), b2 = make_float2(sc.b, sc.b);
         constexpr int PER = 32 / BITS;       // codes per word
@@ -660,6 +684,14 @@ static cudaError_t launch_bm(Params& p, const WDesc& w, const void* x, cudaStrea
 }
 
 static cudaError_t dispatch(Params& p, const WDesc& w, const void* x, cudaStream_t st) {
+    p.gshift = 0;
+    while ((1 << p.gshift) < w.gs) ++p.gshift;
+    // the group size reaches the kernel as p.gshift; the 4- and 8-bit kernels
+    // keep their per-size instantiations, the other widths share one
+    if (w.fmt == QM_AFFINE && w.bits == 2) return launch_bm<QM_AFFINE, 2, 0>(p, w, x, st);
+    if (w.fmt == QM_AFFINE && w.bits == 3) return launch_bm<QM_AFFINE, 3, 0>(p, w, x, st);
+    if (w.fmt == QM_AFFINE && w.bits == 5) return launch_bm<QM_AFFINE, 5, 0>(p, w, x, st);
+    if (w.fmt == QM_AFFINE && w.bits == 6) return launch_bm<QM_AFFINE, 6, 0>(p, w, x, st);
     if (w.fmt == QM_AFFINE && w.bits == 4 && w.gs == 32) return launch_bm<QM_AFFINE, 4, 32>(p, w, x, st);
     if (w.fmt == QM_AFFINE && w.bits == 4 && w.gs == 64) return launch_bm<QM_AFFINE, 4, 64>(p, w, x, st);
     if (w.fmt == QM_AFFINE && w.bits == 4 && w.gs == 128) return launch_bm<QM_AFFINE, 4, 128>(p, w, x, st);
@@ -674,7 +706,7 @@ static cudaError_t dispatch(Params& p, const WDesc& w, const void* x, cudaStream
 }  // namespace gemm
 
 bool gemm_supported(const WDesc& w, int64_t M) {
-    if (M < 1 || w.ndim != 2 || w.n < 1 || w.k < 64 || !pipelined_format(w.fmt)) return false;
+    if (M < 1 || w.ndim != 2 || w.n < 1 || w.k < 64 || !gemm_format(w)) return false;
     if (w.code_row_bytes % 16) return false;  // TMA row stride
     if (M > (int64_t(1) << 31) || w.n > (int64_t(1) << 31)) return false;
     return true;
@@ -702,7 +734,7 @@ qm_status launch_gemm(const WDesc& w, const void* x, int64_t M, void* y, cudaStr
 }
 
 bool gemm_grouped_supported(const WDesc& w, int64_t P) {
-    if (w.ndim != 3 || w.shape[0] < 1 || w.n < 1 || w.k < 64 || P < 1 || !pipelined_format(w.fmt)) return false;
+    if (w.ndim != 3 || w.shape[0] < 1 || w.n < 1 || w.k < 64 || P < 1 || !gemm_format(w)) return false;
     if (w.code_row_bytes % 16 || (w.k * 2) % 16) return false;  // TMA row strides
     if (P >= (int64_t(1) << 31) || w.rows >= (int64_t(1) << 31)) return false;
     return true;

@@ -773,6 +773,30 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
                     }
                 }
             };
+            // a tile's scales (and biases) as float32 from their raw bits, and
+            // whether the group is exceptional for the tile's rows: its values are,
+            // or may be, infinite, or an activation is (a NaN scale or bias needs
+            // no exception: it makes every value of its group NaN, and the scaled
+            // sum NaN too)
+            auto scales_of = [&](const uint32_t (&r)[4], float& s0, float& s8, float& b0, float& b8) -> bool {
+                b0 = b8 = 0.0f;
+                if constexpr (FMT == QM_AFFINE) {
+                    s0 = sval<SDT>(r[0]);
+                    s8 = sval<SDT>(r[1]);
+                    b0 = sval<SDT>(r[2]);
+                    b8 = sval<SDT>(r[3]);
+                    // |code * s + b| < 2^128 whenever |s|, |b| < 2^119 (codes < 2^8)
+                    return fmaxf(fmaxf(fabsf(s0), fabsf(s8)), fmaxf(fabsf(b0), fabsf(b8))) >= 0x1p119f;
+                } else if constexpr (FMT == QM_Q8_0) {
+                    s0 = f16_bits_to_f32(r[0]);
+                    s8 = f16_bits_to_f32(r[1]);
+                    return fmaxf(fabsf(s0), fabsf(s8)) > 0x1p127f;  // an infinite d
+                } else {
+                    e8m0x2_to_f32(r[0] | (r[1] << 8), s0, s8);
+                    return max(r[0], r[1]) >= 253u;  // values that may pass float32's range
+                }
+            };
+            bool any_exc = xbad;
             auto epilogue = [&](int gi, const float (&acc)[2][NT][4], const uint32_t (&raw)[2][4]) {
                 float4 td[NT];  // (O[2t], X[2t], O[2t+1], X[2t+1]) per token half
                 if constexpr (FMT != QM_MXFP4) {
@@ -782,42 +806,10 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
                 }
 #pragma unroll
                 for (int tt = 0; tt < 2; ++tt) {
-                    float s0, s8, b0 = 0.0f, b8 = 0.0f;
-                    bool exc = xbad;
-                    if constexpr (FMT == QM_AFFINE) {
-                        s0 = sval<SDT>(raw[tt][0]);
-                        s8 = sval<SDT>(raw[tt][1]);
-                        b0 = sval<SDT>(raw[tt][2]);
-                        b8 = sval<SDT>(raw[tt][3]);
-                        // |code * s + b| < 2^128 whenever |s|, |b| < 2^119 (codes < 2^8)
-                        exc |= fmaxf(fmaxf(fabsf(s0), fabsf(s8)), fmaxf(fabsf(b0), fabsf(b8))) >= 0x1p119f;
-                    } else if constexpr (FMT == QM_Q8_0) {
-                        s0 = f16_bits_to_f32(raw[tt][0]);
-                        s8 = f16_bits_to_f32(raw[tt][1]);
-                        exc |= fmaxf(fabsf(s0), fabsf(s8)) > 0x1p127f;  // an infinite d
-                    } else {
-                        e8m0x2_to_f32(raw[tt][0] | (raw[tt][1] << 8), s0, s8);
-                        exc |= max(raw[tt][0], raw[tt][1]) >= 253u;  // values that may pass float32's range
-                    }
-                    // (a NaN scale or bias needs no exception: it makes every
-                    // value of its group NaN, and the scaled sum NaN too)
-                    if (exc) {
-                        const CodeRow& ra = rows_[2 * tt];
-                        const CodeRow& rb = rows_[2 * tt + 1];
-#pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                const int m = nt * 8 + 2 * t + h;
-                                if ((ONE && (t != 0 || h != 0)) || m >= M) continue;
-                                const int64_t xr = p.g_off ? s_xrow[m] : m;
-                                const float2 e = group_exact<FMT, BITS, GS>(ra, rb, gi, s0, b0, s8, b8,
-                                                                            p.x + xr * p.k + xk0 + gi * GS);
-                                y[tt][nt][h] += e.x;
-                                y[tt][nt][2 + h] += e.y;
-                            }
-                        continue;
-                    }
+                    float s0, s8, b0, b8;
+                    const bool exc = scales_of(raw[tt], s0, s8, b0, b8);
+                    any_exc |= exc;
+                    if (exc || xbad) continue;  // summed per element after the stage's groups
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         float* yv = y[tt][nt];
@@ -843,6 +835,33 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
                     }
                 }
             };
+            // the exceptional groups of this lane's tiles, element by element
+            // (rare: kept out of the streaming loop)
+            auto exact_pass = [&](int g0, int g1) {
+                #pragma unroll 1
+                for (int gi = g0; gi < g1; ++gi) {
+                    uint32_t raw[2][4];
+                    ep_load(gi, raw);
+                    // (every index into y a constant, so y stays in registers)
+#pragma unroll
+                    for (int tt = 0; tt < 2; ++tt) {
+                        float s0, s8, b0, b8;
+                        if (!scales_of(raw[tt], s0, s8, b0, b8) && !xbad) continue;
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                            for (int h = 0; h < 2; ++h) {
+                                const int m = nt * 8 + 2 * t + h;
+                                if ((ONE && (t != 0 || h != 0)) || m >= M) continue;
+                                const int64_t xr = p.g_off ? s_xrow[m] : m;
+                                const float2 e = group_exact<FMT, BITS, GS>(rows_[2 * tt], rows_[2 * tt + 1], gi, s0, b0,
+                                                                            s8, b8, p.x + xr * p.k + xk0 + gi * GS);
+                                y[tt][nt][h] += e.x;
+                                y[tt][nt][2 + h] += e.y;
+                            }
+                    }
+                }
+            };
             // groups two at a time: four independent MMA chains in flight
             const int gend = live ? ge : gb;
             int gi = gb;
@@ -864,6 +883,7 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
                 do_group(gi, acc0);
                 epilogue(gi, acc0, raw0);
             }
+            if (any_exc) exact_pass(gb, gend);  // before the stage's slot is released
             __syncwarp();
             if (lane == 0 && live) mbar_arrive(bar_empty0 + 8 * slot);
 
@@ -1302,7 +1322,7 @@ static const Prepared* prepared(const WDesc& w, int64_t M, cudaError_t* err = nu
 }  // namespace gemv
 
 bool gemv_supported(const WDesc& w, int64_t M) {
-    if (M < 1 || M > 16 || w.ndim != 2 || !pipelined_format(w.fmt)) return false;
+    if (M < 1 || M > 16 || w.ndim != 2 || !pipelined_format(w)) return false;
     const gemv::Prepared* pr = gemv::prepared(w, M);
     return pr && pr->pl.ok;
 }
@@ -1354,7 +1374,7 @@ static int grouped_q(int64_t P, int64_t E) { return P <= 8 * E ? 8 : 16; }
 
 static bool grouped_plan(const WDesc& w, int64_t P, Plan* out, int64_t* slots) {
     const int64_t E = w.shape[0];
-    if (w.ndim != 3 || E < 1 || P < 1 || E * w.n >= (int64_t(1) << 31) || !pipelined_format(w.fmt)) return false;
+    if (w.ndim != 3 || E < 1 || P < 1 || E * w.n >= (int64_t(1) << 31) || !pipelined_format(w)) return false;
     if ((w.n * w.scale_row_bytes) % 16) return false;  // each expert's scales start 16-byte aligned
     const int Q = grouped_q(P, E);
     *slots = std::min<int64_t>(P, P / Q + E);  // sum over experts of ceil(count / Q) is below P/Q + E

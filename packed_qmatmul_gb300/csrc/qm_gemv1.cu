@@ -1,0 +1,464 @@
+// qm_gemv1.cu -- the one-token product y[1, n] = x[1, k] * W^T over packed
+// weights: the decode step's product, bound by launch latency for small
+// layers and by HBM bandwidth for large ones.
+//
+// The product is the one "Nx_quant (raven-ml.dev API docs)", section
+// "Products", val apply, defines: x times the weight's float32 values, summed
+// at float32 and rounded once to x's dtype. Each lane sums the products of its
+// own codes (exact small integers) with its activations, then scales the sum
+// by its block's scale (and adds bias times the activations' sum): every
+// product is exact, so the only roundings are float32 sums.
+//
+// Design (one GB300: 152 SMs):
+//  * No shared memory, no barrier, no activation prologue: a warp owns R rows
+//    and all of k; lane l holds inputs [1024c + 32l, 1024c + 32l + 32) of
+//    every chunk c of 1024 inputs, reads its codes straight into registers
+//    (16-byte loads where the layout allows) and its 32 activations, and the
+//    warp adds its lanes' partial sums with shuffles.
+//  * Codes become exact float32 integers with one byte permute into a float
+//    of exponent 2^23 and one packed subtraction; products and sums run on the
+//    packed float32 pairs of Blackwell's ALU (fma.rn.f32x2).
+//  * Weights the caller marks static are read before the kernel waits on the
+//    previous one (programmatic dependent launch), so a dependent chain of
+//    small products pays for the activations' round trip only.
+//  * Warps stride over blocks of R rows; each loads the next step's codes
+//    before it works on the current one (large layers stream).
+//  * A lane whose partial sum is not finite, or whose block's scale could make
+//    a value infinite (an MXFP4 scale byte of 253 or more, an affine scale or
+//    bias of magnitude 2^119 or more), sums that block element by element
+//    instead: each value decoded at float32 as dequant decodes it, times its
+//    activation, in ascending k -- the infinities and NaNs IEEE arithmetic
+//    gives a per-element sum ("Nx_quant", "Products": an MXFP4 value past
+//    float32's range is infinite; a block whose float16 scale is infinite or
+//    NaN gives infinite or NaN values).
+//
+// Layouts: MLX affine codes ("GPTQModel wiki: MLX Apple Silicon", "Packed
+// layouts and exact transcoding": one little-endian bit stream per row, code i
+// at bits [i*b, i*b + b)); Q8_0, MXFP4 and MXFP4 in GGUF's blocks ("Nx_quant",
+// "Weights").
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "qm_device.cuh"
+#include "qm_internal.h"
+
+namespace qm {
+
+namespace g1 {
+
+constexpr int kWarps = 4;   // warps per CTA
+constexpr int R = 2;        // rows per warp block
+constexpr int kChunk = 1024;
+
+struct Args {
+    const uint8_t* codes;
+    const uint8_t* scales;
+    const uint8_t* biases;
+    const uint16_t* x;
+    uint16_t* y;
+    int64_t n, k;
+    int64_t code_row_bytes, scale_row_bytes;
+    int gshift;          // log2(group_size): affine scales
+    int sdt;             // affine scale dtype
+    int nchunk;          // chunks of 1024 inputs: ceil(k / 1024)
+    int64_t nblocks;     // blocks of R rows: ceil(n / R)
+    int static_w;        // the weight may be read before the previous kernel ends
+};
+
+// Words of packed data a lane holds for one row and one chunk.
+template <int FMT, int BITS>
+struct Words {
+    static constexpr int N = FMT == QM_AFFINE ? BITS : FMT == QM_Q8_0 ? 9 : FMT == QM_MXFP4 ? 4 : 5;
+};
+
+// One lane's data for one row of one step: code words and the raw scale
+// (and bias) of its block.
+template <int FMT, int BITS>
+struct Lane {
+    uint32_t w[Words<FMT, BITS>::N];
+    uint32_t s, b;   // affine: scale and bias bits; MXFP4: scale byte; others unused
+    uint32_t off;    // Q8_0 / MXFP4 blocks: byte offset of the block in w[0]
+};
+
+// The aligned 32-bit word holding byte `a` of the codes.
+QM_DEV uint32_t ldw(const uint8_t* base, int64_t a) {
+    return __ldg(reinterpret_cast<const uint32_t*>(base + (a & ~int64_t(3))));
+}
+
+// Loads lane data for row `row`, inputs [i0, i0 + 32). Rows past n and inputs
+// past k load nothing (the lane then contributes zero).
+template <int FMT, int BITS>
+QM_DEV void load_lane(const Args& a, int64_t row, int64_t i0, Lane<FMT, BITS>& L) {
+    constexpr int N = Words<FMT, BITS>::N;
+    if (row >= a.n || i0 >= a.k) {
+#pragma unroll
+        for (int j = 0; j < N; ++j) L.w[j] = 0u;
+        L.s = L.b = 0u;
+        L.off = 0u;
+        return;
+    }
+    const uint8_t* rp = a.codes + row * a.code_row_bytes;
+    if constexpr (FMT == QM_AFFINE) {
+        const int64_t byte0 = i0 * BITS / 8;  // 4*BITS-byte aligned
+        if constexpr (BITS % 4 == 0) {
+#pragma unroll
+            for (int q = 0; q < BITS / 4; ++q) {
+                const uint4 v = __ldg(reinterpret_cast<const uint4*>(rp + byte0) + q);
+                L.w[4 * q] = v.x; L.w[4 * q + 1] = v.y; L.w[4 * q + 2] = v.z; L.w[4 * q + 3] = v.w;
+            }
+        } else if constexpr (BITS % 2 == 0) {
+#pragma unroll
+            for (int q = 0; q < BITS / 2; ++q) {
+                const uint2 v = __ldg(reinterpret_cast<const uint2*>(rp + byte0) + q);
+                L.w[2 * q] = v.x; L.w[2 * q + 1] = v.y;
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < BITS; ++q) L.w[q] = __ldg(reinterpret_cast<const uint32_t*>(rp + byte0) + q);
+        }
+        const int64_t gi = row * (a.scale_row_bytes / 2) + (i0 >> a.gshift);
+        L.s = __ldg(reinterpret_cast<const uint16_t*>(a.scales) + gi);
+        L.b = __ldg(reinterpret_cast<const uint16_t*>(a.biases) + gi);
+        L.off = 0u;
+    } else if constexpr (FMT == QM_Q8_0) {
+        // 34 bytes at a 2-byte boundary: the nine aligned words holding them
+        const int64_t a0 = (i0 / 32) * 34;
+        L.off = static_cast<uint32_t>((reinterpret_cast<uintptr_t>(rp) + a0) & 3u);
+#pragma unroll
+        for (int j = 0; j < 9; ++j) L.w[j] = ldw(rp, a0 + 4 * j);
+        L.s = L.b = 0u;
+    } else if constexpr (FMT == QM_MXFP4) {
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(rp + i0 / 2));
+        L.w[0] = v.x; L.w[1] = v.y; L.w[2] = v.z; L.w[3] = v.w;
+        L.s = __ldg(a.scales + row * a.scale_row_bytes + i0 / 32);
+        L.b = 0u;
+        L.off = 0u;
+    } else {  // MXFP4 in GGUF's 17-byte blocks: the five aligned words holding them
+        const int64_t a0 = (i0 / 32) * 17;
+        L.off = static_cast<uint32_t>((reinterpret_cast<uintptr_t>(rp) + a0) & 3u);
+#pragma unroll
+        for (int j = 0; j < 5; ++j) L.w[j] = ldw(rp, a0 + 4 * j);
+        L.s = L.b = 0u;
+    }
+}
+
+// A lane's 32 activations as float32 pairs, in the order its format pairs
+// its codes, and their sum (affine bias).
+template <int FMT, int BITS>
+struct Acts {
+    float2 p[16];
+    float sum;
+};
+
+template <int FMT, int BITS>
+QM_DEV void load_acts(const Args& a, int64_t i0, Acts<FMT, BITS>& X) {
+    uint32_t w[16];
+    if (i0 < a.k) {
+        const uint4* src = reinterpret_cast<const uint4*>(a.x + i0);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint4 v = __ldg(src + q);
+            w[4 * q] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
+        }
+    } else {
+#pragma unroll
+        for (int q = 0; q < 16; ++q) w[q] = 0u;
+    }
+    // w[q] holds inputs 2q (low half) and 2q + 1 (high half), as bf16
+    auto lo = [&](int i) { return __uint_as_float(w[i >> 1] << 16); };
+    auto hi = [&](int i) { return __uint_as_float(w[i >> 1] & 0xFFFF0000u); };
+    auto at = [&](int i) { return (i & 1) ? hi(i) : lo(i); };
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        if constexpr (FMT == QM_AFFINE && BITS == 4) {
+            // word q of codes holds inputs 8q .. 8q + 7; its low nibbles are the
+            // even inputs, its high nibbles the odd ones, paired byte by byte
+            const int q = j >> 2, r = j & 3;
+            const int base = 8 * q + ((r & 2) ? 1 : 0) + ((r & 1) ? 4 : 0);
+            X.p[j] = make_float2(at(base), at(base + 2));
+        } else if constexpr (FMT == QM_MXFP4_BLOCKS) {
+            X.p[j] = make_float2(at(j), at(j + 16));  // byte j: inputs j and j + 16
+        } else {
+            X.p[j] = make_float2(lo(2 * j), hi(2 * j + 1));
+        }
+    }
+    if constexpr (FMT == QM_AFFINE) {
+        float2 s = make_float2(0.0f, 0.0f);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) s = add2(s, X.p[j]);
+        X.sum = s.x + s.y;
+    } else {
+        X.sum = 0.0f;
+    }
+}
+
+constexpr uint32_t kMagic = 0x4B000000u;  // float 2^23: 2^23 + u for a byte u in its low bits
+
+QM_DEV float2 two_bytes(uint32_t w, uint32_t sel_lo, uint32_t sel_hi) {
+    return make_float2(__uint_as_float(prmt(w, kMagic, sel_lo)), __uint_as_float(prmt(w, kMagic, sel_hi)));
+}
+
+// Code i (0..31) of a lane's affine chunk of BITS-bit codes.
+template <int BITS>
+QM_DEV uint32_t code_at(const uint32_t (&w)[BITS], int i) {
+    const int bit = i * BITS, q = bit >> 5, sh = bit & 31;
+    uint32_t v = w[q] >> sh;
+    if (sh + BITS > 32) v |= w[q + 1] << (32 - sh);
+    return v & ((1u << BITS) - 1u);
+}
+
+// sum over the lane's 32 inputs of code * x: the exact integer codes (or e2m1
+// values) times the activations, float32 sums
+template <int FMT, int BITS>
+QM_DEV float lane_dot(const Lane<FMT, BITS>& L, const Acts<FMT, BITS>& X) {
+    float2 acc = make_float2(0.0f, 0.0f);
+    if constexpr (FMT == QM_AFFINE && BITS == 4) {
+        const float2 neg = make_float2(-8388608.0f, -8388608.0f);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t lo = L.w[q] & 0x0F0F0F0Fu, hi = (L.w[q] >> 4) & 0x0F0F0F0Fu;
+            acc = fma2(add2(two_bytes(lo, 0x7540, 0x7541), neg), X.p[4 * q], acc);
+            acc = fma2(add2(two_bytes(lo, 0x7542, 0x7543), neg), X.p[4 * q + 1], acc);
+            acc = fma2(add2(two_bytes(hi, 0x7540, 0x7541), neg), X.p[4 * q + 2], acc);
+            acc = fma2(add2(two_bytes(hi, 0x7542, 0x7543), neg), X.p[4 * q + 3], acc);
+        }
+    } else if constexpr (FMT == QM_AFFINE && BITS == 8) {
+        const float2 neg = make_float2(-8388608.0f, -8388608.0f);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            acc = fma2(add2(two_bytes(L.w[q], 0x7540, 0x7541), neg), X.p[2 * q], acc);
+            acc = fma2(add2(two_bytes(L.w[q], 0x7542, 0x7543), neg), X.p[2 * q + 1], acc);
+        }
+    } else if constexpr (FMT == QM_AFFINE) {
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const float2 c = make_float2(static_cast<float>(code_at<BITS>(L.w, 2 * j)),
+                                         static_cast<float>(code_at<BITS>(L.w, 2 * j + 1)));
+            acc = fma2(c, X.p[j], acc);
+        }
+    } else if constexpr (FMT == QM_Q8_0) {
+        // quants from byte 2 of the block: word j of them is bytes 4j+2 .. 4j+5
+        const float2 neg = make_float2(-8388736.0f, -8388736.0f);  // -(2^23 + 128)
+        const uint32_t sh = 8u * (L.off + 2u);                     // 16 or 32
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint32_t qw =
+                (sh == 32u ? L.w[j + 1] : __funnelshift_r(L.w[j], L.w[j + 1], 16)) ^ 0x80808080u;  // q + 128
+            acc = fma2(add2(two_bytes(qw, 0x7540, 0x7541), neg), X.p[2 * j], acc);
+            acc = fma2(add2(two_bytes(qw, 0x7542, 0x7543), neg), X.p[2 * j + 1], acc);
+        }
+    } else if constexpr (FMT == QM_MXFP4) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            uint32_t h[4];
+            e2m1x8_to_f16x2(L.w[q], h);  // byte i -> (input 2i, input 2i + 1)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                acc = fma2(__half22float2(*reinterpret_cast<const __half2*>(&h[i])), X.p[4 * q + i], acc);
+        }
+    } else {  // MXFP4 blocks: 16 data bytes from byte 1 of the block
+        const uint32_t sh = 8u * (L.off + 1u);  // 8 .. 32
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const uint32_t dw = sh == 32u ? L.w[q + 1] : __funnelshift_r(L.w[q], L.w[q + 1], sh);
+            uint32_t h[4];
+            e2m1x8_to_f16x2(dw, h);  // byte i -> (input j, input j + 16), j = 4q + i
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                acc = fma2(__half22float2(*reinterpret_cast<const __half2*>(&h[i])), X.p[4 * q + i], acc);
+        }
+    }
+    return acc.x + acc.y;
+}
+
+QM_DEV float sval(uint32_t h, int sdt) { return sdt == QM_F16 ? f16_bits_to_f32(h) : bf16_bits_to_f32(h); }
+
+// The e8m0 scale of a GGUF MXFP4 block held in the lane's words.
+QM_DEV uint32_t blocks_scale_byte(const uint32_t (&w)[5], uint32_t off) { return (w[0] >> (8 * off)) & 0xFFu; }
+
+// The lane's contribution for one row and chunk with its block's scale (and
+// bias), and whether that block may hold a value the block-scaled sum does not
+// reproduce exactly (non-finite values, or values that overflow float32).
+template <int FMT, int BITS>
+QM_DEV float lane_part(const Args& a, const Lane<FMT, BITS>& L, const Acts<FMT, BITS>& X, bool& exact) {
+    const float dot = lane_dot<FMT, BITS>(L, X);
+    if constexpr (FMT == QM_AFFINE) {
+        const float s = sval(L.s, a.sdt), b = sval(L.b, a.sdt);
+        exact = fmaxf(fabsf(s), fabsf(b)) >= 0x1p119f;  // |code * s + b| may reach 2^128
+        return fmaf(s, dot, b * X.sum);
+    } else if constexpr (FMT == QM_Q8_0) {
+        const uint32_t dbits = L.off ? (L.w[0] >> 16) : (L.w[0] & 0xFFFFu);
+        exact = false;
+        return f16_bits_to_f32(dbits) * dot;
+    } else if constexpr (FMT == QM_MXFP4) {
+        exact = L.s >= 253u;  // values of magnitude 4 (at 253) or 2 (at 254) pass float32's range
+        return e8m0_to_f32(L.s) * dot;
+    } else {
+        const uint32_t sb = blocks_scale_byte(L.w, L.off);
+        exact = sb >= 253u;
+        return e8m0_to_f32(sb) * dot;
+    }
+}
+
+// Value i of row `row`, decoded at float32 from global memory as dequant decodes it.
+template <int FMT, int BITS>
+QM_DEV float value_g(const Args& a, int64_t row, int64_t i) {
+    const uint8_t* rp = a.codes + row * a.code_row_bytes;
+    if constexpr (FMT == QM_AFFINE) {
+        const int64_t bit = i * BITS;
+        const uint32_t lo = __ldg(rp + bit / 8), hi = (bit % 8 + BITS > 8) ? __ldg(rp + bit / 8 + 1) : 0u;
+        const uint32_t c = ((lo | (hi << 8)) >> (bit % 8)) & ((1u << BITS) - 1u);
+        const int64_t gi = row * (a.scale_row_bytes / 2) + (i >> a.gshift);
+        return fmaf(static_cast<float>(c), sval(__ldg(reinterpret_cast<const uint16_t*>(a.scales) + gi), a.sdt),
+                    sval(__ldg(reinterpret_cast<const uint16_t*>(a.biases) + gi), a.sdt));
+    } else if constexpr (FMT == QM_Q8_0) {
+        const uint8_t* blk = rp + (i / 32) * 34;
+        const float d = f16_bits_to_f32(static_cast<uint32_t>(__ldg(blk)) | (static_cast<uint32_t>(__ldg(blk + 1)) << 8));
+        return d * static_cast<float>(static_cast<int8_t>(__ldg(blk + 2 + i % 32)));
+    } else {
+        uint32_t c, sb;
+        if constexpr (FMT == QM_MXFP4) {
+            const uint32_t byte = __ldg(rp + i / 2);
+            c = (i & 1) ? (byte >> 4) : (byte & 15u);
+            sb = __ldg(a.scales + row * a.scale_row_bytes + i / 32);
+        } else {
+            const uint8_t* blk = rp + (i / 32) * 17;
+            const int t = static_cast<int>(i % 32);
+            const uint32_t byte = __ldg(blk + 1 + (t & 15));
+            c = t < 16 ? (byte & 15u) : (byte >> 4);
+            sb = __ldg(blk);
+        }
+        uint32_t h[4];
+        e2m1x8_to_f16x2(c, h);
+        return __half2float(__ushort_as_half(static_cast<unsigned short>(h[0] & 0xFFFFu))) * e8m0_to_f32(sb);
+    }
+}
+
+// The lane's contribution summed element by element: value times activation
+// at float32, inputs in ascending order. Out of line: rarely taken.
+template <int FMT, int BITS>
+static __device__ __noinline__ float lane_exact(const Args& a, int64_t row, int64_t i0) {
+    float acc = 0.0f;
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+        acc = fmaf(bf16_bits_to_f32(__ldg(a.x + i0 + i)), value_g<FMT, BITS>(a, row, i0 + i), acc);
+    return acc;
+}
+
+template <int FMT, int BITS>
+__global__ void __launch_bounds__(kWarps * 32) gemv1_kernel(const __grid_constant__ Args a) {
+    grid_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarp = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
+    if (warp0 >= a.nblocks) return;  // nothing to read or write
+    const int64_t nb = (a.nblocks - 1 - warp0) / nwarp + 1;  // this warp's blocks
+    const int64_t steps = nb * a.nchunk;                     // (block, chunk) pairs, chunks fastest
+    Lane<FMT, BITS> cur[R], nxt[R];
+    auto load_step = [&](int64_t s, Lane<FMT, BITS> (&L)[R]) {
+        const int64_t b = warp0 + (s / a.nchunk) * nwarp;
+        const int64_t i0 = static_cast<int64_t>(s % a.nchunk) * kChunk + 32 * lane;
+#pragma unroll
+        for (int r = 0; r < R; ++r) load_lane<FMT, BITS>(a, b * R + r, i0, L[r]);
+    };
+    if (a.static_w) {  // the weight is not written by the previous kernel: read it first
+        load_step(0, cur);
+        grid_dependency_wait();
+    } else {
+        grid_dependency_wait();
+        load_step(0, cur);
+    }
+    Acts<FMT, BITS> X;
+    float y[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) y[r] = 0.0f;
+    #pragma unroll 1
+    for (int64_t s = 0; s < steps; ++s) {
+        if (s + 1 < steps) load_step(s + 1, nxt);
+        const int c = static_cast<int>(s % a.nchunk);
+        const int64_t b = warp0 + (s / a.nchunk) * nwarp;
+        const int64_t i0 = static_cast<int64_t>(c) * kChunk + 32 * lane;
+        if (a.nchunk > 1 || s == 0) load_acts<FMT, BITS>(a, i0, X);
+#pragma unroll
+        for (int r = 0; r < R; ++r) {
+            bool exact;
+            float part = lane_part<FMT, BITS>(a, cur[r], X, exact);
+            const int64_t row = b * R + r;
+            if ((exact || !isfinite(part)) && row < a.n && i0 < a.k) part = lane_exact<FMT, BITS>(a, row, i0);
+            y[r] += part;
+        }
+        if (c == a.nchunk - 1) {
+            // the R rows' sums over the warp, in a fixed order: lanes first
+            // exchange halves of their R values, then add down to one each
+            static_assert(R == 2, "the exchange below pairs two rows");
+            const float give = (lane & 1) ? y[0] : y[1];
+            float v = ((lane & 1) ? y[1] : y[0]) + __shfl_xor_sync(0xffffffffu, give, 1);
+#pragma unroll
+            for (int o = 2; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            const int64_t row = b * R + lane;  // lane 0: row 0 of the block, lane 1: row 1
+            if (lane < R && row < a.n) {
+                __nv_bfloat16 bv = __float2bfloat16_rn(v);
+                a.y[row] = *reinterpret_cast<uint16_t*>(&bv);
+            }
+#pragma unroll
+            for (int r = 0; r < R; ++r) y[r] = 0.0f;
+        }
+#pragma unroll
+        for (int r = 0; r < R; ++r) cur[r] = nxt[r];
+    }
+}
+
+template <int FMT, int BITS>
+cudaError_t launch_t(const Args& a, cudaStream_t st) {
+    // all warps resident at once where the rows allow: 16 warps per SM
+    const int64_t warps = std::min<int64_t>(a.nblocks, int64_t(num_sms()) * 16);
+    const unsigned grid = static_cast<unsigned>((warps + kWarps - 1) / kWarps);
+    return launch_pdl(gemv1_kernel<FMT, BITS>, grid, kWarps * 32, 0, st, a);
+}
+
+}  // namespace g1
+
+bool gemv1_supported(const WDesc& w) {
+    if (w.ndim != 2 || w.n < 1 || w.k < 32) return false;
+    if (w.fmt == QM_AFFINE) {
+        if (w.gs < 32 || (w.gs & (w.gs - 1))) return false;
+        return w.bits == 2 || w.bits == 3 || w.bits == 4 || w.bits == 5 || w.bits == 6 || w.bits == 8;
+    }
+    return w.fmt == QM_Q8_0 || w.fmt == QM_MXFP4 || w.fmt == QM_MXFP4_BLOCKS;
+}
+
+cudaError_t launch_gemv1(const WDesc& w, const void* x, void* y, cudaStream_t st) {
+    using namespace g1;
+    Args a{};
+    a.codes = w.codes;
+    a.scales = w.scales;
+    a.biases = w.biases;
+    a.x = static_cast<const uint16_t*>(x);
+    a.y = static_cast<uint16_t*>(y);
+    a.n = w.n;
+    a.k = w.k;
+    a.code_row_bytes = w.code_row_bytes;
+    a.scale_row_bytes = w.scale_row_bytes;
+    a.gshift = 0;
+    while ((1 << a.gshift) < w.gs) ++a.gshift;
+    a.sdt = w.sdt;
+    a.nchunk = static_cast<int>((w.k + kChunk - 1) / kChunk);
+    a.nblocks = (w.n + R - 1) / R;
+    a.static_w = w.is_static ? 1 : 0;
+    if (w.fmt == QM_AFFINE) {
+        switch (w.bits) {
+            case 2: return launch_t<QM_AFFINE, 2>(a, st);
+            case 3: return launch_t<QM_AFFINE, 3>(a, st);
+            case 4: return launch_t<QM_AFFINE, 4>(a, st);
+            case 5: return launch_t<QM_AFFINE, 5>(a, st);
+            case 6: return launch_t<QM_AFFINE, 6>(a, st);
+            default: return launch_t<QM_AFFINE, 8>(a, st);
+        }
+    }
+    if (w.fmt == QM_Q8_0) return launch_t<QM_Q8_0, 8>(a, st);
+    if (w.fmt == QM_MXFP4) return launch_t<QM_MXFP4, 4>(a, st);
+    return launch_t<QM_MXFP4_BLOCKS, 4>(a, st);
+}
+
+}  // namespace qm

@@ -56,13 +56,20 @@ int num_sms();
 // Opt-in shared memory per block on the current device (cached per device).
 int max_smem_optin();
 
-// Formats the tensor-map pipelines (decode GEMV, tensor-core GEMM) decode;
-// the others take the plain kernels for products.
-inline bool pipelined_format(int fmt) { return fmt == QM_AFFINE || fmt == QM_Q8_0 || fmt == QM_MXFP4; }
+// Weights the tensor-map decode GEMV (several tokens) decodes; the others take
+// the plain kernels there.
+inline bool pipelined_format(const WDesc& w) {
+    return (w.fmt == QM_AFFINE && (w.bits == 4 || w.bits == 8)) || w.fmt == QM_Q8_0 || w.fmt == QM_MXFP4;
+}
+// Weights the tensor-core GEMM decodes: affine at every width, Q8_0, MXFP4.
+inline bool gemm_format(const WDesc& w) { return w.fmt == QM_AFFINE || w.fmt == QM_Q8_0 || w.fmt == QM_MXFP4; }
 
 // ------------------------------------------------------------ launchers
 // Each returns the CUDA error of its launch (cudaSuccess when nothing ran).
 cudaError_t launch_dequant(const WDesc& w, int out_dtype, void* out, cudaStream_t st);
+// x [rows, k] of x_dtype (QM_F32, QM_BF16, QM_F16) -> Q8_0 blocks [rows, k/32*34].
+cudaError_t launch_quantize_q8_0(const void* x, int x_dtype, int64_t rows, int64_t k, uint8_t* blocks,
+                                 cudaStream_t st);
 // The parts of a packed take: up to three (codes, scales, biases), each a
 // source of `len` rows of inner[part] bytes per outer index and a destination.
 struct TakeParts {
@@ -76,6 +83,10 @@ cudaError_t launch_take_packed(const TakeParts& tp, int64_t outer, int64_t len, 
 cudaError_t launch_take_dense(const WDesc& w, int axis, const void* ids, int id64, int64_t n_ids,
                               int out_dtype, void* out, cudaStream_t st);
 
+// y [1, n] = x [1, k] * W^T for a 2-d weight (one token), x and y bf16: a
+// register-only kernel, no shared memory (qm_gemv1.cu).
+bool gemv1_supported(const WDesc& w);
+cudaError_t launch_gemv1(const WDesc& w, const void* x, void* y, cudaStream_t st);
 // y [M, n] = x [M, k] * W^T for a 2-d weight, M <= 16, x and y bf16.
 qm_status launch_gemv(const WDesc& w, const void* x, int64_t M, void* y, cudaStream_t st);
 bool gemv_supported(const WDesc& w, int64_t M);

@@ -17,13 +17,19 @@ patterns) plus the metadata a caller needs to describe the weight:
   [..., n, k/32] e8m0 bytes uniform in [lo, hi].
 * MXFP4 in GGUF's blocks: ``codes`` uint8 [..., n, k/32*17], each 17-byte
   block an e8m0 byte uniform in [lo, hi] then 16 uniform bytes.
+* GGUF Q4_K: ``codes`` uint8 [..., n, k/256*144], each 144-byte block a
+  float16 d and dmin = |N(0, sigma)|, then 140 uniform bytes (the packed
+  6-bit scales and mins, and the 4-bit quants).
+* GGUF Q6_K: ``codes`` uint8 [..., n, k/256*210], each 210-byte block 192
+  uniform bytes (quants), 16 int8 scales uniform in [-128, 127], then a
+  float16 d = |N(0, sigma)|.
 """
 from __future__ import annotations
 
 import numpy as np
 import torch
 
-AFFINE, Q8_0, MXFP4, MXFP4_BLOCKS = "affine", "q8_0", "mxfp4", "mxfp4_blocks"
+AFFINE, Q8_0, MXFP4, MXFP4_BLOCKS, Q4_K, Q6_K = "affine", "q8_0", "mxfp4", "mxfp4_blocks", "q4_k", "q6_k"
 
 
 def rng(seed: int) -> np.random.Generator:
@@ -104,6 +110,30 @@ def mxfp4_blocks_weight(g, n, k, lead=(), scale_lo=118, scale_hi=126):
     blocks[..., 0] = g.integers(scale_lo, scale_hi + 1, size=shape + (k // 32,), dtype=np.int64)
     return dict(format=MXFP4_BLOCKS, shape=shape + (k,), bits=4, group_size=32, scale_dtype=None,
                 codes=blocks.astype(np.uint8).reshape(shape + (k // 32 * 17,)), scales=None, biases=None)
+
+
+def q4_k_weight(g, n, k, lead=(), d_sigma=0.002):
+    """GGUF Q4_K weight [*lead, n, k] (k a multiple of 256)."""
+    assert k % 256 == 0
+    shape = tuple(lead) + (n,)
+    nb = k // 256
+    blocks = g.integers(0, 256, size=shape + (nb, 144), dtype=np.int64).astype(np.uint8)
+    dd = np.abs(g.standard_normal(shape + (nb, 2), dtype=np.float32) * np.float32(d_sigma))
+    blocks[..., 0:4] = dd.astype("<f2").view(np.uint8).reshape(shape + (nb, 4))
+    return dict(format=Q4_K, shape=shape + (k,), bits=4, group_size=256, scale_dtype=None,
+                codes=np.ascontiguousarray(blocks.reshape(shape + (nb * 144,))), scales=None, biases=None)
+
+
+def q6_k_weight(g, n, k, lead=(), d_sigma=0.0005):
+    """GGUF Q6_K weight [*lead, n, k] (k a multiple of 256)."""
+    assert k % 256 == 0
+    shape = tuple(lead) + (n,)
+    nb = k // 256
+    blocks = g.integers(0, 256, size=shape + (nb, 210), dtype=np.int64).astype(np.uint8)
+    d = np.abs(g.standard_normal(shape + (nb,), dtype=np.float32) * np.float32(d_sigma))
+    blocks[..., 208:210] = d.astype("<f2").view(np.uint8).reshape(shape + (nb, 2))
+    return dict(format=Q6_K, shape=shape + (k,), bits=6, group_size=256, scale_dtype=None,
+                codes=np.ascontiguousarray(blocks.reshape(shape + (nb * 210,))), scales=None, biases=None)
 
 
 def activations(g, M, k, sigma=1.0):

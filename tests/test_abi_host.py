@@ -59,7 +59,7 @@ def _dequant_err(lib, w, out=1024, dt=qm.QM_BF16):
 
 @pytest.mark.parametrize("mut,part", [
     (dict(shape=(16, 48)), "codes"),          # k not a multiple of 32
-    (dict(bits=3), "w"),
+    (dict(bits=7), "w"),                      # affine widths are 2, 3, 4, 5, 6 and 8
     (dict(gs=16), "w"),
     (dict(shape=(16, 96), gs=64), "scales"),  # k not a multiple of group_size
     (dict(codes=0), "codes"),
@@ -220,3 +220,20 @@ def test_mxfp4_blocks_validation(lib):
     assert 0 < ws == lib.qm_experts_route_workspace(256, 32)  # plain kernels: routing tables only
     qw = qm.QWeight("mxfp4_blocks", (3, 16, 64), None)
     assert qw.part_shapes((3, 5)) == ((3, 5, 34), None, None)
+
+
+def test_quantize_q8_0_validation(lib):
+    def err(*args):
+        st = lib.qm_quantize_q8_0(*args)
+        return st, lib.qm_last_error().decode()
+    st, msg = err(4096, 7, 4, 64, 8192, None)
+    assert st == qm.QM_EINVAL and msg.startswith("x:")
+    st, msg = err(4096, qm.QM_F32, 4, 48, 8192, None)
+    assert st == qm.QM_EINVAL and msg.startswith("x:")
+    st, msg = err(4100, qm.QM_F32, 4, 64, 8192, None)
+    assert st == qm.QM_EINVAL and msg.startswith("x:")
+    st, msg = err(4096, qm.QM_F32, 4, 64, 8194, None)
+    assert st == qm.QM_EINVAL and msg.startswith("out:")
+    st, msg = err(4096, qm.QM_F32, 4, 64, 4096 + 512, None)  # the blocks would overwrite x
+    assert st == qm.QM_EINVAL and msg.startswith("out:")
+    assert lib.qm_quantize_q8_0(None, qm.QM_F32, 0, 64, None, None) == qm.QM_OK  # nothing to do

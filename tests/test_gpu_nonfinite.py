@@ -202,7 +202,8 @@ def _affine_special(g, bits, gs, sdt):
     return w
 
 
-@pytest.mark.parametrize("bits,gs,sdt", [(4, 64, "bf16"), (8, 32, "bf16"), (4, 32, "f16")])
+@pytest.mark.parametrize("bits,gs,sdt", [(4, 64, "bf16"), (8, 32, "bf16"), (4, 32, "f16"), (3, 64, "bf16"),
+                                         (6, 32, "bf16")])
 @pytest.mark.parametrize("M", MS)
 def test_affine_special_scales(bits, gs, sdt, M):
     g = synth.rng(1450 + M + bits + gs)

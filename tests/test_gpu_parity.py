@@ -611,3 +611,99 @@ def test_mxfp4_blocks_apply_experts():
     ids[3, 1] = 4   # out of range: zeros
     ids[7, 0] = -1
     _check_experts(w, ids, synth.activations(g, 16, 256), "mxfp4 blocks experts")
+
+
+# ---------------------------------------------------------------- quantize_q8_0
+def _quantize_cases(g, rows, k):
+    x = (g.standard_normal((rows, k)) * np.exp(2 * g.standard_normal((rows, 1)))).astype(np.float32)
+    b = x.reshape(rows, k // 32, 32)
+    b[0, 0] = 0.0                                 # d = 0
+    b[0, 1, :] = 0.0; b[0, 1, 4] = 1e-39          # 1/d past float32's range: zero bytes
+    b[0, 2, 7] = np.inf; b[0, 3, 9] = -np.inf     # infinities: scale +inf, quants 0
+    b[0, 4, 31] = np.nan; b[0, 5, 0] = np.nan; b[0, 5, 1] = np.inf   # NaN, with and without inf
+    b[0, 6, :] = 0.0; b[0, 6, :6] = [127.0, 2.5, -2.5, 0.5, -0.5, 126.5]   # halves away from zero
+    b[0, 7] *= np.float32(1e6)                     # d past float16's largest
+    b[1] *= np.float32(1e-5)                       # float16 subnormal scales
+    b[2] *= np.float32(1e-30)                      # scales below float16's range: stored as 0
+    b[3, :, :] = -b[3, :, :1]                      # blocks of one repeated value
+    return x
+
+
+def test_quantize_q8_0_bit_exact():
+    # "Nx_quant", val quantize_q8_0: the blocks' bytes, every stated case included
+    g = np.random.default_rng(800)
+    rows, k = 48, 512
+    x = _quantize_cases(g, rows, k)
+    want = oracle.quantize_q8_0(x)
+    got = qm.quantize_q8_0(torch.from_numpy(x).cuda())
+    assert np.array_equal(_host(got.codes), want)
+    w = dict(format="q8_0", shape=(rows, k), codes=want)
+    assert _bits_equal(_host(qm.dequant(got, torch.float32)), oracle.dequant(to_oracle(w), oracle.F32),
+                       torch.float32)
+
+
+@pytest.mark.parametrize("dt", [torch.bfloat16, torch.float16])
+def test_quantize_q8_0_reads_16_bit_inputs_at_float32(dt):
+    # x of a 16-bit dtype is read at float32: the blocks equal the float32 case's
+    g = np.random.default_rng(801)
+    x = _quantize_cases(g, 40, 256)
+    xt = torch.from_numpy(x).to(dt)
+    want = oracle.quantize_q8_0(xt.float().numpy())
+    got = qm.quantize_q8_0(xt.cuda())
+    assert np.array_equal(_host(got.codes), want)
+
+
+def test_quantize_q8_0_large_and_lead_axes():
+    # a [3, 700, 4096] weight: many blocks per launch, leading axes flattened
+    g = np.random.default_rng(802)
+    x = g.standard_normal((3, 700, 4096)).astype(np.float32) * np.float32(0.02)
+    got = qm.quantize_q8_0(torch.from_numpy(x).cuda())
+    assert got.shape == (3, 700, 4096)
+    assert np.array_equal(_host(got.codes).reshape(-1), oracle.quantize_q8_0(x.reshape(-1, 4096)).reshape(-1))
+
+
+# ---------------------------------------------------------------- affine 2, 3, 5 and 6 bits
+# "GPTQModel wiki: MLX Apple Silicon", "Packed layouts and exact transcoding":
+# one little-endian bit stream per row, so 3-, 5- and 6-bit codes cross words.
+WIDTHS = [2, 3, 5, 6]
+
+
+@pytest.mark.parametrize("bits", WIDTHS)
+@pytest.mark.parametrize("gs", [32, 64, 128])
+def test_affine_widths_dequant_and_take(bits, gs):
+    g = synth.rng(1500 + 10 * bits + gs)
+    for n, k, lead in ((37, 256, ()), (5, 1024, (3,)), (3, 128, (2, 2))):
+        w = synth.affine_weight(g, n, k, bits=bits, group_size=gs, lead=lead)
+        ow = to_oracle(w)
+        qw = qm.QWeight.from_arrays(w)
+        for dt in (torch.float32, torch.bfloat16, torch.float16):
+            assert _bits_equal(_host(qm.dequant(qw, dt)), oracle.dequant(ow, ODT[dt]), dt), (n, k, lead, dt)
+        L = ow.shape[0]
+        ids = np.array([L - 1, 0, -1, L, 2 % L, 1 % L], dtype=np.int32)
+        tw, dense = qm.take(qw, 0, torch.from_numpy(ids).cuda(), dense_dtype=torch.bfloat16)
+        ot = oracle.take(ow, 0, ids)
+        for name, part in (("codes", tw.codes), ("scales", tw.scales), ("biases", tw.biases)):
+            assert np.array_equal(_host(part).view(np.uint8).reshape(-1), ot.parts()[name].view(np.uint8).reshape(-1))
+        assert np.array_equal(_host(dense), oracle.dequant(ot, oracle.BF16))
+
+
+@pytest.mark.parametrize("bits", WIDTHS)
+@pytest.mark.parametrize("M", [1, 3, 16, 33, 130])
+def test_affine_widths_apply(bits, M):
+    # M = 1: the one-token kernel; 3 and 16: the plain kernel; 33 and 130: the
+    # tensor cores (k = 96 rows are no 16-byte multiple: the plain kernel)
+    g = synth.rng(1600 + 10 * bits + M)
+    for gs, n, k in ((32, 96, 512), (64, 200, 1024), (128, 130, 2048), (32, 40, 96)):
+        w = synth.affine_weight(g, n, k, bits=bits, group_size=gs)
+        _check_apply(w, synth.activations(g, M, k), f"affine{bits} gs{gs} n={n} k={k} M={M}")
+
+
+@pytest.mark.parametrize("bits", WIDTHS)
+@pytest.mark.parametrize("T", [12, 100])
+def test_affine_widths_experts(bits, T):
+    g = synth.rng(1700 + bits + T)
+    E, n, k = 4, 72, 512
+    w = synth.affine_weight(g, n, k, bits=bits, group_size=64, lead=(E,))
+    ids = synth.expert_ids(g, T, 2, E)
+    ids[2, 1] = -1
+    _check_experts(w, ids, synth.activations(g, T, k), f"affine{bits} experts T={T}")

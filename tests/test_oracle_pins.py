@@ -683,3 +683,153 @@ def test_experts_entries_are_per_matrix_products():
         sub = oracle.Weight(w.fmt, (n, k), w.codes[eid], w.scales[eid], w.biases[eid], bits=4,
                             group_size=32)
         assert ent2[e] == oracle.apply(sub, xp[p_idx[e]:p_idx[e] + 1])[0, j_idx[e]]
+
+
+# ------------------------------------------------------------ Q4_K and Q6_K
+# "Nx_quant (raven-ml.dev API docs)", "Weights": Q4_K is 144 bytes per 256
+# values (float16 d and dmin, 12 bytes of 6-bit scales and mins for eight
+# sub-blocks of 32, 128 bytes of 4-bit quants), value d * sc * q - dmin * m;
+# Q6_K is 210 bytes per 256 values (128 bytes of low 4 bits, 64 of high 2
+# bits, sixteen int8 scales of sub-blocks of 16, float16 d), value
+# d * sc * (q - 32). The arrangement inside the fields is ggml's block layout
+# (the page names it); the packers below write it from the description,
+# independently of the oracle's readers.
+def _pack_q4_k(d, dmin, sc, m, q):
+    """One Q4_K block from d, dmin (float16 bit patterns), scales and mins [8]
+    (0..63) and quants [256] (0..15)."""
+    blk = np.zeros(144, np.uint8)
+    blk[0], blk[1], blk[2], blk[3] = d & 0xFF, d >> 8, dmin & 0xFF, dmin >> 8
+    s = np.zeros(12, np.int64)
+    for j in range(8):
+        if j < 4:  # six bits in bytes 0..3 (scale) and 4..7 (min)
+            s[j] |= sc[j] & 63
+            s[4 + j] |= m[j] & 63
+        else:      # low four bits in a nibble of bytes 8..11, top two on bytes 0..7's top bits
+            s[8 + j - 4] |= (sc[j] & 15) | ((m[j] & 15) << 4)
+            s[j - 4] |= (sc[j] >> 4) << 6
+            s[j] |= (m[j] >> 4) << 6
+    blk[4:16] = s.astype(np.uint8)
+    for c in range(4):  # run c: values 64c .. 64c+31 low nibbles, 64c+32 .. 64c+63 high ones
+        for l in range(32):
+            blk[16 + 32 * c + l] = q[64 * c + l] | (q[64 * c + 32 + l] << 4)
+    return blk
+
+
+def _pack_q6_k(d, sc, q):
+    """One Q6_K block from d (float16 bits), int8 scales [16] and quants [256] (0..63)."""
+    blk = np.zeros(210, np.uint8)
+    for h in range(2):
+        for t in range(4):
+            for l in range(32):
+                v = q[128 * h + 32 * t + l]
+                i = 64 * h + l + 32 * (t % 2)
+                blk[i] |= (v & 15) << (4 if t >= 2 else 0)
+                blk[128 + 32 * h + l] |= (v >> 4) << (2 * t)
+    blk[192:208] = np.asarray(sc, np.int8).view(np.uint8)
+    blk[208], blk[209] = d & 0xFF, d >> 8
+    return blk
+
+
+def _f16(v):
+    return int(np.float16(v).view(np.uint16))
+
+
+def test_k_quants_zero_block_decodes_to_zeros():
+    # the page: a block of zero bytes decodes to zeros, -0. in Q6_K
+    for fmt, nb, neg in ((oracle.Q4_K, 144, False), (oracle.Q6_K, 210, True)):
+        w = oracle.Weight(fmt, (3, 512), np.zeros((3, 2 * nb), np.uint8))
+        v = oracle.dequant(w, oracle.F32)
+        assert np.all(v == 0) and np.all(np.signbit(v) == neg), fmt
+
+
+def test_q4_k_values_from_the_fields():
+    # every sub-block with its own scale and min (the 6-bit ranges' edges
+    # included) and quants covering 0..15: value i = d * sc[i // 32] * q[i] -
+    # dmin * m[i // 32], rounded once to float32
+    g = np.random.default_rng(40)
+    for trial in range(20):
+        sc = g.integers(0, 64, 8)
+        m = g.integers(0, 64, 8)
+        if trial == 0:
+            sc[:] = [0, 63, 1, 62, 32, 31, 48, 15]
+            m[:] = [63, 0, 62, 1, 31, 32, 15, 48]
+        q = g.integers(0, 16, 256)
+        d = float(np.float16(abs(g.standard_normal()) * 0.01))
+        dmin = float(np.float16(abs(g.standard_normal()) * 0.01))
+        blk = _pack_q4_k(_f16(d), _f16(dmin), sc, m, q)
+        v = oracle.dequant(oracle.Weight(oracle.Q4_K, (1, 256), blk[None]), oracle.F32)[0]
+        j = np.arange(256) // 32
+        want = (d * sc[j] * q - dmin * m[j]).astype(np.float32)  # exact in float64, one rounding
+        assert np.array_equal(v.view(np.uint32), want.view(np.uint32)), trial
+
+
+def test_q6_k_values_from_the_fields():
+    g = np.random.default_rng(41)
+    for trial in range(20):
+        sc = g.integers(-128, 128, 16)
+        q = g.integers(0, 64, 256)
+        if trial == 0:
+            sc[:] = [-128, 127, 0, 1, -1, 64, -64, 5, 7, -9, 100, -100, 2, 3, 4, 6]
+            q[:64] = np.arange(64)
+        d = float(np.float16(abs(g.standard_normal()) * 0.001))
+        blk = _pack_q6_k(_f16(d), sc, q)
+        v = oracle.dequant(oracle.Weight(oracle.Q6_K, (1, 256), blk[None]), oracle.F32)[0]
+        want = (d * sc[np.arange(256) // 16] * (q - 32.0)).astype(np.float32)
+        assert np.array_equal(v.view(np.uint32), want.view(np.uint32)), trial
+
+
+def test_q4_k_to_affine_transcode_identity():
+    # "GPTQModel wiki: MLX Apple Silicon", "Packed layouts and exact
+    # transcoding": Q4_K is affine 4-bit with groups of 32, scale d * sc and
+    # bias -dmin * m. With d and dmin powers of two both are exact in bfloat16,
+    # and the affine decoder (another code path) must give the same bits.
+    g = np.random.default_rng(42)
+    rows, k = 6, 512
+    blocks, qs, scl, bia = [], [], [], []
+    for r in range(rows):
+        rb = []
+        for b in range(k // 256):
+            sc, m, q = g.integers(0, 64, 8), g.integers(0, 64, 8), g.integers(0, 16, 256)
+            d, dmin = 2.0 ** int(g.integers(-14, 0)), 2.0 ** int(g.integers(-14, 0))
+            rb.append(_pack_q4_k(_f16(d), _f16(dmin), sc, m, q))
+            qs.append(q)
+            scl.extend(d * sc)
+            bia.extend(-dmin * m)
+        blocks.append(np.concatenate(rb))
+    q = np.concatenate(qs).reshape(rows, k).astype(np.uint64)
+    words = np.zeros((rows, k // 8), np.uint64)
+    for i in range(8):
+        words |= q[:, i::8] << np.uint64(4 * i)
+    wa = oracle.Weight(oracle.AFFINE, (rows, k), words.astype(np.uint32),
+                       synth.to_bf16_bits(np.array(scl, np.float32)).reshape(rows, k // 32),
+                       synth.to_bf16_bits(np.array(bia, np.float32)).reshape(rows, k // 32), bits=4, group_size=32)
+    wk = oracle.Weight(oracle.Q4_K, (rows, k), np.stack(blocks))
+    a, b = oracle.dequant(wa, oracle.F32), oracle.dequant(wk, oracle.F32)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_q6_k_to_affine_transcode_identity():
+    # Q6_K as affine 6-bit with groups of 16: code q, scale d * sc, bias
+    # -32 * d * sc; exact in bfloat16 for d a power of two
+    g = np.random.default_rng(43)
+    rows, k = 5, 512
+    blocks, qs, scl = [], [], []
+    for r in range(rows):
+        rb = []
+        for b in range(k // 256):
+            sc, q = g.integers(-128, 128, 16), g.integers(0, 64, 256)
+            d = 2.0 ** int(g.integers(-14, -2))
+            rb.append(_pack_q6_k(_f16(d), sc, q))
+            qs.append(q)
+            scl.extend(d * sc)
+        blocks.append(np.concatenate(rb))
+    q = np.concatenate(qs).reshape(rows, k)
+    bits = ((q[:, :, None] >> np.arange(6)) & 1).reshape(rows, k * 6)  # little-endian stream
+    words = (bits.reshape(rows, -1, 32).astype(np.uint64) << np.arange(32, dtype=np.uint64)).sum(axis=2)
+    s = np.array(scl, np.float32).reshape(rows, k // 16)
+    wa = oracle.Weight(oracle.AFFINE, (rows, k), words.astype(np.uint32), synth.to_bf16_bits(s),
+                       synth.to_bf16_bits(-32.0 * s), bits=6, group_size=16)
+    wk = oracle.Weight(oracle.Q6_K, (rows, k), np.stack(blocks))
+    a, b = oracle.dequant(wa, oracle.F32), oracle.dequant(wk, oracle.F32)
+    same = (a.view(np.uint32) == b.view(np.uint32)) | ((a == 0) & (b == 0))  # (q - 32) * 0 is -0. in Q6_K
+    assert same.all()

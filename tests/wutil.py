@@ -8,7 +8,8 @@ import numpy as np
 
 import oracle
 
-FMT = {"affine": oracle.AFFINE, "q8_0": oracle.Q8_0, "mxfp4": oracle.MXFP4, "mxfp4_blocks": oracle.MXFP4_BLOCKS}
+FMT = {"affine": oracle.AFFINE, "q8_0": oracle.Q8_0, "mxfp4": oracle.MXFP4, "mxfp4_blocks": oracle.MXFP4_BLOCKS,
+       "q4_k": oracle.Q4_K, "q6_k": oracle.Q6_K}
 SDT = {"bf16": oracle.BF16, "f16": oracle.F16, None: oracle.BF16}
 
 
