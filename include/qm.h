@@ -9,9 +9,11 @@
  *              sections "Concepts: method, checkpoint, runtime, and tensor
  *              layout" and "Packed layouts and exact transcoding"; "Quantized
  *              inference in tinygpt's HFModel", section "Problem").
- *              codes  uint32 [..., n, k*bits/32]: one continuous little-endian
- *                     bit stream per row, code i in bits [i*bits, (i+1)*bits)
- *                     (so a 4-bit word holds codes 8j..8j+7, lowest in bits 0..3);
+ *              codes  uint32 [..., n, k*bits/32], bits 2, 3, 4, 5, 6 or 8: one
+ *                     continuous little-endian bit stream per row, code i in
+ *                     bits [i*bits, (i+1)*bits) (so a 4-bit word holds codes
+ *                     8j..8j+7, lowest in bits 0..3; 3-, 5- and 6-bit codes
+ *                     cross words);
  *              scales [..., n, k/group_size] and
  *              biases [..., n, k/group_size], both of scale_dtype, group g
  *                     covering inputs [g*group_size, (g+1)*group_size).
@@ -29,9 +31,19 @@
  *              Mxfp4_blocks): codes uint8 [..., n, k/32*17]; per 32 values the
  *              e8m0 scale byte, then 16 bytes, byte j holding value j of the
  *              block in its low nibble and value j+16 in its high nibble.
- *              Values as QM_MXFP4. dequant and take decode it in their own
- *              kernels; apply and apply_experts run the plain per-row kernels
- *              for it (no tensor-map pipeline yet).
+ *              Values as QM_MXFP4.
+ *   QM_Q4_K    GGUF Q4_K (same page, "Weights", Q4_K): codes uint8
+ *              [..., n, k/256*144] (k a multiple of 256); per 256 values a
+ *              block of float16 d, float16 dmin, 12 bytes of eight 6-bit
+ *              scales and eight 6-bit mins (one each per sub-block of 32) and
+ *              128 bytes of 4-bit quants, arranged as ggml's block_q4_K;
+ *              value = d*sc*q - dmin*m, products exact, rounded once at the
+ *              subtraction.
+ *   QM_Q6_K    GGUF Q6_K (same page, "Weights", Q6_K): codes uint8
+ *              [..., n, k/256*210]; per 256 values 128 bytes of the quants'
+ *              low 4 bits, 64 bytes of their high 2 bits, sixteen int8 scales
+ *              (sub-blocks of 16) and a float16 d, arranged as ggml's
+ *              block_q6_K; value = d*sc*(q - 32), exact.
  *
  * Every part is contiguous, row-major, on the device, with a 16-byte aligned
  * base address. The caller owns every buffer and the stream. Entry points
@@ -70,7 +82,14 @@ typedef enum qm_status {
     QM_ENOTSUP = 4   /* a valid combination this library does not implement */
 } qm_status;
 
-typedef enum qm_format { QM_AFFINE = 0, QM_Q8_0 = 1, QM_MXFP4 = 2, QM_MXFP4_BLOCKS = 3 } qm_format;
+typedef enum qm_format {
+    QM_AFFINE = 0,
+    QM_Q8_0 = 1,
+    QM_MXFP4 = 2,
+    QM_MXFP4_BLOCKS = 3,
+    QM_Q4_K = 4,
+    QM_Q6_K = 5
+} qm_format;
 typedef enum qm_dtype { QM_F32 = 0, QM_BF16 = 1, QM_F16 = 2 } qm_dtype;
 typedef enum qm_itype { QM_I32 = 0, QM_I64 = 1 } qm_itype;
 
@@ -79,8 +98,9 @@ typedef enum qm_itype { QM_I32 = 0, QM_I64 = 1 } qm_itype;
 /* A packed weight: its format, logical shape [..., n, k] and device parts. */
 typedef struct qm_weight {
     int32_t format;      /* qm_format */
-    int32_t bits;        /* QM_AFFINE: 4 or 8. QM_Q8_0: 8 or 0. QM_MXFP4(_BLOCKS): 4 or 0 */
-    int32_t group_size;  /* QM_AFFINE: 32, 64 or 128. Otherwise 32 or 0 */
+    int32_t bits;        /* QM_AFFINE: 2, 3, 4, 5, 6 or 8. QM_Q8_0: 8 or 0. QM_MXFP4(_BLOCKS),
+                            QM_Q4_K: 4 or 0. QM_Q6_K: 6 or 0 */
+    int32_t group_size;  /* QM_AFFINE: 32, 64 or 128. QM_Q4_K, QM_Q6_K: 256 or 0. Otherwise 32 or 0 */
     int32_t scale_dtype; /* QM_AFFINE: QM_BF16 or QM_F16. Otherwise ignored */
     int32_t ndim;        /* 2 .. QM_MAX_NDIM */
     int64_t shape[QM_MAX_NDIM]; /* logical shape; shape[ndim-1] = k, a multiple of 32 */
@@ -132,7 +152,8 @@ qm_status qm_apply(const qm_weight* w, const void* x, int64_t M, int32_t x_dtype
  * Packed outputs: out_codes / out_scales / out_biases have w's part shapes
  * with shape[axis] replaced by n_ids (pass NULL for parts the format lacks).
  * If out_dense is not NULL it also receives the gathered values decoded and
- * rounded once to out_dtype, shape [..., n_ids, ..., k]. Either the packed
+ * rounded once to out_dtype, shape [..., n_ids, ..., k] (an out-of-range
+ * position decodes its zero bytes: zeros, -0. in Q6_K). Either the packed
  * outputs or out_dense may be omitted (NULL), not both.
  * Defined by "Nx_quant (raven-ml.dev API docs)", section "Products", take. */
 qm_status qm_take(const qm_weight* w, int32_t axis, const void* ids, int32_t id_type,

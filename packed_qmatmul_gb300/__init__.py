@@ -20,7 +20,7 @@ from typing import Optional, Sequence
 import torch
 
 __all__ = [
-    "QM_AFFINE", "QM_Q8_0", "QM_MXFP4", "QM_MXFP4_BLOCKS", "QM_WEIGHT_STATIC", "QM_F32", "QM_BF16", "QM_F16", "QM_I32", "QM_I64",
+    "QM_AFFINE", "QM_Q8_0", "QM_MXFP4", "QM_MXFP4_BLOCKS", "QM_Q4_K", "QM_Q6_K", "QM_WEIGHT_STATIC", "QM_F32", "QM_BF16", "QM_F16", "QM_I32", "QM_I64",
     "QMError", "QWeight", "library_path", "load_library",
     "qm_dequant", "qm_quantize_q8_0", "qm_apply", "qm_take", "qm_apply_experts", "qm_apply_experts_workspace",
     "qm_experts_route_workspace",
@@ -29,7 +29,7 @@ __all__ = [
 ]
 
 QM_OK, QM_EINVAL, QM_ECUDA, QM_ETIMEOUT, QM_ENOTSUP = 0, 1, 2, 3, 4
-QM_AFFINE, QM_Q8_0, QM_MXFP4, QM_MXFP4_BLOCKS = 0, 1, 2, 3
+QM_AFFINE, QM_Q8_0, QM_MXFP4, QM_MXFP4_BLOCKS, QM_Q4_K, QM_Q6_K = 0, 1, 2, 3, 4, 5
 QM_F32, QM_BF16, QM_F16 = 0, 1, 2
 QM_I32, QM_I64 = 0, 1
 QM_WEIGHT_STATIC = 1
@@ -37,7 +37,8 @@ QM_MAX_NDIM = 4
 
 _STATUS = {QM_EINVAL: "QM_EINVAL", QM_ECUDA: "QM_ECUDA", QM_ETIMEOUT: "QM_ETIMEOUT",
            QM_ENOTSUP: "QM_ENOTSUP"}
-_FORMATS = {"affine": QM_AFFINE, "q8_0": QM_Q8_0, "mxfp4": QM_MXFP4, "mxfp4_blocks": QM_MXFP4_BLOCKS}
+_FORMATS = {"affine": QM_AFFINE, "q8_0": QM_Q8_0, "mxfp4": QM_MXFP4, "mxfp4_blocks": QM_MXFP4_BLOCKS,
+            "q4_k": QM_Q4_K, "q6_k": QM_Q6_K}
 _DTYPES = {torch.float32: QM_F32, torch.bfloat16: QM_BF16, torch.float16: QM_F16}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -198,6 +199,10 @@ class QWeight:
             return (tuple(lead) + (k // 32 * 34,), None, None)
         if self.format == QM_MXFP4_BLOCKS:
             return (tuple(lead) + (k // 32 * 17,), None, None)
+        if self.format == QM_Q4_K:
+            return (tuple(lead) + (k // 256 * 144,), None, None)
+        if self.format == QM_Q6_K:
+            return (tuple(lead) + (k // 256 * 210,), None, None)
         return (tuple(lead) + (k // 2,), tuple(lead) + (k // 32,), None)
 
 

@@ -84,7 +84,7 @@ qm_status check_positions(int64_t T, int64_t topk, int64_t E) {
 
 qm_status validate_weight(const qm_weight* w, WDesc* d) {
     if (!w) return fail(QM_EINVAL, "w: NULL weight descriptor");
-    if (w->format != QM_AFFINE && w->format != QM_Q8_0 && w->format != QM_MXFP4 && w->format != QM_MXFP4_BLOCKS)
+    if (w->format < QM_AFFINE || w->format > QM_Q6_K)
         return fail(QM_EINVAL, "w: unknown format " + std::to_string(w->format));
     if (w->ndim < 2 || w->ndim > QM_MAX_NDIM)
         return fail(QM_EINVAL, "w: ndim must be 2.." + std::to_string(QM_MAX_NDIM));
@@ -127,6 +127,19 @@ qm_status validate_weight(const qm_weight* w, WDesc* d) {
         d->bits = 8;
         d->gs = 32;
         d->code_row_bytes = k / 32 * 34;
+    } else if (w->format == QM_Q4_K || w->format == QM_Q6_K) {
+        const bool q4 = w->format == QM_Q4_K;
+        if (w->bits != 0 && w->bits != (q4 ? 4 : 6))
+            return fail(QM_EINVAL, std::string("w: ") + (q4 ? "Q4_K bits must be 4 (or 0)" : "Q6_K bits must be 6 (or 0)"));
+        if (w->group_size != 0 && w->group_size != 256)
+            return fail(QM_EINVAL, "w: K-quant group_size must be 256 (or 0)");
+        if (k % 256 != 0)
+            return fail(QM_EINVAL, "codes: k = " + std::to_string(k) + " is not a multiple of 256 (K-quant blocks)");
+        if (w->scales) return fail(QM_EINVAL, "scales: K-quant blocks hold their scales; pass NULL");
+        if (w->biases) return fail(QM_EINVAL, "biases: K-quant blocks hold their mins; pass NULL");
+        d->bits = q4 ? 4 : 6;
+        d->gs = 256;
+        d->code_row_bytes = k / 256 * (q4 ? 144 : 210);
     } else if (w->format == QM_MXFP4_BLOCKS) {
         if (w->bits != 0 && w->bits != 4) return fail(QM_EINVAL, "w: MXFP4 bits must be 4 (or 0)");
         if (w->group_size != 0 && w->group_size != 32)

@@ -97,6 +97,65 @@ QM_DEV void decode_unit(const DecodeArgs& a, int64_t r, int64_t u, float (&v)[32
             v[2 * i] = d * static_cast<float>(static_cast<int8_t>(two & 0xFF));
             v[2 * i + 1] = d * static_cast<float>(static_cast<int8_t>(two >> 8));
         }
+    } else if constexpr (FMT == QM_Q4_K) {
+        // "Nx_quant", "Weights", Q4_K (ggml's block_q4_K): unit u is sub-block
+        // j = u mod 8 of block u / 8; its 32 quants are the low (j even) or
+        // high (j odd) nibbles of quant bytes 32(j/2) .. 32(j/2) + 31; its
+        // 6-bit scale and min come from the 12 bytes after d and dmin. value
+        // = (d * sc) * q - dmin * m: exact products, one rounding (fmaf).
+        const uint8_t* blk = a.codes + r * a.code_row_bytes + (u / 8) * 144;
+        const int j = static_cast<int>(u % 8);
+        const uint4 hdr = __ldg(reinterpret_cast<const uint4*>(blk));
+        const float d = f16_bits_to_f32(hdr.x & 0xFFFFu), dmin = f16_bits_to_f32(hdr.x >> 16);
+        // byte i of the 12 scale/min bytes (header bytes 4 .. 15), by selects
+        auto sb = [&](int i) -> int {
+            const uint32_t wd = i < 4 ? hdr.y : (i < 8 ? hdr.z : hdr.w);
+            return static_cast<int>((wd >> (8 * (i & 3))) & 0xFFu);
+        };
+        int sc, mn;
+        if (j < 4) {
+            sc = sb(j) & 63;
+            mn = sb(4 + j) & 63;
+        } else {
+            sc = (sb(4 + j) & 15) | ((sb(j - 4) >> 6) << 4);
+            mn = (sb(4 + j) >> 4) | ((sb(j) >> 6) << 4);
+        }
+        const float d1 = d * static_cast<float>(sc), m1 = dmin * static_cast<float>(mn);
+        const uint4* qp = reinterpret_cast<const uint4*>(blk + 16 + 32 * (j / 2));
+        const int sh = (j & 1) ? 4 : 0;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint4 q = __ldg(qp + h);
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+                v[16 * h + e] = fmaf(d1, static_cast<float>((w[e / 4] >> (8 * (e % 4) + sh)) & 15u), -m1);
+        }
+    } else if constexpr (FMT == QM_Q6_K) {
+        // "Nx_quant", "Weights", Q6_K (ggml's block_q6_K): unit u is quarter
+        // t = u mod 4 of half h = (u / 4) mod 2 of block u / 8; value l of it
+        // has its low 4 bits in ql[64h + l + 32(t mod 2)] (low nibble for
+        // t < 2), its high 2 bits at bit 2t of qh[32h + l] and the int8 scale
+        // scales[8h + 2t + l/16]; value = (d * sc) * (q - 32), exact.
+        const uint8_t* blk = a.codes + r * a.code_row_bytes + (u / 8) * 210;  // 2-byte aligned
+        const int h = static_cast<int>((u / 4) % 2), t = static_cast<int>(u % 4);
+        const uint16_t* ql = reinterpret_cast<const uint16_t*>(blk + 64 * h + 32 * (t % 2));
+        const uint16_t* qh = reinterpret_cast<const uint16_t*>(blk + 128 + 32 * h);
+        const float d = f16_bits_to_f32(__ldg(reinterpret_cast<const uint16_t*>(blk + 208)));
+        const uint32_t scw = __ldg(reinterpret_cast<const uint16_t*>(blk + 192 + 8 * h + 2 * t));
+        const float d0 = d * static_cast<float>(static_cast<int8_t>(scw & 0xFF));
+        const float d1 = d * static_cast<float>(static_cast<int8_t>(scw >> 8));
+        const int lsh = t < 2 ? 0 : 4, hsh = 2 * t;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const uint32_t lo2 = __ldg(ql + e), hi2 = __ldg(qh + e);  // values 2e and 2e + 1
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                const int l = 2 * e + b;
+                const int q = static_cast<int>(((lo2 >> (8 * b + lsh)) & 15u) | (((hi2 >> (8 * b + hsh)) & 3u) << 4));
+                v[l] = (l < 16 ? d0 : d1) * static_cast<float>(q - 32);
+            }
+        }
     } else if constexpr (FMT == QM_MXFP4_BLOCKS) {
         // GGUF's 17-byte block: the e8m0 scale byte, then byte j holding value j
         // (low nibble) and value j + 16 (high nibble); blocks are byte-aligned
@@ -197,8 +256,10 @@ __global__ void __launch_bounds__(256) decode_rows_kernel(DecodeArgs a, int64_t 
         if (src >= 0) {
             decode_unit<FMT, BITS>(a, src, u, v);
         } else {
+            // an out-of-range position gathers zero bytes: their values are
+            // zeros, -0. in Q6_K ("Nx_quant", "Weights")
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = 0.0f;
+            for (int i = 0; i < 32; ++i) v[i] = FMT == QM_Q6_K ? -0.0f : 0.0f;
         }
         store_unit<OUT>(out, t * 32, v);
     }
@@ -227,6 +288,8 @@ cudaError_t launch_decode_rows(const WDesc& w, int64_t out_rows, Map map, int ou
     QM_DECODE_OUTS(QM_Q8_0, 8)
     QM_DECODE_OUTS(QM_MXFP4, 4)
     QM_DECODE_OUTS(QM_MXFP4_BLOCKS, 4)
+    QM_DECODE_OUTS(QM_Q4_K, 4)
+    QM_DECODE_OUTS(QM_Q6_K, 6)
 #undef QM_DECODE_OUTS
 #undef QM_DECODE_CASE
     return cudaErrorInvalidValue;
@@ -250,6 +313,24 @@ __global__ void __launch_bounds__(256) take_packed_kernel(TakeParts tp, int64_t 
         const int64_t id = id64 ? __ldg(static_cast<const int64_t*>(ids) + q)
                                 : static_cast<int64_t>(__ldg(static_cast<const int32_t*>(ids) + q));
         const bool in = id >= 0 && id < len;
+        if (tp.one_each) {
+            // every part's row is at most 32 pieces: one piece per lane and part,
+            // all loads issued before any store (one memory round trip, not three)
+            V v[3];
+#pragma unroll
+            for (int part = 0; part < 3; ++part) {
+                memset(&v[part], 0, sizeof(V));
+                const int64_t vpr = tp.inner[part] / static_cast<int64_t>(sizeof(V));
+                if (part < tp.n && in && lane < vpr)
+                    v[part] = __ldg(reinterpret_cast<const V*>(tp.src[part] + (o * len + id) * tp.inner[part]) + lane);
+            }
+#pragma unroll
+            for (int part = 0; part < 3; ++part) {
+                const int64_t vpr = tp.inner[part] / static_cast<int64_t>(sizeof(V));
+                if (part < tp.n && lane < vpr) reinterpret_cast<V*>(tp.dst[part] + r * tp.inner[part])[lane] = v[part];
+            }
+            continue;
+        }
 #pragma unroll 1
         for (int part = 0; part < tp.n; ++part) {
             const int64_t vpr = tp.inner[part] / static_cast<int64_t>(sizeof(V));
@@ -349,7 +430,11 @@ cudaError_t launch_take_packed(const TakeParts& tp, int64_t outer, int64_t len, 
     for (int part = 0; part < tp.n; ++part) common |= tp.inner[part];
     auto go = [&](auto vec) -> cudaError_t {
         using V = decltype(vec);
-        return launch_pdl(take_packed_kernel<V>, static_cast<unsigned>(blocks), 256, 0, st, tp, outer, len, ids,
+        TakeParts t2 = tp;
+        t2.one_each = 1;
+        for (int part = 0; part < tp.n; ++part)
+            if (tp.inner[part] > 32 * static_cast<int64_t>(sizeof(V))) t2.one_each = 0;
+        return launch_pdl(take_packed_kernel<V>, static_cast<unsigned>(blocks), 256, 0, st, t2, outer, len, ids,
                           id64, n_ids);
     };
     if (common % 16 == 0) return go(uint4{});
@@ -423,6 +508,10 @@ cudaError_t launch_apply_simple(const WDesc& w, const void* x, int64_t M, void* 
         apply_simple_kernel<QM_Q8_0, 8><<<static_cast<unsigned>(blocks), 256, 0, st>>>(a, w.n, xb, M, yb);
     else if (w.fmt == QM_MXFP4_BLOCKS)
         apply_simple_kernel<QM_MXFP4_BLOCKS, 4><<<static_cast<unsigned>(blocks), 256, 0, st>>>(a, w.n, xb, M, yb);
+    else if (w.fmt == QM_Q4_K)
+        apply_simple_kernel<QM_Q4_K, 4><<<static_cast<unsigned>(blocks), 256, 0, st>>>(a, w.n, xb, M, yb);
+    else if (w.fmt == QM_Q6_K)
+        apply_simple_kernel<QM_Q6_K, 6><<<static_cast<unsigned>(blocks), 256, 0, st>>>(a, w.n, xb, M, yb);
     else
         apply_simple_kernel<QM_MXFP4, 4><<<static_cast<unsigned>(blocks), 256, 0, st>>>(a, w.n, xb, M, yb);
     return cudaGetLastError();

@@ -219,6 +219,26 @@ QM_DEV float value_at(const ExpArgs& a, int64_t r, int64_t i) {
         const uint8_t* blk = a.codes + r * a.code_row_bytes + (i / 32) * 34;
         const float d = f16_bits_to_f32(*reinterpret_cast<const uint16_t*>(blk));
         return d * static_cast<float>(static_cast<int8_t>(blk[2 + i % 32]));
+    } else if constexpr (FMT == QM_Q4_K) {
+        // ggml's block_q4_K: d, dmin, 12 bytes of 6-bit scales and mins, 128 quant bytes
+        const uint8_t* blk = a.codes + r * a.code_row_bytes + (i / 256) * 144;
+        const int v = static_cast<int>(i % 256), c = v / 64, rr = v % 64, j = 2 * c + (rr >= 32);
+        const float d = f16_bits_to_f32(blk[0] | (blk[1] << 8)), dmin = f16_bits_to_f32(blk[2] | (blk[3] << 8));
+        const uint8_t* sb = blk + 4;
+        const int sc = j < 4 ? (sb[j] & 63) : ((sb[4 + j] & 15) | ((sb[j - 4] >> 6) << 4));
+        const int mn = j < 4 ? (sb[4 + j] & 63) : ((sb[4 + j] >> 4) | ((sb[j] >> 6) << 4));
+        const uint8_t byte = blk[16 + 32 * c + rr % 32];
+        const int q = rr < 32 ? (byte & 15) : (byte >> 4);
+        return fmaf(d * static_cast<float>(sc), static_cast<float>(q), -(dmin * static_cast<float>(mn)));
+    } else if constexpr (FMT == QM_Q6_K) {
+        // ggml's block_q6_K: 128 bytes of low 4 bits, 64 of high 2 bits, 16 int8 scales, d
+        const uint8_t* blk = a.codes + r * a.code_row_bytes + (i / 256) * 210;
+        const int v = static_cast<int>(i % 256), h = v / 128, t = (v % 128) / 32, l = v % 32;
+        const uint8_t lo = blk[64 * h + l + 32 * (t % 2)];
+        const int q = ((t < 2 ? lo : (lo >> 4)) & 15) | (((blk[128 + 32 * h + l] >> (2 * t)) & 3) << 4);
+        const float d = f16_bits_to_f32(blk[208] | (blk[209] << 8));
+        return d * static_cast<float>(static_cast<int8_t>(blk[192 + 8 * h + 2 * t + l / 16])) *
+               static_cast<float>(q - 32);
     } else if constexpr (FMT == QM_MXFP4_BLOCKS) {
         // GGUF's 17-byte block: the scale byte, then byte j holding value j
         // (low nibble) and value j + 16 (high nibble)
@@ -352,6 +372,8 @@ qm_status launch_experts(const WDesc& w, const void* ids, int id64, int64_t T, i
     else if (w.fmt == QM_AFFINE) QM_EXP_CASE(QM_AFFINE, 8);
     else if (w.fmt == QM_Q8_0) QM_EXP_CASE(QM_Q8_0, 8);
     else if (w.fmt == QM_MXFP4_BLOCKS) QM_EXP_CASE(QM_MXFP4_BLOCKS, 4);
+    else if (w.fmt == QM_Q4_K) QM_EXP_CASE(QM_Q4_K, 4);
+    else if (w.fmt == QM_Q6_K) QM_EXP_CASE(QM_Q6_K, 6);
     else QM_EXP_CASE(QM_MXFP4, 4);
 #undef QM_EXP_CASE
     e = cudaGetLastError();

@@ -74,6 +74,7 @@ cudaError_t launch_quantize_q8_0(const void* x, int x_dtype, int64_t rows, int64
 // source of `len` rows of inner[part] bytes per outer index and a destination.
 struct TakeParts {
     int n = 0;
+    int one_each = 0;  // every part's row fits one piece per lane of a warp
     const uint8_t* src[3] = {nullptr, nullptr, nullptr};
     uint8_t* dst[3] = {nullptr, nullptr, nullptr};
     int64_t inner[3] = {0, 0, 0};

@@ -707,3 +707,77 @@ def test_affine_widths_experts(bits, T):
     ids = synth.expert_ids(g, T, 2, E)
     ids[2, 1] = -1
     _check_experts(w, ids, synth.activations(g, T, k), f"affine{bits} experts T={T}")
+
+
+# ---------------------------------------------------------------- GGUF Q4_K and Q6_K
+# "Nx_quant", "Weights": Q4_K (144-byte blocks of 256 values: d, dmin, 6-bit
+# scales and mins, 4-bit quants) and Q6_K (210-byte blocks: 6-bit quants,
+# int8 sub-block scales, d), each arranged as ggml's block layout.
+def _kquant(kind, g, n, k, lead=()):
+    w = (synth.q4_k_weight if kind == "q4_k" else synth.q6_k_weight)(g, n, k, lead=lead)
+    nb = 144 if kind == "q4_k" else 210
+    b = w["codes"].reshape(-1, nb)
+    if b.shape[0] >= 6:  # special blocks: all zero bytes, an infinite d, a NaN d, a subnormal d
+        b[0] = 0
+        dpos = 0 if kind == "q4_k" else 208
+        for i, d in ((1, 0x7C00), (2, 0x7E00), (3, 0x0001)):
+            b[i, dpos], b[i, dpos + 1] = d & 0xFF, d >> 8
+        if kind == "q4_k":
+            b[4, 2], b[4, 3] = 0x00, 0xFC  # dmin = -inf
+    return w
+
+
+@pytest.mark.parametrize("kind", ["q4_k", "q6_k"])
+@pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16, torch.float16])
+def test_kquant_dequant_bit_exact(kind, dt):
+    g = synth.rng(1800)
+    for n, k, lead in ((37, 256, ()), (5, 1024, (3,)), (2, 512, (2, 2))):
+        w = _kquant(kind, g, n, k, lead)
+        got = _host(qm.dequant(qm.QWeight.from_arrays(w), dt))
+        assert _bits_equal(got, oracle.dequant(to_oracle(w), ODT[dt]), dt), (kind, n, k, lead)
+
+
+@pytest.mark.parametrize("kind", ["q4_k", "q6_k"])
+def test_kquant_take(kind):
+    g = synth.rng(1801)
+    for lead, axis in (((), 0), ((3,), 0), ((3,), 1)):
+        w = _kquant(kind, g, 24, 512, lead)
+        ow = to_oracle(w)
+        L = ow.shape[axis]
+        ids = np.array([L - 1, 0, -1, L, 2, 2, 1], dtype=np.int32)
+        tw, dense = qm.take(qm.QWeight.from_arrays(w), axis, torch.from_numpy(ids).cuda(),
+                            dense_dtype=torch.bfloat16)
+        ot = oracle.take(ow, axis, ids)
+        assert tw.scales is None and tw.biases is None
+        assert np.array_equal(_host(tw.codes).view(np.uint8).reshape(-1), ot.codes.reshape(-1)), (lead, axis)
+        assert _bits_equal(_host(dense), oracle.dequant(ot, oracle.BF16), torch.bfloat16), (lead, axis)
+
+
+@pytest.mark.parametrize("kind", ["q4_k", "q6_k"])
+@pytest.mark.parametrize("M", [1, 3, 16, 33, 130])
+def test_kquant_apply(kind, M):
+    g = synth.rng(1810 + M)
+    for n, k in ((96, 256), (200, 1024), (33, 2048)):
+        w = (synth.q4_k_weight if kind == "q4_k" else synth.q6_k_weight)(g, n, k)
+        _check_apply(w, synth.activations(g, M, k), f"{kind} n={n} k={k} M={M}")
+
+
+@pytest.mark.parametrize("kind", ["q4_k", "q6_k"])
+@pytest.mark.parametrize("M", [1, 33])
+def test_kquant_apply_nonfinite_scales(kind, M):
+    # blocks whose d (or Q4_K's dmin) is infinite or NaN: the per-element values'
+    # infinities and NaNs, compared exactly
+    g = synth.rng(1820 + M)
+    w = _kquant(kind, g, 64, 512)
+    _check_apply(w, synth.activations(g, M, 512), f"{kind} special blocks M={M}")
+
+
+@pytest.mark.parametrize("kind", ["q4_k", "q6_k"])
+@pytest.mark.parametrize("T", [12, 100])
+def test_kquant_experts(kind, T):
+    g = synth.rng(1830 + T)
+    E = 4
+    w = (synth.q4_k_weight if kind == "q4_k" else synth.q6_k_weight)(g, 64, 512, lead=(E,))
+    ids = synth.expert_ids(g, T, 2, E)
+    ids[1, 0] = E
+    _check_experts(w, ids, synth.activations(g, T, 512), f"{kind} experts T={T}")

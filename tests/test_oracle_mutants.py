@@ -46,6 +46,18 @@ MUTANTS = {
     "experts_out_of_range_uses_expert0": ("if (id < 0 || id >= E) {\n                for",
                                           "if (id < 0 || id >= E) id = 0;\n            if (0) {\n                for"),
     "experts_broadcast_row": ("return (x_rows == T) ? p / topk : p;", "return (x_rows == T) ? p % T : p;"),
+    "q4_k_nibble_halves": ("int q = (r < 32) ? (byte & 0x0F) : (byte >> 4);",
+                           "int q = (r < 32) ? (byte >> 4) : (byte & 0x0F);"),
+    "q4_k_high_bits_source": ("*sc = (b[8 + (j - 4)] & 0x0F) | ((b[j - 4] >> 6) << 4);",
+                              "*sc = (b[8 + (j - 4)] & 0x0F) | ((b[j] >> 6) << 4);"),
+    "q4_k_scale_min_swap": ("*sc = b[j] & 0x3F;\n        *m = b[4 + j] & 0x3F;",
+                            "*m = b[j] & 0x3F;\n        *sc = b[4 + j] & 0x3F;"),
+    "q4_k_min_sign": ("return (float)(d * sc * q - dmin * m);", "return (float)(d * sc * q + dmin * m);"),
+    "q6_k_offset": ("return (float)(d * sc * (q - 32));", "return (float)(d * sc * (q - 31));"),
+    "q6_k_high_bits": ("int hi = (qh[32 * h + l] >> (2 * t)) & 3;", "int hi = (qh[32 * h + l] >> t) & 3;"),
+    "q6_k_scale_index": ("int sc = scales[8 * h + 2 * t + l / 16];", "int sc = scales[8 * h + 2 * t];"),
+    "q6_k_ql_half": ("uint8_t lo_byte = ql[64 * h + l + 32 * (t % 2)];",
+                     "uint8_t lo_byte = ql[64 * h + l + 32 * (t / 2)];"),
 }
 
 
