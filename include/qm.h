@@ -226,6 +226,15 @@ qm_status qm_experts_route(const void* ids, int32_t id_type, int64_t P, int64_t 
                            int32_t* counts, int32_t* offsets, int32_t* perm, void* workspace,
                            size_t workspace_bytes, qm_stream_t stream);
 
+/* Exercises the failure path of the bounded device waits without a fault:
+ * enqueues one warp that waits on a barrier nothing will complete, with the
+ * same bounded wait the pipelines use but a limit of limit_ns (1 ns .. 10 s,
+ * else QM_EINVAL naming "limit"). The wait gives up, raises the device flag
+ * and the warp exits; a later qm_device_status() reports QM_ETIMEOUT and
+ * clears the flag. The context stays usable. The pages have no counterpart to
+ * this call: it is a check of this library's own error reporting. */
+qm_status qm_check_wait_timeout(uint64_t limit_ns, qm_stream_t stream);
+
 /* Synchronizes `stream`, then reports and clears the device flag raised by a
  * device-side wait that gave up (QM_ETIMEOUT), or QM_ECUDA for an
  * asynchronous CUDA error, or QM_OK. */

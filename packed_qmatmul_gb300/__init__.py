@@ -24,7 +24,8 @@ __all__ = [
     "QMError", "QWeight", "library_path", "load_library",
     "qm_dequant", "qm_quantize_q8_0", "qm_apply", "qm_take", "qm_apply_experts", "qm_apply_experts_workspace",
     "qm_experts_route_workspace",
-    "qm_experts_route", "qm_apply_experts_static", "qm_device_status", "qm_last_error", "qm_version",
+    "qm_experts_route", "qm_apply_experts_static", "qm_check_wait_timeout", "qm_device_status", "qm_last_error",
+    "qm_version",
     "dequant", "quantize_q8_0", "apply", "take", "apply_experts", "route",
 ]
 
@@ -85,6 +86,7 @@ def load_library():
         sigs = {
             "qm_dequant": ([wp, i32, vp, vp], i32),
             "qm_quantize_q8_0": ([vp, i32, i64, i64, vp, vp], i32),
+            "qm_check_wait_timeout": ([ctypes.c_uint64, vp], i32),
             "qm_apply": ([wp, vp, i64, i32, vp, vp], i32),
             "qm_take": ([wp, i32, vp, i32, i64, vp, vp, vp, i32, vp, vp], i32),
             "qm_apply_experts_workspace": ([wp, i64, i64], sz),
@@ -275,6 +277,10 @@ def qm_experts_route(ids: torch.Tensor, E: int, counts: torch.Tensor, offsets: t
     _check(load_library().qm_experts_route(
         _ptr(ids), id_type, ids.numel(), E, _ptr(counts), _ptr(offsets), _ptr(perm),
         _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)))
+
+
+def qm_check_wait_timeout(limit_ns: int, stream=None) -> None:
+    _check(load_library().qm_check_wait_timeout(limit_ns, _stream(stream)))
 
 
 def qm_device_status(stream=None) -> None:

@@ -445,6 +445,13 @@ qm_status qm_experts_route(const void* ids, int32_t id_type, int64_t P, int64_t 
                         "route launch");
 }
 
+qm_status qm_check_wait_timeout(uint64_t limit_ns, qm_stream_t stream) {
+    set_error("");
+    if (limit_ns == 0 || limit_ns > 10ull * 1000 * 1000 * 1000)
+        return fail(QM_EINVAL, "limit: must be between 1 ns and 10 s");
+    return check_launch(launch_wait_timeout(limit_ns, reinterpret_cast<cudaStream_t>(stream)), "wait check launch");
+}
+
 qm_status qm_device_status(qm_stream_t stream) {
     set_error("");
     cudaError_t e = cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream));

@@ -61,14 +61,16 @@ QM_DEV bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // The waiting part of mbar_wait, kept out of line: every call site then
-// costs one try_wait and a call, not a copy of the spin loop.
-static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity) {
+// costs one try_wait and a call, not a copy of the spin loop. Gives up after
+// limit_ns of %globaltimer; the round count is bounded too (64 tries take far
+// longer than a nanosecond each), so the wait ends even if the timer stood still.
+static __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, uint64_t limit_ns = kWaitLimitNs) {
     const uint64_t t0 = globaltimer();
-    for (;;) {
+    for (uint64_t round = 0;; ++round) {
 #pragma unroll 1
         for (int i = 0; i < 64; ++i)
             if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer() - t0 > kWaitLimitNs) return false;
+        if (globaltimer() - t0 > limit_ns || round > limit_ns) return false;
     }
 }
 

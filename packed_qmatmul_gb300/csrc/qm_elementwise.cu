@@ -408,6 +408,28 @@ cudaError_t launch_quantize_q8_0(const void* x, int x_dtype, int64_t rows, int64
     return launch_pdl(quantize_q8_0_kernel<QM_F16>, static_cast<unsigned>(grid), 256, 0, st, x, nblocks, blocks);
 }
 
+// ------------------------------------------------------------ bounded-wait check
+// One warp waits on an mbarrier that nothing arrives at, with the bounded wait
+// every pipeline uses; it gives up after limit_ns, raises this file's device
+// flag and exits. Nothing faults and nothing is left waiting.
+namespace {
+__global__ void __launch_bounds__(32) wait_timeout_kernel(uint64_t limit_ns) {
+    __shared__ __align__(8) uint64_t bar;
+    const uint32_t b = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+        mbar_init(b, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    if (threadIdx.x == 0 && !mbar_wait_slow(b, 0, limit_ns)) atomicOr(&g_err_elementwise, DEV_ERR_TIMEOUT);
+}
+}  // namespace
+
+cudaError_t launch_wait_timeout(uint64_t limit_ns, cudaStream_t st) {
+    wait_timeout_kernel<<<1, 32, 0, st>>>(limit_ns);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_dequant(const WDesc& w, int out_dtype, void* out, cudaStream_t st) {
     return launch_decode_rows(w, w.rows, IdentityMap{}, out_dtype, out, st);
 }

@@ -128,6 +128,9 @@ qm_status apply_experts_checked(const qm_weight* w, const void* ids, int32_t id_
                                 void* workspace, size_t workspace_bytes, qm_stream_t stream,
                                 bool allow_tensor);
 
+// One warp waiting on a barrier nothing arrives at, giving up after limit_ns.
+cudaError_t launch_wait_timeout(uint64_t limit_ns, cudaStream_t st);
+
 // Per-translation-unit device error flags: read-and-clear (after a sync).
 uint32_t elementwise_read_clear_error();
 uint32_t gemv_read_clear_error();
