@@ -59,12 +59,14 @@ constexpr int NR = 2;           // raw chunk slots
 // whether the TMA box is 128B-swizzled, and the tensor map's element size.
 // Affine 2, 3, 5 and 6-bit codes (GEN) come as 128 inputs per row, 16 * BITS
 // bytes, unswizzled (a row's codes then start on a 4-byte boundary).
+// Q4_K comes as one 144-byte block (256 inputs) per row, unswizzled: rows 144
+// bytes (nine 16-byte units) apart put consecutive rows in distinct bank groups.
 template <int FMT, int BITS>
 struct Raw {
     static constexpr bool GEN = FMT == QM_AFFINE && BITS != 4 && BITS != 8;
     static constexpr int RAWK = (GEN || (FMT == QM_AFFINE && BITS == 8)) ? 128 : 256;
-    static constexpr int BYTES = GEN ? 16 * BITS : (FMT == QM_Q8_0) ? 272 : 128;
-    static constexpr bool SW = FMT != QM_Q8_0 && !GEN;
+    static constexpr int BYTES = GEN ? 16 * BITS : (FMT == QM_Q8_0) ? 272 : (FMT == QM_Q4_K) ? 144 : 128;
+    static constexpr bool SW = FMT != QM_Q8_0 && FMT != QM_Q4_K && !GEN;
     static constexpr int ELEM = (FMT == QM_Q8_0) ? 2 : 1;
     static constexpr int SPR = RAWK / BK;  // k steps per chunk
 };
@@ -211,6 +213,40 @@ QM_DEV void decode32(const uint8_t* raw, int row, int kk, int half, Sc sc, uint3
                 const float2 v = fma2(add2(f, neg), s2, b2);  // exact code, then one rounding
                 o[(j * PER + i) / 2] = bf2(v.x, v.y);
             }
+    } else if constexpr (FMT == QM_Q4_K) {
+        // sub-block j = 2 kk + half of the row's block: 32 quant bytes from byte
+        // 16 + 32 kk, their low (half 0) or high (half 1) nibbles; value =
+        // (d * sc) * q - dmin * m, exact products and one rounding
+        const uint8_t* blk = raw + row * 144;
+        const uint4 h = *reinterpret_cast<const uint4*>(blk);
+        const int j = 2 * kk + half;
+        auto sb = [&](int i) -> int {
+            const uint32_t wd = i < 4 ? h.y : (i < 8 ? h.z : h.w);
+            return static_cast<int>((wd >> (8 * (i & 3))) & 0xFFu);
+        };
+        const int sc = j < 4 ? (sb(j) & 63) : ((sb(4 + j) & 15) | ((sb(j - 4) >> 6) << 4));
+        const int mn = j < 4 ? (sb(4 + j) & 63) : ((sb(4 + j) >> 4) | ((sb(j) >> 6) << 4));
+        const float d1 = f16_bits_to_f32(h.x & 0xFFFFu) * static_cast<float>(sc);
+        const float m1 = f16_bits_to_f32(h.x >> 16) * static_cast<float>(mn);
+        const float2 d2 = make_float2(d1, d1), nm2 = make_float2(-m1, -m1);
+        const float2 neg = make_float2(-8388608.0f, -8388608.0f);
+        const int sh = half ? 4 : 0;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const uint4 v = *reinterpret_cast<const uint4*>(blk + 16 + 32 * kk + 16 * q);
+            const uint32_t ws[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t c = (ws[e] >> sh) & 0x0F0F0F0Fu;  // four values, one per byte
+#pragma unroll
+                for (int i = 0; i < 4; i += 2) {
+                    const float2 f = make_float2(__uint_as_float(prmt(c, 0x4B000000u, 0x7540 + i)),
+                                                 __uint_as_float(prmt(c, 0x4B000000u, 0x7541 + i)));
+                    const float2 val = fma2(add2(f, neg), d2, nm2);
+                    o[(16 * q + 4 * e + i) / 2] = bf2(val.x, val.y);
+                }
+            }
+        }
     } else if constexpr (FMT == QM_MXFP4) {
         const uint4 w = *reinterpret_cast<const uint4*>(raw + sw128(row, kk * 2 + half));
         const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
@@ -700,6 +736,7 @@ static cudaError_t dispatch(Params& p, const WDesc& w, const void* x, cudaStream
     if (w.fmt == QM_AFFINE && w.bits == 8 && w.gs == 128) return launch_bm<QM_AFFINE, 8, 128>(p, w, x, st);
     if (w.fmt == QM_Q8_0) return launch_bm<QM_Q8_0, 8, 32>(p, w, x, st);
     if (w.fmt == QM_MXFP4) return launch_bm<QM_MXFP4, 4, 32>(p, w, x, st);
+    if (w.fmt == QM_Q4_K) return launch_bm<QM_Q4_K, 4, 0>(p, w, x, st);
     return cudaErrorInvalidValue;
 }
 

@@ -69,7 +69,12 @@ struct Args {
 // Words of packed data a lane holds for one row and one chunk.
 template <int FMT, int BITS>
 struct Words {
-    static constexpr int N = FMT == QM_AFFINE ? BITS : FMT == QM_Q8_0 ? 9 : FMT == QM_MXFP4 ? 4 : 5;
+    static constexpr int N = FMT == QM_AFFINE  ? BITS
+                             : FMT == QM_Q8_0  ? 9
+                             : FMT == QM_MXFP4 ? 4
+                             : FMT == QM_Q4_K  ? 12
+                             : FMT == QM_Q6_K  ? 20
+                                               : 5;
 };
 
 // One lane's data for one row of one step: code words and the raw scale
@@ -81,9 +86,11 @@ struct Lane {
     uint32_t off;    // Q8_0 / MXFP4 blocks: byte offset of the block in w[0]
 };
 
-// The aligned 32-bit word holding byte `a` of the codes.
+// The aligned 32-bit word holding the byte at base + a (aligned as an address:
+// a row of GGUF blocks may start at any even or odd byte).
 QM_DEV uint32_t ldw(const uint8_t* base, int64_t a) {
-    return __ldg(reinterpret_cast<const uint32_t*>(base + (a & ~int64_t(3))));
+    const uintptr_t p = reinterpret_cast<uintptr_t>(base + a) & ~uintptr_t(3);
+    return __ldg(reinterpret_cast<const uint32_t*>(p));
 }
 
 // Loads lane data for row `row`, inputs [i0, i0 + 32). Rows past n and inputs
@@ -134,6 +141,41 @@ QM_DEV void load_lane(const Args& a, int64_t row, int64_t i0, Lane<FMT, BITS>& L
         L.s = __ldg(a.scales + row * a.scale_row_bytes + i0 / 32);
         L.b = 0u;
         L.off = 0u;
+    } else if constexpr (FMT == QM_Q4_K) {
+        // sub-block j = (i0 / 32) mod 8 of block i0 / 256 (144 bytes, 16-byte aligned):
+        // the 16-byte header (d, dmin, scales and mins), then the 32 quant bytes
+        // whose low (j even) or high (j odd) nibbles are its values
+        const uint8_t* blk = rp + (i0 / 256) * 144;
+        const int j = static_cast<int>((i0 / 32) % 8);
+        const uint4 h = __ldg(reinterpret_cast<const uint4*>(blk));
+        const uint4* qp = reinterpret_cast<const uint4*>(blk + 16 + 32 * (j / 2));
+        const uint4 q0 = __ldg(qp), q1 = __ldg(qp + 1);
+        L.w[0] = h.x; L.w[1] = h.y; L.w[2] = h.z; L.w[3] = h.w;
+        L.w[4] = q0.x; L.w[5] = q0.y; L.w[6] = q0.z; L.w[7] = q0.w;
+        L.w[8] = q1.x; L.w[9] = q1.y; L.w[10] = q1.z; L.w[11] = q1.w;
+        L.off = static_cast<uint32_t>(j);
+        L.s = L.b = 0u;
+    } else if constexpr (FMT == QM_Q6_K) {
+        // quarter t of half h (j = 4h + t = (i0 / 32) mod 8) of block i0 / 256 (210
+        // bytes, 2-byte aligned): the aligned words holding its 32 ql bytes and 32
+        // qh bytes, and those holding its two scales and d
+        const int64_t a0 = (i0 / 256) * 210;
+        const int j = static_cast<int>((i0 / 32) % 8), h = j / 4, t = j % 4;
+        const int64_t aql = a0 + 64 * h + 32 * (t % 2), aqh = a0 + 128 + 32 * h;
+#pragma unroll
+        for (int q = 0; q < 9; ++q) {
+            L.w[q] = ldw(rp, aql + 4 * q);
+            L.w[9 + q] = ldw(rp, aqh + 4 * q);
+        }
+        L.w[18] = ldw(rp, a0 + 192 + 8 * h + 2 * t);
+        L.w[19] = ldw(rp, a0 + 208);
+        // bits 0-1: ql's byte offset within its word; bits 2-3: qh's; bits 4-5: the
+        // scales'; bits 6-7: d's; bits 8-9: t
+        const uintptr_t base = reinterpret_cast<uintptr_t>(rp);
+        L.off = static_cast<uint32_t>(((base + aql) & 3) | (((base + aqh) & 3) << 2) |
+                                      (((base + a0 + 192 + 8 * h + 2 * t) & 3) << 4) | (((base + a0 + 208) & 3) << 6) |
+                                      (t << 8));
+        L.s = L.b = 0u;
     } else {  // MXFP4 in GGUF's 17-byte blocks: the five aligned words holding them
         const int64_t a0 = (i0 / 32) * 17;
         L.off = static_cast<uint32_t>((reinterpret_cast<uintptr_t>(rp) + a0) & 3u);
@@ -183,7 +225,7 @@ QM_DEV void load_acts(const Args& a, int64_t i0, Acts<FMT, BITS>& X) {
             X.p[j] = make_float2(lo(2 * j), hi(2 * j + 1));
         }
     }
-    if constexpr (FMT == QM_AFFINE) {
+    if constexpr (FMT == QM_AFFINE || FMT == QM_Q4_K) {  // for the bias (the Q4_K min) term
         float2 s = make_float2(0.0f, 0.0f);
 #pragma unroll
         for (int j = 0; j < 16; ++j) s = add2(s, X.p[j]);
@@ -248,6 +290,15 @@ QM_DEV float lane_dot(const Lane<FMT, BITS>& L, const Acts<FMT, BITS>& X) {
             acc = fma2(add2(two_bytes(qw, 0x7540, 0x7541), neg), X.p[2 * j], acc);
             acc = fma2(add2(two_bytes(qw, 0x7542, 0x7543), neg), X.p[2 * j + 1], acc);
         }
+    } else if constexpr (FMT == QM_Q4_K) {
+        const float2 neg = make_float2(-8388608.0f, -8388608.0f);
+        const uint32_t sh = (L.off & 1u) ? 4u : 0u;  // odd sub-blocks: the high nibbles
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const uint32_t c = (L.w[4 + q] >> sh) & 0x0F0F0F0Fu;  // values 4q .. 4q + 3
+            acc = fma2(add2(two_bytes(c, 0x7540, 0x7541), neg), X.p[2 * q], acc);
+            acc = fma2(add2(two_bytes(c, 0x7542, 0x7543), neg), X.p[2 * q + 1], acc);
+        }
     } else if constexpr (FMT == QM_MXFP4) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -274,6 +325,41 @@ QM_DEV float lane_dot(const Lane<FMT, BITS>& L, const Acts<FMT, BITS>& X) {
 
 QM_DEV float sval(uint32_t h, int sdt) { return sdt == QM_F16 ? f16_bits_to_f32(h) : bf16_bits_to_f32(h); }
 
+// Q6_K: the lane's two sums over (q - 32) * x, values 0..15 and 16..31 (each
+// half has its own sub-block scale).
+QM_DEV float2 q6_k_dots(const uint32_t (&w)[20], uint32_t off, const float2 (&xp)[16]) {
+    const uint32_t oql = 8u * (off & 3u), oqh = 8u * ((off >> 2) & 3u);
+    const uint32_t t = (off >> 8) & 3u;
+    const uint32_t lsh = t >= 2 ? 4u : 0u, hsh = 2u * t;
+    const float2 neg = make_float2(-8388640.0f, -8388640.0f);  // -(2^23 + 32)
+    float2 a0 = make_float2(0.0f, 0.0f), a1 = make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {  // values 4q .. 4q + 3
+        const uint32_t lw = oql ? __funnelshift_r(w[q], w[q + 1], oql) : w[q];
+        const uint32_t hw = oqh ? __funnelshift_r(w[9 + q], w[10 + q], oqh) : w[9 + q];
+        const uint32_t c = ((lw >> lsh) & 0x0F0F0F0Fu) | (((hw >> hsh) & 0x03030303u) << 4);  // 6-bit q per byte
+        float2& a = q < 4 ? a0 : a1;
+        a = fma2(add2(two_bytes(c, 0x7540, 0x7541), neg), xp[2 * q], a);
+        a = fma2(add2(two_bytes(c, 0x7542, 0x7543), neg), xp[2 * q + 1], a);
+    }
+    return make_float2(a0.x + a0.y, a1.x + a1.y);
+}
+
+// Q4_K: sub-block j's 6-bit scale and min from the 12 bytes after d and dmin
+// (header words 1..3): sub-blocks 0..3 from the low 6 bits of bytes j and
+// j + 4, 4..7 from the nibbles of byte j + 4 with their top two bits from the
+// top bits of bytes j - 4 and j.
+QM_DEV void q4_k_scale_min(const uint32_t (&w)[12], int j, int& sc, int& mn) {
+    auto sb = [&](int i) -> int { return static_cast<int>((w[1 + (i >> 2)] >> (8 * (i & 3))) & 0xFFu); };
+    if (j < 4) {
+        sc = sb(j) & 63;
+        mn = sb(4 + j) & 63;
+    } else {
+        sc = (sb(4 + j) & 15) | ((sb(j - 4) >> 6) << 4);
+        mn = (sb(4 + j) >> 4) | ((sb(j) >> 6) << 4);
+    }
+}
+
 // The e8m0 scale of a GGUF MXFP4 block held in the lane's words.
 QM_DEV uint32_t blocks_scale_byte(const uint32_t (&w)[5], uint32_t off) { return (w[0] >> (8 * off)) & 0xFFu; }
 
@@ -282,19 +368,35 @@ QM_DEV uint32_t blocks_scale_byte(const uint32_t (&w)[5], uint32_t off) { return
 // reproduce exactly (non-finite values, or values that overflow float32).
 template <int FMT, int BITS>
 QM_DEV float lane_part(const Args& a, const Lane<FMT, BITS>& L, const Acts<FMT, BITS>& X, bool& exact) {
-    const float dot = lane_dot<FMT, BITS>(L, X);
-    if constexpr (FMT == QM_AFFINE) {
+    if constexpr (FMT == QM_Q6_K) {
+        const float2 dd = q6_k_dots(L.w, L.off, X.p);
+        const uint32_t sw = L.w[18] >> (8 * ((L.off >> 4) & 3u));
+        const float d = f16_bits_to_f32((L.w[19] >> (8 * ((L.off >> 6) & 3u))) & 0xFFFFu);
+        exact = false;
+        return fmaf(d * static_cast<float>(static_cast<int8_t>(sw & 0xFFu)), dd.x,
+                    d * static_cast<float>(static_cast<int8_t>((sw >> 8) & 0xFFu)) * dd.y);
+    } else if constexpr (FMT == QM_Q4_K) {
+        int sc, mn;
+        q4_k_scale_min(L.w, static_cast<int>(L.off), sc, mn);
+        const float d = f16_bits_to_f32(L.w[0] & 0xFFFFu), dmin = f16_bits_to_f32(L.w[0] >> 16);
+        exact = false;
+        return fmaf(d * static_cast<float>(sc), lane_dot<FMT, BITS>(L, X), -(dmin * static_cast<float>(mn)) * X.sum);
+    } else if constexpr (FMT == QM_AFFINE) {
+        const float dot = lane_dot<FMT, BITS>(L, X);
         const float s = sval(L.s, a.sdt), b = sval(L.b, a.sdt);
         exact = fmaxf(fabsf(s), fabsf(b)) >= 0x1p119f;  // |code * s + b| may reach 2^128
         return fmaf(s, dot, b * X.sum);
     } else if constexpr (FMT == QM_Q8_0) {
+        const float dot = lane_dot<FMT, BITS>(L, X);
         const uint32_t dbits = L.off ? (L.w[0] >> 16) : (L.w[0] & 0xFFFFu);
         exact = false;
         return f16_bits_to_f32(dbits) * dot;
     } else if constexpr (FMT == QM_MXFP4) {
+        const float dot = lane_dot<FMT, BITS>(L, X);
         exact = L.s >= 253u;  // values of magnitude 4 (at 253) or 2 (at 254) pass float32's range
         return e8m0_to_f32(L.s) * dot;
-    } else {
+    } else {  // MXFP4 in GGUF's blocks
+        const float dot = lane_dot<FMT, BITS>(L, X);
         const uint32_t sb = blocks_scale_byte(L.w, L.off);
         exact = sb >= 253u;
         return e8m0_to_f32(sb) * dot;
@@ -316,6 +418,26 @@ QM_DEV float value_g(const Args& a, int64_t row, int64_t i) {
         const uint8_t* blk = rp + (i / 32) * 34;
         const float d = f16_bits_to_f32(static_cast<uint32_t>(__ldg(blk)) | (static_cast<uint32_t>(__ldg(blk + 1)) << 8));
         return d * static_cast<float>(static_cast<int8_t>(__ldg(blk + 2 + i % 32)));
+    } else if constexpr (FMT == QM_Q4_K) {
+        const uint8_t* blk = rp + (i / 256) * 144;
+        const int v = static_cast<int>(i % 256), c = v / 64, rr = v % 64, j = 2 * c + (rr >= 32);
+        uint32_t w[12];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) w[q] = __ldg(reinterpret_cast<const uint32_t*>(blk) + q);
+        int sc, mn;
+        q4_k_scale_min(w, j, sc, mn);
+        const uint32_t byte = __ldg(blk + 16 + 32 * c + rr % 32);
+        const float d = f16_bits_to_f32(w[0] & 0xFFFFu), dmin = f16_bits_to_f32(w[0] >> 16);
+        return fmaf(d * static_cast<float>(sc), static_cast<float>(rr < 32 ? (byte & 15u) : (byte >> 4)),
+                    -(dmin * static_cast<float>(mn)));
+    } else if constexpr (FMT == QM_Q6_K) {
+        const uint8_t* blk = rp + (i / 256) * 210;
+        const int v = static_cast<int>(i % 256), h = v / 128, t = (v % 128) / 32, l = v % 32;
+        const uint32_t lo = __ldg(blk + 64 * h + l + 32 * (t % 2));
+        const uint32_t q = ((t < 2 ? lo : (lo >> 4)) & 15u) | (((static_cast<uint32_t>(__ldg(blk + 128 + 32 * h + l)) >> (2 * t)) & 3u) << 4);
+        const float d = f16_bits_to_f32(static_cast<uint32_t>(__ldg(blk + 208)) | (static_cast<uint32_t>(__ldg(blk + 209)) << 8));
+        return d * static_cast<float>(static_cast<int8_t>(__ldg(blk + 192 + 8 * h + 2 * t + l / 16))) *
+               static_cast<float>(static_cast<int>(q) - 32);
     } else {
         uint32_t c, sb;
         if constexpr (FMT == QM_MXFP4) {
@@ -425,7 +547,7 @@ bool gemv1_supported(const WDesc& w) {
         if (w.gs < 32 || (w.gs & (w.gs - 1))) return false;
         return w.bits == 2 || w.bits == 3 || w.bits == 4 || w.bits == 5 || w.bits == 6 || w.bits == 8;
     }
-    return w.fmt == QM_Q8_0 || w.fmt == QM_MXFP4 || w.fmt == QM_MXFP4_BLOCKS;
+    return w.fmt == QM_Q8_0 || w.fmt == QM_MXFP4 || w.fmt == QM_MXFP4_BLOCKS || w.fmt == QM_Q4_K || w.fmt == QM_Q6_K;
 }
 
 cudaError_t launch_gemv1(const WDesc& w, const void* x, void* y, cudaStream_t st) {
@@ -458,6 +580,8 @@ cudaError_t launch_gemv1(const WDesc& w, const void* x, void* y, cudaStream_t st
     }
     if (w.fmt == QM_Q8_0) return launch_t<QM_Q8_0, 8>(a, st);
     if (w.fmt == QM_MXFP4) return launch_t<QM_MXFP4, 4>(a, st);
+    if (w.fmt == QM_Q4_K) return launch_t<QM_Q4_K, 4>(a, st);
+    if (w.fmt == QM_Q6_K) return launch_t<QM_Q6_K, 6>(a, st);
     return launch_t<QM_MXFP4_BLOCKS, 4>(a, st);
 }
 

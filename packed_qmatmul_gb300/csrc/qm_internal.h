@@ -61,8 +61,11 @@ int max_smem_optin();
 inline bool pipelined_format(const WDesc& w) {
     return (w.fmt == QM_AFFINE && (w.bits == 4 || w.bits == 8)) || w.fmt == QM_Q8_0 || w.fmt == QM_MXFP4;
 }
-// Weights the tensor-core GEMM decodes: affine at every width, Q8_0, MXFP4.
-inline bool gemm_format(const WDesc& w) { return w.fmt == QM_AFFINE || w.fmt == QM_Q8_0 || w.fmt == QM_MXFP4; }
+// Weights the tensor-core GEMM decodes: affine at every width, Q8_0, MXFP4,
+// Q4_K (Q6_K's 210-byte blocks are no 16-byte multiple: no tensor-map tiles).
+inline bool gemm_format(const WDesc& w) {
+    return w.fmt == QM_AFFINE || w.fmt == QM_Q8_0 || w.fmt == QM_MXFP4 || w.fmt == QM_Q4_K;
+}
 
 // ------------------------------------------------------------ launchers
 // Each returns the CUDA error of its launch (cudaSuccess when nothing ran).

@@ -781,3 +781,19 @@ def test_kquant_experts(kind, T):
     ids = synth.expert_ids(g, T, 2, E)
     ids[1, 0] = E
     _check_experts(w, ids, synth.activations(g, T, 512), f"{kind} experts T={T}")
+
+
+@pytest.mark.parametrize("kind", ["q8_0", "mxfp4_blocks", "q6_k"])
+def test_one_token_rows_off_word_boundaries(kind):
+    # GGUF block rows of 102 or 170 (Q8_0), 51 or 85 (MXFP4 blocks) and 210 or
+    # 630 (Q6_K) bytes: row starts fall on every byte offset within a word
+    g = synth.rng(1900)
+    shapes = ((37, 256), (9, 768)) if kind == "q6_k" else ((37, 96), (9, 160))
+    for n, k in shapes:
+        if kind == "q8_0":
+            w = synth.q8_0_weight(g, n, k)
+        elif kind == "mxfp4_blocks":
+            w = synth.mxfp4_blocks_weight(g, n, k)
+        else:
+            w = synth.q6_k_weight(g, n, k)
+        _check_apply(w, synth.activations(g, 1, k), f"{kind} n={n} k={k} M=1")
