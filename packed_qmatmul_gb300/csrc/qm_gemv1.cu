@@ -472,45 +472,53 @@ template <int FMT, int BITS>
 __global__ void __launch_bounds__(kWarps * 32) gemv1_kernel(const __grid_constant__ Args a) {
     grid_launch_dependents();
     const int lane = threadIdx.x & 31;
-    const int64_t warp0 = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarp = (static_cast<int64_t>(gridDim.x) * blockDim.x) >> 5;
-    if (warp0 >= a.nblocks) return;  // nothing to read or write
-    const int64_t nb = (a.nblocks - 1 - warp0) / nwarp + 1;  // this warp's blocks
-    const int64_t steps = nb * a.nchunk;                     // (block, chunk) pairs, chunks fastest
+    // 32-bit block indices (a block is R rows; rows < 2^32) and steps walked
+    // incrementally: no integer division anywhere on the path
+    const int warp0 = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int nwarp = static_cast<int>((gridDim.x * blockDim.x) >> 5);
+    const int nblocks = static_cast<int>(a.nblocks), nchunk = a.nchunk;
+    if (warp0 >= nblocks) return;  // nothing to read or write
     Lane<FMT, BITS> cur[R], nxt[R];
-    auto load_step = [&](int64_t s, Lane<FMT, BITS> (&L)[R]) {
-        const int64_t b = warp0 + (s / a.nchunk) * nwarp;
-        const int64_t i0 = static_cast<int64_t>(s % a.nchunk) * kChunk + 32 * lane;
+    auto load_step = [&](int b, int c, Lane<FMT, BITS> (&L)[R]) {
+        const int64_t i0 = static_cast<int64_t>(c) * kChunk + 32 * lane;
 #pragma unroll
-        for (int r = 0; r < R; ++r) load_lane<FMT, BITS>(a, b * R + r, i0, L[r]);
+        for (int r = 0; r < R; ++r) load_lane<FMT, BITS>(a, static_cast<int64_t>(b) * R + r, i0, L[r]);
     };
     if (a.static_w) {  // the weight is not written by the previous kernel: read it first
-        load_step(0, cur);
+        load_step(warp0, 0, cur);
         grid_dependency_wait();
     } else {
         grid_dependency_wait();
-        load_step(0, cur);
+        load_step(warp0, 0, cur);
     }
     Acts<FMT, BITS> X;
     float y[R];
 #pragma unroll
     for (int r = 0; r < R; ++r) y[r] = 0.0f;
+    bool have_x = false;
+    // (block b, chunk c) steps, chunks fastest
     #pragma unroll 1
-    for (int64_t s = 0; s < steps; ++s) {
-        if (s + 1 < steps) load_step(s + 1, nxt);
-        const int c = static_cast<int>(s % a.nchunk);
-        const int64_t b = warp0 + (s / a.nchunk) * nwarp;
+    for (int b = warp0, c = 0; b < nblocks;) {
+        int b2 = b, c2 = c + 1;
+        if (c2 == nchunk) {
+            c2 = 0;
+            b2 += nwarp;
+        }
+        if (b2 < nblocks) load_step(b2, c2, nxt);
         const int64_t i0 = static_cast<int64_t>(c) * kChunk + 32 * lane;
-        if (a.nchunk > 1 || s == 0) load_acts<FMT, BITS>(a, i0, X);
+        if (nchunk > 1 || !have_x) {
+            load_acts<FMT, BITS>(a, i0, X);
+            have_x = true;
+        }
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             bool exact;
             float part = lane_part<FMT, BITS>(a, cur[r], X, exact);
-            const int64_t row = b * R + r;
+            const int64_t row = static_cast<int64_t>(b) * R + r;
             if ((exact || !isfinite(part)) && row < a.n && i0 < a.k) part = lane_exact<FMT, BITS>(a, row, i0);
             y[r] += part;
         }
-        if (c == a.nchunk - 1) {
+        if (c == nchunk - 1) {
             // the R rows' sums over the warp, in a fixed order: lanes first
             // exchange halves of their R values, then add down to one each
             static_assert(R == 2, "the exchange below pairs two rows");
@@ -518,7 +526,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv1_kernel(const __grid_constan
             float v = ((lane & 1) ? y[1] : y[0]) + __shfl_xor_sync(0xffffffffu, give, 1);
 #pragma unroll
             for (int o = 2; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            const int64_t row = b * R + lane;  // lane 0: row 0 of the block, lane 1: row 1
+            const int64_t row = static_cast<int64_t>(b) * R + lane;  // lane 0: row 0 of the block, lane 1: row 1
             if (lane < R && row < a.n) {
                 __nv_bfloat16 bv = __float2bfloat16_rn(v);
                 a.y[row] = *reinterpret_cast<uint16_t*>(&bv);
@@ -528,6 +536,8 @@ __global__ void __launch_bounds__(kWarps * 32) gemv1_kernel(const __grid_constan
         }
 #pragma unroll
         for (int r = 0; r < R; ++r) cur[r] = nxt[r];
+        b = b2;
+        c = c2;
     }
 }
 
@@ -542,7 +552,7 @@ cudaError_t launch_t(const Args& a, cudaStream_t st) {
 }  // namespace g1
 
 bool gemv1_supported(const WDesc& w) {
-    if (w.ndim != 2 || w.n < 1 || w.k < 32) return false;
+    if (w.ndim != 2 || w.n < 1 || w.k < 32 || w.n > (int64_t(1) << 31)) return false;
     if (w.fmt == QM_AFFINE) {
         if (w.gs < 32 || (w.gs & (w.gs - 1))) return false;
         return w.bits == 2 || w.bits == 3 || w.bits == 4 || w.bits == 5 || w.bits == 6 || w.bits == 8;
