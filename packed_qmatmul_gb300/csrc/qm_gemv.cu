@@ -562,7 +562,6 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
             // 4 MM items sit in adjacent lanes of one warp, which add its sums.
             const int items = (groups * MM * 4 + 31) / 32 * 32;
             const float mul = __uint_as_float(static_cast<uint32_t>(token_exp(0) + 127) << 23);
-            const float inv = __uint_as_float(static_cast<uint32_t>(127 - token_exp(0)) << 23);
             #pragma unroll 1
             for (int it = ctid; it < items; it += kWarps * 32) {
                 const int t = it & 3, mm = (it >> 2) % MM, gi = (it >> 2) / MM;
@@ -600,9 +599,8 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
                         X += __shfl_xor_sync(0xffffffffu, X, o);
                         F += __shfl_xor_sync(0xffffffffu, F, o);
                     }
-                    // at the true size (x, not x'): exact power-of-two products
                     const float magic = (FMT == QM_Q8_0) ? 1152.0f : 1024.0f;
-                    if (t == 0 && mm == 0 && live) tok[gi * 16] = make_float2(magic * F * inv, X * inv);
+                    if (t == 0 && mm == 0 && live) tok[gi * 16] = make_float2(magic * F, X);
                 }
             }
         } else {
@@ -614,7 +612,6 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
                 const int m = nt * 8 + tg;
                 const bool live = m < M;  // padding tokens get exact zeros
                 const float mul = live ? __uint_as_float(static_cast<uint32_t>(token_exp(m) + 127) << 23) : 0.0f;
-                const float inv = __uint_as_float(static_cast<uint32_t>(127 - (live ? token_exp(m) : 0)) << 23);
                 const uint16_t* xr = xs + (live ? m : 0) * p.krange;
                 uint32_t* dst = xfrag + ((gi * 32 + ln) * MM) * NT * 2 + nt * 2;
                 float F = 0.0f, X = 0.0f;
@@ -659,7 +656,7 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
                     X += __shfl_xor_sync(0xffffffffu, X, 2);
                     F += __shfl_xor_sync(0xffffffffu, F, 2);
                     const float magic = (FMT == QM_Q8_0) ? 1152.0f : 1024.0f;
-                    if (t == 0) tok[gi * 16 + m] = make_float2(magic * F * inv, X * inv);
+                    if (t == 0) tok[gi * 16 + m] = make_float2(magic * F, X);
                 }
             }
         }
@@ -774,10 +771,16 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
                 }
             };
             // a tile's scales (and biases) as float32 from their raw bits, and
-            // whether the group is exceptional for the tile's rows: its values are,
-            // or may be, infinite, or an activation is (a NaN scale or bias needs
-            // no exception: it makes every value of its group NaN, and the scaled
-            // sum NaN too)
+            // whether the tile's rows must be summed element by element this stage:
+            // a scale (or bias) so large that a group's sum at the activations'
+            // 2^E scale could leave float32's range over a stage, or values that
+            // are or may be infinite (an infinite Q8_0 d; MXFP4 bytes 253/254 and
+            // affine magnitudes of 2^119 or more lie inside these bounds). Over a
+            // stage a warp adds at most 2^9 groups, each at most 2^22.6 (MXFP4:
+            // 6 * 32 * 2^15) or 2^30 (affine: 256 * 128 * 2^15) times its scale, so
+            // scales below 2^93 (MXFP4) and 2^87 (affine) keep every sum below
+            // 2^127. A NaN scale or bias needs no exception: it makes every value
+            // of its group NaN, and the scaled sum NaN too.
             auto scales_of = [&](const uint32_t (&r)[4], float& s0, float& s8, float& b0, float& b8) -> bool {
                 b0 = b8 = 0.0f;
                 if constexpr (FMT == QM_AFFINE) {
@@ -785,18 +788,18 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
                     s8 = sval<SDT>(r[1]);
                     b0 = sval<SDT>(r[2]);
                     b8 = sval<SDT>(r[3]);
-                    // |code * s + b| < 2^128 whenever |s|, |b| < 2^119 (codes < 2^8)
-                    return fmaxf(fmaxf(fabsf(s0), fabsf(s8)), fmaxf(fabsf(b0), fabsf(b8))) >= 0x1p119f;
+                    return fmaxf(fmaxf(fabsf(s0), fabsf(s8)), fmaxf(fabsf(b0), fabsf(b8))) >= 0x1p87f;
                 } else if constexpr (FMT == QM_Q8_0) {
                     s0 = f16_bits_to_f32(r[0]);
                     s8 = f16_bits_to_f32(r[1]);
                     return fmaxf(fabsf(s0), fabsf(s8)) > 0x1p127f;  // an infinite d
                 } else {
                     e8m0x2_to_f32(r[0] | (r[1] << 8), s0, s8);
-                    return max(r[0], r[1]) >= 253u;  // values that may pass float32's range
+                    return max(r[0], r[1]) >= 220u;  // scales of 2^93 and more
                 }
             };
-            bool any_exc = xbad;
+            uint32_t big = xbad ? 3u : 0u;  // bit tt: tile tt is summed element by element this stage
+            // the group's sums, at the activations' 2^E scale, into y
             auto epilogue = [&](int gi, const float (&acc)[2][NT][4], const uint32_t (&raw)[2][4]) {
                 float4 td[NT];  // (O[2t], X[2t], O[2t+1], X[2t+1]) per token half
                 if constexpr (FMT != QM_MXFP4) {
@@ -807,59 +810,55 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
 #pragma unroll
                 for (int tt = 0; tt < 2; ++tt) {
                     float s0, s8, b0, b8;
-                    const bool exc = scales_of(raw[tt], s0, s8, b0, b8);
-                    any_exc |= exc;
-                    if (exc || xbad) continue;  // summed per element after the stage's groups
+                    if (scales_of(raw[tt], s0, s8, b0, b8)) big |= 1u << tt;
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
                         float* yv = y[tt][nt];
                         const float* c = acc[tt][nt];
                         if constexpr (FMT == QM_MXFP4) {
-                            yv[0] = fmaf(s0, c[0] * tk[nt][0], yv[0]);
-                            yv[2] = fmaf(s8, c[2] * tk[nt][0], yv[2]);
+                            yv[0] = fmaf(s0, c[0], yv[0]);
+                            yv[2] = fmaf(s8, c[2], yv[2]);
                             if constexpr (!ONE) {
-                                yv[1] = fmaf(s0, c[1] * tk[nt][1], yv[1]);
-                                yv[3] = fmaf(s8, c[3] * tk[nt][1], yv[3]);
+                                yv[1] = fmaf(s0, c[1], yv[1]);
+                                yv[3] = fmaf(s8, c[3], yv[3]);
                             }
                         } else {
-                            // (c - offset) at its true size in one rounding: c * 2^-E is
-                            // exact, and d holds the offset and sum of x already scaled
                             const float4 d = td[nt];
-                            yv[0] = fmaf(s0, fmaf(c[0], tk[nt][0], -d.x), fmaf(b0, d.y, yv[0]));
-                            yv[2] = fmaf(s8, fmaf(c[2], tk[nt][0], -d.x), fmaf(b8, d.y, yv[2]));
+                            yv[0] = fmaf(s0, c[0] - d.x, fmaf(b0, d.y, yv[0]));
+                            yv[2] = fmaf(s8, c[2] - d.x, fmaf(b8, d.y, yv[2]));
                             if constexpr (!ONE) {  // odd columns: tokens 2t + 1
-                                yv[1] = fmaf(s0, fmaf(c[1], tk[nt][1], -d.z), fmaf(b0, d.w, yv[1]));
-                                yv[3] = fmaf(s8, fmaf(c[3], tk[nt][1], -d.z), fmaf(b8, d.w, yv[3]));
+                                yv[1] = fmaf(s0, c[1] - d.z, fmaf(b0, d.w, yv[1]));
+                                yv[3] = fmaf(s8, c[3] - d.z, fmaf(b8, d.w, yv[3]));
                             }
                         }
                     }
                 }
             };
-            // the exceptional groups of this lane's tiles, element by element
-            // (rare: kept out of the streaming loop)
-            auto exact_pass = [&](int g0, int g1) {
+            // tile tt's sums over the stage's groups [g0, g1), element by element
+            // at float32 (rare: kept out of the streaming loop)
+            auto exact_tile = [&](int tt, int g0, int g1) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) y[tt][nt][i] = 0.0f;
                 #pragma unroll 1
                 for (int gi = g0; gi < g1; ++gi) {
                     uint32_t raw[2][4];
                     ep_load(gi, raw);
-                    // (every index into y a constant, so y stays in registers)
+                    float s0, s8, b0, b8;
+                    (void)scales_of(raw[tt], s0, s8, b0, b8);
 #pragma unroll
-                    for (int tt = 0; tt < 2; ++tt) {
-                        float s0, s8, b0, b8;
-                        if (!scales_of(raw[tt], s0, s8, b0, b8) && !xbad) continue;
+                    for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                            for (int h = 0; h < 2; ++h) {
-                                const int m = nt * 8 + 2 * t + h;
-                                if ((ONE && (t != 0 || h != 0)) || m >= M) continue;
-                                const int64_t xr = p.g_off ? s_xrow[m] : m;
-                                const float2 e = group_exact<FMT, BITS, GS>(rows_[2 * tt], rows_[2 * tt + 1], gi, s0, b0,
-                                                                            s8, b8, p.x + xr * p.k + xk0 + gi * GS);
-                                y[tt][nt][h] += e.x;
-                                y[tt][nt][2 + h] += e.y;
-                            }
-                    }
+                        for (int h = 0; h < 2; ++h) {
+                            const int m = nt * 8 + 2 * t + h;
+                            if ((ONE && (t != 0 || h != 0)) || m >= M) continue;
+                            const int64_t xr = p.g_off ? s_xrow[m] : m;
+                            const float2 e = group_exact<FMT, BITS, GS>(rows_[2 * tt], rows_[2 * tt + 1], gi, s0, b0,
+                                                                        s8, b8, p.x + xr * p.k + xk0 + gi * GS);
+                            y[tt][nt][h] += e.x;
+                            y[tt][nt][2 + h] += e.y;
+                        }
                 }
             };
             // groups two at a time: four independent MMA chains in flight
@@ -883,7 +882,23 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
                 do_group(gi, acc0);
                 epilogue(gi, acc0, raw0);
             }
-            if (any_exc) exact_pass(gb, gend);  // before the stage's slot is released
+            // the stage's sums at their true size: one power-of-two product per
+            // output (exact), or the element-by-element sums of a big tile; both
+            // before the stage's slot is released
+#pragma unroll
+            for (int tt = 0; tt < 2; ++tt) {
+                if (big & (1u << tt)) {
+                    exact_tile(tt, gb, gend);
+                } else {
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        y[tt][nt][0] *= tk[nt][0];
+                        y[tt][nt][2] *= tk[nt][0];
+                        y[tt][nt][1] *= tk[nt][1];
+                        y[tt][nt][3] *= tk[nt][1];
+                    }
+                }
+            }
             __syncwarp();
             if (lane == 0 && live) mbar_arrive(bar_empty0 + 8 * slot);
 
