@@ -393,13 +393,19 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
         fence_mbar_init();
     }
     __syncthreads();
-    grid_launch_dependents();
+    // each thread lets the next kernel start once its own wait on the previous
+    // one has returned: one kernel waits ahead, with this one's run to stream
+    // its static weights
+    auto wait_prev = [&]() {
+        grid_dependency_wait();
+        grid_launch_dependents();
+    };
     int M = p.M;
     int64_t wrow0 = 0;  // first row of this CTA's matrix in the codes and scales
     if (p.g_off) {
         // which chunk of which expert: the routing tables come from the previous kernel
         if (warp == 0) {
-            grid_dependency_wait();
+            wait_prev();
             group_lookup(p, static_cast<int>(cluster / p.g_wclusters), lane, s_grp, s_pos, s_xrow);
         }
         __syncthreads();
@@ -413,8 +419,8 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
     if (S > 1) cluster_arrive_relaxed();  // waited for before the first access to another CTA
     // x comes from the previous kernel; so may W, unless the caller marked it
     // static, in which case the producer streams its first stages before waiting
-    if (!p.g_off && (!p.static_w || warp != kWarps)) grid_dependency_wait();
-    else if (p.g_off && warp != 0) grid_dependency_wait();
+    if (!p.g_off && (!p.static_w || warp != kWarps)) wait_prev();
+    else if (p.g_off && warp != 0) wait_prev();
 
     if (warp == kWarps) {
         // ------------------------------------------------------------ producer
@@ -437,7 +443,7 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
         #pragma unroll 1
         for (int j = 0; j < nst; ++j, (++slot == p.nstage) ? (slot = 0, ++fill) : 0u) {
             if (p.static_w && !xdone && j == npre) {
-                grid_dependency_wait();
+                wait_prev();
                 copy_x();
                 xdone = true;
             }
@@ -497,7 +503,7 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
             }
         }
         if (!xdone) {  // every stage prefetched, or abandoned before the first
-            if (p.static_w) grid_dependency_wait();
+            if (p.static_w) wait_prev();
             copy_x();
         }
         if (s_abort) {

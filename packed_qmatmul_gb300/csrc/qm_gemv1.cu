@@ -20,7 +20,8 @@
 //    packed float32 pairs of Blackwell's ALU (fma.rn.f32x2).
 //  * Weights the caller marks static are read before the kernel waits on the
 //    previous one (programmatic dependent launch), so a dependent chain of
-//    small products pays for the activations' round trip only.
+//    small products pays for the activations' round trip only. The next
+//    kernel is let start once this one's wait has returned.
 //  * Warps stride over blocks of R rows; each loads the next step's codes
 //    before it works on the current one (large layers stream).
 //  * A lane whose partial sum is not finite, or whose block's scale could make
@@ -470,7 +471,6 @@ static __device__ __noinline__ float lane_exact(const Args& a, int64_t row, int6
 
 template <int FMT, int BITS>
 __global__ void __launch_bounds__(kWarps * 32) gemv1_kernel(const __grid_constant__ Args a) {
-    grid_launch_dependents();
     const int lane = threadIdx.x & 31;
     // 32-bit block indices (a block is R rows; rows < 2^32) and steps walked
     // incrementally: no integer division anywhere on the path
@@ -491,6 +491,11 @@ __global__ void __launch_bounds__(kWarps * 32) gemv1_kernel(const __grid_constan
         grid_dependency_wait();
         load_step(warp0, 0, cur);
     }
+    // Let the next kernel start only now: it still has this kernel's whole
+    // remaining run to read its own static weights, and only one kernel waits
+    // ahead (triggered at entry, several later ones became resident at once
+    // and each launch took about 0.2 us longer)
+    grid_launch_dependents();
     Acts<FMT, BITS> X;
     float y[R];
 #pragma unroll
