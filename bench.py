@@ -54,6 +54,9 @@ def parse():
     ap.add_argument("--M", type=int, default=None)
     ap.add_argument("--no-detail", action="store_true", help="skip the secondary measurements")
     ap.add_argument("--no-cpu", action="store_true", help="skip the cpu_baseline leg")
+    ap.add_argument("--unfused", action="store_true",
+                    help="decode: one qm_apply per product (169 calls) instead of one qm_apply_many "
+                         "per group of products that read the same activations (85 calls)")
     ap.add_argument("--only", default=None,
                     help="profiling aid: a step of just the projections whose name ends with this")
     return ap.parse_args()
@@ -73,11 +76,14 @@ def packed_bytes(n, k, bits, gs=64):
     return n * k * bits // 8 + 2 * n * (k // gs) * 2
 
 
-def config_dict(bits, M):
+def config_dict(bits, M, fused=True):
+    calls = ("85 calls on distinct weights: per layer one qm_apply_many over q/k/v and one over gate/up "
+             "(products that read the same activations share a launch) and qm_apply for down_proj; "
+             "qm_apply for lm_head") if fused else "169 qm_apply calls on distinct weights"
     return {
         "workload": f"qwen3-0.6b-shaped decode step: 28 x (q 2048x1024, k/v 1024x1024, gate/up "
                     f"3072x1024, down 1024x3072) + lm_head 151936x1024, MLX affine {bits}-bit gs64, "
-                    f"M={M}, 169 qm_apply calls on distinct weights",
+                    f"M={M}, {calls}",
         "format": "mlx_affine", "bits": bits, "group_size": 64, "M": M,
         "weight_bytes_per_step": sum(packed_bytes(n, k, bits) for _, n, k in workload_list(bits)),
         "l2": "inputs larger than L2 (distinct weights per layer, 302 MB at 4-bit)",
@@ -158,6 +164,43 @@ def build_step(bits, M, device, only=None):
         y = torch.empty((M, n), dtype=torch.bfloat16, device=device)
         items.append((name, n, k, qw, x, y))
     return items
+
+
+FUSED_GROUPS = (("q_proj", "k_proj", "v_proj"), ("gate_proj", "up_proj"))
+
+
+def step_groups(items, fused=True):
+    """The step's calls in order: lists of items that read the same activations
+    (q/k/v, gate/up of one layer) when fused, every other product alone."""
+    groups, i = [], 0
+    while i < len(items):
+        g = [items[i]]
+        for fg in FUSED_GROUPS if fused else ():
+            if items[i][0].endswith(fg[0]):
+                layer = items[i][0][:-len(fg[0])]
+                for name in fg[1:]:
+                    j = i + len(g)
+                    if j < len(items) and items[j][0] == layer + name:
+                        g.append(items[j])
+        groups.append(g)
+        i += len(g)
+    return groups
+
+
+def call_group(g, stream):
+    """One call of the step: qm_apply for a lone product, qm_apply_many for a group
+    (the group's first activations, which every member reads)."""
+    import packed_qmatmul_gb300 as qm
+
+    if len(g) == 1:
+        qm.qm_apply(g[0][3], g[0][4], g[0][5], stream)
+    else:
+        qm.qm_apply_many([it[3] for it in g], g[0][4], [it[5] for it in g], stream)
+
+
+def group_algo_bytes(g, bits, M):
+    """Packed weights, the activations once, every output."""
+    return sum(packed_bytes(n, k, bits) + 2 * M * n for _, n, k, *_ in g) + 2 * M * g[0][2]
 
 
 def time_graph(step, stream, steps, warmup, clock_index=None):
@@ -546,15 +589,16 @@ def run_ours(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     bits, M = args.bits, (args.M or 1)
+    fused = not args.unfused
     items = build_step(bits, M, dev, args.only)
+    groups = step_groups(items, fused)
     step_bytes = sum(packed_bytes(n, k, bits) for _, n, k, *_ in items)
-    algo_bytes = step_bytes + sum(2 * M * (n + k) for _, n, k, *_ in items)
-    launches_per_step = len(items)
+    launches_per_step = len(groups)
     stream = torch.cuda.Stream()
 
     def step():
-        for _, _, _, qw, x, y in items:
-            qm.qm_apply(qw, x, y, stream)
+        for g in groups:
+            call_group(g, stream)
 
     dist = world > 1
     if dist:
@@ -571,18 +615,18 @@ def run_ours(args, rank, world):
     value = step_bytes * args.steps * world / elapsed / 1e9
     # the dominant kernel: the one-token kernel of the layer projections (all
     # but lm_head), their launches captured and timed alone on the same stream
-    layers = [it for it in items if it[0] != "lm_head"] if M == 1 and not args.only else items
-    lay_algo = sum(packed_bytes(n, k, bits) + 2 * M * (n + k) for _, n, k, *_ in layers)
+    layers = [g for g in groups if g[0][0] != "lm_head"] if M == 1 and not args.only else groups
+    lay_algo = sum(group_algo_bytes(g, bits, M) for g in layers)
 
     def layer_step():
-        for _, _, _, qw, x, y in layers:
-            qm.qm_apply(qw, x, y, stream)
+        for g in layers:
+            call_group(g, stream)
 
     lay_el, _ = time_graph(layer_step, stream, args.steps, args.warmup)
     avg_launch = lay_el / (args.steps * len(layers))
     achieved = lay_algo / len(layers) / avg_launch / 1e9
 
-    e2e = run_e2e(items, stream, args, step_bytes)
+    e2e = run_e2e(groups, stream, args, step_bytes)
 
     peaks = load_peaks()
     peak = peaks.get("hbm_gbs", 6800.0)
@@ -593,15 +637,16 @@ def run_ours(args, rank, world):
         "dtype_note": "codes enter f16 tensor-core products as exact small integers, activations as exact "
                       "power-of-two rescaled f16; sums and scales at f32",
         "data": "synthetic (seeded; weights and activations drawn as the workload states)",
-        "config": config_dict(bits, M),
+        "config": config_dict(bits, M, fused),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
                      "traffic": traffic("decode", bits == 4 and M == 1 and not args.only)[0],
                      "traffic_source": traffic("decode", bits == 4 and M == 1 and not args.only)[1],
                      "algorithmic_bytes_per_launch": round(lay_algo / len(layers)),
                      "launch_us": round(avg_launch * 1e6, 3),
-                     "kernel": (f"gemv1_kernel<affine,{bits}> (the {len(layers)} layer launches of the step, timed "
-                                "alone as a graph of the same launches; lm_head runs gemv_kernel)")
+                     "kernel": (f"gemv1_kernel<affine,{bits}> (the {len(layers)} layer launches of the step"
+                                + (", q/k/v and gate/up one grid each" if fused else "")
+                                + ", timed alone as a graph of the same launches; lm_head runs gemv_kernel)")
                                if M == 1 and not args.only else f"the step's {len(layers)} product launches",
                      "peak_source": "measured" if "hbm_gbs" in peaks else "fallback"},
         "e2e": e2e,
@@ -611,7 +656,7 @@ def run_ours(args, rank, world):
     if args.only:
         res["config"]["workload"] += f" (profiling aid: only *{args.only})"
     if not args.no_detail and not args.only and rank == 0:
-        res["detail"] = detail_measurements(args, dev, stream)
+        res["detail"] = detail_measurements(args, dev, stream, fused)
         res["detail"].update(other_workloads(dev, stream))
         pf = res["detail"].get("prefill_q8_0_M2048")
         if pf:  # the metric's TFLOP/s half, on the Q8_0 prefill config
@@ -621,35 +666,41 @@ def run_ours(args, rank, world):
     return res
 
 
-def run_e2e(items, stream, args, step_bytes):
-    """Same step through the public API with host buffers: every activation row
-    copied in from pinned host memory as one transfer, the 169 qm_apply calls
-    (no graph), every result copied back as one transfer, inside the timed
-    region."""
+def run_e2e(groups, stream, args, step_bytes):
+    """Same step through the public API with host buffers: every call's
+    activation rows copied in from pinned host memory as one transfer, the
+    step's calls (no graph), every result copied back as one transfer, inside
+    the timed region."""
     import torch
 
-    import packed_qmatmul_gb300 as qm
-
-    dev = items[0][4].device
-    x_sizes = [x.numel() for *_, x, _ in items]
-    y_sizes = [y.numel() for *_, y in items]
-    hx = torch.cat([x.reshape(-1).cpu() for *_, x, _ in items]).pin_memory()
+    gx = [g[0][4] for g in groups]  # each call's activations
+    ys_all = [it[5] for g in groups for it in g]
+    dev = gx[0].device
+    y_sizes = [y.numel() for y in ys_all]
+    hx = torch.cat([x.reshape(-1).cpu() for x in gx]).pin_memory()
     hy = torch.empty(sum(y_sizes), dtype=torch.bfloat16).pin_memory()
     dx = torch.empty_like(hx, device=dev)
     dy = torch.empty(sum(y_sizes), dtype=torch.bfloat16, device=dev)
-    xs, ys, ox, oy = [], [], 0, 0
-    for (*_, x, y), nx, ny in zip(items, x_sizes, y_sizes):
-        xs.append(dx[ox:ox + nx].view(x.shape))
-        ys.append(dy[oy:oy + ny].view(y.shape))
-        ox += nx
-        oy += ny
+    xs, ox = [], 0
+    for x in gx:
+        xs.append(dx[ox:ox + x.numel()].view(x.shape))
+        ox += x.numel()
+    ys, oy = [], 0
+    for y in ys_all:
+        ys.append(dy[oy:oy + y.numel()].view(y.shape))
+        oy += y.numel()
+    # the same calls on the staged buffers
+    staged, yi = [], 0
+    for g, x in zip(groups, xs):
+        staged.append([(it[0], it[1], it[2], it[3], x, ys[yi + j]) for j, it in enumerate(g)])
+        yi += len(g)
     h2d = hx.numel() * hx.element_size()
     d2h = hy.numel() * hy.element_size()
 
     def step():
         dx.copy_(hx, non_blocking=True)
-        for (_, _, _, qw, _, _), x, y in zip(items, xs, ys):
-            qm.qm_apply(qw, x, y, stream)
+        for g in staged:
+            call_group(g, stream)
         hy.copy_(dy, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -665,29 +716,30 @@ def run_e2e(items, stream, args, step_bytes):
     el = time.perf_counter() - t0
     return {"value": round(step_bytes * steps / el / 1e9, 2), "unit": "GB/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "note": "169 qm_apply calls per step from Python (no graph); all activation rows H2D as one "
+            "note": f"the step's {len(groups)} calls from Python (no graph); all activation rows H2D as one "
                     "copy before them and all results D2H as one copy after, pinned host memory"}
 
 
-def detail_measurements(args, dev, stream):
-    """Secondary numbers (not the headline): 8-bit and M in {2, 4, 8}."""
+def detail_measurements(args, dev, stream, fused=True):
+    """Secondary numbers (not the headline): 8-bit, M in {2, 4, 8}, and the
+    4-bit M = 1 step the other way (one call per product, or grouped)."""
     import torch
 
-    import packed_qmatmul_gb300 as qm
-
     out = {}
-    for bits, M in ((8, 1), (4, 2), (4, 4), (4, 8)):
+    for bits, M, fz in ((8, 1, fused), (4, 2, fused), (4, 4, fused), (4, 8, fused), (4, 1, not fused)):
         items = build_step(bits, M, dev)
+        groups = step_groups(items, fz)
         sb = sum(packed_bytes(n, k, bits) for _, n, k, *_ in items)
 
         def step():
-            for _, _, _, qw, x, y in items:
-                qm.qm_apply(qw, x, y, stream)
+            for g in groups:
+                call_group(g, stream)
 
         reps = 20
         el, _ = time_graph(step, stream, reps, 3)
-        out[f"affine{bits}_M{M}"] = {"GB/s": round(sb * reps / el / 1e9, 1),
-                                     "ms_per_step": round(el / reps * 1e3, 4)}
+        key = f"affine{bits}_M{M}" + ("" if fz == fused else ("_grouped" if fz else "_one_call_per_product"))
+        out[key] = {"GB/s": round(sb * reps / el / 1e9, 1), "ms_per_step": round(el / reps * 1e3, 4),
+                    "calls_per_step": len(groups)}
         del items
         torch.cuda.empty_cache()
     return out

@@ -145,6 +145,25 @@ qm_status qm_quantize_q8_0(const void* x, int32_t x_dtype, int64_t rows, int64_t
 qm_status qm_apply(const qm_weight* w, const void* x, int64_t M, int32_t x_dtype, void* y,
                    qm_stream_t stream);
 
+/* Most weights qm_apply_many takes in one call. */
+#define QM_MAX_MANY 8
+
+/* apply_many: for `count` 2-d weights ws[i] [n_i, k] (1 <= count <= QM_MAX_MANY)
+ * that read the same x [M, k], ys[i] [M, n_i] receives exactly what
+ * qm_apply(ws[i], x, M, x_dtype, ys[i], stream) would write, bit for bit. The
+ * weights must share format, bits, group_size and k (and scale_dtype for
+ * QM_AFFINE). Each ys[i] must be 16-byte aligned and overlap neither x nor
+ * another output; QM_EINVAL names the offending argument. ws and ys are host
+ * arrays of count entries; the pointers in them are device pointers.
+ * Each product is the one "Nx_quant (raven-ml.dev API docs)", section
+ * "Products", apply, defines. The pages have no multi-weight call: it is this
+ * library's, so that products reading the same activations (a decode step's
+ * q/k/v projections, or gate and up) cost one launch instead of several. At
+ * M = 1 weights of up to 24 MB each run as one grid; otherwise the call makes
+ * the qm_apply launches one after another. */
+qm_status qm_apply_many(const qm_weight* const* ws, int32_t count, const void* x, int64_t M, int32_t x_dtype,
+                        void* const* ys, qm_stream_t stream);
+
 /* take: gathers the rows (or matrices) of w at positions ids[0..n_ids) along
  * `axis` (0 <= axis <= ndim-2; the last axis is refused because a gather along
  * it would cut blocks), from the packed parts, decoding nothing. A position

@@ -22,11 +22,11 @@ import torch
 __all__ = [
     "QM_AFFINE", "QM_Q8_0", "QM_MXFP4", "QM_MXFP4_BLOCKS", "QM_Q4_K", "QM_Q6_K", "QM_WEIGHT_STATIC", "QM_F32", "QM_BF16", "QM_F16", "QM_I32", "QM_I64",
     "QMError", "QWeight", "library_path", "load_library",
-    "qm_dequant", "qm_quantize_q8_0", "qm_apply", "qm_take", "qm_apply_experts", "qm_apply_experts_workspace",
+    "qm_dequant", "qm_quantize_q8_0", "qm_apply", "qm_apply_many", "qm_take", "qm_apply_experts", "qm_apply_experts_workspace",
     "qm_experts_route_workspace",
     "qm_experts_route", "qm_apply_experts_static", "qm_check_wait_timeout", "qm_device_status", "qm_last_error",
     "qm_version",
-    "dequant", "quantize_q8_0", "apply", "take", "apply_experts", "route",
+    "dequant", "quantize_q8_0", "apply", "apply_many", "take", "apply_experts", "route",
 ]
 
 QM_OK, QM_EINVAL, QM_ECUDA, QM_ETIMEOUT, QM_ENOTSUP = 0, 1, 2, 3, 4
@@ -35,6 +35,7 @@ QM_F32, QM_BF16, QM_F16 = 0, 1, 2
 QM_I32, QM_I64 = 0, 1
 QM_WEIGHT_STATIC = 1
 QM_MAX_NDIM = 4
+QM_MAX_MANY = 8
 
 _STATUS = {QM_EINVAL: "QM_EINVAL", QM_ECUDA: "QM_ECUDA", QM_ETIMEOUT: "QM_ETIMEOUT",
            QM_ENOTSUP: "QM_ENOTSUP"}
@@ -88,6 +89,7 @@ def load_library():
             "qm_quantize_q8_0": ([vp, i32, i64, i64, vp, vp], i32),
             "qm_check_wait_timeout": ([ctypes.c_uint64, vp], i32),
             "qm_apply": ([wp, vp, i64, i32, vp, vp], i32),
+            "qm_apply_many": ([ctypes.POINTER(wp), i32, vp, i64, i32, ctypes.POINTER(vp), vp], i32),
             "qm_take": ([wp, i32, vp, i32, i64, vp, vp, vp, i32, vp, vp], i32),
             "qm_apply_experts_workspace": ([wp, i64, i64], sz),
             "qm_experts_route_workspace": ([i64, i64], sz),
@@ -235,6 +237,17 @@ def qm_apply(w: QWeight, x: torch.Tensor, y: torch.Tensor, stream=None) -> None:
                                    _stream(stream)))
 
 
+def qm_apply_many(ws: Sequence[QWeight], x: torch.Tensor, ys: Sequence[torch.Tensor], stream=None) -> None:
+    """ys[i] = x times ws[i]^T for weights that read the same x (one launch at M = 1)."""
+    M = x.shape[0] if x.dim() == 2 else 1
+    n = len(ws)
+    warr = (ctypes.POINTER(_CWeight) * max(n, 1))()
+    for i, w in enumerate(ws):
+        warr[i] = ctypes.pointer(w._ref()._obj)
+    yarr = (ctypes.c_void_p * max(len(ys), 1))(*[_ptr(y) for y in ys])
+    _check(load_library().qm_apply_many(warr, n, _ptr(x), M, _DTYPES[x.dtype], yarr, _stream(stream)))
+
+
 def qm_take(w: QWeight, axis: int, ids: torch.Tensor, out_codes=None, out_scales=None,
             out_biases=None, out_dense: Optional[torch.Tensor] = None, stream=None) -> None:
     id_type = QM_I64 if ids.dtype == torch.int64 else QM_I32
@@ -306,6 +319,12 @@ def apply(w: QWeight, x: torch.Tensor, stream=None) -> torch.Tensor:
     y = torch.empty((x.shape[0], w.shape[-2]), dtype=x.dtype, device=x.device)
     qm_apply(w, x, y, stream)
     return y
+
+
+def apply_many(ws: Sequence[QWeight], x: torch.Tensor, stream=None) -> list:
+    ys = [torch.empty((x.shape[0], w.shape[-2]), dtype=x.dtype, device=x.device) for w in ws]
+    qm_apply_many(ws, x, ys, stream)
+    return ys
 
 
 def take(w: QWeight, axis: int, ids: torch.Tensor, dense_dtype=None, packed=True, stream=None):

@@ -271,6 +271,22 @@ qm_status qm_quantize_q8_0(const void* x, int32_t x_dtype, int64_t rows, int64_t
                         "quantize launch");
 }
 
+// One token: the register kernel for weights up to 24 MB (a dependent chain of
+// such products is latency-bound); larger weights stream through the
+// tensor-map pipeline, which keeps more bytes in flight.
+static bool one_token_register_path(const WDesc& d) {
+    const bool small = d.n * d.code_row_bytes + d.n * (d.scale_row_bytes + d.bias_row_bytes) <= (int64_t(24) << 20);
+    return gemv1_supported(d) && (small || !gemv_supported(d, 1));
+}
+
+// The launches of a validated product (M >= 1, n >= 1, k >= 1).
+static qm_status apply_launch(const WDesc& d, const void* x, int64_t M, void* y, cudaStream_t st) {
+    if (M == 1 && one_token_register_path(d)) return check_launch(launch_gemv1(d, x, y, st), "gemv launch");
+    if (M <= 16 && gemv_supported(d, M)) return launch_gemv(d, x, M, y, st);
+    if (gemm_supported(d, M)) return launch_gemm(d, x, M, y, st);
+    return check_launch(launch_apply_simple(d, x, M, y, st), "apply launch");
+}
+
 qm_status qm_apply(const qm_weight* w, const void* x, int64_t M, int32_t x_dtype, void* y,
                    qm_stream_t stream) {
     set_error("");
@@ -293,15 +309,72 @@ qm_status qm_apply(const qm_weight* w, const void* x, int64_t M, int32_t x_dtype
     const char* xb = static_cast<const char*>(x);
     const char* yb = static_cast<const char*>(y);
     if (xb < yb + M * d.n * 2 && yb < xb + M * d.k * 2) return fail(QM_EINVAL, "y: overlaps x");
-    // one token: the register kernel for weights up to 24 MB (a dependent chain of
-    // such products is latency-bound); larger weights stream through the
-    // tensor-map pipeline, which keeps more bytes in flight
-    const bool small = d.n * d.code_row_bytes + d.n * (d.scale_row_bytes + d.bias_row_bytes) <= (int64_t(24) << 20);
-    if (M == 1 && gemv1_supported(d) && (small || !gemv_supported(d, 1)))
-        return check_launch(launch_gemv1(d, x, y, st), "gemv launch");
-    if (M <= 16 && gemv_supported(d, M)) return launch_gemv(d, x, M, y, st);
-    if (gemm_supported(d, M)) return launch_gemm(d, x, M, y, st);
-    return check_launch(launch_apply_simple(d, x, M, y, st), "apply launch");
+    return apply_launch(d, x, M, y, st);
+}
+
+qm_status qm_apply_many(const qm_weight* const* ws, int32_t count, const void* x, int64_t M, int32_t x_dtype,
+                        void* const* ys, qm_stream_t stream) {
+    set_error("");
+    if (count < 1 || count > QM_MAX_MANY) return fail(QM_EINVAL, "count: must be 1 .. QM_MAX_MANY");
+    if (!ws) return fail(QM_EINVAL, "ws: NULL");
+    if (!ys) return fail(QM_EINVAL, "ys: NULL");
+    WDesc d[QM_MAX_MANY];
+    for (int i = 0; i < count; ++i) {
+        qm_status s = validate_weight(ws[i], &d[i]);
+        if (s != QM_OK) return fail(s, "ws[" + std::to_string(i) + "]: " + qm_last_error());
+        if (d[i].ndim != 2) return fail(QM_ENOTSUP, "ws[" + std::to_string(i) + "]: apply takes a 2-d weight [n, k]");
+        if (d[i].fmt != d[0].fmt || d[i].bits != d[0].bits || d[i].gs != d[0].gs ||
+            (d[i].fmt == QM_AFFINE && d[i].sdt != d[0].sdt))
+            return fail(QM_EINVAL, "ws[" + std::to_string(i) + "]: format, bits, group_size or scale_dtype differs from ws[0]");
+        if (d[i].k != d[0].k) return fail(QM_EINVAL, "ws[" + std::to_string(i) + "]: k differs from ws[0]");
+    }
+    if (M < 0) return fail(QM_EINVAL, "x: negative row count M");
+    if (x_dtype != QM_BF16) return fail(QM_ENOTSUP, "x: apply takes bfloat16 activations");
+    const int64_t k = d[0].k;
+    for (int i = 0; i < count; ++i) {
+        if (M == 0 || d[i].n == 0) continue;
+        const std::string name = "ys[" + std::to_string(i) + "]";
+        if (!ys[i]) return fail(QM_EINVAL, name + ": NULL");
+        if (!aligned16(ys[i])) return fail(QM_EINVAL, name + ": base address must be 16-byte aligned");
+        const char* yb = static_cast<const char*>(ys[i]);
+        if (k > 0) {
+            if (!x) return fail(QM_EINVAL, "x: NULL");
+            const char* xb = static_cast<const char*>(x);
+            if (xb < yb + M * d[i].n * 2 && yb < xb + M * k * 2) return fail(QM_EINVAL, name + ": overlaps x");
+        }
+        for (int j = 0; j < i; ++j) {
+            if (d[j].n == 0) continue;
+            const char* ob = static_cast<const char*>(ys[j]);
+            if (ob < yb + M * d[i].n * 2 && yb < ob + M * d[j].n * 2)
+                return fail(QM_EINVAL, name + ": overlaps ys[" + std::to_string(j) + "]");
+        }
+    }
+    if (M == 0) return QM_OK;
+    if (k > 0 && !aligned16(x)) return fail(QM_EINVAL, "x: base address must be 16-byte aligned");
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // one grid where every weight takes the one-token register kernel on its own
+    WDesc live[QM_MAX_MANY];
+    void* live_y[QM_MAX_MANY];
+    int nlive = 0;
+    bool fused = M == 1 && k > 0;
+    for (int i = 0; i < count; ++i) {
+        if (d[i].n == 0) continue;
+        live[nlive] = d[i];
+        live_y[nlive++] = ys[i];
+        fused = fused && one_token_register_path(d[i]);
+    }
+    if (nlive == 0) return QM_OK;
+    if (fused && gemv1_many_supported(live, nlive))
+        return check_launch(launch_gemv1_many(live, nlive, x, live_y, st), "gemv launch");
+    for (int i = 0; i < nlive; ++i) {
+        qm_status s;
+        if (k == 0)
+            s = check_launch(cudaMemsetAsync(live_y[i], 0, static_cast<size_t>(M * live[i].n * 2), st), "apply memset");
+        else
+            s = apply_launch(live[i], x, M, live_y[i], st);
+        if (s != QM_OK) return s;
+    }
+    return QM_OK;
 }
 
 qm_status qm_take(const qm_weight* w, int32_t axis, const void* ids, int32_t id_type,

@@ -51,20 +51,30 @@ namespace g1 {
 constexpr int kWarps = 4;   // warps per CTA
 constexpr int R = 2;        // rows per warp block
 constexpr int kChunk = 1024;
+constexpr int kMaxParts = 8;  // weights per launch (the C ABI's QM_MAX_MANY)
 
-struct Args {
+// One weight of a launch: several weights that read the same x (and share
+// format, widths and k) run as one grid, their blocks of R rows numbered one
+// after another.
+struct Part {
     const uint8_t* codes;
     const uint8_t* scales;
     const uint8_t* biases;
-    const uint16_t* x;
     uint16_t* y;
-    int64_t n, k;
+    int64_t n;
+};
+
+struct Args {
+    Part part[kMaxParts];
+    int bstart[kMaxParts + 1];  // first block of each part; bstart[nparts]: all blocks
+    int nparts;
+    const uint16_t* x;
+    int64_t k;
     int64_t code_row_bytes, scale_row_bytes;
     int gshift;          // log2(group_size): affine scales
     int sdt;             // affine scale dtype
     int nchunk;          // chunks of 1024 inputs: ceil(k / 1024)
-    int64_t nblocks;     // blocks of R rows: ceil(n / R)
-    int static_w;        // the weight may be read before the previous kernel ends
+    int static_w;        // the weights may be read before the previous kernel ends
 };
 
 // Words of packed data a lane holds for one row and one chunk.
@@ -94,19 +104,19 @@ QM_DEV uint32_t ldw(const uint8_t* base, int64_t a) {
     return __ldg(reinterpret_cast<const uint32_t*>(p));
 }
 
-// Loads lane data for row `row`, inputs [i0, i0 + 32). Rows past n and inputs
-// past k load nothing (the lane then contributes zero).
+// Loads lane data for row `row` of weight P, inputs [i0, i0 + 32). Rows past n
+// and inputs past k load nothing (the lane then contributes zero).
 template <int FMT, int BITS>
-QM_DEV void load_lane(const Args& a, int64_t row, int64_t i0, Lane<FMT, BITS>& L) {
+QM_DEV void load_lane(const Args& a, const Part& P, int64_t row, int64_t i0, Lane<FMT, BITS>& L) {
     constexpr int N = Words<FMT, BITS>::N;
-    if (row >= a.n || i0 >= a.k) {
+    if (row >= P.n || i0 >= a.k) {
 #pragma unroll
         for (int j = 0; j < N; ++j) L.w[j] = 0u;
         L.s = L.b = 0u;
         L.off = 0u;
         return;
     }
-    const uint8_t* rp = a.codes + row * a.code_row_bytes;
+    const uint8_t* rp = P.codes + row * a.code_row_bytes;
     if constexpr (FMT == QM_AFFINE) {
         const int64_t byte0 = i0 * BITS / 8;  // 4*BITS-byte aligned
         if constexpr (BITS % 4 == 0) {
@@ -126,8 +136,8 @@ QM_DEV void load_lane(const Args& a, int64_t row, int64_t i0, Lane<FMT, BITS>& L
             for (int q = 0; q < BITS; ++q) L.w[q] = __ldg(reinterpret_cast<const uint32_t*>(rp + byte0) + q);
         }
         const int64_t gi = row * (a.scale_row_bytes / 2) + (i0 >> a.gshift);
-        L.s = __ldg(reinterpret_cast<const uint16_t*>(a.scales) + gi);
-        L.b = __ldg(reinterpret_cast<const uint16_t*>(a.biases) + gi);
+        L.s = __ldg(reinterpret_cast<const uint16_t*>(P.scales) + gi);
+        L.b = __ldg(reinterpret_cast<const uint16_t*>(P.biases) + gi);
         L.off = 0u;
     } else if constexpr (FMT == QM_Q8_0) {
         // 34 bytes at a 2-byte boundary: the nine aligned words holding them
@@ -139,7 +149,7 @@ QM_DEV void load_lane(const Args& a, int64_t row, int64_t i0, Lane<FMT, BITS>& L
     } else if constexpr (FMT == QM_MXFP4) {
         const uint4 v = __ldg(reinterpret_cast<const uint4*>(rp + i0 / 2));
         L.w[0] = v.x; L.w[1] = v.y; L.w[2] = v.z; L.w[3] = v.w;
-        L.s = __ldg(a.scales + row * a.scale_row_bytes + i0 / 32);
+        L.s = __ldg(P.scales + row * a.scale_row_bytes + i0 / 32);
         L.b = 0u;
         L.off = 0u;
     } else if constexpr (FMT == QM_Q4_K) {
@@ -201,7 +211,7 @@ QM_DEV void load_acts(const Args& a, int64_t i0, Acts<FMT, BITS>& X) {
         const uint4* src = reinterpret_cast<const uint4*>(a.x + i0);
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const uint4 v = __ldg(src + q);
+            const uint4 v = __ldca(src + q);  // written by the previous kernel: a coherent load
             w[4 * q] = v.x; w[4 * q + 1] = v.y; w[4 * q + 2] = v.z; w[4 * q + 3] = v.w;
         }
     } else {
@@ -404,17 +414,18 @@ QM_DEV float lane_part(const Args& a, const Lane<FMT, BITS>& L, const Acts<FMT, 
     }
 }
 
-// Value i of row `row`, decoded at float32 from global memory as dequant decodes it.
+// Value i of row `row` of weight P, decoded at float32 from global memory as
+// dequant decodes it.
 template <int FMT, int BITS>
-QM_DEV float value_g(const Args& a, int64_t row, int64_t i) {
-    const uint8_t* rp = a.codes + row * a.code_row_bytes;
+QM_DEV float value_g(const Args& a, const Part& P, int64_t row, int64_t i) {
+    const uint8_t* rp = P.codes + row * a.code_row_bytes;
     if constexpr (FMT == QM_AFFINE) {
         const int64_t bit = i * BITS;
         const uint32_t lo = __ldg(rp + bit / 8), hi = (bit % 8 + BITS > 8) ? __ldg(rp + bit / 8 + 1) : 0u;
         const uint32_t c = ((lo | (hi << 8)) >> (bit % 8)) & ((1u << BITS) - 1u);
         const int64_t gi = row * (a.scale_row_bytes / 2) + (i >> a.gshift);
-        return fmaf(static_cast<float>(c), sval(__ldg(reinterpret_cast<const uint16_t*>(a.scales) + gi), a.sdt),
-                    sval(__ldg(reinterpret_cast<const uint16_t*>(a.biases) + gi), a.sdt));
+        return fmaf(static_cast<float>(c), sval(__ldg(reinterpret_cast<const uint16_t*>(P.scales) + gi), a.sdt),
+                    sval(__ldg(reinterpret_cast<const uint16_t*>(P.biases) + gi), a.sdt));
     } else if constexpr (FMT == QM_Q8_0) {
         const uint8_t* blk = rp + (i / 32) * 34;
         const float d = f16_bits_to_f32(static_cast<uint32_t>(__ldg(blk)) | (static_cast<uint32_t>(__ldg(blk + 1)) << 8));
@@ -444,7 +455,7 @@ QM_DEV float value_g(const Args& a, int64_t row, int64_t i) {
         if constexpr (FMT == QM_MXFP4) {
             const uint32_t byte = __ldg(rp + i / 2);
             c = (i & 1) ? (byte >> 4) : (byte & 15u);
-            sb = __ldg(a.scales + row * a.scale_row_bytes + i / 32);
+            sb = __ldg(P.scales + row * a.scale_row_bytes + i / 32);
         } else {
             const uint8_t* blk = rp + (i / 32) * 17;
             const int t = static_cast<int>(i % 32);
@@ -461,35 +472,45 @@ QM_DEV float value_g(const Args& a, int64_t row, int64_t i) {
 // The lane's contribution summed element by element: value times activation
 // at float32, inputs in ascending order. Out of line: rarely taken.
 template <int FMT, int BITS>
-static __device__ __noinline__ float lane_exact(const Args& a, int64_t row, int64_t i0) {
+static __device__ __noinline__ float lane_exact(const Args& a, const Part& P, int64_t row, int64_t i0) {
     float acc = 0.0f;
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
-        acc = fmaf(bf16_bits_to_f32(__ldg(a.x + i0 + i)), value_g<FMT, BITS>(a, row, i0 + i), acc);
+        acc = fmaf(bf16_bits_to_f32(__ldca(a.x + i0 + i)), value_g<FMT, BITS>(a, P, row, i0 + i), acc);
     return acc;
 }
 
 template <int FMT, int BITS>
 __global__ void __launch_bounds__(kWarps * 32) gemv1_kernel(const __grid_constant__ Args a) {
     const int lane = threadIdx.x & 31;
-    // 32-bit block indices (a block is R rows; rows < 2^32) and steps walked
-    // incrementally: no integer division anywhere on the path
+    // 32-bit block indices (a block is R rows; fewer than 2^31 blocks) and steps
+    // walked incrementally: no integer division anywhere on the path
     const int warp0 = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int nwarp = static_cast<int>((gridDim.x * blockDim.x) >> 5);
-    const int nblocks = static_cast<int>(a.nblocks), nchunk = a.nchunk;
+    const int nblocks = a.bstart[a.nparts], nchunk = a.nchunk;
     if (warp0 >= nblocks) return;  // nothing to read or write
+    // the weight holding block b, and the block's index within that weight
+    auto locate = [&](int b, int& g, int& lb) {
+        g = 0;
+        #pragma unroll 1
+        while (g + 1 < a.nparts && b >= a.bstart[g + 1]) ++g;
+        lb = b - a.bstart[g];
+    };
     Lane<FMT, BITS> cur[R], nxt[R];
-    auto load_step = [&](int b, int c, Lane<FMT, BITS> (&L)[R]) {
+    auto load_step = [&](int g, int lb, int c, Lane<FMT, BITS> (&L)[R]) {
+        const Part& P = a.part[g];
         const int64_t i0 = static_cast<int64_t>(c) * kChunk + 32 * lane;
 #pragma unroll
-        for (int r = 0; r < R; ++r) load_lane<FMT, BITS>(a, static_cast<int64_t>(b) * R + r, i0, L[r]);
+        for (int r = 0; r < R; ++r) load_lane<FMT, BITS>(a, P, static_cast<int64_t>(lb) * R + r, i0, L[r]);
     };
+    int cg, clb;  // the current block's weight and its block index there
+    locate(warp0, cg, clb);
     if (a.static_w) {  // the weight is not written by the previous kernel: read it first
-        load_step(warp0, 0, cur);
+        load_step(cg, clb, 0, cur);
         grid_dependency_wait();
     } else {
         grid_dependency_wait();
-        load_step(warp0, 0, cur);
+        load_step(cg, clb, 0, cur);
     }
     // Let the next kernel start only now: it still has this kernel's whole
     // remaining run to read its own static weights, and only one kernel waits
@@ -504,23 +525,25 @@ __global__ void __launch_bounds__(kWarps * 32) gemv1_kernel(const __grid_constan
     // (block b, chunk c) steps, chunks fastest
     #pragma unroll 1
     for (int b = warp0, c = 0; b < nblocks;) {
-        int b2 = b, c2 = c + 1;
+        int b2 = b, c2 = c + 1, g2 = cg, lb2 = clb;
         if (c2 == nchunk) {
             c2 = 0;
             b2 += nwarp;
+            if (b2 < nblocks) locate(b2, g2, lb2);
         }
-        if (b2 < nblocks) load_step(b2, c2, nxt);
+        if (b2 < nblocks) load_step(g2, lb2, c2, nxt);
         const int64_t i0 = static_cast<int64_t>(c) * kChunk + 32 * lane;
         if (nchunk > 1 || !have_x) {
             load_acts<FMT, BITS>(a, i0, X);
             have_x = true;
         }
+        const Part& P = a.part[cg];
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             bool exact;
             float part = lane_part<FMT, BITS>(a, cur[r], X, exact);
-            const int64_t row = static_cast<int64_t>(b) * R + r;
-            if ((exact || !isfinite(part)) && row < a.n && i0 < a.k) part = lane_exact<FMT, BITS>(a, row, i0);
+            const int64_t row = static_cast<int64_t>(clb) * R + r;
+            if ((exact || !isfinite(part)) && row < P.n && i0 < a.k) part = lane_exact<FMT, BITS>(a, P, row, i0);
             y[r] += part;
         }
         if (c == nchunk - 1) {
@@ -531,10 +554,10 @@ __global__ void __launch_bounds__(kWarps * 32) gemv1_kernel(const __grid_constan
             float v = ((lane & 1) ? y[1] : y[0]) + __shfl_xor_sync(0xffffffffu, give, 1);
 #pragma unroll
             for (int o = 2; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            const int64_t row = static_cast<int64_t>(b) * R + lane;  // lane 0: row 0 of the block, lane 1: row 1
-            if (lane < R && row < a.n) {
+            const int64_t row = static_cast<int64_t>(clb) * R + lane;  // lane 0: row 0 of the block, lane 1: row 1
+            if (lane < R && row < P.n) {
                 __nv_bfloat16 bv = __float2bfloat16_rn(v);
-                a.y[row] = *reinterpret_cast<uint16_t*>(&bv);
+                P.y[row] = *reinterpret_cast<uint16_t*>(&bv);
             }
 #pragma unroll
             for (int r = 0; r < R; ++r) y[r] = 0.0f;
@@ -543,13 +566,15 @@ __global__ void __launch_bounds__(kWarps * 32) gemv1_kernel(const __grid_constan
         for (int r = 0; r < R; ++r) cur[r] = nxt[r];
         b = b2;
         c = c2;
+        cg = g2;
+        clb = lb2;
     }
 }
 
 template <int FMT, int BITS>
 cudaError_t launch_t(const Args& a, cudaStream_t st) {
     // all warps resident at once where the rows allow: 16 warps per SM
-    const int64_t warps = std::min<int64_t>(a.nblocks, int64_t(num_sms()) * 16);
+    const int64_t warps = std::min<int64_t>(a.bstart[a.nparts], int64_t(num_sms()) * 16);
     const unsigned grid = static_cast<unsigned>((warps + kWarps - 1) / kWarps);
     return launch_pdl(gemv1_kernel<FMT, BITS>, grid, kWarps * 32, 0, st, a);
 }
@@ -565,15 +590,38 @@ bool gemv1_supported(const WDesc& w) {
     return w.fmt == QM_Q8_0 || w.fmt == QM_MXFP4 || w.fmt == QM_MXFP4_BLOCKS || w.fmt == QM_Q4_K || w.fmt == QM_Q6_K;
 }
 
-cudaError_t launch_gemv1(const WDesc& w, const void* x, void* y, cudaStream_t st) {
+bool gemv1_many_supported(const WDesc* ws, int count) {
+    if (count < 1 || count > g1::kMaxParts) return false;
+    int64_t blocks = 0;
+    for (int i = 0; i < count; ++i) {
+        const WDesc& w = ws[i];
+        if (!gemv1_supported(w)) return false;
+        if (w.fmt != ws[0].fmt || w.bits != ws[0].bits || w.gs != ws[0].gs || w.k != ws[0].k ||
+            w.code_row_bytes != ws[0].code_row_bytes || w.scale_row_bytes != ws[0].scale_row_bytes ||
+            (w.fmt == QM_AFFINE && w.sdt != ws[0].sdt))
+            return false;
+        blocks += (w.n + g1::R - 1) / g1::R;
+    }
+    return blocks < (int64_t(1) << 31);
+}
+
+cudaError_t launch_gemv1_many(const WDesc* ws, int count, const void* x, void* const* ys, cudaStream_t st) {
     using namespace g1;
+    const WDesc& w = ws[0];
     Args a{};
-    a.codes = w.codes;
-    a.scales = w.scales;
-    a.biases = w.biases;
+    a.nparts = count;
+    a.bstart[0] = 0;
+    bool all_static = true;
+    for (int i = 0; i < count; ++i) {
+        a.part[i].codes = ws[i].codes;
+        a.part[i].scales = ws[i].scales;
+        a.part[i].biases = ws[i].biases;
+        a.part[i].y = static_cast<uint16_t*>(ys[i]);
+        a.part[i].n = ws[i].n;
+        a.bstart[i + 1] = a.bstart[i] + static_cast<int>((ws[i].n + R - 1) / R);
+        all_static = all_static && ws[i].is_static;
+    }
     a.x = static_cast<const uint16_t*>(x);
-    a.y = static_cast<uint16_t*>(y);
-    a.n = w.n;
     a.k = w.k;
     a.code_row_bytes = w.code_row_bytes;
     a.scale_row_bytes = w.scale_row_bytes;
@@ -581,8 +629,7 @@ cudaError_t launch_gemv1(const WDesc& w, const void* x, void* y, cudaStream_t st
     while ((1 << a.gshift) < w.gs) ++a.gshift;
     a.sdt = w.sdt;
     a.nchunk = static_cast<int>((w.k + kChunk - 1) / kChunk);
-    a.nblocks = (w.n + R - 1) / R;
-    a.static_w = w.is_static ? 1 : 0;
+    a.static_w = all_static ? 1 : 0;
     if (w.fmt == QM_AFFINE) {
         switch (w.bits) {
             case 2: return launch_t<QM_AFFINE, 2>(a, st);
@@ -598,6 +645,11 @@ cudaError_t launch_gemv1(const WDesc& w, const void* x, void* y, cudaStream_t st
     if (w.fmt == QM_Q4_K) return launch_t<QM_Q4_K, 4>(a, st);
     if (w.fmt == QM_Q6_K) return launch_t<QM_Q6_K, 6>(a, st);
     return launch_t<QM_MXFP4_BLOCKS, 4>(a, st);
+}
+
+cudaError_t launch_gemv1(const WDesc& w, const void* x, void* y, cudaStream_t st) {
+    void* ys[1] = {y};
+    return launch_gemv1_many(&w, 1, x, ys, st);
 }
 
 }  // namespace qm

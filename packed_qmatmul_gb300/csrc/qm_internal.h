@@ -88,9 +88,13 @@ cudaError_t launch_take_dense(const WDesc& w, int axis, const void* ids, int id6
                               int out_dtype, void* out, cudaStream_t st);
 
 // y [1, n] = x [1, k] * W^T for a 2-d weight (one token), x and y bf16: a
-// register-only kernel, no shared memory (qm_gemv1.cu).
+// register-only kernel, no shared memory (qm_gemv1.cu). The _many form runs
+// up to 8 weights that read the same x (same format, widths and k) as one
+// grid, y_i for weight i.
 bool gemv1_supported(const WDesc& w);
 cudaError_t launch_gemv1(const WDesc& w, const void* x, void* y, cudaStream_t st);
+bool gemv1_many_supported(const WDesc* ws, int count);
+cudaError_t launch_gemv1_many(const WDesc* ws, int count, const void* x, void* const* ys, cudaStream_t st);
 // y [M, n] = x [M, k] * W^T for a 2-d weight, M <= 16, x and y bf16.
 qm_status launch_gemv(const WDesc& w, const void* x, int64_t M, void* y, cudaStream_t st);
 bool gemv_supported(const WDesc& w, int64_t M);

@@ -237,3 +237,39 @@ def test_quantize_q8_0_validation(lib):
     st, msg = err(4096, qm.QM_F32, 4, 64, 4096 + 512, None)  # the blocks would overwrite x
     assert st == qm.QM_EINVAL and msg.startswith("out:")
     assert lib.qm_quantize_q8_0(None, qm.QM_F32, 0, 64, None, None) == qm.QM_OK  # nothing to do
+
+
+def _many(lib, ws, x, M, ys, dt=qm.QM_BF16):
+    warr = (ctypes.POINTER(qm._CWeight) * max(len(ws), 1))(*[ctypes.pointer(w) for w in ws])
+    yarr = (ctypes.c_void_p * max(len(ys), 1))(*ys)
+    st = lib.qm_apply_many(warr, len(ws), x, M, dt, yarr, None)
+    return st, lib.qm_last_error().decode()
+
+
+def test_apply_many_validation(lib):
+    a, b = _w(), _w(shape=(32, 64), codes=1024, scales=2048, biases=3072)
+    # counts outside 1 .. QM_MAX_MANY
+    assert _many(lib, [], 4096, 1, [])[0] == qm.QM_EINVAL
+    st, msg = _many(lib, [a] * (qm.QM_MAX_MANY + 1), 4096, 1, [8192 + 256 * i for i in range(9)])
+    assert st == qm.QM_EINVAL and msg.startswith("count:")
+    # a bad weight is named by its index and part
+    st, msg = _many(lib, [a, _w(codes=0)], 4096, 1, [8192, 9216])
+    assert st == qm.QM_EINVAL and msg.startswith("ws[1]: codes"), msg
+    # weights must share format, widths and k
+    st, msg = _many(lib, [a, _w(bits=8)], 4096, 1, [8192, 9216])
+    assert st == qm.QM_EINVAL and msg.startswith("ws[1]:") and "bits" in msg, msg
+    st, msg = _many(lib, [a, _w(shape=(16, 128))], 4096, 1, [8192, 9216])
+    assert st == qm.QM_EINVAL and msg.startswith("ws[1]: k"), msg
+    # outputs: present, aligned, apart from x and from each other
+    st, msg = _many(lib, [a, b], 4096, 1, [8192, 0])
+    assert st == qm.QM_EINVAL and msg.startswith("ys[1]: NULL"), msg
+    st, msg = _many(lib, [a, b], 4096, 1, [8192, 9224])
+    assert st == qm.QM_EINVAL and msg.startswith("ys[1]:") and "aligned" in msg, msg
+    st, msg = _many(lib, [a, b], 4096, 1, [8192, 8208])  # ys[0] is 32 bytes long
+    assert st == qm.QM_EINVAL and msg == "ys[1]: overlaps ys[0]", msg
+    st, msg = _many(lib, [a, b], 4096, 1, [4160, 9216])  # x is 128 bytes long
+    assert st == qm.QM_EINVAL and msg == "ys[0]: overlaps x", msg
+    # activations are bfloat16; M = 0 does nothing
+    assert _many(lib, [a, b], 4096, 1, [8192, 9216], dt=qm.QM_F16)[0] == qm.QM_ENOTSUP
+    assert _many(lib, [a, b], 4096, -1, [8192, 9216])[0] == qm.QM_EINVAL
+    assert _many(lib, [a, b], 4096, 0, [8192, 9216])[0] == qm.QM_OK

@@ -797,3 +797,80 @@ def test_one_token_rows_off_word_boundaries(kind):
         else:
             w = synth.q6_k_weight(g, n, k)
         _check_apply(w, synth.activations(g, 1, k), f"{kind} n={n} k={k} M=1")
+
+
+@pytest.mark.parametrize("kind", ["affine4_g64", "q8_0", "mxfp4"])
+def test_one_token_long_and_ragged_k(kind):
+    # the one-token kernel at long k (16 and 17 chunks of 1024 inputs), and a
+    # k that ends inside a chunk
+    g = synth.rng(2000)
+    for n, k in ((40, 16384), (40, 16448), (33, 1088)):
+        w = _make(kind, g, n, k)
+        _check_apply(w, synth.activations(g, 1, k), f"{kind} n={n} k={k} M=1")
+
+
+# ---------------------------------------------------------------- several weights, one x
+def _many_kind(kind, g, n, k):
+    if kind == "q4_k":
+        return synth.q4_k_weight(g, n, k)
+    if kind == "q6_k":
+        return synth.q6_k_weight(g, n, k)
+    if kind == "mxfp4_blocks":
+        return synth.mxfp4_blocks_weight(g, n, k)
+    if kind == "affine3_g64":
+        return synth.affine_weight(g, n, k, bits=3, group_size=64)
+    return _make(kind, g, n, k)
+
+
+def _apply_many_vs_apply(arrays, M, g, static=True):
+    flags = qm.QM_WEIGHT_STATIC if static else 0
+    ws = [qm.QWeight.from_arrays(a, flags=flags) for a in arrays]
+    k = arrays[0]["shape"][-1]
+    x = synth.activations(g, M, k)
+    xd = _dev_bf16(x)
+    got = qm.apply_many(ws, xd)
+    for w, y in zip(ws, got):
+        want = qm.apply(w, xd)
+        assert torch.equal(y.view(torch.int16), want.view(torch.int16)), w.shape
+    return ws, x, got
+
+
+@pytest.mark.parametrize("kind", ["affine4_g64", "affine8_g64", "affine3_g64", "q8_0", "mxfp4",
+                                  "mxfp4_blocks", "q4_k", "q6_k"])
+@pytest.mark.parametrize("M", [1, 3])
+def test_apply_many_bit_identical_to_apply(kind, M):
+    # at M = 1 the weights run as one grid; the outputs are those of one call per weight
+    g = synth.rng(2100 + M)
+    for shapes in (((2048, 1024), (1024, 1024), (1024, 1024)), ((17, 512), (300, 512), (1, 512), (64, 512))):
+        _apply_many_vs_apply([_many_kind(kind, g, n, k) for n, k in shapes], M, g)
+
+
+def test_apply_many_against_the_oracle():
+    g = synth.rng(2200)
+    arrays = [synth.affine_weight(g, n, 1024, bits=4, group_size=64) for n in (2048, 1024, 1024)]
+    _, x, got = _apply_many_vs_apply(arrays, 1, g, static=False)
+    for a, y in zip(arrays, got):
+        ow = to_oracle(a)
+        xn = np.linalg.norm(oracle.decode_array(x, oracle.BF16), axis=1)
+        check_product(bf16_to_f64(_host(y)), oracle.apply(ow, x), row_norms(ow), xn, ow.k, "apply_many")
+
+
+def test_apply_many_edge_cases():
+    g = synth.rng(2300)
+    # an empty weight among others; the most weights a call takes; one weight
+    arrays = [synth.affine_weight(g, n, 256, bits=4, group_size=64) for n in (5, 0, 7, 1, 2, 3, 4, 9)]
+    _apply_many_vs_apply(arrays, 1, g)
+    _apply_many_vs_apply(arrays[:1], 1, g)
+    # a weight above 24 MB keeps its own launch (the streaming GEMV), the others still agree
+    big = [synth.affine_weight(g, 50000, 1024, bits=4, group_size=64),
+           synth.affine_weight(g, 64, 1024, bits=4, group_size=64)]
+    _apply_many_vs_apply(big, 1, g)
+    # non-finite values (MXFP4 scale bytes 254/255) go element by element in the fused grid too
+    w1 = synth.mxfp4_weight(g, 40, 256)
+    w1["scales"][3, 2] = 254
+    w1["scales"][7, 0] = 255
+    w2 = synth.mxfp4_weight(g, 24, 256)
+    ws, x, got = _apply_many_vs_apply([w1, w2], 1, g)
+    ow = to_oracle(w1)
+    xn = np.linalg.norm(oracle.decode_array(x, oracle.BF16), axis=1)
+    check_product(bf16_to_f64(_host(got[0])), oracle.apply(ow, x), row_norms(ow), xn, ow.k, "many nonfinite")
