@@ -640,8 +640,8 @@ def run_ours(args, rank, world):
         "config": config_dict(bits, M, fused),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4),
-                     "traffic": traffic("decode", bits == 4 and M == 1 and not args.only)[0],
-                     "traffic_source": traffic("decode", bits == 4 and M == 1 and not args.only)[1],
+                     "traffic": traffic("decode", bits == 4 and M == 1 and not args.only and fused)[0],
+                     "traffic_source": traffic("decode", bits == 4 and M == 1 and not args.only and fused)[1],
                      "algorithmic_bytes_per_launch": round(lay_algo / len(layers)),
                      "launch_us": round(avg_launch * 1e6, 3),
                      "kernel": (f"gemv1_kernel<affine,{bits}> (the {len(layers)} layer launches of the step"
@@ -749,7 +749,7 @@ def detail_measurements(args, dev, stream, fused=True):
 # capture, with the commit whose kernel was measured. A kernel changed after its
 # capture has None here (reported as null) until it is captured again.
 TRAFFIC = {
-    "decode": (None, None),
+    "decode": (2575360.0, "2e09160"),
     "experts_gemm": (None, None),
     "experts_gemv": (None, None),
     "dequant": (337.4e6, "6d4178e"),

@@ -33,3 +33,19 @@ def test_traffic_figures_name_their_capture():
         v, why = bench.traffic(key)
         assert v == value and commit in why and "profiles/" not in why
     assert bench.traffic("dequant", False) == (None, None)
+
+
+def test_grouped_step_calls():
+    # products that read the same activations share a call: per layer q/k/v and
+    # gate/up, with down_proj and lm_head alone -- 85 calls over the same 169 products
+    items = [(name, n, k, None, None, None) for name, n, k in bench.workload_list(4)]
+    groups = bench.step_groups(items, True)
+    assert len(groups) == 28 * 3 + 1
+    assert [it for g in groups for it in g] == items
+    names = [[it[0].split(".")[-1] for it in g] for g in groups[:3]]
+    assert names == [["q_proj", "k_proj", "v_proj"], ["gate_proj", "up_proj"], ["down_proj"]]
+    assert all(len({it[2] for it in g}) == 1 for g in groups)  # one k per call
+    assert [len(g) for g in bench.step_groups(items, False)] == [1] * 169
+    # algorithmic bytes of a call: its packed weights, x once, every output
+    g = groups[0]
+    assert bench.group_algo_bytes(g, 4, 1) == sum(bench.packed_bytes(n, k, 4) + 2 * n for _, n, k, *_ in g) + 2 * 1024
