@@ -61,13 +61,18 @@ constexpr int NR = 2;           // raw chunk slots
 // bytes, unswizzled (a row's codes then start on a 4-byte boundary).
 // Q4_K comes as one 144-byte block (256 inputs) per row, unswizzled: rows 144
 // bytes (nine 16-byte units) apart put consecutive rows in distinct bank groups.
+// MXFP4 in GGUF's 17-byte blocks comes as 16 blocks (512 inputs, 272 bytes, a
+// 16-byte multiple, as Q8_0's 8 blocks are) per row, unswizzled, read as
+// 16-bit elements (the box's inner extent is then 136 elements).
 template <int FMT, int BITS>
 struct Raw {
     static constexpr bool GEN = FMT == QM_AFFINE && BITS != 4 && BITS != 8;
-    static constexpr int RAWK = (GEN || (FMT == QM_AFFINE && BITS == 8)) ? 128 : 256;
-    static constexpr int BYTES = GEN ? 16 * BITS : (FMT == QM_Q8_0) ? 272 : (FMT == QM_Q4_K) ? 144 : 128;
-    static constexpr bool SW = FMT != QM_Q8_0 && FMT != QM_Q4_K && !GEN;
-    static constexpr int ELEM = (FMT == QM_Q8_0) ? 2 : 1;
+    static constexpr bool MXB = FMT == QM_MXFP4_BLOCKS;
+    static constexpr int RAWK = (GEN || (FMT == QM_AFFINE && BITS == 8)) ? 128 : MXB ? 512 : 256;
+    static constexpr int BYTES =
+        GEN ? 16 * BITS : (FMT == QM_Q8_0 || MXB) ? 272 : (FMT == QM_Q4_K) ? 144 : 128;
+    static constexpr bool SW = FMT != QM_Q8_0 && FMT != QM_Q4_K && !GEN && !MXB;
+    static constexpr int ELEM = (FMT == QM_Q8_0 || MXB) ? 2 : 1;
     static constexpr int SPR = RAWK / BK;  // k steps per chunk
 };
 
@@ -161,6 +166,37 @@ QM_DEV void decode_q8_block(const uint8_t* raw, int row, uint32_t (&o)[16]) {
             const float2 v = mul2(add2(f, neg), d2);
             o[(4 * j + i) / 2] = bf2(v.x, v.y);
         }
+    }
+}
+
+// GGUF MXFP4 block B (0..15) of a raw chunk row as 16 bf16 pairs. Rows are 272
+// bytes apart; block B's 17 bytes start B bytes into the row's 16-byte unit B,
+// so units B and B + 1 hold them (and end inside the row). Data byte j holds
+// values j (low nibble) and j + 16: each byte's decoded pair is split between
+// output pairs j/2 and 8 + j/2 as the bf16 pairs are formed.
+template <int B>
+QM_DEV void decode_mxb_block(const uint8_t* raw, int row, uint32_t (&o)[16]) {
+    const uint4* src = reinterpret_cast<const uint4*>(raw + row * 272 + 16 * B);
+    const uint4 u0 = src[0], u1 = src[1];
+    const uint32_t w[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    const float s = e8m0_to_f32((w[B / 4] >> (8 * (B % 4))) & 0xFFu);
+    constexpr int kW = (B + 1) / 4, kS = 8 * ((B + 1) % 4);  // data byte 0: word, shift
+    const float2 s2 = make_float2(s, s);
+    float2 p[16];  // p[j] = (value j, value j + 16)
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        uint32_t dw;
+        if constexpr (kS == 0) dw = w[kW + q];
+        else dw = __funnelshift_r(w[kW + q], w[kW + q + 1], kS);
+        uint32_t h[4];
+        e2m1x8_to_f16x2(dw, h);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) p[4 * q + i] = mul2(__half22float2(*reinterpret_cast<const __half2*>(&h[i])), s2);
+    }
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+        o[m] = bf2(p[2 * m].x, p[2 * m + 1].x);
+        o[8 + m] = bf2(p[2 * m].y, p[2 * m + 1].y);
     }
 }
 
@@ -260,6 +296,25 @@ QM_DEV void decode32(const uint8_t* raw, int row, int kk, int half, Sc sc, uint3
                 const float2 v = mul2(__half22float2(*reinterpret_cast<const __half2*>(&h2[i])), s2);
                 o[4 * j + i] = bf2(v.x, v.y);
             }
+        }
+    } else if constexpr (FMT == QM_MXFP4_BLOCKS) {  // block kk*2 + half of the chunk
+        switch (2 * kk + half) {
+            case 0: decode_mxb_block<0>(raw, row, o); break;
+            case 1: decode_mxb_block<1>(raw, row, o); break;
+            case 2: decode_mxb_block<2>(raw, row, o); break;
+            case 3: decode_mxb_block<3>(raw, row, o); break;
+            case 4: decode_mxb_block<4>(raw, row, o); break;
+            case 5: decode_mxb_block<5>(raw, row, o); break;
+            case 6: decode_mxb_block<6>(raw, row, o); break;
+            case 7: decode_mxb_block<7>(raw, row, o); break;
+            case 8: decode_mxb_block<8>(raw, row, o); break;
+            case 9: decode_mxb_block<9>(raw, row, o); break;
+            case 10: decode_mxb_block<10>(raw, row, o); break;
+            case 11: decode_mxb_block<11>(raw, row, o); break;
+            case 12: decode_mxb_block<12>(raw, row, o); break;
+            case 13: decode_mxb_block<13>(raw, row, o); break;
+            case 14: decode_mxb_block<14>(raw, row, o); break;
+            default: decode_mxb_block<15>(raw, row, o); break;
         }
     } else {  // Q8_0: block kk*2 + half of the chunk (kk is a constant once the k loop unrolls)
         switch (2 * kk + half) {
@@ -737,6 +792,7 @@ static cudaError_t dispatch(Params& p, const WDesc& w, const void* x, cudaStream
     if (w.fmt == QM_Q8_0) return launch_bm<QM_Q8_0, 8, 32>(p, w, x, st);
     if (w.fmt == QM_MXFP4) return launch_bm<QM_MXFP4, 4, 32>(p, w, x, st);
     if (w.fmt == QM_Q4_K) return launch_bm<QM_Q4_K, 4, 0>(p, w, x, st);
+    if (w.fmt == QM_MXFP4_BLOCKS) return launch_bm<QM_MXFP4_BLOCKS, 4, 32>(p, w, x, st);
     return cudaErrorInvalidValue;
 }
 

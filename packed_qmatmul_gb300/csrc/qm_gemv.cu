@@ -242,6 +242,26 @@ QM_DEV void tile_group(const CodeRow& r0, const CodeRow& r8, int gi, int t,
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) mma_f16(acc[nt], a0, a1, a2, a3, bf[mm][nt][0], bf[mm][nt][1]);
         }
+    } else if constexpr (FMT == QM_MXFP4_BLOCKS) {
+        // data bytes 4t .. 4t+3 of 17-byte block gi (its scale byte, then byte j
+        // holding values j and j + 16), from the aligned words around them. The
+        // second word is read only when the bytes straddle two: a row holds a
+        // multiple of 16 blocks, so its last block's data bytes are aligned and
+        // no read passes the row's end.
+        const uint32_t o = 17 * gi + 1 + 4 * t, a = o & ~3u, sh = 8u * (o & 3u);
+        const uint32_t d8 = r8.line - r0.line;
+        const uint32_t p0 = r0.at(a), p1 = sh ? r0.at(a + 4) : p0;
+        const uint32_t w0 = __funnelshift_r(lds_u32(p0), lds_u32(p1), sh);
+        const uint32_t w8 = __funnelshift_r(lds_u32(p0 + d8), lds_u32(p1 + d8), sh);
+        uint32_t h0[4], h8[4];
+        e2m1x8_to_f16x2(w0, h0);  // byte i -> (value 4t + i, value 4t + i + 16)
+        e2m1x8_to_f16x2(w8, h8);
+#pragma unroll
+        for (int mm = 0; mm < 2; ++mm)
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                mma_f16(acc[nt], h0[2 * mm], h8[2 * mm], h0[2 * mm + 1], h8[2 * mm + 1], bf[mm][nt][0],
+                        bf[mm][nt][1]);
     } else {  // MXFP4
         const uint32_t o = 16 * gi + 4 * t;
         uint32_t h0[4], h8[4];
@@ -269,9 +289,16 @@ QM_DEV float elem_value(const CodeRow& r, int gi, int i, float s, float b) {
         const int q = static_cast<int8_t>(lds_u8(r.at(34 * gi + 2 + i)));
         return s * static_cast<float>(q);
     } else {
-        const uint32_t byte = lds_u8(r.at(16 * gi + (i >> 1)));
+        uint32_t code;
+        if constexpr (FMT == QM_MXFP4_BLOCKS) {  // byte j of the block's data: values j and j + 16
+            const uint32_t byte = lds_u8(r.at(17 * gi + 1 + (i & 15)));
+            code = i < 16 ? (byte & 15u) : (byte >> 4);
+        } else {
+            const uint32_t byte = lds_u8(r.at(16 * gi + (i >> 1)));
+            code = (i & 1) ? (byte >> 4) : (byte & 15u);
+        }
         uint32_t h[4];
-        e2m1x8_to_f16x2((i & 1) ? (byte >> 4) : (byte & 15u), h);
+        e2m1x8_to_f16x2(code, h);
         return __half2float(__ushort_as_half(static_cast<unsigned short>(h[0] & 0xFFFFu))) * s;
     }
 }
@@ -587,6 +614,11 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
                     constexpr int V = GS / 16;
                     const int k0 = 4 * (gi * (GS / 4) + t * V + mm);
                     lo0 = xv(k0); hi0 = xv(k0 + 1); lo1 = xv(k0 + 2); hi1 = xv(k0 + 3);
+                } else if constexpr (FMT == QM_MXFP4_BLOCKS) {
+                    // lane t holds values 4t .. 4t+3 and 4t+16 .. 4t+19 of the block,
+                    // paired (j, j + 16) as its bytes pair them
+                    const int k0 = 32 * gi + 4 * t + 2 * mm;
+                    lo0 = xv(k0); hi0 = xv(k0 + 16); lo1 = xv(k0 + 1); hi1 = xv(k0 + 17);
                 } else {  // Q8_0, MXFP4: lane t holds values 8t .. 8t+7 of the block
                     const int k0 = 32 * gi + 8 * t + 4 * mm;
                     lo0 = xv(k0); hi0 = xv(k0 + 1); lo1 = xv(k0 + 2); hi1 = xv(k0 + 3);
@@ -596,7 +628,7 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
                     dst[0] = pack_f16x2(lo0, hi0);
                     dst[1] = pack_f16x2(lo1 * f1, hi1 * f1);
                 }
-                if constexpr (FMT != QM_MXFP4) {
+                if constexpr (FMT != QM_MXFP4 && FMT != QM_MXFP4_BLOCKS) {
                     // the offset the magic adds: magic * sum of the B values the MMAs see
                     float X = (lo0 + hi0) + (lo1 + hi1);
                     float F = (lo0 + hi0) + (lo1 * f1 + hi1 * f1);
@@ -647,6 +679,13 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
                         put(v * NT * 2 + 0, xv(k0), xv(k0 + 1), 1.0f, 1.0f);
                         put(v * NT * 2 + 1, xv(k0 + 2), xv(k0 + 3), 1.0f, 1.0f);
                     }
+                } else if constexpr (FMT == QM_MXFP4_BLOCKS) {  // values (j, j + 16) as the bytes pair them
+#pragma unroll
+                    for (int mm = 0; mm < 2; ++mm) {
+                        const int k0 = 32 * gi + 4 * t + 2 * mm;
+                        put(mm * NT * 2 + 0, xv(k0), xv(k0 + 16), 1.0f, 1.0f);
+                        put(mm * NT * 2 + 1, xv(k0 + 1), xv(k0 + 17), 1.0f, 1.0f);
+                    }
                 } else {  // Q8_0, MXFP4: lane t holds values 8t .. 8t+7 of the block
 #pragma unroll
                     for (int mm = 0; mm < 2; ++mm) {
@@ -655,7 +694,7 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
                         put(mm * NT * 2 + 1, xv(k0 + 2), xv(k0 + 3), 1.0f, 1.0f);
                     }
                 }
-                if constexpr (FMT != QM_MXFP4) {
+                if constexpr (FMT != QM_MXFP4 && FMT != QM_MXFP4_BLOCKS) {
                     // the offset the magic adds: magic * sum of the B values the MMAs see
                     X += __shfl_xor_sync(0xffffffffu, X, 1);
                     F += __shfl_xor_sync(0xffffffffu, F, 1);
@@ -769,6 +808,10 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
                         const uint32_t da = rows_[2 * tt].at(34 * gi);
                         raw[tt][0] = lds_u16(da);
                         raw[tt][1] = lds_u16(da + (rows_[2 * tt + 1].line - rows_[2 * tt].line));
+                    } else if constexpr (FMT == QM_MXFP4_BLOCKS) {  // the block's first byte
+                        const uint32_t da = rows_[2 * tt].at(17 * gi);
+                        raw[tt][0] = lds_u8(da);
+                        raw[tt][1] = lds_u8(da + (rows_[2 * tt + 1].line - rows_[2 * tt].line));
                     } else {
                         const uint32_t sa = st + p.off_scales + ra * p.scale_pitch + soff + gi;
                         raw[tt][0] = lds_u8(sa);
@@ -808,7 +851,7 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
             // the group's sums, at the activations' 2^E scale, into y
             auto epilogue = [&](int gi, const float (&acc)[2][NT][4], const uint32_t (&raw)[2][4]) {
                 float4 td[NT];  // (O[2t], X[2t], O[2t+1], X[2t+1]) per token half
-                if constexpr (FMT != QM_MXFP4) {
+                if constexpr (FMT != QM_MXFP4 && FMT != QM_MXFP4_BLOCKS) {
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt)
                         td[nt] = *reinterpret_cast<const float4*>(tok + gi * 16 + nt * 8 + 2 * t);
@@ -821,7 +864,7 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
                     for (int nt = 0; nt < NT; ++nt) {
                         float* yv = y[tt][nt];
                         const float* c = acc[tt][nt];
-                        if constexpr (FMT == QM_MXFP4) {
+                        if constexpr (FMT == QM_MXFP4 || FMT == QM_MXFP4_BLOCKS) {
                             yv[0] = fmaf(s0, c[0], yv[0]);
                             yv[2] = fmaf(s8, c[2], yv[2]);
                             if constexpr (!ONE) {
@@ -1040,6 +1083,7 @@ static uint32_t round_up(uint64_t v, uint64_t a) { return static_cast<uint32_t>(
 // Bytes of codes for `kk` values of one row.
 static int64_t code_bytes(const WDesc& w, int64_t kk) {
     if (w.fmt == QM_Q8_0) return kk / 32 * 34;
+    if (w.fmt == QM_MXFP4_BLOCKS) return kk / 32 * 17;
     return kk * w.bits / 8;
 }
 
@@ -1378,6 +1422,7 @@ qm_status launch_gemv(const WDesc& w, const void* x, int64_t M, void* y, cudaStr
     QM_GEMV_CASE(QM_AFFINE, 8, 128)
     QM_GEMV_CASE(QM_Q8_0, 8, 32)
     QM_GEMV_CASE(QM_MXFP4, 4, 32)
+    QM_GEMV_CASE(QM_MXFP4_BLOCKS, 4, 32)
 #undef QM_GEMV_CASE
 done:
     if (e != cudaSuccess) return cuda_fail(e, "gemv launch");
@@ -1467,6 +1512,7 @@ qm_status launch_gemv_grouped(const WDesc& w, const int32_t* offsets, const int3
     QM_GEMV_CASE(QM_AFFINE, 8, 128)
     QM_GEMV_CASE(QM_Q8_0, 8, 32)
     QM_GEMV_CASE(QM_MXFP4, 4, 32)
+    QM_GEMV_CASE(QM_MXFP4_BLOCKS, 4, 32)
 #undef QM_GEMV_CASE
 done:
     if (e != cudaSuccess) return cuda_fail(e, "grouped gemv launch");

@@ -59,12 +59,15 @@ int max_smem_optin();
 // Weights the tensor-map decode GEMV (several tokens) decodes; the others take
 // the plain kernels there.
 inline bool pipelined_format(const WDesc& w) {
-    return (w.fmt == QM_AFFINE && (w.bits == 4 || w.bits == 8)) || w.fmt == QM_Q8_0 || w.fmt == QM_MXFP4;
+    return (w.fmt == QM_AFFINE && (w.bits == 4 || w.bits == 8)) || w.fmt == QM_Q8_0 || w.fmt == QM_MXFP4 ||
+           w.fmt == QM_MXFP4_BLOCKS;
 }
 // Weights the tensor-core GEMM decodes: affine at every width, Q8_0, MXFP4,
-// Q4_K (Q6_K's 210-byte blocks are no 16-byte multiple: no tensor-map tiles).
+// MXFP4 in GGUF's blocks, Q4_K (Q6_K's 210-byte blocks are no 16-byte
+// multiple: no tensor-map tiles).
 inline bool gemm_format(const WDesc& w) {
-    return w.fmt == QM_AFFINE || w.fmt == QM_Q8_0 || w.fmt == QM_MXFP4 || w.fmt == QM_Q4_K;
+    return w.fmt == QM_AFFINE || w.fmt == QM_Q8_0 || w.fmt == QM_MXFP4 || w.fmt == QM_MXFP4_BLOCKS ||
+           w.fmt == QM_Q4_K;
 }
 
 // ------------------------------------------------------------ launchers

@@ -214,7 +214,7 @@ def test_affine_special_scales(bits, gs, sdt, M):
 
 
 # ---------------------------------------------------------------- activations
-@pytest.mark.parametrize("M", [1, 33])
+@pytest.mark.parametrize("M", [1, 8, 33])
 def test_mxfp4_blocks_every_scale_byte(M):
     # MXFP4 in GGUF's 17-byte blocks: row r has one block at scale byte r
     g = synth.rng(1425 + M)

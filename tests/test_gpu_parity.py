@@ -597,11 +597,30 @@ def test_mxfp4_blocks_take(id64):
         assert _bits_equal(_host(dense), oracle.dequant(ot, oracle.BF16), torch.bfloat16), (lead, axis)
 
 
-@pytest.mark.parametrize("M", [1, 8, 33])
+@pytest.mark.parametrize("M", [1, 2, 8, 16, 33, 130])
 def test_mxfp4_blocks_apply(M):
+    # k a multiple of 512: M <= 16 streams the 17-byte blocks through the
+    # tensor-map GEMV (one CTA per stage, a k split over a cluster, many stages
+    # per CTA), M >= 17 decodes them for the tensor cores (128- and 256-token tiles)
     g = synth.rng(702 + M)
-    w = synth.mxfp4_blocks_weight(g, 80, 512)
-    _check_apply(w, synth.activations(g, M, 512), f"mxfp4 blocks M={M}")
+    for n, k in ((80, 512), (64, 4096), (9000, 512)):
+        w = synth.mxfp4_blocks_weight(g, n, k)
+        _check_apply(w, synth.activations(g, M, k), f"mxfp4 blocks n={n} k={k} M={M}")
+
+
+def test_mxfp4_blocks_one_token_full_shape_sampled():
+    # 14336 x 4096 in GGUF blocks (31 MB) at M = 1: the tensor-map GEMV, checked
+    # on sampled outputs the oracle computes one by one
+    g = synth.rng(706)
+    w = synth.mxfp4_blocks_weight(g, 14336, 4096)
+    x = synth.activations(g, 1, 4096)
+    ow = to_oracle(w)
+    y = bf16_to_f64(_host(qm.apply(qm.QWeight.from_arrays(w), _dev_bf16(x))))[0]
+    j = np.unique(np.concatenate([g.integers(0, 14336, 1500), [0, 1, 14335]]))
+    ref = oracle.apply_entries(ow, x, np.zeros_like(j), j)
+    wn = np.array([np.linalg.norm(oracle.row_values(ow, int(r)).astype(np.float64)) for r in j])
+    xn = np.linalg.norm(oracle.decode_array(x, oracle.BF16), axis=1)
+    check_product(y[j][None], ref[None], wn, xn, 4096, "mxfp4 blocks 14336x4096 sampled")
 
 
 def test_mxfp4_blocks_apply_experts():
@@ -611,6 +630,16 @@ def test_mxfp4_blocks_apply_experts():
     ids[3, 1] = 4   # out of range: zeros
     ids[7, 0] = -1
     _check_experts(w, ids, synth.activations(g, 16, 256), "mxfp4 blocks experts")
+    # k a multiple of 512: the grouped tensor-map GEMV
+    w = synth.mxfp4_blocks_weight(g, 64, 512, lead=(8,))
+    ids = synth.expert_ids(g, 24, 2, 8).astype(np.int32)
+    ids[5, 0] = 8
+    _check_experts(w, ids, synth.activations(g, 24, 512), "mxfp4 blocks experts k=512")
+    # more than 32 positions per expert: the grouped tensor-core GEMM
+    w = synth.mxfp4_blocks_weight(g, 160, 1024, lead=(4,))
+    ids = synth.expert_ids(g, 96, 2, 4).astype(np.int32)
+    ids[9, 1] = -1
+    _check_experts(w, ids, synth.activations(g, 96, 1024), "mxfp4 blocks experts tensor path")
 
 
 # ---------------------------------------------------------------- quantize_q8_0
