@@ -520,14 +520,18 @@ __global__ void __launch_bounds__(kThreads, NTOK <= 128 ? 2 : 1) gemm_kernel(con
         const int64_t grow = n0 + row;
         const bool rowok = grow < p.n;
         Sc cur[R::SPR][2], nxt[R::SPR][2];
+        // a chunk holds an even number of k steps, so this thread decodes steps
+        // kk with kk % 2 == grp of every chunk: only their scales are fetched
+        static_assert(R::SPR % 2 == 0, "k steps per chunk");
         auto fetch = [&](int rc, Sc (&dst)[R::SPR][2]) {
 #pragma unroll
             for (int kk = 0; kk < R::SPR; ++kk)
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
-                    dst[kk][h] = rowok ? load_scale<FMT, BITS, GS>(p, wrow0 + grow,
-                                                                   static_cast<int64_t>(rc) * R::RAWK + kk * BK + h * 32)
-                                       : Sc{0.0f, 0.0f};
+                    dst[kk][h] = rowok && (kk & 1) == grp
+                                     ? load_scale<FMT, BITS, GS>(p, wrow0 + grow,
+                                                                 static_cast<int64_t>(rc) * R::RAWK + kk * BK + h * 32)
+                                     : Sc{0.0f, 0.0f};
         };
         fetch(c_lo, cur);
         for (int rc = c_lo; rc < c_hi; ++rc) {

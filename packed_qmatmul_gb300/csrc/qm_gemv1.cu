@@ -99,15 +99,16 @@ struct Lane {
 
 // The aligned 32-bit word holding the byte at base + a (aligned as an address:
 // a row of GGUF blocks may start at any even or odd byte).
-QM_DEV uint32_t ldw(const uint8_t* base, int64_t a) {
+QM_DEV uint32_t ldw(const uint8_t* base, int64_t a, uint64_t pol) {
     const uintptr_t p = reinterpret_cast<uintptr_t>(base + a) & ~uintptr_t(3);
-    return __ldg(reinterpret_cast<const uint32_t*>(p));
+    return ldg_stream(reinterpret_cast<const uint32_t*>(p), pol);
 }
 
 // Loads lane data for row `row` of weight P, inputs [i0, i0 + 32). Rows past n
 // and inputs past k load nothing (the lane then contributes zero).
+// Weights stream (ldg_stream, policy pol): each is read once per product.
 template <int FMT, int BITS>
-QM_DEV void load_lane(const Args& a, const Part& P, int64_t row, int64_t i0, Lane<FMT, BITS>& L) {
+QM_DEV void load_lane(const Args& a, const Part& P, int64_t row, int64_t i0, uint64_t pol, Lane<FMT, BITS>& L) {
     constexpr int N = Words<FMT, BITS>::N;
     if (row >= P.n || i0 >= a.k) {
 #pragma unroll
@@ -122,34 +123,34 @@ QM_DEV void load_lane(const Args& a, const Part& P, int64_t row, int64_t i0, Lan
         if constexpr (BITS % 4 == 0) {
 #pragma unroll
             for (int q = 0; q < BITS / 4; ++q) {
-                const uint4 v = __ldg(reinterpret_cast<const uint4*>(rp + byte0) + q);
+                const uint4 v = ldg_stream(reinterpret_cast<const uint4*>(rp + byte0) + q, pol);
                 L.w[4 * q] = v.x; L.w[4 * q + 1] = v.y; L.w[4 * q + 2] = v.z; L.w[4 * q + 3] = v.w;
             }
         } else if constexpr (BITS % 2 == 0) {
 #pragma unroll
             for (int q = 0; q < BITS / 2; ++q) {
-                const uint2 v = __ldg(reinterpret_cast<const uint2*>(rp + byte0) + q);
+                const uint2 v = ldg_stream(reinterpret_cast<const uint2*>(rp + byte0) + q, pol);
                 L.w[2 * q] = v.x; L.w[2 * q + 1] = v.y;
             }
         } else {
 #pragma unroll
-            for (int q = 0; q < BITS; ++q) L.w[q] = __ldg(reinterpret_cast<const uint32_t*>(rp + byte0) + q);
+            for (int q = 0; q < BITS; ++q) L.w[q] = ldg_stream(reinterpret_cast<const uint32_t*>(rp + byte0) + q, pol);
         }
         const int64_t gi = row * (a.scale_row_bytes / 2) + (i0 >> a.gshift);
-        L.s = __ldg(reinterpret_cast<const uint16_t*>(P.scales) + gi);
-        L.b = __ldg(reinterpret_cast<const uint16_t*>(P.biases) + gi);
+        L.s = ldg_stream(reinterpret_cast<const uint16_t*>(P.scales) + gi, pol);
+        L.b = ldg_stream(reinterpret_cast<const uint16_t*>(P.biases) + gi, pol);
         L.off = 0u;
     } else if constexpr (FMT == QM_Q8_0) {
         // 34 bytes at a 2-byte boundary: the nine aligned words holding them
         const int64_t a0 = (i0 / 32) * 34;
         L.off = static_cast<uint32_t>((reinterpret_cast<uintptr_t>(rp) + a0) & 3u);
 #pragma unroll
-        for (int j = 0; j < 9; ++j) L.w[j] = ldw(rp, a0 + 4 * j);
+        for (int j = 0; j < 9; ++j) L.w[j] = ldw(rp, a0 + 4 * j, pol);
         L.s = L.b = 0u;
     } else if constexpr (FMT == QM_MXFP4) {
-        const uint4 v = __ldg(reinterpret_cast<const uint4*>(rp + i0 / 2));
+        const uint4 v = ldg_stream(reinterpret_cast<const uint4*>(rp + i0 / 2), pol);
         L.w[0] = v.x; L.w[1] = v.y; L.w[2] = v.z; L.w[3] = v.w;
-        L.s = __ldg(P.scales + row * a.scale_row_bytes + i0 / 32);
+        L.s = ldg_stream(P.scales + row * a.scale_row_bytes + i0 / 32, pol);
         L.b = 0u;
         L.off = 0u;
     } else if constexpr (FMT == QM_Q4_K) {
@@ -158,9 +159,9 @@ QM_DEV void load_lane(const Args& a, const Part& P, int64_t row, int64_t i0, Lan
         // whose low (j even) or high (j odd) nibbles are its values
         const uint8_t* blk = rp + (i0 / 256) * 144;
         const int j = static_cast<int>((i0 / 32) % 8);
-        const uint4 h = __ldg(reinterpret_cast<const uint4*>(blk));
+        const uint4 h = ldg_stream(reinterpret_cast<const uint4*>(blk), pol);
         const uint4* qp = reinterpret_cast<const uint4*>(blk + 16 + 32 * (j / 2));
-        const uint4 q0 = __ldg(qp), q1 = __ldg(qp + 1);
+        const uint4 q0 = ldg_stream(qp, pol), q1 = ldg_stream(qp + 1, pol);
         L.w[0] = h.x; L.w[1] = h.y; L.w[2] = h.z; L.w[3] = h.w;
         L.w[4] = q0.x; L.w[5] = q0.y; L.w[6] = q0.z; L.w[7] = q0.w;
         L.w[8] = q1.x; L.w[9] = q1.y; L.w[10] = q1.z; L.w[11] = q1.w;
@@ -175,11 +176,11 @@ QM_DEV void load_lane(const Args& a, const Part& P, int64_t row, int64_t i0, Lan
         const int64_t aql = a0 + 64 * h + 32 * (t % 2), aqh = a0 + 128 + 32 * h;
 #pragma unroll
         for (int q = 0; q < 9; ++q) {
-            L.w[q] = ldw(rp, aql + 4 * q);
-            L.w[9 + q] = ldw(rp, aqh + 4 * q);
+            L.w[q] = ldw(rp, aql + 4 * q, pol);
+            L.w[9 + q] = ldw(rp, aqh + 4 * q, pol);
         }
-        L.w[18] = ldw(rp, a0 + 192 + 8 * h + 2 * t);
-        L.w[19] = ldw(rp, a0 + 208);
+        L.w[18] = ldw(rp, a0 + 192 + 8 * h + 2 * t, pol);
+        L.w[19] = ldw(rp, a0 + 208, pol);
         // bits 0-1: ql's byte offset within its word; bits 2-3: qh's; bits 4-5: the
         // scales'; bits 6-7: d's; bits 8-9: t
         const uintptr_t base = reinterpret_cast<uintptr_t>(rp);
@@ -191,7 +192,7 @@ QM_DEV void load_lane(const Args& a, const Part& P, int64_t row, int64_t i0, Lan
         const int64_t a0 = (i0 / 32) * 17;
         L.off = static_cast<uint32_t>((reinterpret_cast<uintptr_t>(rp) + a0) & 3u);
 #pragma unroll
-        for (int j = 0; j < 5; ++j) L.w[j] = ldw(rp, a0 + 4 * j);
+        for (int j = 0; j < 5; ++j) L.w[j] = ldw(rp, a0 + 4 * j, pol);
         L.s = L.b = 0u;
     }
 }
@@ -361,7 +362,10 @@ QM_DEV float2 q6_k_dots(const uint32_t (&w)[20], uint32_t off, const float2 (&xp
 // j + 4, 4..7 from the nibbles of byte j + 4 with their top two bits from the
 // top bits of bytes j - 4 and j.
 QM_DEV void q4_k_scale_min(const uint32_t (&w)[12], int j, int& sc, int& mn) {
-    auto sb = [&](int i) -> int { return static_cast<int>((w[1 + (i >> 2)] >> (8 * (i & 3))) & 0xFFu); };
+    auto sb = [&](int i) -> int {  // byte i of words 1..3, chosen by selects (no indexed array)
+        const uint32_t wd = i < 4 ? w[1] : (i < 8 ? w[2] : w[3]);
+        return static_cast<int>((wd >> (8 * (i & 3))) & 0xFFu);
+    };
     if (j < 4) {
         sc = sb(j) & 63;
         mn = sb(4 + j) & 63;
@@ -497,11 +501,12 @@ __global__ void __launch_bounds__(kWarps * 32) gemv1_kernel(const __grid_constan
         lb = b - a.bstart[g];
     };
     Lane<FMT, BITS> cur[R], nxt[R];
+    const uint64_t pol = l2_evict_first_policy();
     auto load_step = [&](int g, int lb, int c, Lane<FMT, BITS> (&L)[R]) {
         const Part& P = a.part[g];
         const int64_t i0 = static_cast<int64_t>(c) * kChunk + 32 * lane;
 #pragma unroll
-        for (int r = 0; r < R; ++r) load_lane<FMT, BITS>(a, P, static_cast<int64_t>(lb) * R + r, i0, L[r]);
+        for (int r = 0; r < R; ++r) load_lane<FMT, BITS>(a, P, static_cast<int64_t>(lb) * R + r, i0, pol, L[r]);
     };
     int cg, clb;  // the current block's weight and its block index there
     locate(warp0, cg, clb);
