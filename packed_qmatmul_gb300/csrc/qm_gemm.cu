@@ -523,11 +523,15 @@ __global__ void __launch_bounds__(kThreads, NTOK <= 128 ? 2 : 1) gemm_kernel(con
         // a chunk holds an even number of k steps, so this thread decodes steps
         // kk with kk % 2 == grp of every chunk: only their scales are fetched
         static_assert(R::SPR % 2 == 0, "k steps per chunk");
+        // affine groups of 64 or more inputs: both halves of a k step share one
+        // group, whose scale and bias are fetched once (entry [kk][0])
+        constexpr bool kOneGroup = FMT == QM_AFFINE && GS >= 64;
+        constexpr int kHalves = kOneGroup ? 1 : 2;
         auto fetch = [&](int rc, Sc (&dst)[R::SPR][2]) {
 #pragma unroll
             for (int kk = 0; kk < R::SPR; ++kk)
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
+                for (int h = 0; h < kHalves; ++h)
                     dst[kk][h] = rowok && (kk & 1) == grp
                                      ? load_scale<FMT, BITS, GS>(p, wrow0 + grow,
                                                                  static_cast<int64_t>(rc) * R::RAWK + kk * BK + h * 32)
@@ -558,7 +562,7 @@ __global__ void __launch_bounds__(kThreads, NTOK <= 128 ? 2 : 1) gemm_kernel(con
                     for (int i = 0; i < 16; ++i) o0[i] = 0u;
                 }
                 if (rowok && static_cast<int64_t>(ks) * BK + 32 < p.k) {
-                    decode32<FMT, BITS, GS>(raw, row, kk, 1, cur[kk][1], o1);
+                    decode32<FMT, BITS, GS>(raw, row, kk, 1, cur[kk][kHalves - 1], o1);
                 } else {
 #pragma unroll
                     for (int i = 0; i < 16; ++i) o1[i] = 0u;
@@ -577,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, NTOK <= 128 ? 2 : 1) gemm_kernel(con
 #pragma unroll
             for (int kk = 0; kk < R::SPR; ++kk) {
                 cur[kk][0] = nxt[kk][0];
-                cur[kk][1] = nxt[kk][1];
+                if constexpr (kHalves == 2) cur[kk][1] = nxt[kk][1];
             }
         }
         // ------------------------------------------------------------ epilogue
