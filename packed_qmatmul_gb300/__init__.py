@@ -182,6 +182,15 @@ class QWeight:
             object.__setattr__(self, "_cref", ref)
         return ref
 
+    def _pointer(self):
+        """ctypes pointer to the same cached descriptor (for arrays of weights)."""
+        ref = self._ref()
+        cached = self.__dict__.get("_cptr")
+        if cached is None or cached[0] is not ref:  # the descriptor was rebuilt
+            cached = (ref, ctypes.pointer(ref._obj))
+            object.__setattr__(self, "_cptr", cached)
+        return cached[1]
+
     def _c(self) -> _CWeight:
         w = _CWeight()
         w.format, w.bits, w.group_size, w.scale_dtype = (self.format, self.bits, self.group_size,
@@ -237,14 +246,37 @@ def qm_apply(w: QWeight, x: torch.Tensor, y: torch.Tensor, stream=None) -> None:
                                    _stream(stream)))
 
 
+_WARR = [ctypes.POINTER(_CWeight) * max(i, 1) for i in range(QM_MAX_MANY + 1)]
+_PARR = [ctypes.c_void_p * max(i, 1) for i in range(QM_MAX_MANY + 1)]
+
+
+_MANY = {}
+
+
+def _weight_array(ws):
+    """The C array of descriptor pointers for these weights, kept per tuple of
+    weights and rebuilt when any of their descriptors was (a cached entry holds
+    its descriptors, so a weight reusing an id cannot match a stale one)."""
+    key = tuple(map(id, ws))
+    hit = _MANY.get(key)
+    if hit is not None and tuple([w._cref for w in ws]) == hit[0]:  # descriptors compare by identity
+        return hit[1]
+    refs = tuple(w._ref() for w in ws)
+    arr = _WARR[len(ws)](*[w._pointer() for w in ws])
+    if len(_MANY) >= 1024:
+        _MANY.clear()
+    _MANY[key] = (refs, arr)
+    return arr
+
+
 def qm_apply_many(ws: Sequence[QWeight], x: torch.Tensor, ys: Sequence[torch.Tensor], stream=None) -> None:
     """ys[i] = x times ws[i]^T for weights that read the same x (one launch at M = 1)."""
     M = x.shape[0] if x.dim() == 2 else 1
     n = len(ws)
-    warr = (ctypes.POINTER(_CWeight) * max(n, 1))()
-    for i, w in enumerate(ws):
-        warr[i] = ctypes.pointer(w._ref()._obj)
-    yarr = (ctypes.c_void_p * max(len(ys), 1))(*[_ptr(y) for y in ys])
+    if n > QM_MAX_MANY or len(ys) != n:  # the C call refuses these; keep the arrays in range
+        raise QMError(QM_EINVAL, f"count: {n} weights and {len(ys)} outputs (1 .. {QM_MAX_MANY} each)")
+    warr = _weight_array(ws)
+    yarr = _PARR[n](*[_ptr(y) for y in ys])
     _check(load_library().qm_apply_many(warr, n, _ptr(x), M, _DTYPES[x.dtype], yarr, _stream(stream)))
 
 
