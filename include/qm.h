@@ -159,8 +159,9 @@ qm_status qm_apply(const qm_weight* w, const void* x, int64_t M, int32_t x_dtype
  * "Products", apply, defines. The pages have no multi-weight call: it is this
  * library's, so that products reading the same activations (a decode step's
  * q/k/v projections, or gate and up) cost one launch instead of several. At
- * M = 1 weights of up to 24 MB each run as one grid; otherwise the call makes
- * the qm_apply launches one after another. */
+ * M = 1 weights of up to 24 MB each, and at M = 2..8 MLX affine 4-bit weights
+ * whose k is a multiple of 256, run as one grid; otherwise the call makes the
+ * qm_apply launches one after another. */
 qm_status qm_apply_many(const qm_weight* const* ws, int32_t count, const void* x, int64_t M, int32_t x_dtype,
                         void* const* ys, qm_stream_t stream);
 

@@ -271,17 +271,34 @@ qm_status qm_quantize_q8_0(const void* x, int32_t x_dtype, int64_t rows, int64_t
                         "quantize launch");
 }
 
+static bool small_weight(const WDesc& d) {
+    return d.n * d.code_row_bytes + d.n * (d.scale_row_bytes + d.bias_row_bytes) <= (int64_t(24) << 20);
+}
+
 // One token: the register kernel for weights up to 24 MB (a dependent chain of
 // such products is latency-bound); larger weights stream through the
 // tensor-map pipeline, which keeps more bytes in flight.
 static bool one_token_register_path(const WDesc& d) {
-    const bool small = d.n * d.code_row_bytes + d.n * (d.scale_row_bytes + d.bias_row_bytes) <= (int64_t(24) << 20);
-    return gemv1_supported(d) && (small || !gemv_supported(d, 1));
+    return gemv1_supported(d) && (small_weight(d) || !gemv_supported(d, 1));
+}
+
+// 2..8 tokens of affine 4-bit: weight tiles in registers on mma.sync (one
+// token keeps the register FFMA kernel: 3.4 against 4.1 us per small layer).
+// Weights of every size: an lm_head-sized weight alone streams faster through
+// the tensor-map pipeline (32 against 50 us in a chain of them), but after the
+// small layers of a decode step this kernel's CTAs start early and read ahead
+// (M = 8 step 0.402 against 0.426 ms).
+static bool few_token_register_path(const WDesc& d, int64_t M) {
+    return M >= 2 && M <= 8 && gemvr_supported(d, M);
 }
 
 // The launches of a validated product (M >= 1, n >= 1, k >= 1).
 static qm_status apply_launch(const WDesc& d, const void* x, int64_t M, void* y, cudaStream_t st) {
     if (M == 1 && one_token_register_path(d)) return check_launch(launch_gemv1(d, x, y, st), "gemv launch");
+    if (few_token_register_path(d, M)) {
+        void* ys[1] = {y};
+        return check_launch(launch_gemvr_many(&d, 1, x, M, ys, st), "gemv launch");
+    }
     if (M <= 16 && gemv_supported(d, M)) return launch_gemv(d, x, M, y, st);
     if (gemm_supported(d, M)) return launch_gemm(d, x, M, y, st);
     return check_launch(launch_apply_simple(d, x, M, y, st), "apply launch");
@@ -356,16 +373,19 @@ qm_status qm_apply_many(const qm_weight* const* ws, int32_t count, const void* x
     WDesc live[QM_MAX_MANY];
     void* live_y[QM_MAX_MANY];
     int nlive = 0;
-    bool fused = M == 1 && k > 0;
+    bool fused = M == 1 && k > 0, fused_few = k > 0;
     for (int i = 0; i < count; ++i) {
         if (d[i].n == 0) continue;
         live[nlive] = d[i];
         live_y[nlive++] = ys[i];
         fused = fused && one_token_register_path(d[i]);
+        fused_few = fused_few && few_token_register_path(d[i], M);
     }
     if (nlive == 0) return QM_OK;
     if (fused && gemv1_many_supported(live, nlive))
         return check_launch(launch_gemv1_many(live, nlive, x, live_y, st), "gemv launch");
+    if (fused_few && gemvr_many_supported(live, nlive, M))
+        return check_launch(launch_gemvr_many(live, nlive, x, M, live_y, st), "gemv launch");
     for (int i = 0; i < nlive; ++i) {
         qm_status s;
         if (k == 0)

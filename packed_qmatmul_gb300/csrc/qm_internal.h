@@ -98,6 +98,13 @@ bool gemv1_supported(const WDesc& w);
 cudaError_t launch_gemv1(const WDesc& w, const void* x, void* y, cudaStream_t st);
 bool gemv1_many_supported(const WDesc* ws, int count);
 cudaError_t launch_gemv1_many(const WDesc* ws, int count, const void* x, void* const* ys, cudaStream_t st);
+// y_i [M, n_i] = x [M, k] * W_i^T for up to 8 MLX affine 4-bit weights that
+// read the same x, 1 <= M <= 8, k a multiple of 256: weight tiles in registers,
+// products on mma.sync (qm_gemvr.cu).
+bool gemvr_supported(const WDesc& w, int64_t M);
+bool gemvr_many_supported(const WDesc* ws, int count, int64_t M);
+cudaError_t launch_gemvr_many(const WDesc* ws, int count, const void* x, int64_t M, void* const* ys,
+                              cudaStream_t st);
 // y [M, n] = x [M, k] * W^T for a 2-d weight, M <= 16, x and y bf16.
 qm_status launch_gemv(const WDesc& w, const void* x, int64_t M, void* y, cudaStream_t st);
 bool gemv_supported(const WDesc& w, int64_t M);

@@ -903,3 +903,20 @@ def test_apply_many_edge_cases():
     ow = to_oracle(w1)
     xn = np.linalg.norm(oracle.decode_array(x, oracle.BF16), axis=1)
     check_product(bf16_to_f64(_host(got[0])), oracle.apply(ow, x), row_norms(ow), xn, ow.k, "many nonfinite")
+
+
+@pytest.mark.parametrize("gs", [32, 64, 128])
+@pytest.mark.parametrize("M", [2, 5, 8])
+def test_register_mma_decode(gs, M):
+    # affine 4-bit at 2..8 tokens: weight tiles in registers on mma.sync; every
+    # k split (k = 256, 512, 1024 and up), ragged row counts, f16 scales, and a
+    # weight tall enough that CTAs stride over tiles
+    g = synth.rng(2400 + gs + M)
+    for n, k in ((17, 256), (300, 512), (48, 1024), (40, 3072)):
+        w = synth.affine_weight(g, n, k, bits=4, group_size=gs)
+        _check_apply(w, synth.activations(g, M, k), f"gs{gs} n={n} k={k} M={M}")
+    w = synth.affine_weight(g, 64, 1024, bits=4, group_size=gs, scale_dtype="f16")
+    _check_apply(w, synth.activations(g, M, 1024), f"gs{gs} f16 scales M={M}")
+    if gs == 64:
+        w = synth.affine_weight(g, 40000, 512, bits=4, group_size=gs)
+        _check_apply(w, synth.activations(g, M, 512), f"gs{gs} n=40000 M={M}")
