@@ -241,27 +241,81 @@ struct GatherMap {
     }
 };
 
+// A warp's 32 consecutive units of 16-bit output (2 KB, contiguous) written
+// as four coalesced 512-byte stores: lane l's four 16-byte pieces go to a
+// shared-memory stage (piece j of lane l in slot 4l + (j ^ ((l >> 1) & 3)),
+// so neither the writes nor the reads of a quarter warp share a bank group),
+// then lane l stores pieces l, l + 32, l + 64 and l + 96 of the warp's run.
+template <int OUT>
+QM_DEV void store_warp_units(void* out, int64_t elem0, const float (&v)[32], uint4* stage, int lane) {
+    uint4 p[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t w[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float lo = v[8 * i + 2 * j], hi = v[8 * i + 2 * j + 1];
+            if constexpr (OUT == QM_BF16) {
+                __nv_bfloat162 t = __floats2bfloat162_rn(lo, hi);
+                w[j] = *reinterpret_cast<uint32_t*>(&t);
+            } else {
+                __half2 t = __floats2half2_rn(lo, hi);
+                w[j] = *reinterpret_cast<uint32_t*>(&t);
+            }
+        }
+        p[i] = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) stage[4 * lane + (i ^ ((lane >> 1) & 3))] = p[i];
+    __syncwarp();
+    uint4* o = reinterpret_cast<uint4*>(static_cast<uint16_t*>(out) + elem0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int q = 32 * i + lane, src = q >> 2, c = q & 3;
+        o[q] = stage[4 * src + (c ^ ((src >> 1) & 3))];
+    }
+}
+
+template <class Map>
+constexpr bool kStaged = false;
+template <>
+constexpr bool kStaged<IdentityMap> = true;
+
 template <int FMT, int BITS, int OUT, class Map>
 __global__ void __launch_bounds__(256) decode_rows_kernel(DecodeArgs a, int64_t out_rows, Map map,
                                                           void* out) {
     grid_launch_dependents();
     grid_dependency_wait();  // the weight, ids or output may belong to the previous kernel
+    __shared__ uint4 s_stage[kStaged<Map> ? 8 : 1][128];  // one 2 KB stage per warp (16-bit outputs)
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t upr = a.k / 32;
     const int64_t total = out_rows * upr;
-    for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < total;
+    // the stride is a multiple of 32, so a warp's lanes hold 32 consecutive units
+    // until the last, partial run
+    for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t - lane < total;
          t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t r = t / upr, u = t - r * upr;
-        const int64_t src = map(r);
+        const bool mine = t < total;
         float v[32];
-        if (src >= 0) {
-            decode_unit<FMT, BITS>(a, src, u, v);
-        } else {
-            // an out-of-range position gathers zero bytes: their values are
-            // zeros, -0. in Q6_K ("Nx_quant", "Weights")
+        if (mine) {
+            const int64_t r = t / upr, u = t - r * upr;
+            const int64_t src = map(r);
+            if (src >= 0) {
+                decode_unit<FMT, BITS>(a, src, u, v);
+            } else {
+                // an out-of-range position gathers zero bytes: their values are
+                // zeros, -0. in Q6_K ("Nx_quant", "Weights")
 #pragma unroll
-            for (int i = 0; i < 32; ++i) v[i] = FMT == QM_Q6_K ? -0.0f : 0.0f;
+                for (int i = 0; i < 32; ++i) v[i] = FMT == QM_Q6_K ? -0.0f : 0.0f;
+            }
         }
-        store_unit<OUT>(out, t * 32, v);
+        // staged, coalesced stores for full dequant (2 % faster); a gather, short
+        // and latency-bound, stores directly (its dense take measured slower staged)
+        if (kStaged<Map> && OUT != QM_F32 && t - lane + 31 < total) {
+            store_warp_units<OUT>(out, (t - lane) * 32, v, s_stage[warp], lane);
+        } else if (mine) {
+            store_unit<OUT>(out, t * 32, v);
+        }
     }
 }
 
