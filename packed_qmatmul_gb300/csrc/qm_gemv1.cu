@@ -22,8 +22,9 @@
 //    previous one (programmatic dependent launch), so a dependent chain of
 //    small products pays for the activations' round trip only. The next
 //    kernel is let start once this one's wait has returned.
-//  * Warps stride over blocks of R rows; each loads the next step's codes
-//    before it works on the current one (large layers stream).
+//  * Warps stride over blocks of R rows, keeping the next two steps' codes in
+//    flight (one for the formats with the largest lane data) while they work
+//    on the current one: 3.39 -> 3.25 us per small layer at 4-bit.
 //  * A lane whose partial sum is not finite, or whose block's scale could make
 //    a value infinite (an MXFP4 scale byte of 253 or more, an affine scale or
 //    bias of magnitude 2^119 or more), sums that block element by element
@@ -500,7 +501,11 @@ __global__ void __launch_bounds__(kWarps * 32) gemv1_kernel(const __grid_constan
         while (g + 1 < a.nparts && b >= a.bstart[g + 1]) ++g;
         lb = b - a.bstart[g];
     };
-    Lane<FMT, BITS> cur[R], nxt[R];
+    // two steps' codes in flight where the registers still leave 16 warps per
+    // SM (four CTAs); one for the formats whose lane data is larger (8-bit
+    // affine, Q4_K, Q6_K: with two, fewer CTAs fit and layers take two waves)
+    constexpr bool kDeep = !(FMT == QM_AFFINE && BITS == 8) && FMT != QM_Q4_K && FMT != QM_Q6_K;
+    Lane<FMT, BITS> cur[R], nxt[R], nx2[R];  // this step's codes and the next one's (two)
     const uint64_t pol = l2_evict_first_policy();
     auto load_step = [&](int g, int lb, int c, Lane<FMT, BITS> (&L)[R]) {
         const Part& P = a.part[g];
@@ -508,14 +513,26 @@ __global__ void __launch_bounds__(kWarps * 32) gemv1_kernel(const __grid_constan
 #pragma unroll
         for (int r = 0; r < R; ++r) load_lane<FMT, BITS>(a, P, static_cast<int64_t>(lb) * R + r, i0, pol, L[r]);
     };
+    // the (block, chunk) step after (b, c), and its block's weight and index there
+    auto advance = [&](int& b, int& c, int& g, int& lb) {
+        if (++c == nchunk) {
+            c = 0;
+            b += nwarp;
+            if (b < nblocks) locate(b, g, lb);
+        }
+    };
     int cg, clb;  // the current block's weight and its block index there
     locate(warp0, cg, clb);
+    int b1 = warp0, c1 = 0, g1 = cg, lb1 = clb;  // the next step
+    advance(b1, c1, g1, lb1);
     if (a.static_w) {  // the weight is not written by the previous kernel: read it first
         load_step(cg, clb, 0, cur);
+        if (kDeep && b1 < nblocks) load_step(g1, lb1, c1, nxt);
         grid_dependency_wait();
     } else {
         grid_dependency_wait();
         load_step(cg, clb, 0, cur);
+        if (kDeep && b1 < nblocks) load_step(g1, lb1, c1, nxt);
     }
     // Let the next kernel start only now: it still has this kernel's whole
     // remaining run to read its own static weights, and only one kernel waits
@@ -530,13 +547,13 @@ __global__ void __launch_bounds__(kWarps * 32) gemv1_kernel(const __grid_constan
     // (block b, chunk c) steps, chunks fastest
     #pragma unroll 1
     for (int b = warp0, c = 0; b < nblocks;) {
-        int b2 = b, c2 = c + 1, g2 = cg, lb2 = clb;
-        if (c2 == nchunk) {
-            c2 = 0;
-            b2 += nwarp;
-            if (b2 < nblocks) locate(b2, g2, lb2);
+        int b2 = b1, c2 = c1, g2 = g1, lb2 = lb1;  // the step after the next
+        if (b2 < nblocks) advance(b2, c2, g2, lb2);
+        if constexpr (kDeep) {
+            if (b2 < nblocks) load_step(g2, lb2, c2, nx2);
+        } else {
+            if (b1 < nblocks) load_step(g1, lb1, c1, nxt);
         }
-        if (b2 < nblocks) load_step(g2, lb2, c2, nxt);
         const int64_t i0 = static_cast<int64_t>(c) * kChunk + 32 * lane;
         if (nchunk > 1 || !have_x) {
             load_acts<FMT, BITS>(a, i0, X);
@@ -568,11 +585,18 @@ __global__ void __launch_bounds__(kWarps * 32) gemv1_kernel(const __grid_constan
             for (int r = 0; r < R; ++r) y[r] = 0.0f;
         }
 #pragma unroll
-        for (int r = 0; r < R; ++r) cur[r] = nxt[r];
-        b = b2;
-        c = c2;
-        cg = g2;
-        clb = lb2;
+        for (int r = 0; r < R; ++r) {
+            cur[r] = nxt[r];
+            if constexpr (kDeep) nxt[r] = nx2[r];
+        }
+        b = b1;
+        c = c1;
+        cg = g1;
+        clb = lb1;
+        b1 = b2;
+        c1 = c2;
+        g1 = g2;
+        lb1 = lb2;
     }
 }
 
