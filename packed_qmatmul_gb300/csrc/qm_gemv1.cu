@@ -76,6 +76,7 @@ struct Args {
     int sdt;             // affine scale dtype
     int nchunk;          // chunks of 1024 inputs: ceil(k / 1024)
     int static_w;        // the weights may be read before the previous kernel ends
+    int ks;              // warps splitting one block's chunks (1: a warp takes all of k)
 };
 
 // Words of packed data a lane holds for one row and one chunk.
@@ -489,11 +490,21 @@ template <int FMT, int BITS>
 __global__ void __launch_bounds__(kWarps * 32) gemv1_kernel(const __grid_constant__ Args a) {
     const int lane = threadIdx.x & 31;
     // 32-bit block indices (a block is R rows; fewer than 2^31 blocks) and steps
-    // walked incrementally: no integer division anywhere on the path
-    const int warp0 = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-    const int nwarp = static_cast<int>((gridDim.x * blockDim.x) >> 5);
-    const int nblocks = a.bstart[a.nparts], nchunk = a.nchunk;
-    if (warp0 >= nblocks) return;  // nothing to read or write
+    // walked incrementally: no integer division anywhere on the path.
+    // ks == 1: warp w takes blocks w, w + nwarp, ... and all chunks of each.
+    // ks > 1: the CTA is ks warps taking blocks blockIdx.x, + gridDim.x, ...;
+    // warp kp takes chunks [kp * nchunk / ks, (kp + 1) * nchunk / ks) of each,
+    // and the warps' sums meet in shared memory (added in warp order), so a
+    // long row costs one warp's share of k, not all of it, after the wait.
+    const int ks = a.ks, kp = static_cast<int>(threadIdx.x >> 5);
+    const bool split = ks > 1;
+    const int warp0 = split ? static_cast<int>(blockIdx.x)
+                            : static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int nwarp = split ? static_cast<int>(gridDim.x) : static_cast<int>((gridDim.x * blockDim.x) >> 5);
+    const int nblocks = a.bstart[a.nparts];
+    const int cpw = a.nchunk / ks, c_lo = split ? kp * cpw : 0, c_hi = c_lo + cpw;  // this warp's chunks
+    __shared__ float s_red[kWarps][R];  // split: each warp's row sums of the current block
+    if (warp0 >= nblocks) return;  // nothing to read or write (the whole CTA, when split)
     // the weight holding block b, and the block's index within that weight
     auto locate = [&](int b, int& g, int& lb) {
         g = 0;
@@ -515,23 +526,23 @@ __global__ void __launch_bounds__(kWarps * 32) gemv1_kernel(const __grid_constan
     };
     // the (block, chunk) step after (b, c), and its block's weight and index there
     auto advance = [&](int& b, int& c, int& g, int& lb) {
-        if (++c == nchunk) {
-            c = 0;
+        if (++c == c_hi) {
+            c = c_lo;
             b += nwarp;
             if (b < nblocks) locate(b, g, lb);
         }
     };
     int cg, clb;  // the current block's weight and its block index there
     locate(warp0, cg, clb);
-    int b1 = warp0, c1 = 0, g1 = cg, lb1 = clb;  // the next step
+    int b1 = warp0, c1 = c_lo, g1 = cg, lb1 = clb;  // the next step
     advance(b1, c1, g1, lb1);
     if (a.static_w) {  // the weight is not written by the previous kernel: read it first
-        load_step(cg, clb, 0, cur);
+        load_step(cg, clb, c_lo, cur);
         if (kDeep && b1 < nblocks) load_step(g1, lb1, c1, nxt);
         grid_dependency_wait();
     } else {
         grid_dependency_wait();
-        load_step(cg, clb, 0, cur);
+        load_step(cg, clb, c_lo, cur);
         if (kDeep && b1 < nblocks) load_step(g1, lb1, c1, nxt);
     }
     // Let the next kernel start only now: it still has this kernel's whole
@@ -546,7 +557,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv1_kernel(const __grid_constan
     bool have_x = false;
     // (block b, chunk c) steps, chunks fastest
     #pragma unroll 1
-    for (int b = warp0, c = 0; b < nblocks;) {
+    for (int b = warp0, c = c_lo; b < nblocks;) {
         int b2 = b1, c2 = c1, g2 = g1, lb2 = lb1;  // the step after the next
         if (b2 < nblocks) advance(b2, c2, g2, lb2);
         if constexpr (kDeep) {
@@ -555,7 +566,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv1_kernel(const __grid_constan
             if (b1 < nblocks) load_step(g1, lb1, c1, nxt);
         }
         const int64_t i0 = static_cast<int64_t>(c) * kChunk + 32 * lane;
-        if (nchunk > 1 || !have_x) {
+        if (cpw > 1 || !have_x) {
             load_acts<FMT, BITS>(a, i0, X);
             have_x = true;
         }
@@ -568,7 +579,7 @@ __global__ void __launch_bounds__(kWarps * 32) gemv1_kernel(const __grid_constan
             if ((exact || !isfinite(part)) && row < P.n && i0 < a.k) part = lane_exact<FMT, BITS>(a, P, row, i0);
             y[r] += part;
         }
-        if (c == nchunk - 1) {
+        if (c == c_hi - 1) {
             // the R rows' sums over the warp, in a fixed order: lanes first
             // exchange halves of their R values, then add down to one each
             static_assert(R == 2, "the exchange below pairs two rows");
@@ -577,9 +588,22 @@ __global__ void __launch_bounds__(kWarps * 32) gemv1_kernel(const __grid_constan
 #pragma unroll
             for (int o = 2; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
             const int64_t row = static_cast<int64_t>(clb) * R + lane;  // lane 0: row 0 of the block, lane 1: row 1
-            if (lane < R && row < P.n) {
-                __nv_bfloat16 bv = __float2bfloat16_rn(v);
-                P.y[row] = *reinterpret_cast<uint16_t*>(&bv);
+            if (split) {  // the block's ks warps (every warp of the CTA, in step): their sums in warp order
+                if (lane < R) s_red[kp][lane] = v;
+                __syncthreads();
+                if (kp == 0 && lane < R) {
+                    float sum = s_red[0][lane];
+                    #pragma unroll 1
+                    for (int q = 1; q < ks; ++q) sum += s_red[q][lane];
+                    v = sum;
+                }
+                __syncthreads();  // s_red is written again for the next block
+            }
+            if (kp == 0 || !split) {
+                if (lane < R && row < P.n) {
+                    __nv_bfloat16 bv = __float2bfloat16_rn(v);
+                    P.y[row] = *reinterpret_cast<uint16_t*>(&bv);
+                }
             }
 #pragma unroll
             for (int r = 0; r < R; ++r) y[r] = 0.0f;
@@ -603,7 +627,11 @@ __global__ void __launch_bounds__(kWarps * 32) gemv1_kernel(const __grid_constan
 template <int FMT, int BITS>
 cudaError_t launch_t(const Args& a, cudaStream_t st) {
     // all warps resident at once where the rows allow: 16 warps per SM
-    const int64_t warps = std::min<int64_t>(a.bstart[a.nparts], int64_t(num_sms()) * 16);
+    const int64_t nb = a.bstart[a.nparts], cap = int64_t(num_sms()) * 16;
+    if (a.ks > 1)  // a CTA of ks warps per block
+        return launch_pdl(gemv1_kernel<FMT, BITS>, static_cast<unsigned>(std::min<int64_t>(nb, cap / a.ks)),
+                          a.ks * 32, 0, st, a);
+    const int64_t warps = std::min<int64_t>(nb, cap);
     const unsigned grid = static_cast<unsigned>((warps + kWarps - 1) / kWarps);
     return launch_pdl(gemv1_kernel<FMT, BITS>, grid, kWarps * 32, 0, st, a);
 }
@@ -659,6 +687,14 @@ cudaError_t launch_gemv1_many(const WDesc* ws, int count, const void* x, void* c
     a.sdt = w.sdt;
     a.nchunk = static_cast<int>((w.k + kChunk - 1) / kChunk);
     a.static_w = all_static ? 1 : 0;
+    // chunks split over 4, 3 or 2 warps where that divides them (k alone decides:
+    // a row's sum order must not depend on the other weights of a launch)
+    a.ks = 1;
+    for (int d = kWarps; d >= 2; --d)
+        if (a.nchunk % d == 0) {
+            a.ks = d;
+            break;
+        }
     if (w.fmt == QM_AFFINE) {
         switch (w.bits) {
             case 2: return launch_t<QM_AFFINE, 2>(a, st);
