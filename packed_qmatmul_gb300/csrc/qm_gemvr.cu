@@ -46,7 +46,8 @@ namespace qm {
 
 namespace gr {
 
-constexpr int kWarps = 4;       // warps per CTA
+constexpr int kWarps = 4;       // warps per CTA where ks <= 2 (4 / ks tiles each)
+constexpr int kMaxWarps = 12;   // the most warps a tile's k split takes (a CTA of ks warps)
 constexpr int kStep = 256;      // inputs per step of a warp
 constexpr int kMaxParts = 8;    // weights per launch (the C ABI's QM_MAX_MANY)
 constexpr uint32_t kBf16Magic = 0x43004300u;  // bf16 pair (128, 128)
@@ -69,7 +70,8 @@ struct Args {
     int64_t k;
     int64_t code_row_bytes, scale_row_bytes;
     int sdt;                    // scale dtype (QM_BF16 or QM_F16)
-    int ks;                     // warps splitting one tile's k (1, 2 or 4)
+    int ks;                     // warps splitting one tile's k (1 .. 12)
+    int tpc;                    // tiles per CTA (4 / ks where ks <= 2, else 1)
     int nsteps;                 // steps of kStep inputs in one warp's k range
     int static_w;
 };
@@ -220,14 +222,14 @@ static __device__ __noinline__ float exact_sum(const Args& a, const Part& P, int
 }
 
 template <int GS>
-__global__ void __launch_bounds__(kWarps * 32) gemvr_kernel(const __grid_constant__ Args a) {
+__global__ void __launch_bounds__(kMaxWarps * 32) gemvr_kernel(const __grid_constant__ Args a) {
     using St = Step<GS>;
     constexpr int G = St::G, V = St::V;
     constexpr int GSHIFT = GS == 32 ? 5 : (GS == 64 ? 6 : 7);
-    __shared__ float red[kWarps][32][4];
+    __shared__ float red[kMaxWarps][32][4];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
-    const int ks = a.ks, tpc = kWarps / ks;   // tiles per CTA
+    const int ks = a.ks, tpc = a.tpc;   // tiles per CTA
     const int slot = warp / ks, kpart = warp % ks;
     const int ntiles = a.tstart[a.nparts];
     const int64_t krange = static_cast<int64_t>(a.nsteps) * kStep;  // k / ks
@@ -366,11 +368,11 @@ __global__ void __launch_bounds__(kWarps * 32) gemvr_kernel(const __grid_constan
 
 template <int GS>
 static cudaError_t launch_t(const Args& a, cudaStream_t st) {
-    const int tpc = kWarps / a.ks;
+    const int wpc = a.ks * a.tpc;  // warps per CTA
     const int64_t ntiles = a.tstart[a.nparts];
     // all warps resident at once where the tiles allow: 16 warps per SM
-    const int64_t ctas = std::min<int64_t>((ntiles + tpc - 1) / tpc, int64_t(num_sms()) * (16 / kWarps));
-    return launch_pdl(gemvr_kernel<GS>, static_cast<unsigned>(ctas), kWarps * 32, 0, st, a);
+    const int64_t ctas = std::min<int64_t>((ntiles + a.tpc - 1) / a.tpc, int64_t(num_sms()) * 16 / wpc);
+    return launch_pdl(gemvr_kernel<GS>, static_cast<unsigned>(std::max<int64_t>(1, ctas)), wpc * 32, 0, st, a);
 }
 
 }  // namespace gr
@@ -418,9 +420,18 @@ cudaError_t launch_gemvr_many(const WDesc* ws, int count, const void* x, int64_t
     a.sdt = w.sdt;
     a.static_w = all_static ? 1 : 0;
     // k split by k alone (the sum order of an output must not depend on the
-    // other weights of a launch): four warps per tile where k allows
-    a.ks = w.k % (4 * kStep) == 0 ? 4 : (w.k % (2 * kStep) == 0 ? 2 : 1);
-    a.nsteps = static_cast<int>(w.k / (int64_t(a.ks) * kStep));
+    // other weights of a launch): as many warps per tile, up to 12, as divide
+    // k's steps, so a long row (down_proj's 3072 inputs: 12 steps) costs one
+    // step after the wait
+    const int steps = static_cast<int>(w.k / kStep);
+    a.ks = 1;
+    for (int d = kMaxWarps; d >= 2; --d)
+        if (steps % d == 0) {
+            a.ks = d;
+            break;
+        }
+    a.tpc = a.ks <= 2 ? kWarps / a.ks : 1;
+    a.nsteps = steps / a.ks;
     if (w.gs == 32) return launch_t<32>(a, st);
     if (w.gs == 64) return launch_t<64>(a, st);
     return launch_t<128>(a, st);
