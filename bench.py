@@ -749,7 +749,7 @@ def detail_measurements(args, dev, stream, fused=True):
 # capture, with the commit whose kernel was measured. A kernel changed after its
 # capture has None here (reported as null) until it is captured again.
 TRAFFIC = {
-    "decode": (2579669.0, "3303723"),
+    "decode": (2580267.0, "66cf0e5"),
     "experts_gemm": (538.9e6, "ef3076f"),
     "experts_gemv": (None, None),
     "dequant": (337.4e6, "6d4178e"),
