@@ -250,6 +250,11 @@ def apply_entries(w: Weight, x: np.ndarray, m_idx, j_idx, xdt=None) -> np.ndarra
     x = np.ascontiguousarray(x)
     m_idx = np.ascontiguousarray(m_idx, dtype=np.int64)
     j_idx = np.ascontiguousarray(j_idx, dtype=np.int64)
+    # the C routine reads both index arrays and x's rows unchecked
+    if m_idx.ndim != 1 or m_idx.shape != j_idx.shape:
+        raise ValueError(f"apply_entries: m_idx {m_idx.shape} and j_idx {j_idx.shape} must be equal 1-D arrays")
+    if m_idx.size and (m_idx.min() < 0 or m_idx.max() >= x.shape[0] or j_idx.min() < 0 or j_idx.max() >= w.rows):
+        raise ValueError("apply_entries: an index is out of range")
     out = np.empty(m_idx.shape[0], dtype=np.float64)
     _load().or_apply_entries(*w._args(), w.rows, w.k, _ptr(w.codes), _ptr(w.scales),
                              _ptr(w.biases), _ptr(x), _x_dtype(x, xdt), m_idx.shape[0],

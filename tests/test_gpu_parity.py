@@ -470,9 +470,10 @@ def test_apply_lm_head_shape_sampled():
 # ---------------------------------------------------------------- prefill (tensor cores)
 @pytest.mark.parametrize("kind", KINDS)
 def test_apply_prefill(kind):
-    # several 128 x 128 tiles along both axes, ragged M and n, k not a multiple of 256
+    # several weight and token tiles along both axes (token tiles of 128 or
+    # 256), ragged M and n, k not a multiple of 256
     g = synth.rng(1200)
-    for n, k, M in ((200, 512, 130), (256, 1024, 64), (130, 384, 257)):
+    for n, k, M in ((200, 512, 130), (256, 1024, 64), (130, 384, 257), (136, 512, 192), (130, 384, 385)):
         if kind == "q8_0" and k % 256:
             k = 512  # Q8_0 rows must be 16-byte multiples for the TMA path
         w = _make(kind, g, n, k)
@@ -509,8 +510,8 @@ def test_apply_prefill_q8_0_full_shape_sampled(n, k):
     x = synth.activations(g, 2048, k)
     ow = to_oracle(w)
     y = bf16_to_f64(_host(qm.apply(qm.QWeight.from_arrays(w), _dev_bf16(x))))
-    m_idx = np.concatenate([g.integers(0, 2048, 2000), [0, 2047, 127, 128, 255, 256]])
-    j_idx = np.concatenate([g.integers(0, n, 2000), [0, n - 1, 128, 127, n - 128, 129]])
+    m_idx = np.concatenate([g.integers(0, 2048, 2000), [0, 2047, 127, 128, 191, 192, 383, 384, 1919, 1920]])
+    j_idx = np.concatenate([g.integers(0, n, 2000), [0, n - 1, 128, 127, n - 128, 129, 1, 255, 256, n - 129]])
     ref = oracle.apply_entries(ow, x, m_idx, j_idx)
     wn = np.array([np.linalg.norm(oracle.row_values(ow, int(r)).astype(np.float64)) for r in j_idx])
     xn = np.linalg.norm(oracle.decode_array(x[m_idx], oracle.BF16), axis=1)

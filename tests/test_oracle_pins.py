@@ -554,6 +554,20 @@ def test_product_vs_torch_float64(kind):
     assert np.allclose(ent, [want[0, 6], want[2, 0], want[1, 3]], rtol=1e-12, atol=1e-12)
 
 
+
+def test_apply_entries_rejects_bad_indices():
+    # the C routine reads the index arrays and x's rows unchecked: mismatched
+    # or out-of-range indices are refused before it runs
+    g = synth.rng(77)
+    w = to_oracle(synth.q8_0_weight(g, 8, 64))
+    x = synth.activations(g, 3, 64)
+    with pytest.raises(ValueError):
+        oracle.apply_entries(w, x, [0, 1, 2], [0, 1])
+    with pytest.raises(ValueError):
+        oracle.apply_entries(w, x, [3], [0])
+    with pytest.raises(ValueError):
+        oracle.apply_entries(w, x, [0], [8])
+
 def test_product_all_ones_codes_zero_bias():
     # codes all 1, bias 0: y = sum over groups of s_g * (sum of x over the group)
     g = np.random.default_rng(14)
