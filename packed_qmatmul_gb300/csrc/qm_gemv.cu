@@ -500,22 +500,27 @@ __global__ void __launch_bounds__(kThreadsOf(CW), CW == 8 ? 2 : 1) gemv_kernel(c
             if (lane == 0) {
                 slot_stage[slot] = j;
                 mbar_expect_tx(bar, tx);
+            }
+            __syncwarp();
+            {
+                // The stage's copies are spread over the warp's lanes: a thread
+                // completes about one TMA copy per 0.39 us whatever its size, so
+                // one lane issuing a stage's boxes in turn capped the stream.
                 const int32_t x0 = static_cast<int32_t>(rank * p.code_seg), y0 = static_cast<int32_t>(wrow0 + row0);
                 #pragma unroll 1
-                for (uint32_t c = 0; c < p.nbox; ++c)
+                for (uint32_t c = lane; c < p.nbox; c += 32)
                     tma_load_2d(smem_u32(st + c * kRows * 128), &p.tm_codes, x0 + 128 * c, y0, bar);
                 if (p.scale_seg && !p.scale_span) {
                     const int32_t xs0 = static_cast<int32_t>(rank * p.scale_seg);
-                    tma_load_2d(smem_u32(st + p.off_scales), &p.tm_scales, xs0, y0, bar);
-                    if (p.biases) tma_load_2d(smem_u32(st + p.off_biases), &p.tm_biases, xs0, y0, bar);
+                    if (lane == 31) tma_load_2d(smem_u32(st + p.off_scales), &p.tm_scales, xs0, y0, bar);
+                    if (p.biases && lane == 30) tma_load_2d(smem_u32(st + p.off_biases), &p.tm_biases, xs0, y0, bar);
                 }
             }
-            __syncwarp();
             if (p.scale_seg && p.scale_span) {
                 const int64_t off = (wrow0 + row0) * p.scale_row_bytes;
-                if (lane == 0 && span_bulk) {
-                    bulk_g2s(smem_u32(st + p.off_scales), p.scales + off, span_bulk, bar);
-                    if (p.biases) bulk_g2s(smem_u32(st + p.off_biases), p.biases + off, span_bulk, bar);
+                if (span_bulk) {
+                    if (lane == 31) bulk_g2s(smem_u32(st + p.off_scales), p.scales + off, span_bulk, bar);
+                    if (p.biases && lane == 30) bulk_g2s(smem_u32(st + p.off_biases), p.biases + off, span_bulk, bar);
                 }
                 #pragma unroll 1
                 for (uint32_t b = span_bulk + lane; b < span; b += 32) {  // ragged tail of the last stage
