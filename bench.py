@@ -296,7 +296,8 @@ def run_prefill(args, rank, world):
         "config": {"workload": f"GGUF Q8_0 qmatmul, W 4096x4096, 14336x4096, 4096x14336, M={M}"
                                + (f" (only {args.only})" if args.only else ""),
                    "M": M, "weight_bytes_per_step": wbytes, "flops_per_step": flops,
-                   "l2": "weights 143 MB per step, more than L2"},
+                   "l2": ("weights 143 MB per step, more than L2" if not args.only else
+                          f"profiling aid: weights {wbytes / 1e6:.0f} MB per step, L2 not flushed")},
         "roofline": {"bound": "tensor", "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "traffic": None,
                      "kernel": "gemm_kernel<Q8_0> (every launch of the step)",
